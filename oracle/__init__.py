@@ -1,0 +1,365 @@
+"""fp64 CPU oracle for causal grouped-query attention over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import
+this package.  It shares no code with the CUDA library
+``causal_gqa_attention_02_gb300``; neither imports the other.  The only
+module both sides use is ``workloads`` (seeded inputs, no arithmetic).
+
+Sources, cited by page title and section:
+  [P1] "第二章 Prefill：整层状态演化与 KV 建立" (glenzli.com, vol. 2 ch. 2):
+       2.2 mask M; 2.3 attention equations; 2.5 cache contract and
+       invariants 2.2; 2.6 pseudocode (write valid positions only).
+  [P2] "模型执行：从 token 到 Prefill 与 Decode" (blog.mlxb.cc): the hand-
+       worked attention example; the cached-vs-recompute comparison.
+  [P3] "KV Cache 与 Prefill/Decode 推理路径" (wiki.maxwellmou.com, unit 10):
+       edit-at-m invalidation; PagedAttention block table and free pool;
+       incremental prefill; prefix sharing with reference counts.
+
+Contents:
+  attention()        the definition of [P1] 2.3, in plain fp64 C (threaded).
+  attention_dense()  a second, independent form: materialise S with the -inf
+                     mask M of [P1] 2.2, two-pass softmax, numpy matmuls.
+  CacheModel         the logical cache plus the page-allocation rules (block
+                     table, free pool taken in a fixed order, reference counts,
+                     copy-on-write of a shared tail page, truncation), restated
+                     from [P3] and the library's documented allocator rules.
+  prefill()/decode()/append() drive CacheModel and attention() for a batch.
+
+Every function here is pinned by tests in tests/test_oracle_pins.py against
+values the pages print, closed forms, special cases and brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import heapq
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liborc.so")
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+PAGE_TOKENS = 16
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (IEEE fp64, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lp = ctypes.POINTER(ctypes.c_int64)
+            lib.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          dp, lp, ctypes.c_int, dp, dp, dp, ctypes.c_int]
+            lib.orc_attention.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+# ---------------------------------------------------------------------------
+# Stored values -> fp64 (exact for bf16 and fp32).
+# ---------------------------------------------------------------------------
+
+def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """bf16 bit patterns (uint16) or float32 values -> float64, exactly."""
+    if dtype == "bf16":
+        u = np.asarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+        return u.view(np.float32).astype(np.float64)
+    if dtype == "f32":
+        return np.asarray(x, dtype=np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+# ---------------------------------------------------------------------------
+# The attention definition ([P1] 2.3).
+# ---------------------------------------------------------------------------
+
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos, nthreads: int | None = None):
+    """q [n_q, H_q, d], K/V [L, H_kv, d] (float64), qpos [n_q] absolute
+    positions.  Query i sees keys 0..qpos[i].  Returns O [n_q, H_q, d]."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    K = np.ascontiguousarray(K, dtype=np.float64)
+    V = np.ascontiguousarray(V, dtype=np.float64)
+    qpos = np.ascontiguousarray(qpos, dtype=np.int64)
+    n_q, H_q, d = q.shape
+    L, H_kv, d2 = K.shape
+    assert d2 == d and V.shape == K.shape and qpos.shape == (n_q,)
+    out = np.zeros((n_q, H_q, d), dtype=np.float64)
+    if n_q == 0:
+        return out
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = lib.orc_attention(n_q, H_q, H_kv, d, q.ctypes.data_as(dp),
+                           qpos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                           L, K.ctypes.data_as(dp), V.ctypes.data_as(dp),
+                           out.ctypes.data_as(dp), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle precondition failed (rc=%d)" % rc)
+    return out
+
+
+def attention_dense(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos):
+    """Second form of [P1] 2.3 for small inputs: build S = QK^T/sqrt(d) + M with
+    M = -inf on invisible keys, take each row's finite max, exponentiate the
+    finite entries, normalise, multiply by V."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    qpos = np.asarray(qpos, dtype=np.int64)
+    n_q, H_q, d = q.shape
+    L, H_kv, _ = K.shape
+    out = np.zeros((n_q, H_q, d))
+    M = np.where(np.arange(L)[None, :] <= qpos[:, None], 0.0, -np.inf)
+    for h in range(H_q):
+        g = (h * H_kv) // H_q
+        S = (q[:, h, :] @ K[:, g, :].T) / np.sqrt(d) + M
+        finite = np.isfinite(S)
+        if not finite.any(axis=1).all():
+            raise ValueError("a query row has no finite score")
+        m = np.where(finite, S, -np.inf).max(axis=1)
+        E = np.where(finite, np.exp(np.where(finite, S, 0.0) - m[:, None]), 0.0)
+        A = E / E.sum(axis=1, keepdims=True)
+        out[:, h, :] = A @ V[:, g, :]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Logical paged cache ([P1] 2.5; [P3] PagedAttention, prefix sharing, edit).
+# ---------------------------------------------------------------------------
+
+class CacheError(Exception):
+    def __init__(self, kind: str, msg: str = ""):
+        super().__init__("%s: %s" % (kind, msg))
+        self.kind = kind
+
+
+class CacheModel:
+    """Logical KV cache with a block table per sequence.
+
+    Rules (the pages give the mechanism; the fixed choices are the library's
+    documented ones, restated here independently):
+      * token t of a sequence lives in logical page t // 16 at offset t % 16,
+        and the block table maps logical page -> physical page ([P3]
+        PagedAttention: block size B_s, logical block and offset);
+      * a new page comes from the free pool when the tail page is full, and
+        the pool may hand out any free page ([P3] PagedAttention, growth of a
+        request); the library fixes the choice as the free page of smallest
+        rank in a page order given at creation (identity by default);
+      * pages are reference counted; a page returns to the pool only when no
+        sequence references it ([P3] prefix tree: a shared block is reclaimed
+        once every request that uses it has finished);
+      * writing into a shared tail page first copies it to a fresh page
+        ([P3] prefix tree: a fork inside a block needs copy-on-write);
+      * truncate(m) keeps positions < m and drops the rest ([P3] edit at m:
+        keep the KV before m, truncate the suffix);
+      * fork(src, k) starts a sequence on src's first k positions, sharing
+        their pages ([P1] 2.9 prefix reuse).
+    Within one batched call, pages are taken sequence by sequence in batch
+    order; for each sequence the copy-on-write page comes first, then new
+    pages in logical order.  A call that cannot be satisfied changes nothing.
+    """
+
+    def __init__(self, num_pages, max_seqs, max_pages_per_seq, H_kv, d, dtype,
+                 page_order=None):
+        self.num_pages = int(num_pages)
+        self.max_seqs = int(max_seqs)
+        self.max_pages_per_seq = int(max_pages_per_seq)
+        self.H_kv, self.d, self.dtype = int(H_kv), int(d), dtype
+        order = np.arange(self.num_pages) if page_order is None else np.asarray(page_order)
+        assert sorted(order.tolist()) == list(range(self.num_pages))
+        self.rank = np.empty(self.num_pages, dtype=np.int64)
+        self.rank[order] = np.arange(self.num_pages)
+        self.order = order.astype(np.int64)
+        self.free = list(range(self.num_pages))   # heap of ranks
+        heapq.heapify(self.free)
+        self.ref = np.zeros(self.num_pages, dtype=np.int64)
+        self.seqs = {}                            # id -> dict(pages, len, k, v)
+        self.copies = []                          # (src_page, dst_page, slots) log
+
+    # -- page pool ---------------------------------------------------------
+    def _take(self):
+        r = heapq.heappop(self.free)
+        p = int(self.order[r])
+        assert self.ref[p] == 0
+        self.ref[p] = 1
+        return p
+
+    def _drop(self, p):
+        self.ref[p] -= 1
+        assert self.ref[p] >= 0
+        if self.ref[p] == 0:
+            heapq.heappush(self.free, int(self.rank[p]))
+
+    def free_pages(self):
+        return len(self.free)
+
+    # -- sequences ---------------------------------------------------------
+    def _empty_rows(self):
+        dt = np.uint16 if self.dtype == "bf16" else np.float32
+        return np.zeros((0, self.H_kv, self.d), dtype=dt)
+
+    def create(self):
+        for s in range(self.max_seqs):
+            if s not in self.seqs:
+                self.seqs[s] = {"pages": [], "len": 0, "k": self._empty_rows(), "v": self._empty_rows()}
+                return s
+        raise CacheError("ENOMEM", "no free sequence id")
+
+    def fork(self, src, prefix_len):
+        S = self._seq(src)
+        if not (0 <= prefix_len <= S["len"]):
+            raise CacheError("ERANGE", "prefix beyond source length")
+        s = self.create()
+        keep = -(-prefix_len // PAGE_TOKENS)
+        pages = list(S["pages"][:keep])
+        for p in pages:
+            self.ref[p] += 1
+        self.seqs[s].update(pages=pages, len=prefix_len,
+                            k=S["k"][:prefix_len].copy(), v=S["v"][:prefix_len].copy())
+        return s
+
+    def free_seq(self, s):
+        self.truncate(s, 0)
+        del self.seqs[s]
+
+    def truncate(self, s, m):
+        S = self._seq(s)
+        if not (0 <= m <= S["len"]):
+            raise CacheError("ERANGE", "truncate beyond length")
+        keep = -(-m // PAGE_TOKENS)
+        for p in S["pages"][keep:]:
+            self._drop(p)
+        S["pages"] = S["pages"][:keep]
+        S["len"] = m
+        S["k"] = S["k"][:m].copy()
+        S["v"] = S["v"][:m].copy()
+
+    def _seq(self, s):
+        if s not in self.seqs:
+            raise CacheError("EINVAL", "unknown sequence %r" % (s,))
+        return self.seqs[s]
+
+    def length(self, s):
+        return self._seq(s)["len"]
+
+    def block_table(self, s):
+        return list(self._seq(s)["pages"])
+
+    # -- writes --------------------------------------------------------------
+    def _pages_needed(self, S, count):
+        P = S["len"]
+        need = -(-(P + count) // PAGE_TOKENS) - len(S["pages"])
+        cow = 1 if (count > 0 and P % PAGE_TOKENS != 0 and self.ref[S["pages"][-1]] > 1) else 0
+        return need, cow
+
+    def write(self, seq_ids, k_rows, v_rows):
+        """Append k_rows[b], v_rows[b] ([c_b, H_kv, d] stored values) to
+        sequence seq_ids[b], for every b, as one atomic call."""
+        if len(set(seq_ids)) != len(seq_ids):
+            raise CacheError("EINVAL", "a sequence appears twice in one write")
+        total = 0
+        for s, kr in zip(seq_ids, k_rows):
+            S = self._seq(s)
+            c = kr.shape[0]
+            if -(-(S["len"] + c) // PAGE_TOKENS) > self.max_pages_per_seq:
+                raise CacheError("ERANGE", "sequence capacity exceeded")
+            need, cow = self._pages_needed(S, c)
+            total += need + cow
+        if total > self.free_pages():
+            raise CacheError("ENOMEM", "page pool exhausted")
+        for s, kr, vr in zip(seq_ids, k_rows, v_rows):
+            S = self._seq(s)
+            c = kr.shape[0]
+            need, cow = self._pages_needed(S, c)
+            if cow:
+                old = S["pages"][-1]
+                new = self._take()
+                self.copies.append((old, new, S["len"] % PAGE_TOKENS))
+                self._drop(old)
+                S["pages"][-1] = new
+            for _ in range(need):
+                S["pages"].append(self._take())
+            S["k"] = np.concatenate([S["k"], np.asarray(kr, dtype=S["k"].dtype)], axis=0)
+            S["v"] = np.concatenate([S["v"], np.asarray(vr, dtype=S["v"].dtype)], axis=0)
+            S["len"] += c
+
+    def kv(self, s):
+        """Logical K, V of sequence s as fp64 arrays [len, H_kv, d]."""
+        S = self._seq(s)
+        return to_f64(S["k"], self.dtype), to_f64(S["v"], self.dtype)
+
+    def raw_kv(self, s):
+        S = self._seq(s)
+        return S["k"], S["v"]
+
+
+# ---------------------------------------------------------------------------
+# Batched drivers.
+# ---------------------------------------------------------------------------
+
+def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None):
+    """[P1] 2.6: write each sequence's valid K/V rows at positions P_b.. into
+    the cache, then causal attention of the valid query rows over the cache.
+    q [B, n, H_q, d], k/v [B, n, H_kv, d] stored values.  Padding rows
+    (i >= n_b) are discarded ([P1] 2.2) and returned as zeros."""
+    dt = cache.dtype
+    B, n, H_q, d = q.shape
+    nb = [int(x) for x in valid_lengths]
+    if any(x < 1 or x > n for x in nb):
+        raise CacheError("EMASK", "each sequence needs 1..n valid rows")
+    past = [cache.length(s) for s in seq_ids]
+    cache.write(list(seq_ids), [k[b, :nb[b]] for b in range(B)], [v[b, :nb[b]] for b in range(B)])
+    out = np.zeros((B, n, H_q, d))
+    for b, s in enumerate(seq_ids):
+        K, V = cache.kv(s)
+        qpos = past[b] + np.arange(nb[b])
+        out[b, :nb[b]] = attention(to_f64(q[b, :nb[b]], dt), K, V, qpos, nthreads)
+    return out
+
+
+def append(cache: CacheModel, seq_ids, k_new, v_new, counts=None):
+    """[P3] decode: append each sequence's new k/v rows at its tail.
+    k_new/v_new [B, c, H_kv, d] (or [B, H_kv, d] for one token each)."""
+    if k_new.ndim == 3:
+        k_new, v_new = k_new[:, None], v_new[:, None]
+    B = k_new.shape[0]
+    cnt = [k_new.shape[1]] * B if counts is None else [int(c) for c in counts]
+    cache.write(list(seq_ids), [k_new[b, :cnt[b]] for b in range(B)], [v_new[b, :cnt[b]] for b in range(B)])
+
+
+def decode(cache: CacheModel, seq_ids, q, nthreads=None):
+    """[P3] single-token decode: query b at position L_b - 1 reads all L_b
+    cached entries (its own appended entry included).  q [B, H_q, d]."""
+    dt = cache.dtype
+    B, H_q, d = q.shape
+    out = np.zeros((B, H_q, d))
+    for b, s in enumerate(seq_ids):
+        K, V = cache.kv(s)
+        L = K.shape[0]
+        if L < 1:
+            raise CacheError("EMASK", "decode over an empty cache")
+        out[b] = attention(to_f64(q[b][None], dt), K, V, np.array([L - 1]), nthreads)[0]
+    return out
+

@@ -1,0 +1,318 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong scale, a wrong head map, a future key in the denominator, a transposed
+operand) fails at least one of them.  None of them re-types the oracle's own
+formula: they use printed values, closed forms, special cases and a second,
+independently written form.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+
+def _att(q, K, V, qpos):
+    return oracle.attention(np.asarray(q, float), np.asarray(K, float), np.asarray(V, float),
+                            np.asarray(qpos), nthreads=2)
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_second_position(golden):
+    g = golden("worked_example_2d.txt")
+    q = np.array([[g["q"]]])
+    K = np.array([[g["k1"]], [g["k2"]]])
+    V = np.array([[g["v1"]], [g["v2"]]])
+    out = _att(q, K, V, [1])[0, 0]
+    tol = 0.5 * 10 ** -int(g["decimals_out"])
+    assert np.all(np.abs(out - np.array(g["out_pos2"])) <= tol), out
+    # The weights: out = p1 v1 + p2 v2 with v1 = (10, 0), v2 = (0, 20).
+    tol_p = 0.5 * 10 ** -int(g["decimals_p"])
+    assert abs(out[0] / 10.0 - g["p1"]) <= tol_p
+    assert abs(out[1] / 20.0 - g["p2"]) <= tol_p
+
+
+def test_worked_example_first_position_excludes_future(golden):
+    g = golden("worked_example_2d.txt")
+    q = np.array([[g["q"]]])
+    K = np.array([[g["k1"]], [g["k2"]]])
+    V = np.array([[g["v1"]], [g["v2"]]])
+    out = _att(q, K, V, [0])[0, 0]
+    # Exactly v1: the second position must not enter the denominator either.
+    assert np.array_equal(out, np.array(g["out_pos1"]))
+
+
+def test_worked_example_scores_imply_weights(golden):
+    # The page's printed scores (q.k/sqrt(2)) and weights agree with each other
+    # through the two-element softmax (a logistic): an independent check that
+    # the fixture was transcribed consistently.
+    g = golden("worked_example_2d.txt")
+    p1 = 1.0 / (1.0 + math.exp(g["score2"] - g["score1"]))
+    assert abs(p1 - g["p1"]) <= 0.5e-6
+    assert abs(g["score1"] - 1 / math.sqrt(2)) <= 0.5e-6
+
+
+def test_workloads_worked_example_matches_fixture(golden):
+    g = golden("worked_example_2d.txt")
+    w = workloads.worked_example_2d()
+    assert np.array_equal(w["k"][0, :, 0], np.array([g["k1"], g["k2"]], dtype=np.float32))
+    assert np.array_equal(w["v"][0, :, 0], np.array([g["v1"], g["v2"]], dtype=np.float32))
+    assert np.array_equal(w["q"][0, 1, 0], np.array(g["q"], dtype=np.float32))
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_scale_is_inverse_root_head_dim():
+    # d = 4: q.k1 = 2 so the score is 2/sqrt(4) = 1; q.k2 = 0.  Two-key softmax
+    # weight of key 1 is the logistic e/(e+1) = 0.7310585786300049.
+    q = [[[2.0, 0, 0, 0]]]
+    K = [[[1.0, 0, 0, 0]], [[0.0, 0, 0, 0]]]
+    V = [[[1.0, 0, 0, 0]], [[0.0, 1, 0, 0]]]
+    out = _att(q, K, V, [1])[0, 0]
+    assert abs(out[0] - 0.7310585786300049) < 1e-15
+    assert abs(out[1] - 0.2689414213699951) < 1e-15
+    assert out[2] == 0 and out[3] == 0
+
+
+def test_single_visible_key_returns_its_value():
+    rng = np.random.default_rng(1)
+    q, K, V = rng.normal(size=(1, 3, 8)), rng.normal(size=(5, 1, 8)), rng.normal(size=(5, 1, 8))
+    out = _att(q, K, V, [0])
+    for h in range(3):
+        assert np.array_equal(out[0, h], V[0, 0])
+
+
+def test_zero_query_averages_visible_values():
+    rng = np.random.default_rng(2)
+    K, V = rng.normal(size=(9, 2, 6)), rng.normal(size=(9, 2, 6))
+    q = np.zeros((3, 4, 6))
+    pos = [0, 4, 8]
+    out = _att(q, K, V, pos)
+    for i, p in enumerate(pos):
+        for h in range(4):
+            g = h // 2
+            np.testing.assert_allclose(out[i, h], V[: p + 1, g].mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_identical_values_pass_through():
+    rng = np.random.default_rng(3)
+    c = rng.normal(size=5)
+    K = rng.normal(size=(7, 1, 5))
+    V = np.broadcast_to(c, (7, 1, 5)).copy()
+    out = _att(rng.normal(size=(4, 2, 5)), K, V, [0, 2, 5, 6])
+    np.testing.assert_allclose(out, np.broadcast_to(c, out.shape), rtol=0, atol=1e-14)
+
+
+def test_two_keys_logistic_large_scores_stable():
+    # Scores around 700 would overflow exp() without the max subtraction; the
+    # weights still follow the two-element closed form.
+    d = 2
+    q = [[[1.0, 0.0]]]
+    K = [[[990.0, 0.0]], [[991.0, 0.0]]]
+    V = [[[1.0, 0.0]], [[0.0, 1.0]]]
+    out = _att(q, K, V, [1])[0, 0]
+    s1, s2 = 990 / math.sqrt(d), 991 / math.sqrt(d)
+    p1 = 1.0 / (1.0 + math.exp(s2 - s1))
+    assert np.all(np.isfinite(out))
+    assert abs(out[0] - p1) < 1e-14 and abs(out[1] - (1 - p1)) < 1e-14
+
+
+def test_common_key_shift_leaves_output_unchanged():
+    # Adding the same vector u to every key adds q.u/sqrt(d) to the whole row
+    # of scores; softmax is invariant to that.
+    rng = np.random.default_rng(4)
+    q, K, V = rng.normal(size=(5, 4, 8)), rng.normal(size=(12, 2, 8)), rng.normal(size=(12, 2, 8))
+    u = rng.normal(size=(1, 2, 8)) * 3
+    pos = [3, 5, 7, 9, 11]
+    np.testing.assert_allclose(_att(q, K + u, V, pos), _att(q, K, V, pos), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- GQA head map
+
+@pytest.mark.parametrize("H_q,H_kv,expect", [
+    (4, 2, [0, 0, 1, 1]),
+    (6, 2, [0, 0, 0, 1, 1, 1]),
+    (6, 3, [0, 0, 1, 1, 2, 2]),
+    (3, 3, [0, 1, 2]),
+    (4, 1, [0, 0, 0, 0]),
+])
+def test_query_heads_read_contiguous_kv_groups(H_q, H_kv, expect):
+    # KV head g holds constant value rows equal to (g+1) * ones, so each query
+    # head's output names the KV head it read.  Contiguous groups of H_q/H_kv
+    # query heads share a KV head (the toy model's heads 0 and 1 both read KV
+    # head 0; a kernel indexes the KV head rather than duplicating it).
+    rng = np.random.default_rng(5)
+    d, L = 4, 6
+    V = np.stack([np.full((L, d), g + 1.0) for g in range(H_kv)], axis=1)
+    out = _att(rng.normal(size=(2, H_q, d)), rng.normal(size=(L, H_kv, d)), V, [3, 5])
+    got = [int(round(out[0, h, 0])) - 1 for h in range(H_q)]
+    assert got == expect
+
+
+def test_permuting_query_heads_within_a_group_permutes_outputs():
+    rng = np.random.default_rng(6)
+    q, K, V = rng.normal(size=(3, 8, 16)), rng.normal(size=(10, 2, 16)), rng.normal(size=(10, 2, 16))
+    pos = [2, 6, 9]
+    perm = [3, 1, 0, 2, 7, 5, 4, 6]           # stays inside the two groups of 4
+    a = _att(q, K, V, pos)
+    b = _att(q[:, perm], K, V, pos)
+    assert np.array_equal(a[:, perm], b)
+
+
+# ---------------------------------------------------------------- causality
+
+def test_future_keys_do_not_change_a_row():
+    rng = np.random.default_rng(7)
+    q, K, V = rng.normal(size=(4, 2, 8)), rng.normal(size=(10, 1, 8)), rng.normal(size=(10, 1, 8))
+    pos = [0, 3, 6, 9]
+    a = _att(q, K, V, pos)
+    K2, V2 = K.copy(), V.copy()
+    K2[7:] = rng.normal(size=K2[7:].shape) * 100
+    V2[7:] = np.nan                              # never read for rows at positions <= 6
+    b = _att(q[:3], K2, V2, pos[:3])
+    assert np.array_equal(a[:3], b)
+
+
+def test_streaming_matches_dense_masked_form():
+    rng = np.random.default_rng(8)
+    for (n_q, H_q, H_kv, d, L) in [(1, 1, 1, 1, 1), (3, 2, 1, 4, 3), (6, 6, 2, 5, 9),
+                                   (5, 8, 8, 3, 12), (4, 12, 3, 7, 20)]:
+        q = rng.normal(size=(n_q, H_q, d))
+        K, V = rng.normal(size=(L, H_kv, d)), rng.normal(size=(L, H_kv, d))
+        pos = np.sort(rng.choice(L, size=n_q, replace=n_q > L))
+        np.testing.assert_allclose(_att(q, K, V, pos), oracle.attention_dense(q, K, V, pos),
+                                   rtol=0, atol=1e-13)
+
+
+def test_brute_force_pure_python_tiny():
+    # Plain nested loops over Python floats: math.exp of scores minus the row max.
+    rng = np.random.default_rng(9)
+    H_q, H_kv, d, L = 2, 1, 3, 5
+    q, K, V = rng.normal(size=(L, H_q, d)), rng.normal(size=(L, H_kv, d)), rng.normal(size=(L, H_kv, d))
+    out = _att(q, K, V, list(range(L)))
+    for i in range(L):
+        for h in range(H_q):
+            sc = [sum(q[i, h, e] * K[j, 0, e] for e in range(d)) / math.sqrt(d) for j in range(i + 1)]
+            mx = max(sc)
+            w = [math.exp(s - mx) for s in sc]
+            ref = [sum(w[j] * V[j, 0, e] for j in range(i + 1)) / sum(w) for e in range(d)]
+            np.testing.assert_allclose(out[i, h], ref, rtol=0, atol=1e-14)
+
+
+def test_rejects_rows_without_visible_keys():
+    with pytest.raises(ValueError):
+        _att(np.zeros((1, 1, 2)), np.zeros((2, 1, 2)), np.zeros((2, 1, 2)), [2])
+    with pytest.raises(ValueError):
+        _att(np.zeros((1, 1, 2)), np.zeros((2, 1, 2)), np.zeros((2, 1, 2)), [-1])
+    with pytest.raises(ValueError):   # H_kv must divide H_q
+        _att(np.zeros((1, 3, 2)), np.zeros((2, 2, 2)), np.zeros((2, 2, 2)), [1])
+
+
+def test_thread_count_does_not_change_results():
+    rng = np.random.default_rng(10)
+    q, K, V = rng.normal(size=(7, 4, 8)), rng.normal(size=(30, 2, 8)), rng.normal(size=(30, 2, 8))
+    pos = np.arange(23, 30)
+    a = oracle.attention(q, K, V, pos, nthreads=1)
+    b = oracle.attention(q, K, V, pos, nthreads=5)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- cache drivers
+
+def _model(dtype="f32", H_kv=1, d=4, pages=64):
+    return oracle.CacheModel(pages, 8, 32, H_kv, d, dtype)
+
+
+def test_decode_equals_last_row_of_full_recompute():
+    # Cached decode must reproduce the last row of recomputing the whole
+    # context: the toy decoder compares these after every step.
+    w = workloads.tiny_fp32()
+    cm = _model()
+    s = cm.create()
+    oracle.prefill(cm, [s], w["q"], w["k"], w["v"], w["valid_lengths"])
+    allq, allk, allv = [w["q"][0]], [w["k"][0]], [w["v"][0]]
+    for t in range(3):
+        oracle.append(cm, [s], w["dec_k"][t], w["dec_v"][t])
+        got = oracle.decode(cm, [s], w["dec_q"][t])[0]
+        allq.append(w["dec_q"][t]); allk.append(w["dec_k"][t]); allv.append(w["dec_v"][t])
+        Q = np.concatenate(allq).astype(float)
+        Kf = np.concatenate(allk).astype(float)
+        Vf = np.concatenate(allv).astype(float)
+        L = Kf.shape[0]
+        full = oracle.attention_dense(Q, Kf, Vf, np.arange(L))
+        assert L == 5 + t
+        np.testing.assert_allclose(got, full[-1], rtol=0, atol=1e-12)
+
+
+def test_incremental_prefill_equals_one_shot_prefill():
+    rng = np.random.default_rng(11)
+    n1, n2, H_q, H_kv, d = 5, 7, 4, 2, 6
+    q, k, v = rng.normal(size=(1, n1 + n2, H_q, d)), rng.normal(size=(1, n1 + n2, H_kv, d)), rng.normal(size=(1, n1 + n2, H_kv, d))
+    q, k, v = (x.astype(np.float32) for x in (q, k, v))
+    a = _model(H_kv=H_kv, d=d)
+    s = a.create()
+    one = oracle.prefill(a, [s], q, k, v, [n1 + n2])[0]
+    b = _model(H_kv=H_kv, d=d)
+    t = b.create()
+    first = oracle.prefill(b, [t], q[:, :n1], k[:, :n1], v[:, :n1], [n1])[0]
+    second = oracle.prefill(b, [t], q[:, n1:], k[:, n1:], v[:, n1:], [n2])[0]
+    np.testing.assert_allclose(np.concatenate([first, second]), one, rtol=0, atol=1e-13)
+    assert np.array_equal(a.raw_kv(s)[0], b.raw_kv(t)[0])
+
+
+def test_padding_rows_never_matter():
+    rng = np.random.default_rng(12)
+    B, n, H_q, H_kv, d = 2, 9, 4, 2, 5
+    q = rng.normal(size=(B, n, H_q, d)).astype(np.float32)
+    k = rng.normal(size=(B, n, H_kv, d)).astype(np.float32)
+    v = rng.normal(size=(B, n, H_kv, d)).astype(np.float32)
+    nb = [4, 9]
+    a = _model(H_kv=H_kv, d=d)
+    sa = [a.create(), a.create()]
+    ref = oracle.prefill(a, sa, q, k, v, nb)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    q2[0, 4:], k2[0, 4:], v2[0, 4:] = np.nan, np.inf, np.nan
+    b = _model(H_kv=H_kv, d=d)
+    sb = [b.create(), b.create()]
+    got = oracle.prefill(b, sb, q2, k2, v2, nb)
+    assert np.array_equal(ref, got)
+    assert np.all(got[0, 4:] == 0)
+    assert a.length(sa[0]) == 4 and a.length(sa[1]) == 9
+
+
+def test_edit_at_m_keeps_rows_before_m():
+    # Changing the rows at positions >= m leaves every output row < m and the
+    # cached K/V < m untouched (prefix stable, suffix invalid).
+    rng = np.random.default_rng(13)
+    n, m, H_q, H_kv, d = 24, 10, 4, 2, 6
+    q = rng.normal(size=(1, n, H_q, d)).astype(np.float32)
+    k = rng.normal(size=(1, n, H_kv, d)).astype(np.float32)
+    v = rng.normal(size=(1, n, H_kv, d)).astype(np.float32)
+    a = _model(H_kv=H_kv, d=d)
+    s = a.create()
+    ref = oracle.prefill(a, [s], q, k, v, [n])[0]
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    for x in (q2, k2, v2):
+        x[0, m:] = rng.normal(size=x[0, m:].shape)
+    b = _model(H_kv=H_kv, d=d)
+    t = b.create()
+    got = oracle.prefill(b, [t], q2, k2, v2, [n])[0]
+    assert np.array_equal(ref[:m], got[:m])
+    assert not np.allclose(ref[m:], got[m:])
+    # Truncate at m and re-prefill the suffix: identical to the full re-run.
+    a.truncate(s, m)
+    re = oracle.prefill(a, [s], q2[:, m:], k2[:, m:], v2[:, m:], [n - m])[0]
+    np.testing.assert_allclose(re, got[m:], rtol=0, atol=1e-13)
+    assert np.array_equal(a.raw_kv(s)[0], b.raw_kv(t)[0])
+
+
+def test_bf16_inputs_are_read_exactly():
+    x = np.array([1.0, -2.5, 3.140625, 1e-3], dtype=np.float32)
+    bits = workloads.bf16_bits(x)
+    back = oracle.to_f64(bits, "bf16")
+    assert back[0] == 1.0 and back[1] == -2.5 and back[2] == 3.140625
+    assert abs(back[3] - 1e-3) < 1e-3 * 2 ** -8
