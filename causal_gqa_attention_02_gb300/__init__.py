@@ -1,0 +1,313 @@
+"""Python binding of libgqa (include/gqa.h): causal GQA prefill and decode
+over a paged KV cache on GB300.
+
+This module only marshals arguments: it turns torch tensors into device
+pointers and CUDA streams into handles, and raises on non-zero status.  Every
+step of the hot path runs in the CUDA library.  There is no fallback: if
+``_lib/libgqa.so`` has not been built, importing this package fails.
+
+PyTorch supplies device memory (the page pool, q/k/v/out) and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import work  # noqa: F401  (work counts for throughput figures)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgqa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libgqa.so is not built (%s); run __graft_entry__.build() first" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, EINVAL, ERANGE, EMASK, ENOMEM, ELAYOUT, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+ERRNAMES = {EINVAL: "EINVAL", ERANGE: "ERANGE", EMASK: "EMASK", ENOMEM: "ENOMEM",
+            ELAYOUT: "ELAYOUT", ECUDA: "ECUDA", EDEVICE: "EDEVICE"}
+DTYPE_BF16, DTYPE_F32 = 1, 2
+PAGE_TOKENS = 16
+LAYOUT_VERSION = 1
+DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("keys_post_position", ctypes.c_int32),
+                ("layout_version", ctypes.c_int32), ("page_order", _I32P)]
+
+
+class LayoutMetadata(ctypes.Structure):
+    _fields_ = [("keys_post_position", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32), ("layout_version", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def _sig(name, res, *args):
+    fn = getattr(_lib, name)
+    fn.restype = res
+    fn.argtypes = list(args)
+    return fn
+
+
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_sig("gqa_pool_bytes", _sz, ctypes.POINTER(CacheDesc))
+_sig("gqa_cache_create", ctypes.c_int, ctypes.POINTER(CacheDesc), _vp, _sz, ctypes.POINTER(_vp))
+_sig("gqa_cache_destroy", ctypes.c_int, _vp)
+_sig("gqa_cache_layout", ctypes.c_int, _vp, ctypes.POINTER(LayoutMetadata))
+_sig("gqa_layout_compatible", ctypes.c_int, ctypes.POINTER(LayoutMetadata), ctypes.POINTER(LayoutMetadata))
+_sig("gqa_seq_create", ctypes.c_int, _vp, _I32P)
+_sig("gqa_seq_fork", ctypes.c_int, _vp, _i32, _i32, _I32P)
+_sig("gqa_seq_free", ctypes.c_int, _vp, _i32)
+_sig("gqa_seq_length", ctypes.c_int, _vp, _i32, _I32P)
+_sig("gqa_seq_block_table", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P)
+_sig("gqa_free_pages", ctypes.c_int, _vp, _I32P)
+_sig("gqa_page_refcount", ctypes.c_int, _vp, _i32, _I32P)
+_sig("attn_prefill", ctypes.c_int, _vp, _i32, _I32P, _i32, _i32, _vp, _vp, _vp, _I32P, _I32P, _vp, _vp)
+_sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
+_sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
+_sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
+_sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
+_sig("gqa_last_error", ctypes.c_char_p)
+_sig("gqa_version", ctypes.c_char_p)
+
+
+class GqaError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (ERRNAMES.get(code, "?"), code, msg))
+        self.code = code
+        self.name = ERRNAMES.get(code, "?")
+
+
+def _check(rc):
+    if rc != OK:
+        raise GqaError(rc, _lib.gqa_last_error().decode(errors="replace"))
+
+
+def version() -> str:
+    return _lib.gqa_version().decode()
+
+
+def _i32_array(values):
+    if values is None:
+        return None, None
+    vals = [int(x) for x in (values.reshape(-1).tolist() if hasattr(values, "reshape") else values)]
+    arr = (ctypes.c_int32 * max(1, len(vals)))(*vals)
+    return arr, ctypes.cast(arr, _I32P)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+_TORCH_DTYPE = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
+
+
+class Cache:
+    """A paged KV cache: a torch-owned device page pool plus the library's
+    host metadata.  ``metadata_only=True`` creates no pool (no GPU needed);
+    launching calls then only validate and update block tables/lengths."""
+
+    def __init__(self, num_kv_heads, head_dim, num_pages, max_seqs, max_pages_per_seq,
+                 dtype="bf16", page_order=None, device=None, metadata_only=False,
+                 keys_post_position=1, layout_version=LAYOUT_VERSION):
+        self.dtype_code = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
+        self.torch_dtype = _TORCH_DTYPE[self.dtype_code]
+        self._order_keep, order_ptr = _i32_array(page_order)
+        self.desc = CacheDesc(self.dtype_code, num_kv_heads, head_dim, PAGE_TOKENS, num_pages,
+                              max_seqs, max_pages_per_seq, keys_post_position, layout_version,
+                              order_ptr)
+        self.num_kv_heads, self.head_dim, self.num_pages = num_kv_heads, head_dim, num_pages
+        self.max_seqs, self.max_pages_per_seq = max_seqs, max_pages_per_seq
+        self.pool = None
+        self._h = ctypes.c_void_p()
+        nbytes = _lib.gqa_pool_bytes(ctypes.byref(self.desc))
+        if metadata_only:
+            _check(_lib.gqa_cache_create(ctypes.byref(self.desc), None, 0, ctypes.byref(self._h)))
+        else:
+            dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+            self.pool = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+            with torch.cuda.device(dev):
+                _check(_lib.gqa_cache_create(ctypes.byref(self.desc), ctypes.c_void_p(self.pool.data_ptr()),
+                                             nbytes, ctypes.byref(self._h)))
+
+    @property
+    def handle(self):
+        return self._h
+
+    def pool_view(self):
+        """The pool as [num_pages, 2 (K, V), H_kv, 16, d_h] of the cache dtype."""
+        return self.pool.view(self.torch_dtype).view(self.num_pages, 2, self.num_kv_heads,
+                                                     PAGE_TOKENS, self.head_dim)
+
+    def close(self):
+        if self._h:
+            _lib.gqa_cache_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- sequences -----------------------------------------------------------
+    def seq_create(self) -> int:
+        s = ctypes.c_int32()
+        _check(_lib.gqa_seq_create(self._h, ctypes.byref(s)))
+        return s.value
+
+    def seq_fork(self, src: int, prefix_len: int) -> int:
+        s = ctypes.c_int32()
+        _check(_lib.gqa_seq_fork(self._h, src, prefix_len, ctypes.byref(s)))
+        return s.value
+
+    def seq_free(self, seq: int):
+        _check(_lib.gqa_seq_free(self._h, seq))
+
+    def seq_length(self, seq: int) -> int:
+        n = ctypes.c_int32()
+        _check(_lib.gqa_seq_length(self._h, seq, ctypes.byref(n)))
+        return n.value
+
+    def block_table(self, seq: int):
+        cnt = ctypes.c_int32()
+        buf = (ctypes.c_int32 * max(1, self.max_pages_per_seq))()
+        _check(_lib.gqa_seq_block_table(self._h, seq, buf, self.max_pages_per_seq, ctypes.byref(cnt)))
+        return list(buf[: cnt.value])
+
+    def free_pages(self) -> int:
+        n = ctypes.c_int32()
+        _check(_lib.gqa_free_pages(self._h, ctypes.byref(n)))
+        return n.value
+
+    def refcount(self, page: int) -> int:
+        n = ctypes.c_int32()
+        _check(_lib.gqa_page_refcount(self._h, page, ctypes.byref(n)))
+        return n.value
+
+    def layout(self) -> LayoutMetadata:
+        m = LayoutMetadata()
+        _check(_lib.gqa_cache_layout(self._h, ctypes.byref(m)))
+        return m
+
+    def check(self, stream=None) -> int:
+        """Synchronise and read/clear the device error word (0 = clean)."""
+        flags = ctypes.c_int32()
+        rc = _lib.gqa_cache_check(self._h, _stream_handle(stream) if self.pool is not None else None,
+                                  ctypes.byref(flags))
+        if rc not in (OK, EDEVICE):
+            _check(rc)
+        return flags.value
+
+
+def layout_compatible(a: LayoutMetadata, b: LayoutMetadata) -> bool:
+    rc = _lib.gqa_layout_compatible(ctypes.byref(a), ctypes.byref(b))
+    if rc not in (OK, ELAYOUT):
+        _check(rc)
+    return rc == OK
+
+
+def _dev_ptr(t, what, dtype, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % what)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (what, tuple(t.shape), tuple(shape)))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_prefill(cache: Cache, seq_ids, q, k, v, valid_lengths, positions=None, out=None, stream=None):
+    """Causal GQA prefill (see include/gqa.h).  q [B, n, H_q, d],
+    k/v [B, n, H_kv, d]; returns out [B, n, H_q, d]."""
+    B, n, H_q = len(seq_ids), q.shape[1], q.shape[2]
+    dt = cache.torch_dtype
+    d = cache.head_dim
+    if out is None:
+        out = torch.empty_like(q)
+    keep_s, sp = _i32_array(seq_ids)
+    keep_v, vp = _i32_array(valid_lengths)
+    keep_p, pp = _i32_array(positions)
+    _check(_lib.attn_prefill(cache.handle, B, sp, n, H_q,
+                             _dev_ptr(q, "q", dt, (B, n, H_q, d)),
+                             _dev_ptr(k, "k", dt, (B, n, cache.num_kv_heads, d)),
+                             _dev_ptr(v, "v", dt, (B, n, cache.num_kv_heads, d)),
+                             vp, pp, _dev_ptr(out, "out", dt, (B, n, H_q, d)),
+                             _stream_handle(stream) if cache.pool is not None else None))
+    return out
+
+
+def attn_prefill_meta(cache: Cache, seq_ids, n, H_q, valid_lengths, positions=None):
+    """attn_prefill on a metadata-only cache (no tensors)."""
+    keep_s, sp = _i32_array(seq_ids)
+    keep_v, vp = _i32_array(valid_lengths)
+    keep_p, pp = _i32_array(positions)
+    _check(_lib.attn_prefill(cache.handle, len(seq_ids), sp, n, H_q, None, None, None, vp, pp, None, None))
+
+
+def kv_append(cache: Cache, seq_ids, k_new, v_new, counts=None, stream=None):
+    """Append rows at each sequence's tail.  k_new/v_new [B, n, H_kv, d] or
+    [B, H_kv, d] (one row each)."""
+    if k_new.dim() == 3:
+        k_new, v_new = k_new.unsqueeze(1), v_new.unsqueeze(1)
+    B, n = len(seq_ids), k_new.shape[1]
+    shape = (B, n, cache.num_kv_heads, cache.head_dim)
+    keep_s, sp = _i32_array(seq_ids)
+    keep_c, cp = _i32_array(counts)
+    _check(_lib.kv_append(cache.handle, B, sp, n, cp,
+                          _dev_ptr(k_new, "k_new", cache.torch_dtype, shape),
+                          _dev_ptr(v_new, "v_new", cache.torch_dtype, shape),
+                          _stream_handle(stream)))
+
+
+def kv_append_meta(cache: Cache, seq_ids, n, counts=None):
+    keep_s, sp = _i32_array(seq_ids)
+    keep_c, cp = _i32_array(counts)
+    _check(_lib.kv_append(cache.handle, len(seq_ids), sp, n, cp, None, None, None))
+
+
+def attn_decode(cache: Cache, seq_ids, q, out=None, stream=None):
+    """Single-token decode.  q [B, H_q, d]; returns out [B, H_q, d]."""
+    B, H_q = len(seq_ids), q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    shape = (B, H_q, cache.head_dim)
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
+                            _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+    return out
+
+
+def attn_decode_meta(cache: Cache, seq_ids, H_q):
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode(cache.handle, len(seq_ids), sp, H_q, None, None, None))
+
+
+def kv_truncate(cache: Cache, seq: int, m: int):
+    _check(_lib.kv_truncate(cache.handle, seq, m))
+
+
+def exported_symbols():
+    """Names the header declares; used by the tests to check the exports."""
+    return ["gqa_pool_bytes", "gqa_cache_create", "gqa_cache_destroy", "gqa_cache_layout",
+            "gqa_layout_compatible", "gqa_seq_create", "gqa_seq_fork", "gqa_seq_free",
+            "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
+            "attn_prefill", "kv_append", "attn_decode", "kv_truncate", "gqa_cache_check",
+            "gqa_last_error", "gqa_version"]

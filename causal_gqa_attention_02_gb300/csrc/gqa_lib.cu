@@ -1,0 +1,758 @@
+// gqa_lib.cu -- the C ABI of include/gqa.h: the host-side cache manager
+// (page pool, block tables, reference counts, copy-on-write, truncation),
+// every precondition check, and the launch sequences of the hot path.
+//
+// Sources: "第二章 Prefill：整层状态演化与 KV 建立" (preconditions 2.1, mask
+// and invalid rows 2.2, attention 2.3, cache contract and invariants 2.2 in
+// 2.5, pseudocode 2.6, prefix reuse 2.9, failure table 2.11);
+// "KV Cache 与 Prefill/Decode 推理路径" (edit at token m; PagedAttention block
+// table and free pool; prefix sharing with reference counts).
+//
+// Host/device split.  All bookkeeping lives here, on the host: a call first
+// validates every argument against the current metadata (so a rejected call
+// changes nothing and queues nothing, as preconditions 2.1 demand), then
+// commits the metadata change, uploads the block-table entries it changed
+// and a small per-call descriptor block with stream-ordered copies, and
+// finally queues its kernels.  Nothing here waits for the GPU.
+#include <algorithm>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "gqa.h"
+#include "kernels.cuh"
+
+using namespace gqa;
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(GQA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct SeqState {
+    bool live = false;
+    int32_t len = 0;
+    std::vector<int32_t> pages;
+    int32_t dirty_lo = INT_MAX, dirty_hi = 0;   // block-table entries changed since upload
+};
+
+struct WriteReq {
+    int32_t seq, count;
+};
+
+}  // namespace
+
+struct gqa_cache {
+    gqa_cache_desc desc{};
+    int esize = 0;
+    bool meta_only = false;
+    void *pool = nullptr;
+    std::vector<int32_t> order, rank, ref;
+    std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ranks;
+    std::vector<SeqState> seqs;
+    std::vector<int32_t> dirty_list;
+    std::vector<int32_t> h_tab;          // host mirror [max_seqs][max_pages_per_seq]
+    int32_t *d_tab = nullptr;            // device block tables
+    int32_t *d_err = nullptr;            // device error word
+    char *d_stage = nullptr;             // per-call descriptors
+    size_t stage_cap = 0;
+    float *d_ws = nullptr;               // decode split partials
+    size_t ws_cap = 0;
+    std::vector<char> h_stage;
+    int device = -1;
+    int num_sms = 0;
+    int cc = 0;                          // compute capability major*10+minor
+
+    size_t stride() const { return (size_t)desc.max_pages_per_seq; }
+
+    int32_t take_page()
+    {
+        const int32_t r = free_ranks.top();
+        free_ranks.pop();
+        const int32_t p = order[r];
+        ref[p] = 1;
+        return p;
+    }
+
+    void drop_page(int32_t p)
+    {
+        if (--ref[p] == 0)
+            free_ranks.push(rank[p]);
+    }
+
+    void set_entry(int32_t s, int32_t idx, int32_t page)
+    {
+        h_tab[(size_t)s * stride() + idx] = page;
+        SeqState &S = seqs[s];
+        if (S.dirty_hi <= S.dirty_lo)
+            dirty_list.push_back(s);
+        S.dirty_lo = std::min(S.dirty_lo, idx);
+        S.dirty_hi = std::max(S.dirty_hi, idx + 1);
+    }
+
+    PoolView view() const
+    {
+        PoolView pv;
+        pv.pool = pool;
+        pv.tables = d_tab;
+        pv.stride = desc.max_pages_per_seq;
+        pv.num_pages = desc.num_pages;
+        pv.H_kv = desc.num_kv_heads;
+        pv.d = desc.head_dim;
+        pv.err = d_err;
+        return pv;
+    }
+};
+
+namespace {
+
+bool live(const gqa_cache *c, int32_t s)
+{
+    return s >= 0 && s < c->desc.max_seqs && c->seqs[s].live;
+}
+
+int32_t pages_for(int64_t tokens) { return (int32_t)((tokens + kPageTokens - 1) / kPageTokens); }
+
+// Validate a batched write: live and distinct sequences, capacity, pages.
+int check_write(const gqa_cache *c, const WriteReq *r, int B)
+{
+    std::vector<char> seen((size_t)c->desc.max_seqs, 0);
+    int64_t need_total = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t s = r[b].seq;
+        if (!live(c, s))
+            return fail(GQA_EINVAL, "batch entry %d: sequence %d is not live", b, s);
+        if (seen[s])
+            return fail(GQA_EINVAL, "sequence %d appears twice in one write", s);
+        seen[s] = 1;
+        const SeqState &S = c->seqs[s];
+        const int64_t new_len = (int64_t)S.len + r[b].count;
+        if (pages_for(new_len) > c->desc.max_pages_per_seq)
+            return fail(GQA_ERANGE, "sequence %d: %lld tokens exceed its capacity of %d pages", s,
+                        (long long)new_len, c->desc.max_pages_per_seq);
+        need_total += pages_for(new_len) - (int64_t)S.pages.size();
+        if (r[b].count > 0 && S.len % kPageTokens != 0 && c->ref[S.pages.back()] > 1)
+            need_total += 1;                          // copy-on-write of the shared tail page
+    }
+    if (need_total > (int64_t)c->free_ranks.size())
+        return fail(GQA_ENOMEM, "page pool exhausted: %lld pages needed, %zu free",
+                    (long long)need_total, c->free_ranks.size());
+    return GQA_OK;
+}
+
+// Apply a validated write to the metadata.  Pages are taken sequence by
+// sequence in batch order: the copy-on-write page first, then new pages.
+void commit_write(gqa_cache *c, const WriteReq *r, int B, std::vector<SeqDesc> &sds,
+                  std::vector<CowDesc> &cows)
+{
+    sds.resize(B);
+    for (int b = 0; b < B; ++b) {
+        const int32_t s = r[b].seq;
+        SeqState &S = c->seqs[s];
+        const int32_t past = S.len, count = r[b].count;
+        if (count > 0 && past % kPageTokens != 0 && c->ref[S.pages.back()] > 1) {
+            const int32_t old = S.pages.back();
+            const int32_t np = c->take_page();
+            cows.push_back(CowDesc{old, np, past % kPageTokens, 0});
+            c->drop_page(old);
+            S.pages.back() = np;
+            c->set_entry(s, (int32_t)S.pages.size() - 1, np);
+        }
+        while ((int64_t)S.pages.size() * kPageTokens < (int64_t)past + count) {
+            const int32_t np = c->take_page();
+            S.pages.push_back(np);
+            c->set_entry(s, (int32_t)S.pages.size() - 1, np);
+        }
+        S.len = past + count;
+        sds[b] = SeqDesc{s, past, count, 0};
+    }
+}
+
+int check_device(const gqa_cache *c)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev != c->device)
+        return fail(GQA_EINVAL, "current device %d is not the cache's device %d", dev, c->device);
+    return GQA_OK;
+}
+
+// Upload the block-table entries changed since the last upload.
+int upload_tables(gqa_cache *c, cudaStream_t st)
+{
+    for (int32_t s : c->dirty_list) {
+        SeqState &S = c->seqs[s];
+        if (S.dirty_hi > S.dirty_lo) {
+            const size_t off = (size_t)s * c->stride() + S.dirty_lo;
+            cudaError_t e = cudaMemcpyAsync(c->d_tab + off, c->h_tab.data() + off,
+                                            (size_t)(S.dirty_hi - S.dirty_lo) * sizeof(int32_t),
+                                            cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "block-table upload");
+        }
+        S.dirty_lo = INT_MAX;
+        S.dirty_hi = 0;
+    }
+    c->dirty_list.clear();
+    return GQA_OK;
+}
+
+// Per-call descriptor block: appended pieces are 16-byte aligned.
+struct Stage {
+    std::vector<char> &buf;
+    explicit Stage(std::vector<char> &b) : buf(b) { buf.clear(); }
+    template <typename T>
+    size_t add(const T *p, size_t count)
+    {
+        const size_t off = (buf.size() + 15) & ~(size_t)15;
+        buf.resize(off + count * sizeof(T));
+        if (count)
+            memcpy(buf.data() + off, p, count * sizeof(T));
+        return off;
+    }
+};
+
+int upload_stage(gqa_cache *c, cudaStream_t st)
+{
+    const size_t bytes = c->h_stage.size();
+    if (bytes > c->stage_cap) {
+        if (c->d_stage) {
+            cudaError_t e = cudaFree(c->d_stage);     // synchronises the device
+            c->d_stage = nullptr;
+            c->stage_cap = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaFree(stage)");
+        }
+        const size_t cap = std::max<size_t>((bytes + 65535) & ~(size_t)65535, 65536);
+        cudaError_t e = cudaMalloc((void **)&c->d_stage, cap);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(stage)");
+        c->stage_cap = cap;
+    }
+    if (bytes) {
+        cudaError_t e = cudaMemcpyAsync(c->d_stage, c->h_stage.data(), bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "descriptor upload");
+    }
+    return GQA_OK;
+}
+
+int ensure_ws(gqa_cache *c, size_t floats)
+{
+    const size_t bytes = floats * sizeof(float);
+    if (bytes <= c->ws_cap)
+        return GQA_OK;
+    if (c->d_ws) {
+        cudaError_t e = cudaFree(c->d_ws);
+        c->d_ws = nullptr;
+        c->ws_cap = 0;
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFree(workspace)");
+    }
+    const size_t cap = (bytes + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+    cudaError_t e = cudaMalloc((void **)&c->d_ws, cap);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    c->ws_cap = cap;
+    return GQA_OK;
+}
+
+int launched(cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess)
+        return cuda_fail(e, what);
+    return GQA_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char *gqa_last_error(void) { return t_err.c_str(); }
+
+const char *gqa_version(void) { return "libgqa 0.1.0 (sm_103a)"; }
+
+size_t gqa_pool_bytes(const gqa_cache_desc *d)
+{
+    if (!d || d->num_pages < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
+        (d->dtype != GQA_DTYPE_BF16 && d->dtype != GQA_DTYPE_F32))
+        return 0;
+    const size_t es = d->dtype == GQA_DTYPE_BF16 ? 2 : 4;
+    return (size_t)d->num_pages * 2 * (size_t)d->num_kv_heads * kPageTokens * (size_t)d->head_dim * es;
+}
+
+int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes, gqa_cache **out)
+{
+    if (!desc || !out)
+        return fail(GQA_EINVAL, "NULL argument");
+    *out = nullptr;
+    const gqa_cache_desc &d = *desc;
+    if (d.dtype != GQA_DTYPE_BF16 && d.dtype != GQA_DTYPE_F32)
+        return fail(GQA_EINVAL, "unknown dtype %d", d.dtype);
+    if (d.num_kv_heads < 1 || d.head_dim < 1 || d.head_dim > 256)
+        return fail(GQA_EINVAL, "H_kv must be >= 1 and d_h in 1..256");
+    if (d.page_tokens != GQA_PAGE_TOKENS)
+        return fail(GQA_EINVAL, "page_tokens must be %d", GQA_PAGE_TOKENS);
+    if (d.num_pages < 1 || d.max_seqs < 1 || d.max_pages_per_seq < 1)
+        return fail(GQA_EINVAL, "num_pages, max_seqs and max_pages_per_seq must be >= 1");
+    if ((int64_t)d.max_pages_per_seq * kPageTokens > INT_MAX)
+        return fail(GQA_EINVAL, "max_pages_per_seq too large");
+    if (d.keys_post_position != 1)
+        return fail(GQA_ELAYOUT, "only post-position keys are supported (keys_post_position = 1)");
+    if (d.layout_version != GQA_LAYOUT_VERSION)
+        return fail(GQA_ELAYOUT, "layout_version %d, this library writes %d", d.layout_version,
+                    GQA_LAYOUT_VERSION);
+    const size_t need = gqa_pool_bytes(desc);
+    if (pool_dev) {
+        if (pool_bytes < need)
+            return fail(GQA_EINVAL, "pool has %zu bytes, the description needs %zu", pool_bytes, need);
+        if ((uintptr_t)pool_dev % 256 != 0)
+            return fail(GQA_EINVAL, "pool must be 256-byte aligned");
+    }
+
+    gqa_cache *c = new gqa_cache();
+    c->desc = d;
+    c->desc.page_order = nullptr;
+    c->esize = d.dtype == GQA_DTYPE_BF16 ? 2 : 4;
+    c->meta_only = pool_dev == nullptr;
+    c->pool = pool_dev;
+    c->order.resize(d.num_pages);
+    c->rank.assign(d.num_pages, -1);
+    for (int32_t r = 0; r < d.num_pages; ++r) {
+        const int32_t p = d.page_order ? d.page_order[r] : r;
+        if (p < 0 || p >= d.num_pages || c->rank[p] != -1) {
+            delete c;
+            return fail(GQA_EINVAL, "page_order is not a permutation of 0..num_pages-1");
+        }
+        c->order[r] = p;
+        c->rank[p] = r;
+    }
+    c->ref.assign(d.num_pages, 0);
+    {
+        std::vector<int32_t> ranks(d.num_pages);
+        for (int32_t r = 0; r < d.num_pages; ++r)
+            ranks[r] = r;
+        c->free_ranks = std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>>(
+            std::greater<int32_t>(), std::move(ranks));
+    }
+    c->seqs.resize(d.max_seqs);
+    c->h_tab.assign((size_t)d.max_seqs * d.max_pages_per_seq, 0);
+
+    if (!c->meta_only) {
+        cudaError_t e = cudaGetDevice(&c->device);
+        int major = 0, minor = 0;
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, c->device);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, c->device);
+        c->cc = major * 10 + minor;
+        if (e == cudaSuccess)
+            e = cudaMalloc((void **)&c->d_tab, c->h_tab.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemset(c->d_tab, 0, c->h_tab.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMalloc((void **)&c->d_err, sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemset(c->d_err, 0, sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemset(pool_dev, 0, need);         // every slot starts as a finite +0
+        if (e == cudaSuccess)
+            e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            gqa_cache_destroy(c);
+            return cuda_fail(e, "cache device set-up");
+        }
+    }
+    *out = c;
+    return GQA_OK;
+}
+
+int gqa_cache_destroy(gqa_cache *c)
+{
+    if (!c)
+        return GQA_OK;
+    cudaError_t e = cudaSuccess;
+    if (!c->meta_only) {
+        e = cudaDeviceSynchronize();
+        if (c->d_tab) cudaFree(c->d_tab);
+        if (c->d_err) cudaFree(c->d_err);
+        if (c->d_stage) cudaFree(c->d_stage);
+        if (c->d_ws) cudaFree(c->d_ws);
+    }
+    delete c;
+    return e == cudaSuccess ? GQA_OK : cuda_fail(e, "cache destroy");
+}
+
+int gqa_cache_layout(const gqa_cache *c, gqa_layout_metadata *out)
+{
+    if (!c || !out)
+        return fail(GQA_EINVAL, "NULL argument");
+    out->keys_post_position = c->desc.keys_post_position;
+    out->dtype = c->desc.dtype;
+    out->page_tokens = c->desc.page_tokens;
+    out->layout_version = c->desc.layout_version;
+    out->num_kv_heads = c->desc.num_kv_heads;
+    out->head_dim = c->desc.head_dim;
+    return GQA_OK;
+}
+
+int gqa_layout_compatible(const gqa_layout_metadata *a, const gqa_layout_metadata *b)
+{
+    if (!a || !b)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (a->keys_post_position != b->keys_post_position)
+        return fail(GQA_ELAYOUT, "position convention differs (post- vs pre-position keys)");
+    if (a->dtype != b->dtype || a->page_tokens != b->page_tokens || a->layout_version != b->layout_version ||
+        a->num_kv_heads != b->num_kv_heads || a->head_dim != b->head_dim)
+        return fail(GQA_ELAYOUT, "precision, page size, layout version or KV shape differs");
+    return GQA_OK;
+}
+
+int gqa_seq_create(gqa_cache *c, int32_t *seq_out)
+{
+    if (!c || !seq_out)
+        return fail(GQA_EINVAL, "NULL argument");
+    for (int32_t s = 0; s < c->desc.max_seqs; ++s) {
+        if (!c->seqs[s].live) {
+            SeqState &S = c->seqs[s];
+            S.live = true;
+            S.len = 0;
+            S.pages.clear();
+            *seq_out = s;
+            return GQA_OK;
+        }
+    }
+    return fail(GQA_ENOMEM, "all %d sequence ids are in use", c->desc.max_seqs);
+}
+
+int gqa_seq_fork(gqa_cache *c, int32_t src, int32_t prefix_len, int32_t *seq_out)
+{
+    if (!c || !seq_out)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (!live(c, src))
+        return fail(GQA_EINVAL, "sequence %d is not live", src);
+    if (prefix_len < 0 || prefix_len > c->seqs[src].len)
+        return fail(GQA_ERANGE, "prefix %d outside 0..%d", prefix_len, c->seqs[src].len);
+    int32_t s = -1;
+    int rc = gqa_seq_create(c, &s);
+    if (rc != GQA_OK)
+        return rc;
+    const int32_t keep = pages_for(prefix_len);
+    SeqState &S = c->seqs[s];
+    for (int32_t i = 0; i < keep; ++i) {
+        const int32_t p = c->seqs[src].pages[i];
+        c->ref[p] += 1;
+        S.pages.push_back(p);
+        c->set_entry(s, i, p);
+    }
+    S.len = prefix_len;
+    *seq_out = s;
+    return GQA_OK;
+}
+
+int kv_truncate(gqa_cache *c, int32_t seq, int32_t m)
+{
+    if (!c)
+        return fail(GQA_EINVAL, "NULL cache");
+    if (!live(c, seq))
+        return fail(GQA_EINVAL, "sequence %d is not live", seq);
+    SeqState &S = c->seqs[seq];
+    if (m < 0 || m > S.len)
+        return fail(GQA_ERANGE, "truncate to %d outside 0..%d", m, S.len);
+    const int32_t keep = pages_for(m);
+    for (size_t i = keep; i < S.pages.size(); ++i)
+        c->drop_page(S.pages[i]);
+    S.pages.resize(keep);
+    S.len = m;
+    return GQA_OK;
+}
+
+int gqa_seq_free(gqa_cache *c, int32_t seq)
+{
+    int rc = kv_truncate(c, seq, 0);
+    if (rc != GQA_OK)
+        return rc;
+    c->seqs[seq].live = false;
+    return GQA_OK;
+}
+
+int gqa_seq_length(const gqa_cache *c, int32_t seq, int32_t *len_out)
+{
+    if (!c || !len_out)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (!live(c, seq))
+        return fail(GQA_EINVAL, "sequence %d is not live", seq);
+    *len_out = c->seqs[seq].len;
+    return GQA_OK;
+}
+
+int gqa_seq_block_table(const gqa_cache *c, int32_t seq, int32_t *out, int32_t cap, int32_t *count_out)
+{
+    if (!c || !count_out)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (!live(c, seq))
+        return fail(GQA_EINVAL, "sequence %d is not live", seq);
+    const SeqState &S = c->seqs[seq];
+    *count_out = (int32_t)S.pages.size();
+    if ((size_t)cap < S.pages.size() || (!out && !S.pages.empty()))
+        return fail(GQA_ERANGE, "block table has %zu entries, capacity %d", S.pages.size(), cap);
+    std::copy(S.pages.begin(), S.pages.end(), out);
+    return GQA_OK;
+}
+
+int gqa_free_pages(const gqa_cache *c, int32_t *out)
+{
+    if (!c || !out)
+        return fail(GQA_EINVAL, "NULL argument");
+    *out = (int32_t)c->free_ranks.size();
+    return GQA_OK;
+}
+
+int gqa_page_refcount(const gqa_cache *c, int32_t page, int32_t *out)
+{
+    if (!c || !out)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (page < 0 || page >= c->desc.num_pages)
+        return fail(GQA_ERANGE, "page %d outside 0..%d", page, c->desc.num_pages - 1);
+    *out = c->ref[page];
+    return GQA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The hot path.
+// ---------------------------------------------------------------------------
+
+int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
+                 const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions,
+                 void *out, void *stream)
+{
+    if (!c || !seq_ids || !valid_lengths)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || n < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B, n and H_q must be >= 1");
+    if (H_q % c->desc.num_kv_heads != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", c->desc.num_kv_heads, H_q);
+    if (!c->meta_only && (!q || !k || !v || !out))
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    std::vector<WriteReq> req(B);
+    int32_t max_nb = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t nb = valid_lengths[b];
+        if (nb < 1 || nb > n)
+            return fail(GQA_EMASK, "batch entry %d: valid length %d outside 1..%d leaves a query row "
+                                   "without a finite score", b, nb, n);
+        req[b] = WriteReq{seq_ids[b], nb};
+        max_nb = std::max(max_nb, nb);
+    }
+    int rc = check_write(c, req.data(), B);
+    if (rc != GQA_OK)
+        return rc;
+    if (positions) {
+        for (int b = 0; b < B; ++b) {
+            const int32_t P = c->seqs[seq_ids[b]].len;
+            for (int32_t i = 0; i < req[b].count; ++i)
+                if (positions[(size_t)b * n + i] != P + i)
+                    return fail(GQA_ERANGE, "batch entry %d row %d: position %d, the cache continues at %d",
+                                b, i, positions[(size_t)b * n + i], P + i);
+        }
+    }
+    if (!c->meta_only && (rc = check_device(c)) != GQA_OK)
+        return rc;
+
+    std::vector<SeqDesc> sds;
+    std::vector<CowDesc> cows;
+    commit_write(c, req.data(), B, sds, cows);
+    if (c->meta_only)
+        return GQA_OK;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    Stage stg(c->h_stage);
+    const size_t o_sds = stg.add(sds.data(), sds.size());
+    const size_t o_cow = stg.add(cows.data(), cows.size());
+    if ((rc = upload_stage(c, st)) != GQA_OK)
+        return rc;
+    const PoolView pv = c->view();
+    const SeqDesc *d_sds = (const SeqDesc *)(c->d_stage + o_sds);
+    if (!cows.empty() &&
+        (rc = launched(launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st),
+                       "copy-on-write kernel")) != GQA_OK)
+        return rc;
+    if ((rc = launched(launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st), "cache write kernel")) != GQA_OK)
+        return rc;
+    return launched(launch_attn_simt(pv, c->desc.dtype, d_sds, B, n, H_q, q, out, st), "attention kernel");
+}
+
+int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,
+              const void *k_new, const void *v_new, void *stream)
+{
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || n < 1)
+        return fail(GQA_EINVAL, "B and n must be >= 1");
+    if (!c->meta_only && (!k_new || !v_new))
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    std::vector<WriteReq> req(B);
+    int32_t max_c = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t cnt = counts ? counts[b] : n;
+        if (cnt < 0 || cnt > n)
+            return fail(GQA_EINVAL, "batch entry %d: count %d outside 0..%d", b, cnt, n);
+        req[b] = WriteReq{seq_ids[b], cnt};
+        max_c = std::max(max_c, cnt);
+    }
+    int rc = check_write(c, req.data(), B);
+    if (rc != GQA_OK)
+        return rc;
+    if (!c->meta_only && (rc = check_device(c)) != GQA_OK)
+        return rc;
+    std::vector<SeqDesc> sds;
+    std::vector<CowDesc> cows;
+    commit_write(c, req.data(), B, sds, cows);
+    if (c->meta_only)
+        return GQA_OK;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    Stage stg(c->h_stage);
+    const size_t o_sds = stg.add(sds.data(), sds.size());
+    const size_t o_cow = stg.add(cows.data(), cows.size());
+    if ((rc = upload_stage(c, st)) != GQA_OK)
+        return rc;
+    const PoolView pv = c->view();
+    if (!cows.empty() &&
+        (rc = launched(launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st),
+                       "copy-on-write kernel")) != GQA_OK)
+        return rc;
+    return launched(launch_cache_write(pv, c->esize, (const SeqDesc *)(c->d_stage + o_sds), B, n, max_c, k_new,
+                                       v_new, st),
+                    "cache write kernel");
+}
+
+int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q, void *out,
+                void *stream)
+{
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    if (!c->meta_only && (!q || !out))
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    std::vector<SeqDesc> sds(B);
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t s = seq_ids[b];
+        if (!live(c, s))
+            return fail(GQA_EINVAL, "batch entry %d: sequence %d is not live", b, s);
+        const int32_t L = c->seqs[s].len;
+        if (L < 1)
+            return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
+        sds[b] = SeqDesc{s, L - 1, 1, 0};
+        total += L;
+    }
+    int rc;
+    if (c->meta_only)
+        return GQA_OK;
+    if ((rc = check_device(c)) != GQA_OK)
+        return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    const PoolView pv = c->view();
+    const int G = H_q / H_kv;
+    Stage stg(c->h_stage);
+    const size_t o_sds = stg.add(sds.data(), sds.size());
+    if (c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && decode_split_supported(G)) {
+        // Chunk: a multiple of the page size, large enough to amortise the
+        // partials, small enough for several CTAs per SM.
+        int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
+        int chunk = (int)std::min<int64_t>(512, std::max<int64_t>(128, (target + 127) / 128 * 128));
+        std::vector<DecodeItem> items;
+        std::vector<int32_t> start(B + 1, 0);
+        for (int b = 0; b < B; ++b) {
+            const int32_t L = sds[b].past + 1;
+            const int32_t ns = (L + chunk - 1) / chunk;
+            start[b] = (int32_t)items.size();
+            for (int32_t s = 0; s < ns; ++s)
+                items.push_back(DecodeItem{b, s});
+        }
+        start[B] = (int32_t)items.size();
+        const size_t o_items = stg.add(items.data(), items.size());
+        const size_t o_start = stg.add(start.data(), start.size());
+        const size_t n_part = items.size() * (size_t)H_kv * G;
+        if ((rc = ensure_ws(c, n_part * 128 + n_part * 2)) != GQA_OK)
+            return rc;
+        if ((rc = upload_stage(c, st)) != GQA_OK)
+            return rc;
+        float *ws_o = c->d_ws, *ws_ml = c->d_ws + n_part * 128;
+        if ((rc = launched(launch_decode_split(pv, (const SeqDesc *)(c->d_stage + o_sds),
+                                               (const DecodeItem *)(c->d_stage + o_items), (int)items.size(),
+                                               chunk, H_q, q, ws_o, ws_ml, st),
+                           "decode split kernel")) != GQA_OK)
+            return rc;
+        return launched(launch_decode_combine((const int32_t *)(c->d_stage + o_start), B, H_q, H_kv, ws_o,
+                                              ws_ml, out, st),
+                        "decode combine kernel");
+    }
+    if ((rc = upload_stage(c, st)) != GQA_OK)
+        return rc;
+    return launched(launch_attn_simt(pv, c->desc.dtype, (const SeqDesc *)(c->d_stage + o_sds), B, 1, H_q, q,
+                                     out, st),
+                    "attention kernel");
+}
+
+int gqa_cache_check(gqa_cache *c, void *stream, int32_t *flags_out)
+{
+    if (!c || !flags_out)
+        return fail(GQA_EINVAL, "NULL argument");
+    *flags_out = 0;
+    if (c->meta_only)
+        return GQA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(st);
+    int32_t h = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&h, c->d_err, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h != 0)
+        e = cudaMemset(c->d_err, 0, sizeof(int32_t));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "error-word read");
+    *flags_out = h;
+    if (h)
+        return fail(GQA_EDEVICE, "device error word 0x%x", h);
+    return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// k_simt.cu -- generic causal GQA attention over the paged cache on the
+// CUDA cores, for fp32 caches and head sizes the tensor-core kernels do not
+// take.  It is the precise path (fp32 arithmetic, expf), not the fast one.
+//
+// What it computes: "第二章 Prefill：整层状态演化与 KV 建立", section 2.3:
+// query head h reads KV head g(h) = floor(h*H_kv/H_q); scores are
+// <q, k_j>/sqrt(d_h) over the visible keys; a stable softmax over the finite
+// scores weights V.  Visibility: a row at absolute position p sees cached
+// positions 0..p ("KV Cache 与 Prefill/Decode 推理路径", incremental prefill:
+// the old prefix is a fully visible rectangle, the new block a triangle).
+//
+// Shape of the work: one warp per query row.  Keys are taken 32 at a time,
+// one key per lane (each lane forms its own dot product against the row's q
+// held in shared memory), so a block of 32 scores costs one warp max and one
+// warp sum; the running max / sum / output are rescaled once per block
+// (online softmax, the FlashAttention recurrence).  The value pass keeps the
+// output row spread over the lanes (lane owns elements lane, lane+32, ...).
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMaxD = 256;
+
+__device__ __forceinline__ float ldf(const float *p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float *p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_max(float x)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
+                 const T *__restrict__ q, T *__restrict__ out)
+{
+    __shared__ float sq[kWarps][kMaxD];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int i = blockIdx.x * kWarps + warp;
+    if (i >= n)
+        return;                                   // no block-wide barrier follows
+    const SeqDesc sd = seqs[b];
+    const int d = pv.d, H_kv = pv.H_kv;
+    T *o = out + (((size_t)b * n + i) * H_q + h) * d;
+    if (i >= sd.count) {                          // padding row: discarded, written as 0
+        for (int e = lane; e < d; e += 32)
+            stf(o + e, 0.0f);
+        return;
+    }
+    const int g = (int)(((long long)h * H_kv) / H_q);
+    const T *qi = q + (((size_t)b * n + i) * H_q + h) * d;
+    float *qs = sq[warp];
+    for (int e = lane; e < d; e += 32)
+        qs[e] = ldf(qi + e);
+    __syncwarp();
+
+    const float root_d = sqrtf((float)d);
+    const int pos = sd.past + i;                  // visible keys 0..pos
+    const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
+    const T *pool = (const T *)pv.pool;
+    const size_t page_elems = (size_t)2 * H_kv * kPageTokens * d;
+    const size_t k_off = (size_t)g * kPageTokens * d;
+    const size_t v_off = (size_t)(H_kv + g) * kPageTokens * d;
+
+    float m = -INFINITY, l = 0.0f;
+    float acc[kMaxD / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxD / 32; ++j)
+        acc[j] = 0.0f;
+
+    for (int kb = 0; kb <= pos; kb += 32) {
+        const int t = kb + lane;
+        float s = -INFINITY;
+        if (t <= pos) {
+            const int page = tab[t / kPageTokens];
+            if ((unsigned)page < (unsigned)pv.num_pages) {
+                const T *kr = pool + (size_t)page * page_elems + k_off + (size_t)(t % kPageTokens) * d;
+                float dot = 0.0f;
+                for (int e = 0; e < d; ++e)
+                    dot = fmaf(qs[e], ldf(kr + e), dot);
+                s = dot / root_d;
+            } else {
+                atomicOr(pv.err, kErrPageId);
+            }
+        }
+        const float m_new = fmaxf(m, warp_max(s));
+        const float corr = (m == -INFINITY) ? 0.0f : expf(m - m_new);
+        const float p = (s == -INFINITY) ? 0.0f : expf(s - m_new);
+        l = l * corr + warp_sum(p);
+#pragma unroll
+        for (int j = 0; j < kMaxD / 32; ++j)
+            acc[j] *= corr;
+        const int nk = min(32, pos - kb + 1);
+        for (int u = 0; u < nk; ++u) {
+            const float pu = __shfl_sync(0xffffffffu, p, u);
+            const int tu = kb + u;
+            const int page = tab[tu / kPageTokens];
+            if ((unsigned)page >= (unsigned)pv.num_pages)
+                continue;
+            const T *vr = pool + (size_t)page * page_elems + v_off + (size_t)(tu % kPageTokens) * d;
+#pragma unroll
+            for (int j = 0; j < kMaxD / 32; ++j) {
+                const int e = lane + 32 * j;
+                if (e < d)
+                    acc[j] = fmaf(pu, ldf(vr + e), acc[j]);
+            }
+        }
+        m = m_new;
+    }
+    const float inv = 1.0f / l;
+#pragma unroll
+    for (int j = 0; j < kMaxD / 32; ++j) {
+        const int e = lane + 32 * j;
+        if (e < d)
+            stf(o + e, acc[j] * inv);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const PoolView &pv, int dtype, const SeqDesc *d_seqs, int B, int n,
+                             int H_q, const void *q, void *out, cudaStream_t st)
+{
+    if (pv.d > kMaxD || pv.d < 1)
+        return cudaErrorInvalidValue;
+    if (B <= 0 || n <= 0)
+        return cudaSuccess;
+    dim3 grid((unsigned)((n + kWarps - 1) / kWarps), (unsigned)H_q, (unsigned)B);
+    if (dtype == 2)
+        attn_simt_kernel<float><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
+                                                            (float *)out);
+    else
+        attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(
+            pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,81 @@
+// kernels.cuh -- descriptors and launchers shared by the host library
+// (gqa_lib.cu) and the device kernels (k_*.cu).  Internal; the public
+// boundary is include/gqa.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+constexpr int kPageTokens = 16;
+
+// A view of the paged pool and the block tables as the kernels see them.
+// Pool element (page, kv, head, slot, e) lives at
+//   ((page * 2 + kv) * H_kv + head) * 16 * d + slot * d + e       (kv: 0 = K, 1 = V)
+struct PoolView {
+    void *pool;              // device, element type = cache dtype
+    const int32_t *tables;   // device [max_seqs][stride]: logical page -> physical page
+    int32_t stride;          // max_pages_per_seq
+    int32_t num_pages;
+    int32_t H_kv;
+    int32_t d;
+    int32_t *err;            // device error word (GQA_DEVERR_* bits)
+};
+
+// One batch entry of a launching call.
+struct SeqDesc {
+    int32_t row;    // sequence id == block-table row
+    int32_t past;   // tokens already cached before this call's rows (decode: L - 1)
+    int32_t count;  // rows of this call that are valid (decode: 1)
+    int32_t pad_;
+};
+
+// Copy-on-write of slots [0, slots) of page src into page dst (K and V, all heads).
+struct CowDesc {
+    int32_t src, dst, slots, pad_;
+};
+
+// One split-K decode work item: batch entry b, token chunk `split`.
+struct DecodeItem {
+    int32_t b, split;
+};
+
+// Error-word bits (mirror include/gqa.h).
+constexpr int32_t kErrPageId = 1;
+constexpr int32_t kErrTimeout = 2;
+constexpr int32_t kErrShape = 4;
+
+// ---- launchers (each returns the launch's cudaError_t) --------------------
+
+// Element-wise copy unit in bytes (16, 8, 4 or 2) usable for rows of
+// `row_bytes` with the given base pointers.
+int copy_unit_bytes(size_t row_bytes, const void *a, const void *b, const void *c);
+
+cudaError_t launch_cow_copy(const PoolView &pv, int esize, const CowDesc *d_cows, int ncows,
+                            cudaStream_t st);
+
+// Write rows c < seqs[b].count of k/v [B, n, H_kv, d] to positions past+c.
+cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_seqs, int B, int n,
+                               int max_count, const void *k, const void *v, cudaStream_t st);
+
+// Generic causal attention over the pool (any d <= 256, fp32 or bf16):
+// rows i < n of q [B, n, H_q, d]; row i is valid when i < count and sits at
+// position past + i; invalid rows are written as zeros.
+cudaError_t launch_attn_simt(const PoolView &pv, int dtype, const SeqDesc *d_seqs, int B, int n,
+                             int H_q, const void *q, void *out, cudaStream_t st);
+
+// bf16, d = 128 split-K decode.  Returns cudaErrorNotSupported when the
+// group size H_q / H_kv has no instantiation.
+bool decode_split_supported(int group);
+cudaError_t launch_decode_split(const PoolView &pv, const SeqDesc *d_seqs, const DecodeItem *d_items,
+                                int n_items, int chunk, int H_q, const void *q, float *ws_o,
+                                float *ws_ml, cudaStream_t st);
+cudaError_t launch_decode_combine(const int32_t *d_item_start, int B, int H_q, int H_kv,
+                                  const float *ws_o, const float *ws_ml, void *out, cudaStream_t st);
+
+// bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).
+bool prefill_tc_supported(int group, int H_kv);
+
+}  // namespace gqa

@@ -1,0 +1,33 @@
+"""Algorithmic work counts used to turn times into throughput.
+
+Prefill: the number of (query, key) pairs with a finite score, times
+4 * d_h flops per pair (2 for the QK^T product, 2 for the PV product) and
+H_q heads -- the causal count, excluding padding rows and keys above the
+diagonal even where a kernel touches them.  "模型执行：从 token 到 Prefill 与
+Decode" counts attention work the same way (its "score pairs" table, and
+4 B H_q S^2 d for the full, unmasked matrix products).
+
+Decode: the K/V bytes the method must read, each KV head counted once (the
+query heads of a group share it: "KV Cache 与 Prefill/Decode 推理路径", GQA
+lesson), 2 (K and V) * H_kv * d_h * element size per cached token.
+"""
+from __future__ import annotations
+
+
+def causal_pairs(past: int, new: int) -> int:
+    """Pairs (i, j) with j <= past + i for new query rows i = 0..new-1 at
+    positions past..past+new-1."""
+    past, new = int(past), int(new)
+    return new * past + new * (new + 1) // 2
+
+
+def prefill_flops(pasts, news, H_q: int, d: int) -> int:
+    return 4 * int(d) * int(H_q) * sum(causal_pairs(p, n) for p, n in zip(pasts, news))
+
+
+def decode_kv_bytes(lengths, H_kv: int, d: int, esize: int = 2) -> int:
+    return sum(int(L) for L in lengths) * 2 * int(H_kv) * int(d) * int(esize)
+
+
+def decode_flops(lengths, H_q: int, d: int) -> int:
+    return 4 * int(d) * int(H_q) * sum(int(L) for L in lengths)

@@ -1,0 +1,266 @@
+/*
+ * gqa.h -- C ABI of libgqa: causal grouped-query attention, prefill and
+ * decode, over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *  [P1] "第二章 Prefill：整层状态演化与 KV 建立" (glenzli.com, vol. 2, ch. 2):
+ *       2.1 prefill interface and preconditions 2.1; 2.2 mask M and the rule
+ *       for invalid query rows; 2.3 attention equations (g(h), S, A, O);
+ *       2.5 cache contract, layout_metadata and cache invariants 2.2;
+ *       2.6 prefill pseudocode (write valid positions, then attend);
+ *       2.9 prefix reuse conditions; 2.11 failure table.
+ *  [P2] "模型执行：从 token 到 Prefill 与 Decode" (blog.mlxb.cc): prefill vs
+ *       decode shapes; decode reads the old cache plus its own new entry.
+ *  [P3] "KV Cache 与 Prefill/Decode 推理路径" (wiki.maxwellmou.com, unit 10):
+ *       edit at token m (keep the KV before m, truncate, re-prefill the
+ *       suffix); GQA head axis; causal tile skipping; PagedAttention block
+ *       tables and the free pool; incremental prefill mask; prefix sharing
+ *       with reference counts.
+ *
+ * Conventions for every call
+ *  - Every function returns GQA_OK (0) or a negative GQA_E* status.  The
+ *    message of the last failure on the calling thread is gqa_last_error().
+ *  - Preconditions are checked on the host before anything is queued on the
+ *    GPU.  A call that fails a check changes neither the cache nor any output
+ *    ([P1] preconditions 2.1: fail before the first layer runs).
+ *  - "device" pointers are CUDA device addresses on the current device;
+ *    "host" pointers are ordinary host memory, read before the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Launching calls are asynchronous and stream-ordered; they do
+ *    not synchronise except to report a CUDA error.  All calls on one cache
+ *    must be issued on one stream, or ordered by the caller.
+ *  - Tensors are dense, row-major, in the cache's element type (bf16 or
+ *    fp32).  Shapes below list the outermost dimension first.
+ *  - Token-major layouts: q is [B, n, H_q, d_h] and k, v are
+ *    [B, n, H_kv, d_h] -- a permuted view of [P1] 2.3's [B, H, n, d_h].
+ *
+ * Page pool layout (device memory owned by the caller, described by the
+ * cache): num_pages pages of page_tokens = 16 token slots.  Page p holds
+ *      K at elements [((p*2 + 0)*H_kv + h)*16*d_h + slot*d_h + e]
+ *      V at elements [((p*2 + 1)*H_kv + h)*16*d_h + slot*d_h + e]
+ * so one (page, K|V, kv-head) block of 16 x d_h is contiguous.  Token t of a
+ * sequence lives in logical page t/16 at slot t%16; a per-sequence block
+ * table maps logical pages to physical pages ([P3] PagedAttention).
+ *
+ * Allocation rules (deterministic; the tests restate them independently):
+ *  - a free page is taken in the order `page_order` gives (identity when
+ *    NULL): always the free page that comes first in that order;
+ *  - pages carry reference counts; a page returns to the pool when its count
+ *    reaches zero ([P3] prefix tree: shared blocks are reclaimed only after
+ *    every request that uses them is done);
+ *  - writing into a tail page that another sequence shares first copies its
+ *    occupied slots to a fresh page (copy-on-write);
+ *  - within one batched call, pages are taken sequence by sequence in batch
+ *    order, and per sequence the copy-on-write page first, then new pages in
+ *    logical order;
+ *  - a new sequence gets the smallest unused id in [0, max_seqs).
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GQA_OK        0
+#define GQA_EINVAL   -1  /* bad argument: NULL pointer, bad shape, unknown or duplicated sequence */
+#define GQA_ERANGE   -2  /* a length, position, page id or capacity is out of range */
+#define GQA_EMASK    -3  /* a valid query row would have no finite score ([P1] 2.3: reject at mask construction) */
+#define GQA_ENOMEM   -4  /* the page pool or the sequence-id space is exhausted */
+#define GQA_ELAYOUT  -5  /* layout_metadata incompatible ([P1] invariant 2.2 item 5; 2.9 item 4) */
+#define GQA_ECUDA    -6  /* a CUDA runtime call failed */
+#define GQA_EDEVICE  -7  /* a kernel reported an error word (see gqa_cache_check) */
+
+/* Device error-word bits reported by gqa_cache_check. */
+#define GQA_DEVERR_PAGE_ID   1  /* a block-table entry was >= num_pages (access skipped) */
+#define GQA_DEVERR_TIMEOUT   2  /* a bounded wait inside a kernel gave up */
+#define GQA_DEVERR_SHAPE     4  /* a kernel saw a shape it does not support (work skipped) */
+
+#define GQA_DTYPE_BF16 1
+#define GQA_DTYPE_F32  2
+
+#define GQA_PAGE_TOKENS    16
+#define GQA_LAYOUT_VERSION 1
+
+/* Cache description ([P1] 2.5: cache_config fixes the KV layout and the
+ * position convention). */
+typedef struct {
+    int32_t dtype;               /* GQA_DTYPE_BF16 or GQA_DTYPE_F32                        */
+    int32_t num_kv_heads;        /* H_kv >= 1                                              */
+    int32_t head_dim;            /* d_h, 1..256 (bf16 d_h = 128 takes the tensor-core path) */
+    int32_t page_tokens;         /* must be GQA_PAGE_TOKENS                                 */
+    int32_t num_pages;           /* pages in the pool, >= 1                                 */
+    int32_t max_seqs;            /* sequence ids are 0..max_seqs-1                          */
+    int32_t max_pages_per_seq;   /* block-table capacity of one sequence                    */
+    int32_t keys_post_position;  /* must be 1: keys are stored after the position transform
+                                    ([P1] 2.5: K used by attention; pre-transform caches are
+                                    a different contract)                                    */
+    int32_t layout_version;      /* must be GQA_LAYOUT_VERSION                              */
+    const int32_t *page_order;   /* host, optional: permutation of 0..num_pages-1 giving the
+                                    order in which free pages are handed out (NULL = identity).
+                                    Copied; the caller keeps ownership.                      */
+} gqa_cache_desc;
+
+/* layout_metadata of [P1] 2.5 / invariant 2.2 item 5. */
+typedef struct {
+    int32_t keys_post_position;
+    int32_t dtype;
+    int32_t page_tokens;
+    int32_t layout_version;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} gqa_layout_metadata;
+
+typedef struct gqa_cache gqa_cache;
+
+/* Bytes the page pool of `desc` occupies: num_pages * 2 * H_kv * 16 * d_h *
+ * element size.  Returns 0 for an invalid description. */
+size_t gqa_pool_bytes(const gqa_cache_desc *desc);
+
+/* Create a cache over a caller-owned device pool (`pool_dev`, at least
+ * gqa_pool_bytes(desc) bytes, 256-byte aligned).  The library allocates its
+ * own small device metadata (block tables, lengths, per-call descriptors, an
+ * error word) with cudaMalloc on the current device and clears the pool
+ * (cudaMemset, synchronous) so that every slot holds a finite value.
+ *
+ * pool_dev == NULL makes a metadata-only cache: no device memory is touched
+ * or allocated; launching calls validate their arguments and update block
+ * tables and lengths exactly as they would on a device cache, but queue no
+ * GPU work and write no outputs.  It exists so the host-side allocator can be
+ * exercised without a GPU.
+ * Errors: GQA_EINVAL (bad description, pool too small, misaligned),
+ *         GQA_ELAYOUT (keys_post_position != 1 or unknown layout_version),
+ *         GQA_ECUDA. */
+int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes,
+                     gqa_cache **out);
+
+/* Release the cache's host and device metadata (synchronises the device).
+ * The pool stays the caller's.  NULL is accepted. */
+int gqa_cache_destroy(gqa_cache *cache);
+
+/* The cache's layout_metadata ([P1] 2.5). */
+int gqa_cache_layout(const gqa_cache *cache, gqa_layout_metadata *out);
+
+/* GQA_OK if a cache written under `a` may be read under `b` (every field
+ * equal), else GQA_ELAYOUT ([P1] 2.9 item 4; invariant 2.2 item 5). */
+int gqa_layout_compatible(const gqa_layout_metadata *a, const gqa_layout_metadata *b);
+
+/* ---- sequences (host metadata only; no GPU work) ------------------------ */
+
+/* New empty sequence; smallest unused id.  GQA_ENOMEM if none is free. */
+int gqa_seq_create(gqa_cache *cache, int32_t *seq_out);
+
+/* New sequence that shares the first `prefix_len` positions of `src`
+ * ([P1] 2.9 prefix reuse; [P3] prefix sharing): it references src's first
+ * ceil(prefix_len/16) pages (reference counts + 1) and has length
+ * prefix_len.  GQA_ERANGE unless 0 <= prefix_len <= length(src). */
+int gqa_seq_fork(gqa_cache *cache, int32_t src, int32_t prefix_len, int32_t *seq_out);
+
+/* Drop every page reference of `seq` and release its id. */
+int gqa_seq_free(gqa_cache *cache, int32_t seq);
+
+/* Current logical length of `seq`. */
+int gqa_seq_length(const gqa_cache *cache, int32_t seq, int32_t *len_out);
+
+/* Copy `seq`'s block table (physical page of each logical page) into host
+ * `out` (capacity `cap` entries); *count_out = number of pages in the table.
+ * GQA_ERANGE if cap is too small (nothing copied). */
+int gqa_seq_block_table(const gqa_cache *cache, int32_t seq, int32_t *out, int32_t cap,
+                        int32_t *count_out);
+
+/* Number of free pages and the reference count of page `page`. */
+int gqa_free_pages(const gqa_cache *cache, int32_t *out);
+int gqa_page_refcount(const gqa_cache *cache, int32_t page, int32_t *out);
+
+/* ---- the hot path --------------------------------------------------------- */
+
+/* Causal GQA prefill, incremental when the sequences already hold tokens
+ * ([P1] 2.2-2.3, 2.6; [P3] incremental prefill).
+ *
+ * For each batch entry b, with sequence s = seq_ids[b] of current length P_b
+ * and n_b = valid_lengths[b] valid (right-aligned padding) rows:
+ *  1. the K/V rows i < n_b are written to the cache at positions P_b + i,
+ *     bit for bit; padding rows are never written ([P1] 2.6; invariant 2.2
+ *     item 4);
+ *  2. for every query head h and valid row i, with g(h) = floor(h*H_kv/H_q)
+ *     ([P1] 2.3), the output is softmax over the finite scores
+ *     <q[b,i,h], K[s, j, g(h)]> / sqrt(d_h), j = 0 .. P_b + i, applied to V:
+ *     the old prefix is fully visible and the new block is lower-triangular
+ *     ([P3] incremental prefill);
+ *  3. padding rows i >= n_b of `out` are written as zeros (they are
+ *     discarded, [P1] 2.2);
+ *  4. the sequence's length becomes P_b + n_b.
+ *
+ * Arguments
+ *  seq_ids        host int32[B], distinct live sequences.
+ *  n              padded rows per batch entry (>= 1).
+ *  H_q            query heads; H_kv must divide it ([P1] 2.3).
+ *  q              device [B, n, H_q, d_h]      (read)
+ *  k, v           device [B, n, H_kv, d_h]     (read; post-position keys)
+ *  valid_lengths  host int32[B], 1 <= n_b <= n.
+ *  positions      host int32[B, n] or NULL.  When given, positions[b, i]
+ *                 must equal P_b + i for every valid row: positions continue
+ *                 the cached sequence and never restart ([P1] 2.11, position
+ *                 IDs restarting after reuse).  NULL means exactly that.
+ *  out            device [B, n, H_q, d_h]      (written)
+ * Errors: GQA_EINVAL (NULL pointer, shapes, H_kv does not divide H_q,
+ *         duplicate or unknown sequence), GQA_EMASK (n_b < 1 or n_b > n:
+ *         a row without a finite score), GQA_ERANGE (positions, sequence
+ *         capacity), GQA_ENOMEM (pool exhausted), GQA_ECUDA. */
+int attn_prefill(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q,
+                 const void *q, const void *k, const void *v,
+                 const int32_t *valid_lengths, const int32_t *positions,
+                 void *out, void *stream);
+
+/* Append new K/V rows at each sequence's tail without attention ([P3]
+ * decode: append the step's k_t, v_t after the old cache; [P1] 2.6 cache
+ * write).  Row c < counts[b] of entry b goes to position P_b + c.
+ *  seq_ids  host int32[B], distinct live sequences.
+ *  n        rows per entry in k_new/v_new (1 for a decode step).
+ *  counts   host int32[B] with 0 <= counts[b] <= n, or NULL (= n for all).
+ *  k_new, v_new  device [B, n, H_kv, d_h].
+ * Errors: GQA_EINVAL, GQA_ERANGE (capacity), GQA_ENOMEM, GQA_ECUDA. */
+int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
+              const int32_t *counts, const void *k_new, const void *v_new, void *stream);
+
+/* Single-token decode ([P3] decode lesson: one query reads every cached key;
+ * [P2]: old cache plus this step's own entry).  Query b sits at position
+ * L_b - 1 of sequence seq_ids[b] (L_b = its current length, which includes
+ * the entry appended for this step) and attends over all L_b cached tokens
+ * through the sequence's block table:
+ *      out[b, h, :] = sum_t softmax_t(<q[b,h], K[t, g(h)]>/sqrt(d_h)) V[t, g(h)].
+ *  seq_ids  host int32[B], live sequences of length >= 1 (repeats allowed).
+ *  q        device [B, H_q, d_h];  out  device [B, H_q, d_h].
+ * Split-K partials live in a library-owned device workspace that grows with
+ * cudaMalloc on first use of a larger shape.
+ * Errors: GQA_EINVAL, GQA_EMASK (empty sequence), GQA_ECUDA. */
+int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
+                const void *q, void *out, void *stream);
+
+/* Prefix-edit invalidation ([P3] edit at token m): keep positions < m of
+ * `seq`, drop the rest.  Pages wholly beyond position m lose one reference
+ * (and return to the pool at zero).  A partially kept tail page stays; if it
+ * is shared, the next write copies it first.  Host metadata only.
+ * Errors: GQA_EINVAL (unknown sequence), GQA_ERANGE unless 0 <= m <= length. */
+int kv_truncate(gqa_cache *cache, int32_t seq, int32_t m);
+
+/* Synchronise `stream`, read and clear the cache's device error word.
+ * *flags_out receives GQA_DEVERR_* bits (0 = clean).  Returns GQA_EDEVICE
+ * if any bit was set, GQA_ECUDA on a CUDA error. */
+int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *gqa_last_error(void);
+
+/* Library version string. */
+const char *gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H_ */

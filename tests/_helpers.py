@@ -1,0 +1,66 @@
+"""Shared helpers for the GPU parity tests: host <-> device marshalling of the
+seeded inputs, reading the page pool back through a block table, and the
+comparison protocol (exact for cache bytes, lengths and tables; declared
+tolerances for attention outputs)."""
+import numpy as np
+import torch
+
+import oracle
+
+TOL = {"f32": {"max": 1e-5}, "bf16": {"max": 2e-2, "mean": 2e-3}}
+
+
+def dev(a, dt, device="cuda"):
+    a = np.ascontiguousarray(a)
+    if dt == "bf16":
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def host_f64(t, dt):
+    t = t.detach().cpu()
+    if dt == "bf16":
+        return oracle.to_f64(t.view(torch.int16).numpy().view(np.uint16), "bf16")
+    return t.numpy().astype(np.float64)
+
+
+def raw_pool(cache):
+    """Pool as host raw values [pages, 2, H_kv, 16, d] (uint16 bits or f32)."""
+    pv = cache.pool_view().detach().cpu()
+    if cache.torch_dtype == torch.bfloat16:
+        return pv.view(torch.int16).numpy().view(np.uint16)
+    return pv.numpy()
+
+
+def gather_seq(pool, table, length):
+    """Logical K, V [length, H_kv, d] of one sequence, read through its table."""
+    t = np.arange(length)
+    pages = np.asarray(table, dtype=np.int64)[t // 16]
+    slots = t % 16
+    return pool[pages, 0, :, slots, :], pool[pages, 1, :, slots, :]
+
+
+def assert_cache_matches(cache, model, seq_pairs):
+    """Lengths and block tables equal; every cached K/V value bit-identical."""
+    pool = raw_pool(cache)
+    for s_lib, s_ref in seq_pairs:
+        L = model.length(s_ref)
+        assert cache.seq_length(s_lib) == L
+        assert cache.block_table(s_lib) == model.block_table(s_ref)
+        K, V = gather_seq(pool, cache.block_table(s_lib), L)
+        rk, rv = model.raw_kv(s_ref)
+        assert np.array_equal(K, rk), "cached K differs"
+        assert np.array_equal(V, rv), "cached V differs"
+
+
+def assert_close(got, ref, dt, what=""):
+    diff = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), what + ": non-finite output"
+    assert diff.max() <= TOL[dt]["max"], "%s max abs %g" % (what, diff.max())
+    if "mean" in TOL[dt]:
+        assert diff.mean() <= TOL[dt]["mean"], "%s mean abs %g" % (what, diff.mean())
+    return diff.max(), diff.mean()
+
+
+def valid_mask(valid_lengths, n):
+    return np.arange(n)[None, :] < np.asarray(valid_lengths)[:, None]

@@ -1,0 +1,220 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every symbol the
+header declares, and its host-side logic (validation, allocator, reference
+counts, copy-on-write planning, truncation) agrees with the oracle's cache
+model.  Metadata-only caches need no GPU and queue no device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+gqa = pytest.importorskip("causal_gqa_attention_02_gb300")
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gqa.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    body = text[text.index('extern "C" {'):]
+    names = re.findall(r"^(?:const\s+)?(?:int|size_t|char|void)\s*\*?\s*(\w+)\s*\(", body, re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "attn_prefill" in names and "attn_decode" in names and "kv_truncate" in names
+    lib = ctypes.CDLL(gqa.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(gqa.exported_symbols()) == names
+
+
+def test_version_string():
+    assert "sm_103a" in gqa.version()
+
+
+def _pair(pages=64, seqs=8, per_seq=32, H_kv=2, d=8, order=None):
+    lib = gqa.Cache(H_kv, d, pages, seqs, per_seq, dtype="f32", page_order=order, metadata_only=True)
+    model = oracle.CacheModel(pages, seqs, per_seq, H_kv, d, "f32", page_order=order)
+    return lib, model
+
+
+def _same_state(lib, model):
+    for s in model.seqs:
+        assert lib.seq_length(s) == model.length(s)
+        assert lib.block_table(s) == model.block_table(s)
+    assert lib.free_pages() == model.free_pages()
+    for p in range(model.num_pages):
+        assert lib.refcount(p) == model.ref[p]
+
+
+def _rows(c, H_kv=2, d=8):
+    return np.zeros((c, H_kv, d), dtype=np.float32)
+
+
+def test_allocator_matches_oracle_model_under_random_operations():
+    rng = np.random.default_rng(7)
+    order = rng.permutation(96)
+    lib, model = _pair(pages=96, seqs=6, per_seq=40, order=order)
+    live = []
+    for step in range(400):
+        op = rng.integers(0, 6)
+        try:
+            if op == 0 or not live:
+                s_m = model.create()
+                s_l = lib.seq_create()
+                assert s_l == s_m
+                live.append(s_m)
+            elif op == 1:                                     # batched prefill
+                batch = list(rng.choice(live, size=min(len(live), int(rng.integers(1, 4))), replace=False))
+                n = int(rng.integers(1, 40))
+                nb = [int(rng.integers(1, n + 1)) for _ in batch]
+                err_m = err_l = None
+                try:
+                    model.write(batch, [_rows(x) for x in nb], [_rows(x) for x in nb])
+                except oracle.CacheError as e:
+                    err_m = e.kind
+                try:
+                    gqa.attn_prefill_meta(lib, batch, n, 4, nb)
+                except gqa.GqaError as e:
+                    err_l = e.name
+                assert err_m == err_l
+            elif op == 2:                                     # append
+                batch = list(rng.choice(live, size=min(len(live), int(rng.integers(1, 4))), replace=False))
+                cnt = [int(rng.integers(0, 3)) for _ in batch]
+                err_m = err_l = None
+                try:
+                    model.write(batch, [_rows(x) for x in cnt], [_rows(x) for x in cnt])
+                except oracle.CacheError as e:
+                    err_m = e.kind
+                try:
+                    gqa.kv_append_meta(lib, batch, 2, cnt)
+                except gqa.GqaError as e:
+                    err_l = e.name
+                assert err_m == err_l
+            elif op == 3:                                     # fork
+                src = int(rng.choice(live))
+                k = int(rng.integers(0, model.length(src) + 1))
+                try:
+                    s_m = model.fork(src, k)
+                except oracle.CacheError as e:
+                    with pytest.raises(gqa.GqaError):
+                        lib.seq_fork(src, k)
+                    assert e.kind == "ENOMEM"
+                else:
+                    assert lib.seq_fork(src, k) == s_m
+                    live.append(s_m)
+            elif op == 4:                                     # truncate
+                s = int(rng.choice(live))
+                m = int(rng.integers(0, model.length(s) + 1))
+                model.truncate(s, m)
+                gqa.kv_truncate(lib, s, m)
+            else:                                             # free
+                s = int(rng.choice(live))
+                model.free_seq(s)
+                lib.seq_free(s)
+                live.remove(s)
+        except oracle.CacheError as e:
+            assert e.kind == "ENOMEM"
+            with pytest.raises(gqa.GqaError):
+                lib.seq_create()
+        _same_state(lib, model)
+    assert len(model.copies) > 0          # copy-on-write was exercised
+
+
+def test_prefill_rejections_change_nothing():
+    lib, model = _pair(pages=7, per_seq=4)
+    a, b = lib.seq_create(), lib.seq_create()
+    gqa.attn_prefill_meta(lib, [a], 20, 4, [20])
+    before = (lib.block_table(a), lib.seq_length(a), lib.free_pages())
+    cases = [
+        (dict(seq_ids=[a], n=8, H_q=4, valid_lengths=[0]), "EMASK"),          # no valid row
+        (dict(seq_ids=[a], n=8, H_q=4, valid_lengths=[9]), "EMASK"),          # more valid rows than n
+        (dict(seq_ids=[a], n=8, H_q=3, valid_lengths=[8]), "EINVAL"),         # H_kv does not divide H_q
+        (dict(seq_ids=[a, a], n=8, H_q=4, valid_lengths=[1, 1]), "EINVAL"),   # duplicate sequence
+        (dict(seq_ids=[5], n=8, H_q=4, valid_lengths=[1]), "EINVAL"),         # not live
+        (dict(seq_ids=[a], n=64, H_q=4, valid_lengths=[64]), "ERANGE"),       # past 4 pages/seq
+        (dict(seq_ids=[a, b], n=64, H_q=4, valid_lengths=[30, 64]), "ENOMEM"),
+        (dict(seq_ids=[a], n=4, H_q=4, valid_lengths=[4],
+              positions=np.arange(4, dtype=np.int32)[None]), "ERANGE"),     # positions restart at 0
+    ]
+    for kw, want in cases:
+        with pytest.raises(gqa.GqaError) as e:
+            gqa.attn_prefill_meta(lib, **kw)
+        assert e.value.name == want, (kw, e.value)
+        assert (lib.block_table(a), lib.seq_length(a), lib.free_pages()) == before
+    # Correct positions are accepted.
+    gqa.attn_prefill_meta(lib, [a], 4, 4, [3], positions=np.array([[20, 21, 22, 999]], dtype=np.int32))
+    assert lib.seq_length(a) == 23
+
+
+def test_decode_rejects_an_empty_sequence():
+    lib, _ = _pair()
+    a = lib.seq_create()
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.attn_decode_meta(lib, [a], 4)
+    assert e.value.name == "EMASK"
+    gqa.kv_append_meta(lib, [a], 1)
+    gqa.attn_decode_meta(lib, [a, a], 4)       # repeats are fine for a read
+
+
+def test_truncate_and_fork_bounds():
+    lib, _ = _pair()
+    a = lib.seq_create()
+    gqa.kv_append_meta(lib, [a], 5)
+    for bad in (-1, 6):
+        with pytest.raises(gqa.GqaError) as e:
+            gqa.kv_truncate(lib, a, bad)
+        assert e.value.name == "ERANGE"
+        with pytest.raises(gqa.GqaError) as e:
+            lib.seq_fork(a, bad)
+        assert e.value.name == "ERANGE"
+
+
+def test_layout_metadata_and_compatibility():
+    lib, _ = _pair()
+    m = lib.layout()
+    assert m.keys_post_position == 1 and m.page_tokens == 16 and m.layout_version == gqa.LAYOUT_VERSION
+    assert gqa.layout_compatible(m, lib.layout())
+    other = gqa.LayoutMetadata(**m.as_dict())
+    other.keys_post_position = 0
+    assert not gqa.layout_compatible(m, other)
+    other = gqa.LayoutMetadata(**m.as_dict())
+    other.dtype = gqa.DTYPE_BF16
+    assert not gqa.layout_compatible(m, other)
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(2, 8, 8, 2, 2, dtype="f32", metadata_only=True, keys_post_position=0)
+    assert e.value.name == "ELAYOUT"
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(2, 8, 8, 2, 2, dtype="f32", metadata_only=True, layout_version=99)
+    assert e.value.name == "ELAYOUT"
+
+
+def test_page_order_must_be_a_permutation():
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(1, 4, 4, 2, 2, dtype="f32", metadata_only=True, page_order=[0, 1, 1, 2])
+    assert e.value.name == "EINVAL"
+
+
+def test_sequence_ids_run_out():
+    lib, _ = _pair(seqs=2)
+    lib.seq_create(); lib.seq_create()
+    with pytest.raises(gqa.GqaError) as e:
+        lib.seq_create()
+    assert e.value.name == "ENOMEM"
+
+
+def test_causal_pair_counts_match_the_toy_decoder(golden):
+    # Full recompute at context lengths 4, 5, 6, 7 versus prefill of 4 then
+    # three cached single-token steps, per query head and layer.
+    g = golden("work_counts.txt")
+    W = gqa.work
+    P, steps = int(g["prompt"]), int(g["decode_steps"])
+    per = int(g["layers"]) * int(g["query_heads"])
+    full = sum(W.causal_pairs(0, P + t) for t in range(steps + 1))
+    cached = W.causal_pairs(0, P) + sum(W.causal_pairs(P + t, 1) for t in range(steps))
+    assert per * full == g["score_pairs_full_recompute"]
+    assert per * cached == g["score_pairs_cached"]
