@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Throughput of causal GQA prefill (TFLOP/s) and paged decode (KV-read GB/s)
+on GB300, through the libgqa C ABI.
+
+Default line (one JSON object on stdout, rank 0):
+  * main metric -- bf16 ragged prefill: B=4, H_q=32, H_kv=8, d_h=128, padded
+    n=2048, valid lengths ~U{512..2048} (seeded), right padded, N(0,1) inputs.
+    One step = attn_prefill (host checks, cache write, causal attention,
+    zeroed padding rows) + kv_truncate of every sequence back to 0, so each
+    step starts from an empty cache.  L2 is flushed (512 MiB write) before
+    every timed step; only the step is inside the CUDA events.
+  * "decode" -- bf16 paged decode: B=64, H_q=32, H_kv=8, d_h=128, cache
+    lengths ~U{1024..8192} including the step's own entry, pages placed by a
+    seeded random permutation.  One step = kv_append of one token per
+    sequence + attn_decode + kv_truncate back.  The 1.2 GB of K/V is larger
+    than L2, so no flush is needed.
+Work counts: prefill flops = 4 d_h H_q sum_b causal_pairs; decode bytes =
+sum_b L_b * 2 * H_kv * d_h * 2 (each KV head read once).
+
+Multi-GPU: replicas only (the workloads are independent per GPU); a barrier
+and a max over ranks bracket the timed region; `value` sums all ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "causal GQA prefill TFLOP/s; decode KV-read GB/s (1×GB300, % of roofline)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "prefill_tc": "causal_gqa_attention_02_gb300/csrc/k_prefill_tc.cu",
+    "attn_simt": "causal_gqa_attention_02_gb300/csrc/k_simt.cu",
+    "decode_split": "causal_gqa_attention_02_gb300/csrc/k_decode.cu",
+}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kernel):
+    p = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    if not os.path.exists(p):
+        return None
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+
+
+def traffic_for(kernel, units_scale=1.0):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel)
+    if not rec or rec.get("sha256") != source_sha(kernel):
+        return None
+    return rec["dram_bytes_per_launch"] * units_scale
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def setup(self, torch):
+        torch.cuda.set_device(self.local)
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, torch, x):
+        if not self.pg:
+            return x
+        t = torch.tensor([float(x)], device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def done(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if len(rows) < 3:
+            near = sorted(self.rows, key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))[:5]
+            rows = [r for _, r in near]
+            note = "timed region shorter than the sampling period: nearest samples"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = sorted({name for r in rows for name, val in zip(self.REASONS, r[3:]) if val.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "note": note}
+
+
+def device_uuid(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def to_dev(torch, a, dt="bf16"):
+    a = np.ascontiguousarray(a)
+    if dt == "bf16":
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
+
+
+def pinned(torch, t):
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+def timed_steps(torch, dist, step, K, flush=None):
+    """Per-step CUDA events on the current stream; flush (untimed) between."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.time()
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        evs[i][0].record()
+        step()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t1 = time.time()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return ms, t0, t1
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def prefill_cpu_baseline(w, budget_s=12.0):
+    import oracle
+    import causal_gqa_attention_02_gb300 as gqa
+    nth = oracle.default_threads()
+    B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
+    done_flops, used, seqs = 0, 0.0, 0
+    for b in range(B):
+        nb = int(w["valid_lengths"][b])
+        cm = oracle.CacheModel(workloads.pages_for(nb), 1, workloads.pages_for(nb), H_kv, d, "bf16")
+        s = cm.create()
+        t0 = time.perf_counter()
+        oracle.prefill(cm, [s], w["q"][b:b + 1], w["k"][b:b + 1], w["v"][b:b + 1], [nb], nthreads=nth)
+        used += time.perf_counter() - t0
+        done_flops += gqa.work.prefill_flops([0], [nb], H_q, d)
+        seqs += 1
+        if used >= budget_s:
+            break
+    return {"value": done_flops / used / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+            "sample": "fp64 oracle prefill of sequences 0..%d of the workload (valid lengths %s), all %d query "
+                      "heads: %.1f GFLOP causal in %.1f s" % (seqs - 1, list(map(int, w["valid_lengths"][:seqs])),
+                                                             H_q, done_flops / 1e9, used)}
+
+
+def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
+    w = workloads.ragged_prefill(workloads.seed_for(2))
+    B, n, H_q, H_kv, d = w["B"], w["n"], w["H_q"], w["H_kv"], w["d"]
+    nb = [int(x) for x in w["valid_lengths"]]
+    flops = gqa.work.prefill_flops([0] * B, nb, H_q, d)
+    pages = sum(workloads.pages_for(x) for x in nb) + 16
+    cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16")
+    ids = [cache.seq_create() for _ in range(B)]
+    q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
+    out = torch.empty_like(q)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        gqa.attn_prefill(cache, ids, q, k, v, nb, out=out)
+        for s in ids:
+            gqa.kv_truncate(cache, s, 0)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    cache.profile_read()
+    cache.profile(True)
+    ms, t0, t1 = timed_steps(torch, dist, step, args.steps, flush)
+    cache.profile(False)
+    prof = cache.profile_read()
+    total_ms = dist.max(torch, sum(ms))
+    value = flops * args.steps * dist.world / (total_ms / 1e3) / 1e12
+    kernel = "prefill_tc" if prof["prefill_tc"][0] else "attn_simt"
+    launches, kms = prof[kernel]
+    avg_ms = kms / max(1, launches)
+    achieved = flops / (avg_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel), "kernel": kernel,
+                "kernel_ms": round(avg_ms, 4), "algorithmic_flops_per_launch": flops,
+                "peak_source": "%s bf16 dense (burst)" % peak_src}
+    gpu_launches = sum(nl for nl, _ in prof.values())
+
+    # End to end through the public API from pinned host buffers.
+    qh, kh, vh = pinned(torch, q), pinned(torch, k), pinned(torch, v)
+    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    qd, kd, vd, od = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        gqa.attn_prefill(cache, ids, qd, kd, vd, nb, out=od)
+        oh.copy_(od, non_blocking=True)
+        for s in ids:
+            gqa.kv_truncate(cache, s, 0)
+
+    for _ in range(2):
+        e2e_step()
+    ems, _, _ = timed_steps(torch, dist, e2e_step, args.steps, flush)
+    e2e_total = dist.max(torch, sum(ems))
+    e2e = {"value": round(flops * args.steps * dist.world / (e2e_total / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes), "d2h_bytes_per_step": int(out.nbytes),
+           "ms_per_step": round(e2e_total / args.steps, 4)}
+    flags = cache.check()
+    cache.close()
+    del flush
+    cfg = {"workload": "bf16 ragged prefill: B=%d, H_q=%d, H_kv=%d, d_h=%d, padded n=%d, valid_lengths=%s "
+                       "(~U{512..2048}, seed %d), right padded, N(0,1); one step = attn_prefill + kv_truncate "
+                       "to 0" % (B, H_q, H_kv, d, n, nb, workloads.seed_for(2)),
+           "global_batch": B * dist.world, "seq_len": n, "parallelism": "replicas x%d" % dist.world,
+           "l2": "flushed (512 MiB write, untimed) before every timed step",
+           "causal_gflop_per_step": round(flops / 1e9, 3)}
+    return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
+            "gpu_launches": gpu_launches, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
+            "workload": w}
+
+
+def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
+    w = workloads.paged_decode(workloads.seed_for(3))
+    B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
+    L = [int(x) for x in w["lengths"]]
+    kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, 2)
+    cache = gqa.Cache(H_kv, d, w["num_pages"], B, workloads.pages_for(max(L)) + 1, dtype="bf16",
+                      page_order=w["page_order"])
+    ids = [cache.seq_create() for _ in range(B)]
+    for b in range(B):
+        kb = to_dev(torch, w["hist_k"][b][None])
+        vb = to_dev(torch, w["hist_v"][b][None])
+        gqa.kv_append(cache, [ids[b]], kb, vb)
+        del kb, vb
+    new_k, new_v, q = to_dev(torch, w["new_k"]), to_dev(torch, w["new_v"]), to_dev(torch, w["q"])
+    out = torch.empty_like(q)
+
+    def step():
+        gqa.kv_append(cache, ids, new_k, new_v)
+        gqa.attn_decode(cache, ids, q, out=out)
+        for b in range(B):
+            gqa.kv_truncate(cache, ids[b], L[b] - 1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cache.profile_read()
+    cache.profile(True)
+    ms, t0, t1 = timed_steps(torch, dist, step, args.steps)
+    cache.profile(False)
+    prof = cache.profile_read()
+    total_ms = dist.max(torch, sum(ms))
+    value = kv_bytes * args.steps * dist.world / (total_ms / 1e3) / 1e9
+    kernel = "decode_split" if prof["decode_split"][0] else "attn_simt"
+    launches, kms = prof[kernel]
+    avg_ms = kms / max(1, launches)
+    achieved = kv_bytes / (avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(kernel), "kernel": kernel,
+                "kernel_ms": round(avg_ms, 4), "algorithmic_bytes_per_launch": kv_bytes,
+                "peak_source": "%s HBM copy bandwidth" % peak_src}
+
+    qh, kh, vh = pinned(torch, q), pinned(torch, new_k), pinned(torch, new_v)
+    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    qd, kd, vd, od = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v), torch.empty_like(out)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        gqa.kv_append(cache, ids, kd, vd)
+        gqa.attn_decode(cache, ids, qd, out=od)
+        oh.copy_(od, non_blocking=True)
+        for b in range(B):
+            gqa.kv_truncate(cache, ids[b], L[b] - 1)
+
+    for _ in range(2):
+        e2e_step()
+    ems, _, _ = timed_steps(torch, dist, e2e_step, args.steps)
+    e2e_total = dist.max(torch, sum(ems))
+    res = {"metric": "decode KV-read GB/s", "value": round(value, 1), "unit": "GB/s",
+           "ms_per_step": round(total_ms / args.steps, 4), "roofline": roofline,
+           "e2e": {"value": round(kv_bytes * args.steps * dist.world / (e2e_total / 1e3) / 1e9, 1), "unit": "GB/s",
+                   "h2d_bytes_per_step": int(q.nbytes + new_k.nbytes + new_v.nbytes),
+                   "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4)},
+           "gpu_launches": sum(nl for nl, _ in prof.values()),
+           "config": {"workload": "bf16 paged decode: B=%d, H_q=%d, H_kv=%d, d_h=%d, cache lengths ~U{1024..8192} "
+                                  "(seed %d, sum %d tokens) incl. the appended token, pages placed by a seeded "
+                                  "random permutation; one step = kv_append + attn_decode + kv_truncate back"
+                                  % (B, H_q, H_kv, d, workloads.seed_for(3), sum(L)),
+                      "l2": "not flushed: %.2f GB of K/V per step exceeds the 129 MB L2" % (kv_bytes / 1e9),
+                      "kv_bytes_per_step": kv_bytes}}
+    if want_cpu:
+        import oracle
+        nth = oracle.default_threads()
+        cm = oracle.CacheModel(sum(workloads.pages_for(x) for x in L[:8]), 8, workloads.pages_for(max(L)) + 1,
+                               H_kv, d, "bf16")
+        sm = [cm.create() for _ in range(8)]
+        for j in range(8):
+            cm.write([sm[j]], [w["hist_k"][j]], [w["hist_v"][j]])
+        oracle.append(cm, sm, w["new_k"][:8], w["new_v"][:8])
+        t0c = time.perf_counter()
+        oracle.decode(cm, sm, w["q"][:8], nthreads=nth)
+        dt = time.perf_counter() - t0c
+        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2)
+        res["cpu_baseline"] = {"value": round(by / dt / 1e9, 3), "unit": "GB/s", "cores": nth, "kind": "oracle",
+                               "sample": "fp64 oracle decode of sequences 0..7 (%d cached tokens, %.1f MB of "
+                                         "bf16 K/V) in %.2f s" % (sum(L[:8]), by / 1e6, dt)}
+    res["device_error_flags"] = cache.check()
+    res["t0"], res["t1"] = t0, t1
+    cache.close()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return 0
+    import oracle
+    w = workloads.ragged_prefill(workloads.seed_for(2))
+    B, n, H_q, H_kv, d = w["B"], w["n"], w["H_q"], w["H_kv"], w["d"]
+    g = H_q // H_kv
+    nth = oracle.default_threads()
+
+    def work(b):
+        nb = int(w["valid_lengths"][b])
+        return 4 * d * g * (nb * (nb + 1) // 2)
+
+    def step(i):
+        b = i % B
+        nb = int(w["valid_lengths"][b])
+        cm = oracle.CacheModel(workloads.pages_for(nb), 1, workloads.pages_for(nb), 1, d, "bf16")
+        s = cm.create()
+        # KV group 0 only: its g query heads and its one KV head.
+        oracle.prefill(cm, [s], w["q"][b:b + 1, :, :g], w["k"][b:b + 1, :, :1], w["v"][b:b + 1, :, :1], [nb],
+                       nthreads=nth)
+        return work(b)
+
+    for i in range(args.warmup):
+        step(i)
+    flops, t = 0, 0.0
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        flops += step(i)
+        t += time.perf_counter() - t0
+    value = flops / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "bf16 ragged prefill: B=4, H_q=32, H_kv=8, d_h=128, padded n=2048, valid "
+                                   "lengths %s (seed %d); each reference step is one sequence's KV group 0 "
+                                   "(%d query heads)" % (list(map(int, w["valid_lengths"])),
+                                                         workloads.seed_for(2), g)},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+                             "sample": "per step: fp64 oracle prefill of one sequence (cycling 0..3), KV group 0"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gqa", "reference"], default="gqa")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode object")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+
+    import torch
+    import causal_gqa_attention_02_gb300 as gqa
+    dist.setup(torch)
+    peaks, peak_src = load_peaks()
+    clocks = ClockSampler(device_uuid(torch)) if dist.rank == 0 else None
+    try:
+        time.sleep(0.3 if clocks else 0)
+        pre = bench_prefill(torch, gqa, dist, args, peaks, peak_src)
+        dec = None if args.no_decode else bench_decode(torch, gqa, dist, args, peaks, peak_src,
+                                                       want_cpu=(dist.rank == 0 and not args.no_cpu))
+    finally:
+        if clocks:
+            clocks.stop()
+    if dist.rank == 0:
+        line = {"metric": METRIC, "value": round(pre["value"], 3), "unit": "TFLOP/s", "n_gpus": dist.world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(pre["ms_per_step"], 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": pre["config"], "roofline": pre["roofline"], "e2e": pre["e2e"],
+                "gpu_launches": pre["gpu_launches"], "clocks": clocks.summary(pre["t0"], pre["t1"]),
+                "device_error_flags": pre["device_error_flags"]}
+        if not args.no_cpu and dist.world == 1:
+            line["cpu_baseline"] = prefill_cpu_baseline(pre["workload"])
+        if dec is not None:
+            dec["clocks"] = clocks.summary(dec.pop("t0"), dec.pop("t1"))
+            line["decode"] = dec
+        print(json.dumps(line))
+    dist.done()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -32,6 +32,8 @@ DTYPE_BF16, DTYPE_F32 = 1, 2
 PAGE_TOKENS = 16
 LAYOUT_VERSION = 1
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
+KERNELS = {"cache_write": 0, "cow_copy": 1, "prefill_tc": 2, "attn_simt": 3,
+           "decode_split": 4, "decode_combine": 5}
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
 
@@ -78,6 +80,8 @@ _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
+_sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
+_sig("gqa_profile_read", ctypes.c_int, _vp, _i32, _I32P, ctypes.POINTER(ctypes.c_double))
 _sig("gqa_last_error", ctypes.c_char_p)
 _sig("gqa_version", ctypes.c_char_p)
 
@@ -203,6 +207,19 @@ class Cache:
         _check(_lib.gqa_cache_layout(self._h, ctypes.byref(m)))
         return m
 
+    def profile(self, on: bool):
+        """Bracket every kernel launch with CUDA events (on its stream)."""
+        _check(_lib.gqa_profile_enable(self._h, 1 if on else 0))
+
+    def profile_read(self):
+        """{kernel: (launches, total_ms)} since the last read; waits for events."""
+        res = {}
+        for name, kid in KERNELS.items():
+            n, ms = ctypes.c_int32(), ctypes.c_double()
+            _check(_lib.gqa_profile_read(self._h, kid, ctypes.byref(n), ctypes.byref(ms)))
+            res[name] = (n.value, ms.value)
+        return res
+
     def check(self, stream=None) -> int:
         """Synchronise and read/clear the device error word (0 = clean)."""
         flags = ctypes.c_int32()
@@ -310,4 +327,4 @@ def exported_symbols():
             "gqa_layout_compatible", "gqa_seq_create", "gqa_seq_fork", "gqa_seq_free",
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "kv_truncate", "gqa_cache_check",
-            "gqa_last_error", "gqa_version"]
+            "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version"]

@@ -83,6 +83,16 @@ struct gqa_cache {
     int num_sms = 0;
     int cc = 0;                          // compute capability major*10+minor
 
+    // Profiling: launch counts always; event pairs while `prof` is on.
+    bool prof = false;
+    int32_t launches[GQA_KERNEL_COUNT] = {};
+    struct ProfRec {
+        int kernel;
+        cudaEvent_t start, end;
+    };
+    std::vector<ProfRec> prof_recs;
+    std::vector<cudaEvent_t> spare_events;
+
     size_t stride() const { return (size_t)desc.max_pages_per_seq; }
 
     int32_t take_page()
@@ -286,6 +296,42 @@ int launched(cudaError_t e, const char *what)
     return GQA_OK;
 }
 
+cudaEvent_t get_event(gqa_cache *c)
+{
+    if (!c->spare_events.empty()) {
+        cudaEvent_t e = c->spare_events.back();
+        c->spare_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess)
+        return nullptr;
+    return e;
+}
+
+// Queue one kernel via `launch` (returning cudaError_t), counting it and,
+// when profiling is on, bracketing it with events on its stream.
+template <typename F>
+int run_kernel(gqa_cache *c, int kernel, cudaStream_t st, const char *what, F &&launch)
+{
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (c->prof) {
+        e0 = get_event(c);
+        e1 = get_event(c);
+        if (e0 && e1)
+            cudaEventRecord(e0, st);
+    }
+    const cudaError_t e = launch();
+    if (e != cudaSuccess)
+        return cuda_fail(e, what);
+    c->launches[kernel] += 1;
+    if (e0 && e1) {
+        cudaEventRecord(e1, st);
+        c->prof_recs.push_back(gqa_cache::ProfRec{kernel, e0, e1});
+    }
+    return GQA_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -405,6 +451,12 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_err) cudaFree(c->d_err);
         if (c->d_stage) cudaFree(c->d_stage);
         if (c->d_ws) cudaFree(c->d_ws);
+        for (const auto &r : c->prof_recs) {
+            cudaEventDestroy(r.start);
+            cudaEventDestroy(r.end);
+        }
+        for (cudaEvent_t ev : c->spare_events)
+            cudaEventDestroy(ev);
     }
     delete c;
     return e == cudaSuccess ? GQA_OK : cuda_fail(e, "cache destroy");
@@ -603,12 +655,17 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     const PoolView pv = c->view();
     const SeqDesc *d_sds = (const SeqDesc *)(c->d_stage + o_sds);
     if (!cows.empty() &&
-        (rc = launched(launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st),
-                       "copy-on-write kernel")) != GQA_OK)
+        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&] {
+             return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
+         })) != GQA_OK)
         return rc;
-    if ((rc = launched(launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st), "cache write kernel")) != GQA_OK)
+    if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&] {
+             return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st);
+         })) != GQA_OK)
         return rc;
-    return launched(launch_attn_simt(pv, c->desc.dtype, d_sds, B, n, H_q, q, out, st), "attention kernel");
+    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {
+        return launch_attn_simt(pv, c->desc.dtype, d_sds, B, n, H_q, q, out, st);
+    });
 }
 
 int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,
@@ -650,12 +707,14 @@ int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const 
         return rc;
     const PoolView pv = c->view();
     if (!cows.empty() &&
-        (rc = launched(launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st),
-                       "copy-on-write kernel")) != GQA_OK)
+        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&] {
+             return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
+         })) != GQA_OK)
         return rc;
-    return launched(launch_cache_write(pv, c->esize, (const SeqDesc *)(c->d_stage + o_sds), B, n, max_c, k_new,
-                                       v_new, st),
-                    "cache write kernel");
+    return run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&] {
+        return launch_cache_write(pv, c->esize, (const SeqDesc *)(c->d_stage + o_sds), B, n, max_c, k_new, v_new,
+                                  st);
+    });
 }
 
 int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q, void *out,
@@ -717,20 +776,60 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         if ((rc = upload_stage(c, st)) != GQA_OK)
             return rc;
         float *ws_o = c->d_ws, *ws_ml = c->d_ws + n_part * 128;
-        if ((rc = launched(launch_decode_split(pv, (const SeqDesc *)(c->d_stage + o_sds),
-                                               (const DecodeItem *)(c->d_stage + o_items), (int)items.size(),
-                                               chunk, H_q, q, ws_o, ws_ml, st),
-                           "decode split kernel")) != GQA_OK)
+        if ((rc = run_kernel(c, GQA_KERNEL_DECODE_SPLIT, st, "decode split kernel", [&] {
+                 return launch_decode_split(pv, (const SeqDesc *)(c->d_stage + o_sds),
+                                            (const DecodeItem *)(c->d_stage + o_items), (int)items.size(), chunk,
+                                            H_q, q, ws_o, ws_ml, st);
+             })) != GQA_OK)
             return rc;
-        return launched(launch_decode_combine((const int32_t *)(c->d_stage + o_start), B, H_q, H_kv, ws_o,
-                                              ws_ml, out, st),
-                        "decode combine kernel");
+        return run_kernel(c, GQA_KERNEL_DECODE_COMBINE, st, "decode combine kernel", [&] {
+            return launch_decode_combine((const int32_t *)(c->d_stage + o_start), B, H_q, H_kv, ws_o, ws_ml, out,
+                                         st);
+        });
     }
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
-    return launched(launch_attn_simt(pv, c->desc.dtype, (const SeqDesc *)(c->d_stage + o_sds), B, 1, H_q, q,
-                                     out, st),
-                    "attention kernel");
+    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {
+        return launch_attn_simt(pv, c->desc.dtype, (const SeqDesc *)(c->d_stage + o_sds), B, 1, H_q, q, out, st);
+    });
+}
+
+int gqa_profile_enable(gqa_cache *c, int on)
+{
+    if (!c)
+        return fail(GQA_EINVAL, "NULL cache");
+    c->prof = on != 0 && !c->meta_only;
+    return GQA_OK;
+}
+
+int gqa_profile_read(gqa_cache *c, int32_t kernel, int32_t *launches, double *total_ms)
+{
+    if (!c || !launches || !total_ms)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (kernel < 0 || kernel >= GQA_KERNEL_COUNT)
+        return fail(GQA_ERANGE, "kernel id %d outside 0..%d", kernel, GQA_KERNEL_COUNT - 1);
+    *launches = c->launches[kernel];
+    c->launches[kernel] = 0;
+    double sum = 0.0;
+    std::vector<gqa_cache::ProfRec> keep;
+    for (const auto &r : c->prof_recs) {
+        if (r.kernel != kernel) {
+            keep.push_back(r);
+            continue;
+        }
+        float ms = 0.0f;
+        cudaError_t e = cudaEventSynchronize(r.end);
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&ms, r.start, r.end);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "profile event");
+        sum += ms;
+        c->spare_events.push_back(r.start);
+        c->spare_events.push_back(r.end);
+    }
+    c->prof_recs.swap(keep);
+    *total_ms = sum;
+    return GQA_OK;
 }
 
 int gqa_cache_check(gqa_cache *c, void *stream, int32_t *flags_out)

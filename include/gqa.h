@@ -253,6 +253,27 @@ int kv_truncate(gqa_cache *cache, int32_t seq, int32_t m);
  * if any bit was set, GQA_ECUDA on a CUDA error. */
 int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
 
+/* ---- profiling ------------------------------------------------------------ */
+
+/* Kernel ids for gqa_profile_read. */
+#define GQA_KERNEL_CACHE_WRITE     0  /* new K/V rows into their pages           */
+#define GQA_KERNEL_COW_COPY        1  /* copy-on-write of a shared tail page      */
+#define GQA_KERNEL_PREFILL_TC      2  /* tensor-core causal prefill (bf16, 128)   */
+#define GQA_KERNEL_ATTN_SIMT       3  /* CUDA-core attention (fp32 / other d_h)   */
+#define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode partials (bf16, 128)      */
+#define GQA_KERNEL_DECODE_COMBINE  5  /* split-K combine                          */
+#define GQA_KERNEL_COUNT           6
+
+/* Turn per-launch timing on or off.  While on, every kernel launch of this
+ * cache is bracketed by two CUDA events recorded on the launch's own stream.
+ * Launches are counted whether or not timing is on. */
+int gqa_profile_enable(gqa_cache *cache, int on);
+
+/* For kernel id `kernel`: the number of launches since the last read, and the
+ * summed device time (ms) of the timed ones among them (0 if timing was
+ * off).  Waits for the recorded events; clears the kernel's records. */
+int gqa_profile_read(gqa_cache *cache, int32_t kernel, int32_t *launches, double *total_ms);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char *gqa_last_error(void);
 
