@@ -78,6 +78,7 @@ _sig("gqa_page_refcount", ctypes.c_int, _vp, _i32, _I32P)
 _sig("attn_prefill", ctypes.c_int, _vp, _i32, _I32P, _i32, _i32, _vp, _vp, _vp, _I32P, _I32P, _vp, _vp)
 _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
+_sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
 _sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
@@ -312,6 +313,19 @@ def attn_decode(cache: Cache, seq_ids, q, out=None, stream=None):
     return out
 
 
+def attn_decode_static(cache: Cache, seq_ids, q, out=None, stream=None):
+    """attn_decode without device allocation: the split-K partials live in
+    the library's fixed static device array (see include/gqa.h)."""
+    B, H_q = len(seq_ids), q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    shape = (B, H_q, cache.head_dim)
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode_static(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
+                                   _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+    return out
+
+
 def attn_decode_meta(cache: Cache, seq_ids, H_q):
     keep_s, sp = _i32_array(seq_ids)
     _check(_lib.attn_decode(cache.handle, len(seq_ids), sp, H_q, None, None, None))
@@ -326,5 +340,5 @@ def exported_symbols():
     return ["gqa_pool_bytes", "gqa_cache_create", "gqa_cache_destroy", "gqa_cache_layout",
             "gqa_layout_compatible", "gqa_seq_create", "gqa_seq_fork", "gqa_seq_free",
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
-            "attn_prefill", "kv_append", "attn_decode", "kv_truncate", "gqa_cache_check",
+            "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
             "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version"]

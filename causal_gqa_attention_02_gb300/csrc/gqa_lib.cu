@@ -20,6 +20,7 @@
 #include <cstdio>
 #include <cstring>
 #include <functional>
+#include <mutex>
 #include <queue>
 #include <string>
 #include <vector>
@@ -831,6 +832,138 @@ int gqa_profile_read(gqa_cache *c, int32_t kernel, int32_t *launches, double *to
     *total_ms = sum;
     return GQA_OK;
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode: the split-K partials and the per-call descriptors
+// live in one file-scope device array instead of library-allocated memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[GQA_STATIC_SCRATCH_BYTES];
+
+constexpr size_t kStaticDescBytes = 1u << 20;      // descriptors; the rest holds partials
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+char *g_static_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on `dev` (which must be current).  In
+// host code the array's name only stands for the symbol, so its address is
+// looked up once per device and cached.
+int static_scratch(int dev, char **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GQA_EINVAL, "device %d outside 0..%d", dev, kMaxDevices - 1);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
+        g_static_addr[dev] = (char *)p;
+    }
+    *out = g_static_addr[dev];
+    return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q,
+                                  void *out, void *stream)
+{
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    const int G = H_q / H_kv;
+    if (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || !decode_split_supported(G))
+        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 and H_q/H_kv <= 8");
+    if (c->meta_only)
+        return fail(GQA_EINVAL, "attn_decode_static needs a cache with a device pool");
+    if (!q || !out)
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    std::vector<SeqDesc> sds(B);
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t s = seq_ids[b];
+        if (!live(c, s))
+            return fail(GQA_EINVAL, "batch entry %d: sequence %d is not live", b, s);
+        const int32_t L = c->seqs[s].len;
+        if (L < 1)
+            return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
+        sds[b] = SeqDesc{s, L - 1, 1, 0};
+        total += L;
+    }
+    int rc = check_device(c);
+    if (rc != GQA_OK)
+        return rc;
+
+    // Same chunk rule as attn_decode, widened (up to 512 tokens) until the
+    // partials fit in the static array.
+    const size_t part_cap = (GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes) / sizeof(float);
+    int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
+    int chunk = (int)std::min<int64_t>(512, std::max<int64_t>(128, (target + 127) / 128 * 128));
+    size_t n_items = 0;
+    for (;;) {
+        n_items = 0;
+        for (int b = 0; b < B; ++b)
+            n_items += (size_t)((sds[b].past + 1 + chunk - 1) / chunk);
+        if (n_items * (size_t)H_kv * G * 130 <= part_cap || chunk >= 512)
+            break;
+        chunk = std::min(512, chunk * 2);
+    }
+    const size_t n_part = n_items * (size_t)H_kv * G;
+    if (n_part * 130 > part_cap)
+        return fail(GQA_ERANGE, "decode partials need %zu bytes; the static scratch holds %zu",
+                    n_part * 130 * sizeof(float), part_cap * sizeof(float));
+    std::vector<DecodeItem> items;
+    std::vector<int32_t> start(B + 1, 0);
+    items.reserve(n_items);
+    for (int b = 0; b < B; ++b) {
+        const int32_t ns = (sds[b].past + 1 + chunk - 1) / chunk;
+        start[b] = (int32_t)items.size();
+        for (int32_t s = 0; s < ns; ++s)
+            items.push_back(DecodeItem{b, s});
+    }
+    start[B] = (int32_t)items.size();
+    std::vector<char> desc;
+    Stage stg(desc);
+    const size_t o_sds = stg.add(sds.data(), sds.size());
+    const size_t o_items = stg.add(items.data(), items.size());
+    const size_t o_start = stg.add(start.data(), start.size());
+    if (desc.size() > kStaticDescBytes)
+        return fail(GQA_ERANGE, "decode descriptors need %zu bytes; the static scratch reserves %zu",
+                    desc.size(), kStaticDescBytes);
+
+    char *scratch = nullptr;
+    if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
+        return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "descriptor upload (static scratch)");
+    float *ws_o = (float *)(scratch + kStaticDescBytes);
+    float *ws_ml = ws_o + n_part * 128;
+    const PoolView pv = c->view();
+    e = launch_decode_split(pv, (const SeqDesc *)(scratch + o_sds), (const DecodeItem *)(scratch + o_items),
+                            (int)items.size(), chunk, H_q, q, ws_o, ws_ml, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode split kernel (static scratch)");
+    c->launches[GQA_KERNEL_DECODE_SPLIT] += 1;
+    e = launch_decode_combine((const int32_t *)(scratch + o_start), B, H_q, H_kv, ws_o, ws_ml, out, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode combine kernel (static scratch)");
+    c->launches[GQA_KERNEL_DECODE_COMBINE] += 1;
+    return GQA_OK;
+}
+
+extern "C" {
 
 int gqa_cache_check(gqa_cache *c, void *stream, int32_t *flags_out)
 {

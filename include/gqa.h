@@ -241,6 +241,34 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
 int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                 const void *q, void *out, void *stream);
 
+/* attn_decode_static -- attn_decode that allocates no device memory.
+ *
+ * The pages define no counterpart to this call.  It is for callers that must
+ * not allocate device memory while they decode.  Examples: a serving loop
+ * that reserved all of its GPU memory at start-up; a host process whose
+ * allocator belongs to another framework; a latency-bound step that cannot
+ * afford the device-wide synchronisation of cudaFree.  attn_decode may hit
+ * that synchronisation when its workspace grows.
+ *
+ * Arguments, results and errors are those of attn_decode.  The cache must be
+ * bf16 with d_h = 128, and H_q / H_kv must be at most 8, because this call
+ * runs only the split-K decode kernels.  Other shapes get GQA_EINVAL.
+ * The split-K partials and the per-call descriptors live in one static
+ * device array of GQA_STATIC_SCRATCH_BYTES.  The library reserves that array
+ * on every GPU that loads it, until the process exits.  A call whose partials
+ * or descriptors would not fit returns GQA_ERANGE with the bytes it needed.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ * On each device, the first call looks up the array's device address
+ * (cudaGetSymbolAddress).  Make that first call before any stream capture.
+ * Every call shares the one array, and the array keeps the last call's
+ * contents.  Each call writes every part of the array it reads before
+ * reading it, so nothing needs clearing.  Calls whose GPU work overlaps race
+ * on the array: calls on different streams, or on different caches of one
+ * device.  Order such calls yourself. */
+#define GQA_STATIC_SCRATCH_BYTES (16u << 20)
+int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
+                       const void *q, void *out, void *stream);
+
 /* Prefix-edit invalidation ([P3] edit at token m): keep positions < m of
  * `seq`, drop the rest.  Pages wholly beyond position m lose one reference
  * (and return to the pool at zero).  A partially kept tail page stays; if it
