@@ -290,13 +290,6 @@ int ensure_ws(gqa_cache *c, size_t floats)
     return GQA_OK;
 }
 
-int launched(cudaError_t e, const char *what)
-{
-    if (e != cudaSuccess)
-        return cuda_fail(e, what);
-    return GQA_OK;
-}
-
 cudaEvent_t get_event(gqa_cache *c)
 {
     if (!c->spare_events.empty()) {
@@ -648,9 +641,27 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     cudaStream_t st = (cudaStream_t)stream;
     if ((rc = upload_tables(c, st)) != GQA_OK)
         return rc;
+    const int G = H_q / c->desc.num_kv_heads;
+    const bool use_tc = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
+                        prefill_tc_supported(G, c->desc.num_kv_heads);
+    std::vector<TcItem> items;
+    if (use_tc) {
+        // Two query tiles of 128/G positions per CTA; heaviest items first so
+        // the long causal rows start early and the tail of the grid is short.
+        const int span = 2 * prefill_tc_rows_per_tile(G);
+        for (int b = 0; b < B; ++b)
+            for (int32_t i0 = 0; i0 < sds[b].count; i0 += span) {
+                const int32_t last = std::min<int32_t>(i0 + span, sds[b].count) - 1;
+                const int32_t nt = (sds[b].past + last) / 128 + 1;
+                for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
+                    items.push_back(TcItem{b, h, i0, nt});
+            }
+        std::stable_sort(items.begin(), items.end(), [](const TcItem &x, const TcItem &y) { return x.nt > y.nt; });
+    }
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
     const size_t o_cow = stg.add(cows.data(), cows.size());
+    const size_t o_items = stg.add(items.data(), items.size());
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     const PoolView pv = c->view();
@@ -664,6 +675,21 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
              return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st);
          })) != GQA_OK)
         return rc;
+    if (use_tc) {
+        // Padding rows (discarded, written as zeros): contiguous per entry.
+        const size_t row_bytes = (size_t)H_q * c->desc.head_dim * c->esize;
+        for (int b = 0; b < B; ++b)
+            if (sds[b].count < n) {
+                cudaError_t e = cudaMemsetAsync((char *)out + ((size_t)b * n + sds[b].count) * row_bytes, 0,
+                                                (size_t)(n - sds[b].count) * row_bytes, st);
+                if (e != cudaSuccess)
+                    return cuda_fail(e, "padding rows");
+            }
+        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&] {
+            return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items), (int)items.size(), B, n,
+                                     H_q, q, out, st);
+        });
+    }
     return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {
         return launch_attn_simt(pv, c->desc.dtype, d_sds, B, n, H_q, q, out, st);
     });

@@ -42,6 +42,12 @@ struct DecodeItem {
     int32_t b, split;
 };
 
+// One tensor-core prefill work item: two 128-row query tiles of batch entry
+// b and KV head kvh, starting at row i0 of the entry; nt key tiles of 128.
+struct TcItem {
+    int32_t b, kvh, i0, nt;
+};
+
 // Error-word bits (mirror include/gqa.h).
 constexpr int32_t kErrPageId = 1;
 constexpr int32_t kErrTimeout = 2;
@@ -75,7 +81,11 @@ cudaError_t launch_decode_split(const PoolView &pv, const SeqDesc *d_seqs, const
 cudaError_t launch_decode_combine(const int32_t *d_item_start, int B, int H_q, int H_kv,
                                   const float *ws_o, const float *ws_ml, void *out, cudaStream_t st);
 
-// bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).
+// bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).  Rows of the
+// batch entries must already be in the cache (launch_cache_write first).
 bool prefill_tc_supported(int group, int H_kv);
+int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
+cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items, int n_items, int B,
+                              int n, int H_q, const void *q, void *out, cudaStream_t st);
 
 }  // namespace gqa

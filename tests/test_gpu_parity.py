@@ -72,8 +72,11 @@ def test_tiny_fp32_prefill_then_three_decode_steps():
 def test_bf16_ragged_prefill(B, H_q, H_kv, n, lo, hi):
     w = workloads.ragged_prefill(seed=100 + H_q, B=B, H_q=H_q, H_kv=H_kv, n=n, lo=lo, hi=hi)
     c, m, ids, mids = _prefill_case(w)
+    c.profile_read()
     out = host_f64(gqa.attn_prefill(c, ids, dev(w["q"], "bf16"), dev(w["k"], "bf16"), dev(w["v"], "bf16"),
                                     w["valid_lengths"]), "bf16")
+    launched = c.profile_read()
+    assert launched["prefill_tc"][0] == 1 and launched["attn_simt"][0] == 0, launched
     ref = oracle.prefill(m, mids, w["q"], w["k"], w["v"], w["valid_lengths"])
     mask = valid_mask(w["valid_lengths"], n)
     assert_close(out[mask], ref[mask], "bf16", "ragged prefill")
