@@ -273,6 +273,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
                 "kernel_ms": round(avg_ms, 4), "algorithmic_flops_per_launch": flops,
                 "peak_source": "%s bf16 dense (burst)" % peak_src}
     gpu_launches = sum(nl for nl, _ in prof.values())
+    kernels = {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl}
 
     # End to end through the public API from pinned host buffers.
     qh, kh, vh = pinned(torch, q), pinned(torch, k), pinned(torch, v)
@@ -305,7 +306,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
            "l2": "flushed (512 MiB write, untimed) before every timed step",
            "causal_gflop_per_step": round(flops / 1e9, 3)}
     return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
-            "gpu_launches": gpu_launches, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
+            "gpu_launches": gpu_launches, "kernels": kernels, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
             "workload": w}
 
 
@@ -374,6 +375,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                    "h2d_bytes_per_step": int(q.nbytes + new_k.nbytes + new_v.nbytes),
                    "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4)},
            "gpu_launches": sum(nl for nl, _ in prof.values()),
+           "kernels": {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl},
            "config": {"workload": "bf16 paged decode: B=%d, H_q=%d, H_kv=%d, d_h=%d, cache lengths ~U{1024..8192} "
                                   "(seed %d, sum %d tokens) incl. the appended token, pages placed by a seeded "
                                   "random permutation; one step = kv_append + attn_decode + kv_truncate back"
@@ -460,6 +462,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gqa", "reference"], default="gqa")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode object")
+    ap.add_argument("--no-prefill", action="store_true", help="decode only (for profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -474,18 +477,22 @@ def main():
     clocks = ClockSampler(device_uuid(torch)) if dist.rank == 0 else None
     try:
         time.sleep(0.3 if clocks else 0)
-        pre = bench_prefill(torch, gqa, dist, args, peaks, peak_src)
+        pre = None if args.no_prefill else bench_prefill(torch, gqa, dist, args, peaks, peak_src)
         dec = None if args.no_decode else bench_decode(torch, gqa, dist, args, peaks, peak_src,
                                                        want_cpu=(dist.rank == 0 and not args.no_cpu))
     finally:
         if clocks:
             clocks.stop()
-    if dist.rank == 0:
+    if dist.rank == 0 and pre is None:
+        dec["clocks"] = clocks.summary(dec.pop("t0"), dec.pop("t1"))
+        print(json.dumps({"decode": dec}))
+    elif dist.rank == 0:
         line = {"metric": METRIC, "value": round(pre["value"], 3), "unit": "TFLOP/s", "n_gpus": dist.world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(pre["ms_per_step"], 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic", "config": pre["config"], "roofline": pre["roofline"], "e2e": pre["e2e"],
-                "gpu_launches": pre["gpu_launches"], "clocks": clocks.summary(pre["t0"], pre["t1"]),
+                "gpu_launches": pre["gpu_launches"], "kernels": pre["kernels"],
+                "clocks": clocks.summary(pre["t0"], pre["t1"]),
                 "device_error_flags": pre["device_error_flags"]}
         if not args.no_cpu and dist.world == 1:
             line["cpu_baseline"] = prefill_cpu_baseline(pre["workload"])
