@@ -645,6 +645,7 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     const bool use_tc = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
                         prefill_tc_supported(G, c->desc.num_kv_heads);
     std::vector<TcItem> items;
+    int tc_grid = 1;
     if (use_tc) {
         // Two query tiles of 128/G positions per CTA; heaviest items first so
         // the long causal rows start early and the tail of the grid is short.
@@ -657,6 +658,11 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
                     items.push_back(TcItem{b, h, i0, nt});
             }
         std::stable_sort(items.begin(), items.end(), [](const TcItem &x, const TcItem &y) { return x.nt > y.nt; });
+        // The persistent grid deals items round-robin (CTA c takes c, c + grid,
+        // ...); reverse every other round so each CTA's share stays even.
+        tc_grid = std::max(1, std::min<int>(c->num_sms, (int)items.size()));
+        for (size_t r0 = tc_grid; r0 < items.size(); r0 += 2 * (size_t)tc_grid)
+            std::reverse(items.begin() + r0, items.begin() + std::min(items.size(), r0 + tc_grid));
     }
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
@@ -687,7 +693,7 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
             }
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&] {
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items), (int)items.size(), B, n,
-                                     H_q, q, out, st);
+                                     H_q, q, out, tc_grid, st);
         });
     }
     return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {

@@ -23,10 +23,14 @@
 //    tiles wholly above the diagonal are skipped ("KV Cache 与 Prefill/
 //    Decode 推理路径", causal tile skipping).  Diagonal tiles are masked per
 //    element.
-//  * Warp roles: warp 0 issues TMA (Q once; K and V per key tile, one 16-
-//    token page box at a time through the block table, two stages); warp 1
-//    owns TMEM and issues the MMAs; warps 2-5 and 6-9 are two softmax
-//    warpgroups, one per query tile, thread = row.
+//  * Warp roles: warp 0 issues TMA (Q once per item; K and V per key tile,
+//    one 16-token page box at a time through the block table, two stages,
+//    K and V released separately); warp 1 owns TMEM and issues the MMAs;
+//    warpgroups 1 and 2 (warps 4-7, 8-11) run the softmax, one per query
+//    tile, thread = row.
+//  * Persistent: one CTA per SM walks a host-ordered item list; the MMA
+//    stream runs on across items so the next item's first S = Q K^T is
+//    issued right after the current item's last PV.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  S = Q K^T
 //    is computed into TMEM; the softmax warps read their row, write
 //    P = exp2(S*c - m) back as bf16 over the first 64 columns of S, and the
@@ -43,6 +47,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "sm100.cuh"
 
@@ -52,17 +58,26 @@ using namespace sm100;
 
 namespace {
 
+// Every GQA_EXP2_POLY_EVERY-th pair of exponentials is evaluated by a
+// polynomial on the FMA pipe instead of the MUFU unit (0 = never), to keep
+// the MUFU unit from bounding the softmax.
+#ifndef GQA_EXP2_POLY_EVERY
+#define GQA_EXP2_POLY_EVERY 0
+#endif
+
+constexpr int kPolyEvery = GQA_EXP2_POLY_EVERY > 0 ? GQA_EXP2_POLY_EVERY : 1;
+constexpr bool kPoly = GQA_EXP2_POLY_EVERY > 0;
 constexpr int D = 128;
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 q[2][2][128 * 64];                   // [query tile][column half]
     __nv_bfloat16 k[kStages][2][128 * 64];
     __nv_bfloat16 v[kStages][2][128 * 64];
-    uint64_t bar_q;
-    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t bar_q, q_empty;
+    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
     uint64_t s_full[2], p_full[2], o_full[2], fin;
     uint32_t tmem;
     int abort_;
@@ -71,12 +86,16 @@ struct __align__(1024) TcSmem {
 struct TcParams {
     const SeqDesc *seqs;
     const TcItem *items;
+    int32_t n_items;
     const int32_t *tables;
     int32_t stride;
     int32_t num_pages;
     int32_t H_kv;
+    int32_t H_q;
+    int32_t n;          // padded rows per batch entry
     int32_t G;          // query heads per KV head
     int32_t rows_pos;   // positions per query tile (128 / G)
+    __nv_bfloat16 *out; // [B, n, H_q, 128]
     int32_t *err;
     float scale_log2;   // log2(e) / sqrt(d_h)
 };
@@ -87,17 +106,15 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
     atomicOr(err, bit);
 }
 
+// Persistent: CTA c takes items c, c + gridDim.x, ...  Barrier phases run on
+// across items (global tile counter gt), so the next item's Q and first K/V
+// tile load while the current item's last tiles and epilogue run.
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mO,
-                  const __grid_constant__ CUtensorMap mKV, const TcParams p)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV, const TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem &s = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const TcItem it = p.items[blockIdx.x];
-    const SeqDesc sd = p.seqs[it.b];
-    const int nt = it.nt;
 
     if (warp == 1) {
         tmem_alloc(&s.tmem, 512);
@@ -106,10 +123,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     if (threadIdx.x == 0) {
         s.abort_ = 0;
         mbar_init(&s.bar_q, 1);
+        mbar_init(&s.q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.v_full[i], 1);
-            mbar_init(&s.kv_empty[i], 1);
+            mbar_init(&s.k_empty[i], 1);
+            mbar_init(&s.v_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s.s_full[t], 1);
@@ -130,19 +149,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             prefetch_tmap(&mQ);
             prefetch_tmap(&mKV);
             const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
-            mbar_arrive_expect_tx(&s.bar_q, q_bytes);
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < 2; ++c)
-                    tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
-            const int32_t *tab = p.tables + (size_t)sd.row * p.stride;
-            const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages && !mbar_wait(&s.kv_empty[st], ((j / kStages) - 1) & 1, &s.abort_)) {
-                    abort_with(s, p.err, kErrTimeout);
-                    break;
-                }
+            uint32_t gt = 0;                              // K tiles issued so far
+            int k = 0, q_issued = 0, v_missing = 0;
+            bool ok = true;
+            // Loads one K/V tile (8 pages, one 16-token box per page and
+            // column half) into stage gt % kStages once its last reader is done.
+            auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
+                const int st = gt % kStages;
+                const uint32_t use = gt / kStages;
+                const int32_t *tab = p.tables + (size_t)sd.row * p.stride;
+                const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
                 int page[8];
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg) {
@@ -157,28 +173,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     }
                     page[pg] = ph;
                 }
+                if (use > 0 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_))
+                    return false;
                 mbar_arrive_expect_tx(&s.k_full[st], 2 * kTileBytes);
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg)
                     for (int c = 0; c < 2; ++c)
                         tma_load_4d(&mKV, &s.k_full[st], s.k[st][c] + pg * 16 * 64, 64 * c, 0, it.kvh, page[pg]);
+                ++gt;                                     // K of this tile is in flight from here on
+                if (use > 0 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_)) {
+                    ++v_missing;
+                    return false;
+                }
                 mbar_arrive_expect_tx(&s.v_full[st], 2 * kTileBytes);
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg)
                     for (int c = 0; c < 2; ++c)
                         tma_load_4d(&mKV, &s.v_full[st], s.v[st][c] + pg * 16 * 64, 64 * c, 0, p.H_kv + it.kvh,
                                     page[pg]);
-                ++issued;
+                return true;
+            };
+            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
+                const TcItem it = p.items[idx];
+                const SeqDesc sd = p.seqs[it.b];
+                // The first K/V tile only needs a free stage; issue it before
+                // waiting for the previous item to release the Q buffers.
+                if (!load_kv(it, sd, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (k > 0 && !mbar_wait(&s.q_empty, (k - 1) & 1, &s.abort_)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&s.bar_q, q_bytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
+                ++q_issued;
+                for (int j = 1; j < it.nt; ++j)
+                    if (!load_kv(it, sd, j)) {
+                        ok = false;
+                        break;
+                    }
             }
-            // Drain: every issued copy must land before the CTA exits.
+            if (!ok)
+                abort_with(s, p.err, kErrTimeout);
+            // Drain: every issued copy lands before the CTA exits.
             int never = 0;
-            for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-                const int st = j % kStages;
-                if (!mbar_wait(&s.k_full[st], (j / kStages) & 1, &never) ||
-                    !mbar_wait(&s.v_full[st], (j / kStages) & 1, &never))
+            for (uint32_t g = (gt > kStages ? gt - kStages : 0); g < gt; ++g) {
+                const int st = g % kStages;
+                if (!mbar_wait(&s.k_full[st], (g / kStages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
-            if (!mbar_wait(&s.bar_q, 0, &never))
+            const uint32_t v_done = gt - v_missing;
+            for (uint32_t g = (v_done > kStages ? v_done - kStages : 0); g < v_done; ++g) {
+                const int st = g % kStages;
+                if (!mbar_wait(&s.v_full[st], (g / kStages) & 1, &never))
+                    atomicOr(p.err, kErrTimeout);
+            }
+            if (q_issued > 0 && !mbar_wait(&s.bar_q, (q_issued - 1) & 1, &never))
                 atomicOr(p.err, kErrTimeout);
         }
     } else if (warp == 1) {
@@ -201,6 +255,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     mma_ts(tm + 256 + 128 * t, tm + 128 * t + ks * 8, b, id_o, (acc || ks > 0) ? 1u : 0u);
                 }
             };
+            // One flat stream of key tiles over this CTA's items: tile g is
+            // tile j of item k; S of the next tile (of this item or the next
+            // one) is issued right after the PV that frees its TMEM columns.
+            int idx = blockIdx.x, k = 0, j = 0;
+            int nt = idx < p.n_items ? p.items[idx].nt : 0;
+            uint32_t g = 0;
             bool ok = nt > 0 && mbar_wait(&s.bar_q, 0, &s.abort_) && mbar_wait(&s.k_full[0], 0, &s.abort_);
             if (ok) {
                 tc_fence_after();
@@ -208,38 +268,58 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 mma_commit(&s.s_full[0]);
                 issue_s(1, 0);
                 mma_commit(&s.s_full[1]);
+                mma_commit(&s.k_empty[0]);
+                if (nt == 1)
+                    mma_commit(&s.q_empty);
             }
-            for (int j = 0; ok && j < nt; ++j) {
-                const int st = j % kStages, st2 = (j + 1) % kStages;
-                ok = mbar_wait(&s.p_full[0], j & 1, &s.abort_) && mbar_wait(&s.v_full[st], (j / kStages) & 1, &s.abort_);
+            while (ok) {
+                const int st = g % kStages, st2 = (g + 1) % kStages;
+                const bool last_of_item = j + 1 == nt;
+                const int next_idx = last_of_item ? idx + (int)gridDim.x : idx;
+                const bool has_next = next_idx < p.n_items;
+                const int next_nt = has_next ? (last_of_item ? p.items[next_idx].nt : nt) : 0;
+                const int next_j = last_of_item ? 0 : j + 1;
+                ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
+                     mbar_wait(&s.v_full[st], (g / kStages) & 1, &s.abort_);
                 if (!ok)
                     break;
                 tc_fence_after();
                 issue_o(0, st, j > 0);
-                if (j == nt - 1)
+                if (last_of_item)
                     mma_commit(&s.o_full[0]);
-                if (j + 1 < nt) {
-                    ok = mbar_wait(&s.k_full[st2], ((j + 1) / kStages) & 1, &s.abort_);
+                if (has_next) {
+                    ok = (!last_of_item || mbar_wait(&s.bar_q, (k + 1) & 1, &s.abort_)) &&
+                         mbar_wait(&s.k_full[st2], ((g + 1) / kStages) & 1, &s.abort_);
                     if (!ok)
                         break;
                     tc_fence_after();
                     issue_s(0, st2);
                     mma_commit(&s.s_full[0]);
                 }
-                ok = mbar_wait(&s.p_full[1], j & 1, &s.abort_);
+                ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
                 if (!ok)
                     break;
                 tc_fence_after();
                 issue_o(1, st, j > 0);
-                mma_commit(&s.kv_empty[st]);
-                if (j == nt - 1)
+                mma_commit(&s.v_empty[st]);
+                if (last_of_item)
                     mma_commit(&s.o_full[1]);
-                if (j + 1 < nt) {
-                    issue_s(1, st2);
-                    mma_commit(&s.s_full[1]);
+                if (!has_next)
+                    break;
+                issue_s(1, st2);
+                mma_commit(&s.s_full[1]);
+                mma_commit(&s.k_empty[st2]);
+                if (next_j + 1 == next_nt)
+                    mma_commit(&s.q_empty);              // the last S of that item reads Q now
+                ++g;
+                if (last_of_item) {
+                    idx = next_idx;
+                    ++k;
                 }
+                j = next_j;
+                nt = next_nt;
             }
-            if (!ok && nt > 0)
+            if (!ok)
                 abort_with(s, p.err, kErrTimeout);
             // Every issued MMA completes before TMEM is released.
             int never = 0;
@@ -247,51 +327,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (!mbar_wait(&s.fin, 0, &never))
                 atomicOr(p.err, kErrTimeout);
         }
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
-        const int t = (warp - 2) >> 2;                  // query tile of this warpgroup
+        const int t = (warp >> 2) - 1;                  // query tile of this warpgroup: 0 or 1
         const int quarter = warp & 3;                   // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;              // row of the tile
-        const bool row_in_box = r < p.G * p.rows_pos;
-        const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row index within the batch entry
-        const bool valid = row_in_box && rel < sd.count;
-        const int qpos = sd.past + rel;                 // absolute position: sees keys 0..qpos
         const uint32_t lane_addr = tm + ((uint32_t)(quarter * 32) << 16);
         const uint32_t tS = lane_addr + 128 * t, tO = lane_addr + 256 + 128 * t;
         const float c = p.scale_log2;
-        float m = -INFINITY, l = 0.0f;
+        const float2 cc = make_float2(c, c);
+        uint32_t gt = 0;
+        int k = 0;
         bool ok = true;
-
-        for (int j = 0; j < nt; ++j) {
-            if (!mbar_wait(&s.s_full[t], j & 1, &s.abort_)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float sv[128];
+        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
+            const TcItem it = p.items[idx];
+            const SeqDesc sd = p.seqs[it.b];
+            const int nt = it.nt;
+            const bool row_in_box = r < p.G * p.rows_pos;
+            const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
+            const bool valid = row_in_box && rel < sd.count;
+            const int qpos = sd.past + rel;             // absolute position: sees keys 0..qpos
+            float m = -INFINITY, l = 0.0f;
+            for (int j = 0; j < nt; ++j) {
+                const uint32_t g = gt + j;
+                if (!mbar_wait(&s.s_full[t], g & 1, &s.abort_)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t su[128];
+                tmem_ld128(tS, su);                      // this row of S (fp32)
+                const int key0 = 128 * j;
+                if (key0 + 127 > qpos) {                 // diagonal (or beyond): keys > qpos are masked
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t u[32];
-                tmem_ld32(tS + 32 * q4, u);
+                    for (int i = 0; i < 128; ++i)
+                        if (key0 + i > qpos)
+                            su[i] = 0xff800000u;         // -inf
+                }
+                // Row max: four independent 3-input max chains of depth 16.
+                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    sv[32 * q4 + i] = __uint_as_float(u[i]);
-            }
-            const int key0 = 128 * j;
-            if (key0 + 127 > qpos) {                     // diagonal (or beyond): mask keys > qpos
+                for (int i = 0; i < 128; i += 8) {
+                    a0 = max3(a0, __uint_as_float(su[i]), __uint_as_float(su[i + 1]));
+                    a1 = max3(a1, __uint_as_float(su[i + 2]), __uint_as_float(su[i + 3]));
+                    a2 = max3(a2, __uint_as_float(su[i + 4]), __uint_as_float(su[i + 5]));
+                    a3 = max3(a3, __uint_as_float(su[i + 6]), __uint_as_float(su[i + 7]));
+                }
+                const float mx = max3(fmaxf(a0, a1), a2, a3);
+                const float m_new = fmaxf(m, mx * c);
+                const bool grow = m_new > m + 8.0f;      // rescale only when the max grows by > 2^8
+                float alpha = 1.0f;
+                if (grow) {
+                    alpha = ex2(m - m_new);              // 0 on the first visible tile
+                    l *= alpha;
+                    m = m_new;
+                }
+                const float m_use = (m == -INFINITY) ? 0.0f : m;
+                const float2 mm = make_float2(-m_use, -m_use);
+                // P = 2^(S c - m), bf16, written over the first 64 columns of S.
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (key0 + i > qpos)
-                        sv[i] = -INFINITY;
-            }
-            float mx = sv[0];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[16];
 #pragma unroll
-            for (int i = 1; i < 128; ++i)
-                mx = fmaxf(mx, sv[i]);
-            const float m_new = fmaxf(m, mx * c);
-            if (m_new > m + 8.0f) {                      // rescale only when the max grows by > 2^8
-                const float alpha = ex2(m - m_new);      // 0 on the first visible tile
-                if (j > 0) {
+                    for (int i = 0; i < 16; ++i) {
+                        const int e = 32 * q4 + 2 * i;
+                        const float2 x =
+                            fma2(make_float2(__uint_as_float(su[e]), __uint_as_float(su[e + 1])), cc, mm);
+                        float2 pr;
+                        if (kPoly && (i % kPolyEvery) == kPolyEvery - 1)
+                            pr = exp2_poly2(x);
+                        else
+                            pr = make_float2(ex2(x.x), ex2(x.y));
+                        acc[i & 3] = add2(acc[i & 3], pr);
+                        pk[i] = pack_bf16x2(pr.x, pr.y);
+                    }
+                    tmem_st16(tS + 16 * q4, pk);
+                }
+                const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+                l += (s01.x + s01.y) + (s23.x + s23.y);
+                if (grow && j > 0) {                     // O (PV of tile j-1 is complete) *= alpha
 #pragma unroll 1
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t u[32];
@@ -302,70 +418,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         tmem_st32(tO + 32 * q4, u);
                     }
                 }
-                l *= alpha;
-                m = m_new;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s.p_full[t]);
             }
-            const float m_use = (m == -INFINITY) ? 0.0f : m;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(sv[32 * q4 + 2 * i], c, -m_use));
-                    const float p1 = ex2(fmaf(sv[32 * q4 + 2 * i + 1], c, -m_use));
-                    l += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + 16 * q4, pk);
+            if (!ok)
+                break;
+            // ---- epilogue: O / l -> bf16 -> the row of out, straight from registers.
+            // Padding rows were zeroed by the host; rows outside the tensor are skipped.
+            if (!mbar_wait(&s.o_full[t], k & 1, &s.abort_)) {
+                ok = false;
+                break;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s.p_full[t]);
-        }
-
-        // ---- epilogue: O / l -> bf16 -> shared memory (over this Q tile) -> TMA store
-        ok = ok && (nt == 0 || mbar_wait(&s.o_full[t], 0, &s.abort_));
-        if (!ok)
-            abort_with(s, p.err, kErrTimeout);
-        if (ok) {
             tc_fence_after();
-            const float inv_l = (valid && l > 0.0f) ? 1.0f / l : 0.0f;
-            unsigned char *stage_base = reinterpret_cast<unsigned char *>(s.q[t][0]);
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            __nv_bfloat16 *orow = p.out + (((size_t)it.b * p.n + rel) * p.H_q + it.kvh * p.G + r % p.G) * D;
 #pragma unroll 1
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t u[32];
-                if (nt > 0)
-                    tmem_ld32(tO + 32 * q4, u);
-                else
-                    for (int i = 0; i < 32; ++i)
-                        u[i] = 0;
+                tmem_ld32(tO + 32 * q4, u);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    pk[i] = valid ? pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l)
-                                  : 0u;                  // padding rows are written as zeros
-                // Columns 32*q4 .. +31 = half q4/2, 16-byte units 4*(q4%2) .. +3 of row r,
-                // placed with the 128-byte swizzle the store's tensor map expects.
-                unsigned char *row = stage_base + (q4 >> 1) * kTileBytes + r * 128;
+                    pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * q4);
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int unit = 4 * (q4 & 1) + k4;
-                    *reinterpret_cast<uint4 *>(row + ((unit ^ (r & 7)) * 16)) =
-                        make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        dst[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
                 }
             }
-            fence_proxy_async_smem();
+            tc_fence_before();
+            gt += nt;
         }
-        tc_fence_before();
-        named_bar_sync(1 + t, 128);
-        if (ok && warp == 2 + 4 * t && lane == 0) {
-            for (int h2 = 0; h2 < 2; ++h2)
-                tma_store_4d(&mO, s.q[t][h2], 64 * h2, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
-            tma_store_commit();
-            tma_store_wait_read();
-        }
+        if (!ok)
+            abort_with(s, p.err, kErrTimeout);
     }
 
     tc_fence_before();
@@ -409,15 +498,15 @@ bool prefill_tc_supported(int group, int H_kv) { return group >= 1 && group <= 1
 int prefill_tc_rows_per_tile(int group) { return 128 / group; }
 
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items, int n_items, int B,
-                              int n, int H_q, const void *q, void *out, cudaStream_t st)
+                              int n, int H_q, const void *q, void *out, int grid, cudaStream_t st)
 {
     if (pv.d != D || n_items <= 0)
         return n_items <= 0 ? cudaSuccess : cudaErrorInvalidValue;
     const int G = H_q / pv.H_kv;
     const int rows_pos = 128 / G;
-    if (G < 1 || rows_pos < 1)
+    if (G < 1 || rows_pos < 1 || grid < 1)
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mo, mkv;
+    CUtensorMap mq, mkv;
     const cuuint64_t qdims[4] = {(cuuint64_t)D, (cuuint64_t)H_q, (cuuint64_t)n, (cuuint64_t)B};
     const cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H_q * D * 2, (cuuint64_t)n * H_q * D * 2};
     const cuuint32_t qbox[4] = {64, (cuuint32_t)G, (cuuint32_t)rows_pos, 1};
@@ -426,18 +515,21 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     const cuuint64_t kvstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageTokens * D * 2,
                                  (cuuint64_t)2 * pv.H_kv * kPageTokens * D * 2};
     const cuuint32_t kvbox[4] = {64, (cuuint32_t)kPageTokens, 1, 1};
-    if (!encode4(&mq, q, qdims, qstr, qbox) || !encode4(&mo, out, qdims, qstr, qbox) ||
-        !encode4(&mkv, pv.pool, kvdims, kvstr, kvbox))
+    if (!encode4(&mq, q, qdims, qstr, qbox) || !encode4(&mkv, pv.pool, kvdims, kvstr, kvbox))
         return cudaErrorInvalidValue;
     TcParams prm;
     prm.seqs = d_seqs;
     prm.items = d_items;
+    prm.n_items = n_items;
     prm.tables = pv.tables;
     prm.stride = pv.stride;
     prm.num_pages = pv.num_pages;
     prm.H_kv = pv.H_kv;
+    prm.H_q = H_q;
+    prm.n = n;
     prm.G = G;
     prm.rows_pos = rows_pos;
+    prm.out = (__nv_bfloat16 *)out;
     prm.err = pv.err;
     prm.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     const int smem = (int)sizeof(TcSmem) + 1024;
@@ -448,7 +540,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
             return e;
         attr_set = true;
     }
-    prefill_tc_kernel<<<n_items, kThreads, smem, st>>>(mq, mo, mkv, prm);
+    prefill_tc_kernel<<<std::min(grid, n_items), kThreads, smem, st>>>(mq, mkv, prm);
     return cudaGetLastError();
 }
 

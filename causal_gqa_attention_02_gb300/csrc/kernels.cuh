@@ -85,7 +85,10 @@ cudaError_t launch_decode_combine(const int32_t *d_item_start, int B, int H_q, i
 // batch entries must already be in the cache (launch_cache_write first).
 bool prefill_tc_supported(int group, int H_kv);
 int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
+// Persistent grid of `grid` CTAs; CTA c takes items c, c + grid, ... (the
+// host orders the list so that this deals work evenly).  Padding rows of
+// `out` must be zeroed by the caller; the kernel writes valid rows only.
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items, int n_items, int B,
-                              int n, int H_q, const void *q, void *out, cudaStream_t st);
+                              int n, int H_q, const void *q, void *out, int grid, cudaStream_t st);
 
 }  // namespace gqa
