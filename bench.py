@@ -257,12 +257,17 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
         step()
     torch.cuda.synchronize()
     cache.profile_read()
-    cache.profile(True)
     ms, t0, t1 = timed_steps(torch, dist, step, args.steps, flush)
-    cache.profile(False)
-    prof = cache.profile_read()
+    region_launches = cache.profile_read()            # launch counts of the timed region
     total_ms = dist.max(torch, sum(ms))
     value = flops * args.steps * dist.world / (total_ms / 1e3) / 1e12
+    # Per-kernel durations: a second timed region with each launch bracketed
+    # by events on its stream (events between kernels keep them from
+    # overlapping, so this region is timed separately from the step).
+    cache.profile(True)
+    timed_steps(torch, dist, step, args.steps, flush)
+    cache.profile(False)
+    prof = cache.profile_read()
     kernel = "prefill_tc" if prof["prefill_tc"][0] else "attn_simt"
     launches, kms = prof[kernel]
     avg_ms = kms / max(1, launches)
@@ -272,7 +277,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
                 "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel), "kernel": kernel,
                 "kernel_ms": round(avg_ms, 4), "algorithmic_flops_per_launch": flops,
                 "peak_source": "%s bf16 dense (burst)" % peak_src}
-    gpu_launches = sum(nl for nl, _ in prof.values())
+    gpu_launches = sum(nl for nl, _ in region_launches.values())
     kernels = {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl}
 
     # End to end through the public API from pinned host buffers.
@@ -336,12 +341,14 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         step()
     torch.cuda.synchronize()
     cache.profile_read()
-    cache.profile(True)
     ms, t0, t1 = timed_steps(torch, dist, step, args.steps)
-    cache.profile(False)
-    prof = cache.profile_read()
+    region_launches = cache.profile_read()
     total_ms = dist.max(torch, sum(ms))
     value = kv_bytes * args.steps * dist.world / (total_ms / 1e3) / 1e9
+    cache.profile(True)
+    timed_steps(torch, dist, step, args.steps)
+    cache.profile(False)
+    prof = cache.profile_read()
     kernel = "decode_split" if prof["decode_split"][0] else "attn_simt"
     launches, kms = prof[kernel]
     avg_ms = kms / max(1, launches)
@@ -374,7 +381,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
            "e2e": {"value": round(kv_bytes * args.steps * dist.world / (e2e_total / 1e3) / 1e9, 1), "unit": "GB/s",
                    "h2d_bytes_per_step": int(q.nbytes + new_k.nbytes + new_v.nbytes),
                    "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4)},
-           "gpu_launches": sum(nl for nl, _ in prof.values()),
+           "gpu_launches": sum(nl for nl, _ in region_launches.values()),
            "kernels": {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl},
            "config": {"workload": "bf16 paged decode: B=%d, H_q=%d, H_kv=%d, d_h=%d, cache lengths ~U{1024..8192} "
                                   "(seed %d, sum %d tokens) incl. the appended token, pages placed by a seeded "

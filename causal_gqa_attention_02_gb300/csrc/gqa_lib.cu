@@ -677,20 +677,16 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
              return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
          })) != GQA_OK)
         return rc;
+    // On the tensor-core path the write kernel also zeroes the padding rows
+    // of out (discarded rows are written as zeros); the prefill kernel then
+    // writes the valid rows only.
+    const int out_row_bytes = H_q * c->desc.head_dim * c->esize;
     if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&] {
-             return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st);
+             return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st, use_tc ? out : nullptr,
+                                       out_row_bytes);
          })) != GQA_OK)
         return rc;
     if (use_tc) {
-        // Padding rows (discarded, written as zeros): contiguous per entry.
-        const size_t row_bytes = (size_t)H_q * c->desc.head_dim * c->esize;
-        for (int b = 0; b < B; ++b)
-            if (sds[b].count < n) {
-                cudaError_t e = cudaMemsetAsync((char *)out + ((size_t)b * n + sds[b].count) * row_bytes, 0,
-                                                (size_t)(n - sds[b].count) * row_bytes, st);
-                if (e != cudaSuccess)
-                    return cuda_fail(e, "padding rows");
-            }
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&] {
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items), (int)items.size(), B, n,
                                      H_q, q, out, tc_grid, st);

@@ -32,39 +32,69 @@ template <> struct Unit<4>  { using T = uint32_t; };
 template <> struct Unit<2>  { using T = uint16_t; };
 template <> struct Unit<1>  { using T = uint8_t; };
 
-// grid: (x = blocks over units, y = batch entry).  Unit u of entry b:
-//   chunk c of row (token t, kv, head hh).
+// grid: (x = token blocks, y = batch entry); one warp per token.  A token's
+// K rows for all KV heads are contiguous in k (H_kv * d * esize bytes), so a
+// warp reads them with consecutive lanes on consecutive units and writes each
+// head's row to its (page, slot): both sides coalesced.  Every unit of the
+// token is loaded before any is stored, to keep the loads in flight.
+// With zero_out != nullptr the same grid also writes zeros over the padding
+// rows count..n-1 of zero_out ([B, n, zero_row_bytes]).
 template <int U>
-__global__ void cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int n,
-                                   const char *__restrict__ k, const char *__restrict__ v)
+__global__ void __launch_bounds__(256)
+cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int n, const char *__restrict__ k,
+                   const char *__restrict__ v, char *__restrict__ zero_out, int zero_row_bytes)
 {
     using T = typename Unit<U>::T;
+    constexpr int kMaxPerLane = 8;                      // units per lane held in registers per pass
+    asm volatile("griddepcontrol.launch_dependents;");
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
-    const size_t row_bytes = (size_t)pv.d * esize;
-    const int cpr = (int)(row_bytes / U);                 // units per row
-    const long long units = (long long)sd.count * pv.H_kv * 2 * cpr;
-    const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    const int row_bytes = pv.d * esize;
+    const int cpr = row_bytes / U;                      // units per (token, head) row
+    const int units = pv.H_kv * cpr;                    // units of one token's K (or V)
     const size_t page_bytes = (size_t)2 * pv.H_kv * kPageTokens * row_bytes;
-    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-         u += (long long)gridDim.x * blockDim.x) {
-        const int c = (int)(u % cpr);
-        long long r = u / cpr;
-        const int hh = (int)(r % pv.H_kv);
-        r /= pv.H_kv;
-        const int kv = (int)(r % 2);
-        const int t = (int)(r / 2);
+    const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
+    for (int t = blockIdx.x * wpb + warp; t < sd.count; t += gridDim.x * wpb) {
         const int pos = sd.past + t;
         const int page = tab[pos / kPageTokens];
         if ((unsigned)page >= (unsigned)pv.num_pages) {
-            atomicOr(pv.err, kErrPageId);
+            if (lane == 0)
+                atomicOr(pv.err, kErrPageId);
             continue;
         }
-        const char *src = (kv ? v : k) + (((size_t)b * n + t) * pv.H_kv + hh) * row_bytes + (size_t)c * U;
-        char *dst = (char *)pv.pool + (size_t)page * page_bytes +
-                    ((size_t)(kv * pv.H_kv + hh) * kPageTokens + pos % kPageTokens) * row_bytes +
-                    (size_t)c * U;
-        *(T *)dst = *(const T *)src;
+        const size_t src_off = ((size_t)b * n + t) * (size_t)units * U;
+        char *kd = (char *)pv.pool + (size_t)page * page_bytes + (size_t)(pos % kPageTokens) * row_bytes;
+        char *vd = kd + (size_t)pv.H_kv * kPageTokens * row_bytes;
+        for (int u0 = 0; u0 < units; u0 += 32 * kMaxPerLane) {
+            T kr[kMaxPerLane], vr[kMaxPerLane];
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i) {
+                const int u = u0 + 32 * i + lane;
+                if (u < units) {
+                    kr[i] = *(const T *)(k + src_off + (size_t)u * U);
+                    vr[i] = *(const T *)(v + src_off + (size_t)u * U);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i) {
+                const int u = u0 + 32 * i + lane;
+                if (u < units) {
+                    const int hh = u / cpr, c = u - hh * cpr;
+                    const size_t off = (size_t)hh * kPageTokens * row_bytes + (size_t)c * U;
+                    *(T *)(kd + off) = kr[i];
+                    *(T *)(vd + off) = vr[i];
+                }
+            }
+        }
+    }
+    if (zero_out) {
+        const int zunits = zero_row_bytes / 16;
+        for (int t = sd.count + blockIdx.x * wpb + warp; t < n; t += gridDim.x * wpb) {
+            uint4 *dst = (uint4 *)(zero_out + ((size_t)b * n + t) * zero_row_bytes);
+            for (int u = lane; u < zunits; u += 32)
+                dst[u] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -95,25 +125,29 @@ __global__ void cow_copy_kernel(PoolView pv, int esize, const CowDesc *__restric
 }
 
 cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_seqs, int B, int n,
-                               int max_count, const void *k, const void *v, cudaStream_t st)
+                               int max_count, const void *k, const void *v, cudaStream_t st, void *zero_out,
+                               int zero_row_bytes)
 {
-    if (B <= 0 || max_count <= 0)
+    const int rows = zero_out ? n : max_count;          // padding rows are zeroed too
+    if (B <= 0 || rows <= 0)
         return cudaSuccess;
     const size_t row_bytes = (size_t)pv.d * esize;
     const int U = copy_unit_bytes(row_bytes, k, v, pv.pool);
-    const long long units = (long long)max_count * pv.H_kv * 2 * (long long)(row_bytes / U);
-    const int threads = 256;
-    long long blocks = (units + threads - 1) / threads;
-    if (blocks > 4096)
-        blocks = 4096;
+    if (zero_out && (zero_row_bytes % 16 != 0 || (uintptr_t)zero_out % 16 != 0))
+        return cudaErrorInvalidValue;
+    const int wpb = 8;
+    int blocks = (rows + wpb - 1) / wpb;
+    if (blocks > 1024)
+        blocks = 1024;
     dim3 grid((unsigned)blocks, (unsigned)B);
     const char *kc = (const char *)k, *vc = (const char *)v;
+    char *z = (char *)zero_out;
     switch (U) {
-    case 16: cache_write_kernel<16><<<grid, threads, 0, st>>>(pv, esize, d_seqs, n, kc, vc); break;
-    case 8:  cache_write_kernel<8><<<grid, threads, 0, st>>>(pv, esize, d_seqs, n, kc, vc); break;
-    case 4:  cache_write_kernel<4><<<grid, threads, 0, st>>>(pv, esize, d_seqs, n, kc, vc); break;
-    case 2:  cache_write_kernel<2><<<grid, threads, 0, st>>>(pv, esize, d_seqs, n, kc, vc); break;
-    default: cache_write_kernel<1><<<grid, threads, 0, st>>>(pv, esize, d_seqs, n, kc, vc); break;
+    case 16: cache_write_kernel<16><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
+    case 8:  cache_write_kernel<8><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
+    case 4:  cache_write_kernel<4><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
+    case 2:  cache_write_kernel<2><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
+    default: cache_write_kernel<1><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
     }
     return cudaGetLastError();
 }

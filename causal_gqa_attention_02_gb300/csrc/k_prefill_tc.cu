@@ -193,6 +193,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                                     page[pg]);
                 return true;
             };
+            // This grid may start while the cache write that fills the pool
+            // is still running (programmatic dependent launch): Q does not
+            // depend on it, so the first item's Q load goes out before the
+            // wait, and every pool read after it.
+            bool first_q_issued = false;
+            if (blockIdx.x < p.n_items) {
+                const TcItem it = p.items[blockIdx.x];
+                mbar_arrive_expect_tx(&s.bar_q, q_bytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
+                first_q_issued = true;
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
                 const TcItem it = p.items[idx];
                 const SeqDesc sd = p.seqs[it.b];
@@ -202,14 +216,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     ok = false;
                     break;
                 }
-                if (k > 0 && !mbar_wait(&s.q_empty, (k - 1) & 1, &s.abort_)) {
-                    ok = false;
-                    break;
+                if (k > 0) {
+                    if (!mbar_wait(&s.q_empty, (k - 1) & 1, &s.abort_)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.bar_q, q_bytes);
+                    for (int t = 0; t < 2; ++t)
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos,
+                                        it.b);
                 }
-                mbar_arrive_expect_tx(&s.bar_q, q_bytes);
-                for (int t = 0; t < 2; ++t)
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
                 ++q_issued;
                 for (int j = 1; j < it.nt; ++j)
                     if (!load_kv(it, sd, j)) {
@@ -232,6 +249,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 if (!mbar_wait(&s.v_full[st], (g / kStages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
+            if (first_q_issued && q_issued == 0)
+                q_issued = 1;
             if (q_issued > 0 && !mbar_wait(&s.bar_q, (q_issued - 1) & 1, &never))
                 atomicOr(p.err, kErrTimeout);
         }
@@ -540,8 +559,20 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
             return e;
         attr_set = true;
     }
-    prefill_tc_kernel<<<std::min(grid, n_items), kThreads, smem, st>>>(mq, mkv, prm);
-    return cudaGetLastError();
+    // Launched as a programmatic dependent of the cache write just before
+    // it on the stream: the kernel waits (griddepcontrol.wait) before it
+    // reads the pool.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min(grid, n_items));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mq, mkv, prm);
 }
 
 }  // namespace gqa
