@@ -46,7 +46,6 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
 {
     using T = typename Unit<U>::T;
     constexpr int kMaxPerLane = 8;                      // units per lane held in registers per pass
-    asm volatile("griddepcontrol.launch_dependents;");
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;

@@ -120,6 +120,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
+    // Rows G*rows_pos..127 of each query tile are never written by the Q box
+    // (G not dividing 128); zero them once so they hold finite values.
+    {
+        const int box_rows = p.G * p.rows_pos;
+        const int extra = (128 - box_rows) * 128 / 16;  // 16-byte units per tile half
+        for (int u = threadIdx.x; u < 4 * extra; u += blockDim.x) {
+            const int th = u / extra, r = u % extra;    // th = tile * 2 + half
+            reinterpret_cast<uint4 *>(s.q[th >> 1][th & 1] + box_rows * 64)[r] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         s.abort_ = 0;
         mbar_init(&s.bar_q, 1);
@@ -193,10 +204,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                                     page[pg]);
                 return true;
             };
-            // This grid may start while the cache write that fills the pool
-            // is still running (programmatic dependent launch): Q does not
-            // depend on it, so the first item's Q load goes out before the
-            // wait, and every pool read after it.
+            // The first item's Q load is issued before the K/V loop.
             bool first_q_issued = false;
             if (blockIdx.x < p.n_items) {
                 const TcItem it = p.items[blockIdx.x];
@@ -206,7 +214,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
                 first_q_issued = true;
             }
-            asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
                 const TcItem it = p.items[idx];
                 const SeqDesc sd = p.seqs[it.b];
@@ -374,6 +381,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     break;
                 }
                 tc_fence_after();
+                __syncwarp();                            // tcgen05.ld is warp-collective
                 uint32_t su[128];
                 tmem_ld128(tS, su);                      // this row of S (fp32)
                 const int key0 = 128 * j;
@@ -401,6 +409,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     l *= alpha;
                     m = m_new;
                 }
+                // The O rescale below touches TMEM with warp-collective loads
+                // and stores: do it for the whole warp when any row needs it
+                // (alpha = 1 for the others).
+                const bool rescale_o = __any_sync(0xffffffffu, grow && j > 0);
+                __syncwarp();
                 const float m_use = (m == -INFINITY) ? 0.0f : m;
                 const float2 mm = make_float2(-m_use, -m_use);
                 // P = 2^(S c - m), bf16, written over the first 64 columns of S.
@@ -426,7 +439,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 }
                 const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
                 l += (s01.x + s01.y) + (s23.x + s23.y);
-                if (grow && j > 0) {                     // O (PV of tile j-1 is complete) *= alpha
+                if (rescale_o) {                         // O (PV of tile j-1 is complete) *= alpha
 #pragma unroll 1
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t u[32];
@@ -442,6 +455,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&s.p_full[t]);
+                __syncwarp();
             }
             if (!ok)
                 break;
@@ -457,6 +471,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
 #pragma unroll 1
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t u[32];
+                __syncwarp();                            // the stores below diverge on `valid`
                 tmem_ld32(tO + 32 * q4, u);
                 uint32_t pk[16];
 #pragma unroll
@@ -559,20 +574,8 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
             return e;
         attr_set = true;
     }
-    // Launched as a programmatic dependent of the cache write just before
-    // it on the stream: the kernel waits (griddepcontrol.wait) before it
-    // reads the pool.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min(grid, n_items));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, mq, mkv, prm);
+    prefill_tc_kernel<<<std::min(grid, n_items), kThreads, smem, st>>>(mq, mkv, prm);
+    return cudaGetLastError();
 }
 
 }  // namespace gqa

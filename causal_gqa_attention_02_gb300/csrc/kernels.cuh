@@ -64,9 +64,7 @@ cudaError_t launch_cow_copy(const PoolView &pv, int esize, const CowDesc *d_cows
 
 // Write rows c < seqs[b].count of k/v [B, n, H_kv, d] to positions past+c.
 // If zero_out is given ([B, n, zero_row_bytes], 16-byte aligned rows), its
-// rows count..n-1 of every entry are set to zero in the same launch.  The
-// kernel lets a dependent launch (programmatic stream serialization) start
-// early; that kernel must wait (griddepcontrol.wait) before reading the pool.
+// rows count..n-1 of every entry are set to zero in the same launch.
 cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_seqs, int B, int n,
                                int max_count, const void *k, const void *v, cudaStream_t st,
                                void *zero_out = nullptr, int zero_row_bytes = 0);

@@ -12,7 +12,7 @@ namespace gqa {
 namespace sm100 {
 
 // A bounded wait gives up after this long (ns) and reports a timeout.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -51,12 +51,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Non-blocking probe: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -65,8 +66,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 }
 
 // Wait until the barrier phase of the given parity has completed.  Returns
-// false (without waiting further) once *abort is non-zero or the wait has
-// lasted kWaitTimeoutNs.
+// false once *abort is non-zero or the wait has lasted kWaitTimeoutNs.  The
+// probe never suspends the thread (test_wait, not try_wait), so the bound
+// holds whatever the hardware's suspension policy is; a short sleep between
+// probes keeps a waiting warp from taking issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
 {
     if (mbar_test(bar, parity))
@@ -75,32 +78,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     for (uint32_t it = 1;; ++it) {
         if (mbar_test(bar, parity))
             return true;
+        if (it > 16)
+            __nanosleep(32);
         if ((it & 63) == 0) {
-            if (*abort)
-                return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs)
-                return false;
-        }
-    }
-}
-
-// Same contract as mbar_wait, polling with the non-suspending test_wait: for
-// the one thread on a latency-critical path (the MMA issuer).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, const volatile int *abort)
-{
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (ok)
-            return true;
-        if ((it & 255) == 255) {
             if (*abort)
                 return false;
             if (globaltimer() - t0 > kWaitTimeoutNs)
