@@ -13,14 +13,16 @@
 //  * one CTA per (batch entry, token chunk, KV head): all g = H_q/H_kv query
 //    heads of the group are served from one read of the group's K/V (the
 //    KV head is indexed, never duplicated);
-//  * K pass: a warp takes one 16-token page (4 KiB, contiguous); lane pair
-//    (2t, 2t+1) reads token t's row as eight 16-byte loads each, dots it
-//    with q held in shared memory, and one shuffle joins the two halves;
+//  * K pass: a warp takes one 16-token page (4 KiB, contiguous); each
+//    half-warp reads a whole 256-byte token row per 16-byte-per-lane load
+//    (512 contiguous bytes per instruction), dots its 8 columns with q held
+//    in registers (packed fp32 pairs), and a transpose-reduce over the 16
+//    lanes of a row (token set halved at each exchange) forms the scores;
 //  * softmax of the chunk is exact (chunk max, then exp2 and sum), kept as
 //    (max, sum) for the combine;
-//  * V pass: a warp takes a page; lane l owns output elements 4l..4l+3 and
-//    reads them for all 16 tokens with 8-byte loads (a warp covers one
-//    256-byte row per load: coalesced);
+//  * V pass: the same lane layout; each lane accumulates its 8 columns over
+//    its half-warp's tokens with probabilities broadcast from shared memory,
+//    then the half-warps and the warps are summed;
 //  * partials (max, sum, unnormalised o[g][128]) go to a workspace; the
 //    combine kernel merges a sequence's chunks in a fixed order:
 //        M = max_s m_s,  out = sum_s 2^(m_s-M) o_s / sum_s 2^(m_s-M) l_s.
@@ -62,16 +64,30 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// A bf16 pair (low half = lower index) as two floats.
+__device__ __forceinline__ float2 bf2(uint32_t x) { return make_float2(bf_lo(x), bf_hi(x)); }
+
+// Lane layout for both passes over a 16-token page: lane l covers tokens
+// 2i + l/16 (i = 0..7) and columns 8(l%16)..8(l%16)+7, so one 16-byte load
+// per lane reads two whole 256-byte token rows: 512 contiguous bytes.
 template <int G>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeItem *__restrict__ items,
                     int chunk, int H_q, const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o,
                     float *__restrict__ ws_ml)
 {
-    // q split in two halves of 64, the second offset by 68 floats so the two
-    // halves' broadcasts fall in different banks.
-    __shared__ __align__(16) float qs[G][2][68];
-    __shared__ float sc[G][kMaxChunk];
+    __shared__ __align__(16) float sc[kMaxChunk][G];     // scores, then probabilities (token-major)
     __shared__ __align__(16) float red[kWarps][G][D];
     __shared__ float ml[G][2];
 
@@ -87,60 +103,88 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride + t0 / kPageTokens;
     const __nv_bfloat16 *pool = (const __nv_bfloat16 *)pv.pool;
     const size_t page_elems = (size_t)2 * H_kv * kPageTokens * D;
+    const int half = lane >> 4, col = 8 * (lane & 15);
 
-    const float qscale = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d_h)
-    for (int idx = threadIdx.x; idx < G * D; idx += kWarps * 32) {
-        const int h = idx / D, e = idx % D;
-        qs[h][e / 64][e % 64] = __bfloat162float(q[((size_t)it.b * H_q + kvh * G + h) * D + e]) * qscale;
+    // This lane's eight q columns of every head of the group, pre-scaled by
+    // log2(e)/sqrt(d_h) so scores come out in exp2 units.
+    const float qscale = 1.4426950408889634f / sqrtf((float)D);
+    float2 qr[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint4 qv = *reinterpret_cast<const uint4 *>(q + ((size_t)it.b * H_q + kvh * G + h) * D + col);
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            qr[h][u] = make_float2(bf_lo(w[u]) * qscale, bf_hi(w[u]) * qscale);
     }
-    __syncthreads();
 
     // ---- K pass: scores of the chunk -------------------------------------
-    {
-        const int tok = lane >> 1, half = lane & 1;
-        for (int pg = warp; pg < npages; pg += kWarps) {
-            const int page = tab[pg];
-            const bool ok = (unsigned)page < (unsigned)pv.num_pages;
-            float acc[G];
+    for (int pg = warp; pg < npages; pg += kWarps) {
+        const int page = tab[pg];
+        const bool ok = (unsigned)page < (unsigned)pv.num_pages;
+        float v[8][G];
+        if (ok) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(pool + (size_t)page * page_elems +
+                                                              (size_t)kvh * kPageTokens * D) + lane;
+            uint4 kk[8];
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                acc[h] = 0.0f;
-            if (ok) {
-                const uint4 *kr = reinterpret_cast<const uint4 *>(pool + (size_t)page * page_elems +
-                                                                  (size_t)kvh * kPageTokens * D) +
-                                  tok * 16 + half * 8;
-                uint4 kk[8];
+            for (int i = 0; i < 8; ++i)
+                kk[i] = kr[32 * i];                      // token 2i + half, columns col..col+7
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    kk[j] = kr[j];
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float f[8] = {bf_lo(kk[j].x), bf_hi(kk[j].x), bf_lo(kk[j].y), bf_hi(kk[j].y),
-                                        bf_lo(kk[j].z), bf_hi(kk[j].z), bf_lo(kk[j].w), bf_hi(kk[j].w)};
+                for (int h = 0; h < G; ++h) {
+                    float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(&qs[h][half][j * 8]);
-                        const float4 qb = *reinterpret_cast<const float4 *>(&qs[h][half][j * 8 + 4]);
-                        float a = acc[h];
-                        a = fmaf(f[0], qa.x, a); a = fmaf(f[1], qa.y, a);
-                        a = fmaf(f[2], qa.z, a); a = fmaf(f[3], qa.w, a);
-                        a = fmaf(f[4], qb.x, a); a = fmaf(f[5], qb.y, a);
-                        a = fmaf(f[6], qb.z, a); a = fmaf(f[7], qb.w, a);
-                        acc[h] = a;
-                    }
+                    for (int u = 0; u < 4; ++u)
+                        a = fma2(bf2(w[u]), qr[h][u], a);
+                    v[i][h] = a.x + a.y;
                 }
-            } else if (lane == 0) {
-                atomicOr(pv.err, kErrPageId);
             }
+        } else {
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-            const int tl = pg * kPageTokens + tok;
-            if (half == 0) {
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    sc[h][tl] = (ok && tl < nt) ? acc[h] : -INFINITY;
+                    v[i][h] = 0.f;
+            if (lane == 0)
+                atomicOr(pv.err, kErrPageId);
+        }
+        // Sum each token's 16 column slices: halve the token set at every
+        // exchange (xor 8, 4, 2), then finish the last pair (xor 1).
+        const int b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float send = b3 ? v[i][h] : v[i + 4][h];
+                const float keep = b3 ? v[i + 4][h] : v[i][h];
+                v[i][h] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
             }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float send = b2 ? v[i][h] : v[i + 2][h];
+                const float keep = b2 ? v[i + 2][h] : v[i][h];
+                v[i][h] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float send = b1 ? v[0][h] : v[1][h];
+            const float keep = b1 ? v[1][h] : v[0][h];
+            v[0][h] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            v[0][h] += __shfl_xor_sync(0xffffffffu, v[0][h], 1);
+        // Lane pair (l, l^1) now holds token 2(4 b3 + 2 b2 + b1) + half.
+        const int tl = pg * kPageTokens + 2 * (4 * b3 + 2 * b2 + b1) + half;
+        if ((lane & 1) == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                sc[tl][h] = (ok && tl < nt) ? v[0][h] : -INFINITY;
         }
     }
     __syncthreads();
@@ -150,14 +194,14 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     for (int h = warp; h < G; h += kWarps) {
         float mx = -INFINITY;
         for (int t = lane; t < nslots; t += 32)
-            mx = fmaxf(mx, sc[h][t]);
+            mx = fmaxf(mx, sc[t][h]);
         mx = warp_max(mx);
         float sum = 0.0f;
         for (int t = lane; t < nslots; t += 32) {
-            const float s = sc[h][t];
-            const float p = (s == -INFINITY) ? 0.0f : ex2(s - mx);
-            sc[h][t] = p;
-            sum += p;
+            const float s2 = sc[t][h];
+            const float pr = (s2 == -INFINITY) ? 0.0f : ex2(s2 - mx);
+            sc[t][h] = pr;
+            sum += pr;
         }
         sum = warp_sum(sum);
         if (lane == 0) {
@@ -167,51 +211,63 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     }
     __syncthreads();
 
-    // ---- V pass: o[h][4*lane .. 4*lane+3] ---------------------------------
-    float o[G][4];
+    // ---- V pass: o[h][col..col+7] over this half-warp's tokens -----------
+    float2 o[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h)
-        o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            o[h][u] = make_float2(0.f, 0.f);
     for (int pg = warp; pg < npages; pg += kWarps) {
         const int page = tab[pg];
         if ((unsigned)page >= (unsigned)pv.num_pages)
             continue;
-        const uint2 *vr = reinterpret_cast<const uint2 *>(pool + (size_t)page * page_elems +
+        const uint4 *vr = reinterpret_cast<const uint4 *>(pool + (size_t)page * page_elems +
                                                           (size_t)(H_kv + kvh) * kPageTokens * D) + lane;
-        uint2 vv[kPageTokens];
+        uint4 vv[8];
 #pragma unroll
-        for (int tk = 0; tk < kPageTokens; ++tk)
-            vv[tk] = vr[tk * (D / 4)];
+        for (int i = 0; i < 8; ++i)
+            vv[i] = vr[32 * i];
 #pragma unroll
-        for (int tk = 0; tk < kPageTokens; ++tk) {
-            const int tl = pg * kPageTokens + tk;
-            if (tl < nt) {
-                const float f0 = bf_lo(vv[tk].x), f1 = bf_hi(vv[tk].x);
-                const float f2 = bf_lo(vv[tk].y), f3 = bf_hi(vv[tk].y);
+        for (int i = 0; i < 8; ++i) {
+            const int tl = pg * kPageTokens + 2 * i + half;   // probabilities are 0 past nt
+            const uint32_t w[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float p = sc[h][tl];
-                    o[h][0] = fmaf(p, f0, o[h][0]);
-                    o[h][1] = fmaf(p, f1, o[h][1]);
-                    o[h][2] = fmaf(p, f2, o[h][2]);
-                    o[h][3] = fmaf(p, f3, o[h][3]);
-                }
+            for (int h = 0; h < G; ++h) {
+                const float pr = sc[tl][h];
+                const float2 pp = make_float2(pr, pr);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    o[h][u] = fma2(pp, bf2(w[u]), o[h][u]);
             }
         }
     }
+    // Join the two half-warps (different tokens, same columns), then the warps.
 #pragma unroll
     for (int h = 0; h < G; ++h)
-        *reinterpret_cast<float4 *>(&red[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            o[h][u].x += __shfl_xor_sync(0xffffffffu, o[h][u].x, 16);
+            o[h][u].y += __shfl_xor_sync(0xffffffffu, o[h][u].y, 16);
+        }
+    if (half == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4 *dst = reinterpret_cast<float4 *>(&red[warp][h][col]);
+            dst[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+            dst[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
+        }
+    }
     __syncthreads();
 
     float *wo = ws_o + ((size_t)blockIdx.x * H_kv + kvh) * G * D;
     for (int idx = threadIdx.x; idx < G * D; idx += kWarps * 32) {
         const int h = idx / D, e = idx % D;
-        float s = red[0][h][e];
+        float acc = red[0][h][e];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w)
-            s += red[w][h][e];
-        wo[idx] = s;
+            acc += red[w][h][e];
+        wo[idx] = acc;
     }
     if (threadIdx.x < G) {
         float *wm = ws_ml + (((size_t)blockIdx.x * H_kv + kvh) * G + threadIdx.x) * 2;
