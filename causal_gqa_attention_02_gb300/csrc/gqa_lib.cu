@@ -79,6 +79,8 @@ struct gqa_cache {
     size_t stage_cap = 0;
     float *d_ws = nullptr;               // decode split partials
     size_t ws_cap = 0;
+    int32_t *d_cnt = nullptr;            // decode merge counters [B * H_kv], kept at zero
+    size_t cnt_cap = 0;
     std::vector<char> h_stage;
     int device = -1;
     int num_sms = 0;
@@ -290,6 +292,29 @@ int ensure_ws(gqa_cache *c, size_t floats)
     return GQA_OK;
 }
 
+// Counters the decode kernel's merge uses; zero when allocated, and the
+// kernel leaves them zero.
+int ensure_cnt(gqa_cache *c, size_t n)
+{
+    if (n <= c->cnt_cap)
+        return GQA_OK;
+    if (c->d_cnt) {
+        cudaError_t e = cudaFree(c->d_cnt);
+        c->d_cnt = nullptr;
+        c->cnt_cap = 0;
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFree(counters)");
+    }
+    const size_t cap = std::max<size_t>(n, 4096);
+    cudaError_t e = cudaMalloc((void **)&c->d_cnt, cap * sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(c->d_cnt, 0, cap * sizeof(int32_t));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "counters");
+    c->cnt_cap = cap;
+    return GQA_OK;
+}
+
 cudaEvent_t get_event(gqa_cache *c)
 {
     if (!c->spare_events.empty()) {
@@ -445,6 +470,7 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_err) cudaFree(c->d_err);
         if (c->d_stage) cudaFree(c->d_stage);
         if (c->d_ws) cudaFree(c->d_ws);
+        if (c->d_cnt) cudaFree(c->d_cnt);
         for (const auto &r : c->prof_recs) {
             cudaEventDestroy(r.start);
             cudaEventDestroy(r.end);
@@ -802,19 +828,24 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         const size_t n_part = items.size() * (size_t)H_kv * G;
         if ((rc = ensure_ws(c, n_part * 128 + n_part * 2)) != GQA_OK)
             return rc;
+        if ((rc = ensure_cnt(c, (size_t)B * H_kv)) != GQA_OK)
+            return rc;
         if ((rc = upload_stage(c, st)) != GQA_OK)
             return rc;
-        float *ws_o = c->d_ws, *ws_ml = c->d_ws + n_part * 128;
-        if ((rc = run_kernel(c, GQA_KERNEL_DECODE_SPLIT, st, "decode split kernel", [&] {
-                 return launch_decode_split(pv, (const SeqDesc *)(c->d_stage + o_sds),
-                                            (const DecodeItem *)(c->d_stage + o_items), (int)items.size(), chunk,
-                                            H_q, q, ws_o, ws_ml, st);
-             })) != GQA_OK)
-            return rc;
-        return run_kernel(c, GQA_KERNEL_DECODE_COMBINE, st, "decode combine kernel", [&] {
-            return launch_decode_combine((const int32_t *)(c->d_stage + o_start), B, H_q, H_kv, ws_o, ws_ml, out,
-                                         st);
-        });
+        DecodeLaunch a;
+        a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        a.items = (const DecodeItem *)(c->d_stage + o_items);
+        a.item_start = (const int32_t *)(c->d_stage + o_start);
+        a.n_items = (int)items.size();
+        a.chunk = chunk;
+        a.H_q = H_q;
+        a.q = q;
+        a.ws_o = c->d_ws;
+        a.ws_ml = c->d_ws + n_part * 128;
+        a.counters = c->d_cnt;
+        a.out = out;
+        return run_kernel(c, GQA_KERNEL_DECODE_SPLIT, st, "decode kernel",
+                          [&] { return launch_decode_split(pv, a, st); });
     }
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
@@ -871,7 +902,8 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[GQA_STATIC_SCRATCH_BYTES];
 
-constexpr size_t kStaticDescBytes = 1u << 20;      // descriptors; the rest holds partials
+constexpr size_t kStaticDescBytes = 1u << 20;      // descriptors
+constexpr size_t kStaticCntBytes = 64u << 10;       // merge counters; the rest holds partials
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 char *g_static_addr[kMaxDevices] = {};
@@ -932,7 +964,10 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
 
     // Same chunk rule as attn_decode, widened (up to 512 tokens) until the
     // partials fit in the static array.
-    const size_t part_cap = (GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes) / sizeof(float);
+    const size_t part_cap = (GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes) / sizeof(float);
+    if ((size_t)B * H_kv * sizeof(int32_t) > kStaticCntBytes)
+        return fail(GQA_ERANGE, "B * H_kv = %lld merge counters exceed the static scratch's %zu",
+                    (long long)B * H_kv, kStaticCntBytes / sizeof(int32_t));
     int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
     int chunk = (int)std::min<int64_t>(512, std::max<int64_t>(128, (target + 127) / 128 * 128));
     size_t n_items = 0;
@@ -976,18 +1011,28 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "descriptor upload (static scratch)");
-    float *ws_o = (float *)(scratch + kStaticDescBytes);
-    float *ws_ml = ws_o + n_part * 128;
+    // The merge counters must start at zero: clear the ones this call uses.
+    int32_t *counters = (int32_t *)(scratch + kStaticDescBytes);
+    e = cudaMemsetAsync(counters, 0, (size_t)B * H_kv * sizeof(int32_t), st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "counter clear (static scratch)");
+    DecodeLaunch a;
+    a.seqs = (const SeqDesc *)(scratch + o_sds);
+    a.items = (const DecodeItem *)(scratch + o_items);
+    a.item_start = (const int32_t *)(scratch + o_start);
+    a.n_items = (int)items.size();
+    a.chunk = chunk;
+    a.H_q = H_q;
+    a.q = q;
+    a.ws_o = (float *)(scratch + kStaticDescBytes + kStaticCntBytes);
+    a.ws_ml = a.ws_o + n_part * 128;
+    a.counters = counters;
+    a.out = out;
     const PoolView pv = c->view();
-    e = launch_decode_split(pv, (const SeqDesc *)(scratch + o_sds), (const DecodeItem *)(scratch + o_items),
-                            (int)items.size(), chunk, H_q, q, ws_o, ws_ml, st);
+    e = launch_decode_split(pv, a, st);
     if (e != cudaSuccess)
-        return cuda_fail(e, "decode split kernel (static scratch)");
+        return cuda_fail(e, "decode kernel (static scratch)");
     c->launches[GQA_KERNEL_DECODE_SPLIT] += 1;
-    e = launch_decode_combine((const int32_t *)(scratch + o_start), B, H_q, H_kv, ws_o, ws_ml, out, st);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode combine kernel (static scratch)");
-    c->launches[GQA_KERNEL_DECODE_COMBINE] += 1;
     return GQA_OK;
 }
 

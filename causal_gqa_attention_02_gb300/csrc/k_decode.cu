@@ -23,9 +23,9 @@
 //  * V pass: the same lane layout; each lane accumulates its 8 columns over
 //    its half-warp's tokens with probabilities broadcast from shared memory,
 //    then the half-warps and the warps are summed;
-//  * partials (max, sum, unnormalised o[g][128]) go to a workspace; the
-//    combine kernel merges a sequence's chunks in a fixed order:
-//        M = max_s m_s,  out = sum_s 2^(m_s-M) o_s / sum_s 2^(m_s-M) l_s.
+//  * partials (max, sum, unnormalised o[g][128]) go to a workspace; the last
+//    CTA of a (sequence, KV head) to finish merges its chunks in a fixed
+//    order: M = max_s m_s, out = sum_s 2^(m_s-M) o_s / sum_s 2^(m_s-M) l_s.
 // Scores are carried in log2 units (q pre-scaled by log2(e)/sqrt(128)) so
 // every exponential is one ex2.
 #include <cuda_bf16.h>
@@ -84,8 +84,9 @@ __device__ __forceinline__ float2 bf2(uint32_t x) { return make_float2(bf_lo(x),
 template <int G>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeItem *__restrict__ items,
-                    int chunk, int H_q, const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o,
-                    float *__restrict__ ws_ml)
+                    const int32_t *__restrict__ item_start, int chunk, int H_q,
+                    const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o, float *__restrict__ ws_ml,
+                    int32_t *__restrict__ counters, __nv_bfloat16 *__restrict__ out)
 {
     __shared__ __align__(16) float sc[kMaxChunk][G];     // scores, then probabilities (token-major)
     __shared__ __align__(16) float red[kWarps][G][D];
@@ -260,51 +261,87 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     }
     __syncthreads();
 
+    // ---- merge the chunks ----------------------------------------------------
+    // A single chunk is the whole sequence: write out directly.  Otherwise
+    // each CTA leaves its partial (max, sum, o) in the workspace and bumps the
+    // (entry, KV head) counter; the CTA that arrives last merges all chunks in
+    // chunk order -- M = max m_s, out = sum 2^(m_s-M) o_s / sum 2^(m_s-M) l_s --
+    // and resets the counter for the next call.  No CTA waits on another.
+    const int i0 = item_start[it.b];
+    const int ns = item_start[it.b + 1] - i0;
+    const int e = threadIdx.x;                         // one output column per thread (128 = d_h)
+    if (ns == 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float acc = red[0][h][e];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w)
+                acc += red[w][h][e];
+            out[((size_t)it.b * H_q + kvh * G + h) * D + e] = __float2bfloat16_rn(acc / ml[h][1]);
+        }
+        return;
+    }
     float *wo = ws_o + ((size_t)blockIdx.x * H_kv + kvh) * G * D;
-    for (int idx = threadIdx.x; idx < G * D; idx += kWarps * 32) {
-        const int h = idx / D, e = idx % D;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
         float acc = red[0][h][e];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w)
             acc += red[w][h][e];
-        wo[idx] = acc;
+        wo[h * D + e] = acc;
     }
     if (threadIdx.x < G) {
         float *wm = ws_ml + (((size_t)blockIdx.x * H_kv + kvh) * G + threadIdx.x) * 2;
         wm[0] = ml[threadIdx.x][0];
         wm[1] = ml[threadIdx.x][1];
     }
-}
-
-// One CTA per (query head, batch entry); thread e owns output element e.
-__global__ void __launch_bounds__(D)
-decode_combine_kernel(const int32_t *__restrict__ item_start, int H_q, int H_kv,
-                      const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
-                      __nv_bfloat16 *__restrict__ out)
-{
-    const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;
-    const int G = H_q / H_kv, kvh = h / G, hh = h % G;
-    const int i0 = item_start[b], i1 = item_start[b + 1];
-    float M = -INFINITY;
-    for (int i = i0; i < i1; ++i)
-        M = fmaxf(M, ws_ml[(((size_t)i * H_kv + kvh) * G + hh) * 2]);
-    float den = 0.0f, acc = 0.0f;
-    for (int i = i0; i < i1; ++i) {
-        const float *m = ws_ml + (((size_t)i * H_kv + kvh) * G + hh) * 2;
-        const float w = ex2(m[0] - M);
-        den = fmaf(w, m[1], den);
-        acc = fmaf(w, ws_o[(((size_t)i * H_kv + kvh) * G + hh) * D + e], acc);
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&counters[(size_t)it.b * H_kv + kvh], 1);
+        s_last = prev == ns - 1;
     }
-    out[((size_t)b * H_q + h) * D + e] = __float2bfloat16_rn(acc / den);
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    const size_t stride = (size_t)H_kv * G;            // between consecutive chunks' partials
+#pragma unroll 1
+    for (int h = 0; h < G; ++h) {
+        const float *mlh = ws_ml + (((size_t)i0 * H_kv + kvh) * G + h) * 2;
+        const float *poh = ws_o + (((size_t)i0 * H_kv + kvh) * G + h) * D + e;
+        float M = -INFINITY;
+        for (int i = 0; i < ns; ++i)
+            M = fmaxf(M, __ldcg(mlh + i * stride * 2));
+        float den = 0.f, a0 = 0.f, a1 = 0.f;
+        int i = 0;
+        for (; i + 2 <= ns; i += 2) {
+            const float w0 = ex2(__ldcg(mlh + i * stride * 2) - M);
+            const float w1 = ex2(__ldcg(mlh + (i + 1) * stride * 2) - M);
+            den = fmaf(w0, __ldcg(mlh + i * stride * 2 + 1), den);
+            den = fmaf(w1, __ldcg(mlh + (i + 1) * stride * 2 + 1), den);
+            a0 = fmaf(w0, __ldcg(poh + (size_t)i * stride * D), a0);
+            a1 = fmaf(w1, __ldcg(poh + (size_t)(i + 1) * stride * D), a1);
+        }
+        if (i < ns) {
+            const float w0 = ex2(__ldcg(mlh + i * stride * 2) - M);
+            den = fmaf(w0, __ldcg(mlh + i * stride * 2 + 1), den);
+            a0 = fmaf(w0, __ldcg(poh + (size_t)i * stride * D), a0);
+        }
+        out[((size_t)it.b * H_q + kvh * G + h) * D + e] = __float2bfloat16_rn((a0 + a1) / den);
+    }
+    if (threadIdx.x == 0)
+        counters[(size_t)it.b * H_kv + kvh] = 0;
 }
 
 template <int G>
-cudaError_t launch_g(const PoolView &pv, const SeqDesc *d_seqs, const DecodeItem *d_items, int n_items,
-                     int chunk, int H_q, const void *q, float *ws_o, float *ws_ml, cudaStream_t st)
+cudaError_t launch_g(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st)
 {
-    dim3 grid((unsigned)n_items, (unsigned)pv.H_kv);
-    decode_split_kernel<G><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, d_items, chunk, H_q,
-                                                        (const __nv_bfloat16 *)q, ws_o, ws_ml);
+    dim3 grid((unsigned)a.n_items, (unsigned)pv.H_kv);
+    decode_split_kernel<G><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q,
+                                                        (const __nv_bfloat16 *)a.q, a.ws_o, a.ws_ml, a.counters,
+                                                        (__nv_bfloat16 *)a.out);
     return cudaGetLastError();
 }
 
@@ -312,36 +349,23 @@ cudaError_t launch_g(const PoolView &pv, const SeqDesc *d_seqs, const DecodeItem
 
 bool decode_split_supported(int group) { return group >= 1 && group <= 8; }
 
-cudaError_t launch_decode_split(const PoolView &pv, const SeqDesc *d_seqs, const DecodeItem *d_items,
-                                int n_items, int chunk, int H_q, const void *q, float *ws_o,
-                                float *ws_ml, cudaStream_t st)
+cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st)
 {
-    if (pv.d != D || chunk <= 0 || chunk > kMaxChunk || chunk % kPageTokens != 0)
+    if (pv.d != D || a.chunk <= 0 || a.chunk > kMaxChunk || a.chunk % kPageTokens != 0)
         return cudaErrorInvalidValue;
-    if (n_items <= 0)
+    if (a.n_items <= 0)
         return cudaSuccess;
-    switch (H_q / pv.H_kv) {
-    case 1: return launch_g<1>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 2: return launch_g<2>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 3: return launch_g<3>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 4: return launch_g<4>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 5: return launch_g<5>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 6: return launch_g<6>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 7: return launch_g<7>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
-    case 8: return launch_g<8>(pv, d_seqs, d_items, n_items, chunk, H_q, q, ws_o, ws_ml, st);
+    switch (a.H_q / pv.H_kv) {
+    case 1: return launch_g<1>(pv, a, st);
+    case 2: return launch_g<2>(pv, a, st);
+    case 3: return launch_g<3>(pv, a, st);
+    case 4: return launch_g<4>(pv, a, st);
+    case 5: return launch_g<5>(pv, a, st);
+    case 6: return launch_g<6>(pv, a, st);
+    case 7: return launch_g<7>(pv, a, st);
+    case 8: return launch_g<8>(pv, a, st);
     default: return cudaErrorNotSupported;
     }
-}
-
-cudaError_t launch_decode_combine(const int32_t *d_item_start, int B, int H_q, int H_kv,
-                                  const float *ws_o, const float *ws_ml, void *out, cudaStream_t st)
-{
-    if (B <= 0)
-        return cudaSuccess;
-    dim3 grid((unsigned)H_q, (unsigned)B);
-    decode_combine_kernel<<<grid, D, 0, st>>>(d_item_start, H_q, H_kv, ws_o, ws_ml,
-                                              (__nv_bfloat16 *)out);
-    return cudaGetLastError();
 }
 
 }  // namespace gqa

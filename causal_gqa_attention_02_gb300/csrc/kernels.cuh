@@ -75,14 +75,24 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
 cudaError_t launch_attn_simt(const PoolView &pv, int dtype, const SeqDesc *d_seqs, int B, int n,
                              int H_q, const void *q, void *out, cudaStream_t st);
 
-// bf16, d = 128 split-K decode.  Returns cudaErrorNotSupported when the
-// group size H_q / H_kv has no instantiation.
+// bf16, d = 128 split-K decode with the merge done by the last CTA of each
+// (entry, KV head).  counters[B * H_kv] must be zero on entry; the kernel
+// leaves them zero.
+struct DecodeLaunch {
+    const SeqDesc *seqs;
+    const DecodeItem *items;
+    const int32_t *item_start;   // [B + 1]: items of entry b are item_start[b] .. item_start[b+1]-1
+    int n_items;
+    int chunk;
+    int H_q;
+    const void *q;
+    float *ws_o;
+    float *ws_ml;
+    int32_t *counters;
+    void *out;
+};
 bool decode_split_supported(int group);
-cudaError_t launch_decode_split(const PoolView &pv, const SeqDesc *d_seqs, const DecodeItem *d_items,
-                                int n_items, int chunk, int H_q, const void *q, float *ws_o,
-                                float *ws_ml, cudaStream_t st);
-cudaError_t launch_decode_combine(const int32_t *d_item_start, int B, int H_q, int H_kv,
-                                  const float *ws_o, const float *ws_ml, void *out, cudaStream_t st);
+cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st);
 
 // bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).  Rows of the
 // batch entries must already be in the cache (launch_cache_write first).

@@ -235,7 +235,7 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
  *      out[b, h, :] = sum_t softmax_t(<q[b,h], K[t, g(h)]>/sqrt(d_h)) V[t, g(h)].
  *  seq_ids  host int32[B], live sequences of length >= 1 (repeats allowed).
  *  q        device [B, H_q, d_h];  out  device [B, H_q, d_h].
- * Split-K partials live in a library-owned device workspace that grows with
+ * Split-K partials and merge counters live in library-owned device memory that grows with
  * cudaMalloc on first use of a larger shape.
  * Errors: GQA_EINVAL, GQA_EMASK (empty sequence), GQA_ECUDA. */
 int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
@@ -253,16 +253,17 @@ int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q
  * Arguments, results and errors are those of attn_decode.  The cache must be
  * bf16 with d_h = 128, and H_q / H_kv must be at most 8, because this call
  * runs only the split-K decode kernels.  Other shapes get GQA_EINVAL.
- * The split-K partials and the per-call descriptors live in one static
- * device array of GQA_STATIC_SCRATCH_BYTES.  The library reserves that array
+ * The split-K partials, the per-call descriptors and the merge counters live
+ * in one static device array of GQA_STATIC_SCRATCH_BYTES.  The library reserves that array
  * on every GPU that loads it, until the process exits.  A call whose partials
  * or descriptors would not fit returns GQA_ERANGE with the bytes it needed.
  * No cudaMalloc, cudaFree or other allocating routine is called.
  * On each device, the first call looks up the array's device address
  * (cudaGetSymbolAddress).  Make that first call before any stream capture.
  * Every call shares the one array, and the array keeps the last call's
- * contents.  Each call writes every part of the array it reads before
- * reading it, so nothing needs clearing.  Calls whose GPU work overlaps race
+ * contents.  The merge counters must start at zero, so each call clears the
+ * ones it uses (an asynchronous memset on `stream`); every other part is
+ * written by the call before it is read.  Calls whose GPU work overlaps race
  * on the array: calls on different streams, or on different caches of one
  * device.  Order such calls yourself. */
 #define GQA_STATIC_SCRATCH_BYTES (16u << 20)
@@ -288,8 +289,8 @@ int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
 #define GQA_KERNEL_COW_COPY        1  /* copy-on-write of a shared tail page      */
 #define GQA_KERNEL_PREFILL_TC      2  /* tensor-core causal prefill (bf16, 128)   */
 #define GQA_KERNEL_ATTN_SIMT       3  /* CUDA-core attention (fp32 / other d_h)   */
-#define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode partials (bf16, 128)      */
-#define GQA_KERNEL_DECODE_COMBINE  5  /* split-K combine                          */
+#define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode (bf16, 128), merge included */
+#define GQA_KERNEL_DECODE_COMBINE  5  /* reserved: the merge runs inside the split kernel */
 #define GQA_KERNEL_COUNT           6
 
 /* Turn per-launch timing on or off.  While on, every kernel launch of this
