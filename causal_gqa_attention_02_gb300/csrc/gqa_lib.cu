@@ -34,6 +34,10 @@ namespace {
 
 thread_local std::string t_err;
 
+// Fixed cost of one prefill work item (Q load, pipeline refill, epilogue)
+// in quarters of a key tile, for balancing items over the persistent grid.
+constexpr int64_t kItemCostQuarters = 2;
+
 int fail(int code, const char *fmt, ...)
 {
     char buf[512];
@@ -671,6 +675,7 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     const bool use_tc = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
                         prefill_tc_supported(G, c->desc.num_kv_heads);
     std::vector<TcItem> items;
+    std::vector<int32_t> item_start;
     int tc_grid = 1;
     if (use_tc) {
         // Two query tiles of 128/G positions per CTA; heaviest items first so
@@ -683,17 +688,39 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
                 for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
                     items.push_back(TcItem{b, h, i0, nt});
             }
+        // Longest-processing-time-first: items in decreasing cost, each to the
+        // CTA with the least work so far; a CTA then runs its items in that
+        // order.  Cost of an item ~ its key tiles plus a fixed per-item share
+        // (Q load, pipeline refill, epilogue), in quarter-tile units.
         std::stable_sort(items.begin(), items.end(), [](const TcItem &x, const TcItem &y) { return x.nt > y.nt; });
-        // The persistent grid deals items round-robin (CTA c takes c, c + grid,
-        // ...); reverse every other round so each CTA's share stays even.
         tc_grid = std::max(1, std::min<int>(c->num_sms, (int)items.size()));
-        for (size_t r0 = tc_grid; r0 < items.size(); r0 += 2 * (size_t)tc_grid)
-            std::reverse(items.begin() + r0, items.begin() + std::min(items.size(), r0 + tc_grid));
+        std::vector<std::vector<int>> runs(tc_grid);
+        using Load = std::pair<int64_t, int>;
+        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+        for (int i = 0; i < tc_grid; ++i)
+            heap.push({0, i});
+        for (size_t i = 0; i < items.size(); ++i) {
+            Load top = heap.top();
+            heap.pop();
+            runs[top.second].push_back((int)i);
+            top.first += 4 * (int64_t)items[i].nt + kItemCostQuarters;
+            heap.push(top);
+        }
+        std::vector<TcItem> sorted;
+        sorted.reserve(items.size());
+        item_start.assign(1, 0);
+        for (const auto &run : runs) {
+            for (int i : run)
+                sorted.push_back(items[i]);
+            item_start.push_back((int32_t)sorted.size());
+        }
+        items.swap(sorted);
     }
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
     const size_t o_cow = stg.add(cows.data(), cows.size());
     const size_t o_items = stg.add(items.data(), items.size());
+    const size_t o_start = stg.add(item_start.data(), item_start.size());
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     const PoolView pv = c->view();
@@ -714,8 +741,8 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
         return rc;
     if (use_tc) {
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&] {
-            return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items), (int)items.size(), B, n,
-                                     H_q, q, out, tc_grid, st);
+            return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items),
+                                     (const int32_t *)(c->d_stage + o_start), tc_grid, B, n, H_q, q, out, st);
         });
     }
     return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {

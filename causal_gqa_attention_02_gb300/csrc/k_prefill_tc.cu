@@ -28,9 +28,10 @@
 //    K and V released separately); warp 1 owns TMEM and issues the MMAs;
 //    warpgroups 1 and 2 (warps 4-7, 8-11) run the softmax, one per query
 //    tile, thread = row.
-//  * Persistent: one CTA per SM walks a host-ordered item list; the MMA
-//    stream runs on across items so the next item's first S = Q K^T is
-//    issued right after the current item's last PV.
+//  * Persistent: one CTA per SM walks its own run of items, assigned on the
+//    host longest-first to the least-loaded CTA; the MMA stream runs on
+//    across items so the next item's first S = Q K^T is issued right after
+//    the current item's last PV.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  S = Q K^T
 //    is computed into TMEM; the softmax warps read their row, write
 //    P = exp2(S*c - m) back as bf16 over the first 64 columns of S, and the
@@ -38,9 +39,10 @@
 //  * Online softmax (the FlashAttention recurrence): a running row max m and
 //    sum l; O is rescaled in TMEM only when the max grows by more than 2^8,
 //    otherwise the stale max stays the reference (exact in real arithmetic).
-//  * Epilogue: O / l in fp32 -> bf16, staged in shared memory over the
-//    query tile and written with one TMA store per 64-column half; padding
-//    rows are written as zeros.
+//  * Epilogue: O / l in fp32 -> bf16, staged per 64-column half in a 16 KB
+//    shared-memory buffer per query tile (128-byte swizzle, so the row-per-
+//    thread writes are conflict-free) and written by one TMA store per half;
+//    padding rows of the tile are written as zeros.
 // Every wait is bounded; on a timeout the CTA raises GQA_DEVERR_TIMEOUT,
 // drains what it has in flight (bounded) and exits cleanly.
 #include <cuda.h>
@@ -68,25 +70,38 @@ namespace {
 constexpr int kPolyEvery = GQA_EXP2_POLY_EVERY > 0 ? GQA_EXP2_POLY_EVERY : 1;
 constexpr bool kPoly = GQA_EXP2_POLY_EVERY > 0;
 constexpr int D = 128;
-constexpr int kStages = 2;
+// K and V have pipelines of their own: a V stage is held from PV of the
+// first query tile to the end of PV of the second, so V wants one stage more
+// than K to hide the load latency (about 2 us under full load).
+#ifndef GQA_K_STAGES
+#define GQA_K_STAGES 2
+#endif
+#ifndef GQA_V_STAGES
+#define GQA_V_STAGES 2
+#endif
+constexpr int kKStages = GQA_K_STAGES;
+constexpr int kVStages = GQA_V_STAGES;
 constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 q[2][2][128 * 64];                   // [query tile][column half]
-    __nv_bfloat16 k[kStages][2][128 * 64];
-    __nv_bfloat16 v[kStages][2][128 * 64];
+    __nv_bfloat16 k[kKStages][2][128 * 64];
+    __nv_bfloat16 v[kVStages][2][128 * 64];
+    __nv_bfloat16 o[2][128 * 64];                      // epilogue staging, one column half per query tile
     uint64_t bar_q, q_empty;
-    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+    uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_full[2], fin;
     uint32_t tmem;
     int abort_;
 };
 
+static_assert(sizeof(TcSmem) + 1024 <= 227 * 1024, "shared memory per CTA");
+
 struct TcParams {
     const SeqDesc *seqs;
-    const TcItem *items;
-    int32_t n_items;
+    const TcItem *items;      // grouped by CTA: CTA c takes items[item_start[c] .. item_start[c + 1])
+    const int32_t *item_start;
     const int32_t *tables;
     int32_t stride;
     int32_t num_pages;
@@ -106,15 +121,18 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
     atomicOr(err, bit);
 }
 
-// Persistent: CTA c takes items c, c + gridDim.x, ...  Barrier phases run on
+// Persistent: CTA c takes the host-assigned run of items item_start[c] ..
+// item_start[c + 1] - 1 in order.  Barrier phases run on
 // across items (global tile counter gt), so the next item's Q and first K/V
 // tile load while the current item's last tiles and epilogue run.
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV, const TcParams p)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
+                  const __grid_constant__ CUtensorMap mO, const TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem &s = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i_begin = p.item_start[blockIdx.x], i_end = p.item_start[blockIdx.x + 1];
 
     if (warp == 1) {
         tmem_alloc(&s.tmem, 512);
@@ -135,10 +153,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         s.abort_ = 0;
         mbar_init(&s.bar_q, 1);
         mbar_init(&s.q_empty, 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&s.k_full[i], 1);
-            mbar_init(&s.v_full[i], 1);
             mbar_init(&s.k_empty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&s.v_full[i], 1);
             mbar_init(&s.v_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -164,10 +184,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             int k = 0, q_issued = 0, v_missing = 0;
             bool ok = true;
             // Loads one K/V tile (8 pages, one 16-token box per page and
-            // column half) into stage gt % kStages once its last reader is done.
+            // column half) into stages gt % kKStages and gt % kVStages once
+            // their last readers are done.
             auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
-                const int st = gt % kStages;
-                const uint32_t use = gt / kStages;
+                const int st = gt % kKStages, sv = gt % kVStages;
+                const uint32_t use = gt / kKStages, vuse = gt / kVStages;
                 const int32_t *tab = p.tables + (size_t)sd.row * p.stride;
                 const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
                 int page[8];
@@ -192,29 +213,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     for (int c = 0; c < 2; ++c)
                         tma_load_4d(&mKV, &s.k_full[st], s.k[st][c] + pg * 16 * 64, 64 * c, 0, it.kvh, page[pg]);
                 ++gt;                                     // K of this tile is in flight from here on
-                if (use > 0 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_)) {
+                if (vuse > 0 && !mbar_wait(&s.v_empty[sv], (vuse - 1) & 1, &s.abort_)) {
                     ++v_missing;
                     return false;
                 }
-                mbar_arrive_expect_tx(&s.v_full[st], 2 * kTileBytes);
+                mbar_arrive_expect_tx(&s.v_full[sv], 2 * kTileBytes);
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg)
                     for (int c = 0; c < 2; ++c)
-                        tma_load_4d(&mKV, &s.v_full[st], s.v[st][c] + pg * 16 * 64, 64 * c, 0, p.H_kv + it.kvh,
+                        tma_load_4d(&mKV, &s.v_full[sv], s.v[sv][c] + pg * 16 * 64, 64 * c, 0, p.H_kv + it.kvh,
                                     page[pg]);
                 return true;
             };
             // The first item's Q load is issued before the K/V loop.
             bool first_q_issued = false;
-            if (blockIdx.x < p.n_items) {
-                const TcItem it = p.items[blockIdx.x];
+            if (i_begin < i_end) {
+                const TcItem it = p.items[i_begin];
                 mbar_arrive_expect_tx(&s.bar_q, q_bytes);
                 for (int t = 0; t < 2; ++t)
                     for (int c = 0; c < 2; ++c)
                         tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
                 first_q_issued = true;
             }
-            for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
+            for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
                 const TcItem it = p.items[idx];
                 const SeqDesc sd = p.seqs[it.b];
                 // The first K/V tile only needs a free stage; issue it before
@@ -245,15 +266,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 abort_with(s, p.err, kErrTimeout);
             // Drain: every issued copy lands before the CTA exits.
             int never = 0;
-            for (uint32_t g = (gt > kStages ? gt - kStages : 0); g < gt; ++g) {
-                const int st = g % kStages;
-                if (!mbar_wait(&s.k_full[st], (g / kStages) & 1, &never))
+            for (uint32_t g = (gt > kKStages ? gt - kKStages : 0); g < gt; ++g) {
+                if (!mbar_wait(&s.k_full[g % kKStages], (g / kKStages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
             const uint32_t v_done = gt - v_missing;
-            for (uint32_t g = (v_done > kStages ? v_done - kStages : 0); g < v_done; ++g) {
-                const int st = g % kStages;
-                if (!mbar_wait(&s.v_full[st], (g / kStages) & 1, &never))
+            for (uint32_t g = (v_done > kVStages ? v_done - kVStages : 0); g < v_done; ++g) {
+                if (!mbar_wait(&s.v_full[g % kVStages], (g / kVStages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
             if (first_q_issued && q_issued == 0)
@@ -284,8 +303,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             // One flat stream of key tiles over this CTA's items: tile g is
             // tile j of item k; S of the next tile (of this item or the next
             // one) is issued right after the PV that frees its TMEM columns.
-            int idx = blockIdx.x, k = 0, j = 0;
-            int nt = idx < p.n_items ? p.items[idx].nt : 0;
+            int idx = i_begin, k = 0, j = 0;
+            int nt = idx < i_end ? p.items[idx].nt : 0;
             uint32_t g = 0;
             bool ok = nt > 0 && mbar_wait(&s.bar_q, 0, &s.abort_) && mbar_wait(&s.k_full[0], 0, &s.abort_);
             if (ok) {
@@ -299,23 +318,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     mma_commit(&s.q_empty);
             }
             while (ok) {
-                const int st = g % kStages, st2 = (g + 1) % kStages;
+                const int sv = g % kVStages, st2 = (g + 1) % kKStages;
                 const bool last_of_item = j + 1 == nt;
-                const int next_idx = last_of_item ? idx + (int)gridDim.x : idx;
-                const bool has_next = next_idx < p.n_items;
+                const int next_idx = last_of_item ? idx + 1 : idx;
+                const bool has_next = next_idx < i_end;
                 const int next_nt = has_next ? (last_of_item ? p.items[next_idx].nt : nt) : 0;
                 const int next_j = last_of_item ? 0 : j + 1;
                 ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
-                     mbar_wait(&s.v_full[st], (g / kStages) & 1, &s.abort_);
+                     mbar_wait(&s.v_full[sv], (g / kVStages) & 1, &s.abort_);
                 if (!ok)
                     break;
                 tc_fence_after();
-                issue_o(0, st, j > 0);
+                issue_o(0, sv, j > 0);
                 if (last_of_item)
                     mma_commit(&s.o_full[0]);
                 if (has_next) {
                     ok = (!last_of_item || mbar_wait(&s.bar_q, (k + 1) & 1, &s.abort_)) &&
-                         mbar_wait(&s.k_full[st2], ((g + 1) / kStages) & 1, &s.abort_);
+                         mbar_wait(&s.k_full[st2], ((g + 1) / kKStages) & 1, &s.abort_);
                     if (!ok)
                         break;
                     tc_fence_after();
@@ -326,8 +345,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 if (!ok)
                     break;
                 tc_fence_after();
-                issue_o(1, st, j > 0);
-                mma_commit(&s.v_empty[st]);
+                issue_o(1, sv, j > 0);
+                mma_commit(&s.v_empty[sv]);
                 if (last_of_item)
                     mma_commit(&s.o_full[1]);
                 if (!has_next)
@@ -365,7 +384,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         uint32_t gt = 0;
         int k = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++k) {
+        for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
             const TcItem it = p.items[idx];
             const SeqDesc sd = p.seqs[it.b];
             const int nt = it.nt;
@@ -459,29 +478,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             if (!ok)
                 break;
-            // ---- epilogue: O / l -> bf16 -> the row of out, straight from registers.
-            // Padding rows were zeroed by the host; rows outside the tensor are skipped.
-            if (!mbar_wait(&s.o_full[t], k & 1, &s.abort_)) {
+            // ---- epilogue: O / l -> bf16, staged one 64-column half at a time in
+            // shared memory (128-byte swizzle, the layout of the tensor map) and
+            // written by one TMA store per half.  Rows past the valid length
+            // are written as zeros; positions past n are clipped by the store.
+            // The named barriers below need every thread of the warpgroup, so
+            // a timeout is agreed on by all of them before anyone leaves.
+            if (named_bar_any(1 + t, 128, !mbar_wait(&s.o_full[t], k & 1, &s.abort_))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            __nv_bfloat16 *orow = p.out + (((size_t)it.b * p.n + rel) * p.H_q + it.kvh * p.G + r % p.G) * D;
+            unsigned char *stage = reinterpret_cast<unsigned char *>(s.o[t]) + r * 128;
 #pragma unroll 1
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t u[32];
-                __syncwarp();                            // the stores below diverge on `valid`
-                tmem_ld32(tO + 32 * q4, u);
-                uint32_t pk[16];
+            for (int h = 0; h < 2; ++h) {
+                uint32_t u0[32], u1[32];
+                __syncwarp();
+                tmem_ld32(tO + 64 * h, u0);
+                tmem_ld32(tO + 64 * h + 32, u1);
+                if (r == 0)
+                    tma_store_wait_read();               // the previous store has left the buffer
+                named_bar_sync(1 + t, 128);
+                if (row_in_box) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * q4);
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4)
-                        dst[k4] = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint32_t *u = cc < 4 ? u0 + 8 * cc : u1 + 8 * (cc - 4);
+                        uint4 v4;
+                        v4.x = pack_bf16x2(__uint_as_float(u[0]) * inv_l, __uint_as_float(u[1]) * inv_l);
+                        v4.y = pack_bf16x2(__uint_as_float(u[2]) * inv_l, __uint_as_float(u[3]) * inv_l);
+                        v4.z = pack_bf16x2(__uint_as_float(u[4]) * inv_l, __uint_as_float(u[5]) * inv_l);
+                        v4.w = pack_bf16x2(__uint_as_float(u[6]) * inv_l, __uint_as_float(u[7]) * inv_l);
+                        if (!valid)                      // padding row: zeros, whatever O holds
+                            v4 = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(stage + ((cc ^ (r & 7)) << 4)) = v4;
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + t, 128);
+                if (r == 0 && it.i0 + t * p.rows_pos < p.n) {
+                    tma_store_4d(&mO, s.o[t], 64 * h, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
+                    tma_store_commit();
                 }
             }
             tc_fence_before();
@@ -489,6 +526,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         }
         if (!ok)
             abort_with(s, p.err, kErrTimeout);
+        if (r == 0)
+            tma_store_wait_all();                       // every store has landed before the CTA exits
     }
 
     tc_fence_before();
@@ -531,16 +570,17 @@ bool prefill_tc_supported(int group, int H_kv) { return group >= 1 && group <= 1
 
 int prefill_tc_rows_per_tile(int group) { return 128 / group; }
 
-cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items, int n_items, int B,
-                              int n, int H_q, const void *q, void *out, int grid, cudaStream_t st)
+cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
+                              const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
+                              cudaStream_t st)
 {
-    if (pv.d != D || n_items <= 0)
-        return n_items <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    if (pv.d != D || grid <= 0)
+        return grid <= 0 ? cudaSuccess : cudaErrorInvalidValue;
     const int G = H_q / pv.H_kv;
     const int rows_pos = 128 / G;
     if (G < 1 || rows_pos < 1 || grid < 1)
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mkv;
+    CUtensorMap mq, mkv, mo;
     const cuuint64_t qdims[4] = {(cuuint64_t)D, (cuuint64_t)H_q, (cuuint64_t)n, (cuuint64_t)B};
     const cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H_q * D * 2, (cuuint64_t)n * H_q * D * 2};
     const cuuint32_t qbox[4] = {64, (cuuint32_t)G, (cuuint32_t)rows_pos, 1};
@@ -549,12 +589,14 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     const cuuint64_t kvstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageTokens * D * 2,
                                  (cuuint64_t)2 * pv.H_kv * kPageTokens * D * 2};
     const cuuint32_t kvbox[4] = {64, (cuuint32_t)kPageTokens, 1, 1};
-    if (!encode4(&mq, q, qdims, qstr, qbox) || !encode4(&mkv, pv.pool, kvdims, kvstr, kvbox))
+    // out has the shape and layout of q: the same box serves the stores.
+    if (!encode4(&mq, q, qdims, qstr, qbox) || !encode4(&mkv, pv.pool, kvdims, kvstr, kvbox) ||
+        !encode4(&mo, out, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     TcParams prm;
     prm.seqs = d_seqs;
     prm.items = d_items;
-    prm.n_items = n_items;
+    prm.item_start = d_item_start;
     prm.tables = pv.tables;
     prm.stride = pv.stride;
     prm.num_pages = pv.num_pages;
@@ -574,7 +616,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
             return e;
         attr_set = true;
     }
-    prefill_tc_kernel<<<std::min(grid, n_items), kThreads, smem, st>>>(mq, mkv, prm);
+    prefill_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
     return cudaGetLastError();
 }
 

@@ -98,10 +98,12 @@ cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaS
 // batch entries must already be in the cache (launch_cache_write first).
 bool prefill_tc_supported(int group, int H_kv);
 int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
-// Persistent grid of `grid` CTAs; CTA c takes items c, c + grid, ... (the
-// host orders the list so that this deals work evenly).  Padding rows of
-// `out` must be zeroed by the caller; the kernel writes valid rows only.
-cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items, int n_items, int B,
-                              int n, int H_q, const void *q, void *out, int grid, cudaStream_t st);
+// Persistent grid of `grid` CTAs; CTA c takes items[item_start[c] ..
+// item_start[c + 1]) in order (grid + 1 offsets, every run non-empty).  Rows
+// of the items' query tiles past the valid length are written as zeros;
+// padding rows that no item covers must be zeroed by the caller.
+cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
+                              const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
+                              cudaStream_t st);
 
 }  // namespace gqa

@@ -65,20 +65,53 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Probe that may suspend the thread until the phase completes or about
+// kTrySuspendNs have passed, whichever comes first (mbarrier.try_wait with a
+// suspend-time hint), so a waiter wakes as soon as the phase flips.
+constexpr uint32_t kTrySuspendNs = 1000;
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kTrySuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// How a wait polls: 0 = test_wait with a short sleep between probes,
+// 1 = try_wait (suspends, wakes on the phase flip), 2 = test_wait spin.
+#ifndef GQA_WAIT_MODE
+#define GQA_WAIT_MODE 1
+#endif
+
 // Wait until the barrier phase of the given parity has completed.  Returns
-// false once *abort is non-zero or the wait has lasted kWaitTimeoutNs.  The
-// probe never suspends the thread (test_wait, not try_wait), so the bound
-// holds whatever the hardware's suspension policy is; a short sleep between
-// probes keeps a waiting warp from taking issue slots from working ones.
+// false once *abort is non-zero or the wait has lasted kWaitTimeoutNs.  Every
+// probe returns within a bounded time (test_wait at once, try_wait within
+// its suspend-time hint), so the bound holds.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
 {
     if (mbar_test(bar, parity))
         return true;
     const uint64_t t0 = globaltimer();
+#if GQA_WAIT_MODE == 1
+    for (;;) {
+        if (mbar_try(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer() - t0 > kWaitTimeoutNs)
+            return false;
+    }
+#else
     for (uint32_t it = 1;; ++it) {
         if (mbar_test(bar, parity))
             return true;
-        if (it > 16)
+        if (GQA_WAIT_MODE == 0 && it > 16)
             __nanosleep(32);
         if ((it & 63) == 0) {
             if (*abort)
@@ -87,6 +120,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
                 return false;
         }
     }
+#endif
 }
 
 // ---- TMA (cp.async.bulk.tensor) ------------------------------------------------
@@ -128,6 +162,9 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 
 // Wait until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until every committed bulk store has completed (writes performed).
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) reads.
@@ -353,6 +390,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread learns whether any of them passed `pred`.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t threads, bool pred)
+{
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return any != 0;
 }
 
 }  // namespace sm100
