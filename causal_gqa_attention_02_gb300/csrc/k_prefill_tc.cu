@@ -25,17 +25,22 @@
 //    element.
 //  * Warp roles: warp 0 issues TMA (Q once per item; K and V per key tile,
 //    one 16-token page box at a time through the block table, two stages,
-//    K and V released separately); warp 1 owns TMEM and issues the MMAs;
+//    K and V released separately); warp 1 owns TMEM and issues the S MMAs,
+//    warp 2 the PV MMAs;
 //    warpgroups 1 and 2 (warps 4-7, 8-11) run the softmax, one per query
 //    tile, thread = row.
 //  * Persistent: one CTA per SM walks its own run of items, assigned on the
-//    host longest-first to the least-loaded CTA; the MMA stream runs on
-//    across items so the next item's first S = Q K^T is issued right after
-//    the current item's last PV.
-//  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  S = Q K^T
-//    is computed into TMEM; the softmax warps read their row, write
-//    P = exp2(S*c - m) back as bf16 over the first 64 columns of S, and the
-//    PV MMA takes P straight from TMEM as its A operand: O += P V.
+//    host longest-first to the least-loaded CTA; both MMA streams run on
+//    across items, so the next item's first S = Q K^T is issued as soon as
+//    its Q and K have landed and the S buffer is free.
+//  * TMEM (512 columns): S | P0 | P1 | O0 | O1.  S = Q K^T (fp32, 128
+//    columns) is computed into a buffer the two query tiles take in turn;
+//    the softmax warps read their row of it and release it at once, then
+//    write P = exp2(S*c - m) as bf16 into their tile's P columns, and the
+//    PV MMA takes P straight from TMEM as its A operand: O += P V.  The S
+//    MMAs (one issuing warp) and the PV MMAs (another) form two independent
+//    streams; a softmax has about four MMA groups of time before its PV is
+//    due.
 //  * Online softmax (the FlashAttention recurrence): a running row max m and
 //    sum l; O is rescaled in TMEM only when the max grows by more than 2^8,
 //    otherwise the stale max stays the reference (exact in real arithmetic).
@@ -83,6 +88,9 @@ constexpr int kKStages = GQA_K_STAGES;
 constexpr int kVStages = GQA_V_STAGES;
 constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
+// TMEM columns: one S buffer (fp32, 128 keys) shared by the two query tiles,
+// P of each tile (bf16 pairs, 64 columns) and O of each tile (fp32, 128).
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 q[2][2][128 * 64];                   // [query tile][column half]
@@ -91,7 +99,7 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 o[2][128 * 64];                      // epilogue staging, one column half per query tile
     uint64_t bar_q, q_empty;
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], p_full[2], o_full[2], fin;
+    uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
     int abort_;
 };
@@ -164,9 +172,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s.s_full[t], 1);
             mbar_init(&s.p_full[t], 4);
-            mbar_init(&s.o_full[t], 1);
+            mbar_init(&s.pv_done[t], 1);
         }
-        mbar_init(&s.fin, 1);
+        mbar_init(&s.s_free, 4);
+        mbar_init(&s.fin[0], 1);
+        mbar_init(&s.fin[1], 1);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -280,96 +290,98 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (q_issued > 0 && !mbar_wait(&s.bar_q, (q_issued - 1) & 1, &never))
                 atomicOr(p.err, kErrTimeout);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues every S = Q K^T, warp 2 every O += P V.  The two
+        // streams depend on each other only through the softmax warps, and
+        // a thread issuing MMAs spends most of its time stalled behind the
+        // tensor pipe: with both streams queued, one stream's waits and
+        // bookkeeping no longer leave the pipe idle.
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T: both K-major
             const uint32_t id_o = idesc_bf16(128, 128, 0, 1);   // O += P V: V is N-major
+            // Descriptors are built once; an MMA then costs two adds and the
+            // instruction itself.  Q tile t, K stage st and V stage sv start
+            // 2 * kTileBytes apart; a column half is kTileBytes further.
+            constexpr uint32_t kHalf = kTileBytes >> 4, kStage = 2 * kTileBytes >> 4;
+            const uint32_t hi_kmaj = desc_sw128_hi(1024);
+            const uint32_t q_lo = desc_sw128_lo(smem_u32(s.q[0][0]), 16);
+            const uint32_t k_lo = desc_sw128_lo(smem_u32(s.k[0][0]), 16);
+            const uint32_t v_lo = desc_sw128_lo(smem_u32(s.v[0][0]), kTileBytes);
             auto issue_s = [&](int t, int st) {
+                const uint32_t a0 = q_lo + t * kStage, b0 = k_lo + st * kStage;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t a = desc_sw128(smem_u32(s.q[t][ks / 4]) + (ks % 4) * 32, 16, 1024);
-                    const uint64_t b = desc_sw128(smem_u32(s.k[st][ks / 4]) + (ks % 4) * 32, 16, 1024);
-                    mma_ss(tm + 128 * t, a, b, id_s, ks > 0);
+                    const uint32_t off = (ks / 4) * kHalf + (ks % 4) * 2;   // 32 bytes per k-step
+                    mma_ss(tm + kColS, desc_join(a0 + off, hi_kmaj), desc_join(b0 + off, hi_kmaj), id_s, ks > 0);
                 }
             };
-            auto issue_o = [&](int t, int st, bool acc) {
+            auto issue_o = [&](int t, int sv, bool acc) {
+                const uint32_t b0 = v_lo + sv * kStage;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t b = desc_sw128(smem_u32(s.v[st][0]) + ks * 2048, kTileBytes, 1024);
-                    mma_ts(tm + 256 + 128 * t, tm + 128 * t + ks * 8, b, id_o, (acc || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < 8; ++ks)   // 16 keys = 2048 bytes of the N-major V tile per k-step
+                    mma_ts(tm + kColO + 128 * t, tm + kColP + 64 * t + ks * 8, desc_join(b0 + ks * 128, hi_kmaj), id_o,
+                           (acc || ks > 0) ? 1u : 0u);
             };
             // One flat stream of key tiles over this CTA's items: tile g is
-            // tile j of item k; S of the next tile (of this item or the next
-            // one) is issued right after the PV that frees its TMEM columns.
-            int idx = i_begin, k = 0, j = 0;
-            int nt = idx < i_end ? p.items[idx].nt : 0;
+            // tile j of item k.  The S buffer alternates S0(g), S1(g), S0(g+1),
+            // ...: each S waits until the softmax warps have read the one
+            // before it (s_free completions alternate between the two tiles).
+            bool ok = true;
             uint32_t g = 0;
-            bool ok = nt > 0 && mbar_wait(&s.bar_q, 0, &s.abort_) && mbar_wait(&s.k_full[0], 0, &s.abort_);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                mma_commit(&s.s_full[0]);
-                issue_s(1, 0);
-                mma_commit(&s.s_full[1]);
-                mma_commit(&s.k_empty[0]);
-                if (nt == 1)
-                    mma_commit(&s.q_empty);
-            }
-            while (ok) {
-                const int sv = g % kVStages, st2 = (g + 1) % kKStages;
-                const bool last_of_item = j + 1 == nt;
-                const int next_idx = last_of_item ? idx + 1 : idx;
-                const bool has_next = next_idx < i_end;
-                const int next_nt = has_next ? (last_of_item ? p.items[next_idx].nt : nt) : 0;
-                const int next_j = last_of_item ? 0 : j + 1;
-                ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
-                     mbar_wait(&s.v_full[sv], (g / kVStages) & 1, &s.abort_);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                issue_o(0, sv, j > 0);
-                if (last_of_item)
-                    mma_commit(&s.o_full[0]);
-                if (has_next) {
-                    ok = (!last_of_item || mbar_wait(&s.bar_q, (k + 1) & 1, &s.abort_)) &&
-                         mbar_wait(&s.k_full[st2], ((g + 1) / kKStages) & 1, &s.abort_);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_s(0, st2);
-                    mma_commit(&s.s_full[0]);
+            int k = 0;
+            if (warp == 1) {
+                for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
+                    const int nt = p.items[idx].nt;
+                    for (int j = 0; j < nt; ++j, ++g) {
+                        const int st = g % kKStages;
+                        ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
+                             (j > 0 || mbar_wait(&s.bar_q, k & 1, &s.abort_)) &&
+                             mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_s(0, st);
+                        mma_commit(&s.s_full[0]);
+                        ok = mbar_wait(&s.s_free, 0, &s.abort_);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_s(1, st);
+                        mma_commit(&s.s_full[1]);
+                        mma_commit(&s.k_empty[st]);
+                        if (j + 1 == nt)
+                            mma_commit(&s.q_empty);      // the last S of the item has read Q
+                    }
                 }
-                ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                issue_o(1, sv, j > 0);
-                mma_commit(&s.v_empty[sv]);
-                if (last_of_item)
-                    mma_commit(&s.o_full[1]);
-                if (!has_next)
-                    break;
-                issue_s(1, st2);
-                mma_commit(&s.s_full[1]);
-                mma_commit(&s.k_empty[st2]);
-                if (next_j + 1 == next_nt)
-                    mma_commit(&s.q_empty);              // the last S of that item reads Q now
-                ++g;
-                if (last_of_item) {
-                    idx = next_idx;
-                    ++k;
+            } else {
+                for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
+                    const int nt = p.items[idx].nt;
+                    for (int j = 0; j < nt; ++j, ++g) {
+                        const int sv = g % kVStages;
+                        ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
+                             mbar_wait(&s.v_full[sv], (g / kVStages) & 1, &s.abort_);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_o(0, sv, j > 0);
+                        mma_commit(&s.pv_done[0]);
+                        ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_o(1, sv, j > 0);
+                        mma_commit(&s.pv_done[1]);
+                        mma_commit(&s.v_empty[sv]);
+                    }
                 }
-                j = next_j;
-                nt = next_nt;
             }
             if (!ok)
                 abort_with(s, p.err, kErrTimeout);
-            // Every issued MMA completes before TMEM is released.
+            // Every MMA this thread issued completes before TMEM is released.
             int never = 0;
-            mma_commit(&s.fin);
-            if (!mbar_wait(&s.fin, 0, &never))
+            mma_commit(&s.fin[warp - 1]);
+            if (!mbar_wait(&s.fin[warp - 1], 0, &never))
                 atomicOr(p.err, kErrTimeout);
         }
     } else if (warp >= 4) {
@@ -378,7 +390,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         const int quarter = warp & 3;                   // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;              // row of the tile
         const uint32_t lane_addr = tm + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t tS = lane_addr + 128 * t, tO = lane_addr + 256 + 128 * t;
+        const uint32_t tS = lane_addr + kColS, tP = lane_addr + kColP + 64 * t, tO = lane_addr + kColO + 128 * t;
         const float c = p.scale_log2;
         const float2 cc = make_float2(c, c);
         uint32_t gt = 0;
@@ -402,7 +414,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 tc_fence_after();
                 __syncwarp();                            // tcgen05.ld is warp-collective
                 uint32_t su[128];
-                tmem_ld128(tS, su);                      // this row of S (fp32)
+                tmem_ld128(tS, su);                      // this row of S (fp32), waited for
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s.s_free);              // the MMA may overwrite S now
+                __syncwarp();
                 const int key0 = 128 * j;
                 if (key0 + 127 > qpos) {                 // diagonal (or beyond): keys > qpos are masked
 #pragma unroll
@@ -435,7 +452,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 __syncwarp();
                 const float m_use = (m == -INFINITY) ? 0.0f : m;
                 const float2 mm = make_float2(-m_use, -m_use);
-                // P = 2^(S c - m), bf16, written over the first 64 columns of S.
+                // P of this warpgroup's previous tile and O must have been
+                // consumed by PV(g-1) before P is overwritten or O rescaled.
+                if (g > 0 && !mbar_wait(&s.pv_done[t], (g - 1) & 1, &s.abort_)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                __syncwarp();
+                // P = 2^(S c - m), bf16, into this warpgroup's P columns.
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
 #pragma unroll
@@ -454,11 +479,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         acc[i & 3] = add2(acc[i & 3], pr);
                         pk[i] = pack_bf16x2(pr.x, pr.y);
                     }
-                    tmem_st16(tS + 16 * q4, pk);
+                    tmem_st16(tP + 16 * q4, pk);
                 }
                 const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
                 l += (s01.x + s01.y) + (s23.x + s23.y);
-                if (rescale_o) {                         // O (PV of tile j-1 is complete) *= alpha
+                if (rescale_o) {                         // O (PV of tile g-1 is complete) *= alpha
 #pragma unroll 1
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t u[32];
@@ -484,7 +509,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             // are written as zeros; positions past n are clipped by the store.
             // The named barriers below need every thread of the warpgroup, so
             // a timeout is agreed on by all of them before anyone leaves.
-            if (named_bar_any(1 + t, 128, !mbar_wait(&s.o_full[t], k & 1, &s.abort_))) {
+            if (named_bar_any(1 + t, 128, !mbar_wait(&s.pv_done[t], (gt + nt - 1) & 1, &s.abort_))) {
                 ok = false;
                 break;
             }

@@ -204,6 +204,26 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor as two 32-bit words.  The low word holds the start
+// address (>> 4, bits 0-13) and the leading byte offset; the high word the
+// stride byte offset, the version bit and the swizzle mode.  Operands that
+// differ only by a shared-memory offset share the high word, and their low
+// words differ by offset >> 4 (no carry: shared addresses stay below 256 KB).
+__host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo_bytes)
+{
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes)
+{
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator:
 // D format bits 4-5 (1 = f32), A format 7-9 and B format 10-12 (1 = bf16),
 // A / B major-ness bits 15 / 16 (0 = K-major, 1 = MN-major), N >> 3 at
