@@ -186,92 +186,102 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // The whole warp: lane 0 keeps the barriers, and the copies of a
+        // tile (8 pages x 2 column halves) are issued one per lane, 16 at
+        // once; one thread issuing them in turn spends ~35 ns per copy.
         if (lane == 0) {
             prefetch_tmap(&mQ);
             prefetch_tmap(&mKV);
-            const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
-            uint32_t gt = 0;                              // K tiles issued so far
-            int k = 0, q_issued = 0, v_missing = 0;
-            bool ok = true;
-            // Loads one K/V tile (8 pages, one 16-token box per page and
-            // column half) into stages gt % kKStages and gt % kVStages once
-            // their last readers are done.
-            auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
-                const int st = gt % kKStages, sv = gt % kVStages;
-                const uint32_t use = gt / kKStages, vuse = gt / kVStages;
-                const int32_t *tab = p.tables + (size_t)sd.row * p.stride;
-                const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
-                int page[8];
-#pragma unroll
-                for (int pg = 0; pg < 8; ++pg) {
-                    const int lp = 8 * j + pg;
-                    int ph = p.num_pages;                 // out of range: the box reads zeros
-                    if (lp < seq_pages) {
-                        ph = tab[lp];
-                        if ((unsigned)ph >= (unsigned)p.num_pages) {
-                            atomicOr(p.err, kErrPageId);
-                            ph = p.num_pages;
-                        }
-                    }
-                    page[pg] = ph;
-                }
-                if (use > 0 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_))
-                    return false;
-                mbar_arrive_expect_tx(&s.k_full[st], 2 * kTileBytes);
-#pragma unroll
-                for (int pg = 0; pg < 8; ++pg)
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_4d(&mKV, &s.k_full[st], s.k[st][c] + pg * 16 * 64, 64 * c, 0, it.kvh, page[pg]);
-                ++gt;                                     // K of this tile is in flight from here on
-                if (vuse > 0 && !mbar_wait(&s.v_empty[sv], (vuse - 1) & 1, &s.abort_)) {
-                    ++v_missing;
-                    return false;
-                }
-                mbar_arrive_expect_tx(&s.v_full[sv], 2 * kTileBytes);
-#pragma unroll
-                for (int pg = 0; pg < 8; ++pg)
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_4d(&mKV, &s.v_full[sv], s.v[sv][c] + pg * 16 * 64, 64 * c, 0, p.H_kv + it.kvh,
-                                    page[pg]);
-                return true;
-            };
-            // The first item's Q load is issued before the K/V loop.
-            bool first_q_issued = false;
-            if (i_begin < i_end) {
-                const TcItem it = p.items[i_begin];
+        }
+        const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
+        const int my_pg = (lane >> 1) & 7, my_c = lane & 1;
+        const bool boxer = lane < 16;
+        uint32_t gt = 0;                                  // K tiles issued so far
+        int k = 0, q_issued = 0, v_missing = 0;
+        bool ok = true;
+        // Lane 0 waits; the warp learns the outcome from it.
+        auto wait0 = [&](uint64_t *bar, uint32_t parity) -> bool {
+            int w = 1;
+            if (lane == 0)
+                w = mbar_wait(bar, parity, &s.abort_) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, w, 0) != 0;
+        };
+        auto load_q = [&](const TcItem &it) {
+            if (lane == 0)
                 mbar_arrive_expect_tx(&s.bar_q, q_bytes);
-                for (int t = 0; t < 2; ++t)
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos, it.b);
-                first_q_issued = true;
+            __syncwarp();
+            if (lane < 4)                                 // lane = query tile * 2 + column half
+                tma_load_4d(&mQ, &s.bar_q, s.q[lane >> 1][lane & 1], 64 * (lane & 1), it.kvh * p.G,
+                            it.i0 + (lane >> 1) * p.rows_pos, it.b);
+        };
+        // Loads one K/V tile (8 pages, one 16-token box per page and column
+        // half) into stages gt % kKStages and gt % kVStages once their last
+        // readers are done.
+        auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
+            const int st = gt % kKStages, sv = gt % kVStages;
+            const uint32_t use = gt / kKStages, vuse = gt / kVStages;
+            int ph = p.num_pages;                         // out of range: the box reads zeros
+            if (boxer) {
+                const int lp = 8 * j + my_pg;
+                const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
+                if (lp < seq_pages) {
+                    ph = p.tables[(size_t)sd.row * p.stride + lp];
+                    if ((unsigned)ph >= (unsigned)p.num_pages) {
+                        atomicOr(p.err, kErrPageId);
+                        ph = p.num_pages;
+                    }
+                }
             }
-            for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                const TcItem it = p.items[idx];
-                const SeqDesc sd = p.seqs[it.b];
-                // The first K/V tile only needs a free stage; issue it before
-                // waiting for the previous item to release the Q buffers.
-                if (!load_kv(it, sd, 0)) {
+            if (use > 0 && !wait0(&s.k_empty[st], (use - 1) & 1))
+                return false;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&s.k_full[st], 2 * kTileBytes);
+            __syncwarp();
+            if (boxer)
+                tma_load_4d(&mKV, &s.k_full[st], s.k[st][my_c] + my_pg * 16 * 64, 64 * my_c, 0, it.kvh, ph);
+            ++gt;                                         // K of this tile is in flight from here on
+            if (vuse > 0 && !wait0(&s.v_empty[sv], (vuse - 1) & 1)) {
+                ++v_missing;
+                return false;
+            }
+            if (lane == 0)
+                mbar_arrive_expect_tx(&s.v_full[sv], 2 * kTileBytes);
+            __syncwarp();
+            if (boxer)
+                tma_load_4d(&mKV, &s.v_full[sv], s.v[sv][my_c] + my_pg * 16 * 64, 64 * my_c, 0, p.H_kv + it.kvh,
+                            ph);
+            return true;
+        };
+        // The first item's Q load is issued before the K/V loop.
+        bool first_q_issued = false;
+        if (i_begin < i_end) {
+            load_q(p.items[i_begin]);
+            first_q_issued = true;
+        }
+        for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
+            const TcItem it = p.items[idx];
+            const SeqDesc sd = p.seqs[it.b];
+            // The first K/V tile only needs a free stage; issue it before
+            // waiting for the previous item to release the Q buffers.
+            if (!load_kv(it, sd, 0)) {
+                ok = false;
+                break;
+            }
+            if (k > 0) {
+                if (!wait0(&s.q_empty, (k - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                if (k > 0) {
-                    if (!mbar_wait(&s.q_empty, (k - 1) & 1, &s.abort_)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&s.bar_q, q_bytes);
-                    for (int t = 0; t < 2; ++t)
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_4d(&mQ, &s.bar_q, s.q[t][c], 64 * c, it.kvh * p.G, it.i0 + t * p.rows_pos,
-                                        it.b);
-                }
-                ++q_issued;
-                for (int j = 1; j < it.nt; ++j)
-                    if (!load_kv(it, sd, j)) {
-                        ok = false;
-                        break;
-                    }
+                load_q(it);
             }
+            ++q_issued;
+            for (int j = 1; j < it.nt; ++j)
+                if (!load_kv(it, sd, j)) {
+                    ok = false;
+                    break;
+                }
+        }
+        if (lane == 0) {
             if (!ok)
                 abort_with(s, p.err, kErrTimeout);
             // Drain: every issued copy lands before the CTA exits.
