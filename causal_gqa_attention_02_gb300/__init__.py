@@ -30,7 +30,7 @@ ERRNAMES = {EINVAL: "EINVAL", ERANGE: "ERANGE", EMASK: "EMASK", ENOMEM: "ENOMEM"
             ELAYOUT: "ELAYOUT", ECUDA: "ECUDA", EDEVICE: "EDEVICE"}
 DTYPE_BF16, DTYPE_F32 = 1, 2
 PAGE_TOKENS = 16
-LAYOUT_VERSION = 1
+LAYOUT_VERSION = 2
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
 KERNELS = {"cache_write": 0, "cow_copy": 1, "prefill_tc": 2, "attn_simt": 3,
            "decode_split": 4, "decode_combine": 5}
@@ -153,9 +153,16 @@ class Cache:
         return self._h
 
     def pool_view(self):
-        """The pool as [num_pages, 2 (K, V), H_kv, 16, d_h] of the cache dtype."""
-        return self.pool.view(self.torch_dtype).view(self.num_pages, 2, self.num_kv_heads,
-                                                     PAGE_TOKENS, self.head_dim)
+        """The pool as [num_pages, 2 (K, V), H_kv, 2 (slot groups), C (128-byte
+        chunks of a row), 8 (slots), 128 / element size] of the cache dtype:
+        slot s of a page is group s // 8, position s % 8; element e of its row
+        is chunk e // (128 / element size).  Elements past d_h in the last
+        chunk are padding."""
+        es = 2 if self.torch_dtype == torch.bfloat16 else 4
+        per = 128 // es
+        chunks = -(-self.head_dim * es // 128)
+        return self.pool.view(self.torch_dtype).view(self.num_pages, 2, self.num_kv_heads, 2, chunks,
+                                                     PAGE_TOKENS // 2, per)
 
     def close(self):
         if self._h:

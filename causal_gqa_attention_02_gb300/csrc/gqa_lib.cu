@@ -371,8 +371,8 @@ size_t gqa_pool_bytes(const gqa_cache_desc *d)
     if (!d || d->num_pages < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
         (d->dtype != GQA_DTYPE_BF16 && d->dtype != GQA_DTYPE_F32))
         return 0;
-    const size_t es = d->dtype == GQA_DTYPE_BF16 ? 2 : 4;
-    return (size_t)d->num_pages * 2 * (size_t)d->num_kv_heads * kPageTokens * (size_t)d->head_dim * es;
+    const int es = d->dtype == GQA_DTYPE_BF16 ? 2 : 4;
+    return (size_t)d->num_pages * 2 * (size_t)d->num_kv_heads * pool_block_bytes(d->head_dim * es);
 }
 
 int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes, gqa_cache **out)

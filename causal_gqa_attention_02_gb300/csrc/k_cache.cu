@@ -35,7 +35,8 @@ template <> struct Unit<1>  { using T = uint8_t; };
 // grid: (x = token blocks, y = batch entry); one warp per token.  A token's
 // K rows for all KV heads are contiguous in k (H_kv * d * esize bytes), so a
 // warp reads them with consecutive lanes on consecutive units and writes each
-// head's row to its (page, slot): both sides coalesced.  Every unit of the
+// head's row to its (page, slot), whose 128-byte chunks are contiguous runs:
+// both sides coalesced.  Every unit of the
 // token is loaded before any is stored, to keep the loads in flight.
 // With zero_out != nullptr the same grid also writes zeros over the padding
 // rows count..n-1 of zero_out ([B, n, zero_row_bytes]).
@@ -52,7 +53,8 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
     const int row_bytes = pv.d * esize;
     const int cpr = row_bytes / U;                      // units per (token, head) row
     const int units = pv.H_kv * cpr;                    // units of one token's K (or V)
-    const size_t page_bytes = (size_t)2 * pv.H_kv * kPageTokens * row_bytes;
+    const int chunks = pool_chunks(row_bytes);
+    const size_t blk_bytes = pool_block_bytes(row_bytes);
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
     for (int t = blockIdx.x * wpb + warp; t < sd.count; t += gridDim.x * wpb) {
         const int pos = sd.past + t;
@@ -63,8 +65,9 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
             continue;
         }
         const size_t src_off = ((size_t)b * n + t) * (size_t)units * U;
-        char *kd = (char *)pv.pool + (size_t)page * page_bytes + (size_t)(pos % kPageTokens) * row_bytes;
-        char *vd = kd + (size_t)pv.H_kv * kPageTokens * row_bytes;
+        const int slot = pos % kPageTokens;
+        char *kd = (char *)pv.pool + (size_t)page * 2 * pv.H_kv * blk_bytes;
+        char *vd = kd + (size_t)pv.H_kv * blk_bytes;
         for (int u0 = 0; u0 < units; u0 += 32 * kMaxPerLane) {
             T kr[kMaxPerLane], vr[kMaxPerLane];
 #pragma unroll
@@ -80,7 +83,7 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
                 const int u = u0 + 32 * i + lane;
                 if (u < units) {
                     const int hh = u / cpr, c = u - hh * cpr;
-                    const size_t off = (size_t)hh * kPageTokens * row_bytes + (size_t)c * U;
+                    const size_t off = (size_t)hh * blk_bytes + pool_in_block(chunks, slot, c * U);
                     *(T *)(kd + off) = kr[i];
                     *(T *)(vd + off) = vr[i];
                 }
@@ -102,9 +105,11 @@ __global__ void cow_copy_kernel(PoolView pv, int esize, const CowDesc *__restric
 {
     using T = typename Unit<U>::T;
     const CowDesc cd = cows[blockIdx.y];
-    const size_t row_bytes = (size_t)pv.d * esize;
-    const int cpr = (int)(row_bytes / U);
-    const size_t page_bytes = (size_t)2 * pv.H_kv * kPageTokens * row_bytes;
+    const int row_bytes = pv.d * esize;
+    const int cpr = row_bytes / U;
+    const int chunks = pool_chunks(row_bytes);
+    const size_t blk_bytes = pool_block_bytes(row_bytes);
+    const size_t page_bytes = 2 * (size_t)pv.H_kv * blk_bytes;
     if ((unsigned)cd.src >= (unsigned)pv.num_pages || (unsigned)cd.dst >= (unsigned)pv.num_pages) {
         if (threadIdx.x == 0 && blockIdx.x == 0)
             atomicOr(pv.err, kErrPageId);
@@ -117,7 +122,7 @@ __global__ void cow_copy_kernel(PoolView pv, int esize, const CowDesc *__restric
         long long r = u / cpr;
         const int slot = (int)(r % cd.slots);
         const int blk = (int)(r / cd.slots);           // kv * H_kv + head
-        const size_t off = ((size_t)blk * kPageTokens + slot) * row_bytes + (size_t)c * U;
+        const size_t off = (size_t)blk * blk_bytes + pool_in_block(chunks, slot, c * U);
         *(T *)((char *)pv.pool + (size_t)cd.dst * page_bytes + off) =
             *(const T *)((const char *)pv.pool + (size_t)cd.src * page_bytes + off);
     }

@@ -102,9 +102,13 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     const int nt = min(chunk, L - t0);
     const int npages = (nt + kPageTokens - 1) / kPageTokens;
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride + t0 / kPageTokens;
-    const __nv_bfloat16 *pool = (const __nv_bfloat16 *)pv.pool;
-    const size_t page_elems = (size_t)2 * H_kv * kPageTokens * D;
+    const uint4 *pool = (const uint4 *)pv.pool;
+    // A page block (one head) is 256 uint4; lane l reads token 2i + half,
+    // columns col..col+7, i.e. 128-byte chunk (l >> 3) & 1 of that row, at
+    // uint4 offset (i / 4) * 128 + chunk * 64 + ((2i + half) % 8) * 8 + l % 8.
+    constexpr size_t kBlk = (size_t)kPageTokens * D * 2 / 16;
     const int half = lane >> 4, col = 8 * (lane & 15);
+    const int lane_off = ((lane >> 3) & 1) * 64 + half * 8 + (lane & 7);
 
     // This lane's eight q columns of every head of the group, pre-scaled by
     // log2(e)/sqrt(d_h) so scores come out in exp2 units.
@@ -125,12 +129,11 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         const bool ok = (unsigned)page < (unsigned)pv.num_pages;
         float v[8][G];
         if (ok) {
-            const uint4 *kr = reinterpret_cast<const uint4 *>(pool + (size_t)page * page_elems +
-                                                              (size_t)kvh * kPageTokens * D) + lane;
+            const uint4 *kr = pool + ((size_t)page * 2 * H_kv + kvh) * kBlk + lane_off;
             uint4 kk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                kk[i] = kr[32 * i];                      // token 2i + half, columns col..col+7
+                kk[i] = kr[(i >> 2) * 128 + (i & 3) * 16];   // token 2i + half, columns col..col+7
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t w[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
@@ -223,12 +226,11 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         const int page = tab[pg];
         if ((unsigned)page >= (unsigned)pv.num_pages)
             continue;
-        const uint4 *vr = reinterpret_cast<const uint4 *>(pool + (size_t)page * page_elems +
-                                                          (size_t)(H_kv + kvh) * kPageTokens * D) + lane;
+        const uint4 *vr = pool + ((size_t)page * 2 * H_kv + H_kv + kvh) * kBlk + lane_off;
         uint4 vv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            vv[i] = vr[32 * i];
+            vv[i] = vr[(i >> 2) * 128 + (i & 3) * 16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int tl = pg * kPageTokens + 2 * i + half;   // probabilities are 0 past nt

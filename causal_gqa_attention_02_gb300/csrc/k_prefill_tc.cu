@@ -24,11 +24,10 @@
 //    Decode 推理路径", causal tile skipping).  Diagonal tiles are masked per
 //    element.
 //  * Warp roles: warp 0 issues TMA (Q once per item; K and V per key tile,
-//    one 16-token page box at a time through the block table, two stages,
-//    K and V released separately); warp 1 owns TMEM and issues the S MMAs,
-//    warp 2 the PV MMAs;
-//    warpgroups 1 and 2 (warps 4-7, 8-11) run the softmax, one per query
-//    tile, thread = row.
+//    one 4 KB box per page block through the block table, eight lanes at
+//    once, two stages, K and V released separately); warp 1 owns TMEM and
+//    issues the S MMAs, warp 2 the PV MMAs; warpgroups 1 and 2 (warps 4-7,
+//    8-11) run the softmax, one per query tile, thread = row.
 //  * Persistent: one CTA per SM walks its own run of items, assigned on the
 //    host longest-first to the least-loaded CTA; both MMA streams run on
 //    across items, so the next item's first S = Q K^T is issued as soon as
@@ -88,6 +87,7 @@ constexpr int kKStages = GQA_K_STAGES;
 constexpr int kVStages = GQA_V_STAGES;
 constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
+constexpr int kPageElems = kPageTokens * D;           // one page block of one head (4 KB)
 // TMEM columns: one S buffer (fp32, 128 keys) shared by the two query tiles,
 // P of each tile (bf16 pairs, 64 columns) and O of each tile (fp32, 128).
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
@@ -187,15 +187,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp: lane 0 keeps the barriers, and the copies of a
-        // tile (8 pages x 2 column halves) are issued one per lane, 16 at
-        // once; one thread issuing them in turn spends ~35 ns per copy.
+        // tile are issued one per lane, 8 at once: one 4 KB box per page
+        // (a page block of one head holds the tile's 16 rows in operand
+        // order).  The TMA engine's cost is mostly per box.
         if (lane == 0) {
             prefetch_tmap(&mQ);
             prefetch_tmap(&mKV);
         }
         const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
-        const int my_pg = (lane >> 1) & 7, my_c = lane & 1;
-        const bool boxer = lane < 16;
+        const int my_pg = lane & 7;
+        const bool boxer = lane < 8;
         uint32_t gt = 0;                                  // K tiles issued so far
         int k = 0, q_issued = 0, v_missing = 0;
         bool ok = true;
@@ -214,13 +215,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 tma_load_4d(&mQ, &s.bar_q, s.q[lane >> 1][lane & 1], 64 * (lane & 1), it.kvh * p.G,
                             it.i0 + (lane >> 1) * p.rows_pos, it.b);
         };
-        // Loads one K/V tile (8 pages, one 16-token box per page and column
-        // half) into stages gt % kKStages and gt % kVStages once their last
-        // readers are done.
+        // Loads one K/V tile (8 pages, one box per page) into stages
+        // gt % kKStages and gt % kVStages once their last readers are done.
         auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
             const int st = gt % kKStages, sv = gt % kVStages;
             const uint32_t use = gt / kKStages, vuse = gt / kVStages;
             int ph = p.num_pages;                         // out of range: the box reads zeros
+            const int blk_page = 2 * p.H_kv;                // blocks per page
             if (boxer) {
                 const int lp = 8 * j + my_pg;
                 const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
@@ -238,7 +239,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 mbar_arrive_expect_tx(&s.k_full[st], 2 * kTileBytes);
             __syncwarp();
             if (boxer)
-                tma_load_4d(&mKV, &s.k_full[st], s.k[st][my_c] + my_pg * 16 * 64, 64 * my_c, 0, it.kvh, ph);
+                tma_load_3d(&mKV, &s.k_full[st], s.k[st][0] + my_pg * kPageElems, 0, 0, ph * blk_page + it.kvh);
             ++gt;                                         // K of this tile is in flight from here on
             if (vuse > 0 && !wait0(&s.v_empty[sv], (vuse - 1) & 1)) {
                 ++v_missing;
@@ -248,8 +249,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 mbar_arrive_expect_tx(&s.v_full[sv], 2 * kTileBytes);
             __syncwarp();
             if (boxer)
-                tma_load_4d(&mKV, &s.v_full[sv], s.v[sv][my_c] + my_pg * 16 * 64, 64 * my_c, 0, p.H_kv + it.kvh,
-                            ph);
+                tma_load_3d(&mKV, &s.v_full[sv], s.v[sv][0] + my_pg * kPageElems, 0, 0,
+                            ph * blk_page + p.H_kv + it.kvh);
             return true;
         };
         // The first item's Q load is issued before the K/V loop.
@@ -314,23 +315,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             // instruction itself.  Q tile t, K stage st and V stage sv start
             // 2 * kTileBytes apart; a column half is kTileBytes further.
             constexpr uint32_t kHalf = kTileBytes >> 4, kStage = 2 * kTileBytes >> 4;
-            const uint32_t hi_kmaj = desc_sw128_hi(1024);
+            // Q tile: [column half][128 rows][64], 8-row atoms 1 KB apart.
+            // K and V stages: 8 page blocks of 4 KB, each [8-token group]
+            // [column half][8 tokens][64]: 8-token atoms 2 KB apart, the
+            // second column half 1 KB after the first.
+            const uint32_t hi_q = desc_sw128_hi(1024), hi_kv = desc_sw128_hi(2048);
             const uint32_t q_lo = desc_sw128_lo(smem_u32(s.q[0][0]), 16);
             const uint32_t k_lo = desc_sw128_lo(smem_u32(s.k[0][0]), 16);
-            const uint32_t v_lo = desc_sw128_lo(smem_u32(s.v[0][0]), kTileBytes);
+            const uint32_t v_lo = desc_sw128_lo(smem_u32(s.v[0][0]), 1024);   // N-major: halves 1 KB apart
             auto issue_s = [&](int t, int st) {
                 const uint32_t a0 = q_lo + t * kStage, b0 = k_lo + st * kStage;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks / 4) * kHalf + (ks % 4) * 2;   // 32 bytes per k-step
-                    mma_ss(tm + kColS, desc_join(a0 + off, hi_kmaj), desc_join(b0 + off, hi_kmaj), id_s, ks > 0);
+                for (int ks = 0; ks < 8; ++ks) {   // 16 columns = 32 bytes per k-step
+                    const uint32_t qoff = (ks / 4) * kHalf + (ks % 4) * 2, koff = (ks / 4) * 64 + (ks % 4) * 2;
+                    mma_ss(tm + kColS, desc_join(a0 + qoff, hi_q), desc_join(b0 + koff, hi_kv), id_s, ks > 0);
                 }
             };
             auto issue_o = [&](int t, int sv, bool acc) {
                 const uint32_t b0 = v_lo + sv * kStage;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)   // 16 keys = 2048 bytes of the N-major V tile per k-step
-                    mma_ts(tm + kColO + 128 * t, tm + kColP + 64 * t + ks * 8, desc_join(b0 + ks * 128, hi_kmaj), id_o,
+                for (int ks = 0; ks < 8; ++ks)   // 16 keys = two 8-token atoms = 4 KB per k-step
+                    mma_ts(tm + kColO + 128 * t, tm + kColP + 64 * t + ks * 8, desc_join(b0 + ks * 256, hi_kv), id_o,
                            (acc || ks > 0) ? 1u : 0u);
             };
             // One flat stream of key tiles over this CTA's items: tile g is
@@ -587,14 +592,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
     return fn;
 }
 
-bool encode4(CUtensorMap *m, const void *base, const cuuint64_t dims[4], const cuuint64_t strides[3],
-             const cuuint32_t box[4])
+bool encode(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+            const cuuint32_t *box)
 {
     auto fn = encoder();
     if (!fn)
         return false;
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -619,14 +624,14 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     const cuuint64_t qdims[4] = {(cuuint64_t)D, (cuuint64_t)H_q, (cuuint64_t)n, (cuuint64_t)B};
     const cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H_q * D * 2, (cuuint64_t)n * H_q * D * 2};
     const cuuint32_t qbox[4] = {64, (cuuint32_t)G, (cuuint32_t)rows_pos, 1};
-    const cuuint64_t kvdims[4] = {(cuuint64_t)D, (cuuint64_t)kPageTokens, (cuuint64_t)2 * pv.H_kv,
-                                  (cuuint64_t)pv.num_pages};
-    const cuuint64_t kvstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageTokens * D * 2,
-                                 (cuuint64_t)2 * pv.H_kv * kPageTokens * D * 2};
-    const cuuint32_t kvbox[4] = {64, (cuuint32_t)kPageTokens, 1, 1};
+    // The pool as 128-byte lines: [block][32 lines][64 elements]; a box is
+    // one page block (4 KB).
+    const cuuint64_t kvdims[3] = {64, 32, (cuuint64_t)pv.num_pages * 2 * pv.H_kv};
+    const cuuint64_t kvstr[2] = {128, 32 * 128};
+    const cuuint32_t kvbox[3] = {64, 32, 1};
     // out has the shape and layout of q: the same box serves the stores.
-    if (!encode4(&mq, q, qdims, qstr, qbox) || !encode4(&mkv, pv.pool, kvdims, kvstr, kvbox) ||
-        !encode4(&mo, out, qdims, qstr, qbox))
+    if (!encode(&mq, 4, q, qdims, qstr, qbox) || !encode(&mkv, 3, pv.pool, kvdims, kvstr, kvbox) ||
+        !encode(&mo, 4, out, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     TcParams prm;
     prm.seqs = d_seqs;

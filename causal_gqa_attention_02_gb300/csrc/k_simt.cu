@@ -74,10 +74,15 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
     const float root_d = sqrtf((float)d);
     const int pos = sd.past + i;                  // visible keys 0..pos
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
-    const T *pool = (const T *)pv.pool;
-    const size_t page_elems = (size_t)2 * H_kv * kPageTokens * d;
-    const size_t k_off = (size_t)g * kPageTokens * d;
-    const size_t v_off = (size_t)(H_kv + g) * kPageTokens * d;
+    const char *pool = (const char *)pv.pool;
+    const int chunks = pool_chunks(d * (int)sizeof(T));
+    const size_t blk_bytes = pool_block_bytes(d * (int)sizeof(T));
+    const size_t k_off = (size_t)g * blk_bytes;
+    const size_t v_off = (size_t)(H_kv + g) * blk_bytes;
+    // Element e of the row of `slot` in the block at `blk`.
+    auto elem = [&](const char *blk, int slot, int e) -> const T * {
+        return (const T *)(blk + pool_in_block(chunks, slot, e * (int)sizeof(T)));
+    };
 
     float m = -INFINITY, l = 0.0f;
     float acc[kMaxD / 32];
@@ -91,10 +96,10 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
         if (t <= pos) {
             const int page = tab[t / kPageTokens];
             if ((unsigned)page < (unsigned)pv.num_pages) {
-                const T *kr = pool + (size_t)page * page_elems + k_off + (size_t)(t % kPageTokens) * d;
+                const char *kb_ = pool + (size_t)page * 2 * H_kv * blk_bytes + k_off;
                 float dot = 0.0f;
                 for (int e = 0; e < d; ++e)
-                    dot = fmaf(qs[e], ldf(kr + e), dot);
+                    dot = fmaf(qs[e], ldf(elem(kb_, t % kPageTokens, e)), dot);
                 s = dot / root_d;
             } else {
                 atomicOr(pv.err, kErrPageId);
@@ -114,12 +119,12 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
             const int page = tab[tu / kPageTokens];
             if ((unsigned)page >= (unsigned)pv.num_pages)
                 continue;
-            const T *vr = pool + (size_t)page * page_elems + v_off + (size_t)(tu % kPageTokens) * d;
+            const char *vb_ = pool + (size_t)page * 2 * H_kv * blk_bytes + v_off;
 #pragma unroll
             for (int j = 0; j < kMaxD / 32; ++j) {
                 const int e = lane + 32 * j;
                 if (e < d)
-                    acc[j] = fmaf(pu, ldf(vr + e), acc[j]);
+                    acc[j] = fmaf(pu, ldf(elem(vb_, tu % kPageTokens, e)), acc[j]);
             }
         }
         m = m_new;

@@ -11,9 +11,24 @@ namespace gqa {
 
 constexpr int kPageTokens = 16;
 
+// Page pool layout (version 2).  Block (page, kv, head), kv 0 = K, 1 = V,
+// is number (page * 2 + kv) * H_kv + head and holds the 16 token rows of that
+// page for that head.  A row (d * esize bytes) is cut into C = ceil(row / 128)
+// chunks of 128 bytes; the 16 slots form two groups of 8, and within a group
+// the rows are stored chunk-major: chunk 0 of slots 0..7, then chunk 1 of
+// slots 0..7, ...  Byte b of the row of slot s is at
+//     block * pool_block_bytes + ((s / 8) * C + b / 128) * 1024 + (s % 8) * 128 + b % 128.
+// With 256-byte rows (bf16, d = 128) a block is 4 KB whose 8-line groups are
+// exactly the 1 KB swizzle atoms of a tensor-core operand, so one TMA box
+// moves a page of one head.
+__host__ __device__ constexpr int pool_chunks(int row_bytes) { return (row_bytes + 127) >> 7; }
+__host__ __device__ constexpr size_t pool_block_bytes(int row_bytes) { return (size_t)pool_chunks(row_bytes) << 11; }
+__host__ __device__ constexpr size_t pool_in_block(int chunks, int slot, int b)
+{
+    return ((size_t)((slot >> 3) * chunks + (b >> 7)) << 10) + (size_t)((slot & 7) << 7) + (size_t)(b & 127);
+}
+
 // A view of the paged pool and the block tables as the kernels see them.
-// Pool element (page, kv, head, slot, e) lives at
-//   ((page * 2 + kv) * H_kv + head) * 16 * d + slot * d + e       (kv: 0 = K, 1 = V)
 struct PoolView {
     void *pool;              // device, element type = cache dtype
     const int32_t *tables;   // device [max_seqs][stride]: logical page -> physical page

@@ -34,13 +34,20 @@
  *  - Token-major layouts: q is [B, n, H_q, d_h] and k, v are
  *    [B, n, H_kv, d_h] -- a permuted view of [P1] 2.3's [B, H, n, d_h].
  *
- * Page pool layout (device memory owned by the caller, described by the
- * cache): num_pages pages of page_tokens = 16 token slots.  Page p holds
- *      K at elements [((p*2 + 0)*H_kv + h)*16*d_h + slot*d_h + e]
- *      V at elements [((p*2 + 1)*H_kv + h)*16*d_h + slot*d_h + e]
- * so one (page, K|V, kv-head) block of 16 x d_h is contiguous.  Token t of a
- * sequence lives in logical page t/16 at slot t%16; a per-sequence block
- * table maps logical pages to physical pages ([P3] PagedAttention).
+ * Page pool layout, version 2 (device memory owned by the caller, described
+ * by the cache): num_pages pages of page_tokens = 16 token slots.  A row of
+ * R = d_h * element-size bytes is cut into C = ceil(R / 128) chunks of 128
+ * bytes (the last one zero-padded when 128 does not divide R).  Page p holds,
+ * for kv = 0 (K) and 1 (V) and each KV head h, a block of 16 * C * 128 bytes,
+ * block number (p*2 + kv)*H_kv + h; within it, byte b of the row of slot s is
+ * at byte
+ *      ((s/8)*C + b/128)*1024 + (s%8)*128 + b%128,
+ * i.e. the 16 slots form two groups of 8 and each group stores chunk 0 of its
+ * 8 rows, then chunk 1, ...  (for bf16, d_h = 128 this puts each group of 8
+ * tokens in the layout the tensor-core operands read, so one 4 KB copy moves
+ * a page of one head).  Token t of a sequence lives in logical page t/16 at
+ * slot t%16; a per-sequence block table maps logical pages to physical pages
+ * ([P3] PagedAttention).
  *
  * Allocation rules (deterministic; the tests restate them independently):
  *  - a free page is taken in the order `page_order` gives (identity when
@@ -84,7 +91,7 @@ extern "C" {
 #define GQA_DTYPE_F32  2
 
 #define GQA_PAGE_TOKENS    16
-#define GQA_LAYOUT_VERSION 1
+#define GQA_LAYOUT_VERSION 2
 
 /* Cache description ([P1] 2.5: cache_config fixes the KV layout and the
  * position convention). */
@@ -117,8 +124,9 @@ typedef struct {
 
 typedef struct gqa_cache gqa_cache;
 
-/* Bytes the page pool of `desc` occupies: num_pages * 2 * H_kv * 16 * d_h *
- * element size.  Returns 0 for an invalid description. */
+/* Bytes the page pool of `desc` occupies: num_pages * 2 * H_kv * 16 * C *
+ * 128 with C = ceil(d_h * element size / 128) (layout version 2 above).
+ * Returns 0 for an invalid description. */
 size_t gqa_pool_bytes(const gqa_cache_desc *desc);
 
 /* Create a cache over a caller-owned device pool (`pool_dev`, at least

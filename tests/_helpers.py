@@ -25,11 +25,23 @@ def host_f64(t, dt):
 
 
 def raw_pool(cache):
-    """Pool as host raw values [pages, 2, H_kv, 16, d] (uint16 bits or f32)."""
-    pv = cache.pool_view().detach().cpu()
-    if cache.torch_dtype == torch.bfloat16:
-        return pv.view(torch.int16).numpy().view(np.uint16)
-    return pv.numpy()
+    """Pool as host raw values [pages, 2, H_kv, 16, d] (uint16 bits or f32),
+    decoded from the byte layout the header documents: the block of (page,
+    K|V, head) holds two groups of 8 slots; a group stores its rows' 128-byte
+    chunk 0, then chunk 1, ...; byte b of slot s's row is at
+    ((s // 8) * C + b // 128) * 1024 + (s % 8) * 128 + b % 128."""
+    bf16 = cache.torch_dtype == torch.bfloat16
+    es = 2 if bf16 else 4
+    d, H = cache.head_dim, cache.num_kv_heads
+    C = -(-d * es // 128)
+    raw = cache.pool.detach().cpu().numpy().view(np.uint8)
+    blocks = raw[: cache.num_pages * 2 * H * 16 * C * 128].reshape(cache.num_pages, 2, H, 16 * C * 128)
+    s = np.arange(16)[:, None]
+    b = (np.arange(d) * es)[None, :]
+    off = ((s // 8) * C + b // 128) * 1024 + (s % 8) * 128 + b % 128          # [16, d] byte offsets
+    idx = off[..., None] + np.arange(es)                                       # [16, d, es]
+    vals = np.ascontiguousarray(blocks[..., idx])                              # [P, 2, H, 16, d, es]
+    return vals.view(np.uint16 if bf16 else np.float32)[..., 0]
 
 
 def gather_seq(pool, table, length):
