@@ -23,11 +23,11 @@
 //    tiles wholly above the diagonal are skipped ("KV Cache 与 Prefill/
 //    Decode 推理路径", causal tile skipping).  Diagonal tiles are masked per
 //    element.
-//  * Warp roles: warp 0 issues TMA (Q once per item; K and V per key tile,
-//    one 4 KB box per page block through the block table, eight lanes at
-//    once, two stages, K and V released separately); warp 1 owns TMEM and
-//    issues the S MMAs, warp 2 the PV MMAs; warpgroups 1 and 2 (warps 4-7,
-//    8-11) run the softmax, one per query tile, thread = row.
+//  * Warp roles: warps 0 and 3 issue TMA (warp 0 Q once per item and K per
+//    key tile, warp 3 V per key tile; one 4 KB box per page block through
+//    the block table, eight lanes at once, two stages each); warp 1 owns
+//    TMEM and issues the S MMAs, warp 2 the PV MMAs; warpgroups 1 and 2
+//    (warps 4-7, 8-11) run the softmax, one per query tile, thread = row.
 //  * Persistent: one CTA per SM walks its own run of items, assigned on the
 //    host longest-first to the least-loaded CTA; both MMA streams run on
 //    across items, so the next item's first S = Q K^T is issued as soon as
@@ -84,6 +84,10 @@ constexpr int D = 128;
 #define GQA_V_STAGES 2
 #endif
 constexpr int kKStages = GQA_K_STAGES;
+#ifndef GQA_PV_ORDER
+#define GQA_PV_ORDER 1
+#endif
+constexpr bool kPvOrder = GQA_PV_ORDER != 0;
 constexpr int kVStages = GQA_V_STAGES;
 constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
@@ -102,6 +106,7 @@ struct __align__(1024) TcSmem {
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
     int abort_;
+    int s_issued[2];                                   // S MMAs of tile 0 / 1 issued so far (monotonic)
 };
 
 static_assert(sizeof(TcSmem) + 1024 <= 227 * 1024, "shared memory per CTA");
@@ -159,6 +164,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     }
     if (threadIdx.x == 0) {
         s.abort_ = 0;
+        s.s_issued[0] = s.s_issued[1] = 0;
         mbar_init(&s.bar_q, 1);
         mbar_init(&s.q_empty, 1);
         for (int i = 0; i < kKStages; ++i) {
@@ -184,21 +190,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     tc_fence_after();
     const uint32_t tm = s.tmem;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        // The whole warp: lane 0 keeps the barriers, and the copies of a
-        // tile are issued one per lane, 8 at once: one 4 KB box per page
-        // (a page block of one head holds the tile's 16 rows in operand
-        // order).  The TMA engine's cost is mostly per box.
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------ TMA producers
+        // Warp 0 loads Q and K, warp 3 loads V: with one producer a V stage
+        // that frees late held up the next K tile behind it.  Each is a
+        // whole warp: lane 0 keeps the barriers, and a tile's copies are
+        // issued one per lane, 8 at once, one 4 KB box per page block (a
+        // page block of one head holds the tile's 16 rows in operand order;
+        // the TMA engine's cost is mostly per box).
+        const bool vside = warp == 3;
         if (lane == 0) {
-            prefetch_tmap(&mQ);
+            if (!vside)
+                prefetch_tmap(&mQ);
             prefetch_tmap(&mKV);
         }
+        const int stages = vside ? kVStages : kKStages;
         const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
         const int my_pg = lane & 7;
         const bool boxer = lane < 8;
-        uint32_t gt = 0;                                  // K tiles issued so far
-        int k = 0, q_issued = 0, v_missing = 0;
+        const int blk_page = 2 * p.H_kv;                  // blocks per page
+        uint32_t gt = 0;                                  // tiles issued so far by this warp
+        int k = 0, q_issued = 0;
         bool ok = true;
         // Lane 0 waits; the warp learns the outcome from it.
         auto wait0 = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -215,69 +227,65 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 tma_load_4d(&mQ, &s.bar_q, s.q[lane >> 1][lane & 1], 64 * (lane & 1), it.kvh * p.G,
                             it.i0 + (lane >> 1) * p.rows_pos, it.b);
         };
-        // Loads one K/V tile (8 pages, one box per page) into stages
-        // gt % kKStages and gt % kVStages once their last readers are done.
-        auto load_kv = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
-            const int st = gt % kKStages, sv = gt % kVStages;
-            const uint32_t use = gt / kKStages, vuse = gt / kVStages;
+        // Loads this warp's half (K or V) of key tile j of an item into
+        // stage gt % stages once its last readers are done.
+        auto load_tile = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
+            const int st = gt % stages;
+            const uint32_t use = gt / stages;
             int ph = p.num_pages;                         // out of range: the box reads zeros
-            const int blk_page = 2 * p.H_kv;                // blocks per page
             if (boxer) {
                 const int lp = 8 * j + my_pg;
                 const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
                 if (lp < seq_pages) {
                     ph = p.tables[(size_t)sd.row * p.stride + lp];
                     if ((unsigned)ph >= (unsigned)p.num_pages) {
-                        atomicOr(p.err, kErrPageId);
+                        if (!vside)
+                            atomicOr(p.err, kErrPageId);
                         ph = p.num_pages;
                     }
                 }
             }
-            if (use > 0 && !wait0(&s.k_empty[st], (use - 1) & 1))
+            uint64_t *empty = vside ? &s.v_empty[st] : &s.k_empty[st];
+            uint64_t *full = vside ? &s.v_full[st] : &s.k_full[st];
+            __nv_bfloat16 *dst = vside ? s.v[st][0] : s.k[st][0];
+            if (use > 0 && !wait0(empty, (use - 1) & 1))
                 return false;
             if (lane == 0)
-                mbar_arrive_expect_tx(&s.k_full[st], 2 * kTileBytes);
+                mbar_arrive_expect_tx(full, 2 * kTileBytes);
             __syncwarp();
             if (boxer)
-                tma_load_3d(&mKV, &s.k_full[st], s.k[st][0] + my_pg * kPageElems, 0, 0, ph * blk_page + it.kvh);
-            ++gt;                                         // K of this tile is in flight from here on
-            if (vuse > 0 && !wait0(&s.v_empty[sv], (vuse - 1) & 1)) {
-                ++v_missing;
-                return false;
-            }
-            if (lane == 0)
-                mbar_arrive_expect_tx(&s.v_full[sv], 2 * kTileBytes);
-            __syncwarp();
-            if (boxer)
-                tma_load_3d(&mKV, &s.v_full[sv], s.v[sv][0] + my_pg * kPageElems, 0, 0,
-                            ph * blk_page + p.H_kv + it.kvh);
+                tma_load_3d(&mKV, full, dst + my_pg * kPageElems, 0, 0,
+                            ph * blk_page + (vside ? p.H_kv : 0) + it.kvh);
+            ++gt;                                         // this tile is in flight from here on
             return true;
         };
-        // The first item's Q load is issued before the K/V loop.
+        // The first item's Q load is issued before the K loop.
         bool first_q_issued = false;
-        if (i_begin < i_end) {
+        if (!vside && i_begin < i_end) {
             load_q(p.items[i_begin]);
             first_q_issued = true;
         }
         for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
             const TcItem it = p.items[idx];
             const SeqDesc sd = p.seqs[it.b];
-            // The first K/V tile only needs a free stage; issue it before
+            // The first K tile only needs a free stage; issue it before
             // waiting for the previous item to release the Q buffers.
-            if (!load_kv(it, sd, 0)) {
+            if (!load_tile(it, sd, 0)) {
                 ok = false;
                 break;
             }
-            if (k > 0) {
-                if (!wait0(&s.q_empty, (k - 1) & 1)) {
-                    ok = false;
-                    break;
+            if (!vside) {
+                if (k > 0) {
+                    if (!wait0(&s.q_empty, (k - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    load_q(it);
                 }
-                load_q(it);
+                ++q_issued;
             }
-            ++q_issued;
             for (int j = 1; j < it.nt; ++j)
-                if (!load_kv(it, sd, j)) {
+                if (!load_tile(it, sd, j)) {
                     ok = false;
                     break;
                 }
@@ -287,13 +295,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 abort_with(s, p.err, kErrTimeout);
             // Drain: every issued copy lands before the CTA exits.
             int never = 0;
-            for (uint32_t g = (gt > kKStages ? gt - kKStages : 0); g < gt; ++g) {
-                if (!mbar_wait(&s.k_full[g % kKStages], (g / kKStages) & 1, &never))
-                    atomicOr(p.err, kErrTimeout);
-            }
-            const uint32_t v_done = gt - v_missing;
-            for (uint32_t g = (v_done > kVStages ? v_done - kVStages : 0); g < v_done; ++g) {
-                if (!mbar_wait(&s.v_full[g % kVStages], (g / kVStages) & 1, &never))
+            for (uint32_t g = (gt > (uint32_t)stages ? gt - stages : 0); g < gt; ++g) {
+                uint64_t *full = vside ? &s.v_full[g % stages] : &s.k_full[g % stages];
+                if (!mbar_wait(full, (g / stages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
             if (first_q_issued && q_issued == 0)
@@ -358,32 +362,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         tc_fence_after();
                         issue_s(0, st);
                         mma_commit(&s.s_full[0]);
+                        *(volatile int *)&s.s_issued[0] = (int)g + 1;
                         ok = mbar_wait(&s.s_free, 0, &s.abort_);
                         if (!ok)
                             break;
                         tc_fence_after();
                         issue_s(1, st);
                         mma_commit(&s.s_full[1]);
+                        *(volatile int *)&s.s_issued[1] = (int)g + 1;
                         mma_commit(&s.k_empty[st]);
                         if (j + 1 == nt)
                             mma_commit(&s.q_empty);      // the last S of the item has read Q
                     }
                 }
             } else {
+                // PV_t(g) goes into the tensor pipe right behind S_t(g+1): the
+                // S MMAs, on which the softmax warps wait, then run alone, and
+                // PV_t(g) runs while the softmax warps read S_t(g+1) and the
+                // next S is issued.  A bounded poll on the S issuer's count;
+                // it orders issue only (the barriers carry every dependency),
+                // and is skipped for an item's last tile.
+                auto after_s = [&](int t, uint32_t count) {
+                    const uint64_t t0 = globaltimer();
+                    for (int it = 0; *(volatile int *)&s.s_issued[t] < (int)count; ++it)
+                        if ((it & 63) == 63 && globaltimer() - t0 > 20000)
+                            break;
+                };
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
                     const int nt = p.items[idx].nt;
                     for (int j = 0; j < nt; ++j, ++g) {
                         const int sv = g % kVStages;
+                        const bool order = kPvOrder && j + 1 < nt;
                         ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
                              mbar_wait(&s.v_full[sv], (g / kVStages) & 1, &s.abort_);
                         if (!ok)
                             break;
+                        if (order)
+                            after_s(0, g + 2);
                         tc_fence_after();
                         issue_o(0, sv, j > 0);
                         mma_commit(&s.pv_done[0]);
                         ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
                         if (!ok)
                             break;
+                        if (order)
+                            after_s(1, g + 2);
                         tc_fence_after();
                         issue_o(1, sv, j > 0);
                         mma_commit(&s.pv_done[1]);
