@@ -63,10 +63,15 @@ def load_peaks():
 
 
 def source_sha(kernel):
-    p = os.path.join(ROOT, KERNEL_SOURCES[kernel])
-    if not os.path.exists(p):
-        return None
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+    """Hash of the kernel's source file and the device headers it includes."""
+    h = hashlib.sha256()
+    for rel in (KERNEL_SOURCES[kernel], "causal_gqa_attention_02_gb300/csrc/kernels.cuh",
+                "causal_gqa_attention_02_gb300/csrc/sm100.cuh"):
+        p = os.path.join(ROOT, rel)
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
 
 
 def traffic_for(kernel, units_scale=1.0):
