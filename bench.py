@@ -217,13 +217,16 @@ def timed_steps(torch, dist, step, K, flush=None):
 # workloads
 # ---------------------------------------------------------------------------
 
-def prefill_cpu_baseline(w, budget_s=12.0):
+def prefill_cpu_baseline(w, budget_s):
+    """The fp64 oracle on the host cores, cycling over the workload's
+    sequences until about budget_s seconds of CPU work are done."""
     import oracle
     import causal_gqa_attention_02_gb300 as gqa
     nth = oracle.default_threads()
     B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
-    done_flops, used, seqs = 0, 0.0, 0
-    for b in range(B):
+    done_flops, used, calls = 0, 0.0, 0
+    while used < budget_s:
+        b = calls % B
         nb = int(w["valid_lengths"][b])
         cm = oracle.CacheModel(workloads.pages_for(nb), 1, workloads.pages_for(nb), H_kv, d, "bf16")
         s = cm.create()
@@ -231,13 +234,11 @@ def prefill_cpu_baseline(w, budget_s=12.0):
         oracle.prefill(cm, [s], w["q"][b:b + 1], w["k"][b:b + 1], w["v"][b:b + 1], [nb], nthreads=nth)
         used += time.perf_counter() - t0
         done_flops += gqa.work.prefill_flops([0], [nb], H_q, d)
-        seqs += 1
-        if used >= budget_s:
-            break
+        calls += 1
     return {"value": done_flops / used / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
-            "sample": "fp64 oracle prefill of sequences 0..%d of the workload (valid lengths %s), all %d query "
-                      "heads: %.1f GFLOP causal in %.1f s" % (seqs - 1, list(map(int, w["valid_lengths"][:seqs])),
-                                                             H_q, done_flops / 1e9, used)}
+            "sample": "fp64 oracle prefill of the workload's sequences (valid lengths %s, all %d query heads), "
+                      "%d sequence calls cycling over them: %.1f GFLOP causal in %.1f s"
+                      % (list(map(int, w["valid_lengths"])), H_q, calls, done_flops / 1e9, used)}
 
 
 def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
@@ -285,17 +286,38 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     gpu_launches = sum(nl for nl, _ in region_launches.values())
     kernels = {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl}
 
-    # End to end through the public API from pinned host buffers.
+    # End to end through the public API from pinned host buffers, pipelined
+    # over the batch entries: entry b's valid rows go up on one copy stream,
+    # attn_prefill of entry b runs on the compute stream once they are in,
+    # and its valid output rows come back on a second copy stream while the
+    # next entry computes.  Only valid rows cross the link (padding rows of
+    # out are zeros by contract).  The step's events are on the compute
+    # stream, which waits for the last copy back.
     qh, kh, vh = pinned(torch, q), pinned(torch, k), pinned(torch, v)
     oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     qd, kd, vd, od = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    ev_in = [torch.cuda.Event() for _ in range(B)]
+    ev_out = [torch.cuda.Event() for _ in range(B)]
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        gqa.attn_prefill(cache, ids, qd, kd, vd, nb, out=od)
-        oh.copy_(od, non_blocking=True)
+        up.wait_stream(main)
+        down.wait_stream(main)
+        with torch.cuda.stream(up):
+            for b in range(B):
+                qd[b, :nb[b]].copy_(qh[b, :nb[b]], non_blocking=True)
+                kd[b, :nb[b]].copy_(kh[b, :nb[b]], non_blocking=True)
+                vd[b, :nb[b]].copy_(vh[b, :nb[b]], non_blocking=True)
+                ev_in[b].record(up)
+        for b in range(B):
+            main.wait_event(ev_in[b])
+            gqa.attn_prefill(cache, [ids[b]], qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], [nb[b]], out=od[b:b + 1])
+            ev_out[b].record(main)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_out[b])
+                oh[b, :nb[b]].copy_(od[b, :nb[b]], non_blocking=True)
+        main.wait_stream(down)
         for s in ids:
             gqa.kv_truncate(cache, s, 0)
 
@@ -303,9 +325,12 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
         e2e_step()
     ems, _, _ = timed_steps(torch, dist, e2e_step, args.steps, flush)
     e2e_total = dist.max(torch, sum(ems))
+    row_q, row_kv = H_q * d * 2, H_kv * d * 2
     e2e = {"value": round(flops * args.steps * dist.world / (e2e_total / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes), "d2h_bytes_per_step": int(out.nbytes),
-           "ms_per_step": round(e2e_total / args.steps, 4)}
+           "h2d_bytes_per_step": int(sum(nb) * (row_q + 2 * row_kv)), "d2h_bytes_per_step": int(sum(nb) * row_q),
+           "ms_per_step": round(e2e_total / args.steps, 4),
+           "how": "attn_prefill per batch entry on one stream; valid rows copied up/down on two copy streams, "
+                  "overlapping the other entries' compute"}
     flags = cache.check()
     cache.close()
     del flush
@@ -403,17 +428,160 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         for j in range(8):
             cm.write([sm[j]], [w["hist_k"][j]], [w["hist_v"][j]])
         oracle.append(cm, sm, w["new_k"][:8], w["new_v"][:8])
-        t0c = time.perf_counter()
-        oracle.decode(cm, sm, w["q"][:8], nthreads=nth)
-        dt = time.perf_counter() - t0c
-        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2)
+        dt, reps = 0.0, 0
+        while dt < args.cpu_budget:
+            t0c = time.perf_counter()
+            oracle.decode(cm, sm, w["q"][:8], nthreads=nth)
+            dt += time.perf_counter() - t0c
+            reps += 1
+        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2) * reps
         res["cpu_baseline"] = {"value": round(by / dt / 1e9, 3), "unit": "GB/s", "cores": nth, "kind": "oracle",
                                "sample": "fp64 oracle decode of sequences 0..7 (%d cached tokens, %.1f MB of "
-                                         "bf16 K/V) in %.2f s" % (sum(L[:8]), by / 1e6, dt)}
+                                         "bf16 K/V), %d repetitions: %.1f GB in %.1f s"
+                                         % (sum(L[:8]), by / reps / 1e6, reps, by / 1e9, dt)}
     res["device_error_flags"] = cache.check()
     res["t0"], res["t1"] = t0, t1
     cache.close()
     return res
+
+
+def profiled(torch, dist, cache, step, K, flush=None):
+    """Per-kernel (launches, total ms) of K steps, each launch bracketed by
+    events on its stream."""
+    cache.profile_read()
+    cache.profile(True)
+    timed_steps(torch, dist, step, K, flush)
+    cache.profile(False)
+    return cache.profile_read()
+
+
+def tensor_roofline(flops, prof, peaks):
+    kernel = "prefill_tc" if prof["prefill_tc"][0] else "attn_simt"
+    nl, kms = prof[kernel]
+    avg = kms / max(1, nl)
+    achieved = flops / (avg / 1e3) / 1e12
+    return {"kernel": kernel, "kernel_ms": round(avg, 4), "achieved_tflops": round(achieved, 1),
+            "frac": round(achieved / peaks["bf16_tflops"], 4)}
+
+
+def bench_wide(torch, gqa, dist, args, peaks):
+    """Wide-GQA long context: B=1, H_q=48, H_kv=8, prefill T=8192, then 256
+    steps of kv_append + attn_decode (L = 8193..8448)."""
+    w = workloads.wide_gqa(workloads.seed_for(4))
+    T, H_q, H_kv, d, steps = w["n"], w["H_q"], w["H_kv"], w["d"], w["steps"]
+    per_seq = workloads.pages_for(T + steps) + 1
+    c = gqa.Cache(H_kv, d, per_seq + 4, 1, per_seq, dtype="bf16")
+    s = c.seq_create()
+    q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
+    out = torch.empty_like(q)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flops = gqa.work.prefill_flops([0], [T], H_q, d)
+
+    def pre_step():
+        gqa.attn_prefill(c, [s], q, k, v, [T], out=out)
+        gqa.kv_truncate(c, s, 0)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        pre_step()
+    ms, _, _ = timed_steps(torch, dist, pre_step, args.steps, flush)
+    pre = {"tflops_step": round(flops * args.steps / (sum(ms) / 1e3) / 1e12, 1),
+           "ms_per_step": round(sum(ms) / args.steps, 4), "gflop": round(flops / 1e9, 1)}
+    pre.update(tensor_roofline(flops, profiled(torch, dist, c, pre_step, args.steps, flush), peaks))
+
+    gqa.attn_prefill(c, [s], q, k, v, [T], out=out)
+    dq, dk, dv = to_dev(torch, w["dec_q"]), to_dev(torch, w["dec_k"]), to_dev(torch, w["dec_v"])
+    dout = torch.empty_like(dq[0])
+    kv_bytes = gqa.work.decode_kv_bytes([T + t + 1 for t in range(steps)], H_kv, d, 2)
+
+    def decode_all():
+        for t in range(steps):
+            gqa.kv_append(c, [s], dk[t], dv[t])
+            gqa.attn_decode(c, [s], dq[t], out=dout)
+        gqa.kv_truncate(c, s, T)
+
+    decode_all()
+    ms_res, _, _ = timed_steps(torch, dist, decode_all, 3)
+    t_res = sum(ms_res) / 3
+    step_ms = []
+    for t in range(steps):                          # L2 flushed before every step
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gqa.kv_append(c, [s], dk[t], dv[t])
+        gqa.attn_decode(c, [s], dq[t], out=dout)
+        b.record()
+        b.synchronize()
+        step_ms.append(a.elapsed_time(b))
+    gqa.kv_truncate(c, s, T)
+    dec = {"steps": steps, "kv_gb": round(kv_bytes / 1e9, 3),
+           "l2_resident": {"us_per_step": round(t_res / steps * 1e3, 2),
+                           "gbs": round(kv_bytes / (t_res / 1e3) / 1e9, 1)},
+           "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
+                          "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
+                          "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+           "note": "one step = kv_append + attn_decode of one sequence; 34 MB of K/V fits in L2"}
+    flags = c.check()
+    c.close()
+    return {"workload": "bf16 wide GQA: B=1, H_q=48, H_kv=8 (g=6), d_h=128, prefill T=%d, then %d append+decode "
+                        "steps (seed %d)" % (T, steps, workloads.seed_for(4)),
+            "prefill": pre, "decode": dec, "device_error_flags": flags}
+
+
+def bench_prefix(torch, gqa, dist, args, peaks):
+    """Prefix reuse and edit: one 4096-token prefix, 8 forks each prefilling
+    512 new tokens over it (P = 4096); fork 0 edited at m = 2000 (truncate +
+    re-prefill of the 2608 following tokens)."""
+    w = workloads.prefix_edit(workloads.seed_for(5))
+    P0, B, n_new, m = w["prefix"], w["B"], w["n_new"], w["m"]
+    H_q, H_kv, d = w["H_q"], w["H_kv"], w["d"]
+    per_seq = workloads.pages_for(P0 + n_new) + 1
+    pages = workloads.pages_for(P0) + B * workloads.pages_for(n_new) + workloads.pages_for(P0 + n_new) + 16
+    c = gqa.Cache(H_kv, d, pages, B + 2, per_seq, dtype="bf16")
+    root = c.seq_create()
+    gqa.attn_prefill(c, [root], to_dev(torch, w["pre_q"]), to_dev(torch, w["pre_k"]), to_dev(torch, w["pre_v"]), [P0])
+    forks = [c.seq_fork(root, P0) for _ in range(B)]
+    nq, nk, nv = to_dev(torch, w["new_q"]), to_dev(torch, w["new_k"]), to_dev(torch, w["new_v"])
+    out = torch.empty_like(nq)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flops = gqa.work.prefill_flops([P0] * B, [n_new] * B, H_q, d)
+
+    def inc_step():
+        gqa.attn_prefill(c, forks, nq, nk, nv, [n_new] * B, out=out)
+        for f in forks:
+            gqa.kv_truncate(c, f, P0)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        inc_step()
+    ms, _, _ = timed_steps(torch, dist, inc_step, args.steps, flush)
+    inc = {"tflops_step": round(flops * args.steps / (sum(ms) / 1e3) / 1e12, 1),
+           "ms_per_step": round(sum(ms) / args.steps, 4), "gflop": round(flops / 1e9, 1)}
+    inc.update(tensor_roofline(flops, profiled(torch, dist, c, inc_step, args.steps, flush), peaks))
+
+    gqa.attn_prefill(c, forks, nq, nk, nv, [n_new] * B, out=out)
+    n_re = P0 + n_new - m
+    eq, ek, ev = to_dev(torch, w["edit_q"]), to_dev(torch, w["edit_k"]), to_dev(torch, w["edit_v"])
+    eout = torch.empty_like(eq)
+    eflops = gqa.work.prefill_flops([m], [n_re], H_q, d)
+
+    def edit_step():
+        gqa.kv_truncate(c, forks[0], m)
+        gqa.attn_prefill(c, [forks[0]], eq, ek, ev, [n_re], out=eout)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        edit_step()
+    ms, _, _ = timed_steps(torch, dist, edit_step, args.steps, flush)
+    ed = {"tflops_step": round(eflops * args.steps / (sum(ms) / 1e3) / 1e12, 1),
+          "ms_per_step": round(sum(ms) / args.steps, 4), "gflop": round(eflops / 1e9, 1)}
+    ed.update(tensor_roofline(eflops, profiled(torch, dist, c, edit_step, args.steps, flush), peaks))
+    flags = c.check()
+    c.close()
+    return {"workload": "bf16 prefix reuse: a %d-token prefix shared by %d forks, each prefilling %d new tokens "
+                        "(P=%d); edit of fork 0 at m=%d: truncate + re-prefill of %d tokens (seed %d)"
+                        % (P0, B, n_new, P0, m, n_re, workloads.seed_for(5)),
+            "incremental": inc, "edit": ed, "device_error_flags": flags}
 
 
 # ---------------------------------------------------------------------------
@@ -476,6 +644,10 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode object")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (for profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--extra", action="store_true",
+                    help="also time the wide-GQA long-context and prefix-reuse/edit workloads")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of fp64 oracle work per CPU baseline (rank 0, N=1)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     dist = Dist()
@@ -491,7 +663,8 @@ def main():
         time.sleep(0.3 if clocks else 0)
         pre = None if args.no_prefill else bench_prefill(torch, gqa, dist, args, peaks, peak_src)
         dec = None if args.no_decode else bench_decode(torch, gqa, dist, args, peaks, peak_src,
-                                                       want_cpu=(dist.rank == 0 and not args.no_cpu))
+                                                       want_cpu=(dist.rank == 0 and dist.world == 1
+                                                                 and not args.no_cpu))
     finally:
         if clocks:
             clocks.stop()
@@ -507,10 +680,13 @@ def main():
                 "clocks": clocks.summary(pre["t0"], pre["t1"]),
                 "device_error_flags": pre["device_error_flags"]}
         if not args.no_cpu and dist.world == 1:
-            line["cpu_baseline"] = prefill_cpu_baseline(pre["workload"])
+            line["cpu_baseline"] = prefill_cpu_baseline(pre["workload"], args.cpu_budget)
         if dec is not None:
             dec["clocks"] = clocks.summary(dec.pop("t0"), dec.pop("t1"))
             line["decode"] = dec
+        if args.extra:
+            line["wide_gqa"] = bench_wide(torch, gqa, dist, args, peaks)
+            line["prefix_reuse"] = bench_prefix(torch, gqa, dist, args, peaks)
         print(json.dumps(line))
     dist.done()
     return 0
