@@ -503,6 +503,9 @@ def bench_wide(torch, gqa, dist, args, peaks):
     decode_all()
     ms_res, _, _ = timed_steps(torch, dist, decode_all, 3)
     t_res = sum(ms_res) / 3
+    prof = profiled(torch, dist, c, decode_all, 1)
+    kname = "decode_split" if prof["decode_split"][0] else "attn_simt"
+    k_us = prof[kname][1] / max(1, prof[kname][0]) * 1e3
     step_ms = []
     for t in range(steps):                          # L2 flushed before every step
         flush.zero_()
@@ -517,10 +520,15 @@ def bench_wide(torch, gqa, dist, args, peaks):
     dec = {"steps": steps, "kv_gb": round(kv_bytes / 1e9, 3),
            "l2_resident": {"us_per_step": round(t_res / steps * 1e3, 2),
                            "gbs": round(kv_bytes / (t_res / 1e3) / 1e9, 1)},
+           "kernel": {"name": kname, "us_per_launch": round(k_us, 2),
+                      "gbs": round(kv_bytes / steps / (k_us / 1e6) / 1e9, 1),
+                      "append_us_per_launch": round(prof["cache_write"][1] / max(1, prof["cache_write"][0]) * 1e3, 2)},
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
-           "note": "one step = kv_append + attn_decode of one sequence; 34 MB of K/V fits in L2"}
+           "note": "one step = kv_append + attn_decode of one sequence, called from Python: the step times "
+                   "include the host side of two calls, which is longer than the GPU work; 34 MB of K/V fits "
+                   "in L2; kernel = device time of the decode launch alone (L2-resident)"}
     flags = c.check()
     c.close()
     return {"workload": "bf16 wide GQA: B=1, H_q=48, H_kv=8 (g=6), d_h=128, prefill T=%d, then %d append+decode "

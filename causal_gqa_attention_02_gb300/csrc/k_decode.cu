@@ -308,30 +308,63 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     if (!s_last)
         return;
     __threadfence();
+    // The merge reads ns partials per head; with many chunks (a long
+    // sequence in a small batch) one thread walking them in turn would wait
+    // out an L2 round trip per chunk, so the loads are spread: warp w takes
+    // chunks w, w + 4, ..., lane l columns 4l..4l+3 of every head, and the
+    // four warps' sums meet in shared memory.
     const size_t stride = (size_t)H_kv * G;            // between consecutive chunks' partials
-#pragma unroll 1
-    for (int h = 0; h < G; ++h) {
-        const float *mlh = ws_ml + (((size_t)i0 * H_kv + kvh) * G + h) * 2;
-        const float *poh = ws_o + (((size_t)i0 * H_kv + kvh) * G + h) * D + e;
+    const float *ml0 = ws_ml + ((size_t)i0 * H_kv + kvh) * G * 2;
+    const float *po0 = ws_o + ((size_t)i0 * H_kv + kvh) * G * D;
+    __shared__ float sM[G], sden[kWarps][G];
+    for (int h = warp; h < G; h += kWarps) {           // M = max over chunks of m
         float M = -INFINITY;
-        for (int i = 0; i < ns; ++i)
-            M = fmaxf(M, __ldcg(mlh + i * stride * 2));
-        float den = 0.f, a0 = 0.f, a1 = 0.f;
-        int i = 0;
-        for (; i + 2 <= ns; i += 2) {
-            const float w0 = ex2(__ldcg(mlh + i * stride * 2) - M);
-            const float w1 = ex2(__ldcg(mlh + (i + 1) * stride * 2) - M);
-            den = fmaf(w0, __ldcg(mlh + i * stride * 2 + 1), den);
-            den = fmaf(w1, __ldcg(mlh + (i + 1) * stride * 2 + 1), den);
-            a0 = fmaf(w0, __ldcg(poh + (size_t)i * stride * D), a0);
-            a1 = fmaf(w1, __ldcg(poh + (size_t)(i + 1) * stride * D), a1);
+        for (int i = lane; i < ns; i += 32)
+            M = fmaxf(M, __ldcg(ml0 + (i * stride + h) * 2));
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if (lane == 0)
+            sM[h] = M;
+    }
+    __syncthreads();
+    float4 acc[G];
+    float den[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        den[h] = 0.f;
+    }
+#pragma unroll 1
+    for (int i = warp; i < ns; i += kWarps) {          // a fixed order per warp
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float2 mlv = __ldcg(reinterpret_cast<const float2 *>(ml0 + (i * stride + h) * 2));
+            const float4 o4 = __ldcg(reinterpret_cast<const float4 *>(po0 + (i * stride + h) * D) + lane);
+            const float w = ex2(mlv.x - sM[h]);
+            den[h] = fmaf(w, mlv.y, den[h]);
+            acc[h].x = fmaf(w, o4.x, acc[h].x);
+            acc[h].y = fmaf(w, o4.y, acc[h].y);
+            acc[h].z = fmaf(w, o4.z, acc[h].z);
+            acc[h].w = fmaf(w, o4.w, acc[h].w);
         }
-        if (i < ns) {
-            const float w0 = ex2(__ldcg(mlh + i * stride * 2) - M);
-            den = fmaf(w0, __ldcg(mlh + i * stride * 2 + 1), den);
-            a0 = fmaf(w0, __ldcg(poh + (size_t)i * stride * D), a0);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        *reinterpret_cast<float4 *>(&red[warp][h][4 * lane]) = acc[h];
+        if (lane == 0)
+            sden[warp][h] = den[h];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float a = 0.f, dn = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {             // warps in a fixed order
+            a += red[w][h][e];
+            dn += sden[w][h];
         }
-        out[((size_t)it.b * H_q + kvh * G + h) * D + e] = __float2bfloat16_rn((a0 + a1) / den);
+        out[((size_t)it.b * H_q + kvh * G + h) * D + e] = __float2bfloat16_rn(a / dn);
     }
     if (threadIdx.x == 0)
         counters[(size_t)it.b * H_kv + kvh] = 0;
