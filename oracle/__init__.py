@@ -25,6 +25,11 @@ Contents:
                      copy-on-write of a shared tail page, truncation), restated
                      from [P3] and the library's documented allocator rules.
   prefill()/decode()/append() drive CacheModel and attention() for a batch.
+  rope()             the rotary position mechanism ([P1] 2.3 applies "the
+                     position mechanism" to Q and K; [P3]'s prefix-caching
+                     section describes RoPE as a rotation by the position ID
+                     whose inner products depend only on position differences),
+                     and rope_stored_bf16(), the key bytes a rotating cache holds.
 
 Every function here is pinned by tests in tests/test_oracle_pins.py against
 values the pages print, closed forms, special cases and brute force.
@@ -143,6 +148,56 @@ def attention_dense(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos):
         A = E / E.sum(axis=1, keepdims=True)
         out[:, h, :] = A @ V[:, g, :]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Rotary position mechanism ([P1] 2.3: Q~, K~ are Q, K after the position
+# mechanism; [P3] prefix caching: RoPE rotates Q/K at position i by a
+# rotation fixed by the position ID, and the rotated inner product depends
+# only on the position difference).  The pages give no formula; the reading
+# here: dimension pairs (k, k + d/2), k < d/2, each rotated counter-clockwise
+# by pos * base^(-2k/d).
+# ---------------------------------------------------------------------------
+
+def rope_theta(d: int, base: float) -> np.ndarray:
+    """Frequencies base^(-2k/d), k = 0..d/2-1 (fp64)."""
+    return np.power(float(base), -2.0 * np.arange(d // 2, dtype=np.float64) / d)
+
+
+def rope(x: np.ndarray, positions, base: float) -> np.ndarray:
+    """Rotate the last axis of x [n, ..., d] (fp64) at positions [n]."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    h = d // 2
+    pos = np.asarray(positions, dtype=np.float64).reshape((-1,) + (1,) * (x.ndim - 1))
+    ang = pos * rope_theta(d, base)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def rope_stored_bf16(k_bits: np.ndarray, positions, base: float) -> np.ndarray:
+    """The bytes a rotating bf16 cache stores for keys k [n, H, d] (bf16
+    bits) at positions [n]: cos/sin of pos * theta_k rounded to fp32, each
+    product and the sum or difference rounded to fp32 (no fused
+    multiply-add), then rounded to bf16 (nearest, ties to even)."""
+    x = to_f64(k_bits, "bf16").astype(np.float32)
+    d = x.shape[-1]
+    h = d // 2
+    pos = np.asarray(positions, dtype=np.float64).reshape((-1,) + (1,) * (x.ndim - 1))
+    ang = pos * rope_theta(d, base)
+    c, s = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    x1, x2 = x[..., :h], x[..., h:]
+    y1 = (x1 * c).astype(np.float32) - (x2 * s).astype(np.float32)
+    y2 = (x1 * s).astype(np.float32) + (x2 * c).astype(np.float32)
+    return _f32_to_bf16_bits(np.concatenate([y1, y2], axis=-1).astype(np.float32))
 
 
 # ---------------------------------------------------------------------------
@@ -319,11 +374,13 @@ class CacheModel:
 # Batched drivers.
 # ---------------------------------------------------------------------------
 
-def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None):
+def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None, rope_base=None):
     """[P1] 2.6: write each sequence's valid K/V rows at positions P_b.. into
     the cache, then causal attention of the valid query rows over the cache.
     q [B, n, H_q, d], k/v [B, n, H_kv, d] stored values.  Padding rows
-    (i >= n_b) are discarded ([P1] 2.2) and returned as zeros."""
+    (i >= n_b) are discarded ([P1] 2.2) and returned as zeros.  With
+    rope_base, q and every key are rotated by their positions first (the
+    cache model keeps the unrotated keys)."""
     dt = cache.dtype
     B, n, H_q, d = q.shape
     nb = [int(x) for x in valid_lengths]
@@ -335,7 +392,10 @@ def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None):
     for b, s in enumerate(seq_ids):
         K, V = cache.kv(s)
         qpos = past[b] + np.arange(nb[b])
-        out[b, :nb[b]] = attention(to_f64(q[b, :nb[b]], dt), K, V, qpos, nthreads)
+        qb = to_f64(q[b, :nb[b]], dt)
+        if rope_base is not None:
+            qb, K = rope(qb, qpos, rope_base), rope(K, np.arange(K.shape[0]), rope_base)
+        out[b, :nb[b]] = attention(qb, K, V, qpos, nthreads)
     return out
 
 
@@ -349,9 +409,10 @@ def append(cache: CacheModel, seq_ids, k_new, v_new, counts=None):
     cache.write(list(seq_ids), [k_new[b, :cnt[b]] for b in range(B)], [v_new[b, :cnt[b]] for b in range(B)])
 
 
-def decode(cache: CacheModel, seq_ids, q, nthreads=None):
+def decode(cache: CacheModel, seq_ids, q, nthreads=None, rope_base=None):
     """[P3] single-token decode: query b at position L_b - 1 reads all L_b
-    cached entries (its own appended entry included).  q [B, H_q, d]."""
+    cached entries (its own appended entry included).  q [B, H_q, d].  With
+    rope_base, q and the keys are rotated by their positions first."""
     dt = cache.dtype
     B, H_q, d = q.shape
     out = np.zeros((B, H_q, d))
@@ -360,6 +421,9 @@ def decode(cache: CacheModel, seq_ids, q, nthreads=None):
         L = K.shape[0]
         if L < 1:
             raise CacheError("EMASK", "decode over an empty cache")
-        out[b] = attention(to_f64(q[b][None], dt), K, V, np.array([L - 1]), nthreads)[0]
+        qb = to_f64(q[b][None], dt)
+        if rope_base is not None:
+            qb, K = rope(qb, [L - 1], rope_base), rope(K, np.arange(L), rope_base)
+        out[b] = attention(qb, K, V, np.array([L - 1]), nthreads)[0]
     return out
 

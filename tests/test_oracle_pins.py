@@ -316,3 +316,114 @@ def test_bf16_inputs_are_read_exactly():
     back = oracle.to_f64(bits, "bf16")
     assert back[0] == 1.0 and back[1] == -2.5 and back[2] == 3.140625
     assert abs(back[3] - 1e-3) < 1e-3 * 2 ** -8
+
+
+# ---------------------------------------------------------------- rotary positions
+# The pages describe RoPE only in words ([P3], prefix caching): a rotation of
+# Q/K fixed by the position ID, whose inner products depend only on the
+# position difference; position 0 and equal positions leave inner products
+# unchanged.  The pins check those properties, the pairing and direction
+# read in the design doc through a second form (complex multiplication), and the
+# stored-key rounding rule against exact arithmetic.
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(1).standard_normal((4, 3, 16))
+    assert np.array_equal(oracle.rope(x, np.zeros(4), 10000.0), x)
+
+
+def test_rope_matches_complex_rotation_of_half_split_pairs():
+    rng = np.random.default_rng(2)
+    d, base = 12, 500.0
+    x = rng.standard_normal((5, 2, d))
+    pos = rng.integers(0, 4000, size=5)
+    z = x[..., : d // 2] + 1j * x[..., d // 2:]
+    w = np.exp(1j * pos[:, None, None] * base ** (-np.arange(0, d, 2) / d))
+    want = z * w
+    got = oracle.rope(x, pos, base)
+    assert np.allclose(got[..., : d // 2], want.real, rtol=0, atol=1e-12)
+    assert np.allclose(got[..., d // 2:], want.imag, rtol=0, atol=1e-12)
+
+
+def test_rope_pairs_dimension_k_with_k_plus_half():
+    e0 = np.zeros((1, 1, 8))
+    e0[..., 0] = 1.0
+    r = oracle.rope(e0, [3], 10000.0)[0, 0]
+    nz = set(np.flatnonzero(np.abs(r) > 1e-15))
+    assert nz == {0, 4}
+    assert math.isclose(r[0], math.cos(3.0), abs_tol=1e-15)      # theta_0 = 1
+    assert math.isclose(r[4], math.sin(3.0), abs_tol=1e-15)
+
+
+def test_rope_preserves_norms_and_composes():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 2, 32))
+    a, b = rng.integers(0, 3000, 6), rng.integers(0, 3000, 6)
+    r = oracle.rope(x, a, 10000.0)
+    assert np.allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-14, atol=0)
+    assert np.allclose(oracle.rope(r, b, 10000.0), oracle.rope(x, a + b, 10000.0), rtol=0, atol=1e-10)
+
+
+def test_rope_inner_products_depend_on_position_difference_only():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal((1, 1, 64)), rng.standard_normal((1, 1, 64))
+    base = 10000.0
+    ref = float(np.sum(oracle.rope(q, [700], base) * oracle.rope(k, [650], base)))
+    for shift in (1, 37, 1000, 5000):
+        val = float(np.sum(oracle.rope(q, [700 + shift], base) * oracle.rope(k, [650 + shift], base)))
+        assert abs(val - ref) <= 1e-10 * (1 + abs(ref))
+    same = float(np.sum(oracle.rope(q, [123], base) * oracle.rope(k, [123], base)))
+    assert abs(same - float(np.sum(q * k))) <= 1e-12
+
+
+def test_rope_attention_is_invariant_to_a_common_position_shift():
+    rng = np.random.default_rng(5)
+    n, H_q, H_kv, d = 9, 4, 2, 16
+    q = workloads.normal_bf16(rng, (1, n, H_q, d))
+    k = workloads.normal_bf16(rng, (1, n, H_kv, d))
+    v = workloads.normal_bf16(rng, (1, n, H_kv, d))
+    # The same rows placed at positions 0.. and at 48..: the causal mask is
+    # by relative index, the rotation by absolute position.
+    K, V = oracle.to_f64(k[0], "bf16"), oracle.to_f64(v[0], "bf16")
+    Q = oracle.to_f64(q[0], "bf16")
+    res = []
+    for p0 in (0, 48):
+        pos = p0 + np.arange(n)
+        res.append(_att(oracle.rope(Q, pos, 10000.0), oracle.rope(K, pos, 10000.0), V, np.arange(n)))
+    assert np.allclose(res[0], res[1], rtol=0, atol=1e-12)
+
+
+def test_rope_prefill_equals_rotated_definition_and_decode_last_row():
+    rng = np.random.default_rng(6)
+    n, H_q, H_kv, d, base = 7, 4, 2, 8, 10000.0
+    q = workloads.normal_bf16(rng, (1, n, H_q, d))
+    k = workloads.normal_bf16(rng, (1, n, H_kv, d))
+    v = workloads.normal_bf16(rng, (1, n, H_kv, d))
+    cm = oracle.CacheModel(4, 2, 4, H_kv, d, "bf16")
+    s = cm.create()
+    out = oracle.prefill(cm, [s], q, k, v, [n], nthreads=2, rope_base=base)
+    Q, K, V = (oracle.to_f64(a[0], "bf16") for a in (q, k, v))
+    pos = np.arange(n)
+    want = oracle.attention_dense(oracle.rope(Q, pos, base), oracle.rope(K, pos, base), V, pos)
+    assert np.allclose(out[0], want, rtol=0, atol=1e-12)
+    # decode of the last token after appending it equals the last prefill row
+    cm2 = oracle.CacheModel(4, 2, 4, H_kv, d, "bf16")
+    s2 = cm2.create()
+    oracle.prefill(cm2, [s2], q[:, : n - 1], k[:, : n - 1], v[:, : n - 1], [n - 1], nthreads=2, rope_base=base)
+    oracle.append(cm2, [s2], k[:, n - 1], v[:, n - 1])
+    dec = oracle.decode(cm2, [s2], q[:, n - 1], nthreads=2, rope_base=base)
+    assert np.allclose(dec[0], out[0, n - 1], rtol=0, atol=1e-12)
+
+
+def test_rope_stored_keys_round_to_within_one_bf16_step():
+    rng = np.random.default_rng(7)
+    k = workloads.normal_bf16(rng, (64, 2, 128))
+    pos = rng.integers(0, 8192, 64)
+    stored = oracle.rope_stored_bf16(k, pos, 10000.0)
+    exact = oracle.rope(oracle.to_f64(k, "bf16"), pos, 10000.0)
+    got = oracle.to_f64(stored, "bf16")
+    # one bf16 step at |x| is 2^(floor(log2|x|) - 7); fp32 intermediate
+    # rounding adds far less than that.
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
+    assert np.all(np.abs(got - exact) <= step * 1.0001)
+    # at position 0 the stored bytes are the input bytes
+    assert np.array_equal(oracle.rope_stored_bf16(k, np.zeros(64), 10000.0), k)
