@@ -16,6 +16,7 @@
 // finally queues its kernels.  Nothing here waits for the GPU.
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -85,6 +86,7 @@ struct gqa_cache {
     size_t ws_cap = 0;
     int32_t *d_cnt = nullptr;            // decode merge counters [B * H_kv], kept at zero
     size_t cnt_cap = 0;
+    float2 *d_rope = nullptr;            // rope = 1: (cos, sin) [max positions][d_h / 2]
     std::vector<char> h_stage;
     int device = -1;
     int num_sms = 0;
@@ -137,6 +139,7 @@ struct gqa_cache {
         pv.H_kv = desc.num_kv_heads;
         pv.d = desc.head_dim;
         pv.err = d_err;
+        pv.rope = d_rope;
         return pv;
     }
 };
@@ -396,6 +399,10 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
     if (d.layout_version != GQA_LAYOUT_VERSION)
         return fail(GQA_ELAYOUT, "layout_version %d, this library writes %d", d.layout_version,
                     GQA_LAYOUT_VERSION);
+    if (d.rope != 0 && d.rope != 1)
+        return fail(GQA_EINVAL, "rope must be 0 (none) or 1 (rotary)");
+    if (d.rope == 1 && (d.head_dim % 2 != 0 || !(d.rope_base > 1.0f) || !std::isfinite(d.rope_base)))
+        return fail(GQA_EINVAL, "rope = 1 needs an even d_h and a finite rope_base > 1");
     const size_t need = gqa_pool_bytes(desc);
     if (pool_dev) {
         if (pool_bytes < need)
@@ -452,6 +459,24 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
             e = cudaMemset(c->d_err, 0, sizeof(int32_t));
         if (e == cudaSuccess)
             e = cudaMemset(pool_dev, 0, need);         // every slot starts as a finite +0
+        if (e == cudaSuccess && d.rope == 1) {
+            // cos/sin of pos * base^(-2e/d_h) for every position a sequence
+            // can reach, in fp64, rounded to fp32 once.
+            const int half = d.head_dim / 2;
+            const size_t npos = (size_t)d.max_pages_per_seq * kPageTokens;
+            std::vector<float2> tab(npos * half);
+            std::vector<double> theta(half);
+            for (int i = 0; i < half; ++i)
+                theta[i] = std::pow((double)d.rope_base, -2.0 * i / d.head_dim);
+            for (size_t p = 0; p < npos; ++p)
+                for (int i = 0; i < half; ++i) {
+                    const double a = (double)p * theta[i];
+                    tab[p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+                }
+            e = cudaMalloc((void **)&c->d_rope, tab.size() * sizeof(float2));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(c->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+        }
         if (e == cudaSuccess)
             e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
@@ -475,6 +500,7 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_stage) cudaFree(c->d_stage);
         if (c->d_ws) cudaFree(c->d_ws);
         if (c->d_cnt) cudaFree(c->d_cnt);
+        if (c->d_rope) cudaFree(c->d_rope);
         for (const auto &r : c->prof_recs) {
             cudaEventDestroy(r.start);
             cudaEventDestroy(r.end);
@@ -496,6 +522,8 @@ int gqa_cache_layout(const gqa_cache *c, gqa_layout_metadata *out)
     out->layout_version = c->desc.layout_version;
     out->num_kv_heads = c->desc.num_kv_heads;
     out->head_dim = c->desc.head_dim;
+    out->rope = c->desc.rope;
+    out->rope_base = c->desc.rope == 1 ? c->desc.rope_base : 0.0f;
     return GQA_OK;
 }
 
@@ -508,6 +536,8 @@ int gqa_layout_compatible(const gqa_layout_metadata *a, const gqa_layout_metadat
     if (a->dtype != b->dtype || a->page_tokens != b->page_tokens || a->layout_version != b->layout_version ||
         a->num_kv_heads != b->num_kv_heads || a->head_dim != b->head_dim)
         return fail(GQA_ELAYOUT, "precision, page size, layout version or KV shape differs");
+    if (a->rope != b->rope || (a->rope == 1 && a->rope_base != b->rope_base))
+        return fail(GQA_ELAYOUT, "the keys were rotated with a different position mechanism");
     return GQA_OK;
 }
 

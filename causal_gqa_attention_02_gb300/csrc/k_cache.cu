@@ -11,6 +11,8 @@
 // widest unit (up to 16 bytes) that the row size and base addresses allow,
 // consecutive threads taking consecutive units of one row so that both the
 // read and the write are coalesced.
+#include <cuda_bf16.h>
+
 #include "kernels.cuh"
 
 namespace gqa {
@@ -31,6 +33,42 @@ template <> struct Unit<8>  { using T = uint2; };
 template <> struct Unit<4>  { using T = uint32_t; };
 template <> struct Unit<2>  { using T = uint16_t; };
 template <> struct Unit<1>  { using T = uint8_t; };
+
+// Rotary position mechanism on one unit of a key row: `own` holds elements
+// of one half of the row, `oth` the same elements of the other half; `first`
+// says which half `own` is.  Pair (x, y) = (first half, second half) becomes
+// (x*c - y*s, x*s + y*c), each product, difference and sum rounded to fp32
+// (no fused multiply-add), then to the element type.
+template <int U>
+__device__ __forceinline__ typename Unit<U>::T rope_unit(typename Unit<U>::T own, typename Unit<U>::T oth, bool first,
+                                                         const float2 *__restrict__ cs, int esize)
+{
+    typename Unit<U>::T res = own;
+    if (esize == 2 && U >= 2) {
+        const __nv_bfloat16 *a = reinterpret_cast<const __nv_bfloat16 *>(&own);
+        const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&oth);
+        __nv_bfloat16 *r = reinterpret_cast<__nv_bfloat16 *>(&res);
+#pragma unroll
+        for (int j = 0; j < U / 2; ++j) {
+            const float x = __bfloat162float(first ? a[j] : b[j]), y = __bfloat162float(first ? b[j] : a[j]);
+            const float2 t = cs[j];
+            const float o = first ? __fsub_rn(__fmul_rn(x, t.x), __fmul_rn(y, t.y))
+                                  : __fadd_rn(__fmul_rn(x, t.y), __fmul_rn(y, t.x));
+            r[j] = __float2bfloat16_rn(o);
+        }
+    } else if (esize == 4 && U >= 4) {
+        const float *a = reinterpret_cast<const float *>(&own);
+        const float *b = reinterpret_cast<const float *>(&oth);
+        float *r = reinterpret_cast<float *>(&res);
+#pragma unroll
+        for (int j = 0; j < U / 4; ++j) {
+            const float x = first ? a[j] : b[j], y = first ? b[j] : a[j];
+            const float2 t = cs[j];
+            r[j] = first ? __fsub_rn(__fmul_rn(x, t.x), __fmul_rn(y, t.y)) : __fadd_rn(__fmul_rn(x, t.y), __fmul_rn(y, t.x));
+        }
+    }
+    return res;
+}
 
 // grid: (x = token blocks, y = batch entry); one warp per token.  A token's
 // K rows for all KV heads are contiguous in k (H_kv * d * esize bytes), so a
@@ -68,14 +106,20 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
         const int slot = pos % kPageTokens;
         char *kd = (char *)pv.pool + (size_t)page * 2 * pv.H_kv * blk_bytes;
         char *vd = kd + (size_t)pv.H_kv * blk_bytes;
+        const int half_units = cpr / 2;                   // with rotation: units of half a row
         for (int u0 = 0; u0 < units; u0 += 32 * kMaxPerLane) {
-            T kr[kMaxPerLane], vr[kMaxPerLane];
+            T kr[kMaxPerLane], vr[kMaxPerLane], kp[kMaxPerLane];
 #pragma unroll
             for (int i = 0; i < kMaxPerLane; ++i) {
                 const int u = u0 + 32 * i + lane;
                 if (u < units) {
                     kr[i] = *(const T *)(k + src_off + (size_t)u * U);
                     vr[i] = *(const T *)(v + src_off + (size_t)u * U);
+                    if (pv.rope) {                        // the same unit of the other half
+                        const int c = u % cpr;
+                        const int pu = u + (c < half_units ? half_units : -half_units);
+                        kp[i] = *(const T *)(k + src_off + (size_t)pu * U);
+                    }
                 }
             }
 #pragma unroll
@@ -84,7 +128,13 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
                 if (u < units) {
                     const int hh = u / cpr, c = u - hh * cpr;
                     const size_t off = (size_t)hh * blk_bytes + pool_in_block(chunks, slot, c * U);
-                    *(T *)(kd + off) = kr[i];
+                    T kw = kr[i];
+                    if (pv.rope) {
+                        const bool first = c < half_units;
+                        const int pair0 = (first ? c : c - half_units) * (U / esize);
+                        kw = rope_unit<U>(kr[i], kp[i], first, pv.rope + (size_t)pos * (pv.d / 2) + pair0, esize);
+                    }
+                    *(T *)(kd + off) = kw;
                     *(T *)(vd + off) = vr[i];
                 }
             }
@@ -136,8 +186,12 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     if (B <= 0 || rows <= 0)
         return cudaSuccess;
     const size_t row_bytes = (size_t)pv.d * esize;
-    const int U = copy_unit_bytes(row_bytes, k, v, pv.pool);
+    // With rotation a unit must lie within one half of the row and hold
+    // whole elements.
+    const int U = copy_unit_bytes(pv.rope ? row_bytes / 2 : row_bytes, k, v, pv.pool);
     if (zero_out && (zero_row_bytes % 16 != 0 || (uintptr_t)zero_out % 16 != 0))
+        return cudaErrorInvalidValue;
+    if (pv.rope && U < esize)
         return cudaErrorInvalidValue;
     const int wpb = 8;
     int blocks = (rows + wpb - 1) / wpb;

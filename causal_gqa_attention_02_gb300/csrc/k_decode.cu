@@ -122,6 +122,31 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         for (int u = 0; u < 4; ++u)
             qr[h][u] = make_float2(bf_lo(w[u]) * qscale, bf_hi(w[u]) * qscale);
     }
+    if (pv.rope) {
+        // Rotate q by its position L - 1: column c pairs with c + 64, held by
+        // lane ^ 8 at the same register.
+        const float4 *cs4 = reinterpret_cast<const float4 *>(pv.rope + (size_t)sd.past * (D / 2) + 8 * (lane & 7));
+        const bool first = (lane & 8) == 0;
+        float2 cs[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 t = cs4[j];
+            cs[2 * j] = make_float2(t.x, t.y);
+            cs[2 * j + 1] = make_float2(t.z, t.w);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float ox = __shfl_xor_sync(0xffffffffu, qr[h][u].x, 8);
+                const float oy = __shfl_xor_sync(0xffffffffu, qr[h][u].y, 8);
+                const float2 c0 = cs[2 * u], c1 = cs[2 * u + 1];
+                if (first)
+                    qr[h][u] = make_float2(qr[h][u].x * c0.x - ox * c0.y, qr[h][u].y * c1.x - oy * c1.y);
+                else
+                    qr[h][u] = make_float2(ox * c0.y + qr[h][u].x * c0.x, oy * c1.y + qr[h][u].y * c1.x);
+            }
+    }
 
     // ---- K pass: scores of the chunk -------------------------------------
     for (int pg = warp; pg < npages; pg += kWarps) {

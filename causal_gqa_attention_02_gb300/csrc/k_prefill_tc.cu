@@ -101,7 +101,7 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 k[kKStages][2][128 * 64];
     __nv_bfloat16 v[kVStages][2][128 * 64];
     __nv_bfloat16 o[2][128 * 64];                      // epilogue staging, one column half per query tile
-    uint64_t bar_q, q_empty;
+    uint64_t bar_q, q_empty, q_rot;
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
@@ -126,6 +126,7 @@ struct TcParams {
     __nv_bfloat16 *out; // [B, n, H_q, 128]
     int32_t *err;
     float scale_log2;   // log2(e) / sqrt(d_h)
+    const float2 *rope; // rotary (cos, sin) [position][64], or null
 };
 
 __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
@@ -166,6 +167,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         s.abort_ = 0;
         s.s_issued[0] = s.s_issued[1] = 0;
         mbar_init(&s.bar_q, 1);
+        mbar_init(&s.q_rot, 8);                        // rotary: the 8 softmax warps, per item
         mbar_init(&s.q_empty, 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&s.k_full[i], 1);
@@ -355,7 +357,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     for (int j = 0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
                         ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
-                             (j > 0 || mbar_wait(&s.bar_q, k & 1, &s.abort_)) &&
+                             (j > 0 || mbar_wait(p.rope ? &s.q_rot : &s.bar_q, k & 1, &s.abort_)) &&
                              mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
                         if (!ok)
                             break;
@@ -442,6 +444,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
             const bool valid = row_in_box && rel < sd.count;
             const int qpos = sd.past + rel;             // absolute position: sees keys 0..qpos
+            if (p.rope) {
+                // Rotate this thread's row of the item's Q tile in place, once
+                // Q has landed; the S issuer waits for all eight warps.  Pair
+                // (e, e + 64) sits at the same swizzled offset of the two
+                // column halves.  Rows without a valid position stay as they
+                // are (their outputs are discarded).
+                if (!mbar_wait(&s.bar_q, k & 1, &s.abort_)) {
+                    ok = false;
+                    break;
+                }
+                if (valid) {
+                    unsigned char *h0 = reinterpret_cast<unsigned char *>(s.q[t][0]) + r * 128;
+                    unsigned char *h1 = reinterpret_cast<unsigned char *>(s.q[t][1]) + r * 128;
+                    const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope + (size_t)qpos * (D / 2));
+#pragma unroll 2
+                    for (int cch = 0; cch < 8; ++cch) {
+                        const int off = (cch ^ (r & 7)) << 4;
+                        uint4 a = *reinterpret_cast<const uint4 *>(h0 + off);
+                        uint4 b = *reinterpret_cast<const uint4 *>(h1 + off);
+                        uint32_t *aw = reinterpret_cast<uint32_t *>(&a), *bw = reinterpret_cast<uint32_t *>(&b);
+#pragma unroll
+                        for (int w2 = 0; w2 < 4; ++w2) {      // elements 8*cch + 2*w2, +1
+                            const float4 c = cs4[4 * cch + w2];   // (cos, sin) of both elements
+                            const float x0 = __uint_as_float(aw[w2] << 16), x1 = __uint_as_float(aw[w2] & 0xffff0000u);
+                            const float y0 = __uint_as_float(bw[w2] << 16), y1 = __uint_as_float(bw[w2] & 0xffff0000u);
+                            aw[w2] = pack_bf16x2(x0 * c.x - y0 * c.y, x1 * c.z - y1 * c.w);
+                            bw[w2] = pack_bf16x2(x0 * c.y + y0 * c.x, x1 * c.w + y1 * c.z);
+                        }
+                        *reinterpret_cast<uint4 *>(h0 + off) = a;
+                        *reinterpret_cast<uint4 *>(h1 + off) = b;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s.q_rot);
+            }
             float m = -INFINITY, l = 0.0f;
             for (int j = 0; j < nt; ++j) {
                 const uint32_t g = gt + j;
@@ -671,6 +710,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.out = (__nv_bfloat16 *)out;
     prm.err = pv.err;
     prm.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    prm.rope = pv.rope;
     const int smem = (int)sizeof(TcSmem) + 1024;
     static bool attr_set = false;
     if (!attr_set) {

@@ -70,6 +70,16 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
     for (int e = lane; e < d; e += 32)
         qs[e] = ldf(qi + e);
     __syncwarp();
+    if (pv.rope) {                                // rotate q by its position, pairs (e, e + d/2)
+        const float2 *cs = pv.rope + (size_t)(sd.past + i) * (d / 2);
+        for (int e = lane; e < d / 2; e += 32) {
+            const float x = qs[e], y = qs[e + d / 2];
+            const float2 t = cs[e];
+            qs[e] = x * t.x - y * t.y;
+            qs[e + d / 2] = x * t.y + y * t.x;
+        }
+        __syncwarp();
+    }
 
     const float root_d = sqrtf((float)d);
     const int pos = sd.past + i;                  // visible keys 0..pos

@@ -37,6 +37,7 @@ struct PoolView {
     int32_t H_kv;
     int32_t d;
     int32_t *err;            // device error word (GQA_DEVERR_* bits)
+    const float2 *rope;      // rotary table (cos, sin) [position][d / 2], or null: no rotation
 };
 
 // One batch entry of a launching call.

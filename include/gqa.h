@@ -110,6 +110,14 @@ typedef struct {
     const int32_t *page_order;   /* host, optional: permutation of 0..num_pages-1 giving the
                                     order in which free pages are handed out (NULL = identity).
                                     Copied; the caller keeps ownership.                      */
+    int32_t rope;                /* position mechanism applied by the library ([P1] 2.3: Q~, K~
+                                    are Q, K after it; [P3]: RoPE rotates Q/K by the position
+                                    ID): 0 = none, q/k arrive already transformed; 1 = rotary:
+                                    dimension pairs (e, e + d_h/2), e < d_h/2, rotated
+                                    counter-clockwise by pos * rope_base^(-2e/d_h).  Keys are
+                                    rotated when written (the cache holds post-position keys),
+                                    queries inside the attention kernels.                     */
+    float rope_base;             /* rope = 1: the frequency base, > 1 (e.g. 10000)           */
 } gqa_cache_desc;
 
 /* layout_metadata of [P1] 2.5 / invariant 2.2 item 5. */
@@ -120,6 +128,8 @@ typedef struct {
     int32_t layout_version;
     int32_t num_kv_heads;
     int32_t head_dim;
+    int32_t rope;                /* the cache's position mechanism (keys were rotated with it) */
+    float rope_base;
 } gqa_layout_metadata;
 
 typedef struct gqa_cache gqa_cache;
@@ -140,7 +150,11 @@ size_t gqa_pool_bytes(const gqa_cache_desc *desc);
  * tables and lengths exactly as they would on a device cache, but queue no
  * GPU work and write no outputs.  It exists so the host-side allocator can be
  * exercised without a GPU.
- * Errors: GQA_EINVAL (bad description, pool too small, misaligned),
+ * With rope = 1 the library also allocates a cos/sin table of
+ * max_pages_per_seq * 16 positions x d_h/2 frequencies (fp32, computed in
+ * fp64 on the host).
+ * Errors: GQA_EINVAL (bad description, pool too small, misaligned; rope not
+ *         0/1, or rope = 1 with an odd d_h or rope_base <= 1),
  *         GQA_ELAYOUT (keys_post_position != 1 or unknown layout_version),
  *         GQA_ECUDA. */
 int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes,
@@ -192,13 +206,17 @@ int gqa_page_refcount(const gqa_cache *cache, int32_t page, int32_t *out);
  * For each batch entry b, with sequence s = seq_ids[b] of current length P_b
  * and n_b = valid_lengths[b] valid (right-aligned padding) rows:
  *  1. the K/V rows i < n_b are written to the cache at positions P_b + i,
- *     bit for bit; padding rows are never written ([P1] 2.6; invariant 2.2
- *     item 4);
+ *     bit for bit (with rope = 1, K is rotated by position P_b + i first:
+ *     each pair (x, y) becomes (x*c - y*s, x*s + y*c), every product, sum and
+ *     difference rounded to fp32, then rounded to the cache type; c, s are
+ *     the fp32 cos/sin of the table); padding rows are never written ([P1]
+ *     2.6; invariant 2.2 item 4);
  *  2. for every query head h and valid row i, with g(h) = floor(h*H_kv/H_q)
  *     ([P1] 2.3), the output is softmax over the finite scores
- *     <q[b,i,h], K[s, j, g(h)]> / sqrt(d_h), j = 0 .. P_b + i, applied to V:
- *     the old prefix is fully visible and the new block is lower-triangular
- *     ([P3] incremental prefill);
+ *     <q[b,i,h], K[s, j, g(h)]> / sqrt(d_h), j = 0 .. P_b + i, applied to V
+ *     (with rope = 1, q rotated by its position P_b + i): the old prefix is
+ *     fully visible and the new block is lower-triangular ([P3] incremental
+ *     prefill);
  *  3. padding rows i >= n_b of `out` are written as zeros (they are
  *     discarded, [P1] 2.2);
  *  4. the sequence's length becomes P_b + n_b.
@@ -208,7 +226,8 @@ int gqa_page_refcount(const gqa_cache *cache, int32_t page, int32_t *out);
  *  n              padded rows per batch entry (>= 1).
  *  H_q            query heads; H_kv must divide it ([P1] 2.3).
  *  q              device [B, n, H_q, d_h]      (read)
- *  k, v           device [B, n, H_kv, d_h]     (read; post-position keys)
+ *  k, v           device [B, n, H_kv, d_h]     (read; post-position keys when
+ *                 rope = 0, keys before the rotation when rope = 1)
  *  valid_lengths  host int32[B], 1 <= n_b <= n.
  *  positions      host int32[B, n] or NULL.  When given, positions[b, i]
  *                 must equal P_b + i for every valid row: positions continue
@@ -226,7 +245,8 @@ int attn_prefill(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
 
 /* Append new K/V rows at each sequence's tail without attention ([P3]
  * decode: append the step's k_t, v_t after the old cache; [P1] 2.6 cache
- * write).  Row c < counts[b] of entry b goes to position P_b + c.
+ * write).  Row c < counts[b] of entry b goes to position P_b + c (with
+ * rope = 1 its key is rotated by P_b + c as in attn_prefill step 1).
  *  seq_ids  host int32[B], distinct live sequences.
  *  n        rows per entry in k_new/v_new (1 for a decode step).
  *  counts   host int32[B] with 0 <= counts[b] <= n, or NULL (= n for all).
@@ -240,7 +260,8 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
  * L_b - 1 of sequence seq_ids[b] (L_b = its current length, which includes
  * the entry appended for this step) and attends over all L_b cached tokens
  * through the sequence's block table:
- *      out[b, h, :] = sum_t softmax_t(<q[b,h], K[t, g(h)]>/sqrt(d_h)) V[t, g(h)].
+ *      out[b, h, :] = sum_t softmax_t(<q[b,h], K[t, g(h)]>/sqrt(d_h)) V[t, g(h)]
+ * (with rope = 1, q rotated by L_b - 1).
  *  seq_ids  host int32[B], live sequences of length >= 1 (repeats allowed).
  *  q        device [B, H_q, d_h];  out  device [B, H_q, d_h].
  * Split-K partials and merge counters live in library-owned device memory that grows with

@@ -193,6 +193,28 @@ def test_layout_metadata_and_compatibility():
     assert e.value.name == "ELAYOUT"
 
 
+def test_rope_description_checks_and_layout():
+    m = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, rope=True, rope_base=500.0).layout()
+    assert m.rope == 1 and m.rope_base == 500.0
+    plain = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True).layout()
+    assert plain.rope == 0
+    assert not gqa.layout_compatible(m, plain)
+    other = gqa.LayoutMetadata(**m.as_dict())
+    other.rope_base = 10000.0
+    assert not gqa.layout_compatible(m, other)
+    assert gqa.layout_compatible(m, gqa.LayoutMetadata(**m.as_dict()))
+    for kw in ({"head_dim": 7}, {"rope_base": 1.0}, {"rope_base": 0.5}, {"rope_base": float("inf")}):
+        args = dict(num_kv_heads=2, head_dim=8, num_pages=8, max_seqs=2, max_pages_per_seq=2, dtype="bf16",
+                    metadata_only=True, rope=True, rope_base=10000.0)
+        args.update(kw)
+        with pytest.raises(gqa.GqaError) as e:
+            gqa.Cache(**args)
+        assert e.value.name == "EINVAL", kw
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, rope=2)
+    assert e.value.name == "EINVAL"
+
+
 def test_page_order_must_be_a_permutation():
     with pytest.raises(gqa.GqaError) as e:
         gqa.Cache(1, 4, 4, 2, 2, dtype="f32", metadata_only=True, page_order=[0, 1, 1, 2])
