@@ -247,7 +247,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     nb = [int(x) for x in w["valid_lengths"]]
     flops = gqa.work.prefill_flops([0] * B, nb, H_q, d)
     pages = sum(workloads.pages_for(x) for x in nb) + 16
-    cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16")
+    cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16", rope=args.rope)
     ids = [cache.seq_create() for _ in range(B)]
     q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
     out = torch.empty_like(q)
@@ -340,6 +340,8 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
            "global_batch": B * dist.world, "seq_len": n, "parallelism": "replicas x%d" % dist.world,
            "l2": "flushed (512 MiB write, untimed) before every timed step",
            "causal_gflop_per_step": round(flops / 1e9, 3)}
+    if args.rope:
+        cfg["position_mechanism"] = "rotary (base 10000), applied inside the library: keys at write, queries in-kernel"
     return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
             "gpu_launches": gpu_launches, "kernels": kernels, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
             "workload": w}
@@ -350,7 +352,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
     L = [int(x) for x in w["lengths"]]
     kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, 2)
-    cache = gqa.Cache(H_kv, d, w["num_pages"], B, workloads.pages_for(max(L)) + 1, dtype="bf16",
+    cache = gqa.Cache(H_kv, d, w["num_pages"], B, workloads.pages_for(max(L)) + 1, dtype="bf16", rope=args.rope,
                       page_order=w["page_order"])
     ids = [cache.seq_create() for _ in range(B)]
     for b in range(B):
@@ -419,6 +421,8 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                                   % (B, H_q, H_kv, d, workloads.seed_for(3), sum(L)),
                       "l2": "not flushed: %.2f GB of K/V per step exceeds the 129 MB L2" % (kv_bytes / 1e9),
                       "kv_bytes_per_step": kv_bytes}}
+    if args.rope:
+        res["config"]["position_mechanism"] = "rotary (base 10000): queries rotated in-kernel"
     if want_cpu:
         import oracle
         nth = oracle.default_threads()
@@ -652,6 +656,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode object")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (for profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--rope", action="store_true",
+                    help="caches with the rotary position mechanism applied by the library")
     ap.add_argument("--extra", action="store_true",
                     help="also time the wide-GQA long-context and prefix-reuse/edit workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

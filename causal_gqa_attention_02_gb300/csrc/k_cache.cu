@@ -78,13 +78,13 @@ __device__ __forceinline__ typename Unit<U>::T rope_unit(typename Unit<U>::T own
 // token is loaded before any is stored, to keep the loads in flight.
 // With zero_out != nullptr the same grid also writes zeros over the padding
 // rows count..n-1 of zero_out ([B, n, zero_row_bytes]).
-template <int U>
+template <int U, bool ROPE>
 __global__ void __launch_bounds__(256)
 cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int n, const char *__restrict__ k,
                    const char *__restrict__ v, char *__restrict__ zero_out, int zero_row_bytes)
 {
     using T = typename Unit<U>::T;
-    constexpr int kMaxPerLane = 8;                      // units per lane held in registers per pass
+    constexpr int kMaxPerLane = ROPE ? 4 : 8;           // units per lane held in registers per pass
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
@@ -94,8 +94,17 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
     const int chunks = pool_chunks(row_bytes);
     const size_t blk_bytes = pool_block_bytes(row_bytes);
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
+    // Rotation: the token's row of the cos/sin table, shared by all its KV
+    // heads, staged once per token in this warp's slice of shared memory.
+    __shared__ float2 s_cs[ROPE ? 8 : 1][ROPE ? 128 : 1];
     for (int t = blockIdx.x * wpb + warp; t < sd.count; t += gridDim.x * wpb) {
         const int pos = sd.past + t;
+        if (ROPE) {
+            __syncwarp();
+            for (int e = lane; e < pv.d / 2; e += 32)
+                s_cs[warp][e] = pv.rope[(size_t)pos * (pv.d / 2) + e];
+            __syncwarp();
+        }
         const int page = tab[pos / kPageTokens];
         if ((unsigned)page >= (unsigned)pv.num_pages) {
             if (lane == 0)
@@ -115,7 +124,7 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
                 if (u < units) {
                     kr[i] = *(const T *)(k + src_off + (size_t)u * U);
                     vr[i] = *(const T *)(v + src_off + (size_t)u * U);
-                    if (pv.rope) {                        // the same unit of the other half
+                    if (ROPE) {                           // the same unit of the other half
                         const int c = u % cpr;
                         const int pu = u + (c < half_units ? half_units : -half_units);
                         kp[i] = *(const T *)(k + src_off + (size_t)pu * U);
@@ -129,10 +138,10 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
                     const int hh = u / cpr, c = u - hh * cpr;
                     const size_t off = (size_t)hh * blk_bytes + pool_in_block(chunks, slot, c * U);
                     T kw = kr[i];
-                    if (pv.rope) {
+                    if (ROPE) {
                         const bool first = c < half_units;
                         const int pair0 = (first ? c : c - half_units) * (U / esize);
-                        kw = rope_unit<U>(kr[i], kp[i], first, pv.rope + (size_t)pos * (pv.d / 2) + pair0, esize);
+                        kw = rope_unit<U>(kr[i], kp[i], first, &s_cs[warp][pair0], esize);
                     }
                     *(T *)(kd + off) = kw;
                     *(T *)(vd + off) = vr[i];
@@ -193,20 +202,28 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
         return cudaErrorInvalidValue;
     if (pv.rope && U < esize)
         return cudaErrorInvalidValue;
-    const int wpb = 8;
+    const int wpb = 8;                                  // at most 8: the rotation's table rows
     int blocks = (rows + wpb - 1) / wpb;
     if (blocks > 1024)
         blocks = 1024;
     dim3 grid((unsigned)blocks, (unsigned)B);
     const char *kc = (const char *)k, *vc = (const char *)v;
     char *z = (char *)zero_out;
+    // The rotating kernel is a separate instantiation, so that a cache without
+    // the position mechanism runs the plain copy.
+#define GQA_CACHE_WRITE(UU)                                                                                    \
+    (pv.rope ? (cache_write_kernel<UU, true><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,       \
+                                                                       zero_row_bytes), 0)                    \
+             : (cache_write_kernel<UU, false><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,      \
+                                                                        zero_row_bytes), 0))
     switch (U) {
-    case 16: cache_write_kernel<16><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
-    case 8:  cache_write_kernel<8><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
-    case 4:  cache_write_kernel<4><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
-    case 2:  cache_write_kernel<2><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
-    default: cache_write_kernel<1><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z, zero_row_bytes); break;
+    case 16: GQA_CACHE_WRITE(16); break;
+    case 8:  GQA_CACHE_WRITE(8); break;
+    case 4:  GQA_CACHE_WRITE(4); break;
+    case 2:  GQA_CACHE_WRITE(2); break;
+    default: GQA_CACHE_WRITE(1); break;
     }
+#undef GQA_CACHE_WRITE
     return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ __device__ __forceinline__ float2 bf2(uint32_t x) { return make_float2(bf_lo(x),
 // Lane layout for both passes over a 16-token page: lane l covers tokens
 // 2i + l/16 (i = 0..7) and columns 8(l%16)..8(l%16)+7, so one 16-byte load
 // per lane reads two whole 256-byte token rows: 512 contiguous bytes.
-template <int G>
+template <int G, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeItem *__restrict__ items,
                     const int32_t *__restrict__ item_start, int chunk, int H_q,
@@ -122,7 +122,7 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         for (int u = 0; u < 4; ++u)
             qr[h][u] = make_float2(bf_lo(w[u]) * qscale, bf_hi(w[u]) * qscale);
     }
-    if (pv.rope) {
+    if (ROPE) {
         // Rotate q by its position L - 1: column c pairs with c + 64, held by
         // lane ^ 8 at the same register.
         const float4 *cs4 = reinterpret_cast<const float4 *>(pv.rope + (size_t)sd.past * (D / 2) + 8 * (lane & 7));
@@ -399,9 +399,16 @@ template <int G>
 cudaError_t launch_g(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st)
 {
     dim3 grid((unsigned)a.n_items, (unsigned)pv.H_kv);
-    decode_split_kernel<G><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q,
-                                                        (const __nv_bfloat16 *)a.q, a.ws_o, a.ws_ml, a.counters,
-                                                        (__nv_bfloat16 *)a.out);
+    // The rotating kernel is a separate instantiation, so that a cache
+    // without the position mechanism runs the plain one.
+    if (pv.rope)
+        decode_split_kernel<G, true><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q,
+                                                                  (const __nv_bfloat16 *)a.q, a.ws_o, a.ws_ml,
+                                                                  a.counters, (__nv_bfloat16 *)a.out);
+    else
+        decode_split_kernel<G, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
+                                                                   a.H_q, (const __nv_bfloat16 *)a.q, a.ws_o,
+                                                                   a.ws_ml, a.counters, (__nv_bfloat16 *)a.out);
     return cudaGetLastError();
 }
 

@@ -101,7 +101,7 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 k[kKStages][2][128 * 64];
     __nv_bfloat16 v[kVStages][2][128 * 64];
     __nv_bfloat16 o[2][128 * 64];                      // epilogue staging, one column half per query tile
-    uint64_t bar_q, q_empty, q_rot;
+    uint64_t bar_q, q_empty, q_rot[2];
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
@@ -167,7 +167,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         s.abort_ = 0;
         s.s_issued[0] = s.s_issued[1] = 0;
         mbar_init(&s.bar_q, 1);
-        mbar_init(&s.q_rot, 8);                        // rotary: the 8 softmax warps, per item
+        mbar_init(&s.q_rot[0], 4);                     // rotary: a tile's 4 softmax warps, per item
+        mbar_init(&s.q_rot[1], 4);
         mbar_init(&s.q_empty, 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&s.k_full[i], 1);
@@ -357,7 +358,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     for (int j = 0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
                         ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
-                             (j > 0 || mbar_wait(p.rope ? &s.q_rot : &s.bar_q, k & 1, &s.abort_)) &&
+                             (j > 0 || mbar_wait(p.rope ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
                              mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
                         if (!ok)
                             break;
@@ -365,7 +366,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         issue_s(0, st);
                         mma_commit(&s.s_full[0]);
                         *(volatile int *)&s.s_issued[0] = (int)g + 1;
-                        ok = mbar_wait(&s.s_free, 0, &s.abort_);
+                        ok = mbar_wait(&s.s_free, 0, &s.abort_) &&
+                             (j > 0 || !p.rope || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
                         if (!ok)
                             break;
                         tc_fence_after();
@@ -436,51 +438,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         uint32_t gt = 0;
         int k = 0;
         bool ok = true;
-        for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-            const TcItem it = p.items[idx];
-            const SeqDesc sd = p.seqs[it.b];
-            const int nt = it.nt;
-            const bool row_in_box = r < p.G * p.rows_pos;
-            const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
-            const bool valid = row_in_box && rel < sd.count;
-            const int qpos = sd.past + rel;             // absolute position: sees keys 0..qpos
-            if (p.rope) {
-                // Rotate this thread's row of the item's Q tile in place, once
-                // Q has landed; the S issuer waits for all eight warps.  Pair
-                // (e, e + 64) sits at the same swizzled offset of the two
-                // column halves.  Rows without a valid position stay as they
-                // are (their outputs are discarded).
-                if (!mbar_wait(&s.bar_q, k & 1, &s.abort_)) {
-                    ok = false;
-                    break;
-                }
-                if (valid) {
-                    unsigned char *h0 = reinterpret_cast<unsigned char *>(s.q[t][0]) + r * 128;
-                    unsigned char *h1 = reinterpret_cast<unsigned char *>(s.q[t][1]) + r * 128;
-                    const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope + (size_t)qpos * (D / 2));
-#pragma unroll 2
-                    for (int cch = 0; cch < 8; ++cch) {
-                        const int off = (cch ^ (r & 7)) << 4;
-                        uint4 a = *reinterpret_cast<const uint4 *>(h0 + off);
-                        uint4 b = *reinterpret_cast<const uint4 *>(h1 + off);
-                        uint32_t *aw = reinterpret_cast<uint32_t *>(&a), *bw = reinterpret_cast<uint32_t *>(&b);
+        // Rotary mechanism: rotate this thread's row of an item's Q tile in
+        // place once the tile has landed; the S issuer waits for all eight
+        // warps.  Pair (e, e + 64) sits at the same swizzled offset of the
+        // two column halves.  Rows without a valid position stay as they are
+        // (their outputs are discarded).  Done for the next item right after
+        // this item's last softmax, so the next item's first S overlaps the
+        // epilogue.
+        auto rotate_q = [&](const TcItem &iq, uint32_t parity) -> bool {
+            const SeqDesc sq = p.seqs[iq.b];
+            const int relq = iq.i0 + t * p.rows_pos + r / p.G;
+            if (!mbar_wait(&s.bar_q, parity, &s.abort_))
+                return false;
+            if (r < p.G * p.rows_pos && relq < sq.count) {
+                unsigned char *h0 = reinterpret_cast<unsigned char *>(s.q[t][0]) + r * 128;
+                unsigned char *h1 = reinterpret_cast<unsigned char *>(s.q[t][1]) + r * 128;
+                const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope + (size_t)(sq.past + relq) * (D / 2));
+                // Two rounds of four 16-byte chunks: every table load of a
+                // round is issued before any shared-memory store (read-only
+                // loads), so a round costs one trip to L2.
 #pragma unroll
-                        for (int w2 = 0; w2 < 4; ++w2) {      // elements 8*cch + 2*w2, +1
-                            const float4 c = cs4[4 * cch + w2];   // (cos, sin) of both elements
+                for (int half = 0; half < 2; ++half) {
+                    float4 cv[16];
+                    uint4 a[4], b[4];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        cv[i] = __ldg(cs4 + 16 * half + i);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int off = ((4 * half + c4) ^ (r & 7)) << 4;
+                        a[c4] = *reinterpret_cast<const uint4 *>(h0 + off);
+                        b[c4] = *reinterpret_cast<const uint4 *>(h1 + off);
+                    }
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t *aw = reinterpret_cast<uint32_t *>(&a[c4]), *bw = reinterpret_cast<uint32_t *>(&b[c4]);
+#pragma unroll
+                        for (int w2 = 0; w2 < 4; ++w2) {          // elements 8*chunk + 2*w2, +1
+                            const float4 c = cv[4 * c4 + w2];         // (cos, sin) of both elements
                             const float x0 = __uint_as_float(aw[w2] << 16), x1 = __uint_as_float(aw[w2] & 0xffff0000u);
                             const float y0 = __uint_as_float(bw[w2] << 16), y1 = __uint_as_float(bw[w2] & 0xffff0000u);
                             aw[w2] = pack_bf16x2(x0 * c.x - y0 * c.y, x1 * c.z - y1 * c.w);
                             bw[w2] = pack_bf16x2(x0 * c.y + y0 * c.x, x1 * c.w + y1 * c.z);
                         }
-                        *reinterpret_cast<uint4 *>(h0 + off) = a;
-                        *reinterpret_cast<uint4 *>(h1 + off) = b;
+                        const int off = ((4 * half + c4) ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4 *>(h0 + off) = a[c4];
+                        *reinterpret_cast<uint4 *>(h1 + off) = b[c4];
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&s.q_rot);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.q_rot[t]);
+            return true;
+        };
+        auto prefetch_rows = [&](const TcItem &iq) {
+            const SeqDesc sq = p.seqs[iq.b];
+            const int relq = iq.i0 + t * p.rows_pos + r / p.G;
+            if (r < p.G * p.rows_pos && relq < sq.count) {
+                const char *row = reinterpret_cast<const char *>(p.rope + (size_t)(sq.past + relq) * (D / 2));
+#pragma unroll
+                for (int ln = 0; ln < 4; ++ln)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128 * ln));
+            }
+        };
+        if (p.rope && i_begin < i_end)
+            prefetch_rows(p.items[i_begin]);
+        if (p.rope && i_begin < i_end && !rotate_q(p.items[i_begin], 0)) {
+            ok = false;
+            abort_with(s, p.err, kErrTimeout);
+        }
+        for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
+            const TcItem it = p.items[idx];
+            const SeqDesc sd = p.seqs[it.b];
+            if (p.rope && idx + 1 < i_end)
+                prefetch_rows(p.items[idx + 1]);         // the next item's table rows into L2
+            const int nt = it.nt;
+            const bool row_in_box = r < p.G * p.rows_pos;
+            const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
+            const bool valid = row_in_box && rel < sd.count;
+            const int qpos = sd.past + rel;             // absolute position: sees keys 0..qpos
             float m = -INFINITY, l = 0.0f;
             for (int j = 0; j < nt; ++j) {
                 const uint32_t g = gt + j;
@@ -580,6 +618,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             if (!ok)
                 break;
+            if (p.rope && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
+                ok = false;
+                break;
+            }
             // ---- epilogue: O / l -> bf16, staged one 64-column half at a time in
             // shared memory (128-byte swizzle, the layout of the tensor map) and
             // written by one TMA store per half.  Rows past the valid length
