@@ -75,6 +75,9 @@ def _load():
             lib.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           dp, lp, ctypes.c_int, dp, dp, dp, ctypes.c_int]
             lib.orc_attention.restype = ctypes.c_int
+            lib.orc_attention_window.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 dp, lp, ctypes.c_int, dp, dp, dp, ctypes.c_int, ctypes.c_int64]
+            lib.orc_attention_window.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -101,9 +104,11 @@ def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
 # The attention definition ([P1] 2.3).
 # ---------------------------------------------------------------------------
 
-def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos, nthreads: int | None = None):
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos, nthreads: int | None = None, window: int = 0):
     """q [n_q, H_q, d], K/V [L, H_kv, d] (float64), qpos [n_q] absolute
-    positions.  Query i sees keys 0..qpos[i].  Returns O [n_q, H_q, d]."""
+    positions.  Query i sees keys 0..qpos[i], or with window W > 0 keys
+    max(0, qpos[i] - W + 1)..qpos[i] ([P3] sliding window: the current
+    position counts in the window).  Returns O [n_q, H_q, d]."""
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.float64)
     K = np.ascontiguousarray(K, dtype=np.float64)
@@ -116,16 +121,16 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos, nthreads: int |
     if n_q == 0:
         return out
     dp = ctypes.POINTER(ctypes.c_double)
-    rc = lib.orc_attention(n_q, H_q, H_kv, d, q.ctypes.data_as(dp),
-                           qpos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                           L, K.ctypes.data_as(dp), V.ctypes.data_as(dp),
-                           out.ctypes.data_as(dp), int(nthreads or default_threads()))
+    rc = lib.orc_attention_window(n_q, H_q, H_kv, d, q.ctypes.data_as(dp),
+                                  qpos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                  L, K.ctypes.data_as(dp), V.ctypes.data_as(dp),
+                                  out.ctypes.data_as(dp), int(nthreads or default_threads()), int(window))
     if rc != 0:
         raise ValueError("oracle precondition failed (rc=%d)" % rc)
     return out
 
 
-def attention_dense(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos):
+def attention_dense(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos, window: int = 0):
     """Second form of [P1] 2.3 for small inputs: build S = QK^T/sqrt(d) + M with
     M = -inf on invisible keys, take each row's finite max, exponentiate the
     finite entries, normalise, multiply by V."""
@@ -136,7 +141,11 @@ def attention_dense(q: np.ndarray, K: np.ndarray, V: np.ndarray, qpos):
     n_q, H_q, d = q.shape
     L, H_kv, _ = K.shape
     out = np.zeros((n_q, H_q, d))
-    M = np.where(np.arange(L)[None, :] <= qpos[:, None], 0.0, -np.inf)
+    j = np.arange(L)[None, :]
+    visible = j <= qpos[:, None]
+    if window > 0:
+        visible &= j > qpos[:, None] - window
+    M = np.where(visible, 0.0, -np.inf)
     for h in range(H_q):
         g = (h * H_kv) // H_q
         S = (q[:, h, :] @ K[:, g, :].T) / np.sqrt(d) + M
@@ -230,14 +239,21 @@ class CacheModel:
       * truncate(m) keeps positions < m and drops the rest ([P3] edit at m:
         keep the KV before m, truncate the suffix);
       * fork(src, k) starts a sequence on src's first k positions, sharing
-        their pages ([P1] 2.9 prefix reuse).
+        their pages ([P1] 2.9 prefix reuse);
+      * with a sliding window W ([P3] sliding window and ring cache: K/V
+        outside the window is never read again, so it need not be kept), a
+        write that brings a sequence to length L releases every page whose
+        positions all lie before L - W (no query at a position >= L - 1 sees
+        them); its block-table entry becomes -1.  Truncating or forking at
+        m > 0 needs the positions m - W .. m - 1 still held, else ERANGE.
     Within one batched call, pages are taken sequence by sequence in batch
     order; for each sequence the copy-on-write page comes first, then new
     pages in logical order.  A call that cannot be satisfied changes nothing.
     """
 
     def __init__(self, num_pages, max_seqs, max_pages_per_seq, H_kv, d, dtype,
-                 page_order=None):
+                 page_order=None, window=0):
+        self.window = int(window)
         self.num_pages = int(num_pages)
         self.max_seqs = int(max_seqs)
         self.max_pages_per_seq = int(max_pages_per_seq)
@@ -282,15 +298,25 @@ class CacheModel:
                 return s
         raise CacheError("ENOMEM", "no free sequence id")
 
+    def _released(self, S):
+        return sum(1 for p in S["pages"] if p < 0)
+
+    def _window_holds(self, S, m):
+        """True if positions m - W .. m - 1 are still held (or no window)."""
+        return self.window <= 0 or m == 0 or PAGE_TOKENS * self._released(S) <= m - self.window
+
     def fork(self, src, prefix_len):
         S = self._seq(src)
         if not (0 <= prefix_len <= S["len"]):
             raise CacheError("ERANGE", "prefix beyond source length")
+        if not self._window_holds(S, prefix_len):
+            raise CacheError("ERANGE", "prefix reaches back past the sliding window")
         s = self.create()
         keep = -(-prefix_len // PAGE_TOKENS)
         pages = list(S["pages"][:keep])
         for p in pages:
-            self.ref[p] += 1
+            if p >= 0:
+                self.ref[p] += 1
         self.seqs[s].update(pages=pages, len=prefix_len,
                             k=S["k"][:prefix_len].copy(), v=S["v"][:prefix_len].copy())
         return s
@@ -303,9 +329,12 @@ class CacheModel:
         S = self._seq(s)
         if not (0 <= m <= S["len"]):
             raise CacheError("ERANGE", "truncate beyond length")
+        if not self._window_holds(S, m):
+            raise CacheError("ERANGE", "truncate reaches back past the sliding window")
         keep = -(-m // PAGE_TOKENS)
         for p in S["pages"][keep:]:
-            self._drop(p)
+            if p >= 0:
+                self._drop(p)
         S["pages"] = S["pages"][:keep]
         S["len"] = m
         S["k"] = S["k"][:m].copy()
@@ -359,6 +388,11 @@ class CacheModel:
             S["k"] = np.concatenate([S["k"], np.asarray(kr, dtype=S["k"].dtype)], axis=0)
             S["v"] = np.concatenate([S["v"], np.asarray(vr, dtype=S["v"].dtype)], axis=0)
             S["len"] += c
+            if self.window > 0:
+                for j, p in enumerate(S["pages"]):
+                    if p >= 0 and PAGE_TOKENS * (j + 1) <= S["len"] - self.window:
+                        self._drop(p)
+                        S["pages"][j] = -1
 
     def kv(self, s):
         """Logical K, V of sequence s as fp64 arrays [len, H_kv, d]."""
@@ -395,7 +429,7 @@ def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None, r
         qb = to_f64(q[b, :nb[b]], dt)
         if rope_base is not None:
             qb, K = rope(qb, qpos, rope_base), rope(K, np.arange(K.shape[0]), rope_base)
-        out[b, :nb[b]] = attention(qb, K, V, qpos, nthreads)
+        out[b, :nb[b]] = attention(qb, K, V, qpos, nthreads, window=cache.window)
     return out
 
 
@@ -424,6 +458,6 @@ def decode(cache: CacheModel, seq_ids, q, nthreads=None, rope_base=None):
         qb = to_f64(q[b][None], dt)
         if rope_base is not None:
             qb, K = rope(qb, [L - 1], rope_base), rope(K, np.arange(L), rope_base)
-        out[b] = attention(qb, K, V, np.array([L - 1]), nthreads)[0]
+        out[b] = attention(qb, K, V, np.array([L - 1]), nthreads, window=cache.window)[0]
     return out
 

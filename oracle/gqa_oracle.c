@@ -28,6 +28,11 @@
  * exactly nothing to the max, the denominator or the sum, which is the
  * definition's "sum over finite scores".
  *
+ * Sliding window ("KV Cache 与 Prefill/Decode 推理路径", the sliding-window
+ * and ring-cache lesson: position t reads the most recent W positions, the
+ * current one included): with a window W > 0 the visible keys are
+ * max(0, p - W + 1) .. p.  W <= 0 means no window.
+ *
  * Threads: rows (i, h) are independent; they are dealt round-robin to
  * threads.  Each row is computed by the same sequential loops whatever the
  * thread count, so results do not depend on it.
@@ -40,6 +45,7 @@
 
 typedef struct {
     int n_q, H_q, H_kv, d, L;
+    int64_t window;           /* <= 0: none                                  */
     const double *q;          /* [n_q][H_q][d]  */
     const int64_t *qpos;      /* [n_q]           */
     const double *K, *V;      /* [L][H_kv][d]    */
@@ -61,11 +67,12 @@ static void attend_row(const orc_job *J, int i, int h, double *s, double *a)
     const double *qi = J->q + ((size_t)i * J->H_q + h) * d;
     double *o = J->out + ((size_t)i * J->H_q + h) * d;
     const int64_t p = J->qpos[i];
+    const int64_t j0 = (J->window > 0 && p - J->window + 1 > 0) ? p - J->window + 1 : 0;
     const double root_d = sqrt((double)d);
 
-    /* S row over the visible keys 0..p, and its largest finite entry. */
+    /* S row over the visible keys j0..p, and its largest finite entry. */
     double m = -INFINITY;
-    for (int64_t j = 0; j <= p; ++j) {
+    for (int64_t j = j0; j <= p; ++j) {
         const double *kj = J->K + ((size_t)j * J->H_kv + g) * d;
         double dot = 0.0;
         for (int e = 0; e < d; ++e)
@@ -76,14 +83,14 @@ static void attend_row(const orc_job *J, int i, int h, double *s, double *a)
     }
     /* Denominator over finite scores, then the row of A. */
     double den = 0.0;
-    for (int64_t j = 0; j <= p; ++j)
+    for (int64_t j = j0; j <= p; ++j)
         den += exp(s[j] - m);
-    for (int64_t j = 0; j <= p; ++j)
+    for (int64_t j = j0; j <= p; ++j)
         a[j] = exp(s[j] - m) / den;
     /* O = A V. */
     for (int e = 0; e < d; ++e)
         o[e] = 0.0;
-    for (int64_t j = 0; j <= p; ++j) {
+    for (int64_t j = j0; j <= p; ++j) {
         const double *vj = J->V + ((size_t)j * J->H_kv + g) * d;
         for (int e = 0; e < d; ++e)
             o[e] += a[j] * vj[e];
@@ -116,10 +123,10 @@ static void *worker(void *arg)
  * allocation failure.  Rows with qpos < 0 are rejected too: padding rows are
  * the caller's business and never reach the oracle.
  */
-int orc_attention(int n_q, int H_q, int H_kv, int d,
-                  const double *q, const int64_t *qpos,
-                  int L, const double *K, const double *V,
-                  double *out, int nthreads)
+int orc_attention_window(int n_q, int H_q, int H_kv, int d,
+                         const double *q, const int64_t *qpos,
+                         int L, const double *K, const double *V,
+                         double *out, int nthreads, int64_t window)
 {
     if (n_q < 0 || H_q <= 0 || H_kv <= 0 || d <= 0 || L < 0 || H_q % H_kv != 0)
         return -1;
@@ -135,7 +142,7 @@ int orc_attention(int n_q, int H_q, int H_kv, int d,
     pthread_t th[256];
     int started = 0;
     for (int t = 0; t < nthreads; ++t) {
-        orc_job J = {n_q, H_q, H_kv, d, L, q, qpos, K, V, out, t, nthreads, 0};
+        orc_job J = {n_q, H_q, H_kv, d, L, window, q, qpos, K, V, out, t, nthreads, 0};
         jobs[t] = J;
     }
     for (int t = 1; t < nthreads; ++t) {
@@ -153,4 +160,13 @@ int orc_attention(int n_q, int H_q, int H_kv, int d,
         if (jobs[t].status != 0)
             return jobs[t].status;
     return 0;
+}
+
+/* The same without a window. */
+int orc_attention(int n_q, int H_q, int H_kv, int d,
+                  const double *q, const int64_t *qpos,
+                  int L, const double *K, const double *V,
+                  double *out, int nthreads)
+{
+    return orc_attention_window(n_q, H_q, H_kv, d, q, qpos, L, K, V, out, nthreads, 0);
 }

@@ -427,3 +427,87 @@ def test_rope_stored_keys_round_to_within_one_bf16_step():
     assert np.all(np.abs(got - exact) <= step * 1.0001)
     # at position 0 the stored bytes are the input bytes
     assert np.array_equal(oracle.rope_stored_bf16(k, np.zeros(64), 10000.0), k)
+
+
+# ---------------------------------------------------------------- sliding window
+# [P3] sliding window: position t reads the most recent W positions, the
+# current one included; K/V outside the window is never read again, so a
+# ring cache holds O(W) of it.
+
+def test_window_at_least_the_length_changes_nothing():
+    rng = np.random.default_rng(11)
+    q, K, V = rng.standard_normal((6, 2, 4)), rng.standard_normal((9, 1, 4)), rng.standard_normal((9, 1, 4))
+    pos = np.array([0, 2, 4, 6, 7, 8])
+    assert np.array_equal(oracle.attention(q, K, V, pos, 2, window=9), oracle.attention(q, K, V, pos, 2))
+    assert np.array_equal(oracle.attention(q, K, V, pos, 2, window=1000), oracle.attention(q, K, V, pos, 2))
+
+
+def test_window_of_one_returns_the_own_value():
+    rng = np.random.default_rng(12)
+    q, K, V = rng.standard_normal((4, 2, 4)), rng.standard_normal((7, 1, 4)), rng.standard_normal((7, 1, 4))
+    pos = np.array([0, 3, 5, 6])
+    out = oracle.attention(q, K, V, pos, 2, window=1)
+    for i, p in enumerate(pos):
+        assert np.allclose(out[i, :, :], V[p, 0][None, :], rtol=0, atol=1e-15)
+
+
+def test_window_brute_force_pure_python():
+    rng = np.random.default_rng(13)
+    L, d, W = 7, 3, 3
+    q, K, V = rng.standard_normal((L, 1, d)), rng.standard_normal((L, 1, d)), rng.standard_normal((L, 1, d))
+    out = oracle.attention(q, K, V, np.arange(L), 1, window=W)
+    for p in range(L):
+        js = [j for j in range(L) if p - W < j <= p]
+        sc = [sum(q[p, 0, e] * K[j, 0, e] for e in range(d)) / math.sqrt(d) for j in js]
+        mx = max(sc)
+        w = [math.exp(x - mx) for x in sc]
+        z = sum(w)
+        ref = [sum(w[a] * V[j, 0, e] for a, j in enumerate(js)) / z for e in range(d)]
+        assert np.allclose(out[p, 0], ref, rtol=0, atol=1e-14)
+    # the weight vector of a query whose window is full has W entries ([P3]: W = 4 -> length 4)
+    assert len([j for j in range(L) if (L - 1) - W < j <= L - 1]) == W
+
+
+def test_keys_outside_the_window_never_matter():
+    rng = np.random.default_rng(14)
+    L, W = 30, 8
+    q, K, V = rng.standard_normal((L, 2, 8)), rng.standard_normal((L, 1, 8)), rng.standard_normal((L, 1, 8))
+    base = oracle.attention(q, K, V, np.arange(L), 2, window=W)
+    K2, V2 = K.copy(), V.copy()
+    K2[:L - W] += 100.0
+    V2[:L - W] -= 50.0
+    moved = oracle.attention(q, K2, V2, np.arange(L), 2, window=W)
+    assert np.array_equal(base[L - 1], moved[L - 1])      # the last row's window is L - W .. L - 1
+    assert not np.array_equal(base[L - W - 1], moved[L - W - 1])
+
+
+def test_windowed_cache_releases_pages_and_bounds_rewinds():
+    cm = oracle.CacheModel(16, 2, 16, 1, 4, "f32", window=20)
+    s = cm.create()
+    rows = np.zeros((100, 1, 4), dtype=np.float32)
+    cm.write([s], [rows], [rows])
+    bt = cm.block_table(s)
+    assert bt[:5] == [-1] * 5 and all(p >= 0 for p in bt[5:])   # positions 0..79 released (80 <= 100 - 20)
+    assert cm.free_pages() == 16 - 2
+    with pytest.raises(oracle.CacheError) as e:
+        cm.truncate(s, 90)                                       # needs 70..89 but 0..79 are gone
+    assert e.value.kind == "ERANGE"
+    with pytest.raises(oracle.CacheError):
+        cm.fork(s, 95)
+    cm.truncate(s, 100)
+    f = cm.fork(s, 100)
+    assert cm.block_table(f) == bt
+    cm.truncate(s, 0)
+    assert cm.block_table(s) == []
+
+
+def test_windowed_cache_holds_a_bounded_number_of_pages():
+    W = 40
+    cm = oracle.CacheModel(8, 1, 80, 1, 2, "f32", window=W)
+    s = cm.create()
+    one = np.zeros((1, 1, 2), dtype=np.float32)
+    for _ in range(1000):
+        cm.write([s], [one], [one])
+        live = [p for p in cm.block_table(s) if p >= 0]
+        assert len(live) <= -(-W // 16) + 1
+    assert cm.length(s) == 1000
