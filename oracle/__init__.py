@@ -388,7 +388,12 @@ class CacheModel:
             S["k"] = np.concatenate([S["k"], np.asarray(kr, dtype=S["k"].dtype)], axis=0)
             S["v"] = np.concatenate([S["v"], np.asarray(vr, dtype=S["v"].dtype)], axis=0)
             S["len"] += c
-            if self.window > 0:
+        # Release only once every entry is written: the call's own readers (a
+        # prefill over these rows) still see the keys it wrote, so no page of
+        # this call goes back to the pool before the call ends.
+        if self.window > 0:
+            for s in seq_ids:
+                S = self._seq(s)
                 for j, p in enumerate(S["pages"]):
                     if p >= 0 and PAGE_TOKENS * (j + 1) <= S["len"] - self.window:
                         self._drop(p)
