@@ -44,14 +44,14 @@ class CacheDesc(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("keys_post_position", ctypes.c_int32),
                 ("layout_version", ctypes.c_int32), ("page_order", _I32P),
-                ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+                ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float), ("window", ctypes.c_int32)]
 
 
 class LayoutMetadata(ctypes.Structure):
     _fields_ = [("keys_post_position", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("layout_version", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+                ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float), ("window", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -129,14 +129,14 @@ class Cache:
 
     def __init__(self, num_kv_heads, head_dim, num_pages, max_seqs, max_pages_per_seq,
                  dtype="bf16", page_order=None, device=None, metadata_only=False,
-                 keys_post_position=1, layout_version=LAYOUT_VERSION, rope=False, rope_base=10000.0):
+                 keys_post_position=1, layout_version=LAYOUT_VERSION, rope=False, rope_base=10000.0, window=0):
         self.dtype_code = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
         self.torch_dtype = _TORCH_DTYPE[self.dtype_code]
         self._order_keep, order_ptr = _i32_array(page_order)
         self.desc = CacheDesc(self.dtype_code, num_kv_heads, head_dim, PAGE_TOKENS, num_pages,
                               max_seqs, max_pages_per_seq, keys_post_position, layout_version,
-                              order_ptr, int(rope), float(rope_base))
-        self.rope, self.rope_base = int(rope), float(rope_base)
+                              order_ptr, int(rope), float(rope_base), int(window))
+        self.rope, self.rope_base, self.window = int(rope), float(rope_base), int(window)
         self.num_kv_heads, self.head_dim, self.num_pages = num_kv_heads, head_dim, num_pages
         self.max_seqs, self.max_pages_per_seq = max_seqs, max_pages_per_seq
         self.pool = None

@@ -140,6 +140,7 @@ struct gqa_cache {
         pv.d = desc.head_dim;
         pv.err = d_err;
         pv.rope = d_rope;
+        pv.window = desc.window;
         return pv;
     }
 };
@@ -152,6 +153,42 @@ bool live(const gqa_cache *c, int32_t s)
 }
 
 int32_t pages_for(int64_t tokens) { return (int32_t)((tokens + kPageTokens - 1) / kPageTokens); }
+
+// Sliding window: positions m - W .. m - 1 still held (released pages are a
+// prefix of the table), so queries from position m - 1 on find their keys.
+bool window_holds(const gqa_cache *c, const SeqState &S, int32_t m)
+{
+    if (c->desc.window <= 0 || m == 0)
+        return true;
+    int64_t released = 0;
+    while (released < (int64_t)S.pages.size() && S.pages[released] < 0)
+        ++released;
+    return released * kPageTokens <= (int64_t)m - c->desc.window;
+}
+
+// After a write that brought the sequences to their new lengths L: pages
+// whose positions all lie before L - W go back to the pool (no query from
+// position L - 1 on reads them) and their table entries become -1.  Called
+// once the call's kernels are queued; later writes that reuse the pages are
+// ordered after them on the stream.
+void release_windows(gqa_cache *c, int32_t B, const int32_t *seq_ids)
+{
+    if (c->desc.window <= 0)
+        return;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t s = seq_ids[b];
+        SeqState &S = c->seqs[s];
+        for (size_t j = 0; j < S.pages.size(); ++j) {
+            if ((int64_t)kPageTokens * (int64_t)(j + 1) > (int64_t)S.len - c->desc.window)
+                break;
+            if (S.pages[j] >= 0) {
+                c->drop_page(S.pages[j]);
+                S.pages[j] = -1;
+                c->set_entry(s, (int32_t)j, -1);
+            }
+        }
+    }
+}
 
 // Validate a batched write: live and distinct sequences, capacity, pages.
 int check_write(const gqa_cache *c, const WriteReq *r, int B)
@@ -403,6 +440,8 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
         return fail(GQA_EINVAL, "rope must be 0 (none) or 1 (rotary)");
     if (d.rope == 1 && (d.head_dim % 2 != 0 || !(d.rope_base > 1.0f) || !std::isfinite(d.rope_base)))
         return fail(GQA_EINVAL, "rope = 1 needs an even d_h and a finite rope_base > 1");
+    if (d.window < 0)
+        return fail(GQA_EINVAL, "window must be 0 (none) or a positive number of tokens");
     const size_t need = gqa_pool_bytes(desc);
     if (pool_dev) {
         if (pool_bytes < need)
@@ -524,6 +563,7 @@ int gqa_cache_layout(const gqa_cache *c, gqa_layout_metadata *out)
     out->head_dim = c->desc.head_dim;
     out->rope = c->desc.rope;
     out->rope_base = c->desc.rope == 1 ? c->desc.rope_base : 0.0f;
+    out->window = c->desc.window;
     return GQA_OK;
 }
 
@@ -538,6 +578,8 @@ int gqa_layout_compatible(const gqa_layout_metadata *a, const gqa_layout_metadat
         return fail(GQA_ELAYOUT, "precision, page size, layout version or KV shape differs");
     if (a->rope != b->rope || (a->rope == 1 && a->rope_base != b->rope_base))
         return fail(GQA_ELAYOUT, "the keys were rotated with a different position mechanism");
+    if (a->window != b->window)
+        return fail(GQA_ELAYOUT, "sliding windows differ (pages outside the window were released)");
     return GQA_OK;
 }
 
@@ -566,6 +608,8 @@ int gqa_seq_fork(gqa_cache *c, int32_t src, int32_t prefix_len, int32_t *seq_out
         return fail(GQA_EINVAL, "sequence %d is not live", src);
     if (prefix_len < 0 || prefix_len > c->seqs[src].len)
         return fail(GQA_ERANGE, "prefix %d outside 0..%d", prefix_len, c->seqs[src].len);
+    if (!window_holds(c, c->seqs[src], prefix_len))
+        return fail(GQA_ERANGE, "prefix %d reaches back past the sliding window", prefix_len);
     int32_t s = -1;
     int rc = gqa_seq_create(c, &s);
     if (rc != GQA_OK)
@@ -574,7 +618,8 @@ int gqa_seq_fork(gqa_cache *c, int32_t src, int32_t prefix_len, int32_t *seq_out
     SeqState &S = c->seqs[s];
     for (int32_t i = 0; i < keep; ++i) {
         const int32_t p = c->seqs[src].pages[i];
-        c->ref[p] += 1;
+        if (p >= 0)
+            c->ref[p] += 1;
         S.pages.push_back(p);
         c->set_entry(s, i, p);
     }
@@ -592,9 +637,12 @@ int kv_truncate(gqa_cache *c, int32_t seq, int32_t m)
     SeqState &S = c->seqs[seq];
     if (m < 0 || m > S.len)
         return fail(GQA_ERANGE, "truncate to %d outside 0..%d", m, S.len);
+    if (!window_holds(c, S, m))
+        return fail(GQA_ERANGE, "truncate to %d reaches back past the sliding window", m);
     const int32_t keep = pages_for(m);
     for (size_t i = keep; i < S.pages.size(); ++i)
-        c->drop_page(S.pages[i]);
+        if (S.pages[i] >= 0)
+            c->drop_page(S.pages[i]);
     S.pages.resize(keep);
     S.len = m;
     return GQA_OK;
@@ -655,7 +703,7 @@ int gqa_page_refcount(const gqa_cache *c, int32_t page, int32_t *out)
 // The hot path.
 // ---------------------------------------------------------------------------
 
-int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
+static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
                  const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions,
                  void *out, void *stream)
 {
@@ -715,14 +763,17 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
             for (int32_t i0 = 0; i0 < sds[b].count; i0 += span) {
                 const int32_t last = std::min<int32_t>(i0 + span, sds[b].count) - 1;
                 const int32_t nt = (sds[b].past + last) / 128 + 1;
+                // Under a sliding window the item's first row sees the oldest key.
+                const int32_t j0 = window_start(sds[b].past + i0, c->desc.window) / 128;
                 for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
-                    items.push_back(TcItem{b, h, i0, nt});
+                    items.push_back(TcItem{b, h, i0, nt, j0, 0});
             }
         // Longest-processing-time-first: items in decreasing cost, each to the
         // CTA with the least work so far; a CTA then runs its items in that
         // order.  Cost of an item ~ its key tiles plus a fixed per-item share
         // (Q load, pipeline refill, epilogue), in quarter-tile units.
-        std::stable_sort(items.begin(), items.end(), [](const TcItem &x, const TcItem &y) { return x.nt > y.nt; });
+        std::stable_sort(items.begin(), items.end(),
+                         [](const TcItem &x, const TcItem &y) { return x.nt - x.j0 > y.nt - y.j0; });
         tc_grid = std::max(1, std::min<int>(c->num_sms, (int)items.size()));
         std::vector<std::vector<int>> runs(tc_grid);
         using Load = std::pair<int64_t, int>;
@@ -733,7 +784,7 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
             Load top = heap.top();
             heap.pop();
             runs[top.second].push_back((int)i);
-            top.first += 4 * (int64_t)items[i].nt + kItemCostQuarters;
+            top.first += 4 * (int64_t)(items[i].nt - items[i].j0) + kItemCostQuarters;
             heap.push(top);
         }
         std::vector<TcItem> sorted;
@@ -780,7 +831,7 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     });
 }
 
-int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,
+static int kv_append_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,
               const void *k_new, const void *v_new, void *stream)
 {
     if (!c || !seq_ids)
@@ -829,6 +880,25 @@ int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const 
     });
 }
 
+int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
+                 const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions, void *out,
+                 void *stream)
+{
+    const int rc = attn_prefill_impl(c, B, seq_ids, n, H_q, q, k, v, valid_lengths, positions, out, stream);
+    if (rc == GQA_OK)
+        release_windows(c, B, seq_ids);
+    return rc;
+}
+
+int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,
+              const void *k_new, const void *v_new, void *stream)
+{
+    const int rc = kv_append_impl(c, B, seq_ids, n, counts, k_new, v_new, stream);
+    if (rc == GQA_OK)
+        release_windows(c, B, seq_ids);
+    return rc;
+}
+
 int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q, void *out,
                 void *stream)
 {
@@ -851,7 +921,7 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         if (L < 1)
             return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
         sds[b] = SeqDesc{s, L - 1, 1, 0};
-        total += L;
+        total += L - decode_first_token(L, c->desc.window);
     }
     int rc;
     if (c->meta_only)
@@ -874,7 +944,7 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         std::vector<int32_t> start(B + 1, 0);
         for (int b = 0; b < B; ++b) {
             const int32_t L = sds[b].past + 1;
-            const int32_t ns = (L + chunk - 1) / chunk;
+            const int32_t ns = (L - decode_first_token(L, c->desc.window) + chunk - 1) / chunk;
             start[b] = (int32_t)items.size();
             for (int32_t s = 0; s < ns; ++s)
                 items.push_back(DecodeItem{b, s});
@@ -1013,7 +1083,7 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         if (L < 1)
             return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
         sds[b] = SeqDesc{s, L - 1, 1, 0};
-        total += L;
+        total += L - decode_first_token(L, c->desc.window);
     }
     int rc = check_device(c);
     if (rc != GQA_OK)
@@ -1031,7 +1101,8 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     for (;;) {
         n_items = 0;
         for (int b = 0; b < B; ++b)
-            n_items += (size_t)((sds[b].past + 1 + chunk - 1) / chunk);
+            n_items += (size_t)((sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window) + chunk - 1) /
+                                chunk);
         if (n_items * (size_t)H_kv * G * 130 <= part_cap || chunk >= 512)
             break;
         chunk = std::min(512, chunk * 2);
@@ -1044,7 +1115,8 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     std::vector<int32_t> start(B + 1, 0);
     items.reserve(n_items);
     for (int b = 0; b < B; ++b) {
-        const int32_t ns = (sds[b].past + 1 + chunk - 1) / chunk;
+        const int32_t ns =
+            (sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window) + chunk - 1) / chunk;
         start[b] = (int32_t)items.size();
         for (int32_t s = 0; s < ns; ++s)
             items.push_back(DecodeItem{b, s});

@@ -98,7 +98,8 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     const int H_kv = pv.H_kv;
     const SeqDesc sd = seqs[it.b];
     const int L = sd.past + 1;
-    const int t0 = it.split * chunk;
+    const int ws = window_start(L - 1, pv.window);       // first visible key
+    const int t0 = decode_first_token(L, pv.window) + it.split * chunk;
     const int nt = min(chunk, L - t0);
     const int npages = (nt + kPageTokens - 1) / kPageTokens;
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride + t0 / kPageTokens;
@@ -213,7 +214,7 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         if ((lane & 1) == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                sc[tl][h] = (ok && tl < nt) ? v[0][h] : -INFINITY;
+                sc[tl][h] = (ok && tl < nt && t0 + tl >= ws) ? v[0][h] : -INFINITY;
         }
     }
     __syncthreads();

@@ -127,6 +127,7 @@ struct TcParams {
     int32_t *err;
     float scale_log2;   // log2(e) / sqrt(d_h)
     const float2 *rope; // rotary (cos, sin) [position][64], or null
+    int32_t window;     // sliding window (0 = none)
 };
 
 __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
@@ -241,7 +242,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
                 if (lp < seq_pages) {
                     ph = p.tables[(size_t)sd.row * p.stride + lp];
-                    if ((unsigned)ph >= (unsigned)p.num_pages) {
+                    if (ph < 0)                            // released by the sliding window: never visible
+                        ph = p.num_pages;
+                    else if (ph >= p.num_pages) {
                         if (!vside)
                             atomicOr(p.err, kErrPageId);
                         ph = p.num_pages;
@@ -273,7 +276,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const SeqDesc sd = p.seqs[it.b];
             // The first K tile only needs a free stage; issue it before
             // waiting for the previous item to release the Q buffers.
-            if (!load_tile(it, sd, 0)) {
+            if (!load_tile(it, sd, it.j0)) {
                 ok = false;
                 break;
             }
@@ -287,7 +290,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 }
                 ++q_issued;
             }
-            for (int j = 1; j < it.nt; ++j)
+            for (int j = it.j0 + 1; j < it.nt; ++j)
                 if (!load_tile(it, sd, j)) {
                     ok = false;
                     break;
@@ -354,11 +357,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             int k = 0;
             if (warp == 1) {
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt;
-                    for (int j = 0; j < nt; ++j, ++g) {
+                    const int nt = p.items[idx].nt, j0 = p.items[idx].j0;
+                    for (int j = j0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
                         ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
-                             (j > 0 || mbar_wait(p.rope ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
+                             (j > j0 || mbar_wait(p.rope ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
                              mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
                         if (!ok)
                             break;
@@ -367,7 +370,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         mma_commit(&s.s_full[0]);
                         *(volatile int *)&s.s_issued[0] = (int)g + 1;
                         ok = mbar_wait(&s.s_free, 0, &s.abort_) &&
-                             (j > 0 || !p.rope || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
+                             (j > j0 || !p.rope || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
                         if (!ok)
                             break;
                         tc_fence_after();
@@ -393,8 +396,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                             break;
                 };
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt;
-                    for (int j = 0; j < nt; ++j, ++g) {
+                    const int nt = p.items[idx].nt, j0 = p.items[idx].j0;
+                    for (int j = j0; j < nt; ++j, ++g) {
                         const int sv = g % kVStages;
                         const bool order = kPvOrder && j + 1 < nt;
                         ok = mbar_wait(&s.p_full[0], g & 1, &s.abort_) &&
@@ -404,7 +407,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         if (order)
                             after_s(0, g + 2);
                         tc_fence_after();
-                        issue_o(0, sv, j > 0);
+                        issue_o(0, sv, j > j0);
                         mma_commit(&s.pv_done[0]);
                         ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
                         if (!ok)
@@ -412,7 +415,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         if (order)
                             after_s(1, g + 2);
                         tc_fence_after();
-                        issue_o(1, sv, j > 0);
+                        issue_o(1, sv, j > j0);
                         mma_commit(&s.pv_done[1]);
                         mma_commit(&s.v_empty[sv]);
                     }
@@ -518,10 +521,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const bool row_in_box = r < p.G * p.rows_pos;
             const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
             const bool valid = row_in_box && rel < sd.count;
-            const int qpos = sd.past + rel;             // absolute position: sees keys 0..qpos
+            const int qpos = sd.past + rel;             // absolute position: sees keys qlo..qpos
+            const int qlo = window_start(qpos, p.window);
+            const int j0 = it.j0;
             float m = -INFINITY, l = 0.0f;
-            for (int j = 0; j < nt; ++j) {
-                const uint32_t g = gt + j;
+            for (int j = j0; j < nt; ++j) {
+                const uint32_t g = gt + (j - j0);
                 if (!mbar_wait(&s.s_full[t], g & 1, &s.abort_)) {
                     ok = false;
                     break;
@@ -536,10 +541,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     mbar_arrive(&s.s_free);              // the MMA may overwrite S now
                 __syncwarp();
                 const int key0 = 128 * j;
-                if (key0 + 127 > qpos) {                 // diagonal (or beyond): keys > qpos are masked
+                if (key0 + 127 > qpos || key0 < qlo) {  // diagonal or window edge: mask keys outside qlo..qpos
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
-                        if (key0 + i > qpos)
+                        if (key0 + i > qpos || key0 + i < qlo)
                             su[i] = 0xff800000u;         // -inf
                 }
                 // Row max: four independent 3-input max chains of depth 16.
@@ -563,7 +568,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 // The O rescale below touches TMEM with warp-collective loads
                 // and stores: do it for the whole warp when any row needs it
                 // (alpha = 1 for the others).
-                const bool rescale_o = __any_sync(0xffffffffu, grow && j > 0);
+                const bool rescale_o = __any_sync(0xffffffffu, grow && j > j0);
                 __syncwarp();
                 const float m_use = (m == -INFINITY) ? 0.0f : m;
                 const float2 mm = make_float2(-m_use, -m_use);
@@ -628,7 +633,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             // are written as zeros; positions past n are clipped by the store.
             // The named barriers below need every thread of the warpgroup, so
             // a timeout is agreed on by all of them before anyone leaves.
-            if (named_bar_any(1 + t, 128, !mbar_wait(&s.pv_done[t], (gt + nt - 1) & 1, &s.abort_))) {
+            if (named_bar_any(1 + t, 128, !mbar_wait(&s.pv_done[t], (gt + (nt - j0) - 1) & 1, &s.abort_))) {
                 ok = false;
                 break;
             }
@@ -666,7 +671,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 }
             }
             tc_fence_before();
-            gt += nt;
+            gt += nt - j0;
         }
         if (!ok)
             abort_with(s, p.err, kErrTimeout);
@@ -753,6 +758,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.err = pv.err;
     prm.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     prm.rope = pv.rope;
+    prm.window = pv.window;
     const int smem = (int)sizeof(TcSmem) + 1024;
     static bool attr_set = false;
     if (!attr_set) {

@@ -100,7 +100,7 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
     for (int j = 0; j < kMaxD / 32; ++j)
         acc[j] = 0.0f;
 
-    for (int kb = 0; kb <= pos; kb += 32) {
+    for (int kb = window_start(pos, pv.window); kb <= pos; kb += 32) {   // keys qlo..pos
         const int t = kb + lane;
         float s = -INFINITY;
         if (t <= pos) {

@@ -38,7 +38,21 @@ struct PoolView {
     int32_t d;
     int32_t *err;            // device error word (GQA_DEVERR_* bits)
     const float2 *rope;      // rotary table (cos, sin) [position][d / 2], or null: no rotation
+    int32_t window;          // sliding window W (0 = none): position p sees keys max(0, p-W+1)..p
 };
+
+// First key position visible to a query at absolute position p.
+__host__ __device__ inline int window_start(int p, int window)
+{
+    return (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
+}
+
+// Decode of a sequence of length L reads pages from this token on (the page
+// holding its window's first key).
+__host__ __device__ inline int decode_first_token(int L, int window)
+{
+    return window_start(L - 1, window) / kPageTokens * kPageTokens;
+}
 
 // One batch entry of a launching call.
 struct SeqDesc {
@@ -61,7 +75,8 @@ struct DecodeItem {
 // One tensor-core prefill work item: two 128-row query tiles of batch entry
 // b and KV head kvh, starting at row i0 of the entry; nt key tiles of 128.
 struct TcItem {
-    int32_t b, kvh, i0, nt;
+    int32_t b, kvh, i0, nt;   // key tiles j0 .. nt-1 (j0 > 0 only under a sliding window)
+    int32_t j0, pad_;
 };
 
 // Error-word bits (mirror include/gqa.h).

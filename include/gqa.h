@@ -118,6 +118,14 @@ typedef struct {
                                     rotated when written (the cache holds post-position keys),
                                     queries inside the attention kernels.                     */
     float rope_base;             /* rope = 1: the frequency base, > 1 (e.g. 10000)           */
+    int32_t window;              /* sliding window W ([P3] sliding window and ring cache): 0 =
+                                    none; W >= 1: the query at position p sees keys
+                                    max(0, p - W + 1) .. p (its own position included).  K/V
+                                    outside every future window is released: a write that
+                                    brings a sequence to length L returns to the pool each page
+                                    whose 16 positions all lie before L - W, and its block-table
+                                    entry becomes -1.  A sequence then holds at most
+                                    ceil(W / 16) + 1 pages.                                    */
 } gqa_cache_desc;
 
 /* layout_metadata of [P1] 2.5 / invariant 2.2 item 5. */
@@ -130,6 +138,7 @@ typedef struct {
     int32_t head_dim;
     int32_t rope;                /* the cache's position mechanism (keys were rotated with it) */
     float rope_base;
+    int32_t window;              /* sliding window (pages outside it were released)           */
 } gqa_layout_metadata;
 
 typedef struct gqa_cache gqa_cache;
@@ -179,7 +188,9 @@ int gqa_seq_create(gqa_cache *cache, int32_t *seq_out);
 /* New sequence that shares the first `prefix_len` positions of `src`
  * ([P1] 2.9 prefix reuse; [P3] prefix sharing): it references src's first
  * ceil(prefix_len/16) pages (reference counts + 1) and has length
- * prefix_len.  GQA_ERANGE unless 0 <= prefix_len <= length(src). */
+ * prefix_len.  GQA_ERANGE unless 0 <= prefix_len <= length(src), and, with
+ * a sliding window W, unless prefix_len = 0 or positions prefix_len - W ..
+ * prefix_len - 1 are still held (released entries are shared as -1). */
 int gqa_seq_fork(gqa_cache *cache, int32_t src, int32_t prefix_len, int32_t *seq_out);
 
 /* Drop every page reference of `seq` and release its id. */
@@ -190,6 +201,7 @@ int gqa_seq_length(const gqa_cache *cache, int32_t seq, int32_t *len_out);
 
 /* Copy `seq`'s block table (physical page of each logical page) into host
  * `out` (capacity `cap` entries); *count_out = number of pages in the table.
+ * Entries released by a sliding window are -1.
  * GQA_ERANGE if cap is too small (nothing copied). */
 int gqa_seq_block_table(const gqa_cache *cache, int32_t seq, int32_t *out, int32_t cap,
                         int32_t *count_out);
@@ -303,7 +315,9 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
  * `seq`, drop the rest.  Pages wholly beyond position m lose one reference
  * (and return to the pool at zero).  A partially kept tail page stays; if it
  * is shared, the next write copies it first.  Host metadata only.
- * Errors: GQA_EINVAL (unknown sequence), GQA_ERANGE unless 0 <= m <= length. */
+ * Errors: GQA_EINVAL (unknown sequence), GQA_ERANGE unless 0 <= m <= length,
+ * and, with a sliding window W, unless m = 0 or positions m - W .. m - 1 are
+ * still held (a windowed cache cannot rewind past what it released). */
 int kv_truncate(gqa_cache *cache, int32_t seq, int32_t m);
 
 /* Synchronise `stream`, read and clear the cache's device error word.

@@ -36,9 +36,10 @@ def test_version_string():
     assert "sm_103a" in gqa.version()
 
 
-def _pair(pages=64, seqs=8, per_seq=32, H_kv=2, d=8, order=None):
-    lib = gqa.Cache(H_kv, d, pages, seqs, per_seq, dtype="f32", page_order=order, metadata_only=True)
-    model = oracle.CacheModel(pages, seqs, per_seq, H_kv, d, "f32", page_order=order)
+def _pair(pages=64, seqs=8, per_seq=32, H_kv=2, d=8, order=None, window=0):
+    lib = gqa.Cache(H_kv, d, pages, seqs, per_seq, dtype="f32", page_order=order, metadata_only=True,
+                    window=window)
+    model = oracle.CacheModel(pages, seqs, per_seq, H_kv, d, "f32", page_order=order, window=window)
     return lib, model
 
 
@@ -55,11 +56,15 @@ def _rows(c, H_kv=2, d=8):
     return np.zeros((c, H_kv, d), dtype=np.float32)
 
 
-def test_allocator_matches_oracle_model_under_random_operations():
-    rng = np.random.default_rng(7)
+@pytest.mark.parametrize("window", [0, 1, 16, 37])
+def test_allocator_matches_oracle_model_under_random_operations(window):
+    # With a sliding window the model releases pages wholly before the window
+    # after every write and refuses rewinds past it; the library must agree.
+    rng = np.random.default_rng(7 + window)
     order = rng.permutation(96)
-    lib, model = _pair(pages=96, seqs=6, per_seq=40, order=order)
+    lib, model = _pair(pages=96, seqs=6, per_seq=40, order=order, window=window)
     live = []
+    released_seen, refusals = False, 0
     for step in range(400):
         op = rng.integers(0, 6)
         try:
@@ -101,17 +106,26 @@ def test_allocator_matches_oracle_model_under_random_operations():
                 try:
                     s_m = model.fork(src, k)
                 except oracle.CacheError as e:
-                    with pytest.raises(gqa.GqaError):
+                    with pytest.raises(gqa.GqaError) as el:
                         lib.seq_fork(src, k)
-                    assert e.kind == "ENOMEM"
+                    assert el.value.name == e.kind
+                    assert e.kind == "ENOMEM" or (e.kind == "ERANGE" and window > 0)
                 else:
                     assert lib.seq_fork(src, k) == s_m
                     live.append(s_m)
             elif op == 4:                                     # truncate
                 s = int(rng.choice(live))
                 m = int(rng.integers(0, model.length(s) + 1))
-                model.truncate(s, m)
-                gqa.kv_truncate(lib, s, m)
+                try:
+                    model.truncate(s, m)
+                except oracle.CacheError as e:
+                    assert e.kind == "ERANGE" and window > 0
+                    refusals += 1
+                    with pytest.raises(gqa.GqaError) as el:
+                        gqa.kv_truncate(lib, s, m)
+                    assert el.value.name == "ERANGE"
+                else:
+                    gqa.kv_truncate(lib, s, m)
             else:                                             # free
                 s = int(rng.choice(live))
                 model.free_seq(s)
@@ -122,7 +136,10 @@ def test_allocator_matches_oracle_model_under_random_operations():
             with pytest.raises(gqa.GqaError):
                 lib.seq_create()
         _same_state(lib, model)
+        released_seen |= any(-1 in model.block_table(s) for s in model.seqs)
     assert len(model.copies) > 0          # copy-on-write was exercised
+    if window > 0:                        # pages were released and rewinds refused
+        assert released_seen and refusals > 0
 
 
 def test_prefill_rejections_change_nothing():
@@ -240,3 +257,36 @@ def test_causal_pair_counts_match_the_toy_decoder(golden):
     cached = W.causal_pairs(0, P) + sum(W.causal_pairs(P + t, 1) for t in range(steps))
     assert per * full == g["score_pairs_full_recompute"]
     assert per * cached == g["score_pairs_cached"]
+
+
+def test_window_description_checks_and_layout():
+    m = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, window=100).layout()
+    assert m.window == 100
+    plain = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True).layout()
+    assert plain.window == 0
+    assert not gqa.layout_compatible(m, plain)
+    assert gqa.layout_compatible(m, gqa.LayoutMetadata(**m.as_dict()))
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, window=-1)
+    assert e.value.name == "EINVAL"
+
+
+def test_window_rewinds_need_the_window_held():
+    # W = 40, 215 tokens: pages 0..9 (positions < 160) are released, so a
+    # rewind to m needs m - 40 >= 160.
+    lib, model = _pair(pages=20, per_seq=16, window=40)
+    a = lib.seq_create()
+    model.create()
+    gqa.kv_append_meta(lib, [a], 215)
+    model.write([a], [_rows(215)], [_rows(215)])
+    _same_state(lib, model)
+    assert lib.block_table(a)[:10] == [-1] * 10
+    for m in (1, 150, 199):                 # (m = 0 empties the sequence: always allowed)
+        for call in (lambda: gqa.kv_truncate(lib, a, m), lambda: lib.seq_fork(a, m)):
+            with pytest.raises(gqa.GqaError) as e:
+                call()
+            assert e.value.name == "ERANGE", m
+    f = lib.seq_fork(a, 205)
+    assert lib.block_table(f) == lib.block_table(a)[:13]
+    gqa.kv_truncate(lib, a, 200)
+    assert lib.seq_length(a) == 200 and lib.seq_length(f) == 205
