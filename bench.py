@@ -245,9 +245,10 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     w = workloads.ragged_prefill(workloads.seed_for(2))
     B, n, H_q, H_kv, d = w["B"], w["n"], w["H_q"], w["H_kv"], w["d"]
     nb = [int(x) for x in w["valid_lengths"]]
-    flops = gqa.work.prefill_flops([0] * B, nb, H_q, d)
+    flops = gqa.work.prefill_flops([0] * B, nb, H_q, d, args.window)
     pages = sum(workloads.pages_for(x) for x in nb) + 16
-    cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16", rope=args.rope)
+    cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16", rope=args.rope,
+                      window=args.window)
     ids = [cache.seq_create() for _ in range(B)]
     q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
     out = torch.empty_like(q)
@@ -342,6 +343,8 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
            "causal_gflop_per_step": round(flops / 1e9, 3)}
     if args.rope:
         cfg["position_mechanism"] = "rotary (base 10000), applied inside the library: keys at write, queries in-kernel"
+    if args.window:
+        cfg["sliding_window"] = "W=%d: position p attends to keys max(0, p-W+1)..p; flops count those pairs" % args.window
     return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
             "gpu_launches": gpu_launches, "kernels": kernels, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
             "workload": w}
@@ -351,9 +354,16 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     w = workloads.paged_decode(workloads.seed_for(3))
     B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
     L = [int(x) for x in w["lengths"]]
-    kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, 2)
-    cache = gqa.Cache(H_kv, d, w["num_pages"], B, workloads.pages_for(max(L)) + 1, dtype="bf16", rope=args.rope,
-                      page_order=w["page_order"])
+    W = args.window
+    kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, 2, W)
+    # Under a sliding window the sequences grow by one token a step (a
+    # rewind may reach back past the window), so the pool and the tables
+    # get room for every step of the run; K/V bytes are counted per step.
+    grow = 8 * (args.steps + args.warmup + 4) if W else 0
+    spare = B * workloads.pages_for(grow + 16) if W else 0
+    cache = gqa.Cache(H_kv, d, w["num_pages"] + spare, B, workloads.pages_for(max(L) + grow) + 1, dtype="bf16",
+                      rope=args.rope, page_order=(list(w["page_order"]) + list(range(w["num_pages"],
+                      w["num_pages"] + spare))) if W else w["page_order"], window=W)
     ids = [cache.seq_create() for _ in range(B)]
     for b in range(B):
         kb = to_dev(torch, w["hist_k"][b][None])
@@ -362,23 +372,38 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         del kb, vb
     new_k, new_v, q = to_dev(torch, w["new_k"]), to_dev(torch, w["new_v"]), to_dev(torch, w["q"])
     out = torch.empty_like(q)
+    cur = [x - 1 for x in L]             # cached lengths before the next step's append
+    moved = [0]                          # algorithmic K/V bytes of the steps run so far
+
+    def advance():
+        if W:
+            for b in range(B):
+                cur[b] += 1
+            moved[0] += gqa.work.decode_kv_bytes(cur, H_kv, d, 2, W)
+        else:
+            moved[0] += kv_bytes
+            for b in range(B):
+                gqa.kv_truncate(cache, ids[b], L[b] - 1)
 
     def step():
         gqa.kv_append(cache, ids, new_k, new_v)
         gqa.attn_decode(cache, ids, q, out=out)
-        for b in range(B):
-            gqa.kv_truncate(cache, ids[b], L[b] - 1)
+        advance()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     cache.profile_read()
+    m0 = moved[0]
     ms, t0, t1 = timed_steps(torch, dist, step, args.steps)
+    region_bytes = moved[0] - m0
     region_launches = cache.profile_read()
     total_ms = dist.max(torch, sum(ms))
-    value = kv_bytes * args.steps * dist.world / (total_ms / 1e3) / 1e9
+    value = region_bytes * dist.world / (total_ms / 1e3) / 1e9
     cache.profile(True)
+    m0 = moved[0]
     timed_steps(torch, dist, step, args.steps)
+    kv_bytes = (moved[0] - m0) // args.steps          # per launch (the mean, under a window)
     cache.profile(False)
     prof = cache.profile_read()
     kernel = "decode_split" if prof["decode_split"][0] else "attn_simt"
@@ -401,16 +426,17 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         gqa.kv_append(cache, ids, kd, vd)
         gqa.attn_decode(cache, ids, qd, out=od)
         oh.copy_(od, non_blocking=True)
-        for b in range(B):
-            gqa.kv_truncate(cache, ids[b], L[b] - 1)
+        advance()
 
     for _ in range(2):
         e2e_step()
+    m0 = moved[0]
     ems, _, _ = timed_steps(torch, dist, e2e_step, args.steps)
+    e2e_bytes = moved[0] - m0
     e2e_total = dist.max(torch, sum(ems))
     res = {"metric": "decode KV-read GB/s", "value": round(value, 1), "unit": "GB/s",
            "ms_per_step": round(total_ms / args.steps, 4), "roofline": roofline,
-           "e2e": {"value": round(kv_bytes * args.steps * dist.world / (e2e_total / 1e3) / 1e9, 1), "unit": "GB/s",
+           "e2e": {"value": round(e2e_bytes * dist.world / (e2e_total / 1e3) / 1e9, 1), "unit": "GB/s",
                    "h2d_bytes_per_step": int(q.nbytes + new_k.nbytes + new_v.nbytes),
                    "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4)},
            "gpu_launches": sum(nl for nl, _ in region_launches.values()),
@@ -423,11 +449,14 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                       "kv_bytes_per_step": kv_bytes}}
     if args.rope:
         res["config"]["position_mechanism"] = "rotary (base 10000): queries rotated in-kernel"
+    if W:
+        res["config"]["sliding_window"] = ("W=%d: a decode reads the last min(L, W) tokens; sequences grow by one "
+                                           "token a step (no rewind), K/V bytes counted per step" % W)
     if want_cpu:
         import oracle
         nth = oracle.default_threads()
         cm = oracle.CacheModel(sum(workloads.pages_for(x) for x in L[:8]), 8, workloads.pages_for(max(L)) + 1,
-                               H_kv, d, "bf16")
+                               H_kv, d, "bf16", window=W)
         sm = [cm.create() for _ in range(8)]
         for j in range(8):
             cm.write([sm[j]], [w["hist_k"][j]], [w["hist_v"][j]])
@@ -438,7 +467,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
             oracle.decode(cm, sm, w["q"][:8], nthreads=nth)
             dt += time.perf_counter() - t0c
             reps += 1
-        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2) * reps
+        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2, W) * reps
         res["cpu_baseline"] = {"value": round(by / dt / 1e9, 3), "unit": "GB/s", "cores": nth, "kind": "oracle",
                                "sample": "fp64 oracle decode of sequences 0..7 (%d cached tokens, %.1f MB of "
                                          "bf16 K/V), %d repetitions: %.1f GB in %.1f s"
@@ -658,6 +687,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--rope", action="store_true",
                     help="caches with the rotary position mechanism applied by the library")
+    ap.add_argument("--window", type=int, default=0,
+                    help="caches with a sliding window of this many tokens (0 = none)")
     ap.add_argument("--extra", action="store_true",
                     help="also time the wide-GQA long-context and prefix-reuse/edit workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

@@ -140,6 +140,10 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 // item_start[c + 1] - 1 in order.  Barrier phases run on
 // across items (global tile counter gt), so the next item's Q and first K/V
 // tile load while the current item's last tiles and epilogue run.
+// ROPE: queries rotated in-kernel (p.rope is the table); WIN: sliding window
+// (items start at key tile j0, keys before the window masked).  Both are
+// template flags so the plain path carries none of their instructions.
+template <bool ROPE, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
                   const __grid_constant__ CUtensorMap mO, const TcParams p)
@@ -276,7 +280,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const SeqDesc sd = p.seqs[it.b];
             // The first K tile only needs a free stage; issue it before
             // waiting for the previous item to release the Q buffers.
-            if (!load_tile(it, sd, it.j0)) {
+            if (!load_tile(it, sd, WIN ? it.j0 : 0)) {
                 ok = false;
                 break;
             }
@@ -290,7 +294,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 }
                 ++q_issued;
             }
-            for (int j = it.j0 + 1; j < it.nt; ++j)
+            for (int j = (WIN ? it.j0 : 0) + 1; j < it.nt; ++j)
                 if (!load_tile(it, sd, j)) {
                     ok = false;
                     break;
@@ -357,11 +361,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             int k = 0;
             if (warp == 1) {
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt, j0 = p.items[idx].j0;
+                    const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
                         ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
-                             (j > j0 || mbar_wait(p.rope ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
+                             (j > j0 || mbar_wait(ROPE ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
                              mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
                         if (!ok)
                             break;
@@ -370,7 +374,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         mma_commit(&s.s_full[0]);
                         *(volatile int *)&s.s_issued[0] = (int)g + 1;
                         ok = mbar_wait(&s.s_free, 0, &s.abort_) &&
-                             (j > j0 || !p.rope || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
+                             (j > j0 || !ROPE || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
                         if (!ok)
                             break;
                         tc_fence_after();
@@ -396,7 +400,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                             break;
                 };
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt, j0 = p.items[idx].j0;
+                    const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int sv = g % kVStages;
                         const bool order = kPvOrder && j + 1 < nt;
@@ -506,24 +510,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128 * ln));
             }
         };
-        if (p.rope && i_begin < i_end)
+        if (ROPE && i_begin < i_end)
             prefetch_rows(p.items[i_begin]);
-        if (p.rope && i_begin < i_end && !rotate_q(p.items[i_begin], 0)) {
+        if (ROPE && i_begin < i_end && !rotate_q(p.items[i_begin], 0)) {
             ok = false;
             abort_with(s, p.err, kErrTimeout);
         }
         for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
             const TcItem it = p.items[idx];
             const SeqDesc sd = p.seqs[it.b];
-            if (p.rope && idx + 1 < i_end)
+            if (ROPE && idx + 1 < i_end)
                 prefetch_rows(p.items[idx + 1]);         // the next item's table rows into L2
             const int nt = it.nt;
             const bool row_in_box = r < p.G * p.rows_pos;
             const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
             const bool valid = row_in_box && rel < sd.count;
             const int qpos = sd.past + rel;             // absolute position: sees keys qlo..qpos
-            const int qlo = window_start(qpos, p.window);
-            const int j0 = it.j0;
+            const int qlo = WIN ? window_start(qpos, p.window) : 0;
+            const int j0 = WIN ? it.j0 : 0;
             float m = -INFINITY, l = 0.0f;
             for (int j = j0; j < nt; ++j) {
                 const uint32_t g = gt + (j - j0);
@@ -541,10 +545,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     mbar_arrive(&s.s_free);              // the MMA may overwrite S now
                 __syncwarp();
                 const int key0 = 128 * j;
-                if (key0 + 127 > qpos || key0 < qlo) {  // diagonal or window edge: mask keys outside qlo..qpos
+                if (key0 + 127 > qpos || (WIN && key0 < qlo)) {  // diagonal or window edge: mask keys outside qlo..qpos
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
-                        if (key0 + i > qpos || key0 + i < qlo)
+                        if (key0 + i > qpos || (WIN && key0 + i < qlo))
                             su[i] = 0xff800000u;         // -inf
                 }
                 // Row max: four independent 3-input max chains of depth 16.
@@ -623,7 +627,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             if (!ok)
                 break;
-            if (p.rope && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
+            if (ROPE && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -760,14 +764,18 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.rope = pv.rope;
     prm.window = pv.window;
     const int smem = (int)sizeof(TcSmem) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static bool attr_set[4] = {false, false, false, false};
+    const int which = (pv.rope ? 1 : 0) + (pv.window > 0 ? 2 : 0);
+    void (*const kern[4])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
+        prefill_tc_kernel<false, false>, prefill_tc_kernel<true, false>, prefill_tc_kernel<false, true>,
+        prefill_tc_kernel<true, true>};
+    if (!attr_set[which]) {
+        cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        attr_set[which] = true;
     }
-    prefill_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
+    kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
     return cudaGetLastError();
 }
 

@@ -290,3 +290,18 @@ def test_window_rewinds_need_the_window_held():
     assert lib.block_table(f) == lib.block_table(a)[:13]
     gqa.kv_truncate(lib, a, 200)
     assert lib.seq_length(a) == 200 and lib.seq_length(f) == 205
+
+
+def test_windowed_work_counts_match_brute_force():
+    # The throughput accounting counts the pairs the oracle's dense form
+    # leaves visible: keys max(0, p - W + 1)..p of each position p.
+    for past in (0, 1, 15, 40, 130):
+        for new in (0, 1, 17, 64):
+            for W in (0, 1, 2, 16, 37, 200):
+                qpos = np.arange(past, past + new)
+                j = np.arange(past + new)
+                vis = j[None, :] <= qpos[:, None]
+                if W > 0:
+                    vis &= j[None, :] > qpos[:, None] - W
+                assert gqa.work.causal_pairs(past, new, W) == int(vis.sum()), (past, new, W)
+    assert gqa.work.decode_kv_bytes([10, 100], 2, 8, 2, window=16) == (10 + 16) * 2 * 2 * 8 * 2
