@@ -365,6 +365,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                       rope=args.rope, page_order=(list(w["page_order"]) + list(range(w["num_pages"],
                       w["num_pages"] + spare))) if W else w["page_order"], window=W)
     ids = [cache.seq_create() for _ in range(B)]
+    cache.set_decode_kernel(args.decode_kernel)
     for b in range(B):
         kb = to_dev(torch, w["hist_k"][b][None])
         vb = to_dev(torch, w["hist_v"][b][None])
@@ -406,7 +407,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     kv_bytes = (moved[0] - m0) // args.steps          # per launch (the mean, under a window)
     cache.profile(False)
     prof = cache.profile_read()
-    kernel = "decode_split" if prof["decode_split"][0] else "attn_simt"
+    kernel = max(("prefill_tc", "decode_split", "attn_simt"), key=lambda x: prof[x][1])
     launches, kms = prof[kernel]
     avg_ms = kms / max(1, launches)
     achieved = kv_bytes / (avg_ms / 1e3) / 1e9
@@ -472,10 +473,60 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                                "sample": "fp64 oracle decode of sequences 0..7 (%d cached tokens, %.1f MB of "
                                          "bf16 K/V), %d repetitions: %.1f GB in %.1f s"
                                          % (sum(L[:8]), by / reps / 1e6, reps, by / 1e9, dt)}
+    if not W:
+        res["multi_token"] = bench_multi_token(torch, gqa, dist, args, peaks, peak_src, cache, ids, L, w)
     res["device_error_flags"] = cache.check()
     res["t0"], res["t1"] = t0, t1
     cache.close()
     return res
+
+
+def bench_multi_token(torch, gqa, dist, args, peaks, peak_src, cache, ids, L, w, T=4):
+    """Multi-token decode over the paged-decode cache: T new tokens per
+    sequence (a speculative draft block) attend causally to the cached
+    L_b - 1 tokens and to each other, through attn_prefill with n = T; one
+    step = the chunk + kv_truncate back.  HBM-bound like decode: the work is
+    the K/V bytes read, sum_b (L_b - 1 + T) tokens."""
+    B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
+    ch = workloads.draft_chunk(workloads.seed_for(6), B, T, H_q, H_kv, d)
+    q, k, v = to_dev(torch, ch["q"]), to_dev(torch, ch["k"]), to_dev(torch, ch["v"])
+    out = torch.empty_like(q)
+    counts = [T] * B
+    kv_bytes = gqa.work.decode_kv_bytes([x - 1 + T for x in L], H_kv, d, 2)
+    flops = gqa.work.prefill_flops([x - 1 for x in L], counts, H_q, d)
+
+    def step():
+        gqa.attn_prefill(cache, ids, q, k, v, counts, out=out)
+        for b in range(B):
+            gqa.kv_truncate(cache, ids[b], L[b] - 1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cache.profile_read()
+    ms, _, _ = timed_steps(torch, dist, step, args.steps)
+    region = cache.profile_read()
+    total_ms = dist.max(torch, sum(ms))
+    prof = profiled(torch, dist, cache, step, args.steps)
+    kernel = "prefill_tc" if prof["prefill_tc"][0] else "attn_simt"
+    launches, kms = prof[kernel]
+    avg_ms = kms / max(1, launches)
+    achieved = kv_bytes / (avg_ms / 1e3) / 1e9
+    return {"metric": "multi-token decode KV-read GB/s", "unit": "GB/s",
+            "value": round(kv_bytes * args.steps * dist.world / (total_ms / 1e3) / 1e9, 1),
+            "ms_per_step": round(total_ms / args.steps, 4),
+            "tflops": round(flops * args.steps * dist.world / (total_ms / 1e3) / 1e12, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": kernel,
+                         "kernel_ms": round(avg_ms, 4), "algorithmic_bytes_per_launch": kv_bytes,
+                         "peak_source": "%s HBM copy bandwidth" % peak_src},
+            "gpu_launches": sum(nl for nl, _ in region.values()),
+            "kernels": {name: {"launches": nl, "avg_ms": round(x / nl, 5)} for name, (nl, x) in prof.items() if nl},
+            "config": {"workload": "bf16 multi-token decode: the paged-decode cache (B=%d, H_q=%d, H_kv=%d, d_h=%d, "
+                                   "L_b - 1 cached tokens) plus T=%d new tokens per sequence, N(0,1) (seed %d); "
+                                   "one step = attn_prefill(n=T) + kv_truncate back" % (B, H_q, H_kv, d, T,
+                                                                                        workloads.seed_for(6)),
+                       "kv_bytes_per_step": kv_bytes, "causal_gflop_per_step": round(flops / 1e9, 3)}}
 
 
 def profiled(torch, dist, cache, step, K, flush=None):
@@ -504,6 +555,7 @@ def bench_wide(torch, gqa, dist, args, peaks):
     T, H_q, H_kv, d, steps = w["n"], w["H_q"], w["H_kv"], w["d"], w["steps"]
     per_seq = workloads.pages_for(T + steps) + 1
     c = gqa.Cache(H_kv, d, per_seq + 4, 1, per_seq, dtype="bf16")
+    c.set_decode_kernel(args.decode_kernel)
     s = c.seq_create()
     q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
     out = torch.empty_like(q)
@@ -536,8 +588,29 @@ def bench_wide(torch, gqa, dist, args, peaks):
     decode_all()
     ms_res, _, _ = timed_steps(torch, dist, decode_all, 3)
     t_res = sum(ms_res) / 3
-    prof = profiled(torch, dist, c, decode_all, 1)
-    kname = "decode_split" if prof["decode_split"][0] else "attn_simt"
+    # Device time with the host running ahead: a sleep kernel holds the GPU
+    # while every step is queued (1.5x the host's queueing time at 2.1 GHz),
+    # so no launch waits for the host; per-launch events and the span of the
+    # whole queued run are then GPU time.
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    decode_all()
+    host_s = time.perf_counter() - h0
+    torch.cuda.synchronize()
+    c.profile_read()
+    c.profile(True)
+    qa, qb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(host_s * 1.5 * 2.1e9))
+    qa.record()
+    h0 = time.perf_counter()
+    decode_all()
+    host_q = time.perf_counter() - h0
+    qb.record()
+    qb.synchronize()
+    c.profile(False)
+    prof = c.profile_read()
+    q_ms = qa.elapsed_time(qb)
+    kname = max(("prefill_tc", "decode_split", "attn_simt"), key=lambda x: prof[x][0])
     k_us = prof[kname][1] / max(1, prof[kname][0]) * 1e3
     step_ms = []
     for t in range(steps):                          # L2 flushed before every step
@@ -556,12 +629,17 @@ def bench_wide(torch, gqa, dist, args, peaks):
            "kernel": {"name": kname, "us_per_launch": round(k_us, 2),
                       "gbs": round(kv_bytes / steps / (k_us / 1e6) / 1e9, 1),
                       "append_us_per_launch": round(prof["cache_write"][1] / max(1, prof["cache_write"][0]) * 1e3, 2)},
+           "queued": {"us_per_step": round(q_ms / steps * 1e3, 2), "gbs": round(kv_bytes / (q_ms / 1e3) / 1e9, 1),
+                      "host_us_per_step": round(host_q / steps * 1e6, 2),
+                      "how": "all steps queued behind a sleep kernel; span of the run on the GPU (append + "
+                             "decode + profiling events)"},
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
            "note": "one step = kv_append + attn_decode of one sequence, called from Python: the step times "
                    "include the host side of two calls, which is longer than the GPU work; 34 MB of K/V fits "
-                   "in L2; kernel = device time of the decode launch alone (L2-resident)"}
+                   "in L2; kernel = device time of the decode launch alone (L2-resident), measured with the "
+                   "steps queued ahead of the GPU"}
     flags = c.check()
     c.close()
     return {"workload": "bf16 wide GQA: B=1, H_q=48, H_kv=8 (g=6), d_h=128, prefill T=%d, then %d append+decode "
@@ -687,6 +765,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--rope", action="store_true",
                     help="caches with the rotary position mechanism applied by the library")
+    ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto",
+                    help="decode kernel of attn_decode (auto: tensor-core for bf16, d_h = 128)")
     ap.add_argument("--window", type=int, default=0,
                     help="caches with a sliding window of this many tokens (0 = none)")
     ap.add_argument("--extra", action="store_true",

@@ -34,6 +34,7 @@ LAYOUT_VERSION = 2
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
 KERNELS = {"cache_write": 0, "cow_copy": 1, "prefill_tc": 2, "attn_simt": 3,
            "decode_split": 4, "decode_combine": 5}
+DECODE_KERNELS = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
 
@@ -84,6 +85,7 @@ _sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
 _sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
+_sig("gqa_set_decode_kernel", ctypes.c_int, _vp, ctypes.c_int32)
 _sig("gqa_profile_read", ctypes.c_int, _vp, _i32, _I32P, ctypes.POINTER(ctypes.c_double))
 _sig("gqa_last_error", ctypes.c_char_p)
 _sig("gqa_version", ctypes.c_char_p)
@@ -218,6 +220,11 @@ class Cache:
         _check(_lib.gqa_cache_layout(self._h, ctypes.byref(m)))
         return m
 
+    def set_decode_kernel(self, kernel: str):
+        """Decode kernel of attn_decode / attn_decode_static: "auto",
+        "tensor_core" or "cuda_core"."""
+        _check(_lib.gqa_set_decode_kernel(self._h, DECODE_KERNELS[kernel]))
+
     def profile(self, on: bool):
         """Bracket every kernel launch with CUDA events (on its stream)."""
         _check(_lib.gqa_profile_enable(self._h, 1 if on else 0))
@@ -351,4 +358,4 @@ def exported_symbols():
             "gqa_layout_compatible", "gqa_seq_create", "gqa_seq_fork", "gqa_seq_free",
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
-            "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version"]
+            "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel"]

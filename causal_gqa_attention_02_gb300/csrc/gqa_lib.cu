@@ -38,6 +38,14 @@ thread_local std::string t_err;
 // Fixed cost of one prefill work item (Q load, pipeline refill, epilogue)
 // in quarters of a key tile, for balancing items over the persistent grid.
 constexpr int64_t kItemCostQuarters = 2;
+#ifndef GQA_SPLIT_ITEMS_PER_SM
+#define GQA_SPLIT_ITEMS_PER_SM 1
+#endif
+#ifndef GQA_SPLIT_MIN_TILES
+#define GQA_SPLIT_MIN_TILES 4
+#endif
+constexpr int kSplitItemsPerSm = GQA_SPLIT_ITEMS_PER_SM;   // tensor-core split items: target per SM
+constexpr int kSplitMinTiles = GQA_SPLIT_MIN_TILES;         // and the shortest piece, in key tiles
 
 int fail(int code, const char *fmt, ...)
 {
@@ -94,6 +102,7 @@ struct gqa_cache {
 
     // Profiling: launch counts always; event pairs while `prof` is on.
     bool prof = false;
+    int32_t decode_kernel = GQA_DECODE_AUTO;
     int32_t launches[GQA_KERNEL_COUNT] = {};
     struct ProfRec {
         int kernel;
@@ -372,8 +381,16 @@ cudaEvent_t get_event(gqa_cache *c)
     return e;
 }
 
-// Queue one kernel via `launch` (returning cudaError_t), counting it and,
-// when profiling is on, bracketing it with events on its stream.
+// Record the start event of a profiled launch (no-op when not profiling).
+inline void rec(cudaEvent_t ev, cudaStream_t st)
+{
+    if (ev)
+        cudaEventRecord(ev, st);
+}
+
+// Queue one kernel via `launch` (given the start event or null, returning
+// cudaError_t), counting it and, when profiling is on, bracketing it with
+// events on its stream.
 template <typename F>
 int run_kernel(gqa_cache *c, int kernel, cudaStream_t st, const char *what, F &&launch)
 {
@@ -381,10 +398,12 @@ int run_kernel(gqa_cache *c, int kernel, cudaStream_t st, const char *what, F &&
     if (c->prof) {
         e0 = get_event(c);
         e1 = get_event(c);
-        if (e0 && e1)
-            cudaEventRecord(e0, st);
+        if (!e0 || !e1)
+            e0 = e1 = nullptr;
     }
-    const cudaError_t e = launch();
+    // The launcher records e0 right before its kernel, after its host-side
+    // preparation, so a GPU that waits for the host does not count that wait.
+    const cudaError_t e = launch(e0);
     if (e != cudaSuccess)
         return cuda_fail(e, what);
     c->launches[kernel] += 1;
@@ -700,6 +719,129 @@ int gqa_page_refcount(const gqa_cache *c, int32_t page, int32_t *out)
 }
 
 // ---------------------------------------------------------------------------
+// Work plan of the tensor-core kernel.
+// ---------------------------------------------------------------------------
+
+struct TcPlan {
+    std::vector<TcItem> items;        // grouped by CTA
+    std::vector<int32_t> item_start;  // grid + 1 offsets
+    int grid = 1;
+    int32_t slots = 0;                // split workspace slots
+    int32_t slot_rows = 0;
+    bool ranged = false;              // an item starts past key tile 0
+};
+
+// Items: two query tiles of 128 / G positions of one (entry, KV head) each;
+// the second tile is skipped when it has no valid row.  An entry whose rows
+// all fit the first tile (decode, multi-token decode) may be split along its
+// key tiles into pieces of about `piece` tiles so that there are several
+// items per SM; the pieces' partial results are merged by the kernel.
+// Items are then placed longest-first on the least-loaded CTA (LPT); a CTA
+// runs its items in that order.  Cost of an item, in quarter key tiles:
+// 4 per tile with two query tiles, 3 with one, plus a fixed share for the
+// Q load, the pipeline refill and the epilogue.
+void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan &pl)
+{
+    const int rows_pos = prefill_tc_rows_per_tile(G), span = 2 * rows_pos;
+    const int B = (int)sds.size();
+    std::vector<TcItem> items;
+    int64_t split_tiles = 0;
+    for (int b = 0; b < B; ++b)
+        for (int32_t i0 = 0; i0 < sds[b].count; i0 += span) {
+            const int32_t last = std::min<int32_t>(i0 + span, sds[b].count) - 1;
+            const int32_t nt = (sds[b].past + last) / 128 + 1;
+            // Under a sliding window the item's first row sees the oldest key.
+            const int32_t j0 = window_start(sds[b].past + i0, c->desc.window) / 128;
+            const int32_t tiles = i0 + rows_pos < sds[b].count ? 2 : 1;
+            for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
+                items.push_back(TcItem{b, h, i0, nt, j0, tiles, -1, 0, 1, 0});
+            split_tiles += (int64_t)(nt - j0) * c->desc.num_kv_heads;
+        }
+    // Pieces of at least kSplitMinTiles key tiles, sized for about
+    // kSplitItemsPerSm items per SM.
+    const int64_t per = (int64_t)kSplitItemsPerSm * c->num_sms;
+    const int64_t piece = std::max<int64_t>(kSplitMinTiles, (split_tiles + per - 1) / per);
+    std::vector<TcItem> all;
+    all.reserve(items.size());
+    for (const TcItem &it : items) {
+        const int32_t K = it.nt - it.j0;
+        if (it.i0 != 0 || it.tiles != 1 || sds[it.b].count > rows_pos || K <= piece) {
+            all.push_back(it);
+            continue;
+        }
+        const int32_t S = (int32_t)((K + piece - 1) / piece);
+        for (int32_t q = 0; q < S; ++q) {
+            TcItem x = it;
+            x.j0 = it.j0 + (int32_t)((int64_t)q * K / S);
+            x.nt = it.j0 + (int32_t)((int64_t)(q + 1) * K / S);
+            x.part = pl.slots + q;
+            x.split = q;
+            x.nsplit = S;
+            all.push_back(x);
+        }
+        pl.slots += S;
+        pl.slot_rows = std::max<int32_t>(pl.slot_rows, sds[it.b].count * G);
+    }
+    auto cost = [](const TcItem &x) { return (int64_t)(x.tiles > 1 ? 4 : 3) * (x.nt - x.j0) + kItemCostQuarters; };
+    std::stable_sort(all.begin(), all.end(), [&](const TcItem &x, const TcItem &y) { return cost(x) > cost(y); });
+    pl.grid = std::max(1, std::min<int>(c->num_sms, (int)all.size()));
+    std::vector<std::vector<int>> runs(pl.grid);
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int i = 0; i < pl.grid; ++i)
+        heap.push({0, i});
+    for (size_t i = 0; i < all.size(); ++i) {
+        Load top = heap.top();
+        heap.pop();
+        runs[top.second].push_back((int)i);
+        top.first += cost(all[i]);
+        heap.push(top);
+    }
+    pl.items.clear();
+    pl.items.reserve(all.size());
+    pl.item_start.assign(1, 0);
+    for (const auto &run : runs) {
+        for (int i : run) {
+            pl.items.push_back(all[i]);
+            pl.ranged |= all[i].j0 > 0;
+        }
+        pl.item_start.push_back((int32_t)pl.items.size());
+    }
+}
+
+// Split workspace of a plan in the cache's growable buffers.
+int tc_workspace(gqa_cache *c, const TcPlan &pl, TcSplitWs &ws)
+{
+    ws.ranged = pl.ranged;
+    ws.slot_rows = pl.slot_rows;
+    if (pl.slots == 0)
+        return GQA_OK;
+    const size_t rows = (size_t)pl.slots * pl.slot_rows;
+    int rc = ensure_ws(c, rows * 128 + rows * 2);
+    if (rc == GQA_OK)
+        rc = ensure_cnt(c, (size_t)pl.slots);
+    if (rc != GQA_OK)
+        return rc;
+    ws.o = c->d_ws;
+    ws.ml = reinterpret_cast<float2 *>(c->d_ws + rows * 128);
+    ws.counters = c->d_cnt;
+    return GQA_OK;
+}
+
+// Which decode kernel a call runs: 1 = tensor-core, 0 = CUDA-core, -1 = the
+// tensor-core kernel was asked for but cannot serve this cache or group.
+int decode_uses_tc(const gqa_cache *c, int G)
+{
+    const bool ok = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
+                    prefill_tc_supported(G, c->desc.num_kv_heads);
+    if (c->decode_kernel == GQA_DECODE_CUDA_CORE)
+        return 0;
+    if (c->decode_kernel == GQA_DECODE_TENSOR_CORE)
+        return ok ? 1 : -1;
+    return ok ? 1 : 0;
+}
+
+// ---------------------------------------------------------------------------
 // The hot path.
 // ---------------------------------------------------------------------------
 
@@ -752,62 +894,24 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     const int G = H_q / c->desc.num_kv_heads;
     const bool use_tc = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
                         prefill_tc_supported(G, c->desc.num_kv_heads);
-    std::vector<TcItem> items;
-    std::vector<int32_t> item_start;
-    int tc_grid = 1;
-    if (use_tc) {
-        // Two query tiles of 128/G positions per CTA; heaviest items first so
-        // the long causal rows start early and the tail of the grid is short.
-        const int span = 2 * prefill_tc_rows_per_tile(G);
-        for (int b = 0; b < B; ++b)
-            for (int32_t i0 = 0; i0 < sds[b].count; i0 += span) {
-                const int32_t last = std::min<int32_t>(i0 + span, sds[b].count) - 1;
-                const int32_t nt = (sds[b].past + last) / 128 + 1;
-                // Under a sliding window the item's first row sees the oldest key.
-                const int32_t j0 = window_start(sds[b].past + i0, c->desc.window) / 128;
-                for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
-                    items.push_back(TcItem{b, h, i0, nt, j0, 0});
-            }
-        // Longest-processing-time-first: items in decreasing cost, each to the
-        // CTA with the least work so far; a CTA then runs its items in that
-        // order.  Cost of an item ~ its key tiles plus a fixed per-item share
-        // (Q load, pipeline refill, epilogue), in quarter-tile units.
-        std::stable_sort(items.begin(), items.end(),
-                         [](const TcItem &x, const TcItem &y) { return x.nt - x.j0 > y.nt - y.j0; });
-        tc_grid = std::max(1, std::min<int>(c->num_sms, (int)items.size()));
-        std::vector<std::vector<int>> runs(tc_grid);
-        using Load = std::pair<int64_t, int>;
-        std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-        for (int i = 0; i < tc_grid; ++i)
-            heap.push({0, i});
-        for (size_t i = 0; i < items.size(); ++i) {
-            Load top = heap.top();
-            heap.pop();
-            runs[top.second].push_back((int)i);
-            top.first += 4 * (int64_t)(items[i].nt - items[i].j0) + kItemCostQuarters;
-            heap.push(top);
-        }
-        std::vector<TcItem> sorted;
-        sorted.reserve(items.size());
-        item_start.assign(1, 0);
-        for (const auto &run : runs) {
-            for (int i : run)
-                sorted.push_back(items[i]);
-            item_start.push_back((int32_t)sorted.size());
-        }
-        items.swap(sorted);
-    }
+    TcPlan plan;
+    if (use_tc)
+        plan_tc(c, sds, G, plan);
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
     const size_t o_cow = stg.add(cows.data(), cows.size());
-    const size_t o_items = stg.add(items.data(), items.size());
-    const size_t o_start = stg.add(item_start.data(), item_start.size());
+    const size_t o_items = stg.add(plan.items.data(), plan.items.size());
+    const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
+    TcSplitWs ws;
+    if (use_tc && (rc = tc_workspace(c, plan, ws)) != GQA_OK)
+        return rc;
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     const PoolView pv = c->view();
     const SeqDesc *d_sds = (const SeqDesc *)(c->d_stage + o_sds);
     if (!cows.empty() &&
-        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&] {
+        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
+             rec(ev, st);
              return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
          })) != GQA_OK)
         return rc;
@@ -815,18 +919,20 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     // of out (discarded rows are written as zeros); the prefill kernel then
     // writes the valid rows only.
     const int out_row_bytes = H_q * c->desc.head_dim * c->esize;
-    if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&] {
+    if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&](cudaEvent_t ev) {
+             rec(ev, st);
              return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st, use_tc ? out : nullptr,
                                        out_row_bytes);
          })) != GQA_OK)
         return rc;
     if (use_tc) {
-        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&] {
+        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&](cudaEvent_t ev) {
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items),
-                                     (const int32_t *)(c->d_stage + o_start), tc_grid, B, n, H_q, q, out, st);
+                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, n, H_q, q, out, ws, st, ev);
         });
     }
-    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {
+    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&](cudaEvent_t ev) {
+        rec(ev, st);
         return launch_attn_simt(pv, c->desc.dtype, d_sds, B, n, H_q, q, out, st);
     });
 }
@@ -870,11 +976,13 @@ static int kv_append_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32
         return rc;
     const PoolView pv = c->view();
     if (!cows.empty() &&
-        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&] {
+        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
+             rec(ev, st);
              return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
          })) != GQA_OK)
         return rc;
-    return run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&] {
+    return run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&](cudaEvent_t ev) {
+        rec(ev, st);
         return launch_cache_write(pv, c->esize, (const SeqDesc *)(c->d_stage + o_sds), B, n, max_c, k_new, v_new,
                                   st);
     });
@@ -935,6 +1043,26 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
     const int G = H_q / H_kv;
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
+    if ((rc = decode_uses_tc(c, G)) < 0)
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+    if (rc == 1) {
+        // The prefill kernel at one query row per sequence, each sequence's
+        // key tiles split across SMs and merged in the kernel.
+        TcPlan plan;
+        plan_tc(c, sds, G, plan);
+        const size_t o_items = stg.add(plan.items.data(), plan.items.size());
+        const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
+        TcSplitWs ws;
+        if ((rc = tc_workspace(c, plan, ws)) != GQA_OK)
+            return rc;
+        if ((rc = upload_stage(c, st)) != GQA_OK)
+            return rc;
+        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core decode kernel", [&](cudaEvent_t ev) {
+            return launch_prefill_tc(pv, (const SeqDesc *)(c->d_stage + o_sds),
+                                     (const TcItem *)(c->d_stage + o_items),
+                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev);
+        });
+    }
     if (c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && decode_split_supported(G)) {
         // Chunk: a multiple of the page size, large enough to amortise the
         // partials, small enough for several CTAs per SM.
@@ -972,13 +1100,29 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         a.counters = c->d_cnt;
         a.out = out;
         return run_kernel(c, GQA_KERNEL_DECODE_SPLIT, st, "decode kernel",
-                          [&] { return launch_decode_split(pv, a, st); });
+                          [&](cudaEvent_t ev) {
+                              rec(ev, st);
+                              return launch_decode_split(pv, a, st);
+                          });
     }
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
-    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&] {
+    return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&](cudaEvent_t ev) {
+        rec(ev, st);
         return launch_attn_simt(pv, c->desc.dtype, (const SeqDesc *)(c->d_stage + o_sds), B, 1, H_q, q, out, st);
     });
+}
+
+int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
+{
+    if (!c)
+        return fail(GQA_EINVAL, "NULL cache");
+    if (kernel != GQA_DECODE_AUTO && kernel != GQA_DECODE_TENSOR_CORE && kernel != GQA_DECODE_CUDA_CORE)
+        return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE or _CUDA_CORE", kernel);
+    if (kernel == GQA_DECODE_TENSOR_CORE && (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128))
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128");
+    c->decode_kernel = kernel;
+    return GQA_OK;
 }
 
 int gqa_profile_enable(gqa_cache *c, int on)
@@ -1067,8 +1211,12 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     if (H_q % H_kv != 0)
         return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
     const int G = H_q / H_kv;
-    if (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || !decode_split_supported(G))
-        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 and H_q/H_kv <= 8");
+    const int use_tc = decode_uses_tc(c, G);
+    if (use_tc < 0)
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+    if (!use_tc && (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || !decode_split_supported(G)))
+        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 (and H_q/H_kv <= 8 on the "
+                                "CUDA-core kernel)");
     if (c->meta_only)
         return fail(GQA_EINVAL, "attn_decode_static needs a cache with a device pool");
     if (!q || !out)
@@ -1088,6 +1236,54 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     int rc = check_device(c);
     if (rc != GQA_OK)
         return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    if (use_tc) {
+        // The plan of attn_decode (so the results are the same bits), with
+        // its descriptors, merge counters and partials in the static array.
+        TcPlan plan;
+        plan_tc(c, sds, G, plan);
+        std::vector<char> desc;
+        Stage stg(desc);
+        const size_t o_sds = stg.add(sds.data(), sds.size());
+        const size_t o_items = stg.add(plan.items.data(), plan.items.size());
+        const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
+        const size_t rows = (size_t)plan.slots * plan.slot_rows;
+        const size_t part_bytes = GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes;
+        if (desc.size() > kStaticDescBytes)
+            return fail(GQA_ERANGE, "decode descriptors need %zu bytes; the static scratch reserves %zu",
+                        desc.size(), kStaticDescBytes);
+        if ((size_t)plan.slots * sizeof(int32_t) > kStaticCntBytes)
+            return fail(GQA_ERANGE, "%d merge counters exceed the static scratch's %zu", plan.slots,
+                        kStaticCntBytes / sizeof(int32_t));
+        if (rows * 130 * sizeof(float) > part_bytes)
+            return fail(GQA_ERANGE, "decode partials need %zu bytes; the static scratch holds %zu",
+                        rows * 130 * sizeof(float), part_bytes);
+        char *scratch = nullptr;
+        if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
+            return rc;
+        if ((rc = upload_tables(c, st)) != GQA_OK)
+            return rc;
+        cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "descriptor upload (static scratch)");
+        int32_t *counters = (int32_t *)(scratch + kStaticDescBytes);
+        if (plan.slots > 0 && (e = cudaMemsetAsync(counters, 0, (size_t)plan.slots * sizeof(int32_t), st)) !=
+                                  cudaSuccess)
+            return cuda_fail(e, "counter clear (static scratch)");
+        TcSplitWs ws;
+        ws.o = (float *)(scratch + kStaticDescBytes + kStaticCntBytes);
+        ws.ml = reinterpret_cast<float2 *>(ws.o + rows * 128);
+        ws.counters = counters;
+        ws.slot_rows = plan.slot_rows;
+        ws.ranged = plan.ranged;
+        e = launch_prefill_tc(c->view(), (const SeqDesc *)(scratch + o_sds), (const TcItem *)(scratch + o_items),
+                              (const int32_t *)(scratch + o_start), plan.grid, B, 1, H_q, q, out, ws, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "tensor-core decode kernel (static scratch)");
+        c->launches[GQA_KERNEL_PREFILL_TC] += 1;
+        return GQA_OK;
+    }
 
     // Same chunk rule as attn_decode, widened (up to 512 tokens) until the
     // partials fit in the static array.
@@ -1134,7 +1330,6 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     char *scratch = nullptr;
     if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
         return rc;
-    cudaStream_t st = (cudaStream_t)stream;
     if ((rc = upload_tables(c, st)) != GQA_OK)
         return rc;
     cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);

@@ -106,6 +106,8 @@ struct __align__(1024) TcSmem {
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
     int abort_;
+    int last_;                                         // this CTA completed a split group
+    float mrg_m[128], mrg_inv[128];                    // split merge: max and 1 / sum per row
     int s_issued[2];                                   // S MMAs of tile 0 / 1 issued so far (monotonic)
 };
 
@@ -128,6 +130,10 @@ struct TcParams {
     float scale_log2;   // log2(e) / sqrt(d_h)
     const float2 *rope; // rotary (cos, sin) [position][64], or null
     int32_t window;     // sliding window (0 = none)
+    float *ws_o;        // split items' partial O, m, l (TcSplitWs)
+    float2 *ws_ml;
+    int32_t *counters;
+    int32_t slot_rows;
 };
 
 __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
@@ -140,9 +146,10 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 // item_start[c + 1] - 1 in order.  Barrier phases run on
 // across items (global tile counter gt), so the next item's Q and first K/V
 // tile load while the current item's last tiles and epilogue run.
-// ROPE: queries rotated in-kernel (p.rope is the table); WIN: sliding window
-// (items start at key tile j0, keys before the window masked).  Both are
-// template flags so the plain path carries none of their instructions.
+// ROPE: queries rotated in-kernel (p.rope is the table); WIN: items may start
+// past key tile 0 (a sliding window, whose keys before the window are
+// masked, or split items).  Both are template flags so the plain path
+// carries none of their instructions.
 template <bool ROPE, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
@@ -353,18 +360,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                            (acc || ks > 0) ? 1u : 0u);
             };
             // One flat stream of key tiles over this CTA's items: tile g is
-            // tile j of item k.  The S buffer alternates S0(g), S1(g), S0(g+1),
-            // ...: each S waits until the softmax warps have read the one
-            // before it (s_free completions alternate between the two tiles).
+            // tile j of item k.  The S buffer takes S0(g), S1(g), S0(g+1), ...
+            // (S1 only for items whose second query tile holds a valid row):
+            // each S waits until the softmax warps have read the one before
+            // it, s_free completing once per S read.
             bool ok = true;
-            uint32_t g = 0;
+            uint32_t g = 0, ns = 0, g1 = 0;                 // key tiles, S MMAs, tile-1 PVs
             int k = 0;
             if (warp == 1) {
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
                     const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
+                    const bool two = p.items[idx].tiles > 1;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
-                        ok = (g == 0 || mbar_wait(&s.s_free, 1, &s.abort_)) &&
+                        ok = (ns == 0 || mbar_wait(&s.s_free, (ns - 1) & 1, &s.abort_)) &&
                              (j > j0 || mbar_wait(ROPE ? &s.q_rot[0] : &s.bar_q, k & 1, &s.abort_)) &&
                              mbar_wait(&s.k_full[st], (g / kKStages) & 1, &s.abort_);
                         if (!ok)
@@ -373,14 +382,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         issue_s(0, st);
                         mma_commit(&s.s_full[0]);
                         *(volatile int *)&s.s_issued[0] = (int)g + 1;
-                        ok = mbar_wait(&s.s_free, 0, &s.abort_) &&
-                             (j > j0 || !ROPE || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
+                        ++ns;
+                        // The second tile's rotation is awaited once per item
+                        // either way, which keeps q_rot[1]'s phases in step.
+                        ok = (j > j0 || !ROPE || mbar_wait(&s.q_rot[1], k & 1, &s.abort_));
+                        if (ok && two) {
+                            ok = mbar_wait(&s.s_free, (ns - 1) & 1, &s.abort_);
+                            if (ok) {
+                                tc_fence_after();
+                                issue_s(1, st);
+                                mma_commit(&s.s_full[1]);
+                                *(volatile int *)&s.s_issued[1] = (int)g + 1;
+                                ++ns;
+                            }
+                        }
                         if (!ok)
                             break;
-                        tc_fence_after();
-                        issue_s(1, st);
-                        mma_commit(&s.s_full[1]);
-                        *(volatile int *)&s.s_issued[1] = (int)g + 1;
                         mma_commit(&s.k_empty[st]);
                         if (j + 1 == nt)
                             mma_commit(&s.q_empty);      // the last S of the item has read Q
@@ -401,6 +418,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 };
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
                     const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
+                    const bool two = p.items[idx].tiles > 1;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int sv = g % kVStages;
                         const bool order = kPvOrder && j + 1 < nt;
@@ -413,14 +431,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                         tc_fence_after();
                         issue_o(0, sv, j > j0);
                         mma_commit(&s.pv_done[0]);
-                        ok = mbar_wait(&s.p_full[1], g & 1, &s.abort_);
-                        if (!ok)
-                            break;
-                        if (order)
-                            after_s(1, g + 2);
-                        tc_fence_after();
-                        issue_o(1, sv, j > j0);
-                        mma_commit(&s.pv_done[1]);
+                        if (two) {
+                            ok = mbar_wait(&s.p_full[1], g1 & 1, &s.abort_);
+                            if (!ok)
+                                break;
+                            if (order)
+                                after_s(1, g + 2);
+                            tc_fence_after();
+                            issue_o(1, sv, j > j0);
+                            mma_commit(&s.pv_done[1]);
+                            ++g1;
+                        }
                         mma_commit(&s.v_empty[sv]);
                     }
                 }
@@ -521,6 +542,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const SeqDesc sd = p.seqs[it.b];
             if (ROPE && idx + 1 < i_end)
                 prefetch_rows(p.items[idx + 1]);         // the next item's table rows into L2
+            if (t == 1 && it.tiles < 2) {
+                // No valid row in this item's second tile: nothing is issued
+                // for it (its rows are padding, zeroed with the cache write).
+                // Only the next item's rotation, which the S issuer awaits
+                // once per item, is this warpgroup's part.
+                if (ROPE && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                continue;
+            }
             const int nt = it.nt;
             const bool row_in_box = r < p.G * p.rows_pos;
             const int rel = it.i0 + t * p.rows_pos + r / p.G;   // row within the batch entry
@@ -642,6 +674,74 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 break;
             }
             tc_fence_after();
+            if (WIN && it.part >= 0) {
+                // Split item: this range's unnormalised O and its (m, l) go
+                // to workspace slot it.part, column-major so that a warp's
+                // rows are adjacent; the CTA that completes the group's last
+                // split merges the group's slots into out.
+                const bool mine = valid && r < p.slot_rows;
+                float *po = p.ws_o + (size_t)it.part * D * p.slot_rows + r;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t u[32];
+                    __syncwarp();
+                    tmem_ld32(tO + 32 * h, u);
+                    if (mine) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            __stcg(po + (size_t)(32 * h + i) * p.slot_rows, __uint_as_float(u[i]));
+                    }
+                }
+                if (mine)
+                    __stcg(p.ws_ml + (size_t)it.part * p.slot_rows + r, make_float2(m, l));
+                __threadfence();
+                tc_fence_before();
+                named_bar_sync(1 + t, 128);
+                const int first = it.part - it.split;
+                if (r == 0)
+                    s.last_ = atomicAdd(p.counters + first, 1) == it.nsplit - 1;
+                named_bar_sync(1 + t, 128);
+                if (s.last_) {
+                    // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max_s m_s (a
+                    // split without a visible key for a row has m = -inf, l = 0): per
+                    // row M and 1 / sum first, then one thread per column over the rows.
+                    __threadfence();
+                    const int rows = min(p.slot_rows, sd.count * p.G);
+                    const float2 *ml = p.ws_ml + (size_t)first * p.slot_rows;
+                    if (r < rows) {
+                        float M = -INFINITY, Lsum = 0.0f;
+                        for (int q2 = 0; q2 < it.nsplit; ++q2)
+                            M = fmaxf(M, __ldcg(ml + (size_t)q2 * p.slot_rows + r).x);
+                        if (M == -INFINITY)                  // no visible key at all: zeros, not NaN
+                            M = 0.0f;
+                        for (int q2 = 0; q2 < it.nsplit; ++q2) {
+                            const float2 v2 = __ldcg(ml + (size_t)q2 * p.slot_rows + r);
+                            Lsum += ex2(v2.x - M) * v2.y;
+                        }
+                        s.mrg_m[r] = M;
+                        s.mrg_inv[r] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+                    }
+                    named_bar_sync(1 + t, 128);
+                    const int col = r;                          // this thread's column
+                    const float *o0 = p.ws_o + ((size_t)first * D + col) * p.slot_rows;
+                    for (int rr = 0; rr < rows; ++rr) {
+                        const float M = s.mrg_m[rr];
+                        float acc = 0.0f;
+#pragma unroll 4
+                        for (int q2 = 0; q2 < it.nsplit; ++q2) {
+                            const float w = ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rr).x - M);
+                            acc += w * __ldcg(o0 + (size_t)q2 * D * p.slot_rows + rr);
+                        }
+                        const int relr = it.i0 + rr / p.G;
+                        p.out[(((size_t)it.b * p.n + relr) * p.H_q + it.kvh * p.G + rr % p.G) * D + col] =
+                            __float2bfloat16_rn(acc * s.mrg_inv[rr]);
+                    }
+                    if (r == 0)
+                        p.counters[first] = 0;               // ready for the next launch
+                }
+                gt += nt - j0;
+                continue;
+            }
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             unsigned char *stage = reinterpret_cast<unsigned char *>(s.o[t]) + r * 128;
 #pragma unroll 1
@@ -725,7 +825,7 @@ int prefill_tc_rows_per_tile(int group) { return 128 / group; }
 
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
-                              cudaStream_t st)
+                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start)
 {
     if (pv.d != D || grid <= 0)
         return grid <= 0 ? cudaSuccess : cudaErrorInvalidValue;
@@ -763,9 +863,13 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     prm.rope = pv.rope;
     prm.window = pv.window;
+    prm.ws_o = ws.o;
+    prm.ws_ml = ws.ml;
+    prm.counters = ws.counters;
+    prm.slot_rows = ws.slot_rows;
     const int smem = (int)sizeof(TcSmem) + 1024;
     static bool attr_set[4] = {false, false, false, false};
-    const int which = (pv.rope ? 1 : 0) + (pv.window > 0 ? 2 : 0);
+    const int which = (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
     void (*const kern[4])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
         prefill_tc_kernel<false, false>, prefill_tc_kernel<true, false>, prefill_tc_kernel<false, true>,
         prefill_tc_kernel<true, true>};
@@ -775,6 +879,8 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
             return e;
         attr_set[which] = true;
     }
+    if (ev_start)
+        cudaEventRecord(ev_start, st);       // after the host-side preparation above
     kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
     return cudaGetLastError();
 }

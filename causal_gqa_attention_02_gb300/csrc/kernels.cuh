@@ -73,10 +73,30 @@ struct DecodeItem {
 };
 
 // One tensor-core prefill work item: two 128-row query tiles of batch entry
-// b and KV head kvh, starting at row i0 of the entry; nt key tiles of 128.
+// b and KV head kvh, starting at row i0 of the entry; key tiles j0 .. nt-1
+// of 128.  tiles = 1 when the second query tile holds no valid row (short
+// calls such as decode and multi-token decode): it is then skipped, and its
+// rows are padding.  A split item (part >= 0; one tile holding every row of
+// the entry) covers one range of the entry's key tiles: its unnormalised
+// O, m and l go to workspace slot `part`, the group's nsplit slots are
+// part - split .. part - split + nsplit - 1, and the CTA that finishes the
+// group's last split merges them into out.
 struct TcItem {
-    int32_t b, kvh, i0, nt;   // key tiles j0 .. nt-1 (j0 > 0 only under a sliding window)
-    int32_t j0, pad_;
+    int32_t b, kvh, i0, nt;
+    int32_t j0, tiles;
+    int32_t part, split, nsplit, pad_;
+};
+
+// Workspace of split items: slot s holds rows 0 .. slot_rows-1 of one query
+// tile, column-major (o[(s * 128 + column) * slot_rows + row]), and (m, l)
+// per row (ml[s * slot_rows + row]).  counters[first slot of a group] must
+// be zero on entry; the kernel leaves them zero.
+struct TcSplitWs {
+    float *o = nullptr;
+    float2 *ml = nullptr;
+    int32_t *counters = nullptr;
+    int32_t slot_rows = 0;
+    bool ranged = false;      // some item starts past key tile 0 (window or split)
 };
 
 // Error-word bits (mirror include/gqa.h).
@@ -132,9 +152,11 @@ int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // Persistent grid of `grid` CTAs; CTA c takes items[item_start[c] ..
 // item_start[c + 1]) in order (grid + 1 offsets, every run non-empty).  Rows
 // of the items' query tiles past the valid length are written as zeros;
-// padding rows that no item covers must be zeroed by the caller.
+// padding rows that no item covers must be zeroed by the caller.  ev_start,
+// if given, is recorded on st right before the kernel, after the tensor maps
+// are encoded on the host.
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
-                              cudaStream_t st);
+                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start = nullptr);
 
 }  // namespace gqa

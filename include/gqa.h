@@ -276,8 +276,9 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
  * (with rope = 1, q rotated by L_b - 1).
  *  seq_ids  host int32[B], live sequences of length >= 1 (repeats allowed).
  *  q        device [B, H_q, d_h];  out  device [B, H_q, d_h].
- * Split-K partials and merge counters live in library-owned device memory that grows with
- * cudaMalloc on first use of a larger shape.
+ * The kernel is chosen by gqa_set_decode_kernel.  Split-K partials and merge
+ * counters live in library-owned device memory that grows with cudaMalloc on
+ * first use of a larger shape.
  * Errors: GQA_EINVAL, GQA_EMASK (empty sequence), GQA_ECUDA. */
 int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                 const void *q, void *out, void *stream);
@@ -291,9 +292,10 @@ int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q
  * afford the device-wide synchronisation of cudaFree.  attn_decode may hit
  * that synchronisation when its workspace grows.
  *
- * Arguments, results and errors are those of attn_decode.  The cache must be
- * bf16 with d_h = 128, and H_q / H_kv must be at most 8, because this call
- * runs only the split-K decode kernels.  Other shapes get GQA_EINVAL.
+ * Arguments, results and errors are those of attn_decode, and so are the
+ * kernel and its work split: the results are the same bits.  The cache must
+ * be bf16 with d_h = 128 (and H_q / H_kv at most 8 on the CUDA-core kernel);
+ * other shapes get GQA_EINVAL.
  * The split-K partials, the per-call descriptors and the merge counters live
  * in one static device array of GQA_STATIC_SCRATCH_BYTES.  The library reserves that array
  * on every GPU that loads it, until the process exits.  A call whose partials
@@ -310,6 +312,26 @@ int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q
 #define GQA_STATIC_SCRATCH_BYTES (16u << 20)
 int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                        const void *q, void *out, void *stream);
+
+/* Decode kernel of attn_decode and attn_decode_static.
+ *  GQA_DECODE_AUTO         (default) tensor-core when the cache is bf16 with
+ *                          d_h = 128, else CUDA-core.
+ *  GQA_DECODE_TENSOR_CORE  the prefill kernel with one query row per
+ *                          sequence: every KV head's key tiles are read once
+ *                          by TMA, a sequence's tiles are split into ranges
+ *                          across SMs when there are too few sequences, and
+ *                          the ranges' partial (m, l, O) are merged inside
+ *                          the kernel by the CTA that finishes last.  Needs
+ *                          bf16 and d_h = 128 (else GQA_EINVAL here).
+ *  GQA_DECODE_CUDA_CORE    the split-K CUDA-core decode kernel (bf16, d_h =
+ *                          128, H_q / H_kv <= 8), else the generic CUDA-core
+ *                          kernel.
+ * Both compute the same softmax; they differ in rounding order only.
+ * Errors: GQA_EINVAL (unknown choice, or tensor-core on another cache). */
+#define GQA_DECODE_AUTO         0
+#define GQA_DECODE_TENSOR_CORE  1
+#define GQA_DECODE_CUDA_CORE    2
+int gqa_set_decode_kernel(gqa_cache *cache, int32_t kernel);
 
 /* Prefix-edit invalidation ([P3] edit at token m): keep positions < m of
  * `seq`, drop the rest.  Pages wholly beyond position m lose one reference
@@ -330,7 +352,7 @@ int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
 /* Kernel ids for gqa_profile_read. */
 #define GQA_KERNEL_CACHE_WRITE     0  /* new K/V rows into their pages           */
 #define GQA_KERNEL_COW_COPY        1  /* copy-on-write of a shared tail page      */
-#define GQA_KERNEL_PREFILL_TC      2  /* tensor-core causal prefill (bf16, 128)   */
+#define GQA_KERNEL_PREFILL_TC      2  /* tensor-core attention (bf16, 128): prefill, multi-token and tensor-core decode */
 #define GQA_KERNEL_ATTN_SIMT       3  /* CUDA-core attention (fp32 / other d_h)   */
 #define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode (bf16, 128), merge included */
 #define GQA_KERNEL_DECODE_COMBINE  5  /* reserved: the merge runs inside the split kernel */

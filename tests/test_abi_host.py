@@ -305,3 +305,17 @@ def test_windowed_work_counts_match_brute_force():
                     vis &= j[None, :] > qpos[:, None] - W
                 assert gqa.work.causal_pairs(past, new, W) == int(vis.sum()), (past, new, W)
     assert gqa.work.decode_kv_bytes([10, 100], 2, 8, 2, window=16) == (10 + 16) * 2 * 2 * 8 * 2
+
+
+def test_decode_kernel_choice_is_checked():
+    c = gqa.Cache(2, 8, 8, 2, 2, dtype="f32", metadata_only=True)
+    c.set_decode_kernel("cuda_core")
+    c.set_decode_kernel("auto")
+    with pytest.raises(gqa.GqaError) as e:          # the tensor-core kernel is bf16, d_h = 128 only
+        c.set_decode_kernel("tensor_core")
+    assert e.value.name == "EINVAL"
+    with pytest.raises(gqa.GqaError) as e:
+        gqa._check(gqa._lib.gqa_set_decode_kernel(c.handle, 7))
+    assert e.value.name == "EINVAL"
+    b = gqa.Cache(2, 128, 8, 2, 2, dtype="bf16", metadata_only=True)
+    b.set_decode_kernel("tensor_core")

@@ -15,7 +15,8 @@ Workload shapes follow the five configurations the path is specified on:
   2. bf16 ragged prefill, right padded,
   3. bf16 paged decode with a randomly permuted page placement,
   4. wide-GQA long context: 8192-token prefill then 256 decode steps,
-  5. prefix reuse: one shared 4096-token prefix, 8 forks, then an edit.
+  5. prefix reuse: one shared 4096-token prefix, 8 forks, then an edit,
+  6. multi-token decode: T-token draft chunks over configuration 3's cache.
 """
 from __future__ import annotations
 
@@ -139,6 +140,17 @@ def paged_decode(seed: int = seed_for(3), B=64, H_q=32, H_kv=8, d=128,
             "new_k": draw(rng, dtype, (B, H_kv, d)),
             "new_v": draw(rng, dtype, (B, H_kv, d)),
             "q": draw(rng, dtype, (B, H_q, d))}
+
+
+def draft_chunk(seed: int = seed_for(6), B=64, T=4, H_q=32, H_kv=8, d=128, dtype="bf16"):
+    """T new tokens per sequence (a multi-token decode / speculative draft
+    block) to run over an existing cache: q [B, T, H_q, d], k and v
+    [B, T, H_kv, d]."""
+    rng = np.random.default_rng(seed)
+    return {"dtype": dtype, "B": B, "T": T, "H_q": H_q, "H_kv": H_kv, "d": d,
+            "q": draw(rng, dtype, (B, T, H_q, d)),
+            "k": draw(rng, dtype, (B, T, H_kv, d)),
+            "v": draw(rng, dtype, (B, T, H_kv, d))}
 
 
 # --------------------------------------------------------------------------
