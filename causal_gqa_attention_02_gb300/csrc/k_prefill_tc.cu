@@ -675,12 +675,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             tc_fence_after();
             if (WIN && it.part >= 0) {
-                // Split item: this range's unnormalised O and its (m, l) go
-                // to workspace slot it.part, column-major so that a warp's
-                // rows are adjacent; the CTA that completes the group's last
-                // split merges the group's slots into out.
+                // Split item: this range's unnormalised O row and its (m, l)
+                // go to workspace slot it.part; the CTA that completes the
+                // group's last split merges the group's slots into out.
                 const bool mine = valid && r < p.slot_rows;
-                float *po = p.ws_o + (size_t)it.part * D * p.slot_rows + r;
+                float4 *po = reinterpret_cast<float4 *>(p.ws_o + ((size_t)it.part * p.slot_rows + r) * D);
 #pragma unroll 1
                 for (int h = 0; h < 4; ++h) {
                     uint32_t u[32];
@@ -688,8 +687,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     tmem_ld32(tO + 32 * h, u);
                     if (mine) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            __stcg(po + (size_t)(32 * h + i) * p.slot_rows, __uint_as_float(u[i]));
+                        for (int i = 0; i < 8; ++i)
+                            __stcg(po + 8 * h + i, make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                                               __uint_as_float(u[4 * i + 2]),
+                                                               __uint_as_float(u[4 * i + 3])));
                     }
                 }
                 if (mine)
@@ -703,39 +704,100 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 named_bar_sync(1 + t, 128);
                 if (s.last_) {
                     // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max_s m_s (a
-                    // split without a visible key for a row has m = -inf, l = 0): per
-                    // row M and 1 / sum first, then one thread per column over the rows.
+                    // split without a visible key for a row has m = -inf, l = 0).  Per
+                    // row M and 1 / sum, and the weights 2^(m_s - M) / sum into this
+                    // warpgroup's staging buffer when they fit; then one thread per
+                    // column, up to 16 rows at a time, so that its loads of all the
+                    // rows and of several splits are in flight together.
                     __threadfence();
                     const int rows = min(p.slot_rows, sd.count * p.G);
+                    const int nsp = it.nsplit;
                     const float2 *ml = p.ws_ml + (size_t)first * p.slot_rows;
                     if (r < rows) {
-                        float M = -INFINITY, Lsum = 0.0f;
-                        for (int q2 = 0; q2 < it.nsplit; ++q2)
-                            M = fmaxf(M, __ldcg(ml + (size_t)q2 * p.slot_rows + r).x);
+                        // Sixteen (m, l) pairs per round, all loads in flight.
+                        float M = -INFINITY;
+                        for (int q0 = 0; q0 < nsp; q0 += 16) {
+                            float2 v2[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v2[i] = q0 + i < nsp ? __ldcg(ml + (size_t)(q0 + i) * p.slot_rows + r)
+                                                     : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                M = fmaxf(M, v2[i].x);
+                        }
                         if (M == -INFINITY)                  // no visible key at all: zeros, not NaN
                             M = 0.0f;
-                        for (int q2 = 0; q2 < it.nsplit; ++q2) {
-                            const float2 v2 = __ldcg(ml + (size_t)q2 * p.slot_rows + r);
-                            Lsum += ex2(v2.x - M) * v2.y;
+                        float Lsum = 0.0f;
+                        for (int q0 = 0; q0 < nsp; q0 += 16) {
+                            float2 v2[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v2[i] = q0 + i < nsp ? __ldcg(ml + (size_t)(q0 + i) * p.slot_rows + r)
+                                                     : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                Lsum += ex2(v2[i].x - M) * v2[i].y;
                         }
                         s.mrg_m[r] = M;
                         s.mrg_inv[r] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
                     }
+                    float *wsm = reinterpret_cast<float *>(s.o[t]);
+                    const bool wfit = nsp * rows <= (int)(sizeof(s.o[0]) / sizeof(float));
+                    if (r == 0)
+                        tma_store_wait_read();               // earlier stores have left the buffer
                     named_bar_sync(1 + t, 128);
-                    const int col = r;                          // this thread's column
-                    const float *o0 = p.ws_o + ((size_t)first * D + col) * p.slot_rows;
-                    for (int rr = 0; rr < rows; ++rr) {
-                        const float M = s.mrg_m[rr];
-                        float acc = 0.0f;
-#pragma unroll 4
-                        for (int q2 = 0; q2 < it.nsplit; ++q2) {
-                            const float w = ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rr).x - M);
-                            acc += w * __ldcg(o0 + (size_t)q2 * D * p.slot_rows + rr);
+                    if (wfit)
+                        for (int f = r; f < nsp * rows; f += 128) {
+                            const int q2 = f / rows, rr = f - q2 * rows;
+                            wsm[f] = ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rr).x - s.mrg_m[rr]) * s.mrg_inv[rr];
                         }
-                        const int relr = it.i0 + rr / p.G;
-                        p.out[(((size_t)it.b * p.n + relr) * p.H_q + it.kvh * p.G + rr % p.G) * D + col] =
-                            __float2bfloat16_rn(acc * s.mrg_inv[rr]);
+                    named_bar_sync(1 + t, 128);
+                    // Thread r: columns 4 * (r % 32) .. + 3 of rows r / 32, + 4, + 8, ...,
+                    // two rows and eight splits per round (16 loads of 16 bytes in flight).
+                    const int c4 = r & 31, sub = r >> 5;
+                    const float4 *o4 = reinterpret_cast<const float4 *>(p.ws_o) + c4;
+                    for (int ra = sub; ra < rows; ra += 8) {
+                        const int rb = ra + 4;                  // second row of the pair (if < rows)
+                        float4 acc_a = make_float4(0.f, 0.f, 0.f, 0.f), acc_b = acc_a;
+                        for (int q0 = 0; q0 < nsp; q0 += 8) {
+                            float4 va[8], vb[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const size_t sl = (size_t)(first + q0 + i) * p.slot_rows;
+                                va[i] = q0 + i < nsp ? __ldcg(o4 + (sl + ra) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                vb[i] = q0 + i < nsp && rb < rows ? __ldcg(o4 + (sl + rb) * (D / 4))
+                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (q0 + i >= nsp)
+                                    break;
+                                const int q2 = q0 + i;
+                                const float wa = wfit ? wsm[q2 * rows + ra]
+                                                      : ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + ra).x - s.mrg_m[ra]) *
+                                                            s.mrg_inv[ra];
+                                acc_a.x += wa * va[i].x, acc_a.y += wa * va[i].y;
+                                acc_a.z += wa * va[i].z, acc_a.w += wa * va[i].w;
+                                if (rb < rows) {
+                                    const float wb = wfit ? wsm[q2 * rows + rb]
+                                                          : ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rb).x -
+                                                                s.mrg_m[rb]) * s.mrg_inv[rb];
+                                    acc_b.x += wb * vb[i].x, acc_b.y += wb * vb[i].y;
+                                    acc_b.z += wb * vb[i].z, acc_b.w += wb * vb[i].w;
+                                }
+                            }
+                        }
+                        auto put = [&](int rr, const float4 &a) {
+                            __nv_bfloat16 *o = p.out +
+                                (((size_t)it.b * p.n + it.i0 + rr / p.G) * p.H_q + it.kvh * p.G + rr % p.G) * D + 4 * c4;
+                            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+                        };
+                        put(ra, acc_a);
+                        if (rb < rows)
+                            put(rb, acc_b);
                     }
+                    named_bar_sync(1 + t, 128);              // the staging buffer is free again
                     if (r == 0)
                         p.counters[first] = 0;               // ready for the next launch
                 }

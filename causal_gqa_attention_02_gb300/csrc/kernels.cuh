@@ -88,8 +88,8 @@ struct TcItem {
 };
 
 // Workspace of split items: slot s holds rows 0 .. slot_rows-1 of one query
-// tile, column-major (o[(s * 128 + column) * slot_rows + row]), and (m, l)
-// per row (ml[s * slot_rows + row]).  counters[first slot of a group] must
+// tile (o[(s * slot_rows + row) * 128 + column]) and (m, l) per row
+// (ml[s * slot_rows + row]).  counters[first slot of a group] must
 // be zero on entry; the kernel leaves them zero.
 struct TcSplitWs {
     float *o = nullptr;
