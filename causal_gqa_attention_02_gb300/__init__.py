@@ -82,6 +82,7 @@ _sig("attn_prefill", ctypes.c_int, _vp, _i32, _I32P, _i32, _i32, _vp, _vp, _vp, 
 _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
+_sig("attn_decode_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
 _sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
@@ -330,6 +331,27 @@ def attn_decode(cache: Cache, seq_ids, q, out=None, stream=None):
     return out
 
 
+def attn_decode_append(cache: Cache, seq_ids, q, k_new, v_new, out=None, stream=None):
+    """One decode step: append k_new, v_new [B, H_kv, d] at each sequence's
+    tail and attend q [B, H_q, d] to the cache including them."""
+    B, H_q = len(seq_ids), q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    shape = (B, H_q, cache.head_dim)
+    kv_shape = (B, cache.num_kv_heads, cache.head_dim)
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode_append(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
+                                   _dev_ptr(k_new, "k_new", cache.torch_dtype, kv_shape),
+                                   _dev_ptr(v_new, "v_new", cache.torch_dtype, kv_shape),
+                                   _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+    return out
+
+
+def attn_decode_append_meta(cache: Cache, seq_ids, H_q):
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode_append(cache.handle, len(seq_ids), sp, H_q, None, None, None, None, None))
+
+
 def attn_decode_static(cache: Cache, seq_ids, q, out=None, stream=None):
     """attn_decode without device allocation: the split-K partials live in
     the library's fixed static device array (see include/gqa.h)."""
@@ -358,4 +380,5 @@ def exported_symbols():
             "gqa_layout_compatible", "gqa_seq_create", "gqa_seq_fork", "gqa_seq_free",
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
-            "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel"]
+            "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel",
+            "attn_decode_append"]

@@ -1113,6 +1113,70 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
     });
 }
 
+int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q,
+                       const void *k_new, const void *v_new, void *out, void *stream)
+{
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    if (!c->meta_only && (!q || !k_new || !v_new || !out))
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    const int G = H_q / H_kv;
+    const int use_tc = c->meta_only ? 0 : decode_uses_tc(c, G);
+    if (use_tc < 0)
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+    if (!use_tc) {
+        // CUDA-core kernels: the write, then the decode.
+        int rc = kv_append(c, B, seq_ids, 1, nullptr, k_new, v_new, stream);
+        return rc != GQA_OK ? rc : attn_decode(c, B, seq_ids, H_q, q, out, stream);
+    }
+    std::vector<WriteReq> req(B);
+    for (int b = 0; b < B; ++b)
+        req[b] = WriteReq{seq_ids[b], 1};
+    int rc = check_write(c, req.data(), B);
+    if (rc != GQA_OK)
+        return rc;
+    if ((rc = check_device(c)) != GQA_OK)
+        return rc;
+    std::vector<SeqDesc> sds;                 // past = the length before this call, count = 1
+    std::vector<CowDesc> cows;
+    commit_write(c, req.data(), B, sds, cows);
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    TcPlan plan;
+    plan_tc(c, sds, G, plan);
+    Stage stg(c->h_stage);
+    const size_t o_sds = stg.add(sds.data(), sds.size());
+    const size_t o_cow = stg.add(cows.data(), cows.size());
+    const size_t o_items = stg.add(plan.items.data(), plan.items.size());
+    const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
+    TcSplitWs ws;
+    if ((rc = tc_workspace(c, plan, ws)) != GQA_OK)
+        return rc;
+    if ((rc = upload_stage(c, st)) != GQA_OK)
+        return rc;
+    const PoolView pv = c->view();
+    if (!cows.empty() &&
+        (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
+             rec(ev, st);
+             return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
+         })) != GQA_OK)
+        return rc;
+    rc = run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core decode kernel", [&](cudaEvent_t ev) {
+        return launch_prefill_tc(pv, (const SeqDesc *)(c->d_stage + o_sds), (const TcItem *)(c->d_stage + o_items),
+                                 (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev,
+                                 k_new, v_new);
+    });
+    if (rc == GQA_OK)
+        release_windows(c, B, seq_ids);
+    return rc;
+}
+
 int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
 {
     if (!c)

@@ -118,6 +118,7 @@ struct TcParams {
     const TcItem *items;      // grouped by CTA: CTA c takes items[item_start[c] .. item_start[c + 1])
     const int32_t *item_start;
     const int32_t *tables;
+    void *pool;               // page pool (bf16), for the appended rows below
     int32_t stride;
     int32_t num_pages;
     int32_t H_kv;
@@ -134,6 +135,8 @@ struct TcParams {
     float2 *ws_ml;
     int32_t *counters;
     int32_t slot_rows;
+    const __nv_bfloat16 *app_k;   // fused append: this call's one new K and V row per entry
+    const __nv_bfloat16 *app_v;   // ([B, H_kv, 128]), written at position past; null = none
 };
 
 __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
@@ -242,6 +245,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 tma_load_4d(&mQ, &s.bar_q, s.q[lane >> 1][lane & 1], 64 * (lane & 1), it.kvh * p.G,
                             it.i0 + (lane >> 1) * p.rows_pos, it.b);
         };
+        // Fused append (decode, count = 1): the warp writes this call's K
+        // (warp 0) or V (warp 3) row of head kvh at position past into its
+        // page slot, with the rotation of the cache write for K under ROPE
+        // (pairs (e, e + 64) rotated by the position, each product, sum and
+        // difference rounded to fp32), then orders the writes before the
+        // TMA load that reads them.  Lane l holds elements 4l .. 4l + 3.
+        auto append_row = [&](const TcItem &it, const SeqDesc &sd) {
+            const int pos = sd.past;
+            const int pg = p.tables[(size_t)sd.row * p.stride + pos / kPageTokens];
+            if (pg < 0 || pg >= p.num_pages) {
+                if (lane == 0)
+                    atomicOr(p.err, kErrPageId);
+                return;
+            }
+            const __nv_bfloat16 *src = (vside ? p.app_v : p.app_k) + ((size_t)it.b * p.H_kv + it.kvh) * D;
+            uint2 val = reinterpret_cast<const uint2 *>(src)[lane];
+            if (ROPE && !vside) {
+                uint2 oth;
+                oth.x = __shfl_xor_sync(0xffffffffu, val.x, 16);
+                oth.y = __shfl_xor_sync(0xffffffffu, val.y, 16);
+                const bool first = lane < 16;            // elements < 64: the x of each pair
+                const float2 *cs = p.rope + (size_t)pos * (D / 2) + 4 * (lane & 15);
+                const __nv_bfloat16 *a = reinterpret_cast<const __nv_bfloat16 *>(&val);
+                const __nv_bfloat16 *b2 = reinterpret_cast<const __nv_bfloat16 *>(&oth);
+                uint2 res;
+                __nv_bfloat16 *rr = reinterpret_cast<__nv_bfloat16 *>(&res);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = __bfloat162float(first ? a[e] : b2[e]);
+                    const float y = __bfloat162float(first ? b2[e] : a[e]);
+                    const float2 tcs = __ldg(cs + e);
+                    const float o = first ? __fsub_rn(__fmul_rn(x, tcs.x), __fmul_rn(y, tcs.y))
+                                          : __fadd_rn(__fmul_rn(x, tcs.y), __fmul_rn(y, tcs.x));
+                    rr[e] = __float2bfloat16_rn(o);
+                }
+                val = res;
+            }
+            const int slot = pos & (kPageTokens - 1), bo = lane * 8;
+            char *blk = reinterpret_cast<char *>(p.pool) +
+                        ((size_t)(pg * 2 + (vside ? 1 : 0)) * p.H_kv + it.kvh) * (size_t)(kPageElems * 2);
+            *reinterpret_cast<uint2 *>(blk + (((slot >> 3) * 2 + (bo >> 7)) << 10) + ((slot & 7) << 7) + (bo & 127)) = val;
+            fence_proxy_async_global();
+            __syncwarp();
+        };
         // Loads this warp's half (K or V) of key tile j of an item into
         // stage gt % stages once its last readers are done.
         auto load_tile = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
@@ -267,6 +314,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             __nv_bfloat16 *dst = vside ? s.v[st][0] : s.k[st][0];
             if (use > 0 && !wait0(empty, (use - 1) & 1))
                 return false;
+            if (p.app_k && j == it.nt - 1 && (sd.past >> 7) == j)
+                append_row(it, sd);                       // the tile holds this call's new token: write it first
             if (lane == 0)
                 mbar_arrive_expect_tx(full, 2 * kTileBytes);
             __syncwarp();
@@ -887,7 +936,8 @@ int prefill_tc_rows_per_tile(int group) { return 128 / group; }
 
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
-                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start)
+                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start, const void *app_k,
+                              const void *app_v)
 {
     if (pv.d != D || grid <= 0)
         return grid <= 0 ? cudaSuccess : cudaErrorInvalidValue;
@@ -913,6 +963,9 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.items = d_items;
     prm.item_start = d_item_start;
     prm.tables = pv.tables;
+    prm.pool = pv.pool;
+    prm.app_k = (const __nv_bfloat16 *)app_k;
+    prm.app_v = (const __nv_bfloat16 *)app_v;
     prm.stride = pv.stride;
     prm.num_pages = pv.num_pages;
     prm.H_kv = pv.H_kv;

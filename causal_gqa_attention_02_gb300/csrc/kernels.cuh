@@ -154,9 +154,12 @@ int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // of the items' query tiles past the valid length are written as zeros;
 // padding rows that no item covers must be zeroed by the caller.  ev_start,
 // if given, is recorded on st right before the kernel, after the tensor maps
-// are encoded on the host.
+// are encoded on the host.  app_k / app_v (decode only: count = 1 for every
+// entry, [B, H_kv, 128]) fuse the append: the row of each entry is written
+// at position past by the CTA that reads that page, before it reads it.
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
-                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start = nullptr);
+                              const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start = nullptr,
+                              const void *app_k = nullptr, const void *app_v = nullptr);
 
 }  // namespace gqa

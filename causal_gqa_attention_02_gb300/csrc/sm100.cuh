@@ -178,6 +178,9 @@ __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bu
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) reads.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Orders this thread's generic-proxy writes to global memory before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // ---- tcgen05: tensor memory ------------------------------------------------------
 

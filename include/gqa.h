@@ -283,6 +283,25 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
 int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                 const void *q, void *out, void *stream);
 
+/* attn_decode_append -- one decode step: kv_append of one token per
+ * sequence, then attn_decode at that token ([P3] decode: the step's own key
+ * and value join the cache and the query attends to the old cache plus
+ * them; [P2] toy decoder).  For each b, k_new[b] and v_new[b] are written at
+ * position L_b (the length before the call; rotated as in kv_append when
+ * rope = 1), the length becomes L_b + 1, and out[b] is attn_decode's result
+ * for the query at position L_b.  The cache and out hold the same bits as
+ * kv_append(n = 1) followed by attn_decode.  On the tensor-core decode
+ * kernel the write happens inside the attention kernel: the CTA that reads
+ * a sequence's last page writes the row there first, so a step is one
+ * launch (two when a shared tail page must first be copied).  Otherwise
+ * the two calls run in turn.
+ *  seq_ids  host int32[B], distinct live sequences.
+ *  q        device [B, H_q, d_h];  k_new, v_new  device [B, H_kv, d_h];
+ *  out      device [B, H_q, d_h].
+ * Errors: those of kv_append and attn_decode. */
+int attn_decode_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
+                       const void *q, const void *k_new, const void *v_new, void *out, void *stream);
+
 /* attn_decode_static -- attn_decode that allocates no device memory.
  *
  * The pages define no counterpart to this call.  It is for callers that must

@@ -319,3 +319,18 @@ def test_decode_kernel_choice_is_checked():
     assert e.value.name == "EINVAL"
     b = gqa.Cache(2, 128, 8, 2, 2, dtype="bf16", metadata_only=True)
     b.set_decode_kernel("tensor_core")
+
+
+def test_fused_decode_step_bookkeeping_matches_append():
+    lib, model = _pair(pages=10, per_seq=6)
+    a, b = lib.seq_create(), lib.seq_create()
+    model.create(), model.create()
+    gqa.kv_append_meta(lib, [a, b], 16, [15, 3])
+    model.write([a, b], [_rows(15), _rows(3)], [_rows(15), _rows(3)])
+    for t in range(20):
+        gqa.attn_decode_append_meta(lib, [a, b], 4)
+        model.write([a, b], [_rows(1), _rows(1)], [_rows(1), _rows(1)])
+        _same_state(lib, model)
+    with pytest.raises(gqa.GqaError) as e:                      # distinct sequences, as for a write
+        gqa.attn_decode_append_meta(lib, [a, a], 4)
+    assert e.value.name == "EINVAL"
