@@ -11,8 +11,8 @@ Default line (one JSON object on stdout, rank 0):
     every timed step; only the step is inside the CUDA events.
   * "decode" -- bf16 paged decode: B=64, H_q=32, H_kv=8, d_h=128, cache
     lengths ~U{1024..8192} including the step's own entry, pages placed by a
-    seeded random permutation.  One step = kv_append of one token per
-    sequence + attn_decode + kv_truncate back.  The 1.2 GB of K/V is larger
+    seeded random permutation.  One step = attn_decode_append (one token
+    per sequence appended and attended in one call) + kv_truncate back.  The 1.2 GB of K/V is larger
     than L2, so no flush is needed.
 Work counts: prefill flops = 4 d_h H_q sum_b causal_pairs; decode bytes =
 sum_b L_b * 2 * H_kv * d_h * 2 (each KV head read once).
@@ -387,8 +387,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                 gqa.kv_truncate(cache, ids[b], L[b] - 1)
 
     def step():
-        gqa.kv_append(cache, ids, new_k, new_v)
-        gqa.attn_decode(cache, ids, q, out=out)
+        gqa.attn_decode_append(cache, ids, q, new_k, new_v, out=out)
         advance()
 
     for _ in range(args.warmup):
@@ -424,8 +423,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
-        gqa.kv_append(cache, ids, kd, vd)
-        gqa.attn_decode(cache, ids, qd, out=od)
+        gqa.attn_decode_append(cache, ids, qd, kd, vd, out=od)
         oh.copy_(od, non_blocking=True)
         advance()
 
@@ -444,7 +442,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
            "kernels": {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl},
            "config": {"workload": "bf16 paged decode: B=%d, H_q=%d, H_kv=%d, d_h=%d, cache lengths ~U{1024..8192} "
                                   "(seed %d, sum %d tokens) incl. the appended token, pages placed by a seeded "
-                                  "random permutation; one step = kv_append + attn_decode + kv_truncate back"
+                                  "random permutation; one step = attn_decode_append (the token appended and attended in one call) + kv_truncate back"
                                   % (B, H_q, H_kv, d, workloads.seed_for(3), sum(L)),
                       "l2": "not flushed: %.2f GB of K/V per step exceeds the 129 MB L2" % (kv_bytes / 1e9),
                       "kv_bytes_per_step": kv_bytes}}
@@ -550,7 +548,7 @@ def tensor_roofline(flops, prof, peaks):
 
 def bench_wide(torch, gqa, dist, args, peaks):
     """Wide-GQA long context: B=1, H_q=48, H_kv=8, prefill T=8192, then 256
-    steps of kv_append + attn_decode (L = 8193..8448)."""
+    steps of attn_decode_append (L = 8193..8448)."""
     w = workloads.wide_gqa(workloads.seed_for(4))
     T, H_q, H_kv, d, steps = w["n"], w["H_q"], w["H_kv"], w["d"], w["steps"]
     per_seq = workloads.pages_for(T + steps) + 1
@@ -581,8 +579,7 @@ def bench_wide(torch, gqa, dist, args, peaks):
 
     def decode_all():
         for t in range(steps):
-            gqa.kv_append(c, [s], dk[t], dv[t])
-            gqa.attn_decode(c, [s], dq[t], out=dout)
+            gqa.attn_decode_append(c, [s], dq[t], dk[t], dv[t], out=dout)
         gqa.kv_truncate(c, s, T)
 
     decode_all()
@@ -617,8 +614,7 @@ def bench_wide(torch, gqa, dist, args, peaks):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        gqa.kv_append(c, [s], dk[t], dv[t])
-        gqa.attn_decode(c, [s], dq[t], out=dout)
+        gqa.attn_decode_append(c, [s], dq[t], dk[t], dv[t], out=dout)
         b.record()
         b.synchronize()
         step_ms.append(a.elapsed_time(b))
@@ -636,8 +632,8 @@ def bench_wide(torch, gqa, dist, args, peaks):
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
-           "note": "one step = kv_append + attn_decode of one sequence, called from Python: the step times "
-                   "include the host side of two calls, which is longer than the GPU work; 34 MB of K/V fits "
+           "note": "one step = attn_decode_append of one sequence, called from Python: the step times "
+                   "include the host side of the call, which is longer than the GPU work; 34 MB of K/V fits "
                    "in L2; kernel = device time of the decode launch alone (L2-resident), measured with the "
                    "steps queued ahead of the GPU"}
     flags = c.check()
