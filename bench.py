@@ -74,14 +74,14 @@ def source_sha(kernel):
     return h.hexdigest()
 
 
-def traffic_for(kernel, units_scale=1.0):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel; else None."""
+def traffic_for(workload, kernel, units_scale=1.0):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on the kernel's current source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path)).get(kernel)
-    if not rec or rec.get("sha256") != source_sha(kernel):
+    rec = json.load(open(path)).get(workload)
+    if not rec or rec.get("kernel") != kernel or rec.get("sha256") != source_sha(kernel):
         return None
     return rec["dram_bytes_per_launch"] * units_scale
 
@@ -281,7 +281,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     achieved = flops / (avg_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel), "kernel": kernel,
+                "frac": round(achieved / peak, 4), "traffic": traffic_for("prefill", kernel), "kernel": kernel,
                 "kernel_ms": round(avg_ms, 4), "algorithmic_flops_per_launch": flops,
                 "peak_source": "%s bf16 dense (burst)" % peak_src}
     gpu_launches = sum(nl for nl, _ in region_launches.values())
@@ -411,7 +411,8 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     avg_ms = kms / max(1, launches)
     achieved = kv_bytes / (avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(kernel), "kernel": kernel,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for("decode", kernel),
+                "kernel": kernel,
                 "kernel_ms": round(avg_ms, 4), "algorithmic_bytes_per_launch": kv_bytes,
                 "peak_source": "%s HBM copy bandwidth" % peak_src}
 
