@@ -30,6 +30,12 @@ Contents:
                      section describes RoPE as a rotation by the position ID
                      whose inner products depend only on position differences),
                      and rope_stored_bf16(), the key bytes a rotating cache holds.
+  e4m3_encode/_decode, quantize_e4m3_rows(), dequantize_e4m3_rows()
+                     the quantised cache ([P1] 2.5: the physical cache may be
+                     quantised as long as the logical order is kept): FP8
+                     E4M3 codes (the OCP 8-bit floating-point format, written
+                     out from its definition) with one fp32 scale per token
+                     row of each KV head.
 
 Every function here is pinned by tests in tests/test_oracle_pins.py against
 values the pages print, closed forms, special cases and brute force.
@@ -91,7 +97,10 @@ def default_threads() -> int:
 # ---------------------------------------------------------------------------
 
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """bf16 bit patterns (uint16) or float32 values -> float64, exactly."""
+    """bf16 bit patterns (uint16) or float32 values -> float64, exactly; a
+    quantised ("fp8") cache's packed rows -> their dequantised values."""
+    if dtype == "fp8":
+        return dequantize_e4m3_rows(np.asarray(x, dtype=np.uint8)).astype(np.float64)
     if dtype == "bf16":
         u = np.asarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
         return u.view(np.float32).astype(np.float64)
@@ -213,6 +222,82 @@ def rope_stored_bf16(k_bits: np.ndarray, positions, base: float) -> np.ndarray:
 # Logical paged cache ([P1] 2.5; [P3] PagedAttention, prefix sharing, edit).
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# Quantised cache: FP8 E4M3 codes with one fp32 scale per row ([P1] 2.5
+# allows a quantised physical layout; the scheme below is this library's).
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """FP8 E4M3 code bytes -> float64, from the format's definition: sign bit,
+    4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal
+    (m/8 * 2^-6); exponent 15 with mantissa 7 is NaN, so the largest finite
+    value is 1.75 * 2^8 = 448; there are no infinities."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float values -> E4M3 code bytes: round to nearest, ties to even
+    mantissa, magnitudes beyond 448 saturate to 448 (no NaN for finite
+    input).  Computed in fp64 from the definition above."""
+    x = np.asarray(x, dtype=np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # Subnormals (and the boundary into the first normal binade): m = a / 2^-9.
+    code = np.where(sub, np.rint(a / 2.0 ** -9).astype(np.int64), code)
+    # Normals: a = 2^e (1 + f), m = rint(8 f); a carry moves to the next binade.
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(sub, 1.0, a))).astype(np.int64)
+    frac = np.where(sub, 0.0, a / np.exp2(e.astype(np.float64)) - 1.0)
+    m = np.rint(frac * 8.0).astype(np.int64)
+    e = np.where(m == 8, e + 1, e)
+    m = np.where(m == 8, 0, m)
+    normal = ((e + 7) << 3) | m
+    code = np.where(sub, code, normal)
+    code = np.where(a >= E4M3_MAX, 0x7E, np.minimum(code, 0x7E))
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_rows(x) -> tuple:
+    """Rows x [..., d] (float32 values) -> (codes [..., d] uint8, scales [...]
+    float32).  Per row: s = amax / 448 in fp32; code = E4M3(x / s) with x / s
+    in fp32 (round to nearest); a row of zeros gets s = 0 and zero codes.
+    Dequantised value: fp32(decode(code) * s)."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    y = (x / safe[..., None]).astype(np.float32)
+    codes = e4m3_encode(y)
+    codes = np.where((s > 0)[..., None], codes, np.uint8(0)).astype(np.uint8)
+    return codes, s
+
+
+def pack_e4m3_rows(codes, scales) -> np.ndarray:
+    """A quantised row as the cache model stores it: d code bytes followed
+    by the 4 bytes of its fp32 scale."""
+    sb = np.ascontiguousarray(np.asarray(scales, dtype=np.float32)).view(np.uint8).reshape(*np.shape(scales), 4)
+    return np.concatenate([np.asarray(codes, dtype=np.uint8), sb], axis=-1)
+
+
+def dequantize_e4m3_rows(packed) -> np.ndarray:
+    """Packed rows [..., d + 4] -> float32 values fp32(decode(code) * s)."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    codes = packed[..., :-4]
+    s = np.ascontiguousarray(packed[..., -4:]).view(np.float32)[..., 0]
+    return (e4m3_decode(codes).astype(np.float32) * s[..., None]).astype(np.float32)
+
+
 class CacheError(Exception):
     def __init__(self, kind: str, msg: str = ""):
         super().__init__("%s: %s" % (kind, msg))
@@ -287,9 +372,23 @@ class CacheModel:
         return len(self.free)
 
     # -- sequences ---------------------------------------------------------
+    @property
+    def io_dtype(self):
+        """Type of q, k, v and out at the interface (bf16 for a quantised cache)."""
+        return "bf16" if self.dtype == "fp8" else self.dtype
+
     def _empty_rows(self):
+        if self.dtype == "fp8":                   # codes + 4 scale bytes per row
+            return np.zeros((0, self.H_kv, self.d + 4), dtype=np.uint8)
         dt = np.uint16 if self.dtype == "bf16" else np.float32
         return np.zeros((0, self.H_kv, self.d), dtype=dt)
+
+    def _stored(self, rows):
+        """Input rows (bf16 bits, or fp32 values) as this cache stores them."""
+        if self.dtype == "fp8":
+            codes, sc = quantize_e4m3_rows(to_f64(rows, "bf16").astype(np.float32))
+            return pack_e4m3_rows(codes, sc)
+        return np.asarray(rows, dtype=np.uint16 if self.dtype == "bf16" else np.float32)
 
     def create(self):
         for s in range(self.max_seqs):
@@ -385,8 +484,8 @@ class CacheModel:
                 S["pages"][-1] = new
             for _ in range(need):
                 S["pages"].append(self._take())
-            S["k"] = np.concatenate([S["k"], np.asarray(kr, dtype=S["k"].dtype)], axis=0)
-            S["v"] = np.concatenate([S["v"], np.asarray(vr, dtype=S["v"].dtype)], axis=0)
+            S["k"] = np.concatenate([S["k"], self._stored(kr)], axis=0)
+            S["v"] = np.concatenate([S["v"], self._stored(vr)], axis=0)
             S["len"] += c
         # Release only once every entry is written: the call's own readers (a
         # prefill over these rows) still see the keys it wrote, so no page of
@@ -420,7 +519,7 @@ def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None, r
     (i >= n_b) are discarded ([P1] 2.2) and returned as zeros.  With
     rope_base, q and every key are rotated by their positions first (the
     cache model keeps the unrotated keys)."""
-    dt = cache.dtype
+    dt = cache.io_dtype
     B, n, H_q, d = q.shape
     nb = [int(x) for x in valid_lengths]
     if any(x < 1 or x > n for x in nb):
@@ -452,7 +551,7 @@ def decode(cache: CacheModel, seq_ids, q, nthreads=None, rope_base=None):
     """[P3] single-token decode: query b at position L_b - 1 reads all L_b
     cached entries (its own appended entry included).  q [B, H_q, d].  With
     rope_base, q and the keys are rotated by their positions first."""
-    dt = cache.dtype
+    dt = cache.io_dtype
     B, H_q, d = q.shape
     out = np.zeros((B, H_q, d))
     for b, s in enumerate(seq_ids):

@@ -511,3 +511,79 @@ def test_windowed_cache_holds_a_bounded_number_of_pages():
         live = [p for p in cm.block_table(s) if p >= 0]
         assert len(live) <= -(-W // 16) + 1
     assert cm.length(s) == 1000
+
+
+# --- quantised cache: FP8 E4M3 codes with a per-row fp32 scale -------------
+
+def test_e4m3_decode_matches_torch_float8_for_every_code():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(mine)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_e4m3_known_codes_and_rounding():
+    dec = oracle.e4m3_decode
+    assert dec(0x7E) == 448.0 and dec(0xFE) == -448.0 and np.isnan(dec(0x7F))
+    assert dec(0x38) == 1.0 and dec(0x08) == 2.0 ** -6 and dec(0x01) == 2.0 ** -9 and dec(0x00) == 0.0
+    enc = lambda v: int(oracle.e4m3_encode(np.array([v]))[0])
+    assert enc(1.0625) == 0x38            # halfway between 1 and 1.125: to the even mantissa (1)
+    assert enc(1.1875) == 0x3A            # halfway between 1.125 and 1.25: to 1.25
+    assert enc(1.5 * 2.0 ** -9) == 0x02   # subnormal tie: m = 1.5 -> 2
+    assert enc(1000.0) == 0x7E and enc(-1000.0) == 0xFE and enc(460.0) == 0x7E
+    finite = [c for c in range(256) if not np.isnan(dec(c))]
+    assert all(enc(dec(c)) == c for c in finite)                    # every code round-trips
+    # Brute force: the code is the nearest representable value (ties even).
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(4000) * np.exp2(rng.integers(-12, 9, 4000))
+    x = x[np.abs(x) < 448]
+    vals = np.array([dec(c) for c in finite])
+    got = oracle.e4m3_decode(oracle.e4m3_encode(x))
+    best = np.min(np.abs(vals[None, :] - x[:, None]), axis=1)
+    assert np.all(np.abs(got - x) <= best + 1e-300)
+
+
+def test_quantized_rows_scale_error_and_zero_rows():
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((50, 4, 128)) * np.exp2(rng.integers(-6, 6, (50, 4, 1)))).astype(np.float32)
+    x[3, 1] = 0.0
+    codes, s = oracle.quantize_e4m3_rows(x)
+    amax = np.max(np.abs(x), axis=-1)
+    assert np.array_equal(s, (amax / np.float32(448.0)).astype(np.float32))
+    assert s[3, 1] == 0 and not codes[3, 1].any()
+    # The largest element of each non-zero row is coded as +-448.
+    arg = np.argmax(np.abs(x), axis=-1)
+    top = np.take_along_axis(codes, arg[..., None], axis=-1)[..., 0]
+    nz = amax > 0
+    assert np.all((top[nz] & 0x7F) == 0x7E)
+    deq = oracle.dequantize_e4m3_rows(oracle.pack_e4m3_rows(codes, s)).astype(np.float64)
+    # Round to nearest: half a unit in the last place (3 mantissa bits) for
+    # normals, half the subnormal step (s * 2^-10) below 2^-6 * s.
+    err = np.abs(deq - x)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, s[..., None] * 2.0 ** -10) * (1 + 1e-6) + 1e-30
+    assert np.all(err <= bound)
+
+
+def test_quantized_cache_model_serves_the_dequantized_rows():
+    rng = np.random.default_rng(7)
+    m = oracle.CacheModel(8, 1, 8, 2, 16, "fp8")
+    s = m.create()
+    k = workloads.normal_bf16(rng, (20, 2, 16))
+    v = workloads.normal_bf16(rng, (20, 2, 16))
+    m.write([s], [k], [v])
+    K, V = m.kv(s)
+    kc, ks = oracle.quantize_e4m3_rows(oracle.to_f64(k, "bf16").astype(np.float32))
+    want = (oracle.e4m3_decode(kc).astype(np.float32) * ks[..., None]).astype(np.float64)
+    assert np.array_equal(K, want)
+    assert m.raw_kv(s)[0].shape == (20, 2, 20)
+    m.truncate(s, 9)
+    assert np.array_equal(m.kv(s)[0], want[:9])
+    q = workloads.normal_bf16(rng, (1, 4, 16))
+    got = oracle.decode(m, [s], q)
+    ref = oracle.attention_dense(oracle.to_f64(q, "bf16"), m.kv(s)[0], m.kv(s)[1], [8])
+    assert np.allclose(got, ref, atol=1e-12)
