@@ -28,7 +28,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK, EINVAL, ERANGE, EMASK, ENOMEM, ELAYOUT, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 ERRNAMES = {EINVAL: "EINVAL", ERANGE: "ERANGE", EMASK: "EMASK", ENOMEM: "ENOMEM",
             ELAYOUT: "ELAYOUT", ECUDA: "ECUDA", EDEVICE: "EDEVICE"}
-DTYPE_BF16, DTYPE_F32 = 1, 2
+DTYPE_BF16, DTYPE_F32, DTYPE_FP8_E4M3 = 1, 2, 3
 PAGE_TOKENS = 16
 LAYOUT_VERSION = 2
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
@@ -122,7 +122,9 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-_TORCH_DTYPE = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
+# Element type of q, k, v and out (a quantised cache takes and returns bf16).
+_TORCH_DTYPE = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32, DTYPE_FP8_E4M3: torch.bfloat16}
+_DTYPE_CODE = {"bf16": DTYPE_BF16, "f32": DTYPE_F32, "fp8": DTYPE_FP8_E4M3}
 
 
 class Cache:
@@ -133,7 +135,8 @@ class Cache:
     def __init__(self, num_kv_heads, head_dim, num_pages, max_seqs, max_pages_per_seq,
                  dtype="bf16", page_order=None, device=None, metadata_only=False,
                  keys_post_position=1, layout_version=LAYOUT_VERSION, rope=False, rope_base=10000.0, window=0):
-        self.dtype_code = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
+        self.dtype_code = (DTYPE_BF16 if dtype is torch.bfloat16 else DTYPE_F32 if dtype is torch.float32
+                           else _DTYPE_CODE[dtype])
         self.torch_dtype = _TORCH_DTYPE[self.dtype_code]
         self._order_keep, order_ptr = _i32_array(page_order)
         self.desc = CacheDesc(self.dtype_code, num_kv_heads, head_dim, PAGE_TOKENS, num_pages,
@@ -164,11 +167,21 @@ class Cache:
         slot s of a page is group s // 8, position s % 8; element e of its row
         is chunk e // (128 / element size).  Elements past d_h in the last
         chunk are padding."""
+        if self.dtype_code == DTYPE_FP8_E4M3:             # code bytes; the scales follow
+            chunks = -(-self.head_dim // 128)
+            nb = self.num_pages * 2 * self.num_kv_heads * PAGE_TOKENS * chunks * 128
+            return self.pool[:nb].view(self.num_pages, 2, self.num_kv_heads, 2, chunks, PAGE_TOKENS // 2, 128)
         es = 2 if self.torch_dtype == torch.bfloat16 else 4
         per = 128 // es
         chunks = -(-self.head_dim * es // 128)
         return self.pool.view(self.torch_dtype).view(self.num_pages, 2, self.num_kv_heads, 2, chunks,
                                                      PAGE_TOKENS // 2, per)
+
+    def scales_view(self):
+        """FP8 E4M3 cache: the fp32 scales as [num_pages, 2 (K, V), H_kv, 16 slots]."""
+        chunks = -(-self.head_dim // 128)
+        nb = self.num_pages * 2 * self.num_kv_heads * PAGE_TOKENS * chunks * 128
+        return self.pool[nb:].view(torch.float32).view(self.num_pages, 2, self.num_kv_heads, PAGE_TOKENS)
 
     def close(self):
         if self._h:

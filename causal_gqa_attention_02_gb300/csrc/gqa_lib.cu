@@ -78,7 +78,8 @@ struct WriteReq {
 
 struct gqa_cache {
     gqa_cache_desc desc{};
-    int esize = 0;
+    int esize = 0;                       // bytes of a stored element (1 for FP8 E4M3)
+    int io_esize = 0;                    // bytes of a q/k/v/out element
     bool meta_only = false;
     void *pool = nullptr;
     std::vector<int32_t> order, rank, ref;
@@ -150,6 +151,12 @@ struct gqa_cache {
         pv.err = d_err;
         pv.rope = d_rope;
         pv.window = desc.window;
+        pv.dtype = desc.dtype;
+        pv.scales = nullptr;
+        if (pool && desc.dtype == GQA_DTYPE_FP8_E4M3)   // the scales follow the blocks
+            pv.scales = reinterpret_cast<float *>(
+                static_cast<char *>(pool) +
+                (size_t)desc.num_pages * 2 * desc.num_kv_heads * pool_block_bytes(desc.head_dim));
         return pv;
     }
 };
@@ -428,10 +435,12 @@ const char *gqa_version(void) { return "libgqa 0.1.0 (sm_103a)"; }
 size_t gqa_pool_bytes(const gqa_cache_desc *d)
 {
     if (!d || d->num_pages < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
-        (d->dtype != GQA_DTYPE_BF16 && d->dtype != GQA_DTYPE_F32))
+        (d->dtype != GQA_DTYPE_BF16 && d->dtype != GQA_DTYPE_F32 && d->dtype != GQA_DTYPE_FP8_E4M3))
         return 0;
-    const int es = d->dtype == GQA_DTYPE_BF16 ? 2 : 4;
-    return (size_t)d->num_pages * 2 * (size_t)d->num_kv_heads * pool_block_bytes(d->head_dim * es);
+    const int es = pool_esize(d->dtype);
+    const size_t blocks = (size_t)d->num_pages * 2 * (size_t)d->num_kv_heads;
+    return blocks * pool_block_bytes(d->head_dim * es) +
+           (d->dtype == GQA_DTYPE_FP8_E4M3 ? blocks * kPageTokens * sizeof(float) : 0);
 }
 
 int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes, gqa_cache **out)
@@ -440,8 +449,10 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
         return fail(GQA_EINVAL, "NULL argument");
     *out = nullptr;
     const gqa_cache_desc &d = *desc;
-    if (d.dtype != GQA_DTYPE_BF16 && d.dtype != GQA_DTYPE_F32)
+    if (d.dtype != GQA_DTYPE_BF16 && d.dtype != GQA_DTYPE_F32 && d.dtype != GQA_DTYPE_FP8_E4M3)
         return fail(GQA_EINVAL, "unknown dtype %d", d.dtype);
+    if (d.dtype == GQA_DTYPE_FP8_E4M3 && (d.head_dim % 32 != 0 || d.rope != 0))
+        return fail(GQA_EINVAL, "an FP8 E4M3 cache needs d_h a multiple of 32 and no rotary mechanism");
     if (d.num_kv_heads < 1 || d.head_dim < 1 || d.head_dim > 256)
         return fail(GQA_EINVAL, "H_kv must be >= 1 and d_h in 1..256");
     if (d.page_tokens != GQA_PAGE_TOKENS)
@@ -472,7 +483,8 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
     gqa_cache *c = new gqa_cache();
     c->desc = d;
     c->desc.page_order = nullptr;
-    c->esize = d.dtype == GQA_DTYPE_BF16 ? 2 : 4;
+    c->esize = pool_esize(d.dtype);
+    c->io_esize = d.dtype == GQA_DTYPE_F32 ? 4 : 2;
     c->meta_only = pool_dev == nullptr;
     c->pool = pool_dev;
     c->order.resize(d.num_pages);
@@ -918,7 +930,7 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     // On the tensor-core path the write kernel also zeroes the padding rows
     // of out (discarded rows are written as zeros); the prefill kernel then
     // writes the valid rows only.
-    const int out_row_bytes = H_q * c->desc.head_dim * c->esize;
+    const int out_row_bytes = H_q * c->desc.head_dim * c->io_esize;
     if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&](cudaEvent_t ev) {
              rec(ev, st);
              return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st, use_tc ? out : nullptr,

@@ -12,6 +12,7 @@
 // consecutive threads taking consecutive units of one row so that both the
 // read and the write are coalesced.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.cuh"
 
@@ -159,6 +160,62 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
     }
 }
 
+// Quantised cache ("第二章 Prefill：整层状态演化与 KV 建立" section 2.5: the
+// physical cache may be quantised; the logical order is kept): a warp per
+// (token, K|V, head) row of d_h bf16 values; lane l holds elements
+// l*P .. l*P + P - 1 (P = d_h / 32).  s = amax / 448 (fp32 division), each
+// code = E4M3(x / s) with the quotient in fp32 and the conversion rounding
+// to nearest-even and saturating; a row of zeros gets s = 0 and zero codes.
+// The codes go to the row's place in the block layout, s to the scale array.
+template <int P>
+__global__ void __launch_bounds__(256)
+cache_write_q8_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, const __nv_bfloat16 *__restrict__ k,
+                      const __nv_bfloat16 *__restrict__ v)
+{
+    const int b = blockIdx.y;
+    const SeqDesc sd = seqs[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    const int H_kv = pv.H_kv, d = pv.d;
+    const int chunks = pool_chunks(d);
+    const size_t blk_bytes = pool_block_bytes(d);
+    const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
+    const int rows = sd.count * 2 * H_kv;
+    for (int task = blockIdx.x * wpb + warp; task < rows; task += gridDim.x * wpb) {
+        const int t = task / (2 * H_kv), kv = (task / H_kv) & 1, h = task % H_kv;
+        const int pos = sd.past + t;
+        const int page = tab[pos / kPageTokens];
+        if ((unsigned)page >= (unsigned)pv.num_pages) {
+            if (lane == 0)
+                atomicOr(pv.err, kErrPageId);
+            continue;
+        }
+        const __nv_bfloat16 *src = (kv ? v : k) + (((size_t)b * n + t) * H_kv + h) * d + lane * P;
+        float x[P];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            x[i] = __bfloat162float(src[i]);
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = __fdiv_rn(amax, kE4m3Max);
+        unsigned char code[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i)
+            code[i] = sc > 0.0f ? (unsigned char)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], sc), __NV_SATFINITE, __NV_E4M3)
+                                : (unsigned char)0;
+        const int slot = pos % kPageTokens;
+        const size_t blk = ((size_t)page * 2 + kv) * H_kv + h;
+        unsigned char *dst = (unsigned char *)pv.pool + blk * blk_bytes;
+#pragma unroll
+        for (int i = 0; i < P; ++i)                    // (a lane's bytes may straddle a 128-byte chunk)
+            dst[pool_in_block(chunks, slot, lane * P + i)] = code[i];
+        if (lane == 0)
+            pv.scales[blk * kPageTokens + slot] = sc;
+    }
+}
+
 template <int U>
 __global__ void cow_copy_kernel(PoolView pv, int esize, const CowDesc *__restrict__ cows)
 {
@@ -185,6 +242,14 @@ __global__ void cow_copy_kernel(PoolView pv, int esize, const CowDesc *__restric
         *(T *)((char *)pv.pool + (size_t)cd.dst * page_bytes + off) =
             *(const T *)((const char *)pv.pool + (size_t)cd.src * page_bytes + off);
     }
+    if (pv.scales && blockIdx.x == 0) {                // a quantised cache: the rows' scales too
+        const int n_sc = 2 * pv.H_kv * cd.slots;
+        for (int i = threadIdx.x; i < n_sc; i += blockDim.x) {
+            const int blk = i / cd.slots, slot = i % cd.slots;
+            pv.scales[((size_t)cd.dst * 2 * pv.H_kv + blk) * kPageTokens + slot] =
+                pv.scales[((size_t)cd.src * 2 * pv.H_kv + blk) * kPageTokens + slot];
+        }
+    }
 }
 
 cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_seqs, int B, int n,
@@ -194,6 +259,26 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     const int rows = zero_out ? n : max_count;          // padding rows are zeroed too
     if (B <= 0 || rows <= 0)
         return cudaSuccess;
+    if (pv.dtype == kDtypeFp8) {                        // quantising write (no padding rows to zero)
+        if (zero_out || pv.d % 32 != 0 || pv.d > 256 || !pv.scales)
+            return cudaErrorInvalidValue;
+        int blocks = (max_count * 2 * pv.H_kv + 7) / 8;
+        if (blocks > 1024)
+            blocks = 1024;
+        dim3 grid((unsigned)blocks, (unsigned)B);
+        const __nv_bfloat16 *kb = (const __nv_bfloat16 *)k, *vb = (const __nv_bfloat16 *)v;
+        switch (pv.d / 32) {
+        case 1: cache_write_q8_kernel<1><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 2: cache_write_q8_kernel<2><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 3: cache_write_q8_kernel<3><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 4: cache_write_q8_kernel<4><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 5: cache_write_q8_kernel<5><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 6: cache_write_q8_kernel<6><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 7: cache_write_q8_kernel<7><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        default: cache_write_q8_kernel<8><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        }
+        return cudaGetLastError();
+    }
     const size_t row_bytes = (size_t)pv.d * esize;
     // With rotation a unit must lie within one half of the row and hold
     // whole elements.

@@ -16,6 +16,7 @@
 // (online softmax, the FlashAttention recurrence).  The value pass keeps the
 // output row spread over the lanes (lane owns elements lane, lane+32, ...).
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.cuh"
 
@@ -45,7 +46,9 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-template <typename T>
+// T: element type of q and out (and of the pool unless Q8); Q8: the pool
+// holds FP8 E4M3 codes with a scale per row, read as fp32(decode(code) * s).
+template <typename T, bool Q8>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
                  const T *__restrict__ q, T *__restrict__ out)
@@ -85,13 +88,20 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
     const int pos = sd.past + i;                  // visible keys 0..pos
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride;
     const char *pool = (const char *)pv.pool;
-    const int chunks = pool_chunks(d * (int)sizeof(T));
-    const size_t blk_bytes = pool_block_bytes(d * (int)sizeof(T));
+    const int es = Q8 ? 1 : (int)sizeof(T);
+    const int chunks = pool_chunks(d * es);
+    const size_t blk_bytes = pool_block_bytes(d * es);
     const size_t k_off = (size_t)g * blk_bytes;
     const size_t v_off = (size_t)(H_kv + g) * blk_bytes;
-    // Element e of the row of `slot` in the block at `blk`.
-    auto elem = [&](const char *blk, int slot, int e) -> const T * {
-        return (const T *)(blk + pool_in_block(chunks, slot, e * (int)sizeof(T)));
+    // Element e of the row of `slot` in block `bi` (page * 2 H_kv + kv * H_kv + g),
+    // whose bytes start at `blk`.
+    auto elem = [&](const char *blk, size_t bi, int slot, int e) -> float {
+        if (Q8) {
+            const __nv_fp8_storage_t c = *(const __nv_fp8_storage_t *)(blk + pool_in_block(chunks, slot, e));
+            const float x = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+            return __fmul_rn(x, pv.scales[bi * kPageTokens + slot]);
+        }
+        return ldf((const T *)(blk + pool_in_block(chunks, slot, e * es)));
     };
 
     float m = -INFINITY, l = 0.0f;
@@ -107,9 +117,10 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
             const int page = tab[t / kPageTokens];
             if ((unsigned)page < (unsigned)pv.num_pages) {
                 const char *kb_ = pool + (size_t)page * 2 * H_kv * blk_bytes + k_off;
+                const size_t kbi = (size_t)page * 2 * H_kv + g;
                 float dot = 0.0f;
                 for (int e = 0; e < d; ++e)
-                    dot = fmaf(qs[e], ldf(elem(kb_, t % kPageTokens, e)), dot);
+                    dot = fmaf(qs[e], elem(kb_, kbi, t % kPageTokens, e), dot);
                 s = dot / root_d;
             } else {
                 atomicOr(pv.err, kErrPageId);
@@ -130,11 +141,12 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
             if ((unsigned)page >= (unsigned)pv.num_pages)
                 continue;
             const char *vb_ = pool + (size_t)page * 2 * H_kv * blk_bytes + v_off;
+            const size_t vbi = (size_t)page * 2 * H_kv + H_kv + g;
 #pragma unroll
             for (int j = 0; j < kMaxD / 32; ++j) {
                 const int e = lane + 32 * j;
                 if (e < d)
-                    acc[j] = fmaf(pu, ldf(elem(vb_, tu % kPageTokens, e)), acc[j]);
+                    acc[j] = fmaf(pu, elem(vb_, vbi, tu % kPageTokens, e), acc[j]);
             }
         }
         m = m_new;
@@ -158,11 +170,14 @@ cudaError_t launch_attn_simt(const PoolView &pv, int dtype, const SeqDesc *d_seq
     if (B <= 0 || n <= 0)
         return cudaSuccess;
     dim3 grid((unsigned)((n + kWarps - 1) / kWarps), (unsigned)H_q, (unsigned)B);
-    if (dtype == 2)
-        attn_simt_kernel<float><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
-                                                            (float *)out);
+    if (dtype == kDtypeF32)
+        attn_simt_kernel<float, false><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
+                                                                   (float *)out);
+    else if (dtype == kDtypeFp8)
+        attn_simt_kernel<__nv_bfloat16, true><<<grid, kWarps * 32, 0, st>>>(
+            pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
     else
-        attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(
+        attn_simt_kernel<__nv_bfloat16, false><<<grid, kWarps * 32, 0, st>>>(
             pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
     return cudaGetLastError();
 }

@@ -22,6 +22,15 @@ constexpr int kPageTokens = 16;
 // exactly the 1 KB swizzle atoms of a tensor-core operand, so one TMA box
 // moves a page of one head.
 __host__ __device__ constexpr int pool_chunks(int row_bytes) { return (row_bytes + 127) >> 7; }
+
+// Cache element types (mirror include/gqa.h) and the bytes of a stored element.
+constexpr int32_t kDtypeBf16 = 1, kDtypeF32 = 2, kDtypeFp8 = 3;
+__host__ __device__ constexpr int pool_esize(int32_t dtype)
+{
+    return dtype == kDtypeFp8 ? 1 : dtype == kDtypeBf16 ? 2 : 4;
+}
+// Largest finite FP8 E4M3 value: a quantised row's scale is amax / 448.
+constexpr float kE4m3Max = 448.0f;
 __host__ __device__ constexpr size_t pool_block_bytes(int row_bytes) { return (size_t)pool_chunks(row_bytes) << 11; }
 __host__ __device__ constexpr size_t pool_in_block(int chunks, int slot, int b)
 {
@@ -39,6 +48,8 @@ struct PoolView {
     int32_t *err;            // device error word (GQA_DEVERR_* bits)
     const float2 *rope;      // rotary table (cos, sin) [position][d / 2], or null: no rotation
     int32_t window;          // sliding window W (0 = none): position p sees keys max(0, p-W+1)..p
+    int32_t dtype;           // kDtype*: the stored element type
+    float *scales;           // FP8 E4M3: scale of (block, slot) at block * 16 + slot; else null
 };
 
 // First key position visible to a query at absolute position p.

@@ -30,7 +30,8 @@
  *    not synchronise except to report a CUDA error.  All calls on one cache
  *    must be issued on one stream, or ordered by the caller.
  *  - Tensors are dense, row-major, in the cache's element type (bf16 or
- *    fp32).  Shapes below list the outermost dimension first.
+ *    fp32; bf16 for a GQA_DTYPE_FP8_E4M3 cache, whose pages hold quantised
+ *    K/V).  Shapes below list the outermost dimension first.
  *  - Token-major layouts: q is [B, n, H_q, d_h] and k, v are
  *    [B, n, H_kv, d_h] -- a permuted view of [P1] 2.3's [B, H, n, d_h].
  *
@@ -48,6 +49,17 @@
  * a page of one head).  Token t of a sequence lives in logical page t/16 at
  * slot t%16; a per-sequence block table maps logical pages to physical pages
  * ([P3] PagedAttention).
+ *
+ * Quantised cache (dtype GQA_DTYPE_FP8_E4M3; [P1] 2.5: the physical cache
+ * may be quantised as long as the logical order is kept).  A row is d_h
+ * bytes of FP8 E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; largest finite value 448) in the block layout above, plus one fp32
+ * scale per row.  The scales follow the blocks in the same buffer: after
+ * the num_pages * 2 * H_kv blocks, scale of (block, slot s) at float index
+ * block*16 + s.  A row x (the bf16 values given) is stored as s = amax|x| /
+ * 448 (fp32) and codes E4M3(x_i / s) (the quotient in fp32, rounded to
+ * nearest-even, saturating at +-448); a row of zeros has s = 0 and zero
+ * codes.  Attention reads the value fp32(decode(code) * s).
  *
  * Allocation rules (deterministic; the tests restate them independently):
  *  - a free page is taken in the order `page_order` gives (identity when
@@ -87,8 +99,9 @@ extern "C" {
 #define GQA_DEVERR_TIMEOUT   2  /* a bounded wait inside a kernel gave up */
 #define GQA_DEVERR_SHAPE     4  /* a kernel saw a shape it does not support (work skipped) */
 
-#define GQA_DTYPE_BF16 1
-#define GQA_DTYPE_F32  2
+#define GQA_DTYPE_BF16     1
+#define GQA_DTYPE_F32      2
+#define GQA_DTYPE_FP8_E4M3 3  /* quantised pages; q, k, v and out in bf16 (layout above) */
 
 #define GQA_PAGE_TOKENS    16
 #define GQA_LAYOUT_VERSION 2
@@ -96,9 +109,10 @@ extern "C" {
 /* Cache description ([P1] 2.5: cache_config fixes the KV layout and the
  * position convention). */
 typedef struct {
-    int32_t dtype;               /* GQA_DTYPE_BF16 or GQA_DTYPE_F32                        */
+    int32_t dtype;               /* GQA_DTYPE_BF16, GQA_DTYPE_F32 or GQA_DTYPE_FP8_E4M3     */
     int32_t num_kv_heads;        /* H_kv >= 1                                              */
-    int32_t head_dim;            /* d_h, 1..256 (bf16 d_h = 128 takes the tensor-core path) */
+    int32_t head_dim;            /* d_h, 1..256 (bf16 d_h = 128 takes the tensor-core path;
+                                    FP8_E4M3 needs a multiple of 32)                        */
     int32_t page_tokens;         /* must be GQA_PAGE_TOKENS                                 */
     int32_t num_pages;           /* pages in the pool, >= 1                                 */
     int32_t max_seqs;            /* sequence ids are 0..max_seqs-1                          */
@@ -144,8 +158,9 @@ typedef struct {
 typedef struct gqa_cache gqa_cache;
 
 /* Bytes the page pool of `desc` occupies: num_pages * 2 * H_kv * 16 * C *
- * 128 with C = ceil(d_h * element size / 128) (layout version 2 above).
- * Returns 0 for an invalid description. */
+ * 128 with C = ceil(d_h * element size / 128) (layout version 2 above;
+ * element size 1 for FP8_E4M3, whose pool adds num_pages * 2 * H_kv * 16
+ * fp32 scales).  Returns 0 for an invalid description. */
 size_t gqa_pool_bytes(const gqa_cache_desc *desc);
 
 /* Create a cache over a caller-owned device pool (`pool_dev`, at least
@@ -163,7 +178,8 @@ size_t gqa_pool_bytes(const gqa_cache_desc *desc);
  * max_pages_per_seq * 16 positions x d_h/2 frequencies (fp32, computed in
  * fp64 on the host).
  * Errors: GQA_EINVAL (bad description, pool too small, misaligned; rope not
- *         0/1, or rope = 1 with an odd d_h or rope_base <= 1),
+ *         0/1, or rope = 1 with an odd d_h or rope_base <= 1; FP8_E4M3 with
+ *         d_h not a multiple of 32 or with rope = 1),
  *         GQA_ELAYOUT (keys_post_position != 1 or unknown layout_version),
  *         GQA_ECUDA. */
 int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes,

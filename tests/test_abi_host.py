@@ -334,3 +334,21 @@ def test_fused_decode_step_bookkeeping_matches_append():
     with pytest.raises(gqa.GqaError) as e:                      # distinct sequences, as for a write
         gqa.attn_decode_append_meta(lib, [a, a], 4)
     assert e.value.name == "EINVAL"
+
+
+def test_fp8_cache_description_and_pool_size():
+    c = gqa.Cache(2, 128, 8, 2, 4, dtype="fp8", metadata_only=True)
+    m = c.layout()
+    assert m.dtype == gqa.DTYPE_FP8_E4M3
+    assert not gqa.layout_compatible(m, gqa.Cache(2, 128, 8, 2, 4, dtype="bf16", metadata_only=True).layout())
+    # Blocks of 16 one-byte rows of d_h codes, then one fp32 scale per row.
+    assert gqa._lib.gqa_pool_bytes(ctypes.byref(c.desc)) == 8 * 2 * 2 * 16 * 128 + 8 * 2 * 2 * 16 * 4
+    d96 = gqa.Cache(1, 96, 4, 1, 2, dtype="fp8", metadata_only=True)
+    assert gqa._lib.gqa_pool_bytes(ctypes.byref(d96.desc)) == 4 * 2 * 16 * 128 + 4 * 2 * 16 * 4
+    for kw in ({"head_dim": 100}, {"head_dim": 130}, {"rope": True}):
+        args = dict(num_kv_heads=2, head_dim=128, num_pages=8, max_seqs=2, max_pages_per_seq=4, dtype="fp8",
+                    metadata_only=True)
+        args.update(kw)
+        with pytest.raises(gqa.GqaError) as e:
+            gqa.Cache(**args)
+        assert e.value.name == "EINVAL", kw

@@ -1,0 +1,112 @@
+"""GPU parity of the quantised (FP8 E4M3) cache against the fp64 oracle:
+the stored codes and per-row scales bit for bit (the cache write's rounding
+decides integers, so both sides decide them in fp32 as the header states),
+block tables and lengths exact, and attention outputs -- over the
+dequantised values -- within the bf16 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _helpers import assert_close, dev, host_f64
+
+gqa = pytest.importorskip("causal_gqa_attention_02_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def _raw_rows(cache):
+    """Codes [pages, 2, H_kv, 16, d] and scales [pages, 2, H_kv, 16] read back
+    from the pool bytes with the documented layout (row bytes = d_h)."""
+    d, H = cache.head_dim, cache.num_kv_heads
+    C = -(-d // 128)
+    raw = cache.pool.detach().cpu().numpy().view(np.uint8)
+    nb = cache.num_pages * 2 * H * 16 * C * 128
+    blocks = raw[:nb].reshape(cache.num_pages, 2, H, 16 * C * 128)
+    s = np.arange(16)[:, None]
+    b = np.arange(d)[None, :]
+    off = ((s // 8) * C + b // 128) * 1024 + (s % 8) * 128 + b % 128
+    codes = blocks[..., off]                                                # [P, 2, H, 16, d]
+    scales = raw[nb: nb + cache.num_pages * 2 * H * 16 * 4].view(np.float32).reshape(cache.num_pages, 2, H, 16)
+    return codes, scales
+
+
+def _check_stored(c, m, pairs):
+    codes, scales = _raw_rows(c)
+    d = c.head_dim
+    for s, ms in pairs:
+        L = m.length(ms)
+        table = c.block_table(s)
+        assert c.seq_length(s) == L and table == m.block_table(ms)
+        t = np.arange(L)
+        pg = np.asarray(table)[t // 16]
+        rk, rv = m.raw_kv(ms)
+        for kv, raw in ((0, rk), (1, rv)):
+            got_c = codes[pg, kv, :, t % 16, :]                              # [L, H, d]
+            got_s = scales[pg, kv, :, t % 16]
+            assert np.array_equal(got_c, raw[..., :d]), "stored codes differ"
+            want_s = np.ascontiguousarray(raw[..., d:]).view(np.float32)[..., 0]
+            assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32)), "stored scales differ"
+
+
+def _caches(B, H_kv, d, pages, per_seq, max_seqs=None):
+    c = gqa.Cache(H_kv, d, pages, max_seqs or B, per_seq, dtype="fp8")
+    m = oracle.CacheModel(pages, max_seqs or B, per_seq, H_kv, d, "fp8")
+    return c, m, [c.seq_create() for _ in range(B)], [m.create() for _ in range(B)]
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,n,nb", [
+    (8, 2, 128, 70, [70, 33, 1]),
+    (6, 3, 64, 40, [40, 17, 29]),
+    (4, 2, 160, 37, [37, 20, 5]),        # a lane's bytes straddle the first 128-byte chunk
+    (8, 8, 256, 24, [24, 9, 16]),
+])
+def test_fp8_prefill_codes_scales_and_outputs(H_q, H_kv, d, n, nb):
+    rng = np.random.default_rng(110 + d)
+    B = len(nb)
+    q = workloads.normal_bf16(rng, (B, n, H_q, d))
+    k = workloads.normal_bf16(rng, (B, n, H_kv, d))
+    v = workloads.normal_bf16(rng, (B, n, H_kv, d))
+    k[0, 3, 0] = 0                                           # a row of zeros: scale 0, zero codes
+    c, m, ids, mids = _caches(B, H_kv, d, 32, 8)
+    out = host_f64(gqa.attn_prefill(c, ids, dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"), nb), "bf16")
+    ref = oracle.prefill(m, mids, q, k, v, nb)
+    mask = np.arange(n)[None, :] < np.asarray(nb)[:, None]
+    assert_close(out[mask], ref[mask], "bf16", "fp8 prefill")
+    assert np.all(out[~mask] == 0)
+    _check_stored(c, m, list(zip(ids, mids)))
+    assert c.check() == 0
+
+
+def test_fp8_decode_steps_fork_and_fused_call():
+    rng = np.random.default_rng(120)
+    H_q, H_kv, d = 8, 2, 128
+    c, m, ids, mids = _caches(2, H_kv, d, 40, 16, max_seqs=3)
+    k = workloads.normal_bf16(rng, (2, 45, H_kv, d))
+    v = workloads.normal_bf16(rng, (2, 45, H_kv, d))
+    gqa.kv_append(c, ids, dev(k, "bf16"), dev(v, "bf16"), counts=[45, 30])
+    oracle.append(m, mids, k, v, counts=[45, 30])
+    f = c.seq_fork(ids[0], 37)                                # shares a partly filled page
+    fm = m.fork(mids[0], 37)
+    allids, allm = ids + [f], mids + [fm]
+    for t in range(20):
+        qt = workloads.normal_bf16(rng, (3, H_q, d))
+        kt = workloads.normal_bf16(rng, (3, H_kv, d))
+        vt = workloads.normal_bf16(rng, (3, H_kv, d))
+        if t % 2:
+            o = gqa.attn_decode_append(c, allids, dev(qt, "bf16"), dev(kt, "bf16"), dev(vt, "bf16"))
+        else:
+            gqa.kv_append(c, allids, dev(kt, "bf16"), dev(vt, "bf16"))
+            o = gqa.attn_decode(c, allids, dev(qt, "bf16"))
+        oracle.append(m, allm, kt, vt)
+        assert_close(host_f64(o, "bf16"), oracle.decode(m, allm, qt), "bf16", "fp8 decode %d" % t)
+    assert len(m.copies) >= 1
+    _check_stored(c, m, list(zip(allids, allm)))
+    assert c.check() == 0
+
+
+def test_fp8_cache_rejects_the_tensor_core_choices():
+    c = gqa.Cache(2, 128, 8, 2, 4, dtype="fp8")
+    with pytest.raises(gqa.GqaError):
+        c.set_decode_kernel("tensor_core")
