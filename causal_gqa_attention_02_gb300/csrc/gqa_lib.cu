@@ -1075,7 +1075,8 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
                                      (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev);
         });
     }
-    if (c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && decode_split_supported(G)) {
+    if ((c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) && c->desc.head_dim == 128 &&
+        decode_split_supported(G)) {
         // Chunk: a multiple of the page size, large enough to amortise the
         // partials, small enough for several CTAs per SM.
         int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
@@ -1290,7 +1291,8 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     const int use_tc = decode_uses_tc(c, G);
     if (use_tc < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
-    if (!use_tc && (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || !decode_split_supported(G)))
+    if (!use_tc && ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) ||
+                    c->desc.head_dim != 128 || !decode_split_supported(G)))
         return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 (and H_q/H_kv <= 8 on the "
                                 "CUDA-core kernel)");
     if (c->meta_only)

@@ -29,6 +29,7 @@
 // Scores are carried in log2 units (q pre-scaled by log2(e)/sqrt(128)) so
 // every exponential is one ex2.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.cuh"
 
@@ -78,10 +79,41 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
 // A bf16 pair (low half = lower index) as two floats.
 __device__ __forceinline__ float2 bf2(uint32_t x) { return make_float2(bf_lo(x), bf_hi(x)); }
 
+// Two FP8 E4M3 codes (low byte = lower index) as two floats (exact).
+__device__ __forceinline__ float2 e4m3x2(uint32_t x)
+{
+    return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(x & 0xffffu), __NV_E4M3)));
+}
+
+// Eight consecutive row elements of this lane as float pairs: a 16-byte
+// load of bf16, or an 8-byte load of E4M3 codes (the row's scale is applied
+// by the caller).
+template <bool Q8>
+struct RowLoad;
+template <>
+struct RowLoad<false> {
+    using T = uint4;
+    static __device__ __forceinline__ void pairs(const T &x, float2 (&f)[4])
+    {
+        f[0] = bf2(x.x), f[1] = bf2(x.y), f[2] = bf2(x.z), f[3] = bf2(x.w);
+    }
+};
+template <>
+struct RowLoad<true> {
+    using T = uint2;
+    static __device__ __forceinline__ void pairs(const T &x, float2 (&f)[4])
+    {
+        f[0] = e4m3x2(x.x), f[1] = e4m3x2(x.x >> 16), f[2] = e4m3x2(x.y), f[3] = e4m3x2(x.y >> 16);
+    }
+};
+
 // Lane layout for both passes over a 16-token page: lane l covers tokens
 // 2i + l/16 (i = 0..7) and columns 8(l%16)..8(l%16)+7, so one 16-byte load
-// per lane reads two whole 256-byte token rows: 512 contiguous bytes.
-template <int G, bool ROPE>
+// per lane reads two whole 256-byte token rows: 512 contiguous bytes.  Q8:
+// the pool holds FP8 E4M3 codes (a page block is [16 slots][128 bytes]) and
+// a scale per row; one 8-byte load per lane reads two 128-byte rows, and a
+// row's scale multiplies its score (K) or its probability (V).
+template <int G, bool ROPE, bool Q8>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeItem *__restrict__ items,
                     const int32_t *__restrict__ item_start, int chunk, int H_q,
@@ -103,13 +135,17 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
     const int nt = min(chunk, L - t0);
     const int npages = (nt + kPageTokens - 1) / kPageTokens;
     const int32_t *tab = pv.tables + (size_t)sd.row * pv.stride + t0 / kPageTokens;
-    const uint4 *pool = (const uint4 *)pv.pool;
-    // A page block (one head) is 256 uint4; lane l reads token 2i + half,
-    // columns col..col+7, i.e. 128-byte chunk (l >> 3) & 1 of that row, at
-    // uint4 offset (i / 4) * 128 + chunk * 64 + ((2i + half) % 8) * 8 + l % 8.
-    constexpr size_t kBlk = (size_t)kPageTokens * D * 2 / 16;
+    using RL = RowLoad<Q8>;
+    using LT = typename RL::T;
+    const LT *pool = (const LT *)pv.pool;
+    // bf16: a page block (one head) is 256 uint4; lane l reads token 2i +
+    // half, columns col..col+7, i.e. 128-byte chunk (l >> 3) & 1 of that row,
+    // at uint4 offset (i / 4) * 128 + chunk * 64 + ((2i + half) % 8) * 8 + l % 8.
+    // E4M3: a page block is 256 uint2, token t's row at uint2 offset 16 t.
+    constexpr size_t kBlk = (size_t)kPageTokens * D * (Q8 ? 1 : 2) / sizeof(LT);
     const int half = lane >> 4, col = 8 * (lane & 15);
-    const int lane_off = ((lane >> 3) & 1) * 64 + half * 8 + (lane & 7);
+    const int lane_off = Q8 ? half * 16 + (lane & 15) : ((lane >> 3) & 1) * 64 + half * 8 + (lane & 7);
+    auto row_at = [](int i) { return Q8 ? i * 32 : (i >> 2) * 128 + (i & 3) * 16; };   // token 2i + half
 
     // This lane's eight q columns of every head of the group, pre-scaled by
     // log2(e)/sqrt(d_h) so scores come out in exp2 units.
@@ -155,20 +191,21 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         const bool ok = (unsigned)page < (unsigned)pv.num_pages;
         float v[8][G];
         if (ok) {
-            const uint4 *kr = pool + ((size_t)page * 2 * H_kv + kvh) * kBlk + lane_off;
-            uint4 kk[8];
+            const LT *kr = pool + ((size_t)page * 2 * H_kv + kvh) * kBlk + lane_off;
+            LT kk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                kk[i] = kr[(i >> 2) * 128 + (i & 3) * 16];   // token 2i + half, columns col..col+7
+                kk[i] = kr[row_at(i)];                       // token 2i + half, columns col..col+7
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t w[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+                float2 w[4];
+                RL::pairs(kk[i], w);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     float2 a = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        a = fma2(bf2(w[u]), qr[h][u], a);
+                        a = fma2(w[u], qr[h][u], a);
                     v[i][h] = a.x + a.y;
                 }
             }
@@ -212,9 +249,11 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         // Lane pair (l, l^1) now holds token 2(4 b3 + 2 b2 + b1) + half.
         const int tl = pg * kPageTokens + 2 * (4 * b3 + 2 * b2 + b1) + half;
         if ((lane & 1) == 0) {
+            const float ks = (Q8 && ok) ? pv.scales[((size_t)page * 2 * H_kv + kvh) * kPageTokens + tl % kPageTokens]
+                                        : 1.0f;
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                sc[tl][h] = (ok && tl < nt && t0 + tl >= ws) ? v[0][h] : -INFINITY;
+                sc[tl][h] = (ok && tl < nt && t0 + tl >= ws) ? (Q8 ? v[0][h] * ks : v[0][h]) : -INFINITY;
         }
     }
     __syncthreads();
@@ -252,22 +291,25 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
         const int page = tab[pg];
         if ((unsigned)page >= (unsigned)pv.num_pages)
             continue;
-        const uint4 *vr = pool + ((size_t)page * 2 * H_kv + H_kv + kvh) * kBlk + lane_off;
-        uint4 vv[8];
+        const LT *vr = pool + ((size_t)page * 2 * H_kv + H_kv + kvh) * kBlk + lane_off;
+        const float *vsc = Q8 ? pv.scales + ((size_t)page * 2 * H_kv + H_kv + kvh) * kPageTokens : nullptr;
+        LT vv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            vv[i] = vr[(i >> 2) * 128 + (i & 3) * 16];
+            vv[i] = vr[row_at(i)];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int tl = pg * kPageTokens + 2 * i + half;   // probabilities are 0 past nt
-            const uint32_t w[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
+            float2 w[4];
+            RL::pairs(vv[i], w);
+            const float vs = Q8 ? vsc[2 * i + half] : 1.0f;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float pr = sc[tl][h];
+                const float pr = Q8 ? sc[tl][h] * vs : sc[tl][h];
                 const float2 pp = make_float2(pr, pr);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    o[h][u] = fma2(pp, bf2(w[u]), o[h][u]);
+                    o[h][u] = fma2(pp, w[u], o[h][u]);
             }
         }
     }
@@ -400,16 +442,19 @@ template <int G>
 cudaError_t launch_g(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st)
 {
     dim3 grid((unsigned)a.n_items, (unsigned)pv.H_kv);
-    // The rotating kernel is a separate instantiation, so that a cache
-    // without the position mechanism runs the plain one.
-    if (pv.rope)
-        decode_split_kernel<G, true><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q,
-                                                                  (const __nv_bfloat16 *)a.q, a.ws_o, a.ws_ml,
-                                                                  a.counters, (__nv_bfloat16 *)a.out);
+    // The rotating and the quantised kernels are separate instantiations, so
+    // that a plain bf16 cache runs the plain one.
+    const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q;
+    __nv_bfloat16 *out = (__nv_bfloat16 *)a.out;
+    if (pv.dtype == kDtypeFp8)
+        decode_split_kernel<G, false, true><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
+                                                                         a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
+    else if (pv.rope)
+        decode_split_kernel<G, true, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
+                                                                         a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
     else
-        decode_split_kernel<G, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
-                                                                   a.H_q, (const __nv_bfloat16 *)a.q, a.ws_o,
-                                                                   a.ws_ml, a.counters, (__nv_bfloat16 *)a.out);
+        decode_split_kernel<G, false, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
+                                                                          a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
     return cudaGetLastError();
 }
 

@@ -106,6 +106,31 @@ def test_fp8_decode_steps_fork_and_fused_call():
     assert c.check() == 0
 
 
+@pytest.mark.parametrize("H_q,H_kv,lengths", [(32, 8, [1, 17, 300, 2049, 5000]), (8, 8, [4097, 33]), (64, 8, [700])])
+def test_fp8_split_decode_kernel(H_q, H_kv, lengths):
+    # bf16, d_h = 128, H_q/H_kv <= 8: the split-K CUDA-core decode kernel reads
+    # the codes and scales directly (half the bytes of a bf16 cache).
+    rng = np.random.default_rng(130 + H_q)
+    B, d = len(lengths), 128
+    pages = sum(workloads.pages_for(L) for L in lengths) + 4
+    c, m, ids, mids = _caches(B, H_kv, d, pages, workloads.pages_for(max(lengths)) + 1)
+    for b, L in enumerate(lengths):
+        k = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        v = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        gqa.kv_append(c, [ids[b]], dev(k, "bf16"), dev(v, "bf16"))
+        oracle.append(m, [mids[b]], k, v)
+    q = workloads.normal_bf16(rng, (B, H_q, d))
+    c.profile_read()
+    o = gqa.attn_decode(c, ids, dev(q, "bf16"))
+    launched = c.profile_read()
+    assert launched["decode_split" if H_q // H_kv <= 8 else "attn_simt"][0] == 1, launched
+    assert_close(host_f64(o, "bf16"), oracle.decode(m, mids, q), "bf16", "fp8 split decode")
+    if H_q // H_kv <= 8:
+        s = gqa.attn_decode_static(c, ids, dev(q, "bf16"))
+        assert torch.equal(o.view(torch.int16), s.view(torch.int16))
+    assert c.check() == 0
+
+
 def test_fp8_cache_rejects_the_tensor_core_choices():
     c = gqa.Cache(2, 128, 8, 2, 4, dtype="fp8")
     with pytest.raises(gqa.GqaError):
