@@ -355,13 +355,15 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     B, H_q, H_kv, d = w["B"], w["H_q"], w["H_kv"], w["d"]
     L = [int(x) for x in w["lengths"]]
     W = args.window
-    kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, 2, W)
+    q8 = args.kv == "fp8"                    # quantised cache: 1-byte codes + a 4-byte scale per row
+    kv_es, kv_extra = (1, 4) if q8 else (2, 0)
+    kv_bytes = gqa.work.decode_kv_bytes(L, H_kv, d, kv_es, W, kv_extra)
     # Under a sliding window the sequences grow by one token a step (a
     # rewind may reach back past the window), so the pool and the tables
     # get room for every step of the run; K/V bytes are counted per step.
     grow = 8 * (args.steps + args.warmup + 4) if W else 0
     spare = B * workloads.pages_for(grow + 16) if W else 0
-    cache = gqa.Cache(H_kv, d, w["num_pages"] + spare, B, workloads.pages_for(max(L) + grow) + 1, dtype="bf16",
+    cache = gqa.Cache(H_kv, d, w["num_pages"] + spare, B, workloads.pages_for(max(L) + grow) + 1, dtype=args.kv,
                       rope=args.rope, page_order=(list(w["page_order"]) + list(range(w["num_pages"],
                       w["num_pages"] + spare))) if W else w["page_order"], window=W)
     ids = [cache.seq_create() for _ in range(B)]
@@ -380,7 +382,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         if W:
             for b in range(B):
                 cur[b] += 1
-            moved[0] += gqa.work.decode_kv_bytes(cur, H_kv, d, 2, W)
+            moved[0] += gqa.work.decode_kv_bytes(cur, H_kv, d, kv_es, W, kv_extra)
         else:
             moved[0] += kv_bytes
             for b in range(B):
@@ -456,7 +458,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
         import oracle
         nth = oracle.default_threads()
         cm = oracle.CacheModel(sum(workloads.pages_for(x) for x in L[:8]), 8, workloads.pages_for(max(L)) + 1,
-                               H_kv, d, "bf16", window=W)
+                               H_kv, d, args.kv, window=W)
         sm = [cm.create() for _ in range(8)]
         for j in range(8):
             cm.write([sm[j]], [w["hist_k"][j]], [w["hist_v"][j]])
@@ -467,12 +469,15 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
             oracle.decode(cm, sm, w["q"][:8], nthreads=nth)
             dt += time.perf_counter() - t0c
             reps += 1
-        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, 2, W) * reps
+        by = gqa.work.decode_kv_bytes(L[:8], H_kv, d, kv_es, W, kv_extra) * reps
         res["cpu_baseline"] = {"value": round(by / dt / 1e9, 3), "unit": "GB/s", "cores": nth, "kind": "oracle",
                                "sample": "fp64 oracle decode of sequences 0..7 (%d cached tokens, %.1f MB of "
                                          "bf16 K/V), %d repetitions: %.1f GB in %.1f s"
                                          % (sum(L[:8]), by / reps / 1e6, reps, by / 1e9, dt)}
-    if not W:
+    if q8:
+        res["config"]["kv_cache"] = ("FP8 E4M3 codes + one fp32 scale per (token, head) row, written by the "
+                                     "library from the bf16 K/V; bytes counted as read (codes and scales)")
+    if not W and not q8:
         res["multi_token"] = bench_multi_token(torch, gqa, dist, args, peaks, peak_src, cache, ids, L, w)
     res["device_error_flags"] = cache.check()
     res["t0"], res["t1"] = t0, t1
@@ -764,6 +769,8 @@ def main():
                     help="caches with the rotary position mechanism applied by the library")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto",
                     help="decode kernel of attn_decode (auto: tensor-core for bf16, d_h = 128)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="decode cache type (fp8: FP8 E4M3 codes with per-row scales; decode only)")
     ap.add_argument("--window", type=int, default=0,
                     help="caches with a sliding window of this many tokens (0 = none)")
     ap.add_argument("--extra", action="store_true",
@@ -772,6 +779,9 @@ def main():
                     help="seconds of fp64 oracle work per CPU baseline (rank 0, N=1)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.kv == "fp8":
+        args.no_prefill = True               # the quantised cache is measured on decode
+        args.extra = False
     dist = Dist()
     if args.impl == "reference":
         return run_reference(args, dist)

@@ -844,13 +844,17 @@ int tc_workspace(gqa_cache *c, const TcPlan &pl, TcSplitWs &ws)
 // tensor-core kernel was asked for but cannot serve this cache or group.
 int decode_uses_tc(const gqa_cache *c, int G)
 {
-    const bool ok = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
-                    prefill_tc_supported(G, c->desc.num_kv_heads);
+    const bool ok = (c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) &&
+                    c->desc.head_dim == 128 && c->cc >= 100 && prefill_tc_supported(G, c->desc.num_kv_heads);
     if (c->decode_kernel == GQA_DECODE_CUDA_CORE)
         return 0;
     if (c->decode_kernel == GQA_DECODE_TENSOR_CORE)
         return ok ? 1 : -1;
-    return ok ? 1 : 0;
+    // Automatic: the tensor-core kernel for bf16.  A quantised cache decodes
+    // faster on the CUDA-core kernel, which reads the codes directly; on the
+    // tensor-core kernel each tile's codes are first converted to bf16
+    // operands by the producer warps, whose conversion rate bounds decode.
+    return ok && c->desc.dtype == GQA_DTYPE_BF16 ? 1 : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -904,7 +908,8 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     if ((rc = upload_tables(c, st)) != GQA_OK)
         return rc;
     const int G = H_q / c->desc.num_kv_heads;
-    const bool use_tc = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
+    const bool use_tc = (c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) &&
+                        c->desc.head_dim == 128 && c->cc >= 100 &&
                         prefill_tc_supported(G, c->desc.num_kv_heads);
     TcPlan plan;
     if (use_tc)
@@ -1142,8 +1147,9 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     const int use_tc = c->meta_only ? 0 : decode_uses_tc(c, G);
     if (use_tc < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
-    if (!use_tc) {
-        // CUDA-core kernels: the write, then the decode.
+    if (!use_tc || c->desc.dtype == GQA_DTYPE_FP8_E4M3) {
+        // CUDA-core kernels (and the quantised cache, whose write rounds in
+        // its own kernel): the write, then the decode.
         int rc = kv_append(c, B, seq_ids, 1, nullptr, k_new, v_new, stream);
         return rc != GQA_OK ? rc : attn_decode(c, B, seq_ids, H_q, q, out, stream);
     }
@@ -1196,8 +1202,9 @@ int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
         return fail(GQA_EINVAL, "NULL cache");
     if (kernel != GQA_DECODE_AUTO && kernel != GQA_DECODE_TENSOR_CORE && kernel != GQA_DECODE_CUDA_CORE)
         return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE or _CUDA_CORE", kernel);
-    if (kernel == GQA_DECODE_TENSOR_CORE && (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128))
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128");
+    if (kernel == GQA_DECODE_TENSOR_CORE &&
+        ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128))
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 or FP8 E4M3 cache with d_h = 128");
     c->decode_kernel = kernel;
     return GQA_OK;
 }

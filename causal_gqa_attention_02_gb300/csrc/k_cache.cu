@@ -167,10 +167,12 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
 // code = E4M3(x / s) with the quotient in fp32 and the conversion rounding
 // to nearest-even and saturating; a row of zeros gets s = 0 and zero codes.
 // The codes go to the row's place in the block layout, s to the scale array.
+// With zero_out, rows count..n-1 of zero_out ([B, n, zero_row_bytes]) are
+// set to zero in the same grid, as in cache_write_kernel.
 template <int P>
 __global__ void __launch_bounds__(256)
 cache_write_q8_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, const __nv_bfloat16 *__restrict__ k,
-                      const __nv_bfloat16 *__restrict__ v)
+                      const __nv_bfloat16 *__restrict__ v, char *__restrict__ zero_out, int zero_row_bytes)
 {
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
@@ -213,6 +215,14 @@ cache_write_q8_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, cons
             dst[pool_in_block(chunks, slot, lane * P + i)] = code[i];
         if (lane == 0)
             pv.scales[blk * kPageTokens + slot] = sc;
+    }
+    if (zero_out) {
+        const int zunits = zero_row_bytes / 16;
+        for (int t = sd.count + blockIdx.x * wpb + warp; t < n; t += gridDim.x * wpb) {
+            uint4 *dst = (uint4 *)(zero_out + ((size_t)b * n + t) * zero_row_bytes);
+            for (int u = lane; u < zunits; u += 32)
+                dst[u] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -259,23 +269,25 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     const int rows = zero_out ? n : max_count;          // padding rows are zeroed too
     if (B <= 0 || rows <= 0)
         return cudaSuccess;
-    if (pv.dtype == kDtypeFp8) {                        // quantising write (no padding rows to zero)
-        if (zero_out || pv.d % 32 != 0 || pv.d > 256 || !pv.scales)
+    if (pv.dtype == kDtypeFp8) {                        // quantising write
+        if (pv.d % 32 != 0 || pv.d > 256 || !pv.scales ||
+            (zero_out && (zero_row_bytes % 16 != 0 || (uintptr_t)zero_out % 16 != 0)))
             return cudaErrorInvalidValue;
-        int blocks = (max_count * 2 * pv.H_kv + 7) / 8;
+        int blocks = (max(max_count * 2 * pv.H_kv, rows) + 7) / 8;
         if (blocks > 1024)
             blocks = 1024;
         dim3 grid((unsigned)blocks, (unsigned)B);
         const __nv_bfloat16 *kb = (const __nv_bfloat16 *)k, *vb = (const __nv_bfloat16 *)v;
+        char *z = (char *)zero_out;
         switch (pv.d / 32) {
-        case 1: cache_write_q8_kernel<1><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 2: cache_write_q8_kernel<2><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 3: cache_write_q8_kernel<3><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 4: cache_write_q8_kernel<4><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 5: cache_write_q8_kernel<5><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 6: cache_write_q8_kernel<6><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        case 7: cache_write_q8_kernel<7><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
-        default: cache_write_q8_kernel<8><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb); break;
+        case 1: cache_write_q8_kernel<1><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 2: cache_write_q8_kernel<2><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 3: cache_write_q8_kernel<3><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 4: cache_write_q8_kernel<4><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 5: cache_write_q8_kernel<5><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 6: cache_write_q8_kernel<6><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        case 7: cache_write_q8_kernel<7><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
+        default: cache_write_q8_kernel<8><<<grid, 256, 0, st>>>(pv, d_seqs, n, kb, vb, z, zero_row_bytes); break;
         }
         return cudaGetLastError();
     }

@@ -51,6 +51,7 @@
 // drains what it has in flight (bounded) and exits cleanly.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -103,6 +104,7 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 o[2][128 * 64];                      // epilogue staging, one column half per query tile
     uint64_t bar_q, q_empty, q_rot[2];
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t k_land[kKStages], v_land[kVStages];       // Q8: a stage's codes have landed
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
     uint32_t tmem;
     int abort_;
@@ -137,7 +139,19 @@ struct TcParams {
     int32_t slot_rows;
     const __nv_bfloat16 *app_k;   // fused append: this call's one new K and V row per entry
     const __nv_bfloat16 *app_v;   // ([B, H_kv, 128]), written at position past; null = none
+    const float *scales;          // Q8: per-row scales of the FP8 E4M3 pool (block * 16 + slot)
 };
+
+// Two FP8 E4M3 codes (low byte first) dequantised with their row's scale:
+// decode (exact, through f16), times the scale in fp32, rounded to a bf16
+// pair for the tensor cores.
+__device__ __forceinline__ uint32_t e4m3x2_bf16x2(uint32_t pair, float2 sc)
+{
+    const float2 f =
+        __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair & 0xffffu), __NV_E4M3)));
+    const float2 x = fma2(f, sc, make_float2(0.f, 0.f));
+    return pack_bf16x2(x.x, x.y);
+}
 
 __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 {
@@ -151,9 +165,10 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 // tile load while the current item's last tiles and epilogue run.
 // ROPE: queries rotated in-kernel (p.rope is the table); WIN: items may start
 // past key tile 0 (a sliding window, whose keys before the window are
-// masked, or split items).  Both are template flags so the plain path
-// carries none of their instructions.
-template <bool ROPE, bool WIN>
+// masked, or split items); Q8: the pool holds FP8 E4M3 codes with a scale
+// per row (mKV then maps the code bytes).  All are template flags so the
+// plain path carries none of their instructions.
+template <bool ROPE, bool WIN, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
                   const __grid_constant__ CUtensorMap mO, const TcParams p)
@@ -188,10 +203,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.k_empty[i], 1);
+            mbar_init(&s.k_land[i], 1);
         }
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(&s.v_full[i], 1);
             mbar_init(&s.v_empty[i], 1);
+            mbar_init(&s.v_land[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s.s_full[t], 1);
@@ -289,6 +306,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             fence_proxy_async_global();
             __syncwarp();
         };
+        // Q8: the codes of a stage's 8 page blocks land in its upper half
+        // (block pg at byte 16384 + 2048 pg: [16 rows][128 codes]); the warp
+        // rewrites the stage in place as the bf16 operand (block pg at 4096 pg:
+        // [8-row group][column half][8 rows][64 elements], 128-byte rows with
+        // the 16-byte chunks swizzled by row), each code dequantised with its
+        // row's scale (fp32 product, rounded to bf16).  Block pg's output
+        // overlaps only blocks below pg and its own input, which the warp has
+        // read in full before it writes.  Then the stage is marked full.
+        // The scales of the lane's row in each of the tile's 8 pages are
+        // loaded when the tile is issued, so they are in registers by the
+        // time the tile is converted.
+        bool pending = false;                             // Q8: a landed tile still to convert
+        int pend_st = 0;
+        uint32_t pend_use = 0;
+        float pend_sc[8];
+        auto convert = [&](int st, uint32_t use, const float (&scl)[8]) -> bool {
+            if (!wait0(vside ? &s.v_land[st] : &s.k_land[st], use & 1))
+                return false;
+            unsigned char *base = reinterpret_cast<unsigned char *>(vside ? s.v[st][0] : s.k[st][0]);
+            const int r = lane >> 1, h = lane & 1;        // this lane's row (slot) and column half
+#pragma unroll
+            for (int pg = 0; pg < 8; ++pg) {
+                const float2 sc2 = make_float2(scl[pg], scl[pg]);
+                const uint4 *src = reinterpret_cast<const uint4 *>(base + 16384 + 2048 * pg + r * 128 + h * 64);
+                uint4 c4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    c4[i] = src[i];
+                __syncwarp();
+                unsigned char *dst = base + 4096 * pg + (r >> 3) * 2048 + h * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {             // chunk c: elements 8c .. 8c + 7 of the half
+                    const uint32_t w0 = (c & 1) ? c4[c >> 1].z : c4[c >> 1].x;
+                    const uint32_t w1 = (c & 1) ? c4[c >> 1].w : c4[c >> 1].y;
+                    uint4 o;
+                    o.x = e4m3x2_bf16x2(w0, sc2);
+                    o.y = e4m3x2_bf16x2(w0 >> 16, sc2);
+                    o.z = e4m3x2_bf16x2(w1, sc2);
+                    o.w = e4m3x2_bf16x2(w1 >> 16, sc2);
+                    *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = o;
+                }
+                __syncwarp();
+            }
+            fence_proxy_async_smem();                     // the MMA reads the stage through the async proxy
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(vside ? &s.v_full[st] : &s.k_full[st]);
+            return true;
+        };
         // Loads this warp's half (K or V) of key tile j of an item into
         // stage gt % stages once its last readers are done.
         auto load_tile = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
@@ -312,10 +378,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             uint64_t *empty = vside ? &s.v_empty[st] : &s.k_empty[st];
             uint64_t *full = vside ? &s.v_full[st] : &s.k_full[st];
             __nv_bfloat16 *dst = vside ? s.v[st][0] : s.k[st][0];
+            // Q8: the previous tile (landed in the other stage) is converted
+            // first, so that its conversion overlaps the MMAs still reading
+            // this stage.
+            if (Q8 && pending) {
+                if (!convert(pend_st, pend_use, pend_sc))
+                    return false;
+                pending = false;
+            }
             if (use > 0 && !wait0(empty, (use - 1) & 1))
                 return false;
-            if (p.app_k && j == it.nt - 1 && (sd.past >> 7) == j)
+            if (!Q8 && p.app_k && j == it.nt - 1 && (sd.past >> 7) == j)
                 append_row(it, sd);                       // the tile holds this call's new token: write it first
+            if (Q8) {
+                // Codes (2 KB per page block) into the stage's upper half; the
+                // rows' scales are pulled into L1 for the softmax warps.
+                uint64_t *land = vside ? &s.v_land[st] : &s.k_land[st];
+                if (lane == 0)
+                    mbar_arrive_expect_tx(land, kTileBytes);
+                __syncwarp();
+                const int blk = ph * blk_page + (vside ? p.H_kv : 0) + it.kvh;
+                if (boxer) {
+                    tma_load_3d(&mKV, land, reinterpret_cast<unsigned char *>(dst) + 16384 + 2048 * my_pg, 0, 0, blk);
+                    if (ph < p.num_pages)
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.scales + (size_t)blk * kPageTokens));
+                }
+                ++gt;
+                float nsc[8];                             // this tile's scales of row lane / 2
+                const int my_blk = boxer && ph < p.num_pages ? blk : -1;
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg) {
+                    const int b2 = __shfl_sync(0xffffffffu, my_blk, pg);
+                    nsc[pg] = b2 >= 0 ? __ldg(p.scales + (size_t)b2 * kPageTokens + (lane >> 1)) : 0.0f;
+                }
+                pending = true, pend_st = st, pend_use = use;
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg)
+                    pend_sc[pg] = nsc[pg];
+                return true;
+            }
             if (lane == 0)
                 mbar_arrive_expect_tx(full, 2 * kTileBytes);
             __syncwarp();
@@ -356,13 +457,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     break;
                 }
         }
+        if (Q8 && ok && pending && !convert(pend_st, pend_use, pend_sc))   // the last tile
+            ok = false;
         if (lane == 0) {
             if (!ok)
                 abort_with(s, p.err, kErrTimeout);
             // Drain: every issued copy lands before the CTA exits.
             int never = 0;
             for (uint32_t g = (gt > (uint32_t)stages ? gt - stages : 0); g < gt; ++g) {
-                uint64_t *full = vside ? &s.v_full[g % stages] : &s.k_full[g % stages];
+                uint64_t *full = Q8 ? (vside ? &s.v_land[g % stages] : &s.k_land[g % stages])
+                                    : (vside ? &s.v_full[g % stages] : &s.k_full[g % stages]);
                 if (!mbar_wait(full, (g / stages) & 1, &never))
                     atomicOr(p.err, kErrTimeout);
             }
@@ -917,14 +1021,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 }
 
 bool encode(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
-            const cuuint32_t *box)
+            const cuuint32_t *box, bool bytes = false)
 {
     auto fn = encoder();
     if (!fn)
         return false;
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    // bytes: FP8 code blocks, copied as they are (the kernel lays them out).
+    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+              const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -954,8 +1060,16 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     const cuuint64_t kvdims[3] = {64, 32, (cuuint64_t)pv.num_pages * 2 * pv.H_kv};
     const cuuint64_t kvstr[2] = {128, 32 * 128};
     const cuuint32_t kvbox[3] = {64, 32, 1};
+    // FP8 E4M3 pool: a block is [16 rows][128 code bytes]; one 2 KB box each.
+    const bool q8 = pv.dtype == kDtypeFp8;
+    const cuuint64_t kv8dims[3] = {128, 16, (cuuint64_t)pv.num_pages * 2 * pv.H_kv};
+    const cuuint64_t kv8str[2] = {128, 16 * 128};
+    const cuuint32_t kv8box[3] = {128, 16, 1};
+    if (q8 && (pv.rope || app_k || !pv.scales))
+        return cudaErrorInvalidValue;
     // out has the shape and layout of q: the same box serves the stores.
-    if (!encode(&mq, 4, q, qdims, qstr, qbox) || !encode(&mkv, 3, pv.pool, kvdims, kvstr, kvbox) ||
+    if (!encode(&mq, 4, q, qdims, qstr, qbox) ||
+        !(q8 ? encode(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true) : encode(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)) ||
         !encode(&mo, 4, out, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     TcParams prm;
@@ -966,6 +1080,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.pool = pv.pool;
     prm.app_k = (const __nv_bfloat16 *)app_k;
     prm.app_v = (const __nv_bfloat16 *)app_v;
+    prm.scales = pv.scales;
     prm.stride = pv.stride;
     prm.num_pages = pv.num_pages;
     prm.H_kv = pv.H_kv;
@@ -983,11 +1098,13 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.counters = ws.counters;
     prm.slot_rows = ws.slot_rows;
     const int smem = (int)sizeof(TcSmem) + 1024;
-    static bool attr_set[4] = {false, false, false, false};
-    const int which = (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
-    void (*const kern[4])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
-        prefill_tc_kernel<false, false>, prefill_tc_kernel<true, false>, prefill_tc_kernel<false, true>,
-        prefill_tc_kernel<true, true>};
+    static bool attr_set[6] = {false, false, false, false, false, false};
+    const int which = q8 ? 4 + (pv.window > 0 || ws.ranged ? 1 : 0)
+                         : (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
+    void (*const kern[6])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
+        prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
+        prefill_tc_kernel<false, true, false>,  prefill_tc_kernel<true, true, false>,
+        prefill_tc_kernel<false, false, true>,  prefill_tc_kernel<false, true, true>};
     if (!attr_set[which]) {
         cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)

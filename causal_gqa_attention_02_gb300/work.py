@@ -41,8 +41,10 @@ def window_tokens(L: int, window: int = 0) -> int:
     return min(int(L), int(window)) if window > 0 else int(L)
 
 
-def decode_kv_bytes(lengths, H_kv: int, d: int, esize: int = 2, window: int = 0) -> int:
-    return sum(window_tokens(L, window) for L in lengths) * 2 * int(H_kv) * int(d) * int(esize)
+def decode_kv_bytes(lengths, H_kv: int, d: int, esize: int = 2, window: int = 0, row_extra: int = 0) -> int:
+    """K and V bytes a decode reads: per visible token and KV head, d * esize
+    bytes of each, plus row_extra (a quantised cache's per-row scale)."""
+    return sum(window_tokens(L, window) for L in lengths) * 2 * int(H_kv) * (int(d) * int(esize) + int(row_extra))
 
 
 def decode_flops(lengths, H_q: int, d: int, window: int = 0) -> int:

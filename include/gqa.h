@@ -59,7 +59,8 @@
  * block*16 + s.  A row x (the bf16 values given) is stored as s = amax|x| /
  * 448 (fp32) and codes E4M3(x_i / s) (the quotient in fp32, rounded to
  * nearest-even, saturating at +-448); a row of zeros has s = 0 and zero
- * codes.  Attention reads the value fp32(decode(code) * s).
+ * codes.  Attention reads the value fp32(decode(code) * s) (the tensor-core
+ * kernel rounds it to bf16 for its operands).
  *
  * Allocation rules (deterministic; the tests restate them independently):
  *  - a free page is taken in the order `page_order` gives (identity when
@@ -350,17 +351,21 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
 
 /* Decode kernel of attn_decode and attn_decode_static.
  *  GQA_DECODE_AUTO         (default) tensor-core when the cache is bf16 with
- *                          d_h = 128, else CUDA-core.
+ *                          d_h = 128, else CUDA-core (an FP8 E4M3 cache
+ *                          decodes faster on the CUDA-core kernel).
  *  GQA_DECODE_TENSOR_CORE  the prefill kernel with one query row per
  *                          sequence: every KV head's key tiles are read once
  *                          by TMA, a sequence's tiles are split into ranges
  *                          across SMs when there are too few sequences, and
  *                          the ranges' partial (m, l, O) are merged inside
  *                          the kernel by the CTA that finishes last.  Needs
- *                          bf16 and d_h = 128 (else GQA_EINVAL here).
- *  GQA_DECODE_CUDA_CORE    the split-K CUDA-core decode kernel (bf16, d_h =
- *                          128, H_q / H_kv <= 8), else the generic CUDA-core
- *                          kernel.
+ *                          bf16 or FP8 E4M3 and d_h = 128 (else GQA_EINVAL
+ *                          here).  FP8 codes are dequantised into bf16
+ *                          operands in shared memory (code times scale in
+ *                          fp32, rounded to bf16).
+ *  GQA_DECODE_CUDA_CORE    the split-K CUDA-core decode kernel (bf16 or FP8
+ *                          E4M3, d_h = 128, H_q / H_kv <= 8), else the
+ *                          generic CUDA-core kernel.
  * Both compute the same softmax; they differ in rounding order only.
  * Errors: GQA_EINVAL (unknown choice, or tensor-core on another cache). */
 #define GQA_DECODE_AUTO         0

@@ -2,7 +2,9 @@
 the stored codes and per-row scales bit for bit (the cache write's rounding
 decides integers, so both sides decide them in fp32 as the header states),
 block tables and lengths exact, and attention outputs -- over the
-dequantised values -- within the bf16 tolerance."""
+dequantised values -- within the bf16 tolerance, on the CUDA-core kernels
+and on the tensor-core kernel (which dequantises each tile into bf16
+operands in shared memory)."""
 import numpy as np
 import pytest
 import torch
@@ -114,6 +116,7 @@ def test_fp8_split_decode_kernel(H_q, H_kv, lengths):
     B, d = len(lengths), 128
     pages = sum(workloads.pages_for(L) for L in lengths) + 4
     c, m, ids, mids = _caches(B, H_kv, d, pages, workloads.pages_for(max(lengths)) + 1)
+    c.set_decode_kernel("cuda_core")
     for b, L in enumerate(lengths):
         k = workloads.normal_bf16(rng, (1, L, H_kv, d))
         v = workloads.normal_bf16(rng, (1, L, H_kv, d))
@@ -131,7 +134,65 @@ def test_fp8_split_decode_kernel(H_q, H_kv, lengths):
     assert c.check() == 0
 
 
-def test_fp8_cache_rejects_the_tensor_core_choices():
-    c = gqa.Cache(2, 128, 8, 2, 4, dtype="fp8")
-    with pytest.raises(gqa.GqaError):
-        c.set_decode_kernel("tensor_core")
+@pytest.mark.parametrize("H_q,H_kv,lengths,window", [
+    (32, 8, [1, 17, 300, 2049, 5000], 0),
+    (48, 8, [8300], 0),                  # one long sequence: key ranges split across SMs and merged
+    (128, 8, [700, 3000], 0),            # g = 16
+    (32, 8, [6000, 250, 1800], 500),
+])
+def test_fp8_tensor_core_decode(H_q, H_kv, lengths, window):
+    rng = np.random.default_rng(140 + H_q + window)
+    B, d = len(lengths), 128
+    pages = sum(workloads.pages_for(L) for L in lengths) + 4
+    per_seq = workloads.pages_for(max(lengths)) + 1
+    c = gqa.Cache(H_kv, d, pages, B, per_seq, dtype="fp8", window=window)
+    m = oracle.CacheModel(pages, B, per_seq, H_kv, d, "fp8", window=window)
+    ids, mids = [c.seq_create() for _ in range(B)], [m.create() for _ in range(B)]
+    c.set_decode_kernel("tensor_core")
+    for b, L in enumerate(lengths):
+        k = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        v = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        gqa.kv_append(c, [ids[b]], dev(k, "bf16"), dev(v, "bf16"))
+        oracle.append(m, [mids[b]], k, v)
+    for t in range(3):
+        q = workloads.normal_bf16(rng, (B, H_q, d))
+        kt = workloads.normal_bf16(rng, (B, H_kv, d))
+        vt = workloads.normal_bf16(rng, (B, H_kv, d))
+        c.profile_read()
+        o = gqa.attn_decode_append(c, ids, dev(q, "bf16"), dev(kt, "bf16"), dev(vt, "bf16"))
+        launched = c.profile_read()
+        assert launched["prefill_tc"][0] == 1 and launched["cache_write"][0] == 1, launched
+        oracle.append(m, mids, kt, vt)
+        assert_close(host_f64(o, "bf16"), oracle.decode(m, mids, q), "bf16", "fp8 tensor-core decode %d" % t)
+        s = gqa.attn_decode_static(c, ids, dev(q, "bf16"))
+        assert torch.equal(o.view(torch.int16), s.view(torch.int16))
+    if window == 0:
+        _check_stored(c, m, list(zip(ids, mids)))
+    assert c.check() == 0
+
+
+@pytest.mark.parametrize("B,H_q,H_kv,n,lo,hi", [
+    (3, 32, 8, 300, 100, 300),
+    (2, 16, 2, 520, 300, 520),
+])
+def test_fp8_tensor_core_prefill(B, H_q, H_kv, n, lo, hi):
+    w = workloads.ragged_prefill(seed=150 + H_q, B=B, H_q=H_q, H_kv=H_kv, n=n, lo=lo, hi=hi)
+    nb = w["valid_lengths"]
+    pages = sum(workloads.pages_for(x) for x in nb) + 8
+    c, m, ids, mids = _caches(B, H_kv, 128, pages, workloads.pages_for(n) + 1)
+    c.profile_read()
+    out = host_f64(gqa.attn_prefill(c, ids, dev(w["q"], "bf16"), dev(w["k"], "bf16"), dev(w["v"], "bf16"), nb),
+                   "bf16")
+    assert c.profile_read()["prefill_tc"][0] == 1
+    ref = oracle.prefill(m, mids, w["q"], w["k"], w["v"], nb)
+    mask = np.arange(n)[None, :] < np.asarray(nb)[:, None]
+    assert_close(out[mask], ref[mask], "bf16", "fp8 tensor-core prefill")
+    assert np.all(out[~mask] == 0)
+    _check_stored(c, m, list(zip(ids, mids)))
+    # A second, incremental call reads the first call's codes.
+    q2 = workloads.normal_bf16(np.random.default_rng(1), (B, 40, H_q, 128))
+    k2 = workloads.normal_bf16(np.random.default_rng(2), (B, 40, H_kv, 128))
+    v2 = workloads.normal_bf16(np.random.default_rng(3), (B, 40, H_kv, 128))
+    o2 = host_f64(gqa.attn_prefill(c, ids, dev(q2, "bf16"), dev(k2, "bf16"), dev(v2, "bf16"), [40] * B), "bf16")
+    assert_close(o2, oracle.prefill(m, mids, q2, k2, v2, [40] * B), "bf16", "fp8 incremental prefill")
+    assert c.check() == 0
