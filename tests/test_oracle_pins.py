@@ -323,7 +323,7 @@ def test_bf16_inputs_are_read_exactly():
 # Q/K fixed by the position ID, whose inner products depend only on the
 # position difference; position 0 and equal positions leave inner products
 # unchanged.  The pins check those properties, the pairing and direction
-# read in the design doc through a second form (complex multiplication), and the
+# read through a second form (complex multiplication), and the
 # stored-key rounding rule against exact arithmetic.
 
 def test_rope_position_zero_is_identity():
