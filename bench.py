@@ -288,7 +288,9 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     kernels = {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl}
 
     # End to end through the public API from pinned host buffers, pipelined
-    # over the batch entries: entry b's valid rows go up on one copy stream,
+    # over the batch entries, largest first (the last entry's compute and
+    # copy back are the part that does not overlap): entry b's valid rows go
+    # up on one copy stream,
     # attn_prefill of entry b runs on the compute stream once they are in,
     # and its valid output rows come back on a second copy stream while the
     # next entry computes.  Only valid rows cross the link (padding rows of
@@ -302,16 +304,18 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     ev_in = [torch.cuda.Event() for _ in range(B)]
     ev_out = [torch.cuda.Event() for _ in range(B)]
 
+    order = sorted(range(B), key=lambda x: -nb[x])
+
     def e2e_step():
         up.wait_stream(main)
         down.wait_stream(main)
         with torch.cuda.stream(up):
-            for b in range(B):
+            for b in order:
                 qd[b, :nb[b]].copy_(qh[b, :nb[b]], non_blocking=True)
                 kd[b, :nb[b]].copy_(kh[b, :nb[b]], non_blocking=True)
                 vd[b, :nb[b]].copy_(vh[b, :nb[b]], non_blocking=True)
                 ev_in[b].record(up)
-        for b in range(B):
+        for b in order:
             main.wait_event(ev_in[b])
             gqa.attn_prefill(cache, [ids[b]], qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], [nb[b]], out=od[b:b + 1])
             ev_out[b].record(main)
@@ -330,8 +334,8 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     e2e = {"value": round(flops * args.steps * dist.world / (e2e_total / 1e3) / 1e12, 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(sum(nb) * (row_q + 2 * row_kv)), "d2h_bytes_per_step": int(sum(nb) * row_q),
            "ms_per_step": round(e2e_total / args.steps, 4),
-           "how": "attn_prefill per batch entry on one stream; valid rows copied up/down on two copy streams, "
-                  "overlapping the other entries' compute"}
+           "how": "attn_prefill per batch entry on one stream, largest first; valid rows copied up/down on two "
+                  "copy streams, overlapping the other entries' compute"}
     flags = cache.check()
     cache.close()
     del flush

@@ -116,10 +116,16 @@ def _i32_array(values):
     return arr, ctypes.cast(arr, _I32P)
 
 
-def _stream_handle(stream):
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream, device=None):
+    """cudaStream_t of `stream` (default: the current stream of `device`)."""
     if stream is None:
+        if _raw_stream is not None and device is not None:
+            return _raw_stream(device)
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 # Element type of q, k, v and out (a quantised cache takes and returns bf16).
@@ -146,6 +152,7 @@ class Cache:
         self.num_kv_heads, self.head_dim, self.num_pages = num_kv_heads, head_dim, num_pages
         self.max_seqs, self.max_pages_per_seq = max_seqs, max_pages_per_seq
         self.pool = None
+        self.device_index = None
         self._h = ctypes.c_void_p()
         nbytes = _lib.gqa_pool_bytes(ctypes.byref(self.desc))
         if metadata_only:
@@ -153,6 +160,7 @@ class Cache:
         else:
             dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
             self.pool = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+            self.device_index = self.pool.device.index
             with torch.cuda.device(dev):
                 _check(_lib.gqa_cache_create(ctypes.byref(self.desc), ctypes.c_void_p(self.pool.data_ptr()),
                                              nbytes, ctypes.byref(self._h)))
@@ -255,7 +263,8 @@ class Cache:
     def check(self, stream=None) -> int:
         """Synchronise and read/clear the device error word (0 = clean)."""
         flags = ctypes.c_int32()
-        rc = _lib.gqa_cache_check(self._h, _stream_handle(stream) if self.pool is not None else None,
+        st = _stream_handle(stream, self.device_index) if self.pool is not None else None
+        rc = _lib.gqa_cache_check(self._h, st,
                                   ctypes.byref(flags))
         if rc not in (OK, EDEVICE):
             _check(rc)
@@ -272,6 +281,9 @@ def layout_compatible(a: LayoutMetadata, b: LayoutMetadata) -> bool:
 def _dev_ptr(t, what, dtype, shape=None):
     if t is None:
         return None
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous()
+            and (shape is None or t.shape == shape)):
+        return t.data_ptr()                       # the common case, checked in one pass
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError("%s must be a CUDA tensor" % what)
     if t.dtype != dtype:
@@ -299,7 +311,7 @@ def attn_prefill(cache: Cache, seq_ids, q, k, v, valid_lengths, positions=None, 
                              _dev_ptr(k, "k", dt, (B, n, cache.num_kv_heads, d)),
                              _dev_ptr(v, "v", dt, (B, n, cache.num_kv_heads, d)),
                              vp, pp, _dev_ptr(out, "out", dt, (B, n, H_q, d)),
-                             _stream_handle(stream) if cache.pool is not None else None))
+                             _stream_handle(stream, cache.device_index) if cache.pool is not None else None))
     return out
 
 
@@ -323,7 +335,7 @@ def kv_append(cache: Cache, seq_ids, k_new, v_new, counts=None, stream=None):
     _check(_lib.kv_append(cache.handle, B, sp, n, cp,
                           _dev_ptr(k_new, "k_new", cache.torch_dtype, shape),
                           _dev_ptr(v_new, "v_new", cache.torch_dtype, shape),
-                          _stream_handle(stream)))
+                          _stream_handle(stream, cache.device_index)))
 
 
 def kv_append_meta(cache: Cache, seq_ids, n, counts=None):
@@ -340,7 +352,8 @@ def attn_decode(cache: Cache, seq_ids, q, out=None, stream=None):
     shape = (B, H_q, cache.head_dim)
     keep_s, sp = _i32_array(seq_ids)
     _check(_lib.attn_decode(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
-                            _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+                            _dev_ptr(out, "out", cache.torch_dtype, shape),
+                            _stream_handle(stream, cache.device_index)))
     return out
 
 
@@ -356,7 +369,8 @@ def attn_decode_append(cache: Cache, seq_ids, q, k_new, v_new, out=None, stream=
     _check(_lib.attn_decode_append(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
                                    _dev_ptr(k_new, "k_new", cache.torch_dtype, kv_shape),
                                    _dev_ptr(v_new, "v_new", cache.torch_dtype, kv_shape),
-                                   _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+                                   _dev_ptr(out, "out", cache.torch_dtype, shape),
+                            _stream_handle(stream, cache.device_index)))
     return out
 
 
@@ -374,7 +388,8 @@ def attn_decode_static(cache: Cache, seq_ids, q, out=None, stream=None):
     shape = (B, H_q, cache.head_dim)
     keep_s, sp = _i32_array(seq_ids)
     _check(_lib.attn_decode_static(cache.handle, B, sp, H_q, _dev_ptr(q, "q", cache.torch_dtype, shape),
-                                   _dev_ptr(out, "out", cache.torch_dtype, shape), _stream_handle(stream)))
+                                   _dev_ptr(out, "out", cache.torch_dtype, shape),
+                            _stream_handle(stream, cache.device_index)))
     return out
 
 
