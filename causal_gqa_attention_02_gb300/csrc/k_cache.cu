@@ -86,6 +86,9 @@ cache_write_kernel(PoolView pv, int esize, const SeqDesc *__restrict__ seqs, int
 {
     using T = typename Unit<U>::T;
     constexpr int kMaxPerLane = ROPE ? 4 : 8;           // units per lane held in registers per pass
+    // A dependent attention grid may be scheduled once every block of this
+    // one has started; it waits for this grid's writes before reading pages.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(256)
 cache_write_q8_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, const __nv_bfloat16 *__restrict__ k,
                       const __nv_bfloat16 *__restrict__ v, char *__restrict__ zero_out, int zero_row_bytes)
 {
+    asm volatile("griddepcontrol.launch_dependents;");   // as in cache_write_kernel
     const int b = blockIdx.y;
     const SeqDesc sd = seqs[b];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;

@@ -89,6 +89,11 @@ constexpr int kKStages = GQA_K_STAGES;
 #define GQA_PV_ORDER 1
 #endif
 constexpr bool kPvOrder = GQA_PV_ORDER != 0;
+// Programmatic dependent launch: the kernel may start while the cache write
+// that precedes it finishes; only the K/V loads wait for that grid.
+#ifndef GQA_PDL
+#define GQA_PDL 1
+#endif
 constexpr int kVStages = GQA_V_STAGES;
 constexpr int kThreads = 384;     // warpgroup 0: TMA + MMA; warpgroups 1, 2: softmax
 constexpr uint32_t kTileBytes = 128 * 64 * 2;        // one 128-row x 64-column bf16 half tile
@@ -432,6 +437,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             load_q(p.items[i_begin]);
             first_q_issued = true;
         }
+#if GQA_PDL
+        // The pages are written by the preceding cache-write grid: its
+        // writes are complete and visible once this returns (at once when
+        // no grid precedes).  Q above does not depend on it.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
         for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
             const TcItem it = p.items[idx];
             const SeqDesc sd = p.seqs[it.b];
@@ -1113,8 +1124,22 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     }
     if (ev_start)
         cudaEventRecord(ev_start, st);       // after the host-side preparation above
+#if GQA_PDL
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern[which], mq, mkv, mo, prm);
+#else
     kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
     return cudaGetLastError();
+#endif
 }
 
 }  // namespace gqa
