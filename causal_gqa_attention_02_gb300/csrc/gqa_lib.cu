@@ -273,22 +273,28 @@ int check_device(const gqa_cache *c)
 }
 
 // Upload the block-table entries changed since the last upload.
+// One copy of the span of the flat table that covers every dirty entry
+// (rows are contiguous, and clean entries between equal the device's), so a
+// call pays one copy however many sequences it touched.
 int upload_tables(gqa_cache *c, cudaStream_t st)
 {
+    size_t lo = SIZE_MAX, hi = 0;
     for (int32_t s : c->dirty_list) {
         SeqState &S = c->seqs[s];
         if (S.dirty_hi > S.dirty_lo) {
-            const size_t off = (size_t)s * c->stride() + S.dirty_lo;
-            cudaError_t e = cudaMemcpyAsync(c->d_tab + off, c->h_tab.data() + off,
-                                            (size_t)(S.dirty_hi - S.dirty_lo) * sizeof(int32_t),
-                                            cudaMemcpyHostToDevice, st);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "block-table upload");
+            lo = std::min(lo, (size_t)s * c->stride() + S.dirty_lo);
+            hi = std::max(hi, (size_t)s * c->stride() + S.dirty_hi);
         }
         S.dirty_lo = INT_MAX;
         S.dirty_hi = 0;
     }
     c->dirty_list.clear();
+    if (hi > lo) {
+        cudaError_t e = cudaMemcpyAsync(c->d_tab + lo, c->h_tab.data() + lo, (hi - lo) * sizeof(int32_t),
+                                        cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "block-table upload");
+    }
     return GQA_OK;
 }
 
