@@ -87,6 +87,7 @@ _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
 _sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
 _sig("gqa_set_decode_kernel", ctypes.c_int, _vp, ctypes.c_int32)
+_sig("gqa_selftest_bounded_wait", ctypes.c_int, _vp, ctypes.c_int64, _vp)
 _sig("gqa_profile_read", ctypes.c_int, _vp, _i32, _I32P, ctypes.POINTER(ctypes.c_double))
 _sig("gqa_last_error", ctypes.c_char_p)
 _sig("gqa_version", ctypes.c_char_p)
@@ -246,6 +247,12 @@ class Cache:
         """Decode kernel of attn_decode / attn_decode_static: "auto",
         "tensor_core" or "cuda_core"."""
         _check(_lib.gqa_set_decode_kernel(self._h, DECODE_KERNELS[kernel]))
+
+    def selftest_bounded_wait(self, limit_ns: int, stream=None):
+        """Queue a block whose bounded wait runs out after limit_ns and sets
+        the timeout bit of the error word (see include/gqa.h)."""
+        st = _stream_handle(stream, self.device_index) if self.pool is not None else None
+        _check(_lib.gqa_selftest_bounded_wait(self._h, int(limit_ns), st))
 
     def profile(self, on: bool):
         """Bracket every kernel launch with CUDA events (on its stream)."""
@@ -409,4 +416,4 @@ def exported_symbols():
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
             "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel",
-            "attn_decode_append"]
+            "attn_decode_append", "gqa_selftest_bounded_wait"]

@@ -1202,6 +1202,21 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     return rc;
 }
 
+int gqa_selftest_bounded_wait(gqa_cache *c, int64_t limit_ns, void *stream)
+{
+    if (!c)
+        return fail(GQA_EINVAL, "NULL cache");
+    if (limit_ns < 1 || limit_ns > 10000000000ll)
+        return fail(GQA_ERANGE, "limit_ns %lld outside 1..10^10", (long long)limit_ns);
+    if (c->meta_only)
+        return fail(GQA_EINVAL, "the self-test needs a cache with a device pool");
+    int rc = check_device(c);
+    if (rc != GQA_OK)
+        return rc;
+    const cudaError_t e = launch_wait_probe(c->d_err, (uint64_t)limit_ns, (cudaStream_t)stream);
+    return e == cudaSuccess ? GQA_OK : cuda_fail(e, "wait probe");
+}
+
 int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
 {
     if (!c)

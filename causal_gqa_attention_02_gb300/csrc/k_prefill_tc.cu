@@ -1045,7 +1045,31 @@ bool encode(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The bounded wait every kernel here uses, on a barrier phase that nothing
+// completes: it gives up after limit_ns and records a timeout in the error
+// word, as a pipeline wait would.  Exercises the failure path without a
+// fault.
+__global__ void wait_probe_kernel(int32_t *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_ = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_for(&bar, 0, &abort_, limit_ns))
+        atomicOr(err, kErrTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(int32_t *err, uint64_t limit_ns, cudaStream_t st)
+{
+    wait_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+    return cudaGetLastError();
+}
 
 bool prefill_tc_supported(int group, int H_kv) { return group >= 1 && group <= 128 && H_kv >= 1; }
 

@@ -159,6 +159,9 @@ cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaS
 // bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).  Rows of the
 // batch entries must already be in the cache (launch_cache_write first).
 bool prefill_tc_supported(int group, int H_kv);
+// One block waiting, with the kernels' bounded wait, on a barrier phase that
+// never completes; sets kErrTimeout in *err after limit_ns.
+cudaError_t launch_wait_probe(int32_t *err, uint64_t limit_ns, cudaStream_t st);
 int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // Persistent grid of `grid` CTAs; CTA c takes items[item_start[c] ..
 // item_start[c + 1]) in order (grid + 1 offsets, every run non-empty).  Rows

@@ -90,10 +90,12 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
 #endif
 
 // Wait until the barrier phase of the given parity has completed.  Returns
-// false once *abort is non-zero or the wait has lasted kWaitTimeoutNs.  Every
+// false once *abort is non-zero or the wait has lasted limit_ns (mbar_wait:
+// kWaitTimeoutNs).  Every
 // probe returns within a bounded time (test_wait at once, try_wait within
 // its suspend-time hint), so the bound holds.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                              uint64_t limit_ns)
 {
     if (mbar_test(bar, parity))
         return true;
@@ -104,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
             return true;
         if (*abort)
             return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs)
+        if (globaltimer() - t0 > limit_ns)
             return false;
     }
 #else
@@ -116,11 +118,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
         if ((it & 63) == 0) {
             if (*abort)
                 return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs)
+            if (globaltimer() - t0 > limit_ns)
                 return false;
         }
     }
 #endif
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+{
+    return mbar_wait_for(bar, parity, abort, kWaitTimeoutNs);
 }
 
 // ---- TMA (cp.async.bulk.tensor) ------------------------------------------------

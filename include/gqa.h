@@ -373,6 +373,16 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
 #define GQA_DECODE_CUDA_CORE    2
 int gqa_set_decode_kernel(gqa_cache *cache, int32_t kernel);
 
+/* Self-test of the failure path of the kernels' waits.  Queues one block
+ * that waits, with the bounded wait the pipelines use, on a barrier phase
+ * nothing completes; after limit_ns it gives up and sets GQA_DEVERR_TIMEOUT
+ * in the cache's error word (read it with gqa_cache_check), as a timed-out
+ * pipeline wait would.  Nothing faults or traps, and the context stays
+ * usable.  Not part of the hot path.
+ * Errors: GQA_EINVAL (no device pool), GQA_ERANGE (limit_ns outside
+ * 1..10^10), GQA_ECUDA. */
+int gqa_selftest_bounded_wait(gqa_cache *cache, int64_t limit_ns, void *stream);
+
 /* Prefix-edit invalidation ([P3] edit at token m): keep positions < m of
  * `seq`, drop the rest.  Pages wholly beyond position m lose one reference
  * (and return to the pool at zero).  A partially kept tail page stays; if it

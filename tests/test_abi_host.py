@@ -352,3 +352,13 @@ def test_fp8_cache_description_and_pool_size():
         with pytest.raises(gqa.GqaError) as e:
             gqa.Cache(**args)
         assert e.value.name == "EINVAL", kw
+
+
+def test_bounded_wait_selftest_arguments():
+    c = gqa.Cache(2, 128, 8, 2, 4, dtype="bf16", metadata_only=True)
+    with pytest.raises(gqa.GqaError) as e:
+        c.selftest_bounded_wait(1000)
+    assert e.value.name == "EINVAL"
+    with pytest.raises(gqa.GqaError) as e:
+        gqa._check(gqa._lib.gqa_selftest_bounded_wait(c.handle, 0, None))
+    assert e.value.name == "ERANGE"
