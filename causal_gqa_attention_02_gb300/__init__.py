@@ -83,6 +83,7 @@ _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp, _vp, _vp)
+_sig("attn_decode_tables", ctypes.c_int, _vp, _i32, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
 _sig("gqa_profile_enable", ctypes.c_int, _vp, ctypes.c_int)
@@ -364,6 +365,25 @@ def attn_decode(cache: Cache, seq_ids, q, out=None, stream=None):
     return out
 
 
+def attn_decode_tables(cache: Cache, block_table, lengths, q, out=None, stream=None):
+    """Decode over caller-owned block tables: block_table is a device int32
+    tensor [B, stride] of page ids of this cache's pool, lengths a host
+    sequence of B lengths; q [B, H_q, d]."""
+    B, H_q = len(lengths), q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if (not isinstance(block_table, torch.Tensor) or not block_table.is_cuda or block_table.dtype != torch.int32
+            or block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous()):
+        raise ValueError("block_table must be a contiguous CUDA int32 tensor [B, stride]")
+    shape = (B, H_q, cache.head_dim)
+    keep_l, lp = _i32_array(lengths)
+    _check(_lib.attn_decode_tables(cache.handle, B, block_table.data_ptr(), block_table.shape[1], lp, H_q,
+                                   _dev_ptr(q, "q", cache.torch_dtype, shape),
+                                   _dev_ptr(out, "out", cache.torch_dtype, shape),
+                                   _stream_handle(stream, cache.device_index)))
+    return out
+
+
 def attn_decode_append(cache: Cache, seq_ids, q, k_new, v_new, out=None, stream=None):
     """One decode step: append k_new, v_new [B, H_kv, d] at each sequence's
     tail and attend q [B, H_q, d] to the cache including them."""
@@ -416,4 +436,4 @@ def exported_symbols():
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
             "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel",
-            "attn_decode_append", "gqa_selftest_bounded_wait"]
+            "attn_decode_append", "gqa_selftest_bounded_wait", "attn_decode_tables"]

@@ -1030,42 +1030,21 @@ int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const 
     return rc;
 }
 
-int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q, void *out,
-                void *stream)
+// Decode of B queries described by sds (row = block-table row, past = L - 1)
+// through the tables and stride of pv: the kernel choice, its work plan and
+// its launch.  The caller has validated everything and uploaded the tables.
+static int decode_launch(gqa_cache *c, const PoolView &pv, const std::vector<SeqDesc> &sds, int32_t H_q,
+                         const void *q, void *out, cudaStream_t st)
 {
-    if (!c || !seq_ids)
-        return fail(GQA_EINVAL, "NULL argument");
-    if (B < 1 || H_q < 1)
-        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int B = (int)sds.size();
     const int32_t H_kv = c->desc.num_kv_heads;
-    if (H_q % H_kv != 0)
-        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
-    if (!c->meta_only && (!q || !out))
-        return fail(GQA_EINVAL, "NULL tensor pointer");
-    std::vector<SeqDesc> sds(B);
-    int64_t total = 0;
-    for (int b = 0; b < B; ++b) {
-        const int32_t s = seq_ids[b];
-        if (!live(c, s))
-            return fail(GQA_EINVAL, "batch entry %d: sequence %d is not live", b, s);
-        const int32_t L = c->seqs[s].len;
-        if (L < 1)
-            return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
-        sds[b] = SeqDesc{s, L - 1, 1, 0};
-        total += L - decode_first_token(L, c->desc.window);
-    }
-    int rc;
-    if (c->meta_only)
-        return GQA_OK;
-    if ((rc = check_device(c)) != GQA_OK)
-        return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    if ((rc = upload_tables(c, st)) != GQA_OK)
-        return rc;
-    const PoolView pv = c->view();
     const int G = H_q / H_kv;
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b)
+        total += sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window);
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
+    int rc;
     if ((rc = decode_uses_tc(c, G)) < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
     if (rc == 1) {
@@ -1135,6 +1114,73 @@ int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, co
         rec(ev, st);
         return launch_attn_simt(pv, c->desc.dtype, (const SeqDesc *)(c->d_stage + o_sds), B, 1, H_q, q, out, st);
     });
+}
+
+int attn_decode(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q, void *out,
+                void *stream)
+{
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    if (!c->meta_only && (!q || !out))
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    std::vector<SeqDesc> sds(B);
+    for (int b = 0; b < B; ++b) {
+        const int32_t s = seq_ids[b];
+        if (!live(c, s))
+            return fail(GQA_EINVAL, "batch entry %d: sequence %d is not live", b, s);
+        const int32_t L = c->seqs[s].len;
+        if (L < 1)
+            return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
+        sds[b] = SeqDesc{s, L - 1, 1, 0};
+    }
+    int rc;
+    if (c->meta_only)
+        return GQA_OK;
+    if ((rc = check_device(c)) != GQA_OK)
+        return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((rc = upload_tables(c, st)) != GQA_OK)
+        return rc;
+    return decode_launch(c, c->view(), sds, H_q, q, out, st);
+}
+
+int attn_decode_tables(gqa_cache *c, int32_t B, const int32_t *block_table_dev, int32_t stride,
+                       const int32_t *lengths, int32_t H_q, const void *q, void *out, void *stream)
+{
+    if (!c || !lengths)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1 || stride < 1)
+        return fail(GQA_EINVAL, "B, H_q and stride must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    if (c->meta_only)
+        return fail(GQA_EINVAL, "attn_decode_tables needs a cache with a device pool");
+    if (!block_table_dev || !q || !out)
+        return fail(GQA_EINVAL, "NULL tensor pointer");
+    if (c->desc.rope == 1 && (int64_t)stride > c->desc.max_pages_per_seq)
+        return fail(GQA_ERANGE, "stride %d exceeds the rotary table's %d pages", stride, c->desc.max_pages_per_seq);
+    std::vector<SeqDesc> sds(B);
+    for (int b = 0; b < B; ++b) {
+        const int32_t L = lengths[b];
+        if (L < 1)
+            return fail(GQA_EMASK, "batch entry %d: length %d leaves the decode query without a visible key", b, L);
+        if ((int64_t)L > (int64_t)stride * kPageTokens)
+            return fail(GQA_ERANGE, "batch entry %d: length %d exceeds the table row's %d pages", b, L, stride);
+        sds[b] = SeqDesc{b, L - 1, 1, 0};
+    }
+    int rc = check_device(c);
+    if (rc != GQA_OK)
+        return rc;
+    PoolView pv = c->view();
+    pv.tables = block_table_dev;
+    pv.stride = stride;
+    return decode_launch(c, pv, sds, H_q, q, out, (cudaStream_t)stream);
 }
 
 int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q,

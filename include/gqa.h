@@ -300,6 +300,26 @@ int kv_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
 int attn_decode(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                 const void *q, void *out, void *stream);
 
+/* attn_decode_tables -- attn_decode over block tables the caller owns (the
+ * spec call attn_decode(q, cache, block_table, lengths)): the cache
+ * supplies the pool and its layout (dtype, window, rotation), the caller the
+ * page mapping and the lengths, and no sequence state of the cache is read
+ * or changed.  Query b sits at position lengths[b] - 1 and attends over
+ * tokens 0 .. lengths[b] - 1, token t in physical page
+ * block_table[b * stride + t / 16] at slot t % 16.
+ *  block_table  device int32 [B][stride], page ids of this cache's pool (-1
+ *               for pages a sliding window released; such pages are never
+ *               read).  Read on `stream`.
+ *  lengths      host int32[B], 1 <= lengths[b] <= stride * 16.
+ *  q, out       device [B, H_q, d_h].
+ * Page ids outside 0..num_pages-1 where a key is read are skipped and
+ * reported as GQA_DEVERR_PAGE_ID by gqa_cache_check.  The kernel is the one
+ * attn_decode would choose, with the same bits for the same tables.
+ * Errors: GQA_EINVAL, GQA_EMASK (a length < 1), GQA_ERANGE (a length beyond
+ * the row, or with rope = 1 a stride beyond max_pages_per_seq), GQA_ECUDA. */
+int attn_decode_tables(gqa_cache *cache, int32_t B, const int32_t *block_table_dev, int32_t stride,
+                       const int32_t *lengths, int32_t H_q, const void *q, void *out, void *stream);
+
 /* attn_decode_append -- one decode step: kv_append of one token per
  * sequence, then attn_decode at that token ([P3] decode: the step's own key
  * and value join the cache and the query attends to the old cache plus

@@ -88,3 +88,41 @@ def test_tensor_core_decode_repeated_sequences_and_steps():
         ref = oracle.decode(m, [mids[0], mids[1], mids[0]], q)
         assert_close(o, ref, "bf16", "step %d" % t)
     assert c.check() == 0
+
+
+@pytest.mark.parametrize("kernel", ["tensor_core", "cuda_core"])
+def test_decode_over_caller_block_tables(kernel):
+    # The caller's tables address the cache's pages directly: the cache's own
+    # rows give the same bits as attn_decode, and rows that reuse a
+    # sequence's first pages with a shorter length decode that prefix.
+    rng = np.random.default_rng(170)
+    H_q, H_kv, lengths = 32, 8, [3000, 129, 1700]
+    c, m, ids, mids = _filled(rng, H_q, H_kv, lengths)
+    c.set_decode_kernel(kernel)
+    stride = c.max_pages_per_seq
+    rows = []
+    for s in ids:
+        t = c.block_table(s)
+        rows.append(t + [-1] * (stride - len(t)))
+    q = workloads.normal_bf16(rng, (3, H_q, 128))
+    own = gqa.attn_decode(c, ids, dev(q, "bf16"))
+    tab = torch.tensor(rows, dtype=torch.int32, device="cuda")
+    ext = gqa.attn_decode_tables(c, tab, lengths, dev(q, "bf16"))
+    assert torch.equal(own.view(torch.int16), ext.view(torch.int16))
+    # Prefixes of sequence 0 at lengths 1000 and 17, and sequence 2 reversed in the batch.
+    tab2 = torch.tensor([rows[0], rows[0], rows[2]], dtype=torch.int32, device="cuda")
+    q2 = workloads.normal_bf16(rng, (3, H_q, 128))
+    o2 = host_f64(gqa.attn_decode_tables(c, tab2, [1000, 17, 1700], dev(q2, "bf16")), "bf16")
+    K0, V0 = m.kv(mids[0])
+    K2, V2 = m.kv(mids[2])
+    ref = np.stack([oracle.attention(oracle.to_f64(q2[0][None], "bf16"), K0[:1000], V0[:1000], [999])[0],
+                    oracle.attention(oracle.to_f64(q2[1][None], "bf16"), K0[:17], V0[:17], [16])[0],
+                    oracle.attention(oracle.to_f64(q2[2][None], "bf16"), K2, V2, [1699])[0]])
+    assert_close(o2, ref, "bf16", "caller tables")
+    assert c.check() == 0
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.attn_decode_tables(c, tab2, [1000, 0, 1700], dev(q2, "bf16"))
+    assert e.value.name == "EMASK"
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.attn_decode_tables(c, tab2, [1000, stride * 16 + 1, 1700], dev(q2, "bf16"))
+    assert e.value.name == "ERANGE"
