@@ -87,17 +87,24 @@ def traffic_for(workload, kernel, units_scale=1.0):
 
 
 class Dist:
-    def __init__(self):
+    """One process per GPU (RANK / LOCAL_RANK / WORLD_SIZE from the launcher);
+    replicas only: the ranks share nothing but a barrier around the timed
+    region and the max of their times.  `backend` is nccl on GPUs (gloo lets
+    the same logic run on CPU processes)."""
+
+    def __init__(self, backend="nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.backend = backend
         self.pg = None
 
     def setup(self, torch):
-        torch.cuda.set_device(self.local)
+        if self.backend == "nccl":
+            torch.cuda.set_device(self.local)
         if self.world > 1:
             import torch.distributed as dist
-            dist.init_process_group("nccl")
+            dist.init_process_group(self.backend)
             self.pg = dist
 
     def barrier(self):
@@ -107,7 +114,7 @@ class Dist:
     def max(self, torch, x):
         if not self.pg:
             return x
-        t = torch.tensor([float(x)], device="cuda")
+        t = torch.tensor([float(x)], device="cuda" if self.backend == "nccl" else "cpu")
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
