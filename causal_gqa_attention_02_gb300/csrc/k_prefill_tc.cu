@@ -55,6 +55,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "kernels.cuh"
 #include "sm100.cuh"
@@ -1133,18 +1134,23 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.counters = ws.counters;
     prm.slot_rows = ws.slot_rows;
     const int smem = (int)sizeof(TcSmem) + 1024;
-    static bool attr_set[6] = {false, false, false, false, false, false};
+    // The shared-memory opt-in is per device: remember it per device.
+    constexpr int kMaxDev = 64;
+    static std::atomic<bool> attr_set[kMaxDev][6];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return cudaErrorInvalidDevice;
     const int which = q8 ? 4 + (pv.window > 0 || ws.ranged ? 1 : 0)
                          : (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
     void (*const kern[6])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
         prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
         prefill_tc_kernel<false, true, false>,  prefill_tc_kernel<true, true, false>,
         prefill_tc_kernel<false, false, true>,  prefill_tc_kernel<false, true, true>};
-    if (!attr_set[which]) {
+    if (!attr_set[dev][which].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        attr_set[which] = true;
+        attr_set[dev][which].store(true, std::memory_order_release);
     }
     if (ev_start)
         cudaEventRecord(ev_start, st);       // after the host-side preparation above
