@@ -272,10 +272,10 @@ int check_device(const gqa_cache *c)
     return GQA_OK;
 }
 
-// Upload the block-table entries changed since the last upload.
-// One copy of the span of the flat table that covers every dirty entry
-// (rows are contiguous, and clean entries between equal the device's), so a
-// call pays one copy however many sequences it touched.
+// Upload the block-table entries changed since the last upload: one copy of
+// the span of the flat table that covers every dirty entry (rows are
+// contiguous, and clean entries in between equal the device's), so a call
+// pays one copy however many sequences it touched.
 int upload_tables(gqa_cache *c, cudaStream_t st)
 {
     size_t lo = SIZE_MAX, hi = 0;
