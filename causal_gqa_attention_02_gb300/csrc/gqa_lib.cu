@@ -858,8 +858,9 @@ int decode_uses_tc(const gqa_cache *c, int G)
         return ok ? 1 : -1;
     // Automatic: the tensor-core kernel for bf16.  A quantised cache decodes
     // faster on the CUDA-core kernel, which reads the codes directly; on the
-    // tensor-core kernel each tile's codes are first converted to bf16
-    // operands by the producer warps, whose conversion rate bounds decode.
+    // tensor-core kernel each stage's codes are converted in place to bf16
+    // operands before use, so a stage's next load waits for its landing,
+    // conversion and use, and the load latency is no longer hidden.
     return ok && c->desc.dtype == GQA_DTYPE_BF16 ? 1 : 0;
 }
 
