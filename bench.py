@@ -294,42 +294,17 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     gpu_launches = sum(nl for nl, _ in region_launches.values())
     kernels = {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl}
 
-    # End to end through the public API from pinned host buffers, pipelined
-    # over the batch entries, largest first (the last entry's compute and
-    # copy back are the part that does not overlap): entry b's valid rows go
-    # up on one copy stream,
-    # attn_prefill of entry b runs on the compute stream once they are in,
-    # and its valid output rows come back on a second copy stream while the
-    # next entry computes.  Only valid rows cross the link (padding rows of
-    # out are zeros by contract).  The step's events are on the compute
-    # stream, which waits for the last copy back.
+    # End to end through the public API from pinned host buffers: one
+    # attn_prefill_host call per step, which copies each entry's valid rows
+    # up, runs it, and copies its valid output rows back, largest entry
+    # first, the copies of one entry overlapping the others' attention (only
+    # valid rows cross the link).  The step's events are on the compute
+    # stream, which the call makes wait for the last copy back.
     qh, kh, vh = pinned(torch, q), pinned(torch, k), pinned(torch, v)
     oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    qd, kd, vd, od = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    main = torch.cuda.current_stream()
-    ev_in = [torch.cuda.Event() for _ in range(B)]
-    ev_out = [torch.cuda.Event() for _ in range(B)]
-
-    order = sorted(range(B), key=lambda x: -nb[x])
 
     def e2e_step():
-        up.wait_stream(main)
-        down.wait_stream(main)
-        with torch.cuda.stream(up):
-            for b in order:
-                qd[b, :nb[b]].copy_(qh[b, :nb[b]], non_blocking=True)
-                kd[b, :nb[b]].copy_(kh[b, :nb[b]], non_blocking=True)
-                vd[b, :nb[b]].copy_(vh[b, :nb[b]], non_blocking=True)
-                ev_in[b].record(up)
-        for b in order:
-            main.wait_event(ev_in[b])
-            gqa.attn_prefill(cache, [ids[b]], qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], [nb[b]], out=od[b:b + 1])
-            ev_out[b].record(main)
-            with torch.cuda.stream(down):
-                down.wait_event(ev_out[b])
-                oh[b, :nb[b]].copy_(od[b, :nb[b]], non_blocking=True)
-        main.wait_stream(down)
+        gqa.attn_prefill_host(cache, ids, qh, kh, vh, nb, out=oh)
         for s in ids:
             gqa.kv_truncate(cache, s, 0)
 
@@ -341,8 +316,9 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     e2e = {"value": round(flops * args.steps * dist.world / (e2e_total / 1e3) / 1e12, 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(sum(nb) * (row_q + 2 * row_kv)), "d2h_bytes_per_step": int(sum(nb) * row_q),
            "ms_per_step": round(e2e_total / args.steps, 4),
-           "how": "attn_prefill per batch entry on one stream, largest first; valid rows copied up/down on two "
-                  "copy streams, overlapping the other entries' compute"}
+           "how": "attn_prefill_host (C ABI, pinned host buffers): valid rows up on the library's upload stream, "
+                  "one-entry prefills largest first, valid output rows down on its download stream, overlapping "
+                  "the other entries' attention"}
     flags = cache.check()
     cache.close()
     del flush

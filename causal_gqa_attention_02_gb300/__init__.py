@@ -79,6 +79,7 @@ _sig("gqa_seq_block_table", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P)
 _sig("gqa_free_pages", ctypes.c_int, _vp, _I32P)
 _sig("gqa_page_refcount", ctypes.c_int, _vp, _i32, _I32P)
 _sig("attn_prefill", ctypes.c_int, _vp, _i32, _I32P, _i32, _i32, _vp, _vp, _vp, _I32P, _I32P, _vp, _vp)
+_sig("attn_prefill_host", ctypes.c_int, _vp, _i32, _I32P, _i32, _i32, _vp, _vp, _vp, _I32P, _I32P, _vp, _vp)
 _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
@@ -323,6 +324,48 @@ def attn_prefill(cache: Cache, seq_ids, q, k, v, valid_lengths, positions=None, 
     return out
 
 
+def _host_ptr(t, what, dtype, shape):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host (CPU) tensor" % what)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (what, tuple(t.shape), tuple(shape)))
+    return t.data_ptr()
+
+
+def attn_prefill_host(cache: Cache, seq_ids, q, k, v, valid_lengths, positions=None, out=None, stream=None):
+    """attn_prefill on host tensors (see include/gqa.h): q [B, n, H_q, d],
+    k/v [B, n, H_kv, d] on the CPU, pinned for overlapped copies; returns
+    out [B, n, H_q, d] on the CPU (allocated pinned like q if not given).
+    Only valid rows of out are written.  The result is complete once
+    `stream` (default: the current stream) is synchronised."""
+    B, n, H_q = len(seq_ids), q.shape[1], q.shape[2]
+    dt, d, H_kv = cache.torch_dtype, cache.head_dim, cache.num_kv_heads
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    keep_s, sp = _i32_array(seq_ids)
+    keep_v, vp = _i32_array(valid_lengths)
+    keep_p, pp = _i32_array(positions)
+    _check(_lib.attn_prefill_host(cache.handle, B, sp, n, H_q,
+                                  _host_ptr(q, "q", dt, (B, n, H_q, d)),
+                                  _host_ptr(k, "k", dt, (B, n, H_kv, d)),
+                                  _host_ptr(v, "v", dt, (B, n, H_kv, d)),
+                                  vp, pp, _host_ptr(out, "out", dt, (B, n, H_q, d)),
+                                  _stream_handle(stream, cache.device_index)))
+    return out
+
+
+def attn_prefill_host_meta(cache: Cache, seq_ids, n, H_q, valid_lengths, positions=None):
+    """attn_prefill_host on a metadata-only cache (no buffers)."""
+    keep_s, sp = _i32_array(seq_ids)
+    keep_v, vp = _i32_array(valid_lengths)
+    keep_p, pp = _i32_array(positions)
+    _check(_lib.attn_prefill_host(cache.handle, len(seq_ids), sp, n, H_q, None, None, None, vp, pp, None, None))
+
+
 def attn_prefill_meta(cache: Cache, seq_ids, n, H_q, valid_lengths, positions=None):
     """attn_prefill on a metadata-only cache (no tensors)."""
     keep_s, sp = _i32_array(seq_ids)
@@ -436,4 +479,4 @@ def exported_symbols():
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
             "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel",
-            "attn_decode_append", "gqa_selftest_bounded_wait", "attn_decode_tables"]
+            "attn_decode_append", "gqa_selftest_bounded_wait", "attn_decode_tables", "attn_prefill_host"]

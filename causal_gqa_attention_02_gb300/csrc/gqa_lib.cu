@@ -96,6 +96,12 @@ struct gqa_cache {
     int32_t *d_cnt = nullptr;            // decode merge counters [B * H_kv], kept at zero
     size_t cnt_cap = 0;
     float2 *d_rope = nullptr;            // rope = 1: (cos, sin) [max positions][d_h / 2]
+    // attn_prefill_host: packed device copies of a call's valid q, k, v and
+    // out rows, an upload and a download stream, and per-entry events.
+    char *d_io = nullptr;
+    size_t io_cap = 0;
+    cudaStream_t io_up = nullptr, io_down = nullptr;
+    std::vector<cudaEvent_t> io_events;
     std::vector<char> h_stage;
     int device = -1;
     int num_sms = 0;
@@ -577,6 +583,11 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_ws) cudaFree(c->d_ws);
         if (c->d_cnt) cudaFree(c->d_cnt);
         if (c->d_rope) cudaFree(c->d_rope);
+        if (c->d_io) cudaFree(c->d_io);
+        if (c->io_up) cudaStreamDestroy(c->io_up);
+        if (c->io_down) cudaStreamDestroy(c->io_down);
+        for (cudaEvent_t ev : c->io_events)
+            cudaEventDestroy(ev);
         for (const auto &r : c->prof_recs) {
             cudaEventDestroy(r.start);
             cudaEventDestroy(r.end);
@@ -868,9 +879,11 @@ int decode_uses_tc(const gqa_cache *c, int G)
 // The hot path.
 // ---------------------------------------------------------------------------
 
-static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
-                 const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions,
-                 void *out, void *stream)
+// Every precondition of a prefill call, checked before anything changes
+// (req: one write request per entry; max_nb: the longest valid length).
+static int validate_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, bool have_io,
+                            const int32_t *valid_lengths, const int32_t *positions, std::vector<WriteReq> &req,
+                            int32_t &max_nb)
 {
     if (!c || !seq_ids || !valid_lengths)
         return fail(GQA_EINVAL, "NULL argument");
@@ -878,10 +891,10 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         return fail(GQA_EINVAL, "B, n and H_q must be >= 1");
     if (H_q % c->desc.num_kv_heads != 0)
         return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", c->desc.num_kv_heads, H_q);
-    if (!c->meta_only && (!q || !k || !v || !out))
+    if (!c->meta_only && !have_io)
         return fail(GQA_EINVAL, "NULL tensor pointer");
-    std::vector<WriteReq> req(B);
-    int32_t max_nb = 0;
+    req.assign(B, WriteReq{});
+    max_nb = 0;
     for (int b = 0; b < B; ++b) {
         const int32_t nb = valid_lengths[b];
         if (nb < 1 || nb > n)
@@ -903,6 +916,18 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         }
     }
     if (!c->meta_only && (rc = check_device(c)) != GQA_OK)
+        return rc;
+    return GQA_OK;
+}
+
+static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
+                 const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions,
+                 void *out, void *stream)
+{
+    std::vector<WriteReq> req;
+    int32_t max_nb = 0;
+    int rc = validate_prefill(c, B, seq_ids, n, H_q, q && k && v && out, valid_lengths, positions, req, max_nb);
+    if (rc != GQA_OK)
         return rc;
 
     std::vector<SeqDesc> sds;
@@ -1020,6 +1045,119 @@ int attn_prefill(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int
     if (rc == GQA_OK)
         release_windows(c, B, seq_ids);
     return rc;
+}
+
+// The packed device rows, copy streams and events of attn_prefill_host,
+// grown on demand (a growth frees the old rows, which waits for the device).
+static int ensure_io(gqa_cache *c, size_t bytes, size_t events)
+{
+    cudaError_t e = cudaSuccess;
+    if (bytes > c->io_cap) {
+        if (c->d_io) {
+            e = cudaFree(c->d_io);
+            c->d_io = nullptr;
+            c->io_cap = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaFree(host-call rows)");
+        }
+        const size_t cap = (bytes + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+        if ((e = cudaMalloc((void **)&c->d_io, cap)) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(host-call rows)");
+        c->io_cap = cap;
+    }
+    if (!c->io_up && (e = cudaStreamCreateWithFlags(&c->io_up, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "upload stream");
+    if (!c->io_down && (e = cudaStreamCreateWithFlags(&c->io_down, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "download stream");
+    while (c->io_events.size() < events) {
+        cudaEvent_t ev;
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "event");
+        c->io_events.push_back(ev);
+    }
+    return GQA_OK;
+}
+
+int attn_prefill_host(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q, const void *q,
+                      const void *k, const void *v, const int32_t *valid_lengths, const int32_t *positions,
+                      void *out, void *stream)
+{
+    // The whole batch is checked first, so a rejected call queues and
+    // changes nothing; each entry then runs as a one-entry prefill whose
+    // checks repeat what was checked here.
+    std::vector<WriteReq> req;
+    int32_t max_nb = 0;
+    int rc = validate_prefill(c, B, seq_ids, n, H_q, q && k && v && out, valid_lengths, positions, req, max_nb);
+    if (rc != GQA_OK)
+        return rc;
+    // Largest entries first: the last entry's prefill and download are the
+    // part of the call that nothing overlaps.
+    std::vector<int> order(B);
+    for (int b = 0; b < B; ++b)
+        order[b] = b;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return valid_lengths[x] > valid_lengths[y]; });
+    if (c->meta_only) {
+        for (int b : order) {
+            if ((rc = attn_prefill_impl(c, 1, seq_ids + b, valid_lengths[b], H_q, nullptr, nullptr, nullptr,
+                                        valid_lengths + b, positions ? positions + (size_t)b * n : nullptr, nullptr,
+                                        nullptr)) != GQA_OK)
+                return rc;
+            release_windows(c, 1, seq_ids + b);
+        }
+        return GQA_OK;
+    }
+    const size_t d = (size_t)c->desc.head_dim, es = (size_t)c->io_esize;
+    const size_t row_q = (size_t)H_q * d * es, row_kv = (size_t)c->desc.num_kv_heads * d * es;
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    std::vector<size_t> off(B);                      // entry b's packed q, k, v, out rows, in call order
+    size_t bytes = 0;
+    for (int b : order) {
+        off[b] = bytes;
+        bytes += al((size_t)valid_lengths[b] * row_q) * 2 + al((size_t)valid_lengths[b] * row_kv) * 2;
+    }
+    if ((rc = ensure_io(c, bytes, 2 * (size_t)B + 2)) != GQA_OK)
+        return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaEvent_t *ev = c->io_events.data();            // [0] call start, [1] downloads done, then in/out per entry
+    cudaError_t e = cudaEventRecord(ev[0], st);      // the previous call's users of the rows are done
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(c->io_up, ev[0], 0);
+    for (int i = 0; e == cudaSuccess && i < B; ++i) {
+        const int b = order[i];
+        const size_t nb = (size_t)valid_lengths[b];
+        char *base = c->d_io + off[b];
+        const char *qh = (const char *)q + (size_t)b * n * row_q, *kh = (const char *)k + (size_t)b * n * row_kv,
+                   *vh = (const char *)v + (size_t)b * n * row_kv;
+        if ((e = cudaMemcpyAsync(base, qh, nb * row_q, cudaMemcpyHostToDevice, c->io_up)) == cudaSuccess &&
+            (e = cudaMemcpyAsync(base + al(nb * row_q), kh, nb * row_kv, cudaMemcpyHostToDevice, c->io_up)) ==
+                cudaSuccess &&
+            (e = cudaMemcpyAsync(base + al(nb * row_q) + al(nb * row_kv), vh, nb * row_kv, cudaMemcpyHostToDevice,
+                                 c->io_up)) == cudaSuccess)
+            e = cudaEventRecord(ev[2 + 2 * i], c->io_up);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "host-call upload");
+    for (int i = 0; i < B; ++i) {
+        const int b = order[i];
+        const size_t nb = (size_t)valid_lengths[b];
+        char *dq = c->d_io + off[b], *dk = dq + al(nb * row_q), *dv = dk + al(nb * row_kv),
+             *dout = dv + al(nb * row_kv);
+        if ((e = cudaStreamWaitEvent(st, ev[2 + 2 * i], 0)) != cudaSuccess)
+            return cuda_fail(e, "host-call wait for upload");
+        if ((rc = attn_prefill_impl(c, 1, seq_ids + b, (int32_t)nb, H_q, dq, dk, dv, valid_lengths + b,
+                                    positions ? positions + (size_t)b * n : nullptr, dout, st)) != GQA_OK)
+            return rc;
+        release_windows(c, 1, seq_ids + b);
+        if ((e = cudaEventRecord(ev[3 + 2 * i], st)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(c->io_down, ev[3 + 2 * i], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync((char *)out + (size_t)b * n * row_q, dout, nb * row_q, cudaMemcpyDeviceToHost,
+                                 c->io_down)) != cudaSuccess)
+            return cuda_fail(e, "host-call download");
+    }
+    if ((e = cudaEventRecord(ev[1], c->io_down)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, ev[1], 0)) != cudaSuccess)
+        return cuda_fail(e, "host-call completion");
+    return GQA_OK;
 }
 
 int kv_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n, const int32_t *counts,

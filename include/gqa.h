@@ -272,6 +272,36 @@ int attn_prefill(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n,
                  const int32_t *valid_lengths, const int32_t *positions,
                  void *out, void *stream);
 
+/* attn_prefill on HOST buffers: the same computation and cache effects,
+ * with the host<->device transfers inside the call.
+ *
+ * The whole batch is checked first (every error of attn_prefill; nothing is
+ * queued or changed when a check fails).  Then, largest n_b first, entry b's
+ * valid rows of q, k, v (n_b of its n rows each) are copied to library-owned
+ * device memory on the cache's upload stream, the entry runs as a one-entry
+ * attn_prefill on `stream` once its rows are in, and its n_b valid output
+ * rows are copied back on the cache's download stream while later entries
+ * compute.  `stream` waits for the last download before the call's work
+ * ends, so `out` is complete once `stream` is synchronised.
+ *
+ * Arguments as attn_prefill, except:
+ *  q              host [B, n, H_q, d_h]   (read when the call's work runs)
+ *  k, v           host [B, n, H_kv, d_h]  (read when the call's work runs)
+ *  out            host [B, n, H_q, d_h]   (written); rows i >= n_b of an
+ *                 entry are NOT written (only valid rows cross the link)
+ * The host buffers must stay valid until `stream` has passed the call.
+ * Page-locked (pinned) buffers let the copies overlap the attention of other
+ * entries; pageable ones work, with copies the driver may serialise.
+ * Calls on one cache must be ordered on one stream (the device copies of
+ * the rows are reused by the next call).  The device memory for the rows
+ * grows on demand (a growth frees the old block, which waits for the device).
+ * Errors: those of attn_prefill; a GQA_ECUDA after some entries were queued
+ * leaves those entries written (as a sequence of one-entry calls would). */
+int attn_prefill_host(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t n, int32_t H_q,
+                      const void *q, const void *k, const void *v,
+                      const int32_t *valid_lengths, const int32_t *positions,
+                      void *out, void *stream);
+
 /* Append new K/V rows at each sequence's tail without attention ([P3]
  * decode: append the step's k_t, v_t after the old cache; [P1] 2.6 cache
  * write).  Row c < counts[b] of entry b goes to position P_b + c (with

@@ -2,6 +2,7 @@
 header declares, and its host-side logic (validation, allocator, reference
 counts, copy-on-write planning, truncation) agrees with the oracle's cache
 model.  Metadata-only caches need no GPU and queue no device work."""
+import copy
 import ctypes
 import os
 import re
@@ -142,7 +143,9 @@ def test_allocator_matches_oracle_model_under_random_operations(window):
         assert released_seen and refusals > 0
 
 
-def test_prefill_rejections_change_nothing():
+@pytest.mark.parametrize("call", ["attn_prefill_meta", "attn_prefill_host_meta"])
+def test_prefill_rejections_change_nothing(call):
+    prefill = getattr(gqa, call)
     lib, model = _pair(pages=7, per_seq=4)
     a, b = lib.seq_create(), lib.seq_create()
     gqa.attn_prefill_meta(lib, [a], 20, 4, [20])
@@ -160,12 +163,49 @@ def test_prefill_rejections_change_nothing():
     ]
     for kw, want in cases:
         with pytest.raises(gqa.GqaError) as e:
-            gqa.attn_prefill_meta(lib, **kw)
+            prefill(lib, **kw)
         assert e.value.name == want, (kw, e.value)
         assert (lib.block_table(a), lib.seq_length(a), lib.free_pages()) == before
     # Correct positions are accepted.
-    gqa.attn_prefill_meta(lib, [a], 4, 4, [3], positions=np.array([[20, 21, 22, 999]], dtype=np.int32))
+    prefill(lib, [a], 4, 4, [3], positions=np.array([[20, 21, 22, 999]], dtype=np.int32))
     assert lib.seq_length(a) == 23
+
+
+@pytest.mark.parametrize("window", [0, 48])
+def test_host_buffer_prefill_bookkeeping(window):
+    # attn_prefill_host checks the whole batch like attn_prefill, then runs
+    # its entries as one-entry prefills, longest first (ties in batch order):
+    # pages, tables and refusals must match the model doing exactly that.
+    rng = np.random.default_rng(11 + window)
+    lib, model = _pair(pages=30, seqs=6, per_seq=12, order=rng.permutation(30), window=window)
+    ids = [lib.seq_create() for _ in range(5)]
+    assert ids == [model.create() for _ in range(5)]
+    refusals = 0
+    for step in range(150):
+        batch = [int(x) for x in rng.choice(ids, size=int(rng.integers(1, 4)), replace=False)]
+        n = int(rng.integers(1, 40))
+        nb = [int(rng.integers(1, n + 1)) for _ in batch]
+        err_m = err_l = None
+        try:
+            copy.deepcopy(model).write(batch, [_rows(x) for x in nb], [_rows(x) for x in nb])
+        except oracle.CacheError as e:
+            err_m = e.kind
+        if err_m is None:
+            for i in sorted(range(len(batch)), key=lambda i: -nb[i]):
+                model.write([batch[i]], [_rows(nb[i])], [_rows(nb[i])])
+        try:
+            gqa.attn_prefill_host_meta(lib, batch, n, 4, nb)
+        except gqa.GqaError as e:
+            err_l = e.name
+        assert err_m == err_l
+        refusals += err_m is not None
+        _same_state(lib, model)
+        if rng.random() < 0.15:
+            s = int(rng.choice(ids))
+            gqa.kv_truncate(lib, s, 0)
+            model.truncate(s, 0)
+            _same_state(lib, model)
+    assert refusals > 0
 
 
 def test_decode_rejects_an_empty_sequence():
