@@ -758,6 +758,7 @@ struct TcPlan {
     int32_t slots = 0;                // split workspace slots
     int32_t slot_rows = 0;
     bool ranged = false;              // an item starts past key tile 0
+    std::vector<int64_t> load;        // per CTA: cost of its items (quarter key tiles)
 };
 
 // Items: two query tiles of 128 / G positions of one (entry, KV head) each;
@@ -826,6 +827,11 @@ void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan 
         top.first += cost(all[i]);
         heap.push(top);
     }
+    pl.load.assign(pl.grid, 0);
+    while (!heap.empty()) {
+        pl.load[heap.top().second] = heap.top().first;
+        heap.pop();
+    }
     pl.items.clear();
     pl.items.reserve(all.size());
     pl.item_start.assign(1, 0);
@@ -836,6 +842,40 @@ void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan 
         }
         pl.item_start.push_back((int32_t)pl.items.size());
     }
+}
+
+// Fused prefill: the padding rows of out that no item stores (`units`
+// 16-byte units in all) are cleared by the CTAs after their items, the
+// least-loaded CTAs taking the most (water-filling their loads up to a
+// common level, about 16 KB per quarter key tile of spare time).  Returns
+// grid + 1 offsets into the units.
+std::vector<int64_t> zero_shares(const TcPlan &pl, int64_t units)
+{
+    constexpr double kUnitsPerQuarter = 1024.0;
+    const int g = pl.grid;
+    std::vector<int64_t> start(g + 1, 0);
+    if (units <= 0 || g < 1)
+        return start;
+    std::vector<int64_t> L = pl.load;
+    std::sort(L.begin(), L.end());
+    const double need = (double)units / kUnitsPerQuarter;
+    double level = (double)L[g - 1], below = 0.0;
+    for (int k = 1; k <= g; ++k) {
+        below += (double)L[k - 1];                    // sum of the k smallest loads
+        const double t = (need + below) / k;          // level filling exactly the k smallest
+        if (k == g || t <= (double)L[k]) {
+            level = t;
+            break;
+        }
+    }
+    int64_t given = 0;
+    for (int c = 0; c < g; ++c) {
+        const int64_t share = (int64_t)std::max(0.0, (level - (double)pl.load[c]) * kUnitsPerQuarter);
+        start[c + 1] = start[c] + std::min(share, units - given);
+        given = start[c + 1];
+    }
+    start[g] = units;                                 // rounding: the last CTA takes the rest
+    return start;
 }
 
 // Split workspace of a plan in the cache's growable buffers.
@@ -946,11 +986,39 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     TcPlan plan;
     if (use_tc)
         plan_tc(c, sds, G, plan);
+    // Fused cache write: the tensor-core kernel reads this call's rows from
+    // k and v and writes their pages itself when every entry starts on a
+    // page boundary (each page then holds old rows only or new rows only;
+    // no copy-on-write), for a bf16 cache without rotation; k and v are
+    // read as groups of 8 rows, so n must be a multiple of 8.
+    bool fused = use_tc && c->desc.dtype == GQA_DTYPE_BF16 && c->desc.rope == 0 && cows.empty() && n % 8 == 0 &&
+                 ((uintptr_t)k | (uintptr_t)v) % 16 == 0;
+    for (int b = 0; fused && b < B; ++b)
+        fused = sds[b].past % kPageTokens == 0;
+    if (fused) {
+        // Rows an item's epilogue stores: its query tiles' rows (a split
+        // item's merge stores the valid rows only); out rows from zero_from
+        // on are zeroed by the kernel.
+        const int rows_pos = prefill_tc_rows_per_tile(G);
+        std::vector<int32_t> cover(B, 0);
+        for (const TcItem &it : plan.items)
+            cover[it.b] = std::max(cover[it.b], it.part >= 0 ? sds[it.b].count : it.i0 + it.tiles * rows_pos);
+        for (int b = 0; b < B; ++b)
+            sds[b].zero_from = std::min(n, cover[b]);
+    }
+    std::vector<int64_t> zstart;
+    if (fused) {
+        int64_t units = 0;
+        for (int b = 0; b < B; ++b)
+            units += (int64_t)(n - sds[b].zero_from) * H_q * (c->desc.head_dim * c->io_esize / 16);
+        zstart = zero_shares(plan, units);
+    }
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
     const size_t o_cow = stg.add(cows.data(), cows.size());
     const size_t o_items = stg.add(plan.items.data(), plan.items.size());
     const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
+    const size_t o_zero = stg.add(zstart.data(), zstart.size());
     TcSplitWs ws;
     if (use_tc && (rc = tc_workspace(c, plan, ws)) != GQA_OK)
         return rc;
@@ -964,20 +1032,22 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
              return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
          })) != GQA_OK)
         return rc;
-    // On the tensor-core path the write kernel also zeroes the padding rows
-    // of out (discarded rows are written as zeros); the prefill kernel then
-    // writes the valid rows only.
+    // Unfused, on the tensor-core path the write kernel also zeroes the
+    // padding rows of out (discarded rows are written as zeros); the
+    // prefill kernel then writes the valid rows only.
     const int out_row_bytes = H_q * c->desc.head_dim * c->io_esize;
-    if ((rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&](cudaEvent_t ev) {
-             rec(ev, st);
-             return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st, use_tc ? out : nullptr,
-                                       out_row_bytes);
-         })) != GQA_OK)
+    if (!fused && (rc = run_kernel(c, GQA_KERNEL_CACHE_WRITE, st, "cache write kernel", [&](cudaEvent_t ev) {
+                       rec(ev, st);
+                       return launch_cache_write(pv, c->esize, d_sds, B, n, max_nb, k, v, st, use_tc ? out : nullptr,
+                                                 out_row_bytes);
+                   })) != GQA_OK)
         return rc;
     if (use_tc) {
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&](cudaEvent_t ev) {
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items),
-                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, n, H_q, q, out, ws, st, ev);
+                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, n, H_q, q, out, ws, st, ev,
+                                     nullptr, nullptr, fused ? k : nullptr, fused ? v : nullptr,
+                                     fused ? (const int64_t *)(c->d_stage + o_zero) : nullptr);
         });
     }
     return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&](cudaEvent_t ev) {
@@ -1109,11 +1179,15 @@ int attn_prefill_host(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n
     const size_t d = (size_t)c->desc.head_dim, es = (size_t)c->io_esize;
     const size_t row_q = (size_t)H_q * d * es, row_kv = (size_t)c->desc.num_kv_heads * d * es;
     auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    // Each entry's packed rows are padded to a multiple of 8 (the one-entry
+    // prefill runs with n = that, so the tensor-core kernel can read its k
+    // and v rows in groups of 8; the padding rows are never valid).
+    auto rows8 = [&](int b) { return ((size_t)valid_lengths[b] + 7) & ~(size_t)7; };
     std::vector<size_t> off(B);                      // entry b's packed q, k, v, out rows, in call order
     size_t bytes = 0;
     for (int b : order) {
         off[b] = bytes;
-        bytes += al((size_t)valid_lengths[b] * row_q) * 2 + al((size_t)valid_lengths[b] * row_kv) * 2;
+        bytes += al(rows8(b) * row_q) * 2 + al(rows8(b) * row_kv) * 2;
     }
     if ((rc = ensure_io(c, bytes, 2 * (size_t)B + 2)) != GQA_OK)
         return rc;
@@ -1124,14 +1198,14 @@ int attn_prefill_host(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n
         e = cudaStreamWaitEvent(c->io_up, ev[0], 0);
     for (int i = 0; e == cudaSuccess && i < B; ++i) {
         const int b = order[i];
-        const size_t nb = (size_t)valid_lengths[b];
+        const size_t nb = (size_t)valid_lengths[b], n8 = rows8(b);
         char *base = c->d_io + off[b];
         const char *qh = (const char *)q + (size_t)b * n * row_q, *kh = (const char *)k + (size_t)b * n * row_kv,
                    *vh = (const char *)v + (size_t)b * n * row_kv;
         if ((e = cudaMemcpyAsync(base, qh, nb * row_q, cudaMemcpyHostToDevice, c->io_up)) == cudaSuccess &&
-            (e = cudaMemcpyAsync(base + al(nb * row_q), kh, nb * row_kv, cudaMemcpyHostToDevice, c->io_up)) ==
+            (e = cudaMemcpyAsync(base + al(n8 * row_q), kh, nb * row_kv, cudaMemcpyHostToDevice, c->io_up)) ==
                 cudaSuccess &&
-            (e = cudaMemcpyAsync(base + al(nb * row_q) + al(nb * row_kv), vh, nb * row_kv, cudaMemcpyHostToDevice,
+            (e = cudaMemcpyAsync(base + al(n8 * row_q) + al(n8 * row_kv), vh, nb * row_kv, cudaMemcpyHostToDevice,
                                  c->io_up)) == cudaSuccess)
             e = cudaEventRecord(ev[2 + 2 * i], c->io_up);
     }
@@ -1139,12 +1213,12 @@ int attn_prefill_host(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t n
         return cuda_fail(e, "host-call upload");
     for (int i = 0; i < B; ++i) {
         const int b = order[i];
-        const size_t nb = (size_t)valid_lengths[b];
-        char *dq = c->d_io + off[b], *dk = dq + al(nb * row_q), *dv = dk + al(nb * row_kv),
-             *dout = dv + al(nb * row_kv);
+        const size_t nb = (size_t)valid_lengths[b], n8 = rows8(b);
+        char *dq = c->d_io + off[b], *dk = dq + al(n8 * row_q), *dv = dk + al(n8 * row_kv),
+             *dout = dv + al(n8 * row_kv);
         if ((e = cudaStreamWaitEvent(st, ev[2 + 2 * i], 0)) != cudaSuccess)
             return cuda_fail(e, "host-call wait for upload");
-        if ((rc = attn_prefill_impl(c, 1, seq_ids + b, (int32_t)nb, H_q, dq, dk, dv, valid_lengths + b,
+        if ((rc = attn_prefill_impl(c, 1, seq_ids + b, (int32_t)n8, H_q, dq, dk, dv, valid_lengths + b,
                                     positions ? positions + (size_t)b * n : nullptr, dout, st)) != GQA_OK)
             return rc;
         release_windows(c, 1, seq_ids + b);

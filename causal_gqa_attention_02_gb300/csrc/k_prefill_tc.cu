@@ -5,12 +5,15 @@
 // What it computes ("第二章 Prefill：整层状态演化与 KV 建立", section 2.3):
 // for query head h of KV group g = floor(h*H_kv/H_q) and a query row at
 // absolute position p, the softmax over the finite scores
-// <q, k_j>/sqrt(d_h), j = 0..p, applied to V.  Keys come from the paged
-// cache through the block table ("KV Cache 与 Prefill/Decode 推理路径",
-// PagedAttention): the cache write kernel has already stored this call's new
-// rows, so a prefill over an existing prefix (incremental prefill: the old
-// prefix fully visible, the new block lower-triangular) and a fresh prefill
-// are the same loop.
+// <q, k_j>/sqrt(d_h), j = 0..p, applied to V.  Keys before this call's
+// rows come from the paged cache through the block table ("KV Cache 与
+// Prefill/Decode 推理路径", PagedAttention), so a prefill over an existing
+// prefix (incremental prefill: the old prefix fully visible, the new block
+// lower-triangular) and a fresh prefill are the same loop.  This call's own
+// rows either were stored by a cache-write launch before this kernel, or
+// (fused write, section 2.6's write-then-attend done in one kernel) are read
+// from the call's k and v and each new page is stored to the pool by the
+// one CTA whose query rows begin on it.
 //
 // Mapping to the hardware.
 //  * A CTA owns two 128-row query tiles of one (batch entry, KV head).  A
@@ -46,7 +49,8 @@
 //  * Epilogue: O / l in fp32 -> bf16, staged per 64-column half in a 16 KB
 //    shared-memory buffer per query tile (128-byte swizzle, so the row-per-
 //    thread writes are conflict-free) and written by one TMA store per half;
-//    padding rows of the tile are written as zeros.
+//    padding rows of the tile are written as zeros (with the fused write,
+//    padding rows no tile covers are cleared by the producer warps).
 // Every wait is bounded; on a timeout the CTA raises GQA_DEVERR_TIMEOUT,
 // drains what it has in flight (bounded) and exits cleanly.
 #include <cuda.h>
@@ -112,6 +116,7 @@ struct __align__(1024) TcSmem {
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t k_land[kKStages], v_land[kVStages];       // Q8: a stage's codes have landed
     uint64_t s_full[2], s_free, p_full[2], pv_done[2], fin[2];
+    uint64_t fix_bar[2];                               // fused write: a K (V) tile that needs its tail cleared landed
     uint32_t tmem;
     int abort_;
     int last_;                                         // this CTA completed a split group
@@ -146,6 +151,9 @@ struct TcParams {
     const __nv_bfloat16 *app_k;   // fused append: this call's one new K and V row per entry
     const __nv_bfloat16 *app_v;   // ([B, H_kv, 128]), written at position past; null = none
     const float *scales;          // Q8: per-row scales of the FP8 E4M3 pool (block * 16 + slot)
+    int32_t fused;                // 1: rows of this call are read from k / v and written to their pages here
+    int32_t B;
+    const int64_t *zero_start;    // fused: CTA c clears padding units zero_start[c] .. zero_start[c + 1] - 1
 };
 
 // Two FP8 E4M3 codes (low byte first) dequantised with their row's scale:
@@ -177,7 +185,9 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 template <bool ROPE, bool WIN, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
-                  const __grid_constant__ CUtensorMap mO, const TcParams p)
+                  const __grid_constant__ CUtensorMap mO, const __grid_constant__ CUtensorMap mKt,
+                  const __grid_constant__ CUtensorMap mVt, const __grid_constant__ CUtensorMap mKp,
+                  const __grid_constant__ CUtensorMap mVp, const TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem &s = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,6 +234,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         mbar_init(&s.s_free, 4);
         mbar_init(&s.fin[0], 1);
         mbar_init(&s.fin[1], 1);
+        mbar_init(&s.fix_bar[0], 1);
+        mbar_init(&s.fix_bar[1], 1);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -244,6 +256,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (!vside)
                 prefetch_tmap(&mQ);
             prefetch_tmap(&mKV);
+            if (p.fused) {
+                prefetch_tmap(vside ? &mVt : &mKt);
+                prefetch_tmap(vside ? &mVp : &mKp);
+            }
         }
         const int stages = vside ? kVStages : kKStages;
         const uint32_t q_bytes = 2u * 2u * (uint32_t)(p.G * p.rows_pos) * 64u * 2u;
@@ -361,15 +377,77 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 mbar_arrive(vside ? &s.v_full[st] : &s.k_full[st]);
             return true;
         };
+        // Fused calls: the padding rows of out that no item stores (rows
+        // zero_from .. n-1 of each entry, all heads) are cleared by the two
+        // producer warps once their loads are issued; the host gives the
+        // least-loaded CTAs the largest shares.
+        const int64_t row_units = (int64_t)p.H_q * (D * 2 / 16);   // 16-byte units of one output row
+        int64_t z_next = 0, z_end = 0, zb_start = 0, zb_end = 0;
+        int zb = -1;
+        uint4 *zb_base = nullptr;                         // out row zero_from of entry zb
+        if (p.fused) {
+            const int64_t c0 = p.zero_start[blockIdx.x], c1 = p.zero_start[blockIdx.x + 1];
+            const int64_t mid = c0 + (c1 - c0) / 2;
+            z_next = vside ? mid : c0;
+            z_end = vside ? c1 : mid;
+        }
+        auto zero_some = [&](int64_t units) {
+            const int64_t stop = min(z_end, z_next + units);
+            for (int64_t u = z_next + lane; u < stop; u += 32) {
+                // Each lane's units increase: the entry changes rarely.
+                while (u >= zb_end) {
+                    ++zb;
+                    zb_start = zb_end;
+                    zb_end = zb_start + (int64_t)(p.n - p.seqs[zb].zero_from) * row_units;
+                    zb_base = reinterpret_cast<uint4 *>(p.out) +
+                              ((size_t)zb * p.n + p.seqs[zb].zero_from) * (size_t)row_units;
+                }
+                zb_base[u - zb_start] = make_uint4(0, 0, 0, 0);
+            }
+            z_next = stop;
+        };
+        // Fused write (p.fused; every entry's past is a multiple of 16, so
+        // each page holds old rows only or this call's rows only).  Pages at
+        // positions >= past are read from this call's k / v, not from the
+        // pool: a tile wholly past `past` as one 32 KB box (mKt / mVt), a
+        // tile that straddles it page by page (mKp / mVp for the new pages).
+        // Both maps view k / v [B, n, H_kv, 128] as [H_kv][8-row group]
+        // [column half][8 rows][64], so a box lands in exactly the layout a
+        // page box from the pool lands in.  Rows past the entry's valid
+        // length (padding, or the next entry's rows) are cleared in shared
+        // memory after landing, before the stage is marked full.  The item
+        // whose query rows include a new page's first position owns that
+        // page: once the tile has landed (checked when its stage is next
+        // refilled) lane pg stores page block pg to the pool with one TMA
+        // store, so every new page is written exactly once and no CTA reads
+        // a page this launch writes.
+        int own_blk[2] = {-1, -1};                        // per stage: pool block this lane stores, or -1
+        bool stores_out = false;                          // this lane has bulk stores in flight
+        uint32_t fix_uses = 0;
+        auto flush_stores = [&](int st, uint32_t parity) -> bool {
+            uint64_t *full = vside ? &s.v_full[st] : &s.k_full[st];
+            if (!__any_sync(0xffffffffu, own_blk[st] >= 0))
+                return true;
+            if (!wait0(full, parity))                     // the tile has landed (and been fixed up)
+                return false;
+            if (own_blk[st] >= 0) {
+                const __nv_bfloat16 *src = (vside ? s.v[st][0] : s.k[st][0]) + my_pg * kPageElems;
+                tma_store_3d(&mKV, src, 0, 0, own_blk[st]);
+                tma_store_commit();
+                stores_out = true;
+            }
+            own_blk[st] = -1;
+            return true;
+        };
         // Loads this warp's half (K or V) of key tile j of an item into
         // stage gt % stages once its last readers are done.
         auto load_tile = [&](const TcItem &it, const SeqDesc &sd, int j) -> bool {
             const int st = gt % stages;
             const uint32_t use = gt / stages;
             int ph = p.num_pages;                         // out of range: the box reads zeros
+            const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
             if (boxer) {
                 const int lp = 8 * j + my_pg;
-                const int seq_pages = (sd.past + sd.count + kPageTokens - 1) / kPageTokens;
                 if (lp < seq_pages) {
                     ph = p.tables[(size_t)sd.row * p.stride + lp];
                     if (ph < 0)                            // released by the sliding window: never visible
@@ -392,8 +470,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     return false;
                 pending = false;
             }
+            // Owned pages of the stage's previous tile go to the pool first;
+            // their reads of the stage must end before it is refilled.
+            if (!Q8 && p.fused && use > 0 && !flush_stores(st, (use - 1) & 1))
+                return false;
             if (use > 0 && !wait0(empty, (use - 1) & 1))
                 return false;
+            if (!Q8 && p.fused) {
+                if (stores_out)
+                    tma_store_wait_read();
+                stores_out = false;
+                __syncwarp();
+            }
             if (!Q8 && p.app_k && j == it.nt - 1 && (sd.past >> 7) == j)
                 append_row(it, sd);                       // the tile holds this call's new token: write it first
             if (Q8) {
@@ -423,12 +511,56 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     pend_sc[pg] = nsc[pg];
                 return true;
             }
+            // 0: every page from the pool; 1: the whole tile from k / v;
+            // 2: old pages from the pool, new ones from k / v.
+            int mode = 0;
+            if (p.fused && 128 * (j + 1) > sd.past)
+                mode = 128 * j >= sd.past ? 1 : 2;
+            const int l_end = sd.past + sd.count;
+            const bool fix = mode != 0 && 128 * (j + 1) > l_end;   // rows past the valid length to clear
+            uint64_t *bar = fix ? &s.fix_bar[vside ? 1 : 0] : full;
             if (lane == 0)
-                mbar_arrive_expect_tx(full, 2 * kTileBytes);
+                mbar_arrive_expect_tx(bar, 2 * kTileBytes);
             __syncwarp();
-            if (boxer)
-                tma_load_3d(&mKV, full, dst + my_pg * kPageElems, 0, 0,
-                            ph * blk_page + (vside ? p.H_kv : 0) + it.kvh);
+            const int blk0 = (vside ? p.H_kv : 0) + it.kvh;
+            const int grow0 = it.b * p.n - sd.past;      // row of k / v (over all entries) of position 0
+            if (mode == 1) {
+                if (lane == 0)
+                    tma_load_5d(vside ? &mVt : &mKt, bar, dst, 0, 0, 0, (grow0 + 128 * j) >> 3, it.kvh);
+            } else if (boxer) {
+                const int lp = 8 * j + my_pg;
+                if (mode == 2 && 16 * lp >= sd.past && lp < seq_pages)
+                    tma_load_5d(vside ? &mVp : &mKp, bar, dst + my_pg * kPageElems, 0, 0, 0, (grow0 + 16 * lp) >> 3,
+                                it.kvh);
+                else
+                    tma_load_3d(&mKV, bar, dst + my_pg * kPageElems, 0, 0, ph * blk_page + blk0);
+            }
+            if (mode != 0) {
+                const int lp = 8 * j + my_pg, r0 = 16 * lp - sd.past;
+                own_blk[st] = (boxer && r0 >= 0 && lp < seq_pages && r0 >= it.i0 && r0 < it.i0 + 2 * p.rows_pos &&
+                               ph < p.num_pages)
+                                  ? ph * blk_page + blk0
+                                  : -1;
+            }
+            if (fix) {
+                if (!wait0(&s.fix_bar[vside ? 1 : 0], fix_uses & 1))
+                    return false;
+                ++fix_uses;
+                // Whole rows are cleared, so the 128-byte swizzle inside a
+                // row does not matter: row r is slot r % 16 of page block
+                // r / 16, its column halves 1 KB apart within the 8-row group.
+                unsigned char *base = reinterpret_cast<unsigned char *>(dst);
+                const int r_lo = l_end - 128 * j > 0 ? l_end - 128 * j : 0;
+                for (int u = r_lo * 16 + lane; u < 128 * 16; u += 32) {
+                    const int r = u >> 4, c = u & 15;
+                    *reinterpret_cast<uint4 *>(base + (r >> 4) * 4096 + ((r >> 3) & 1) * 2048 + (c >> 3) * 1024 +
+                                               (r & 7) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(full);
+            }
             ++gt;                                         // this tile is in flight from here on
             return true;
         };
@@ -463,12 +595,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 }
                 ++q_issued;
             }
-            for (int j = (WIN ? it.j0 : 0) + 1; j < it.nt; ++j)
+            for (int j = (WIN ? it.j0 : 0) + 1; j < it.nt; ++j) {
                 if (!load_tile(it, sd, j)) {
                     ok = false;
                     break;
                 }
+            }
         }
+        if (z_next < z_end)
+            zero_some(z_end - z_next);
+        // The stages' last tiles: their owned pages go to the pool now.
+        if (!Q8 && p.fused && ok) {
+            for (uint32_t g = (gt > (uint32_t)stages ? gt - stages : 0); ok && g < gt; ++g)
+                ok = flush_stores(g % stages, (g / stages) & 1);
+        }
+        if (!Q8 && p.fused)
+            tma_store_wait_all();                         // every store has completed before the CTA exits
         if (Q8 && ok && pending && !convert(pend_st, pend_use, pend_sc))   // the last tile
             ok = false;
         if (lane == 0) {
@@ -1038,7 +1180,7 @@ bool encode(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, 
     auto fn = encoder();
     if (!fn)
         return false;
-    const cuuint32_t es[4] = {1, 1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     // bytes: FP8 code blocks, copied as they are (the kernel lays them out).
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1079,7 +1221,8 @@ int prefill_tc_rows_per_tile(int group) { return 128 / group; }
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
                               const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start, const void *app_k,
-                              const void *app_v)
+                              const void *app_v, const void *fused_k, const void *fused_v,
+                              const int64_t *d_zero_start)
 {
     if (pv.d != D || grid <= 0)
         return grid <= 0 ? cudaSuccess : cudaErrorInvalidValue;
@@ -1108,6 +1251,23 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
         !(q8 ? encode(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true) : encode(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)) ||
         !encode(&mo, 4, out, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
+    // Fused write: k and v [B, n, H_kv, 128] as [H_kv][B * n / 8 row groups]
+    // [column half][8 rows][64 elements] (n a multiple of 8), boxes of one
+    // key tile (16 groups, 32 KB) and of one page (2 groups, 4 KB).
+    const bool fused = fused_k != nullptr;
+    CUtensorMap mkt, mvt, mkp, mvp;
+    if (fused) {
+        if (q8 || pv.rope || app_k || !fused_v || !d_zero_start || n % 8 != 0)
+            return cudaErrorInvalidValue;
+        const cuuint64_t fdims[5] = {64, 8, 2, (cuuint64_t)B * n / 8, (cuuint64_t)pv.H_kv};
+        const cuuint64_t fstr[4] = {(cuuint64_t)pv.H_kv * D * 2, 128, (cuuint64_t)8 * pv.H_kv * D * 2, (cuuint64_t)D * 2};
+        const cuuint32_t tbox[5] = {64, 8, 2, 16, 1}, pbox[5] = {64, 8, 2, 2, 1};
+        if (!encode(&mkt, 5, fused_k, fdims, fstr, tbox) || !encode(&mvt, 5, fused_v, fdims, fstr, tbox) ||
+            !encode(&mkp, 5, fused_k, fdims, fstr, pbox) || !encode(&mvp, 5, fused_v, fdims, fstr, pbox))
+            return cudaErrorInvalidValue;
+    } else {
+        mkt = mvt = mkp = mvp = mkv;               // unused
+    }
     TcParams prm;
     prm.seqs = d_seqs;
     prm.items = d_items;
@@ -1133,6 +1293,9 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.ws_ml = ws.ml;
     prm.counters = ws.counters;
     prm.slot_rows = ws.slot_rows;
+    prm.fused = fused ? 1 : 0;
+    prm.B = B;
+    prm.zero_start = d_zero_start;
     const int smem = (int)sizeof(TcSmem) + 1024;
     // The shared-memory opt-in is per device: remember it per device.
     constexpr int kMaxDev = 64;
@@ -1142,7 +1305,8 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
         return cudaErrorInvalidDevice;
     const int which = q8 ? 4 + (pv.window > 0 || ws.ranged ? 1 : 0)
                          : (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
-    void (*const kern[6])(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = {
+    void (*const kern[6])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                          TcParams) = {
         prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
         prefill_tc_kernel<false, true, false>,  prefill_tc_kernel<true, true, false>,
         prefill_tc_kernel<false, false, true>,  prefill_tc_kernel<false, true, true>};
@@ -1165,9 +1329,9 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern[which], mq, mkv, mo, prm);
+    return cudaLaunchKernelEx(&cfg, kern[which], mq, mkv, mo, mkt, mvt, mkp, mvp, prm);
 #else
-    kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, prm);
+    kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, mkt, mvt, mkp, mvp, prm);
     return cudaGetLastError();
 #endif
 }

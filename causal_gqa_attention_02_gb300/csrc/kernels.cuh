@@ -70,7 +70,7 @@ struct SeqDesc {
     int32_t row;    // sequence id == block-table row
     int32_t past;   // tokens already cached before this call's rows (decode: L - 1)
     int32_t count;  // rows of this call that are valid (decode: 1)
-    int32_t pad_;
+    int32_t zero_from;  // fused prefill: rows zero_from .. n-1 of out are zeroed by the kernel (no item stores them)
 };
 
 // Copy-on-write of slots [0, slots) of page src into page dst (K and V, all heads).
@@ -157,7 +157,8 @@ bool decode_split_supported(int group);
 cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st);
 
 // bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).  Rows of the
-// batch entries must already be in the cache (launch_cache_write first).
+// batch entries must already be in the cache (launch_cache_write first),
+// unless fused_k / fused_v are given (see launch_prefill_tc).
 bool prefill_tc_supported(int group, int H_kv);
 // One block waiting, with the kernels' bounded wait, on a barrier phase that
 // never completes; sets kErrTimeout in *err after limit_ns.
@@ -171,9 +172,18 @@ int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // are encoded on the host.  app_k / app_v (decode only: count = 1 for every
 // entry, [B, H_kv, 128]) fuse the append: the row of each entry is written
 // at position past by the CTA that reads that page, before it reads it.
+// fused_k / fused_v (the call's k and v, [B, n, H_kv, 128], n a multiple of
+// 8, every entry's past a multiple of 16, bf16 cache without rotation) fuse
+// the cache write: the kernel reads the call's rows from them, writes each
+// new page to the pool once, and zeroes rows zero_from .. n-1 of out for
+// every entry; no cache-write launch precedes it.  Those rows, counted in
+// 16-byte units entry after entry, are cleared by CTA c from unit
+// d_zero_start[c] to d_zero_start[c + 1] (grid + 1 offsets).
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
                               const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start = nullptr,
-                              const void *app_k = nullptr, const void *app_v = nullptr);
+                              const void *app_k = nullptr, const void *app_v = nullptr,
+                              const void *fused_k = nullptr, const void *fused_v = nullptr,
+                              const int64_t *d_zero_start = nullptr);
 
 }  // namespace gqa
