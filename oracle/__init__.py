@@ -30,6 +30,10 @@ Contents:
                      section describes RoPE as a rotation by the position ID
                      whose inner products depend only on position differences),
                      and rope_stored_bf16(), the key bytes a rotating cache holds.
+  keys_at_read(), attention_pre_position()
+                     a pre-position cache ([P1] 2.5's layout_metadata: keys
+                     stored before the position transform): keys kept as given,
+                     rotated by their positions when read.
   e4m3_encode/_decode, quantize_e4m3_rows(), dequantize_e4m3_rows()
                      the quantised cache ([P1] 2.5: the physical cache may be
                      quantised as long as the logical order is kept): FP8
@@ -216,6 +220,35 @@ def rope_stored_bf16(k_bits: np.ndarray, positions, base: float) -> np.ndarray:
     y1 = (x1 * c).astype(np.float32) - (x2 * s).astype(np.float32)
     y2 = (x1 * s).astype(np.float32) + (x2 * c).astype(np.float32)
     return _f32_to_bf16_bits(np.concatenate([y1, y2], axis=-1).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# Pre-position keys ([P1] 2.5: layout_metadata records whether the cached
+# keys are taken before or after the position transform; [P3] prefix
+# caching: keys rotated by their position ID can only be reused at the same
+# absolute positions).  A pre-position cache stores each key as given and a
+# reader rotates it by its position before the score; in exact arithmetic
+# that is the post-position definition, and the stored keys can be read at
+# any common position offset.
+# ---------------------------------------------------------------------------
+
+def keys_at_read(K_stored: np.ndarray, positions, base: float) -> np.ndarray:
+    """Keys a reader of a pre-position cache uses: each stored key K_stored
+    [L, H, d] (fp64 values, as given to the cache) rotated by its position."""
+    return rope(K_stored, positions, base)
+
+
+def attention_pre_position(q: np.ndarray, K_stored: np.ndarray, V: np.ndarray, qpos, base: float,
+                           offset: int = 0, window: int = 0, nthreads: int | None = None):
+    """Attention over a pre-position cache: queries q [n, H_q, d] (before the
+    rotation) at positions qpos, stored keys K_stored [L, H_kv, d] at
+    positions 0..L-1; both read at absolute positions shifted by `offset`
+    (0: as written) and rotated there, then the definition of [P1] 2.3
+    (visibility by qpos)."""
+    qpos = np.asarray(qpos, dtype=np.int64)
+    L = K_stored.shape[0]
+    return attention(rope(q, qpos + offset, base), keys_at_read(K_stored, np.arange(L) + offset, base), V, qpos,
+                     nthreads, window)
 
 
 # ---------------------------------------------------------------------------
@@ -518,7 +551,8 @@ def prefill(cache: CacheModel, seq_ids, q, k, v, valid_lengths, nthreads=None, r
     q [B, n, H_q, d], k/v [B, n, H_kv, d] stored values.  Padding rows
     (i >= n_b) are discarded ([P1] 2.2) and returned as zeros.  With
     rope_base, q and every key are rotated by their positions first (the
-    cache model keeps the unrotated keys)."""
+    cache model keeps the unrotated keys: the bytes a pre-position cache
+    stores; a post-position cache stores rope_stored_bf16 of them)."""
     dt = cache.io_dtype
     B, n, H_q, d = q.shape
     nb = [int(x) for x in valid_lengths]

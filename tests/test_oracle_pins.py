@@ -429,6 +429,83 @@ def test_rope_stored_keys_round_to_within_one_bf16_step():
     assert np.array_equal(oracle.rope_stored_bf16(k, np.zeros(64), 10000.0), k)
 
 
+# ---------------------------------------------------------------- pre-position keys
+# [P1] 2.5: the cache records whether its keys were taken before or after the
+# position transform.  A pre-position cache keeps each key as given and the
+# reader rotates it by its position.  Pinned by: the stored bytes are the
+# input bytes; in exact arithmetic the result is the post-position one; the
+# stored keys read at a common offset give the same result (what a
+# post-position cache cannot do: its keys carry their absolute positions,
+# [P3] prefix caching); a pure-Python brute force on a tiny case.
+
+def test_pre_position_cache_stores_the_input_bytes():
+    rng = np.random.default_rng(21)
+    k = workloads.normal_bf16(rng, (1, 37, 2, 8))
+    v = workloads.normal_bf16(rng, (1, 37, 2, 8))
+    q = workloads.normal_bf16(rng, (1, 37, 4, 8))
+    cm = oracle.CacheModel(8, 1, 8, 2, 8, "bf16")
+    s = cm.create()
+    oracle.prefill(cm, [s], q, k, v, [37], nthreads=2, rope_base=10000.0)
+    rk, rv = cm.raw_kv(s)
+    assert np.array_equal(rk, k[0]) and np.array_equal(rv, v[0])
+    # a post-position cache would hold other bytes for every position > 0
+    post = oracle.rope_stored_bf16(k[0], np.arange(37), 10000.0)
+    assert not np.array_equal(post[1:], k[0, 1:])
+
+
+def test_pre_position_read_equals_post_position_definition():
+    rng = np.random.default_rng(22)
+    n, H_q, H_kv, d, base = 11, 6, 2, 16, 10000.0
+    Q, K, V = rng.standard_normal((n, H_q, d)), rng.standard_normal((n, H_kv, d)), rng.standard_normal((n, H_kv, d))
+    pos = np.arange(n)
+    pre = oracle.attention_pre_position(Q, K, V, pos, base, nthreads=2)
+    post = oracle.attention_dense(oracle.rope(Q, pos, base), oracle.rope(K, pos, base), V, pos)
+    assert np.allclose(pre, post, rtol=0, atol=1e-12)
+    # the window form too
+    prew = oracle.attention_pre_position(Q, K, V, pos, base, window=3, nthreads=2)
+    postw = oracle.attention_dense(oracle.rope(Q, pos, base), oracle.rope(K, pos, base), V, pos, window=3)
+    assert np.allclose(prew, postw, rtol=0, atol=1e-12)
+
+
+def test_pre_position_keys_read_at_an_offset_give_the_same_result():
+    rng = np.random.default_rng(23)
+    n, H_q, H_kv, d, base = 13, 4, 2, 32, 10000.0
+    Q, K, V = rng.standard_normal((n, H_q, d)), rng.standard_normal((n, H_kv, d)), rng.standard_normal((n, H_kv, d))
+    pos = np.arange(n)
+    ref = oracle.attention_pre_position(Q, K, V, pos, base, nthreads=2)
+    for off in (1, 100, 4096):
+        got = oracle.attention_pre_position(Q, K, V, pos, base, offset=off, nthreads=2)
+        assert np.allclose(got, ref, rtol=0, atol=1e-10)
+    # post-position keys (rotated once at their original positions) read by
+    # queries at an offset give a different result
+    K_post = oracle.rope(K, pos, base)
+    moved = _att(oracle.rope(Q, pos + 100, base), K_post, V, pos)
+    assert np.abs(moved - ref).max() > 1e-3
+
+
+def test_pre_position_read_brute_force_tiny():
+    rng = np.random.default_rng(24)
+    n, d, base = 4, 4, 10.0
+    Q, K, V = rng.standard_normal((n, 1, d)), rng.standard_normal((n, 1, d)), rng.standard_normal((n, 1, d))
+    got = oracle.attention_pre_position(Q, K, V, np.arange(n), base, nthreads=1)
+
+    def rot(x, p):
+        out = [0.0] * d
+        for e in range(d // 2):
+            a = p * base ** (-2.0 * e / d)
+            out[e] = x[e] * math.cos(a) - x[e + d // 2] * math.sin(a)
+            out[e + d // 2] = x[e] * math.sin(a) + x[e + d // 2] * math.cos(a)
+        return out
+
+    for i in range(n):
+        qi = rot(list(Q[i, 0]), i)
+        sc = [sum(a * b for a, b in zip(qi, rot(list(K[j, 0]), j))) / math.sqrt(d) for j in range(i + 1)]
+        m = max(sc)
+        w = [math.exp(x - m) for x in sc]
+        o = [sum(w[j] * V[j, 0, e] for j in range(i + 1)) / sum(w) for e in range(d)]
+        assert np.allclose(got[i, 0], o, rtol=0, atol=1e-13)
+
+
 # ---------------------------------------------------------------- sliding window
 # [P3] sliding window: position t reads the most recent W positions, the
 # current one included; K/V outside the window is never read again, so a
