@@ -255,7 +255,7 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     flops = gqa.work.prefill_flops([0] * B, nb, H_q, d, args.window)
     pages = sum(workloads.pages_for(x) for x in nb) + 16
     cache = gqa.Cache(H_kv, d, pages, B, workloads.pages_for(n) + 1, dtype="bf16", rope=args.rope,
-                      window=args.window)
+                      window=args.window, keys_post_position=0 if args.pre_position else 1)
     ids = [cache.seq_create() for _ in range(B)]
     q, k, v = to_dev(torch, w["q"]), to_dev(torch, w["k"]), to_dev(torch, w["v"])
     out = torch.empty_like(q)
@@ -329,7 +329,10 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
            "l2": "flushed (512 MiB write, untimed) before every timed step",
            "causal_gflop_per_step": round(flops / 1e9, 3)}
     if args.rope:
-        cfg["position_mechanism"] = "rotary (base 10000), applied inside the library: keys at write, queries in-kernel"
+        cfg["position_mechanism"] = ("rotary (base 10000), applied inside the library: keys at write, queries in-kernel"
+                                     if not args.pre_position else
+                                     "rotary (base 10000), pre-position cache: keys stored as given and rotated when "
+                                     "read (CUDA-core kernels), queries in-kernel")
     if args.window:
         cfg["sliding_window"] = "W=%d: position p attends to keys max(0, p-W+1)..p; flops count those pairs" % args.window
     return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
@@ -352,7 +355,8 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     spare = B * workloads.pages_for(grow + 16) if W else 0
     cache = gqa.Cache(H_kv, d, w["num_pages"] + spare, B, workloads.pages_for(max(L) + grow) + 1, dtype=args.kv,
                       rope=args.rope, page_order=(list(w["page_order"]) + list(range(w["num_pages"],
-                      w["num_pages"] + spare))) if W else w["page_order"], window=W)
+                      w["num_pages"] + spare))) if W else w["page_order"], window=W,
+                      keys_post_position=0 if args.pre_position else 1)
     ids = [cache.seq_create() for _ in range(B)]
     cache.set_decode_kernel(args.decode_kernel)
     for b in range(B):
@@ -437,7 +441,9 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                       "l2": "not flushed: %.2f GB of K/V per step exceeds the 129 MB L2" % (kv_bytes / 1e9),
                       "kv_bytes_per_step": kv_bytes}}
     if args.rope:
-        res["config"]["position_mechanism"] = "rotary (base 10000): queries rotated in-kernel"
+        res["config"]["position_mechanism"] = ("rotary (base 10000): queries rotated in-kernel" if not args.pre_position
+                                               else "rotary (base 10000), pre-position cache: keys rotated as the "
+                                                    "split-K decode reads them, queries in-kernel")
     if W:
         res["config"]["sliding_window"] = ("W=%d: a decode reads the last min(L, W) tokens; sequences grow by one "
                                            "token a step (no rewind), K/V bytes counted per step" % W)
@@ -754,6 +760,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--rope", action="store_true",
                     help="caches with the rotary position mechanism applied by the library")
+    ap.add_argument("--pre-position", action="store_true",
+                    help="with --rope: caches that store keys before the rotation and rotate them when read")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto",
                     help="decode kernel of attn_decode (auto: tensor-core for bf16, d_h = 128)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
@@ -766,6 +774,8 @@ def main():
                     help="seconds of fp64 oracle work per CPU baseline (rank 0, N=1)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.pre_position and not args.rope:
+        ap.error("--pre-position needs --rope (the cache rotates the keys it stores before the rotation)")
     if args.kv == "fp8":
         args.no_prefill = True               # the quantised cache is measured on decode
         args.extra = False

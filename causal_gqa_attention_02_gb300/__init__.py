@@ -33,7 +33,7 @@ PAGE_TOKENS = 16
 LAYOUT_VERSION = 2
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
 KERNELS = {"cache_write": 0, "cow_copy": 1, "prefill_tc": 2, "attn_simt": 3,
-           "decode_split": 4, "decode_combine": 5}
+           "decode_split": 4, "decode_combine": 5, "rotate_pages": 6}
 DECODE_KERNELS = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
 
 _I32P = ctypes.POINTER(ctypes.c_int32)

@@ -93,6 +93,9 @@ struct gqa_cache {
     size_t stage_cap = 0;
     float *d_ws = nullptr;               // decode split partials
     size_t ws_cap = 0;
+    char *d_rot = nullptr;               // pre-position prefill: the call's pages with rotated keys
+    size_t rot_cap = 0;
+    std::vector<int32_t> rot_slot;       // scratch slot of a pool page during one call (-1 = none)
     int32_t *d_cnt = nullptr;            // decode merge counters [B * H_kv], kept at zero
     size_t cnt_cap = 0;
     float2 *d_rope = nullptr;            // rope = 1: (cos, sin) [max positions][d_h / 2]
@@ -159,6 +162,7 @@ struct gqa_cache {
         pv.window = desc.window;
         pv.dtype = desc.dtype;
         pv.scales = nullptr;
+        pv.keys_pre = desc.keys_post_position == 0 ? 1 : 0;
         if (pool && desc.dtype == GQA_DTYPE_FP8_E4M3)   // the scales follow the blocks
             pv.scales = reinterpret_cast<float *>(
                 static_cast<char *>(pool) +
@@ -364,6 +368,26 @@ int ensure_ws(gqa_cache *c, size_t floats)
     return GQA_OK;
 }
 
+// Device pages for a pre-position prefill's rotated copy, grown on demand.
+int ensure_rot(gqa_cache *c, size_t bytes)
+{
+    if (bytes <= c->rot_cap)
+        return GQA_OK;
+    if (c->d_rot) {
+        cudaError_t e = cudaFree(c->d_rot);
+        c->d_rot = nullptr;
+        c->rot_cap = 0;
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFree(rotated pages)");
+    }
+    const size_t cap = (bytes + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+    cudaError_t e = cudaMalloc((void **)&c->d_rot, cap);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(rotated pages)");
+    c->rot_cap = cap;
+    return GQA_OK;
+}
+
 // Counters the decode kernel's merge uses; zero when allocated, and the
 // kernel leaves them zero.
 int ensure_cnt(gqa_cache *c, size_t n)
@@ -473,8 +497,9 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
         return fail(GQA_EINVAL, "num_pages, max_seqs and max_pages_per_seq must be >= 1");
     if ((int64_t)d.max_pages_per_seq * kPageTokens > INT_MAX)
         return fail(GQA_EINVAL, "max_pages_per_seq too large");
-    if (d.keys_post_position != 1)
-        return fail(GQA_ELAYOUT, "only post-position keys are supported (keys_post_position = 1)");
+    if (d.keys_post_position != 1 && !(d.keys_post_position == 0 && d.rope == 1))
+        return fail(GQA_ELAYOUT, "keys_post_position must be 1, or 0 with rope = 1 (keys stored before the "
+                                 "library's rotation and rotated when read)");
     if (d.layout_version != GQA_LAYOUT_VERSION)
         return fail(GQA_ELAYOUT, "layout_version %d, this library writes %d", d.layout_version,
                     GQA_LAYOUT_VERSION);
@@ -581,6 +606,7 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_err) cudaFree(c->d_err);
         if (c->d_stage) cudaFree(c->d_stage);
         if (c->d_ws) cudaFree(c->d_ws);
+        if (c->d_rot) cudaFree(c->d_rot);
         if (c->d_cnt) cudaFree(c->d_cnt);
         if (c->d_rope) cudaFree(c->d_rope);
         if (c->d_io) cudaFree(c->d_io);
@@ -901,8 +927,10 @@ int tc_workspace(gqa_cache *c, const TcPlan &pl, TcSplitWs &ws)
 // tensor-core kernel was asked for but cannot serve this cache or group.
 int decode_uses_tc(const gqa_cache *c, int G)
 {
+    // Pre-position keys are rotated as they are read, on the CUDA cores.
     const bool ok = (c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) &&
-                    c->desc.head_dim == 128 && c->cc >= 100 && prefill_tc_supported(G, c->desc.num_kv_heads);
+                    c->desc.head_dim == 128 && c->cc >= 100 && c->desc.keys_post_position == 1 &&
+                    prefill_tc_supported(G, c->desc.num_kv_heads);
     if (c->decode_kernel == GQA_DECODE_CUDA_CORE)
         return 0;
     if (c->decode_kernel == GQA_DECODE_TENSOR_CORE)
@@ -981,8 +1009,41 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         return rc;
     const int G = H_q / c->desc.num_kv_heads;
     const bool use_tc = (c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) &&
-                        c->desc.head_dim == 128 && c->cc >= 100 &&
-                        prefill_tc_supported(G, c->desc.num_kv_heads);
+                        c->desc.head_dim == 128 && c->cc >= 100 && prefill_tc_supported(G, c->desc.num_kv_heads);
+    // Pre-position keys on the tensor-core path: the kernel reads keys as
+    // stored, so every distinct page the call reads is first copied, keys
+    // rotated by their positions, to a compact scratch pool, and the kernel
+    // reads that copy through block tables remapped to it (row b = entry b).
+    // Each page is rotated once per call however many items read it.
+    const bool pre_tc = use_tc && c->desc.keys_post_position == 0;
+    std::vector<int2> rot_pages;
+    std::vector<int32_t> rot_tab;
+    std::vector<SeqDesc> rot_sds;
+    int32_t rot_stride = 1;
+    if (pre_tc) {
+        for (int b = 0; b < B; ++b)
+            rot_stride = std::max<int32_t>(rot_stride, (int32_t)c->seqs[sds[b].row].pages.size());
+        rot_tab.assign((size_t)B * rot_stride, -1);
+        c->rot_slot.resize(c->desc.num_pages, -1);
+        for (int b = 0; b < B; ++b) {
+            const std::vector<int32_t> &pg = c->seqs[sds[b].row].pages;
+            for (size_t lp = 0; lp < pg.size(); ++lp) {
+                const int32_t ph = pg[lp];
+                if (ph < 0)
+                    continue;                             // released by the sliding window
+                if (c->rot_slot[ph] < 0) {
+                    c->rot_slot[ph] = (int32_t)rot_pages.size();
+                    rot_pages.push_back(make_int2(ph, (int)lp));   // shared pages sit at one logical index
+                }
+                rot_tab[(size_t)b * rot_stride + lp] = c->rot_slot[ph];
+            }
+        }
+        for (const int2 &x : rot_pages)
+            c->rot_slot[x.x] = -1;
+        rot_sds = sds;
+        for (int b = 0; b < B; ++b)
+            rot_sds[b].row = b;
+    }
     TcPlan plan;
     if (use_tc)
         plan_tc(c, sds, G, plan);
@@ -1019,6 +1080,11 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     const size_t o_items = stg.add(plan.items.data(), plan.items.size());
     const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
     const size_t o_zero = stg.add(zstart.data(), zstart.size());
+    const size_t o_rpages = stg.add(rot_pages.data(), rot_pages.size());
+    const size_t o_rtab = stg.add(rot_tab.data(), rot_tab.size());
+    const size_t o_rsds = stg.add(rot_sds.data(), rot_sds.size());
+    if (pre_tc && (rc = ensure_rot(c, rot_pages.size() * 2 * (size_t)c->desc.num_kv_heads * 4096)) != GQA_OK)
+        return rc;
     TcSplitWs ws;
     if (use_tc && (rc = tc_workspace(c, plan, ws)) != GQA_OK)
         return rc;
@@ -1042,6 +1108,24 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
                                                  out_row_bytes);
                    })) != GQA_OK)
         return rc;
+    if (pre_tc) {
+        if ((rc = run_kernel(c, GQA_KERNEL_ROTATE_PAGES, st, "page rotation kernel", [&](cudaEvent_t ev) {
+                 rec(ev, st);
+                 return launch_rotate_pages(pv, (const int2 *)(c->d_stage + o_rpages), (int)rot_pages.size(),
+                                            c->d_rot, st);
+             })) != GQA_OK)
+            return rc;
+        PoolView rv = pv;
+        rv.pool = c->d_rot;
+        rv.tables = (const int32_t *)(c->d_stage + o_rtab);
+        rv.stride = rot_stride;
+        rv.num_pages = (int32_t)rot_pages.size();
+        rv.keys_pre = 0;                                  // the copy holds the keys as attention uses them
+        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&](cudaEvent_t ev) {
+            return launch_prefill_tc(rv, (const SeqDesc *)(c->d_stage + o_rsds), (const TcItem *)(c->d_stage + o_items),
+                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, n, H_q, q, out, ws, st, ev);
+        });
+    }
     if (use_tc) {
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core prefill kernel", [&](cudaEvent_t ev) {
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items),
@@ -1259,7 +1343,7 @@ static int decode_launch(gqa_cache *c, const PoolView &pv, const std::vector<Seq
     const size_t o_sds = stg.add(sds.data(), sds.size());
     int rc;
     if ((rc = decode_uses_tc(c, G)) < 0)
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
     if (rc == 1) {
         // The prefill kernel at one query row per sequence, each sequence's
         // key tiles split across SMs and merged in the kernel.
@@ -1411,7 +1495,7 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     const int G = H_q / H_kv;
     const int use_tc = c->meta_only ? 0 : decode_uses_tc(c, G);
     if (use_tc < 0)
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
     if (!use_tc || c->desc.dtype == GQA_DTYPE_FP8_E4M3) {
         // CUDA-core kernels (and the quantised cache, whose write rounds in
         // its own kernel): the write, then the decode.
@@ -1483,8 +1567,10 @@ int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
     if (kernel != GQA_DECODE_AUTO && kernel != GQA_DECODE_TENSOR_CORE && kernel != GQA_DECODE_CUDA_CORE)
         return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE or _CUDA_CORE", kernel);
     if (kernel == GQA_DECODE_TENSOR_CORE &&
-        ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128))
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 or FP8 E4M3 cache with d_h = 128");
+        ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128 ||
+         c->desc.keys_post_position != 1))
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 or FP8 E4M3 cache with d_h = 128 and "
+                                "post-position keys");
     c->decode_kernel = kernel;
     return GQA_OK;
 }
@@ -1577,7 +1663,7 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     const int G = H_q / H_kv;
     const int use_tc = decode_uses_tc(c, G);
     if (use_tc < 0)
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128 and H_q/H_kv <= 128");
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
     if (!use_tc && ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) ||
                     c->desc.head_dim != 128 || !decode_split_supported(G)))
         return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 (and H_q/H_kv <= 8 on the "

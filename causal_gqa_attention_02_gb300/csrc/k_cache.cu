@@ -298,10 +298,13 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     const size_t row_bytes = (size_t)pv.d * esize;
     // With rotation a unit must lie within one half of the row and hold
     // whole elements.
-    const int U = copy_unit_bytes(pv.rope ? row_bytes / 2 : row_bytes, k, v, pv.pool);
+    // Keys are rotated when written unless the cache stores them before the
+    // rotation (then the write is a plain copy and the readers rotate).
+    const bool rot = pv.rope && !pv.keys_pre;
+    const int U = copy_unit_bytes(rot ? row_bytes / 2 : row_bytes, k, v, pv.pool);
     if (zero_out && (zero_row_bytes % 16 != 0 || (uintptr_t)zero_out % 16 != 0))
         return cudaErrorInvalidValue;
-    if (pv.rope && U < esize)
+    if (rot && U < esize)
         return cudaErrorInvalidValue;
     const int wpb = 8;                                  // at most 8: the rotation's table rows
     int blocks = (rows + wpb - 1) / wpb;
@@ -313,10 +316,10 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     // The rotating kernel is a separate instantiation, so that a cache without
     // the position mechanism runs the plain copy.
 #define GQA_CACHE_WRITE(UU)                                                                                    \
-    (pv.rope ? (cache_write_kernel<UU, true><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,       \
+    (rot ? (cache_write_kernel<UU, true><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,           \
                                                                        zero_row_bytes), 0)                    \
-             : (cache_write_kernel<UU, false><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,      \
-                                                                        zero_row_bytes), 0))
+         : (cache_write_kernel<UU, false><<<grid, 32 * wpb, 0, st>>>(pv, esize, d_seqs, n, kc, vc, z,          \
+                                                                    zero_row_bytes), 0))
     switch (U) {
     case 16: GQA_CACHE_WRITE(16); break;
     case 8:  GQA_CACHE_WRITE(8); break;
@@ -325,6 +328,65 @@ cudaError_t launch_cache_write(const PoolView &pv, int esize, const SeqDesc *d_s
     default: GQA_CACHE_WRITE(1); break;
     }
 #undef GQA_CACHE_WRITE
+    return cudaGetLastError();
+}
+
+// Pre-position cache read by the tensor-core prefill: page u of the list
+// (pool page pages[u].x at logical page pages[u].y of its sequences) is
+// copied to page u of `dst` (a pool of the same block layout), its keys
+// rotated by their positions 16 * pages[u].y + slot with the cache-write
+// rule (fp32 cos/sin of the table, each product, sum and difference rounded
+// to fp32, then to bf16), its values as they are.  bf16, d = 128: a block
+// is 4 KB; thread (slot, unit) of a K block rotates the 16-byte unit of
+// column half 0 with the same unit of column half 1 (columns e and e + 64
+// sit at the same offset of the two 128-byte chunks of a row).
+__global__ void __launch_bounds__(128)
+rotate_pages_kernel(PoolView pv, const int2 *__restrict__ pages, char *__restrict__ dst)
+{
+    const int2 pg = pages[blockIdx.x];
+    const int head = blockIdx.y, kv = blockIdx.z;
+    constexpr size_t kBlk = 4096;
+    if ((unsigned)pg.x >= (unsigned)pv.num_pages) {
+        if (threadIdx.x == 0)
+            atomicOr(pv.err, kErrPageId);
+        return;
+    }
+    const size_t blk_src = ((size_t)pg.x * 2 + kv) * pv.H_kv + head;
+    const size_t blk_dst = ((size_t)blockIdx.x * 2 + kv) * pv.H_kv + head;
+    const uint4 *src = reinterpret_cast<const uint4 *>((const char *)pv.pool + blk_src * kBlk);
+    uint4 *out = reinterpret_cast<uint4 *>(dst + blk_dst * kBlk);
+    if (kv) {                                            // values: a plain copy
+        out[threadIdx.x] = src[threadIdx.x];
+        out[threadIdx.x + 128] = src[threadIdx.x + 128];
+        return;
+    }
+    const int slot = threadIdx.x >> 3, u = threadIdx.x & 7;   // unit u of the slot's column half 0
+    // uint4 index of (slot, chunk c, unit u): ((slot / 8) * 2 + c) * 64 + (slot % 8) * 8 + u
+    const int i0 = ((slot >> 3) * 2) * 64 + (slot & 7) * 8 + u, i1 = i0 + 64;
+    const uint4 a = src[i0], b = src[i1];
+    const float2 *cs = pv.rope + (size_t)(kPageTokens * pg.y + slot) * 64 + 8 * u;
+    const __nv_bfloat16 *xa = reinterpret_cast<const __nv_bfloat16 *>(&a);
+    const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(&b);
+    uint4 ra, rb;
+    __nv_bfloat16 *ya = reinterpret_cast<__nv_bfloat16 *>(&ra), *yb = reinterpret_cast<__nv_bfloat16 *>(&rb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float x = __bfloat162float(xa[j]), y = __bfloat162float(xb[j]);
+        const float2 t = cs[j];
+        ya[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x, t.x), __fmul_rn(y, t.y)));
+        yb[j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x, t.y), __fmul_rn(y, t.x)));
+    }
+    out[i0] = ra;
+    out[i1] = rb;
+}
+
+cudaError_t launch_rotate_pages(const PoolView &pv, const int2 *d_pages, int npages, void *dst, cudaStream_t st)
+{
+    if (pv.d != 128 || pv.dtype != kDtypeBf16 || !pv.rope)
+        return cudaErrorInvalidValue;
+    if (npages <= 0)
+        return cudaSuccess;
+    rotate_pages_kernel<<<dim3((unsigned)npages, (unsigned)pv.H_kv, 2), 128, 0, st>>>(pv, d_pages, (char *)dst);
     return cudaGetLastError();
 }
 

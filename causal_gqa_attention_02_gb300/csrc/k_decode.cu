@@ -371,7 +371,10 @@ __device__ __forceinline__ void q8_values(const PoolView &pv, int kvh, const int
 // Q8: the pool holds FP8 E4M3 codes (a page block is [16 slots][128 bytes])
 // and a scale per row, and both passes run on mma.sync (q8_scores,
 // q8_values); the softmax and the merge are shared.
-template <int G, bool ROPE, bool Q8>
+// KPRE (with ROPE): the pool holds keys before the rotation; each key row is
+// rotated by its position as it is read (column c pairs with c + 64, held by
+// lane ^ 8; cos/sin of the token's table row), in fp32.
+template <int G, bool ROPE, bool Q8, bool KPRE>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeItem *__restrict__ items,
                     const int32_t *__restrict__ item_start, int chunk, int H_q,
@@ -464,6 +467,21 @@ decode_split_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, const DecodeI
             for (int i = 0; i < 8; ++i) {
                 float2 w[4];
                 bf16x8(kk[i], w);
+                if (KPRE) {
+                    const int pos = t0 + pg * kPageTokens + 2 * i + half;
+                    const float4 *cs4 = reinterpret_cast<const float4 *>(pv.rope + (size_t)pos * (D / 2) + (col & 63));
+                    const bool first = (lane & 8) == 0;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 c2 = __ldg(cs4 + u);     // (cos, sin) of columns 2u, 2u + 1 of the pair half
+                        const float ox = __shfl_xor_sync(0xffffffffu, w[u].x, 8);
+                        const float oy = __shfl_xor_sync(0xffffffffu, w[u].y, 8);
+                        if (first)
+                            w[u] = make_float2(w[u].x * c2.x - ox * c2.y, w[u].y * c2.z - oy * c2.w);
+                        else
+                            w[u] = make_float2(ox * c2.y + w[u].x * c2.x, oy * c2.w + w[u].y * c2.z);
+                    }
+                }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     float2 a = make_float2(0.f, 0.f);
@@ -716,14 +734,17 @@ cudaError_t launch_g(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st)
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q;
     __nv_bfloat16 *out = (__nv_bfloat16 *)a.out;
     if (pv.dtype == kDtypeFp8)
-        decode_split_kernel<G, false, true><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
-                                                                         a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
+        decode_split_kernel<G, false, true, false><<<grid, kWarps * 32, 0, st>>>(
+            pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
+    else if (pv.rope && pv.keys_pre)
+        decode_split_kernel<G, true, false, true><<<grid, kWarps * 32, 0, st>>>(
+            pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
     else if (pv.rope)
-        decode_split_kernel<G, true, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
-                                                                         a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
+        decode_split_kernel<G, true, false, false><<<grid, kWarps * 32, 0, st>>>(
+            pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
     else
-        decode_split_kernel<G, false, false><<<grid, kWarps * 32, 0, st>>>(pv, a.seqs, a.items, a.item_start, a.chunk,
-                                                                          a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
+        decode_split_kernel<G, false, false, false><<<grid, kWarps * 32, 0, st>>>(
+            pv, a.seqs, a.items, a.item_start, a.chunk, a.H_q, q, a.ws_o, a.ws_ml, a.counters, out);
     return cudaGetLastError();
 }
 

@@ -47,8 +47,10 @@ __device__ __forceinline__ float warp_sum(float x)
 }
 
 // T: element type of q and out (and of the pool unless Q8); Q8: the pool
-// holds FP8 E4M3 codes with a scale per row, read as fp32(decode(code) * s).
-template <typename T, bool Q8>
+// holds FP8 E4M3 codes with a scale per row, read as fp32(decode(code) * s);
+// KPRE: the pool holds keys before the rotation, and each key is rotated by
+// its position as it is read (pairs (e, e + d/2), fp32).
+template <typename T, bool Q8, bool KPRE>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
                  const T *__restrict__ q, T *__restrict__ out)
@@ -119,8 +121,19 @@ attn_simt_kernel(PoolView pv, const SeqDesc *__restrict__ seqs, int n, int H_q,
                 const char *kb_ = pool + (size_t)page * 2 * H_kv * blk_bytes + k_off;
                 const size_t kbi = (size_t)page * 2 * H_kv + g;
                 float dot = 0.0f;
-                for (int e = 0; e < d; ++e)
-                    dot = fmaf(qs[e], elem(kb_, kbi, t % kPageTokens, e), dot);
+                if (KPRE) {
+                    const float2 *cs = pv.rope + (size_t)t * (d / 2);
+                    for (int e = 0; e < d / 2; ++e) {
+                        const float x = elem(kb_, kbi, t % kPageTokens, e);
+                        const float y = elem(kb_, kbi, t % kPageTokens, e + d / 2);
+                        const float2 r = cs[e];
+                        dot = fmaf(qs[e], x * r.x - y * r.y, dot);
+                        dot = fmaf(qs[e + d / 2], x * r.y + y * r.x, dot);
+                    }
+                } else {
+                    for (int e = 0; e < d; ++e)
+                        dot = fmaf(qs[e], elem(kb_, kbi, t % kPageTokens, e), dot);
+                }
                 s = dot / root_d;
             } else {
                 atomicOr(pv.err, kErrPageId);
@@ -170,14 +183,21 @@ cudaError_t launch_attn_simt(const PoolView &pv, int dtype, const SeqDesc *d_seq
     if (B <= 0 || n <= 0)
         return cudaSuccess;
     dim3 grid((unsigned)((n + kWarps - 1) / kWarps), (unsigned)H_q, (unsigned)B);
-    if (dtype == kDtypeF32)
-        attn_simt_kernel<float, false><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
-                                                                   (float *)out);
+    const bool kpre = pv.keys_pre && pv.rope;
+    if (dtype == kDtypeF32 && kpre)
+        attn_simt_kernel<float, false, true><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
+                                                                         (float *)out);
+    else if (dtype == kDtypeF32)
+        attn_simt_kernel<float, false, false><<<grid, kWarps * 32, 0, st>>>(pv, d_seqs, n, H_q, (const float *)q,
+                                                                          (float *)out);
     else if (dtype == kDtypeFp8)
-        attn_simt_kernel<__nv_bfloat16, true><<<grid, kWarps * 32, 0, st>>>(
+        attn_simt_kernel<__nv_bfloat16, true, false><<<grid, kWarps * 32, 0, st>>>(
+            pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
+    else if (kpre)
+        attn_simt_kernel<__nv_bfloat16, false, true><<<grid, kWarps * 32, 0, st>>>(
             pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
     else
-        attn_simt_kernel<__nv_bfloat16, false><<<grid, kWarps * 32, 0, st>>>(
+        attn_simt_kernel<__nv_bfloat16, false, false><<<grid, kWarps * 32, 0, st>>>(
             pv, d_seqs, n, H_q, (const __nv_bfloat16 *)q, (__nv_bfloat16 *)out);
     return cudaGetLastError();
 }

@@ -50,6 +50,8 @@ struct PoolView {
     int32_t window;          // sliding window W (0 = none): position p sees keys max(0, p-W+1)..p
     int32_t dtype;           // kDtype*: the stored element type
     float *scales;           // FP8 E4M3: scale of (block, slot) at block * 16 + slot; else null
+    int32_t keys_pre;        // 1: keys are stored before the rotation (rope != null) and rotated
+                             // when read; 0: keys are stored as attention uses them
 };
 
 // First key position visible to a query at absolute position p.
@@ -123,6 +125,12 @@ int copy_unit_bytes(size_t row_bytes, const void *a, const void *b, const void *
 
 cudaError_t launch_cow_copy(const PoolView &pv, int esize, const CowDesc *d_cows, int ncows,
                             cudaStream_t st);
+
+// Pre-position cache (bf16, d = 128, rope): page u of dst = pool page
+// d_pages[u].x (logical page d_pages[u].y of its sequences) with its keys
+// rotated by their positions (the cache-write rounding rule) and its values
+// copied; dst has npages pages in the pool's block layout.
+cudaError_t launch_rotate_pages(const PoolView &pv, const int2 *d_pages, int npages, void *dst, cudaStream_t st);
 
 // Write rows c < seqs[b].count of k/v [B, n, H_kv, d] to positions past+c.
 // If zero_out is given ([B, n, zero_row_bytes], 16-byte aligned rows), its

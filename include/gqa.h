@@ -118,9 +118,15 @@ typedef struct {
     int32_t num_pages;           /* pages in the pool, >= 1                                 */
     int32_t max_seqs;            /* sequence ids are 0..max_seqs-1                          */
     int32_t max_pages_per_seq;   /* block-table capacity of one sequence                    */
-    int32_t keys_post_position;  /* must be 1: keys are stored after the position transform
-                                    ([P1] 2.5: K used by attention; pre-transform caches are
-                                    a different contract)                                    */
+    int32_t keys_post_position;  /* [P1] 2.5: whether the cached keys were taken after (1) or
+                                    before (0) the position transform.  1: keys are stored as
+                                    attention uses them (rotated when written if rope = 1).
+                                    0 (only with rope = 1): keys are stored exactly as given
+                                    and every attention kernel rotates each key by its
+                                    position as it reads it, so the stored keys do not depend
+                                    on where they sit ([P3] prefix caching).  Such a cache is
+                                    read by the CUDA-core kernels (the generic prefill and the
+                                    split-K decode), not the tensor-core ones.               */
     int32_t layout_version;      /* must be GQA_LAYOUT_VERSION                              */
     const int32_t *page_order;   /* host, optional: permutation of 0..num_pages-1 giving the
                                     order in which free pages are handed out (NULL = identity).
@@ -130,8 +136,9 @@ typedef struct {
                                     ID): 0 = none, q/k arrive already transformed; 1 = rotary:
                                     dimension pairs (e, e + d_h/2), e < d_h/2, rotated
                                     counter-clockwise by pos * rope_base^(-2e/d_h).  Keys are
-                                    rotated when written (the cache holds post-position keys),
-                                    queries inside the attention kernels.                     */
+                                    rotated when written (keys_post_position = 1) or when read
+                                    (keys_post_position = 0), queries inside the attention
+                                    kernels.                                                  */
     float rope_base;             /* rope = 1: the frequency base, > 1 (e.g. 10000)           */
     int32_t window;              /* sliding window W ([P3] sliding window and ring cache): 0 =
                                     none; W >= 1: the query at position p sees keys
@@ -181,7 +188,8 @@ size_t gqa_pool_bytes(const gqa_cache_desc *desc);
  * Errors: GQA_EINVAL (bad description, pool too small, misaligned; rope not
  *         0/1, or rope = 1 with an odd d_h or rope_base <= 1; FP8_E4M3 with
  *         d_h not a multiple of 32 or with rope = 1),
- *         GQA_ELAYOUT (keys_post_position != 1 or unknown layout_version),
+ *         GQA_ELAYOUT (keys_post_position not 1, or 0 without rope = 1; unknown
+ *         layout_version),
  *         GQA_ECUDA. */
 int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_bytes,
                      gqa_cache **out);
@@ -235,15 +243,17 @@ int gqa_page_refcount(const gqa_cache *cache, int32_t page, int32_t *out);
  * For each batch entry b, with sequence s = seq_ids[b] of current length P_b
  * and n_b = valid_lengths[b] valid (right-aligned padding) rows:
  *  1. the K/V rows i < n_b are written to the cache at positions P_b + i,
- *     bit for bit (with rope = 1, K is rotated by position P_b + i first:
- *     each pair (x, y) becomes (x*c - y*s, x*s + y*c), every product, sum and
- *     difference rounded to fp32, then rounded to the cache type; c, s are
- *     the fp32 cos/sin of the table); padding rows are never written ([P1]
- *     2.6; invariant 2.2 item 4);
+ *     bit for bit (with rope = 1 and post-position keys, K is rotated by
+ *     position P_b + i first: each pair (x, y) becomes (x*c - y*s, x*s + y*c),
+ *     every product, sum and difference rounded to fp32, then rounded to the
+ *     cache type; c, s are the fp32 cos/sin of the table; pre-position keys
+ *     are stored as given); padding rows are never written ([P1] 2.6;
+ *     invariant 2.2 item 4);
  *  2. for every query head h and valid row i, with g(h) = floor(h*H_kv/H_q)
  *     ([P1] 2.3), the output is softmax over the finite scores
  *     <q[b,i,h], K[s, j, g(h)]> / sqrt(d_h), j = 0 .. P_b + i, applied to V
- *     (with rope = 1, q rotated by its position P_b + i): the old prefix is
+ *     (with rope = 1, q rotated by its position P_b + i, and pre-position
+ *     keys rotated by theirs, in fp32, as they are read): the old prefix is
  *     fully visible and the new block is lower-triangular ([P3] incremental
  *     prefill);
  *  3. padding rows i >= n_b of `out` are written as zeros (they are
@@ -257,6 +267,10 @@ int gqa_page_refcount(const gqa_cache *cache, int32_t page, int32_t *out);
  *  q              device [B, n, H_q, d_h]      (read)
  *  k, v           device [B, n, H_kv, d_h]     (read; post-position keys when
  *                 rope = 0, keys before the rotation when rope = 1)
+ * With every entry starting on a page boundary (P_b a multiple of 16), n a
+ * multiple of 8, a bf16 cache without rotation and d_h = 128, the cache
+ * write is part of the attention kernel (one launch); otherwise a write
+ * launch precedes it.  The results are the same bits either way.
  *  valid_lengths  host int32[B], 1 <= n_b <= n.
  *  positions      host int32[B, n] or NULL.  When given, positions[b, i]
  *                 must equal P_b + i for every valid row: positions continue
@@ -456,7 +470,8 @@ int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
 #define GQA_KERNEL_ATTN_SIMT       3  /* CUDA-core attention (fp32 / other d_h)   */
 #define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode (bf16, 128), merge included */
 #define GQA_KERNEL_DECODE_COMBINE  5  /* reserved: the merge runs inside the split kernel */
-#define GQA_KERNEL_COUNT           6
+#define GQA_KERNEL_ROTATE_PAGES    6  /* pre-position prefill: the call's pages, keys rotated */
+#define GQA_KERNEL_COUNT           7
 
 /* Turn per-launch timing on or off.  While on, every kernel launch of this
  * cache is bracketed by two CUDA events recorded on the launch's own stream.

@@ -250,6 +250,29 @@ def test_layout_metadata_and_compatibility():
     assert e.value.name == "ELAYOUT"
 
 
+def test_pre_position_layout_rules():
+    # Keys stored before the position transform ([P1] 2.5) need the
+    # library's own position mechanism to rotate them when read.
+    pre = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, rope=True, keys_post_position=0)
+    m = pre.layout()
+    assert m.keys_post_position == 0 and m.rope == 1
+    post = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, rope=True).layout()
+    assert post.keys_post_position == 1
+    # a post-position reader refuses a pre-position cache and the reverse
+    import ctypes
+    assert gqa._lib.gqa_layout_compatible(ctypes.byref(post), ctypes.byref(m)) == gqa.ELAYOUT
+    assert gqa._lib.gqa_layout_compatible(ctypes.byref(m), ctypes.byref(post)) == gqa.ELAYOUT
+    assert gqa.layout_compatible(m, pre.layout())
+    # without a position mechanism there is nothing to apply at read
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, keys_post_position=0)
+    assert e.value.name == "ELAYOUT"
+    # prefill, append and decode bookkeeping as for any cache
+    s = pre.seq_create()
+    gqa.attn_prefill_meta(pre, [s], 20, 4, [20])
+    assert pre.seq_length(s) == 20
+
+
 def test_rope_description_checks_and_layout():
     m = gqa.Cache(2, 8, 8, 2, 2, dtype="bf16", metadata_only=True, rope=True, rope_base=500.0).layout()
     assert m.rope == 1 and m.rope_base == 500.0
