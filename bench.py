@@ -5,15 +5,24 @@ on GB300, through the libgqa C ABI.
 Default line (one JSON object on stdout, rank 0):
   * main metric -- bf16 ragged prefill: B=4, H_q=32, H_kv=8, d_h=128, padded
     n=2048, valid lengths ~U{512..2048} (seeded), right padded, N(0,1) inputs.
-    One step = attn_prefill (host checks, cache write, causal attention,
-    zeroed padding rows) + kv_truncate of every sequence back to 0, so each
-    step starts from an empty cache.  L2 is flushed (512 MiB write) before
+    One step = attn_prefill (host checks, then one launch: causal attention
+    with the cache write fused and the padding rows zeroed) + kv_truncate of
+    every sequence back to 0, so each step starts from an empty cache.  L2 is flushed (512 MiB write) before
     every timed step; only the step is inside the CUDA events.
   * "decode" -- bf16 paged decode: B=64, H_q=32, H_kv=8, d_h=128, cache
     lengths ~U{1024..8192} including the step's own entry, pages placed by a
     seeded random permutation.  One step = attn_decode_append (one token
     per sequence appended and attended in one call) + kv_truncate back.  The 1.2 GB of K/V is larger
     than L2, so no flush is needed.
+  * "wide_gqa" -- B=1, H_q=48, H_kv=8, prefill T=8192 (TFLOP/s, roofline),
+    then 256 attn_decode_append steps: kernel time L2-resident, per-step time
+    with and without an L2 flush.
+  * "prefix_reuse" -- a 4096-token prefix shared by 8 forks, each prefilling
+    512 tokens over it; fork 0 edited at m=2000 (truncate + re-prefill).
+  (--no-extra skips the last two.)  Each object carries a roofline for its
+  dominant kernel and, on rank 0 at N=1, a bounded fp64-oracle sample.
+  "clocks" comes from nvidia-smi samples taken while the headline step runs
+  back to back for 0.6 s right after its event-timed region.
 Work counts: prefill flops = 4 d_h H_q sum_b causal_pairs; decode bytes =
 sum_b L_b * 2 * H_kv * d_h * 2 (each KV head read once).
 
@@ -160,7 +169,8 @@ class ClockSampler:
 
     def summary(self, t0, t1):
         rows = [r for t, r in self.rows if t0 <= t <= t1]
-        note = "samples inside the timed region"
+        note = ("samples during a back-to-back run of the timed step (with its L2 flush) for %.2f s right after "
+                "the event-timed region" % (t1 - t0))
         if len(rows) < 3:
             near = sorted(self.rows, key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))[:5]
             rows = [r for _, r in near]
@@ -220,6 +230,28 @@ def timed_steps(torch, dist, step, K, flush=None):
     return ms, t0, t1
 
 
+def sustain(torch, step, flush=None, seconds=0.6):
+    """Run the timed step back to back (with its flush) for at least
+    `seconds` of wall time, so that the clock sampler sees the GPU under this
+    load; returns (t0, t1, steps, median ms per step from events)."""
+    torch.cuda.synchronize()
+    t0 = time.time()
+    evs = []
+    while time.time() - t0 < seconds:
+        for _ in range(8):
+            if flush is not None:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            evs.append((a, b))
+        evs[-1][1].synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    return t0, t1, len(evs), statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
@@ -275,6 +307,10 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
     region_launches = cache.profile_read()            # launch counts of the timed region
     total_ms = dist.max(torch, sum(ms))
     value = flops * args.steps * dist.world / (total_ms / 1e3) / 1e12
+    median_ms = statistics.median(ms)
+    # The same step back to back for 0.6 s, for the clock record.
+    s0, s1, s_steps, s_med = sustain(torch, step, flush)
+    cache.profile_read()
     # Per-kernel durations: a second timed region with each launch bracketed
     # by events on its stream (events between kernels keep them from
     # overlapping, so this region is timed separately from the step).
@@ -335,9 +371,11 @@ def bench_prefill(torch, gqa, dist, args, peaks, peak_src):
                                      "read (CUDA-core kernels), queries in-kernel")
     if args.window:
         cfg["sliding_window"] = "W=%d: position p attends to keys max(0, p-W+1)..p; flops count those pairs" % args.window
-    return {"value": value, "ms_per_step": total_ms / args.steps, "roofline": roofline, "e2e": e2e,
-            "gpu_launches": gpu_launches, "kernels": kernels, "config": cfg, "t0": t0, "t1": t1, "device_error_flags": flags,
-            "workload": w}
+    return {"value": value, "ms_per_step": total_ms / args.steps, "ms_per_step_median": round(median_ms, 4),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "kernels": kernels, "config": cfg,
+            "t0": s0, "t1": s1, "sustain": {"steps": s_steps, "ms_per_step_median": round(s_med, 4),
+                                            "seconds": round(s1 - s0, 3)},
+            "timed_region_s": round(t1 - t0, 4), "device_error_flags": flags, "workload": w}
 
 
 def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
@@ -409,16 +447,17 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
                 "kernel_ms": round(avg_ms, 4), "algorithmic_bytes_per_launch": kv_bytes,
                 "peak_source": "%s HBM copy bandwidth" % peak_src}
 
+    # The same step back to back for 0.6 s, for the clock record.
+    s0, s1, s_steps, s_med = sustain(torch, step)
+    cache.profile_read()
+
+    # End to end through the public API: one attn_decode_append_host call
+    # per step (pinned host q, k, v up; the step; out back down).
     qh, kh, vh = pinned(torch, q), pinned(torch, new_k), pinned(torch, new_v)
     oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    qd, kd, vd, od = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v), torch.empty_like(out)
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        gqa.attn_decode_append(cache, ids, qd, kd, vd, out=od)
-        oh.copy_(od, non_blocking=True)
+        gqa.attn_decode_append_host(cache, ids, qh, kh, vh, out=oh)
         advance()
 
     for _ in range(2):
@@ -431,7 +470,11 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
            "ms_per_step": round(total_ms / args.steps, 4), "roofline": roofline,
            "e2e": {"value": round(e2e_bytes * dist.world / (e2e_total / 1e3) / 1e9, 1), "unit": "GB/s",
                    "h2d_bytes_per_step": int(q.nbytes + new_k.nbytes + new_v.nbytes),
-                   "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4)},
+                   "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": round(e2e_total / args.steps, 4),
+                   "how": "attn_decode_append_host (C ABI, pinned host buffers): q, k, v up, the fused step, out "
+                          "down, all on the caller's stream"},
+           "ms_per_step_median": round(statistics.median(ms), 4),
+           "sustain": {"steps": s_steps, "ms_per_step_median": round(s_med, 4), "seconds": round(s1 - s0, 3)},
            "gpu_launches": sum(nl for nl, _ in region_launches.values()),
            "kernels": {name: {"launches": nl, "avg_ms": round(ms / nl, 5)} for name, (nl, ms) in prof.items() if nl},
            "config": {"workload": "bf16 paged decode: B=%d, H_q=%d, H_kv=%d, d_h=%d, cache lengths ~U{1024..8192} "
@@ -473,7 +516,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     if not W and not q8:
         res["multi_token"] = bench_multi_token(torch, gqa, dist, args, peaks, peak_src, cache, ids, L, w)
     res["device_error_flags"] = cache.check()
-    res["t0"], res["t1"] = t0, t1
+    res["t0"], res["t1"] = s0, s1
     cache.close()
     return res
 
@@ -542,10 +585,37 @@ def tensor_roofline(flops, prof, peaks):
     avg = kms / max(1, nl)
     achieved = flops / (avg / 1e3) / 1e12
     return {"kernel": kernel, "kernel_ms": round(avg, 4), "achieved_tflops": round(achieved, 1),
-            "frac": round(achieved / peaks["bf16_tflops"], 4)}
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                         "kernel": kernel, "kernel_ms": round(avg, 4), "algorithmic_flops_per_launch": flops}}
 
 
-def bench_wide(torch, gqa, dist, args, peaks):
+def oracle_group_rate(q_bits, k_bits, v_bits, qpos, g, budget_s, what):
+    """The fp64 oracle on the host cores over KV group 0 (its g query heads)
+    of the given query rows, repeated until about budget_s seconds; causal
+    TFLOP/s counted as for the GPU (4 d_h per visible pair and head)."""
+    import oracle
+    nth = oracle.default_threads()
+    d = q_bits.shape[-1]
+    Q = oracle.to_f64(q_bits[:, :g], "bf16")
+    K = oracle.to_f64(k_bits[:, :1], "bf16")
+    V = oracle.to_f64(v_bits[:, :1], "bf16")
+    qpos = np.asarray(qpos)
+    flops = 4 * d * g * int(np.sum(qpos + 1))
+    used, reps = 0.0, 0
+    while used < budget_s:
+        t0 = time.perf_counter()
+        oracle.attention(Q, K, V, qpos, nthreads=nth)
+        used += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(flops * reps / used / 1e12, 4), "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+            "sample": "%s: KV group 0 (%d query heads), %d query rows at positions %d..%d, %d repetitions: %.2f "
+                      "GFLOP causal in %.1f s" % (what, g, len(qpos), qpos.min(), qpos.max(), reps,
+                                                 flops * reps / 1e9, used)}
+
+
+def bench_wide(torch, gqa, dist, args, peaks, want_cpu=False):
     """Wide-GQA long context: B=1, H_q=48, H_kv=8, prefill T=8192, then 256
     steps of attn_decode_append (L = 8193..8448)."""
     w = workloads.wide_gqa(workloads.seed_for(4))
@@ -570,6 +640,10 @@ def bench_wide(torch, gqa, dist, args, peaks):
     pre = {"tflops_step": round(flops * args.steps / (sum(ms) / 1e3) / 1e12, 1),
            "ms_per_step": round(sum(ms) / args.steps, 4), "gflop": round(flops / 1e9, 1)}
     pre.update(tensor_roofline(flops, profiled(torch, dist, c, pre_step, args.steps, flush), peaks))
+    if want_cpu:
+        rows = np.arange(T - 256, T)
+        pre["cpu_baseline"] = oracle_group_rate(w["q"][0, rows], w["k"][0], w["v"][0], rows, H_q // H_kv,
+                                                min(args.cpu_budget, 4.0), "fp64 oracle, wide-GQA prefill")
 
     gqa.attn_prefill(c, [s], q, k, v, [T], out=out)
     dq, dk, dv = to_dev(torch, w["dec_q"]), to_dev(torch, w["dec_k"]), to_dev(torch, w["dec_v"])
@@ -631,10 +705,16 @@ def bench_wide(torch, gqa, dist, args, peaks):
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+           "roofline": {"bound": "hbm", "achieved": round(kv_bytes / steps / (k_us / 1e6) / 1e9, 1),
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(kv_bytes / steps / (k_us / 1e6) / 1e9 / peaks["hbm_gbs"], 4), "traffic": None,
+                        "kernel": kname, "kernel_ms": round(k_us / 1e3, 5),
+                        "algorithmic_bytes_per_launch": kv_bytes // steps,
+                        "note": "kernel device time with the 34 MB of K/V L2-resident (steps queued ahead)"},
            "note": "one step = attn_decode_append of one sequence, called from Python: the step times "
                    "include the host side of the call, which is longer than the GPU work; 34 MB of K/V fits "
                    "in L2; kernel = device time of the decode launch alone (L2-resident), measured with the "
-                   "steps queued ahead of the GPU"}
+                   "steps queued ahead of the GPU; l2_flushed = each step after a 512 MiB L2 flush"}
     flags = c.check()
     c.close()
     return {"workload": "bf16 wide GQA: B=1, H_q=48, H_kv=8 (g=6), d_h=128, prefill T=%d, then %d append+decode "
@@ -642,7 +722,7 @@ def bench_wide(torch, gqa, dist, args, peaks):
             "prefill": pre, "decode": dec, "device_error_flags": flags}
 
 
-def bench_prefix(torch, gqa, dist, args, peaks):
+def bench_prefix(torch, gqa, dist, args, peaks, want_cpu=False):
     """Prefix reuse and edit: one 4096-token prefix, 8 forks each prefilling
     512 new tokens over it (P = 4096); fork 0 edited at m = 2000 (truncate +
     re-prefill of the 2608 following tokens)."""
@@ -672,6 +752,12 @@ def bench_prefix(torch, gqa, dist, args, peaks):
     inc = {"tflops_step": round(flops * args.steps / (sum(ms) / 1e3) / 1e12, 1),
            "ms_per_step": round(sum(ms) / args.steps, 4), "gflop": round(flops / 1e9, 1)}
     inc.update(tensor_roofline(flops, profiled(torch, dist, c, inc_step, args.steps, flush), peaks))
+    if want_cpu:
+        rows = P0 + np.arange(n_new)
+        inc["cpu_baseline"] = oracle_group_rate(w["new_q"][0], np.concatenate([w["pre_k"][0], w["new_k"][0]]),
+                                                np.concatenate([w["pre_v"][0], w["new_v"][0]]), rows,
+                                                H_q // H_kv, min(args.cpu_budget, 3.0),
+                                                "fp64 oracle, fork 0's incremental prefill")
 
     gqa.attn_prefill(c, forks, nq, nk, nv, [n_new] * B, out=out)
     n_re = P0 + n_new - m
@@ -768,14 +854,15 @@ def main():
                     help="decode cache type (fp8: FP8 E4M3 codes with per-row scales; decode only)")
     ap.add_argument("--window", type=int, default=0,
                     help="caches with a sliding window of this many tokens (0 = none)")
-    ap.add_argument("--extra", action="store_true",
-                    help="also time the wide-GQA long-context and prefix-reuse/edit workloads")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the wide-GQA long-context and prefix-reuse/edit workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of fp64 oracle work per CPU baseline (rank 0, N=1)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.pre_position and not args.rope:
         ap.error("--pre-position needs --rope (the cache rotates the keys it stores before the rotation)")
+    args.extra = not args.no_extra
     if args.kv == "fp8":
         args.no_prefill = True               # the quantised cache is measured on decode
         args.extra = False
@@ -788,12 +875,16 @@ def main():
     dist.setup(torch)
     peaks, peak_src = load_peaks()
     clocks = ClockSampler(device_uuid(torch)) if dist.rank == 0 else None
+    want_cpu = dist.rank == 0 and dist.world == 1 and not args.no_cpu
+    wide = prefix = None
     try:
         time.sleep(0.3 if clocks else 0)
         pre = None if args.no_prefill else bench_prefill(torch, gqa, dist, args, peaks, peak_src)
-        dec = None if args.no_decode else bench_decode(torch, gqa, dist, args, peaks, peak_src,
-                                                       want_cpu=(dist.rank == 0 and dist.world == 1
-                                                                 and not args.no_cpu))
+        dec = None if args.no_decode else bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu=want_cpu)
+        # Every rank runs the replicas (the timed regions have barriers).
+        if pre is not None and args.extra:
+            wide = bench_wide(torch, gqa, dist, args, peaks, want_cpu)
+            prefix = bench_prefix(torch, gqa, dist, args, peaks, want_cpu)
     finally:
         if clocks:
             clocks.stop()
@@ -805,17 +896,22 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(pre["ms_per_step"], 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic", "config": pre["config"], "roofline": pre["roofline"], "e2e": pre["e2e"],
+                "ms_per_step_median": pre["ms_per_step_median"],
                 "gpu_launches": pre["gpu_launches"], "kernels": pre["kernels"],
-                "clocks": clocks.summary(pre["t0"], pre["t1"]),
+                "clocks": clocks.summary(pre["t0"], pre["t1"]), "sustain": pre["sustain"],
+                "timed_region_s": pre["timed_region_s"],
                 "device_error_flags": pre["device_error_flags"]}
+        if line["clocks"].get("sm_mhz"):
+            # time x clock: the step's cost in clock cycles, comparable across clocks
+            line["clocks"]["ms_per_step_x_ghz"] = round(pre["ms_per_step"] * line["clocks"]["sm_mhz"] / 1e3, 5)
         if not args.no_cpu and dist.world == 1:
             line["cpu_baseline"] = prefill_cpu_baseline(pre["workload"], args.cpu_budget)
         if dec is not None:
             dec["clocks"] = clocks.summary(dec.pop("t0"), dec.pop("t1"))
             line["decode"] = dec
-        if args.extra:
-            line["wide_gqa"] = bench_wide(torch, gqa, dist, args, peaks)
-            line["prefix_reuse"] = bench_prefix(torch, gqa, dist, args, peaks)
+        if wide is not None:
+            line["wide_gqa"] = wide
+            line["prefix_reuse"] = prefix
         print(json.dumps(line))
     dist.done()
     return 0

@@ -84,6 +84,7 @@ _sig("kv_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _I32P, _vp, _vp, _vp)
 _sig("attn_decode", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_static", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("attn_decode_append", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp, _vp, _vp)
+_sig("attn_decode_append_host", ctypes.c_int, _vp, _i32, _I32P, _i32, _vp, _vp, _vp, _vp, _vp)
 _sig("attn_decode_tables", ctypes.c_int, _vp, _i32, _vp, _i32, _I32P, _i32, _vp, _vp, _vp)
 _sig("kv_truncate", ctypes.c_int, _vp, _i32, _i32)
 _sig("gqa_cache_check", ctypes.c_int, _vp, _vp, _I32P)
@@ -444,6 +445,24 @@ def attn_decode_append(cache: Cache, seq_ids, q, k_new, v_new, out=None, stream=
     return out
 
 
+def attn_decode_append_host(cache: Cache, seq_ids, q, k_new, v_new, out=None, stream=None):
+    """attn_decode_append on host tensors (see include/gqa.h): q [B, H_q, d],
+    k_new/v_new [B, H_kv, d] on the CPU (pinned for asynchronous copies);
+    returns out [B, H_q, d] on the CPU (allocated like q if not given),
+    complete once `stream` (default: the current stream) is synchronised."""
+    B, H_q = len(seq_ids), q.shape[1]
+    dt, d, H_kv = cache.torch_dtype, cache.head_dim, cache.num_kv_heads
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    keep_s, sp = _i32_array(seq_ids)
+    _check(_lib.attn_decode_append_host(cache.handle, B, sp, H_q, _host_ptr(q, "q", dt, (B, H_q, d)),
+                                        _host_ptr(k_new, "k_new", dt, (B, H_kv, d)),
+                                        _host_ptr(v_new, "v_new", dt, (B, H_kv, d)),
+                                        _host_ptr(out, "out", dt, (B, H_q, d)),
+                                        _stream_handle(stream, cache.device_index)))
+    return out
+
+
 def attn_decode_append_meta(cache: Cache, seq_ids, H_q):
     keep_s, sp = _i32_array(seq_ids)
     _check(_lib.attn_decode_append(cache.handle, len(seq_ids), sp, H_q, None, None, None, None, None))
@@ -479,4 +498,5 @@ def exported_symbols():
             "gqa_seq_length", "gqa_seq_block_table", "gqa_free_pages", "gqa_page_refcount",
             "attn_prefill", "kv_append", "attn_decode", "attn_decode_static", "kv_truncate", "gqa_cache_check",
             "gqa_profile_enable", "gqa_profile_read", "gqa_last_error", "gqa_version", "gqa_set_decode_kernel",
-            "attn_decode_append", "gqa_selftest_bounded_wait", "attn_decode_tables", "attn_prefill_host"]
+            "attn_decode_append", "gqa_selftest_bounded_wait", "attn_decode_tables", "attn_prefill_host",
+            "attn_decode_append_host"]

@@ -46,6 +46,10 @@ constexpr int64_t kItemCostQuarters = 2;
 #endif
 constexpr int kSplitItemsPerSm = GQA_SPLIT_ITEMS_PER_SM;   // tensor-core split items: target per SM
 constexpr int kSplitMinTiles = GQA_SPLIT_MIN_TILES;         // and the shortest piece, in key tiles
+// attn_decode_static: descriptors at most 1 MiB, block-table entries at most
+// 1 MiB; each of the two page-locked staging slots holds both.
+constexpr size_t kStaticDescBytes = 1u << 20;
+constexpr size_t kStaticStageBytes = 2u << 20;
 
 int fail(int code, const char *fmt, ...)
 {
@@ -93,6 +97,12 @@ struct gqa_cache {
     size_t stage_cap = 0;
     float *d_ws = nullptr;               // decode split partials
     size_t ws_cap = 0;
+    // attn_decode_static: page-locked staging for its descriptors and block
+    // tables, reserved at creation (two slots used in turn; a slot's event
+    // marks the end of the copies that last read it).
+    char *h_pin = nullptr;
+    cudaEvent_t pin_done[2] = {nullptr, nullptr};
+    int pin_next = 0;
     char *d_rot = nullptr;               // pre-position prefill: the call's pages with rotated keys
     size_t rot_cap = 0;
     std::vector<int32_t> rot_slot;       // scratch slot of a pool page during one call (-1 = none)
@@ -282,11 +292,35 @@ int check_device(const gqa_cache *c)
     return GQA_OK;
 }
 
+// Copy `bytes` from host memory to device `dst` on `st` through the cache's
+// page-locked staging slots (taken in turn, at most kStaticStageBytes a
+// piece); before reusing a slot it waits for the copies that last read it.
+// Allocates nothing.
+int staged_copy(gqa_cache *c, void *dst, const void *src, size_t bytes, cudaStream_t st)
+{
+    for (size_t off = 0; off < bytes;) {
+        const size_t piece = std::min(bytes - off, kStaticStageBytes);
+        const int slot = c->pin_next;
+        c->pin_next ^= 1;
+        cudaError_t e = cudaEventSynchronize(c->pin_done[slot]);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "staging slot wait");
+        char *h = c->h_pin + (size_t)slot * kStaticStageBytes;
+        memcpy(h, (const char *)src + off, piece);
+        if ((e = cudaMemcpyAsync((char *)dst + off, h, piece, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+            (e = cudaEventRecord(c->pin_done[slot], st)) != cudaSuccess)
+            return cuda_fail(e, "staged upload");
+        off += piece;
+    }
+    return GQA_OK;
+}
+
 // Upload the block-table entries changed since the last upload: one copy of
 // the span of the flat table that covers every dirty entry (rows are
 // contiguous, and clean entries in between equal the device's), so a call
-// pays one copy however many sequences it touched.
-int upload_tables(gqa_cache *c, cudaStream_t st)
+// pays one copy however many sequences it touched.  staged: through the
+// page-locked staging slots (attn_decode_static).
+int upload_tables(gqa_cache *c, cudaStream_t st, bool staged = false)
 {
     size_t lo = SIZE_MAX, hi = 0;
     for (int32_t s : c->dirty_list) {
@@ -299,6 +333,8 @@ int upload_tables(gqa_cache *c, cudaStream_t st)
         S.dirty_hi = 0;
     }
     c->dirty_list.clear();
+    if (hi > lo && staged)
+        return staged_copy(c, c->d_tab + lo, c->h_tab.data() + lo, (hi - lo) * sizeof(int32_t), st);
     if (hi > lo) {
         cudaError_t e = cudaMemcpyAsync(c->d_tab + lo, c->h_tab.data() + lo, (hi - lo) * sizeof(int32_t),
                                         cudaMemcpyHostToDevice, st);
@@ -563,6 +599,10 @@ int gqa_cache_create(const gqa_cache_desc *desc, void *pool_dev, size_t pool_byt
         if (e == cudaSuccess)
             e = cudaMalloc((void **)&c->d_err, sizeof(int32_t));
         if (e == cudaSuccess)
+            e = cudaHostAlloc((void **)&c->h_pin, 2 * kStaticStageBytes, cudaHostAllocDefault);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+            e = cudaEventCreateWithFlags(&c->pin_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess)
             e = cudaMemset(c->d_err, 0, sizeof(int32_t));
         if (e == cudaSuccess)
             e = cudaMemset(pool_dev, 0, need);         // every slot starts as a finite +0
@@ -607,6 +647,9 @@ int gqa_cache_destroy(gqa_cache *c)
         if (c->d_stage) cudaFree(c->d_stage);
         if (c->d_ws) cudaFree(c->d_ws);
         if (c->d_rot) cudaFree(c->d_rot);
+        if (c->h_pin) cudaFreeHost(c->h_pin);
+        for (cudaEvent_t ev : c->pin_done)
+            if (ev) cudaEventDestroy(ev);
         if (c->d_cnt) cudaFree(c->d_cnt);
         if (c->d_rope) cudaFree(c->d_rope);
         if (c->d_io) cudaFree(c->d_io);
@@ -1545,6 +1588,50 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     return rc;
 }
 
+int attn_decode_append_host(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t H_q, const void *q,
+                            const void *k_new, const void *v_new, void *out, void *stream)
+{
+    // The checks of attn_decode_append first, so a rejected call queues and
+    // changes nothing.
+    if (!c || !seq_ids)
+        return fail(GQA_EINVAL, "NULL argument");
+    if (B < 1 || H_q < 1)
+        return fail(GQA_EINVAL, "B and H_q must be >= 1");
+    const int32_t H_kv = c->desc.num_kv_heads;
+    if (H_q % H_kv != 0)
+        return fail(GQA_EINVAL, "H_kv = %d does not divide H_q = %d", H_kv, H_q);
+    if (c->meta_only)
+        return attn_decode_append(c, B, seq_ids, H_q, nullptr, nullptr, nullptr, nullptr, stream);
+    if (!q || !k_new || !v_new || !out)
+        return fail(GQA_EINVAL, "NULL buffer");
+    if (decode_uses_tc(c, H_q / H_kv) < 0)
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys "
+                                "and H_q/H_kv <= 128");
+    std::vector<WriteReq> req(B);
+    for (int b = 0; b < B; ++b)
+        req[b] = WriteReq{seq_ids[b], 1};
+    int rc = check_write(c, req.data(), B);
+    if (rc != GQA_OK || (rc = check_device(c)) != GQA_OK)
+        return rc;
+    const size_t es = (size_t)c->io_esize, d = (size_t)c->desc.head_dim;
+    const size_t bq = (size_t)B * H_q * d * es, bkv = (size_t)B * H_kv * d * es;
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    if ((rc = ensure_io(c, 2 * al(bq) + 2 * al(bkv), 2)) != GQA_OK)
+        return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *dq = c->d_io, *dk = dq + al(bq), *dv = dk + al(bkv), *dout = dv + al(bkv);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(dq, q, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk, k_new, bkv, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv, v_new, bkv, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(e, "host-call upload");
+    if ((rc = attn_decode_append(c, B, seq_ids, H_q, dq, dk, dv, dout, stream)) != GQA_OK)
+        return rc;
+    if ((e = cudaMemcpyAsync(out, dout, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e, "host-call download");
+    return GQA_OK;
+}
+
 int gqa_selftest_bounded_wait(gqa_cache *c, int64_t limit_ns, void *stream)
 {
     if (!c)
@@ -1623,7 +1710,6 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[GQA_STATIC_SCRATCH_BYTES];
 
-constexpr size_t kStaticDescBytes = 1u << 20;      // descriptors
 constexpr size_t kStaticCntBytes = 64u << 10;       // merge counters; the rest holds partials
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
@@ -1663,11 +1749,12 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     const int G = H_q / H_kv;
     const int use_tc = decode_uses_tc(c, G);
     if (use_tc < 0)
-        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
+        return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys "
+                                "and H_q/H_kv <= 128");
     if (!use_tc && ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) ||
                     c->desc.head_dim != 128 || !decode_split_supported(G)))
-        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 cache with d_h = 128 (and H_q/H_kv <= 8 on the "
-                                "CUDA-core kernel)");
+        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 or FP8 E4M3 cache with d_h = 128 (and H_q/H_kv <= "
+                                "8 on the CUDA-core kernel)");
     if (c->meta_only)
         return fail(GQA_EINVAL, "attn_decode_static needs a cache with a device pool");
     if (!q || !out)
@@ -1688,6 +1775,7 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     if (rc != GQA_OK)
         return rc;
     cudaStream_t st = (cudaStream_t)stream;
+    const size_t part_bytes = GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes;
 
     if (use_tc) {
         // The plan of attn_decode (so the results are the same bits), with
@@ -1700,7 +1788,6 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         const size_t o_items = stg.add(plan.items.data(), plan.items.size());
         const size_t o_start = stg.add(plan.item_start.data(), plan.item_start.size());
         const size_t rows = (size_t)plan.slots * plan.slot_rows;
-        const size_t part_bytes = GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes;
         if (desc.size() > kStaticDescBytes)
             return fail(GQA_ERANGE, "decode descriptors need %zu bytes; the static scratch reserves %zu",
                         desc.size(), kStaticDescBytes);
@@ -1713,12 +1800,10 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         char *scratch = nullptr;
         if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
             return rc;
-        if ((rc = upload_tables(c, st)) != GQA_OK)
+        if ((rc = upload_tables(c, st, true)) != GQA_OK || (rc = staged_copy(c, scratch, desc.data(), desc.size(), st)) != GQA_OK)
             return rc;
-        cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "descriptor upload (static scratch)");
         int32_t *counters = (int32_t *)(scratch + kStaticDescBytes);
+        cudaError_t e;
         if (plan.slots > 0 && (e = cudaMemsetAsync(counters, 0, (size_t)plan.slots * sizeof(int32_t), st)) !=
                                   cudaSuccess)
             return cuda_fail(e, "counter clear (static scratch)");
@@ -1728,39 +1813,25 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         ws.counters = counters;
         ws.slot_rows = plan.slot_rows;
         ws.ranged = plan.ranged;
-        e = launch_prefill_tc(c->view(), (const SeqDesc *)(scratch + o_sds), (const TcItem *)(scratch + o_items),
-                              (const int32_t *)(scratch + o_start), plan.grid, B, 1, H_q, q, out, ws, st);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "tensor-core decode kernel (static scratch)");
-        c->launches[GQA_KERNEL_PREFILL_TC] += 1;
-        return GQA_OK;
+        const PoolView pv = c->view();
+        return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core decode kernel (static scratch)",
+                          [&](cudaEvent_t ev) {
+                              return launch_prefill_tc(pv, (const SeqDesc *)(scratch + o_sds),
+                                                       (const TcItem *)(scratch + o_items),
+                                                       (const int32_t *)(scratch + o_start), plan.grid, B, 1, H_q, q,
+                                                       out, ws, st, ev);
+                          });
     }
 
-    // Same chunk rule as attn_decode, widened (up to 512 tokens) until the
-    // partials fit in the static array.
-    const size_t part_cap = (GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes) / sizeof(float);
+    // The chunk rule of attn_decode (the same work split, so the same bits);
+    // a call whose partials do not fit the array is refused.
     if ((size_t)B * H_kv * sizeof(int32_t) > kStaticCntBytes)
         return fail(GQA_ERANGE, "B * H_kv = %lld merge counters exceed the static scratch's %zu",
                     (long long)B * H_kv, kStaticCntBytes / sizeof(int32_t));
-    int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
-    int chunk = (int)std::min<int64_t>(512, std::max<int64_t>(128, (target + 127) / 128 * 128));
-    size_t n_items = 0;
-    for (;;) {
-        n_items = 0;
-        for (int b = 0; b < B; ++b)
-            n_items += (size_t)((sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window) + chunk - 1) /
-                                chunk);
-        if (n_items * (size_t)H_kv * G * 130 <= part_cap || chunk >= 512)
-            break;
-        chunk = std::min(512, chunk * 2);
-    }
-    const size_t n_part = n_items * (size_t)H_kv * G;
-    if (n_part * 130 > part_cap)
-        return fail(GQA_ERANGE, "decode partials need %zu bytes; the static scratch holds %zu",
-                    n_part * 130 * sizeof(float), part_cap * sizeof(float));
+    const int64_t target = total * H_kv / (int64_t)std::max(1, c->num_sms * 4);
+    const int chunk = (int)std::min<int64_t>(512, std::max<int64_t>(128, (target + 127) / 128 * 128));
     std::vector<DecodeItem> items;
     std::vector<int32_t> start(B + 1, 0);
-    items.reserve(n_items);
     for (int b = 0; b < B; ++b) {
         const int32_t ns =
             (sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window) + chunk - 1) / chunk;
@@ -1769,6 +1840,10 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
             items.push_back(DecodeItem{b, s});
     }
     start[B] = (int32_t)items.size();
+    const size_t n_part = items.size() * (size_t)H_kv * G;
+    if (n_part * 130 * sizeof(float) > part_bytes)
+        return fail(GQA_ERANGE, "decode partials need %zu bytes; the static scratch holds %zu",
+                    n_part * 130 * sizeof(float), part_bytes);
     std::vector<char> desc;
     Stage stg(desc);
     const size_t o_sds = stg.add(sds.data(), sds.size());
@@ -1781,14 +1856,11 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     char *scratch = nullptr;
     if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
         return rc;
-    if ((rc = upload_tables(c, st)) != GQA_OK)
+    if ((rc = upload_tables(c, st, true)) != GQA_OK || (rc = staged_copy(c, scratch, desc.data(), desc.size(), st)) != GQA_OK)
         return rc;
-    cudaError_t e = cudaMemcpyAsync(scratch, desc.data(), desc.size(), cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "descriptor upload (static scratch)");
     // The merge counters must start at zero: clear the ones this call uses.
     int32_t *counters = (int32_t *)(scratch + kStaticDescBytes);
-    e = cudaMemsetAsync(counters, 0, (size_t)B * H_kv * sizeof(int32_t), st);
+    cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)B * H_kv * sizeof(int32_t), st);
     if (e != cudaSuccess)
         return cuda_fail(e, "counter clear (static scratch)");
     DecodeLaunch a;
@@ -1804,11 +1876,10 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     a.counters = counters;
     a.out = out;
     const PoolView pv = c->view();
-    e = launch_decode_split(pv, a, st);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode kernel (static scratch)");
-    c->launches[GQA_KERNEL_DECODE_SPLIT] += 1;
-    return GQA_OK;
+    return run_kernel(c, GQA_KERNEL_DECODE_SPLIT, st, "decode kernel (static scratch)", [&](cudaEvent_t ev) {
+        rec(ev, st);
+        return launch_decode_split(pv, a, st);
+    });
 }
 
 extern "C" {

@@ -184,7 +184,9 @@ size_t gqa_pool_bytes(const gqa_cache_desc *desc);
  * exercised without a GPU.
  * With rope = 1 the library also allocates a cos/sin table of
  * max_pages_per_seq * 16 positions x d_h/2 frequencies (fp32, computed in
- * fp64 on the host).
+ * fp64 on the host).  It also reserves 4 MiB of page-locked host memory
+ * (cudaHostAlloc) through which attn_decode_static uploads its descriptors
+ * and block tables.
  * Errors: GQA_EINVAL (bad description, pool too small, misaligned; rope not
  *         0/1, or rope = 1 with an odd d_h or rope_base <= 1; FP8_E4M3 with
  *         d_h not a multiple of 32 or with rope = 1),
@@ -383,6 +385,21 @@ int attn_decode_tables(gqa_cache *cache, int32_t B, const int32_t *block_table_d
 int attn_decode_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
                        const void *q, const void *k_new, const void *v_new, void *out, void *stream);
 
+/* attn_decode_append on HOST buffers: one decode step with the transfers
+ * inside the call.  The checks of attn_decode_append come first (nothing is
+ * queued or changed when one fails); then q, k_new and v_new are copied to
+ * library-owned device memory on `stream`, the step runs as
+ * attn_decode_append, and out is copied back on `stream`.  out is complete
+ * once `stream` is synchronised; the host buffers must stay valid until
+ * then.  Page-locked buffers make the copies asynchronous.
+ *  q        host [B, H_q, d_h];  k_new, v_new  host [B, H_kv, d_h];
+ *  out      host [B, H_q, d_h] (written).
+ * Calls on one cache must be ordered on one stream (the device copies are
+ * reused by the next call); the device memory grows on demand.
+ * Errors: those of attn_decode_append. */
+int attn_decode_append_host(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int32_t H_q,
+                            const void *q, const void *k_new, const void *v_new, void *out, void *stream);
+
 /* attn_decode_static -- attn_decode that allocates no device memory.
  *
  * The pages define no counterpart to this call.  It is for callers that must
@@ -394,13 +411,19 @@ int attn_decode_append(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
  *
  * Arguments, results and errors are those of attn_decode, and so are the
  * kernel and its work split: the results are the same bits.  The cache must
- * be bf16 with d_h = 128 (and H_q / H_kv at most 8 on the CUDA-core kernel);
- * other shapes get GQA_EINVAL.
+ * be bf16 or FP8 E4M3 with d_h = 128 (and H_q / H_kv at most 8 on the
+ * CUDA-core kernel); other shapes get GQA_EINVAL.
  * The split-K partials, the per-call descriptors and the merge counters live
  * in one static device array of GQA_STATIC_SCRATCH_BYTES.  The library reserves that array
  * on every GPU that loads it, until the process exits.  A call whose partials
- * or descriptors would not fit returns GQA_ERANGE with the bytes it needed.
- * No cudaMalloc, cudaFree or other allocating routine is called.
+ * or descriptors would not fit returns GQA_ERANGE with the bytes it needed
+ * and queues nothing (the work split is never changed to make it fit).
+ * No cudaMalloc, cudaFree or other allocating routine is called.  The
+ * descriptors and the changed block-table entries are copied into one of
+ * two page-locked host slots that the cache reserved when it was created,
+ * and uploaded from there on `stream`.  Before reusing a slot, the call waits
+ * on the host until the copies that last read it have finished, which
+ * happens only when the host is two calls ahead of the GPU.
  * On each device, the first call looks up the array's device address
  * (cudaGetSymbolAddress).  Make that first call before any stream capture.
  * Every call shares the one array, and the array keeps the last call's

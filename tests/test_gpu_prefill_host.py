@@ -1,9 +1,10 @@
-"""GPU parity of attn_prefill_host: the prefill on host buffers, its copies
-inside the call.  The batch is checked as a whole, then each entry runs as a
+"""GPU parity of the host-buffer entry points.  attn_prefill_host: the prefill
+on host buffers, its copies inside the call.  The batch is checked as a whole, then each entry runs as a
 one-entry prefill, longest valid length first (ties in batch order), so the
 oracle's cache model takes its pages in that order.  Outputs within the
 declared tolerance of the oracle, cache bytes and tables exact, output rows
-past an entry's valid length left untouched."""
+past an entry's valid length left untouched.  attn_decode_append_host: one
+decode step on host buffers, the same bits as the device-buffer step."""
 import numpy as np
 import pytest
 import torch
@@ -117,3 +118,56 @@ def test_host_buffer_prefill_rejection_queues_nothing():
     assert np.all(out.view(torch.int16).numpy() == 0)
     with pytest.raises(TypeError):
         gqa.attn_prefill_host(c, ids, dev(w["q"], "bf16"), _host(w["k"], "bf16"), _host(w["v"], "bf16"), [1, 1])
+
+
+# ---- attn_decode_append_host: one decode step on host buffers --------------
+
+@pytest.mark.parametrize("dt,d,pinned", [("bf16", 128, True), ("bf16", 128, False), ("f32", 64, True)])
+def test_host_buffer_decode_step_equals_device_step(dt, d, pinned):
+    # The same step through device buffers and through host buffers gives
+    # the same bits in out and in the pool, and matches the oracle.
+    rng = np.random.default_rng(900 + d)
+    B, H_q, H_kv = 5, 16, 4
+    lengths = [1, 15, 16, 200, 1030]
+    per_seq = workloads.pages_for(max(lengths) + 4) + 1
+    pages = B * per_seq
+    caches = [gqa.Cache(H_kv, d, pages, B, per_seq, dtype=dt) for _ in range(2)]
+    m = oracle.CacheModel(pages, B, per_seq, H_kv, d, dt)
+    ids = [[c.seq_create() for _ in range(B)] for c in caches]
+    mids = [m.create() for _ in range(B)]
+    n = max(lengths)
+    k = np.zeros((B, n, H_kv, d), np.uint16 if dt == "bf16" else np.float32)
+    v = np.zeros_like(k)
+    for b, L in enumerate(lengths):
+        k[b, :L] = workloads.draw(rng, dt, (L, H_kv, d))
+        v[b, :L] = workloads.draw(rng, dt, (L, H_kv, d))
+    for c, s in zip(caches, ids):
+        gqa.kv_append(c, s, dev(k, dt), dev(v, dt), counts=lengths)
+    oracle.append(m, mids, k, v, counts=lengths)
+    for step in range(2):
+        q, kn, vn = (workloads.draw(rng, dt, (B, H, d)) for H in (H_q, H_kv, H_kv))
+        a = gqa.attn_decode_append(caches[0], ids[0], dev(q, dt), dev(kn, dt), dev(vn, dt))
+        b = gqa.attn_decode_append_host(caches[1], ids[1], _host(q, dt, pinned), _host(kn, dt, pinned),
+                                        _host(vn, dt, pinned))
+        torch.cuda.synchronize()
+        av = a.cpu().view(torch.int32 if dt == "f32" else torch.int16)
+        bv = b.view(torch.int32 if dt == "f32" else torch.int16)
+        assert torch.equal(av, bv), "host-buffer step differs from the device step"
+        oracle.append(m, mids, kn, vn)
+        assert_close(_f64(b, dt), oracle.decode(m, mids, q), dt, "host-buffer decode step %d" % step)
+    for c, s in zip(caches, ids):
+        assert_cache_matches(c, m, zip(s, mids))
+        assert c.check() == 0
+
+
+def test_host_buffer_decode_step_rejection_changes_nothing():
+    c = gqa.Cache(2, 128, 8, 2, 4, dtype="bf16")
+    s = c.seq_create()
+    q = torch.zeros((2, 8, 128), dtype=torch.bfloat16)
+    kv = torch.zeros((2, 2, 128), dtype=torch.bfloat16)
+    out = torch.full((2, 8, 128), 5.0, dtype=torch.bfloat16)
+    with pytest.raises(gqa.GqaError) as e:
+        gqa.attn_decode_append_host(c, [s, 7], q, kv, kv, out=out)    # sequence 7 is not live
+    assert e.value.name == "EINVAL"
+    torch.cuda.synchronize()
+    assert c.seq_length(s) == 0 and bool((out == 5.0).all())
