@@ -1011,85 +1011,78 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 named_bar_sync(1 + t, 128);
                 if (s.last_) {
                     // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max_s m_s (a
-                    // split without a visible key for a row has m = -inf, l = 0).  Per
-                    // row M and 1 / sum, and the weights 2^(m_s - M) / sum into this
-                    // warpgroup's staging buffer when they fit; then one thread per
-                    // column, up to 16 rows at a time, so that its loads of all the
-                    // rows and of several splits are in flight together.
+                    // split without a visible key for a row has m = -inf, l = 0).  The
+                    // merge is a chain of loads from L2, kept short: each thread first
+                    // issues the loads of its first two rows' partial columns over
+                    // eight splits, then every (m, l) pair of the group goes to this
+                    // warpgroup's staging buffer in one round; per row M and 1 / sum
+                    // come from there, and the weights 2^(m_s - M) / sum are formed as
+                    // the columns are summed, eight splits and two rows per round.
                     __threadfence();
                     const int rows = min(p.slot_rows, sd.count * p.G);
                     const int nsp = it.nsplit;
                     const float2 *ml = p.ws_ml + (size_t)first * p.slot_rows;
-                    if (r < rows) {
-                        // Sixteen (m, l) pairs per round, all loads in flight.
-                        float M = -INFINITY;
-                        for (int q0 = 0; q0 < nsp; q0 += 16) {
-                            float2 v2[16];
+                    float2 *sml = reinterpret_cast<float2 *>(s.o[t]);   // (m, l) of split q, row rr at q * rows + rr
+                    const bool fit = nsp * rows <= (int)(sizeof(s.o[0]) / sizeof(float2));
+                    auto ml_at = [&](int q2, int rr) {
+                        return fit ? sml[q2 * rows + rr] : __ldcg(ml + (size_t)q2 * p.slot_rows + rr);
+                    };
+                    // Thread r: columns 4 * (r % 32) .. + 3 of rows r / 32 and r / 32 + 4,
+                    // then + 8, ...
+                    const int c4 = r & 31, sub = r >> 5;
+                    const float4 *o4 = reinterpret_cast<const float4 *>(p.ws_o) + c4;
+                    float4 va[8], vb[8];
+                    auto load8 = [&](int q0, int ra, int rb) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v2[i] = q0 + i < nsp ? __ldcg(ml + (size_t)(q0 + i) * p.slot_rows + r)
-                                                     : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                M = fmaxf(M, v2[i].x);
+                        for (int i = 0; i < 8; ++i) {
+                            const size_t sl = (size_t)(first + q0 + i) * p.slot_rows;
+                            va[i] = q0 + i < nsp && ra < rows ? __ldcg(o4 + (sl + ra) * (D / 4))
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                            vb[i] = q0 + i < nsp && rb < rows ? __ldcg(o4 + (sl + rb) * (D / 4))
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
+                    };
+                    load8(0, sub, sub + 4);                  // in flight over the (m, l) round below
+                    if (r == 0)
+                        tma_store_wait_read();               // earlier stores have left the buffer
+                    named_bar_sync(1 + t, 128);
+                    if (fit)
+                        for (int f = r; f < nsp * rows; f += 128) {
+                            const int q2 = f / rows, rr = f - q2 * rows;
+                            sml[f] = __ldcg(ml + (size_t)q2 * p.slot_rows + rr);
+                        }
+                    named_bar_sync(1 + t, 128);
+                    if (r < rows) {
+                        float M = -INFINITY;
+                        for (int q2 = 0; q2 < nsp; ++q2)
+                            M = fmaxf(M, ml_at(q2, r).x);
                         if (M == -INFINITY)                  // no visible key at all: zeros, not NaN
                             M = 0.0f;
                         float Lsum = 0.0f;
-                        for (int q0 = 0; q0 < nsp; q0 += 16) {
-                            float2 v2[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v2[i] = q0 + i < nsp ? __ldcg(ml + (size_t)(q0 + i) * p.slot_rows + r)
-                                                     : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                Lsum += ex2(v2[i].x - M) * v2[i].y;
+                        for (int q2 = 0; q2 < nsp; ++q2) {
+                            const float2 v2 = ml_at(q2, r);
+                            Lsum += ex2(v2.x - M) * v2.y;
                         }
                         s.mrg_m[r] = M;
                         s.mrg_inv[r] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
                     }
-                    float *wsm = reinterpret_cast<float *>(s.o[t]);
-                    const bool wfit = nsp * rows <= (int)(sizeof(s.o[0]) / sizeof(float));
-                    if (r == 0)
-                        tma_store_wait_read();               // earlier stores have left the buffer
                     named_bar_sync(1 + t, 128);
-                    if (wfit)
-                        for (int f = r; f < nsp * rows; f += 128) {
-                            const int q2 = f / rows, rr = f - q2 * rows;
-                            wsm[f] = ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rr).x - s.mrg_m[rr]) * s.mrg_inv[rr];
-                        }
-                    named_bar_sync(1 + t, 128);
-                    // Thread r: columns 4 * (r % 32) .. + 3 of rows r / 32, + 4, + 8, ...,
-                    // two rows and eight splits per round (16 loads of 16 bytes in flight).
-                    const int c4 = r & 31, sub = r >> 5;
-                    const float4 *o4 = reinterpret_cast<const float4 *>(p.ws_o) + c4;
                     for (int ra = sub; ra < rows; ra += 8) {
                         const int rb = ra + 4;                  // second row of the pair (if < rows)
                         float4 acc_a = make_float4(0.f, 0.f, 0.f, 0.f), acc_b = acc_a;
                         for (int q0 = 0; q0 < nsp; q0 += 8) {
-                            float4 va[8], vb[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const size_t sl = (size_t)(first + q0 + i) * p.slot_rows;
-                                va[i] = q0 + i < nsp ? __ldcg(o4 + (sl + ra) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                vb[i] = q0 + i < nsp && rb < rows ? __ldcg(o4 + (sl + rb) * (D / 4))
-                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
+                            if (ra != sub || q0 != 0)            // the first round is already in flight
+                                load8(q0, ra, rb);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 if (q0 + i >= nsp)
                                     break;
                                 const int q2 = q0 + i;
-                                const float wa = wfit ? wsm[q2 * rows + ra]
-                                                      : ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + ra).x - s.mrg_m[ra]) *
-                                                            s.mrg_inv[ra];
+                                const float wa = ex2(ml_at(q2, ra).x - s.mrg_m[ra]) * s.mrg_inv[ra];
                                 acc_a.x += wa * va[i].x, acc_a.y += wa * va[i].y;
                                 acc_a.z += wa * va[i].z, acc_a.w += wa * va[i].w;
                                 if (rb < rows) {
-                                    const float wb = wfit ? wsm[q2 * rows + rb]
-                                                          : ex2(__ldcg(ml + (size_t)q2 * p.slot_rows + rb).x -
-                                                                s.mrg_m[rb]) * s.mrg_inv[rb];
+                                    const float wb = ex2(ml_at(q2, rb).x - s.mrg_m[rb]) * s.mrg_inv[rb];
                                     acc_b.x += wb * vb[i].x, acc_b.y += wb * vb[i].y;
                                     acc_b.z += wb * vb[i].z, acc_b.w += wb * vb[i].w;
                                 }
