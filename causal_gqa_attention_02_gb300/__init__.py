@@ -33,8 +33,8 @@ PAGE_TOKENS = 16
 LAYOUT_VERSION = 2
 DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4
 KERNELS = {"cache_write": 0, "cow_copy": 1, "prefill_tc": 2, "attn_simt": 3,
-           "decode_split": 4, "decode_combine": 5, "rotate_pages": 6}
-DECODE_KERNELS = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
+           "decode_split": 4, "decode_combine": 5, "rotate_pages": 6, "decode_cluster": 7}
+DECODE_KERNELS = {"auto": 0, "tensor_core": 1, "cuda_core": 2, "cluster": 3}
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
 
@@ -248,7 +248,7 @@ class Cache:
 
     def set_decode_kernel(self, kernel: str):
         """Decode kernel of attn_decode / attn_decode_static: "auto",
-        "tensor_core" or "cuda_core"."""
+        "tensor_core", "cuda_core" or "cluster"."""
         _check(_lib.gqa_set_decode_kernel(self._h, DECODE_KERNELS[kernel]))
 
     def selftest_bounded_wait(self, limit_ns: int, stream=None):

@@ -986,6 +986,40 @@ int decode_uses_tc(const gqa_cache *c, int G)
     return ok && c->desc.dtype == GQA_DTYPE_BF16 ? 1 : 0;
 }
 
+// Cluster size of the clustered decode kernel for a call of B single-token
+// queries whose longest sequence holds max_len tokens (the query's own
+// included), with query rows q and, for a fused append, new rows k_new and
+// v_new; 0 when another kernel serves the call; -1 when the clustered kernel
+// was asked for but cannot serve it.  Automatic choice: when there are at
+// most half as many (entry, KV head) pairs as SMs, so every pair gets two or
+// more SMs.  The cluster is the largest power of two (at most 16) such that
+// the pairs' clusters fit the SMs and are resident together.
+int decode_cluster_for(const gqa_cache *c, int G, int B, int32_t max_len, const void *q,
+                       const void *k_new = nullptr, const void *v_new = nullptr)
+{
+    const int32_t H_kv = c->desc.num_kv_heads;
+    const bool ok = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
+                    c->desc.rope == 0 && decode_cluster_supported(G) && B >= 1 && B <= 65535 && H_kv <= 65535 &&
+                    ((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new) % 16 == 0;
+    if (c->decode_kernel == GQA_DECODE_CLUSTER) {
+        if (!ok)
+            return -1;
+    } else if (c->decode_kernel != GQA_DECODE_AUTO || !ok) {
+        return 0;
+    }
+    const int64_t pairs = (int64_t)B * H_kv;
+    if (c->decode_kernel == GQA_DECODE_AUTO && pairs * 2 > c->num_sms)
+        return 0;
+    const int32_t pages = (max_len - decode_first_token(max_len, c->desc.window) + kPageTokens - 1) / kPageTokens;
+    for (int cs = 16; cs >= 2; cs /= 2)
+        if (cs <= pages && pairs * cs <= c->num_sms && decode_cluster_capacity(cs) >= pairs)
+            return cs;
+    return 1;
+}
+
+static const char *kClusterNeeds = "the clustered decode kernel needs a bf16 cache with d_h = 128, no rotary, "
+                                   "H_q/H_kv <= 16 and 16-byte aligned q (and k_new, v_new)";
+
 // ---------------------------------------------------------------------------
 // The hot path.
 // ---------------------------------------------------------------------------
@@ -1382,9 +1416,28 @@ static int decode_launch(gqa_cache *c, const PoolView &pv, const std::vector<Seq
     int64_t total = 0;
     for (int b = 0; b < B; ++b)
         total += sds[b].past + 1 - decode_first_token(sds[b].past + 1, c->desc.window);
+    int32_t max_len = 1;
+    for (int b = 0; b < B; ++b)
+        max_len = std::max(max_len, sds[b].past + 1);
     Stage stg(c->h_stage);
     const size_t o_sds = stg.add(sds.data(), sds.size());
     int rc;
+    const int cs = decode_cluster_for(c, G, B, max_len, q);
+    if (cs < 0)
+        return fail(GQA_EINVAL, "%s", kClusterNeeds);
+    if (cs > 0) {
+        if ((rc = upload_stage(c, st)) != GQA_OK)
+            return rc;
+        ClusterDecodeLaunch a;
+        a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        a.B = B;
+        a.H_q = H_q;
+        a.cluster = cs;
+        a.q = q;
+        a.out = out;
+        return run_kernel(c, GQA_KERNEL_DECODE_CLUSTER, st, "clustered decode kernel",
+                          [&](cudaEvent_t ev) { return launch_decode_cluster(pv, a, st, ev); });
+    }
     if ((rc = decode_uses_tc(c, G)) < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
     if (rc == 1) {
@@ -1539,7 +1592,21 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     const int use_tc = c->meta_only ? 0 : decode_uses_tc(c, G);
     if (use_tc < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys and H_q/H_kv <= 128");
-    if (!use_tc || c->desc.dtype == GQA_DTYPE_FP8_E4M3) {
+    int cs = 0;
+    if (!c->meta_only) {
+        // The clustered kernel's choice needs the lengths: unknown sequences
+        // are reported by the write checks below.
+        int32_t max_len = 1;
+        bool known = true;
+        for (int b = 0; b < B && known; ++b) {
+            known = live(c, seq_ids[b]);
+            if (known)
+                max_len = std::max(max_len, c->seqs[seq_ids[b]].len + 1);
+        }
+        if (known && (cs = decode_cluster_for(c, G, B, max_len, q, k_new, v_new)) < 0)
+            return fail(GQA_EINVAL, "%s", kClusterNeeds);
+    }
+    if (cs == 0 && (!use_tc || c->desc.dtype == GQA_DTYPE_FP8_E4M3)) {
         // CUDA-core kernels (and the quantised cache, whose write rounds in
         // its own kernel): the write, then the decode.
         int rc = kv_append(c, B, seq_ids, 1, nullptr, k_new, v_new, stream);
@@ -1559,6 +1626,36 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     cudaStream_t st = (cudaStream_t)stream;
     if ((rc = upload_tables(c, st)) != GQA_OK)
         return rc;
+    const PoolView pv = c->view();
+    if (cs > 0) {
+        // Clustered decode: the CTA that reads the new position's page
+        // writes the row.
+        Stage stg(c->h_stage);
+        const size_t o_sds = stg.add(sds.data(), sds.size());
+        const size_t o_cow = stg.add(cows.data(), cows.size());
+        if ((rc = upload_stage(c, st)) != GQA_OK)
+            return rc;
+        if (!cows.empty() &&
+            (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
+                 rec(ev, st);
+                 return launch_cow_copy(pv, c->esize, (const CowDesc *)(c->d_stage + o_cow), (int)cows.size(), st);
+             })) != GQA_OK)
+            return rc;
+        ClusterDecodeLaunch a;
+        a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        a.B = B;
+        a.H_q = H_q;
+        a.cluster = cs;
+        a.q = q;
+        a.out = out;
+        a.app_k = k_new;
+        a.app_v = v_new;
+        rc = run_kernel(c, GQA_KERNEL_DECODE_CLUSTER, st, "clustered decode kernel",
+                        [&](cudaEvent_t ev) { return launch_decode_cluster(pv, a, st, ev); });
+        if (rc == GQA_OK)
+            release_windows(c, B, seq_ids);
+        return rc;
+    }
     TcPlan plan;
     plan_tc(c, sds, G, plan);
     Stage stg(c->h_stage);
@@ -1571,7 +1668,6 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
         return rc;
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
-    const PoolView pv = c->view();
     if (!cows.empty() &&
         (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
              rec(ev, st);
@@ -1651,8 +1747,13 @@ int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
 {
     if (!c)
         return fail(GQA_EINVAL, "NULL cache");
-    if (kernel != GQA_DECODE_AUTO && kernel != GQA_DECODE_TENSOR_CORE && kernel != GQA_DECODE_CUDA_CORE)
-        return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE or _CUDA_CORE", kernel);
+    if (kernel != GQA_DECODE_AUTO && kernel != GQA_DECODE_TENSOR_CORE && kernel != GQA_DECODE_CUDA_CORE &&
+        kernel != GQA_DECODE_CLUSTER)
+        return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE, _CUDA_CORE or _CLUSTER",
+                    kernel);
+    if (kernel == GQA_DECODE_CLUSTER &&
+        (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || c->desc.rope != 0))
+        return fail(GQA_EINVAL, "the clustered decode kernel needs a bf16 cache with d_h = 128 and no rotary");
     if (kernel == GQA_DECODE_TENSOR_CORE &&
         ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128 ||
          c->desc.keys_post_position != 1))
@@ -1761,6 +1862,7 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         return fail(GQA_EINVAL, "NULL tensor pointer");
     std::vector<SeqDesc> sds(B);
     int64_t total = 0;
+    int32_t max_len = 1;
     for (int b = 0; b < B; ++b) {
         const int32_t s = seq_ids[b];
         if (!live(c, s))
@@ -1770,12 +1872,43 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
             return fail(GQA_EMASK, "sequence %d is empty: the decode query has no visible key", s);
         sds[b] = SeqDesc{s, L - 1, 1, 0};
         total += L - decode_first_token(L, c->desc.window);
+        max_len = std::max(max_len, L);
     }
     int rc = check_device(c);
     if (rc != GQA_OK)
         return rc;
     cudaStream_t st = (cudaStream_t)stream;
     const size_t part_bytes = GQA_STATIC_SCRATCH_BYTES - kStaticDescBytes - kStaticCntBytes;
+
+    const int cs = decode_cluster_for(c, G, B, max_len, q);
+    if (cs < 0)
+        return fail(GQA_EINVAL, "%s", kClusterNeeds);
+    if (cs > 0) {
+        // The clustered kernel of attn_decode: no partials leave the
+        // cluster, so only the descriptors go to the static array.
+        std::vector<char> desc;
+        Stage stg(desc);
+        const size_t o_sds = stg.add(sds.data(), sds.size());
+        if (desc.size() > kStaticDescBytes)
+            return fail(GQA_ERANGE, "decode descriptors need %zu bytes; the static scratch reserves %zu",
+                        desc.size(), kStaticDescBytes);
+        char *scratch = nullptr;
+        if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
+            return rc;
+        if ((rc = upload_tables(c, st, true)) != GQA_OK ||
+            (rc = staged_copy(c, scratch, desc.data(), desc.size(), st)) != GQA_OK)
+            return rc;
+        ClusterDecodeLaunch a;
+        a.seqs = (const SeqDesc *)(scratch + o_sds);
+        a.B = B;
+        a.H_q = H_q;
+        a.cluster = cs;
+        a.q = q;
+        a.out = out;
+        const PoolView pv = c->view();
+        return run_kernel(c, GQA_KERNEL_DECODE_CLUSTER, st, "clustered decode kernel (static scratch)",
+                          [&](cudaEvent_t ev) { return launch_decode_cluster(pv, a, st, ev); });
+    }
 
     if (use_tc) {
         // The plan of attn_decode (so the results are the same bits), with

@@ -1,0 +1,546 @@
+// k_decode_cluster.cu -- single-token decode of a small batch over the paged
+// cache (bf16, d_h = 128): each (batch entry, KV head) is served by one
+// thread-block cluster whose CTAs split its pages, and the CTAs' partial
+// softmax states are merged inside the cluster through distributed shared
+// memory.
+//
+// What it computes ("KV Cache 与 Prefill/Decode 推理路径", decode lesson: the
+// single new query reads every cached key, its own included; the
+// PagedAttention section: keys are found through the block table;
+// "第二章 Prefill：整层状态演化与 KV 建立" section 2.3 for the scores and the
+// softmax): for query head h of KV group g,
+//     out[b,h] = sum_t softmax_t(<q[b,h], K[t,g]>/sqrt(128)) V[t,g]
+// over the visible positions t (every cached one, or the last W of them with
+// a sliding window).
+//
+// Why a kernel of its own: with few sequences (B * H_kv well below the SM
+// count) each (entry, head) holds many bytes but there are few of them, so
+// its keys are split across SMs and the parts merged.  The persistent
+// tensor-core kernel merges through a global workspace and the CTA that
+// finishes last, which puts a fence, an atomic and two rounds of L2 reads
+// after the data has streamed, and its per-CTA set-up (TMEM, twelve warps)
+// and 128-key tile chain add more.  Here:
+//  * grid (cs, H_kv, B) in clusters of cs CTAs along x: CTA r of the cluster
+//    of (b, kvh) takes pages [r P / cs, (r + 1) P / cs) of the P pages that
+//    hold visible keys;
+//  * sixteen producer lanes request the CTA's pages up front, as far as a
+//    ring of kStages stages allows: a stage is the page's K block and V block
+//    (4 KB each, one TMA box each, 128-byte swizzled, issued by two lanes),
+//    completed on an mbarrier.  Lane 2p + kv issues block kv of pages p,
+//    p + 8, ...: the copies of eight pages are issued at once, since one
+//    thread issuing them in turn leaves the SM's copy engine idle between
+//    boxes;
+//  * kWarps consumer warps take the pages round robin.  The group's g heads
+//    are the rows of a 16-row mma.sync m16n8k16 tile (bf16 operands, fp32
+//    accumulation; rows past g hold zeros): S = Q K^T over the page's 16 keys
+//    (8 k-steps x 2 n-tiles, K fragments by ldmatrix from the swizzled
+//    stage), an online softmax per row in exp2 units, then O += P V with P
+//    rounded to bf16 as the A operand straight from the score registers and
+//    V fragments by ldmatrix.trans;
+//  * the warps' (m, l, O) meet in shared memory; then each CTA stores its
+//    (m, l) into every CTA of the cluster and column slice j of its summed O
+//    into CTA j (distributed shared memory), one cluster barrier makes the
+//    stores visible, and CTA j merges the slices it holds and writes those
+//    columns of out.  Nothing goes through global memory but q, the pages
+//    and out, and no CTA waits on a flag another one sets.
+// Decode with append (app_k / app_v): the warp that holds the page of
+// position past writes the new K/V row into the landed stage, before reading
+// it, and into the pool.
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "kernels.cuh"
+#include "sm100.cuh"
+
+namespace gqa {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int D = 128;
+constexpr int kWarps = 8;                          // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;        // + one producer warp
+#ifndef GQA_DC_STAGES
+#define GQA_DC_STAGES 24
+#endif
+#ifndef GQA_DC_LANES
+#define GQA_DC_LANES 16
+#endif
+#ifndef GQA_DC_RED_APART
+#define GQA_DC_RED_APART 0
+#endif
+constexpr int kStages = GQA_DC_STAGES;
+constexpr int kIssuePages = GQA_DC_LANES / 2;      // pages whose copies are issued at once
+// A stage is refilled by the lane that filled it (page i and i + kStages
+// have one issuing lane), so a lane's final wait on a stage is for its own
+// last copy into it; and by the warp that read it (page i and i + kStages
+// have one consumer warp), so stages free in each warp's own order.
+static_assert(kStages % kIssuePages == 0, "a stage must be refilled by the lane that filled it");
+static_assert(kStages % kWarps == 0, "a stage must be read by one consumer warp");
+constexpr int kBlockBytes = kPageTokens * D * 2;   // one page of one head: 4 KB
+constexpr int kMaxCluster = 16;
+constexpr int kRows = 16;                          // MMA rows: the group's heads, zero-padded
+
+constexpr int kRedStride = D + 4;                  // warp-combine rows, padded against bank conflicts
+struct __align__(1024) DcSmem {
+    unsigned char ring[kStages][2 * kBlockBytes];  // stage: K block, then V block
+#if GQA_DC_RED_APART
+    float red[kWarps][kRows][kRedStride];
+#endif
+    // Received from the cluster's CTAs (rank r): unnormalised O rows,
+    // columns [r * nc, (r + 1) * nc) = this CTA's slice as CTA r holds it,
+    // nc = 128 / cluster size; and (m, l) per row.
+    float in_o[kRows][D];
+    float in_m[kMaxCluster][kRows], in_l[kMaxCluster][kRows];
+    float wm[kWarps][kRows], wl[kWarps][kRows];    // per consumer warp
+    uint64_t full[kStages], empty[kStages];
+    int abort_;
+};
+static_assert(GQA_DC_RED_APART || kWarps * kRows * kRedStride * sizeof(float) <= sizeof(DcSmem::ring), "the warp combine reuses the ring");
+
+struct DcParams {
+    const SeqDesc *seqs;
+    const int32_t *tables;
+    unsigned char *pool;
+    int32_t *err;
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *app_k, *app_v;
+    int stride, num_pages, H_kv, H_q, G, window;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_ncta()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: writes before it are visible to
+// the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Store v into the shared memory of cluster CTA `rank`, at the offset
+// `local` has in this CTA's.
+__device__ __forceinline__ void st_cluster(float *local, uint32_t rank, float v)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset, within a landed page block, of 16-byte unit c (columns
+// 8c .. 8c + 7) of slot s: the pool's block layout (two groups of 8 slots,
+// each stored 128-byte chunk by chunk) as the 128-byte swizzle of the TMA
+// copy places it: line (s / 8) * 16 + (c / 8) * 8 + s % 8, unit (c % 8) xor (s % 8).
+__device__ __forceinline__ uint32_t stage_off(int s, int c)
+{
+    return (uint32_t)((((s >> 3) << 4) + ((c >> 3) << 3) + (s & 7)) << 7) + (uint32_t)(((c & 7) ^ (s & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    DcSmem &s = *reinterpret_cast<DcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, kvh = blockIdx.y;
+    const uint32_t rank = cluster_rank(), cs = cluster_ncta();
+    const SeqDesc sd = p.seqs[b];
+    const int past = sd.past;                              // the query's position (L - 1)
+    const int L = past + 1;
+    const int ws = window_start(past, p.window);           // first visible key
+    const int pfirst = decode_first_token(L, p.window) / kPageTokens;
+    const int P = (L - pfirst * kPageTokens + kPageTokens - 1) / kPageTokens;
+    const int i_lo = (int)((int64_t)rank * P / cs), i_hi = (int)((int64_t)(rank + 1) * P / cs);
+    const int npg = i_hi - i_lo;
+    const int32_t *tab = p.tables + (size_t)sd.row * p.stride + pfirst + i_lo;
+    const int G = p.G;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s.full[i], 2);
+            mbar_init(&s.empty[i], 1);
+        }
+        s.abort_ = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int r0 = lane >> 2, qc = (lane & 3) * 2;         // fragment row / column pair of this lane
+    float o[D / 8][4];                                     // O rows r0, r0 + 8; columns 8j + qc, + 1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    if (warp == kWarps) {
+        // ---- producer ---------------------------------------------------
+        if (lane < 2 * kIssuePages) {
+            const int kv = lane & 1;
+            if (lane == 0)
+                prefetch_tmap(&mKV);
+            int issued = 0;                                // pages lane issued: lane/2, lane/2 + 8, ...
+            for (int i = lane >> 1; i < npg; i += kIssuePages) {
+                const int st = i % kStages;
+                if (i >= kStages && !mbar_wait(&s.empty[st], ((i / kStages) - 1) & 1, &s.abort_)) {
+                    s.abort_ = 1;
+                    atomicOr(p.err, kErrTimeout);
+                    break;
+                }
+                int page = tab[i];
+                if ((unsigned)page >= (unsigned)p.num_pages) {
+                    if (kv == 0)
+                        atomicOr(p.err, kErrPageId);
+                    page = p.num_pages;                    // out of range: the box reads zeros
+                }
+                mbar_arrive_expect_tx(&s.full[st], kBlockBytes);
+                tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kBlockBytes, 0, 0, (page * 2 + kv) * p.H_kv + kvh);
+                issued = i + 1;
+            }
+            // Every issued copy lands before the ring is reused or the CTA
+            // ends (copies of earlier uses of a stage were waited for by
+            // their consumers before the stage was issued again).
+            const int never = 0;
+            for (int i = lane >> 1; i < issued; i += kIssuePages)
+                if (i + kStages >= issued && !mbar_wait(&s.full[i % kStages], (i / kStages) & 1, &never)) {
+                    s.abort_ = 1;
+                    atomicOr(p.err, kErrTimeout);
+                }
+        }
+        __syncwarp();                                      // the warp meets the block barrier converged
+    } else {
+        // ---- consumers --------------------------------------------------
+        // Q as the A operand of each k-step: rows r0 / r0 + 8 (zero past g),
+        // columns 16 kk + qc, + 1 and 16 kk + 8 + qc, + 1.
+        uint32_t qa[D / 16][4];
+        {
+            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * p.H_q + kvh * G + r0) * D);
+            const uint32_t *q1 = q0 + 8 * D / 2;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qa[kk][0] = r0 < G ? q0[8 * kk + qc / 2] : 0u;
+                qa[kk][1] = r0 + 8 < G ? q1[8 * kk + qc / 2] : 0u;
+                qa[kk][2] = r0 < G ? q0[8 * kk + 4 + qc / 2] : 0u;
+                qa[kk][3] = r0 + 8 < G ? q1[8 * kk + 4 + qc / 2] : 0u;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+            o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        const float kScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+        const int mi = lane >> 3, rr = lane & 7;           // ldmatrix: matrix and row this lane addresses
+        const uint32_t ring0 = smem_u32(s.ring[0]);
+        for (int i = warp; i < npg; i += kWarps) {
+            const int st = i % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (i / kStages) & 1, &s.abort_))) {
+                if (lane == 0) {
+                    s.abort_ = 1;
+                    atomicOr(p.err, kErrTimeout);
+                }
+                break;
+            }
+            const uint32_t kb = ring0 + (uint32_t)st * (2 * kBlockBytes), vb = kb + kBlockBytes;
+            const int pos0 = (pfirst + i_lo + i) * kPageTokens;    // position of the page's slot 0
+            if (p.app_k && pos0 <= past && past < pos0 + kPageTokens) {
+                // The appended row: lanes 0-15 its K units, 16-31 its V units.
+                const int slot = past - pos0, kv = lane >> 4, c = lane & 15;
+                const __nv_bfloat16 *src = (kv ? p.app_v : p.app_k) + ((size_t)b * p.H_kv + kvh) * D + 8 * c;
+                const uint4 val = *reinterpret_cast<const uint4 *>(src);
+                *reinterpret_cast<uint4 *>(s.ring[st] + kv * kBlockBytes + stage_off(slot, c)) = val;
+                const int page = tab[i];
+                if ((unsigned)page < (unsigned)p.num_pages)
+                    *reinterpret_cast<uint4 *>(p.pool + (((size_t)page * 2 + kv) * p.H_kv + kvh) * kBlockBytes +
+                                               pool_in_block(2, slot, 16 * c)) = val;
+                __syncwarp();
+            }
+            // S = Q K^T: n-tile 0 = keys 0-7, n-tile 1 = keys 8-15.
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kb + stage_off(8 * (mi >> 1) + rr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                mma_bf16(sc[0], qa[kk], b0, b1);
+                mma_bf16(sc[1], qa[kk], b2, b3);
+            }
+            // Visible keys only, in exp2 units.
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = pos0 + 8 * nt + qc + (e & 1);
+                    sc[nt][e] = (t <= past && t >= ws) ? sc[nt][e] * kScale : -INFINITY;
+                }
+            float x0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+            float x1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+            const float f0 = n0 == -INFINITY ? 0.f : n0, f1 = n1 == -INFINITY ? 0.f : n1;
+            const float a0 = ex2(m0 - f0), a1 = ex2(m1 - f1);   // 0 while nothing was visible
+            m0 = n0;
+            m1 = n1;
+            float pr[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pr[nt][e] = ex2(sc[nt][e] - (e < 2 ? f0 : f1));
+            l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+            l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    o[j][0] *= a0;
+                    o[j][1] *= a0;
+                    o[j][2] *= a1;
+                    o[j][3] *= a1;
+                }
+            }
+            // O += P V: P (16 rows x 16 keys) is the A operand as the score
+            // fragments hold it; n-tile j = columns 8j .. 8j + 7.
+            const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                                    pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb + stage_off(8 * (mi & 1) + rr, 2 * j + (mi >> 1)), b0, b1, b2, b3);
+                mma_bf16(o[2 * j], pa, b0, b1);
+                mma_bf16(o[2 * j + 1], pa, b2, b3);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.empty[st]);
+        }
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if ((lane & 3) == 0) {
+            s.wm[warp][r0] = m0;
+            s.wm[warp][r0 + 8] = m1;
+            s.wl[warp][r0] = l0;
+            s.wl[warp][r0 + 8] = l1;
+        }
+    }
+    __syncthreads();          // the ring is idle: every copy landed and was read
+
+    // ---- the CTA's partial: warps combined -----------------------------------
+    const bool ok = s.abort_ == 0;
+#if GQA_DC_RED_APART
+    float *red = &s.red[0][0][0];
+#else
+    float *red = reinterpret_cast<float *>(s.ring[0]);     // [kWarps][kRows][kRedStride]
+#endif
+    if (warp < kWarps && ok) {
+        float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            M0 = fmaxf(M0, s.wm[w][r0]);
+            M1 = fmaxf(M1, s.wm[w][r0 + 8]);
+        }
+        const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0), c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
+        float *w0 = red + ((size_t)warp * kRows + r0) * kRedStride + qc, *w1 = w0 + 8 * kRedStride;
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+            if (r0 < G)
+                *reinterpret_cast<float2 *>(w0 + 8 * j) = make_float2(o[j][0] * c0, o[j][1] * c0);
+            if (r0 + 8 < G)
+                *reinterpret_cast<float2 *>(w1 + 8 * j) = make_float2(o[j][2] * c1, o[j][3] * c1);
+        }
+    }
+    __syncthreads();
+    // ---- into the cluster: column slice j of every row goes to CTA j ----------
+    const int nc = D / (int)cs;                        // cs is a power of two <= 16
+    if (ok) {
+        for (int e = threadIdx.x; e < G * D; e += kThreads) {
+            const int row = e >> 7, col = e & (D - 1);
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)              // a fixed order
+                a += red[((size_t)w * kRows + row) * kRedStride + col];
+            const int j = col / nc;
+            st_cluster(&s.in_o[row][rank * nc + (col - j * nc)], (uint32_t)j, a);
+        }
+    }
+    for (int t = threadIdx.x; t < G * (int)cs; t += kThreads) {
+        const int j = t / G, row = t - j * G;
+        float M = -INFINITY, l = 0.f;
+        for (int w = 0; w < kWarps; ++w)
+            M = fmaxf(M, s.wm[w][row]);
+        for (int w = 0; w < kWarps; ++w)
+            if (s.wm[w][row] != -INFINITY)
+                l += s.wl[w][row] * ex2(s.wm[w][row] - M);
+        st_cluster(&s.in_m[rank][row], (uint32_t)j, ok ? M : -INFINITY);
+        st_cluster(&s.in_l[rank][row], (uint32_t)j, ok ? l : 0.f);
+    }
+    cluster_sync();           // every CTA's stores into this one are visible
+
+    // ---- the merge of this CTA's columns [rank * nc, (rank + 1) * nc) ------------
+    if (threadIdx.x < G) {
+        // Weights 2^(m_r - M) / sum_r 2^(m_r - M) l_r, in cluster rank order.
+        const int row = threadIdx.x;
+        float M = -INFINITY, den = 0.f;
+        for (uint32_t r = 0; r < cs; ++r)
+            M = fmaxf(M, s.in_m[r][row]);
+        for (uint32_t r = 0; r < cs; ++r) {
+            const float w = s.in_m[r][row] == -INFINITY ? 0.f : ex2(s.in_m[r][row] - M);
+            s.in_m[r][row] = w;
+            den += w * s.in_l[r][row];
+        }
+        const float inv = 1.0f / den;
+        for (uint32_t r = 0; r < cs; ++r)
+            s.in_m[r][row] *= inv;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * nc; e += kThreads) {
+        const int row = e / nc, c = e - row * nc;
+        float a = 0.f;
+        for (uint32_t r = 0; r < cs; ++r)
+            a = fmaf(s.in_m[r][row], s.in_o[row][r * nc + c], a);
+        p.out[((size_t)b * p.H_q + kvh * G + row) * D + rank * nc + c] = __float2bfloat16_rn(a);
+    }
+}
+
+constexpr int kSmemBytes = (int)sizeof(DcSmem) + 1024;
+constexpr int kMaxDev = 64;
+
+// The shared-memory and cluster-size opt-ins are per device.
+cudaError_t configure(int dev)
+{
+    static std::atomic<bool> done[kMaxDev];
+    if (dev < 0 || dev >= kMaxDev)
+        return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess)
+        done[dev].store(true, std::memory_order_release);
+    return e;
+}
+
+}  // namespace
+
+bool decode_cluster_supported(int group) { return group >= 1 && group <= kRows; }
+
+int decode_cluster_capacity(int cluster)
+{
+    // Sizes 1, 2, 4, 8, 16, looked up once per device.
+    static std::atomic<int> cap[kMaxDev][5];
+    int dev = 0, k = 0;
+    while (k < 5 && (1 << k) != cluster)
+        ++k;
+    if (k == 5 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || configure(dev) != cudaSuccess)
+        return 0;
+    int v = cap[dev][k].load(std::memory_order_acquire);
+    if (v != 0)
+        return v < 0 ? 0 : v;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cap[dev][k].store(n > 0 ? n : -1, std::memory_order_release);
+    return n;
+}
+
+cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch &a, cudaStream_t st,
+                                  cudaEvent_t ev_start)
+{
+    const int G = pv.H_kv > 0 ? a.H_q / pv.H_kv : 0;
+    if (pv.d != D || pv.dtype != kDtypeBf16 || pv.rope || !decode_cluster_supported(G) || a.cluster < 1 ||
+        a.cluster > kMaxCluster || a.B < 1 || a.B > 65535 || pv.H_kv > 65535)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || (e = configure(dev)) != cudaSuccess)
+        return e;
+    // The pool as 128-byte lines: [block][32 lines][64 elements]; a box is
+    // one page block (4 KB).
+    CUtensorMap mkv;
+    const cuuint64_t kvdims[3] = {64, 32, (cuuint64_t)pv.num_pages * 2 * pv.H_kv};
+    const cuuint64_t kvstr[2] = {128, 32 * 128};
+    const cuuint32_t kvbox[3] = {64, 32, 1};
+    if (!encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox))
+        return cudaErrorInvalidValue;
+    DcParams prm;
+    prm.seqs = a.seqs;
+    prm.tables = pv.tables;
+    prm.pool = (unsigned char *)pv.pool;
+    prm.err = pv.err;
+    prm.q = (const __nv_bfloat16 *)a.q;
+    prm.out = (__nv_bfloat16 *)a.out;
+    prm.app_k = (const __nv_bfloat16 *)a.app_k;
+    prm.app_v = (const __nv_bfloat16 *)a.app_v;
+    prm.stride = pv.stride;
+    prm.num_pages = pv.num_pages;
+    prm.H_kv = pv.H_kv;
+    prm.H_q = a.H_q;
+    prm.G = G;
+    prm.window = pv.window;
+    if (ev_start)
+        cudaEventRecord(ev_start, st);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.cluster, (unsigned)pv.H_kv, (unsigned)a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_cluster_kernel, mkv, prm);
+}
+
+}  // namespace gqa

@@ -1153,34 +1153,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-    }
-    return fn;
-}
-
-bool encode(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
-            const cuuint32_t *box, bool bytes = false)
-{
-    auto fn = encoder();
-    if (!fn)
-        return false;
-    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    // bytes: FP8 code blocks, copied as they are (the kernel lays them out).
-    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-              const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The bounded wait every kernel here uses, on a barrier phase that nothing
 // completes: it gives up after limit_ns and records a timeout in the error
 // word, as a pipeline wait would.  Exercises the failure path without a
@@ -1200,6 +1172,34 @@ __global__ void wait_probe_kernel(int32_t *err, uint64_t limit_ns)
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }
+    return fn;
+}
+
+bool encode_tmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+                 const cuuint32_t *box, bool bytes)
+{
+    auto fn = encoder();
+    if (!fn)
+        return false;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    // bytes: FP8 code blocks, copied as they are (the kernel lays them out).
+    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+              const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_wait_probe(int32_t *err, uint64_t limit_ns, cudaStream_t st)
 {
@@ -1240,9 +1240,9 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     if (q8 && (pv.rope || app_k || !pv.scales))
         return cudaErrorInvalidValue;
     // out has the shape and layout of q: the same box serves the stores.
-    if (!encode(&mq, 4, q, qdims, qstr, qbox) ||
-        !(q8 ? encode(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true) : encode(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)) ||
-        !encode(&mo, 4, out, qdims, qstr, qbox))
+    if (!encode_tmap(&mq, 4, q, qdims, qstr, qbox) ||
+        !(q8 ? encode_tmap(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true) : encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)) ||
+        !encode_tmap(&mo, 4, out, qdims, qstr, qbox))
         return cudaErrorInvalidValue;
     // Fused write: k and v [B, n, H_kv, 128] as [H_kv][B * n / 8 row groups]
     // [column half][8 rows][64 elements] (n a multiple of 8), boxes of one
@@ -1255,8 +1255,8 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
         const cuuint64_t fdims[5] = {64, 8, 2, (cuuint64_t)B * n / 8, (cuuint64_t)pv.H_kv};
         const cuuint64_t fstr[4] = {(cuuint64_t)pv.H_kv * D * 2, 128, (cuuint64_t)8 * pv.H_kv * D * 2, (cuuint64_t)D * 2};
         const cuuint32_t tbox[5] = {64, 8, 2, 16, 1}, pbox[5] = {64, 8, 2, 2, 1};
-        if (!encode(&mkt, 5, fused_k, fdims, fstr, tbox) || !encode(&mvt, 5, fused_v, fdims, fstr, tbox) ||
-            !encode(&mkp, 5, fused_k, fdims, fstr, pbox) || !encode(&mvp, 5, fused_v, fdims, fstr, pbox))
+        if (!encode_tmap(&mkt, 5, fused_k, fdims, fstr, tbox) || !encode_tmap(&mvt, 5, fused_v, fdims, fstr, tbox) ||
+            !encode_tmap(&mkp, 5, fused_k, fdims, fstr, pbox) || !encode_tmap(&mvp, 5, fused_v, fdims, fstr, pbox))
             return cudaErrorInvalidValue;
     } else {
         mkt = mvt = mkp = mvp = mkv;               // unused

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gqa {
@@ -162,6 +163,36 @@ struct DecodeLaunch {
     void *out;
 };
 bool decode_split_supported(int group);
+
+// Tiled tensor map over `base` (bf16 elements, 128-byte swizzle; bytes:
+// uint8 elements, no swizzle) with the driver's encoder.  False if the
+// encoder is unavailable or refuses the shape.
+bool encode_tmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+                 const cuuint32_t *box, bool bytes = false);
+
+// bf16, d = 128 single-token decode with each (entry, KV head) served by a
+// cluster of `cluster` CTAs that split its pages and merge their partials
+// through distributed shared memory.  No workspace.  app_k / app_v
+// ([B, H_kv, 128], optional) fuse the append: the row of each entry is
+// written at position past (its page already in the block table) by the CTA
+// that reads that page.  ev_start, if given, is recorded right before the
+// launch.
+struct ClusterDecodeLaunch {
+    const SeqDesc *seqs;
+    int B;
+    int H_q;
+    int cluster;
+    const void *q;
+    void *out;
+    const void *app_k = nullptr;
+    const void *app_v = nullptr;
+};
+bool decode_cluster_supported(int group);
+// Largest number of clusters of `cluster` CTAs the device holds at once (0:
+// that size cannot be launched).  The device must be current.
+int decode_cluster_capacity(int cluster);
+cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch &a, cudaStream_t st,
+                                  cudaEvent_t ev_start = nullptr);
 cudaError_t launch_decode_split(const PoolView &pv, const DecodeLaunch &a, cudaStream_t st);
 
 // bf16, d = 128 tensor-core prefill (tcgen05 + TMEM + TMA).  Rows of the

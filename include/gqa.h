@@ -437,9 +437,12 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
                        const void *q, void *out, void *stream);
 
 /* Decode kernel of attn_decode and attn_decode_static.
- *  GQA_DECODE_AUTO         (default) tensor-core when the cache is bf16 with
- *                          d_h = 128, else CUDA-core (an FP8 E4M3 cache
- *                          decodes faster on the CUDA-core kernel).
+ *  GQA_DECODE_AUTO         (default) for a bf16 cache with d_h = 128: the
+ *                          clustered kernel when it can serve the call and
+ *                          there are at most half as many (entry, KV head)
+ *                          pairs as SMs, else tensor-core; CUDA-core for
+ *                          other caches (an FP8 E4M3 cache decodes faster
+ *                          on the CUDA-core kernel).
  *  GQA_DECODE_TENSOR_CORE  the prefill kernel with one query row per
  *                          sequence: every KV head's key tiles are read once
  *                          by TMA, a sequence's tiles are split into ranges
@@ -453,11 +456,23 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
  *  GQA_DECODE_CUDA_CORE    the split-K CUDA-core decode kernel (bf16 or FP8
  *                          E4M3, d_h = 128, H_q / H_kv <= 8), else the
  *                          generic CUDA-core kernel.
- * Both compute the same softmax; they differ in rounding order only.
- * Errors: GQA_EINVAL (unknown choice, or tensor-core on another cache). */
+ *  GQA_DECODE_CLUSTER      the clustered decode kernel: each (entry, KV
+ *                          head) is one thread-block cluster of up to 16
+ *                          CTAs that split its pages (each page's K and V
+ *                          read once by TMA, both products on mma.sync) and
+ *                          merge their partial (m, l, O) through distributed
+ *                          shared memory; no workspace.  Needs a bf16 cache
+ *                          with d_h = 128 and no rotary (else GQA_EINVAL
+ *                          here), H_q / H_kv <= 16 and q (for the fused
+ *                          append also k_new and v_new) 16-byte aligned
+ *                          (else GQA_EINVAL from the decode call).
+ * All compute the same softmax; they differ in rounding order only.
+ * Errors: GQA_EINVAL (unknown choice, or a kernel that cannot serve this
+ * cache). */
 #define GQA_DECODE_AUTO         0
 #define GQA_DECODE_TENSOR_CORE  1
 #define GQA_DECODE_CUDA_CORE    2
+#define GQA_DECODE_CLUSTER      3
 int gqa_set_decode_kernel(gqa_cache *cache, int32_t kernel);
 
 /* Self-test of the failure path of the kernels' waits.  Queues one block
@@ -494,7 +509,8 @@ int gqa_cache_check(gqa_cache *cache, void *stream, int32_t *flags_out);
 #define GQA_KERNEL_DECODE_SPLIT    4  /* split-K decode (bf16, 128), merge included */
 #define GQA_KERNEL_DECODE_COMBINE  5  /* reserved: the merge runs inside the split kernel */
 #define GQA_KERNEL_ROTATE_PAGES    6  /* pre-position prefill: the call's pages, keys rotated */
-#define GQA_KERNEL_COUNT           7
+#define GQA_KERNEL_DECODE_CLUSTER  7  /* clustered decode (bf16, 128), merge in the cluster */
+#define GQA_KERNEL_COUNT           8
 
 /* Turn per-launch timing on or off.  While on, every kernel launch of this
  * cache is bracketed by two CUDA events recorded on the launch's own stream.

@@ -55,7 +55,7 @@ def _step(rng, caches, ids, m, mids, H_q, H_kv, base=None):
     return launched
 
 
-@pytest.mark.parametrize("kernel", ["tensor_core", "cuda_core"])
+@pytest.mark.parametrize("kernel", ["tensor_core", "cuda_core", "cluster"])
 def test_fused_step_equals_append_then_decode(kernel):
     rng = np.random.default_rng(100)
     H_q, H_kv = 32, 8
@@ -65,6 +65,8 @@ def test_fused_step_equals_append_then_decode(kernel):
         launched = _step(rng, caches, ids, m, mids, H_q, H_kv)
         if kernel == "tensor_core":
             assert launched["prefill_tc"][0] == 1 and launched["cache_write"][0] == 0, launched
+        elif kernel == "cluster":
+            assert launched["decode_cluster"][0] == 1 and launched["cache_write"][0] == 0, launched
         else:
             assert launched["cache_write"][0] == 1, launched
     for c, i in zip(caches, ids):

@@ -9,7 +9,7 @@ The test calls it through the C ABI twice in a row, with the cache state and
 the query changed in between, so the second call reuses a scratch array that
 still holds the first call's contents.  Each result must be the same bits as
 attn_decode, the allocating entry point, on the same state (same kernel, same
-work split), on both decode kernels, and match the fp64 oracle within the
+work split), on every decode kernel, and match the fp64 oracle within the
 bf16 decode tolerance used elsewhere (max abs 2e-2, mean abs 2e-3).  A call
 whose partials would not fit the array is refused with GQA_ERANGE and leaves
 the output untouched.  The file name sorts last, so a run that stops at the
@@ -56,7 +56,7 @@ def _compare(got, ref):
     assert diff.max() <= 2e-2 and diff.mean() <= 2e-3, (diff.max(), diff.mean())
 
 
-@pytest.mark.parametrize("kernel", ["tensor_core", "cuda_core"])
+@pytest.mark.parametrize("kernel", ["tensor_core", "cuda_core", "cluster"])
 def test_static_decode_matches_allocating_decode_on_two_calls(kernel):
     H_kv, G, d = 4, 4, 128
     H_q = H_kv * G
