@@ -992,8 +992,9 @@ int decode_uses_tc(const gqa_cache *c, int G)
 // v_new; 0 when another kernel serves the call; -1 when the clustered kernel
 // was asked for but cannot serve it.  Automatic choice: when there are at
 // most half as many (entry, KV head) pairs as SMs, so every pair gets two or
-// more SMs.  The cluster is the largest power of two (at most 16) such that
-// the pairs' clusters fit the SMs and are resident together.
+// more SMs.  The cluster is the largest size (at most 16, and at most the
+// pages of the longest sequence) such that the pairs' clusters fit the SMs
+// and are resident together.
 int decode_cluster_for(const gqa_cache *c, int G, int B, int32_t max_len, const void *q,
                        const void *k_new = nullptr, const void *v_new = nullptr)
 {
@@ -1011,7 +1012,7 @@ int decode_cluster_for(const gqa_cache *c, int G, int B, int32_t max_len, const 
     if (c->decode_kernel == GQA_DECODE_AUTO && pairs * 2 > c->num_sms)
         return 0;
     const int32_t pages = (max_len - decode_first_token(max_len, c->desc.window) + kPageTokens - 1) / kPageTokens;
-    for (int cs = 16; cs >= 2; cs /= 2)
+    for (int cs = 16; cs >= 2; --cs)
         if (cs <= pages && pairs * cs <= c->num_sms && decode_cluster_capacity(cs) >= pairs)
             return cs;
     return 1;
@@ -1426,10 +1427,16 @@ static int decode_launch(gqa_cache *c, const PoolView &pv, const std::vector<Seq
     if (cs < 0)
         return fail(GQA_EINVAL, "%s", kClusterNeeds);
     if (cs > 0) {
-        if ((rc = upload_stage(c, st)) != GQA_OK)
-            return rc;
+        // Small batches pass their descriptors in the launch parameters: no
+        // upload precedes the kernel.
         ClusterDecodeLaunch a;
-        a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        if (B <= decode_cluster_inline()) {
+            a.host_seqs = sds.data();
+        } else {
+            if ((rc = upload_stage(c, st)) != GQA_OK)
+                return rc;
+            a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        }
         a.B = B;
         a.H_q = H_q;
         a.cluster = cs;
@@ -1633,7 +1640,8 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
         Stage stg(c->h_stage);
         const size_t o_sds = stg.add(sds.data(), sds.size());
         const size_t o_cow = stg.add(cows.data(), cows.size());
-        if ((rc = upload_stage(c, st)) != GQA_OK)
+        const bool inl = B <= decode_cluster_inline();
+        if ((!inl || !cows.empty()) && (rc = upload_stage(c, st)) != GQA_OK)
             return rc;
         if (!cows.empty() &&
             (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
@@ -1642,7 +1650,10 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
              })) != GQA_OK)
             return rc;
         ClusterDecodeLaunch a;
-        a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
+        if (inl)
+            a.host_seqs = sds.data();
+        else
+            a.seqs = (const SeqDesc *)(c->d_stage + o_sds);
         a.B = B;
         a.H_q = H_q;
         a.cluster = cs;
@@ -1885,21 +1896,26 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         return fail(GQA_EINVAL, "%s", kClusterNeeds);
     if (cs > 0) {
         // The clustered kernel of attn_decode: no partials leave the
-        // cluster, so only the descriptors go to the static array.
+        // cluster, so at most the descriptors go to the static array (small
+        // batches pass them in the launch parameters).
         std::vector<char> desc;
         Stage stg(desc);
         const size_t o_sds = stg.add(sds.data(), sds.size());
         if (desc.size() > kStaticDescBytes)
             return fail(GQA_ERANGE, "decode descriptors need %zu bytes; the static scratch reserves %zu",
                         desc.size(), kStaticDescBytes);
+        const bool inl = B <= decode_cluster_inline();
         char *scratch = nullptr;
-        if ((rc = static_scratch(c->device, &scratch)) != GQA_OK)
+        if (!inl && (rc = static_scratch(c->device, &scratch)) != GQA_OK)
             return rc;
         if ((rc = upload_tables(c, st, true)) != GQA_OK ||
-            (rc = staged_copy(c, scratch, desc.data(), desc.size(), st)) != GQA_OK)
+            (!inl && (rc = staged_copy(c, scratch, desc.data(), desc.size(), st)) != GQA_OK))
             return rc;
         ClusterDecodeLaunch a;
-        a.seqs = (const SeqDesc *)(scratch + o_sds);
+        if (inl)
+            a.host_seqs = sds.data();
+        else
+            a.seqs = (const SeqDesc *)(scratch + o_sds);
         a.B = B;
         a.H_q = H_q;
         a.cluster = cs;

@@ -38,10 +38,16 @@
 //    rounded to bf16 as the A operand straight from the score registers and
 //    V fragments by ldmatrix.trans;
 //  * the warps' (m, l, O) meet in shared memory; then each CTA stores its
-//    (m, l) into every CTA of the cluster and column slice j of its summed O
-//    into CTA j (distributed shared memory), one cluster barrier makes the
-//    stores visible, and CTA j merges the slices it holds and writes those
-//    columns of out.  Nothing goes through global memory but q, the pages
+//    (m, l) into every CTA of the cluster and column slice j (columns
+//    j * 128 / cs .. (j + 1) * 128 / cs - 1) of its summed O into CTA j
+//    (distributed shared memory), one cluster barrier makes the stores
+//    visible, and CTA j merges the slices it holds and writes those columns
+//    of out.  Cluster sizes need not be powers of two: 12-CTA clusters, for
+//    instance, put 96 SMs on eight (entry, head) pairs where 16-CTA ones do
+//    not all fit on the GPU at once.  (Stores of each warp's own partial
+//    straight into the merging CTAs, skipping the combine in shared memory,
+//    measured slower: eight times the remote stores and a merge over
+//    eight times the partials.)  Nothing goes through global memory but q, the pages
 //    and out, and no CTA waits on a flag another one sets.
 // Decode with append (app_k / app_v): the warp that holds the page of
 // position past writes the new K/V row into the landed stage, before reading
@@ -62,17 +68,8 @@ using namespace sm100;
 constexpr int D = 128;
 constexpr int kWarps = 8;                          // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;        // + one producer warp
-#ifndef GQA_DC_STAGES
-#define GQA_DC_STAGES 24
-#endif
-#ifndef GQA_DC_LANES
-#define GQA_DC_LANES 16
-#endif
-#ifndef GQA_DC_RED_APART
-#define GQA_DC_RED_APART 0
-#endif
-constexpr int kStages = GQA_DC_STAGES;
-constexpr int kIssuePages = GQA_DC_LANES / 2;      // pages whose copies are issued at once
+constexpr int kStages = 24;
+constexpr int kIssuePages = 8;                     // pages whose copies are issued at once
 // A stage is refilled by the lane that filled it (page i and i + kStages
 // have one issuing lane), so a lane's final wait on a stage is for its own
 // last copy into it; and by the warp that read it (page i and i + kStages
@@ -84,24 +81,29 @@ constexpr int kMaxCluster = 16;
 constexpr int kRows = 16;                          // MMA rows: the group's heads, zero-padded
 
 constexpr int kRedStride = D + 4;                  // warp-combine rows, padded against bank conflicts
+// CTA j of a cluster of cs merges columns [lo(j), lo(j + 1)), lo(j) =
+// j * 128 / cs; cs times the widest slice is at most 140 for cs <= 16.
+constexpr int kInStride = 144;
+__host__ __device__ constexpr int slice_lo(int j, int cs) { return j * D / cs; }
+// The CTA whose slice holds column col.
+__device__ __forceinline__ int slice_owner(int col, int cs) { return ((col + 1) * cs - 1) / D; }
+constexpr int kInline = 16;                        // entries whose descriptors travel in the parameters
 struct __align__(1024) DcSmem {
     unsigned char ring[kStages][2 * kBlockBytes];  // stage: K block, then V block
-#if GQA_DC_RED_APART
-    float red[kWarps][kRows][kRedStride];
-#endif
     // Received from the cluster's CTAs (rank r): unnormalised O rows,
-    // columns [r * nc, (r + 1) * nc) = this CTA's slice as CTA r holds it,
-    // nc = 128 / cluster size; and (m, l) per row.
-    float in_o[kRows][D];
+    // columns [r * w, (r + 1) * w) = this CTA's slice of w columns as CTA r
+    // holds it; and (m, l) per row.
+    float in_o[kRows][kInStride];
     float in_m[kMaxCluster][kRows], in_l[kMaxCluster][kRows];
     float wm[kWarps][kRows], wl[kWarps][kRows];    // per consumer warp
     uint64_t full[kStages], empty[kStages];
     int abort_;
 };
-static_assert(GQA_DC_RED_APART || kWarps * kRows * kRedStride * sizeof(float) <= sizeof(DcSmem::ring), "the warp combine reuses the ring");
+static_assert(kWarps * kRows * kRedStride * sizeof(float) <= sizeof(DcSmem::ring), "the warp combine reuses the ring");
 
 struct DcParams {
-    const SeqDesc *seqs;
+    const SeqDesc *seqs;                           // device descriptors, or null: inl[] holds them
+    SeqDesc inl[kInline];
     const int32_t *tables;
     unsigned char *pool;
     int32_t *err;
@@ -182,7 +184,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
     const uint32_t rank = cluster_rank(), cs = cluster_ncta();
-    const SeqDesc sd = p.seqs[b];
+    const SeqDesc sd = p.seqs ? p.seqs[b] : p.inl[b];
     const int past = sd.past;                              // the query's position (L - 1)
     const int L = past + 1;
     const int ws = window_start(past, p.window);           // first visible key
@@ -362,11 +364,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 
     // ---- the CTA's partial: warps combined -----------------------------------
     const bool ok = s.abort_ == 0;
-#if GQA_DC_RED_APART
-    float *red = &s.red[0][0][0];
-#else
     float *red = reinterpret_cast<float *>(s.ring[0]);     // [kWarps][kRows][kRedStride]
-#endif
     if (warp < kWarps && ok) {
         float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
@@ -386,7 +384,6 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
     }
     __syncthreads();
     // ---- into the cluster: column slice j of every row goes to CTA j ----------
-    const int nc = D / (int)cs;                        // cs is a power of two <= 16
     if (ok) {
         for (int e = threadIdx.x; e < G * D; e += kThreads) {
             const int row = e >> 7, col = e & (D - 1);
@@ -394,8 +391,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 #pragma unroll
             for (int w = 0; w < kWarps; ++w)              // a fixed order
                 a += red[((size_t)w * kRows + row) * kRedStride + col];
-            const int j = col / nc;
-            st_cluster(&s.in_o[row][rank * nc + (col - j * nc)], (uint32_t)j, a);
+            const int j = slice_owner(col, (int)cs), lo = slice_lo(j, (int)cs);
+            st_cluster(&s.in_o[row][rank * (slice_lo(j + 1, (int)cs) - lo) + (col - lo)], (uint32_t)j, a);
         }
     }
     for (int t = threadIdx.x; t < G * (int)cs; t += kThreads) {
@@ -411,7 +408,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
     }
     cluster_sync();           // every CTA's stores into this one are visible
 
-    // ---- the merge of this CTA's columns [rank * nc, (rank + 1) * nc) ------------
+    // ---- the merge of this CTA's columns [lo, lo + w) ---------------------------
+    const int lo = slice_lo((int)rank, (int)cs), w = slice_lo((int)rank + 1, (int)cs) - lo;
     if (threadIdx.x < G) {
         // Weights 2^(m_r - M) / sum_r 2^(m_r - M) l_r, in cluster rank order.
         const int row = threadIdx.x;
@@ -428,12 +426,12 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
             s.in_m[r][row] *= inv;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * nc; e += kThreads) {
-        const int row = e / nc, c = e - row * nc;
+    for (int e = threadIdx.x; e < G * w; e += kThreads) {
+        const int row = e / w, c = e - row * w;
         float a = 0.f;
         for (uint32_t r = 0; r < cs; ++r)
-            a = fmaf(s.in_m[r][row], s.in_o[row][r * nc + c], a);
-        p.out[((size_t)b * p.H_q + kvh * G + row) * D + rank * nc + c] = __float2bfloat16_rn(a);
+            a = fmaf(s.in_m[r][row], s.in_o[row][r * w + c], a);
+        p.out[((size_t)b * p.H_q + kvh * G + row) * D + lo + c] = __float2bfloat16_rn(a);
     }
 }
 
@@ -460,14 +458,16 @@ cudaError_t configure(int dev)
 
 bool decode_cluster_supported(int group) { return group >= 1 && group <= kRows; }
 
+int decode_cluster_inline() { return kInline; }
+
 int decode_cluster_capacity(int cluster)
 {
-    // Sizes 1, 2, 4, 8, 16, looked up once per device.
-    static std::atomic<int> cap[kMaxDev][5];
-    int dev = 0, k = 0;
-    while (k < 5 && (1 << k) != cluster)
-        ++k;
-    if (k == 5 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || configure(dev) != cudaSuccess)
+    // Looked up once per device and size.
+    static std::atomic<int> cap[kMaxDev][kMaxCluster + 1];
+    int dev = 0;
+    const int k = cluster;
+    if (k < 1 || k > kMaxCluster || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev ||
+        configure(dev) != cudaSuccess)
         return 0;
     int v = cap[dev][k].load(std::memory_order_acquire);
     if (v != 0)
@@ -512,7 +512,15 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     if (!encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox))
         return cudaErrorInvalidValue;
     DcParams prm;
-    prm.seqs = a.seqs;
+    if (a.host_seqs && a.B <= kInline) {
+        prm.seqs = nullptr;
+        for (int i = 0; i < a.B; ++i)
+            prm.inl[i] = a.host_seqs[i];
+    } else if (a.seqs) {
+        prm.seqs = a.seqs;
+    } else {
+        return cudaErrorInvalidValue;
+    }
     prm.tables = pv.tables;
     prm.pool = (unsigned char *)pv.pool;
     prm.err = pv.err;

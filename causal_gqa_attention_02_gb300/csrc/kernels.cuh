@@ -178,7 +178,8 @@ bool encode_tmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *d
 // that reads that page.  ev_start, if given, is recorded right before the
 // launch.
 struct ClusterDecodeLaunch {
-    const SeqDesc *seqs;
+    const SeqDesc *seqs = nullptr;       // device descriptors [B], or
+    const SeqDesc *host_seqs = nullptr;  // host descriptors, passed in the parameters (B <= decode_cluster_inline())
     int B;
     int H_q;
     int cluster;
@@ -188,6 +189,7 @@ struct ClusterDecodeLaunch {
     const void *app_v = nullptr;
 };
 bool decode_cluster_supported(int group);
+int decode_cluster_inline();   // largest B whose descriptors travel in the launch parameters
 // Largest number of clusters of `cluster` CTAs the device holds at once (0:
 // that size cannot be launched).  The device must be current.
 int decode_cluster_capacity(int cluster);

@@ -5,7 +5,9 @@ Prefill/Decode 推理路径", decode lesson: the new query reads every cached ke
 its own included; PagedAttention: keys through the block table): each
 (entry, KV head) is one thread-block cluster whose CTAs split its pages and
 merge their partial (m, l, O) in distributed shared memory.  Cases: every
-group size it serves (g = 1 .. 16), ragged lengths from one token (so some
+group size it serves (g = 1 .. 16), cluster sizes from 3 to 16 (powers of
+two and not), descriptors in the launch parameters (up to 16 entries) and
+in device memory (20 entries), ragged lengths from one token (so some
 CTAs of a cluster hold no page) to past 8K, page-boundary lengths, the
 wide-GQA decode at full size (every output element), sliding windows,
 scores whose maximum grows by far more than 2^8 from page range to page
@@ -65,6 +67,7 @@ CASES = [
     (64, 8, [3000]),                      # g = 8
     (12, 1, [9000, 257]),                 # g = 12, one KV head
     (128, 8, [700, 3000]),                # g = 16: every MMA row a head
+    (8, 2, [40 * i + 3 for i in range(20)]),   # 20 entries: descriptors from device memory, clusters of 3
 ]
 
 
