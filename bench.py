@@ -56,6 +56,7 @@ KERNEL_SOURCES = {
     "prefill_tc": "causal_gqa_attention_02_gb300/csrc/k_prefill_tc.cu",
     "attn_simt": "causal_gqa_attention_02_gb300/csrc/k_simt.cu",
     "decode_split": "causal_gqa_attention_02_gb300/csrc/k_decode.cu",
+    "decode_cluster": "causal_gqa_attention_02_gb300/csrc/k_decode_cluster.cu",
 }
 
 
@@ -437,7 +438,7 @@ def bench_decode(torch, gqa, dist, args, peaks, peak_src, want_cpu):
     kv_bytes = (moved[0] - m0) // args.steps          # per launch (the mean, under a window)
     cache.profile(False)
     prof = cache.profile_read()
-    kernel = max(("prefill_tc", "decode_split", "attn_simt"), key=lambda x: prof[x][1])
+    kernel = max(("prefill_tc", "decode_split", "decode_cluster", "attn_simt"), key=lambda x: prof[x][1])
     launches, kms = prof[kernel]
     avg_ms = kms / max(1, launches)
     achieved = kv_bytes / (avg_ms / 1e3) / 1e9
@@ -680,8 +681,18 @@ def bench_wide(torch, gqa, dist, args, peaks, want_cpu=False):
     c.profile(False)
     prof = c.profile_read()
     q_ms = qa.elapsed_time(qb)
-    kname = max(("prefill_tc", "decode_split", "attn_simt"), key=lambda x: prof[x][0])
+    kname = max(("prefill_tc", "decode_split", "decode_cluster", "attn_simt"), key=lambda x: prof[x][0])
     k_us = prof[kname][1] / max(1, prof[kname][0]) * 1e3
+    # The same queued run without per-launch events: the device time of a
+    # step as a decode loop sees it (launch gaps included, no event pairs).
+    torch.cuda.synchronize()
+    na, nb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(host_s * 1.5 * 2.1e9))
+    na.record()
+    decode_all()
+    nb.record()
+    nb.synchronize()
+    n_us = na.elapsed_time(nb) / steps * 1e3
     step_ms = []
     for t in range(steps):                          # L2 flushed before every step
         flush.zero_()
@@ -695,26 +706,35 @@ def bench_wide(torch, gqa, dist, args, peaks, want_cpu=False):
     dec = {"steps": steps, "kv_gb": round(kv_bytes / 1e9, 3),
            "l2_resident": {"us_per_step": round(t_res / steps * 1e3, 2),
                            "gbs": round(kv_bytes / (t_res / 1e3) / 1e9, 1)},
-           "kernel": {"name": kname, "us_per_launch": round(k_us, 2),
+           "kernel": {"name": kname, "us_per_launch_events": round(k_us, 2),
                       "gbs": round(kv_bytes / steps / (k_us / 1e6) / 1e9, 1),
+                      "note": "each launch bracketed by the library's profiling events (start event after the "
+                              "host-side preparation): launch latency and event overhead included",
                       "append_us_per_launch": round(prof["cache_write"][1] / max(1, prof["cache_write"][0]) * 1e3, 2)},
            "queued": {"us_per_step": round(q_ms / steps * 1e3, 2), "gbs": round(kv_bytes / (q_ms / 1e3) / 1e9, 1),
                       "host_us_per_step": round(host_q / steps * 1e6, 2),
                       "how": "all steps queued behind a sleep kernel; span of the run on the GPU (append + "
                              "decode + profiling events)"},
+           "queued_no_events": {"us_per_step": round(n_us, 2), "gbs": round(kv_bytes / steps / (n_us / 1e6) / 1e9, 1),
+                                "how": "the queued run again without per-launch events: device time per step "
+                                       "(descriptor uploads, launch gaps and the fused append+decode kernel)"},
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
-           "roofline": {"bound": "hbm", "achieved": round(kv_bytes / steps / (k_us / 1e6) / 1e9, 1),
+           "roofline": {"bound": "hbm", "achieved": round(kv_bytes / steps / (n_us / 1e6) / 1e9, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(kv_bytes / steps / (k_us / 1e6) / 1e9 / peaks["hbm_gbs"], 4), "traffic": None,
-                        "kernel": kname, "kernel_ms": round(k_us / 1e3, 5),
+                        "frac": round(kv_bytes / steps / (n_us / 1e6) / 1e9 / peaks["hbm_gbs"], 4),
+                        "traffic": traffic_for("wide_decode", kname),
+                        "kernel": kname, "kernel_ms": round(n_us / 1e3, 5),
                         "algorithmic_bytes_per_launch": kv_bytes // steps,
-                        "note": "kernel device time with the 34 MB of K/V L2-resident (steps queued ahead)"},
+                        "note": "device time per queued step, one event pair around all steps (no per-launch "
+                                "events); the 34 MB of K/V is L2-resident; traffic: one launch with cold caches "
+                                "under ncu"},
            "note": "one step = attn_decode_append of one sequence, called from Python: the step times "
                    "include the host side of the call, which is longer than the GPU work; 34 MB of K/V fits "
-                   "in L2; kernel = device time of the decode launch alone (L2-resident), measured with the "
-                   "steps queued ahead of the GPU; l2_flushed = each step after a 512 MiB L2 flush"}
+                   "in L2; queued_no_events = device time per step with the steps queued ahead of the GPU and "
+                   "no per-launch events (L2-resident); kernel = each launch bracketed by events; l2_flushed = "
+                   "each step after a 512 MiB L2 flush"}
     flags = c.check()
     c.close()
     return {"workload": "bf16 wide GQA: B=1, H_q=48, H_kv=8 (g=6), d_h=128, prefill T=%d, then %d append+decode "
@@ -848,7 +868,7 @@ def main():
                     help="caches with the rotary position mechanism applied by the library")
     ap.add_argument("--pre-position", action="store_true",
                     help="with --rope: caches that store keys before the rotation and rotate them when read")
-    ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto",
+    ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core", "cluster"], default="auto",
                     help="decode kernel of attn_decode (auto: tensor-core for bf16, d_h = 128)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="decode cache type (fp8: FP8 E4M3 codes with per-row scales; decode only)")
