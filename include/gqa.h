@@ -124,9 +124,12 @@ typedef struct {
                                     0 (only with rope = 1): keys are stored exactly as given
                                     and every attention kernel rotates each key by its
                                     position as it reads it, so the stored keys do not depend
-                                    on where they sit ([P3] prefix caching).  Such a cache is
-                                    read by the CUDA-core kernels (the generic prefill and the
-                                    split-K decode), not the tensor-core ones.               */
+                                    on where they sit ([P3] prefix caching).  A bf16 prefill
+                                    with d_h = 128 on such a cache first copies every page the
+                                    call reads, keys rotated, to library-owned scratch (one
+                                    rotation per page per call) and runs the tensor-core kernel
+                                    on the copy; decode runs on the split-K CUDA-core kernel,
+                                    which rotates each key in registers as it reads it.       */
     int32_t layout_version;      /* must be GQA_LAYOUT_VERSION                              */
     const int32_t *page_order;   /* host, optional: permutation of 0..num_pages-1 giving the
                                     order in which free pages are handed out (NULL = identity).
@@ -426,6 +429,10 @@ int attn_decode_append_host(gqa_cache *cache, int32_t B, const int32_t *seq_ids,
  * happens only when the host is two calls ahead of the GPU.
  * On each device, the first call looks up the array's device address
  * (cudaGetSymbolAddress).  Make that first call before any stream capture.
+ * On the clustered decode kernel (GQA_DECODE_CLUSTER, the automatic choice
+ * for small batches) partials never leave the cluster: only the descriptors
+ * of a call with more than 16 entries go to the array (up to 16 travel in
+ * the launch parameters), and no counters are used.
  * Every call shares the one array, and the array keeps the last call's
  * contents.  The merge counters must start at zero, so each call clears the
  * ones it uses (an asynchronous memset on `stream`); every other part is
