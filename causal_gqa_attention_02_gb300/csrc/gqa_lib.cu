@@ -989,19 +989,24 @@ int decode_uses_tc(const gqa_cache *c, int G)
 // Cluster size of the clustered decode kernel for a call of B single-token
 // queries whose longest sequence holds max_len tokens (the query's own
 // included), with query rows q and, for a fused append, new rows k_new and
-// v_new; 0 when another kernel serves the call; -1 when the clustered kernel
-// was asked for but cannot serve it.  Automatic choice: when there are at
-// most half as many (entry, KV head) pairs as SMs, so every pair gets two or
-// more SMs.  The cluster is the largest size (at most 16, and at most the
-// pages of the longest sequence) such that the pairs' clusters fit the SMs
-// and are resident together.
+// v_new (bf16 caches only: an FP8 cache's write quantises in its own
+// kernel); 0 when another kernel serves the call; -1 when the clustered
+// kernel was asked for but cannot serve it.  Automatic choice: when there
+// are at most half as many (entry, KV head) pairs as SMs, so every pair
+// gets two or more SMs (larger batches run the tensor-core kernel, or for
+// an FP8 cache the split-K CUDA-core one: one CTA per pair walking a whole
+// sequence leaves an SM too few warps to hide HBM latency behind the
+// conversions of the codes).  The cluster is the largest size (at most 16,
+// and at most the pages of the longest sequence) such that the pairs'
+// clusters fit the SMs and are resident together.
 int decode_cluster_for(const gqa_cache *c, int G, int B, int32_t max_len, const void *q,
                        const void *k_new = nullptr, const void *v_new = nullptr)
 {
     const int32_t H_kv = c->desc.num_kv_heads;
-    const bool ok = c->desc.dtype == GQA_DTYPE_BF16 && c->desc.head_dim == 128 && c->cc >= 100 &&
+    const bool q8 = c->desc.dtype == GQA_DTYPE_FP8_E4M3;
+    const bool ok = (c->desc.dtype == GQA_DTYPE_BF16 || q8) && c->desc.head_dim == 128 && c->cc >= 100 &&
                     c->desc.rope == 0 && decode_cluster_supported(G) && B >= 1 && B <= 65535 && H_kv <= 65535 &&
-                    ((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new) % 16 == 0;
+                    !(q8 && k_new) && ((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new) % 16 == 0;
     if (c->decode_kernel == GQA_DECODE_CLUSTER) {
         if (!ok)
             return -1;
@@ -1018,8 +1023,8 @@ int decode_cluster_for(const gqa_cache *c, int G, int B, int32_t max_len, const 
     return 1;
 }
 
-static const char *kClusterNeeds = "the clustered decode kernel needs a bf16 cache with d_h = 128, no rotary, "
-                                   "H_q/H_kv <= 16 and 16-byte aligned q (and k_new, v_new)";
+static const char *kClusterNeeds = "the clustered decode kernel needs a bf16 or FP8 E4M3 cache with d_h = 128, "
+                                   "no rotary, H_q/H_kv <= 16 and 16-byte aligned q (and k_new, v_new)";
 
 // ---------------------------------------------------------------------------
 // The hot path.
@@ -1610,7 +1615,9 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
             if (known)
                 max_len = std::max(max_len, c->seqs[seq_ids[b]].len + 1);
         }
-        if (known && (cs = decode_cluster_for(c, G, B, max_len, q, k_new, v_new)) < 0)
+        // An FP8 cache's write quantises in its own kernel: write, then decode.
+        if (known && c->desc.dtype != GQA_DTYPE_FP8_E4M3 &&
+            (cs = decode_cluster_for(c, G, B, max_len, q, k_new, v_new)) < 0)
             return fail(GQA_EINVAL, "%s", kClusterNeeds);
     }
     if (cs == 0 && (!use_tc || c->desc.dtype == GQA_DTYPE_FP8_E4M3)) {
@@ -1763,8 +1770,10 @@ int gqa_set_decode_kernel(gqa_cache *c, int32_t kernel)
         return fail(GQA_EINVAL, "decode kernel %d is not GQA_DECODE_AUTO, _TENSOR_CORE, _CUDA_CORE or _CLUSTER",
                     kernel);
     if (kernel == GQA_DECODE_CLUSTER &&
-        (c->desc.dtype != GQA_DTYPE_BF16 || c->desc.head_dim != 128 || c->desc.rope != 0))
-        return fail(GQA_EINVAL, "the clustered decode kernel needs a bf16 cache with d_h = 128 and no rotary");
+        ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128 ||
+         c->desc.rope != 0))
+        return fail(GQA_EINVAL, "the clustered decode kernel needs a bf16 or FP8 E4M3 cache with d_h = 128 and "
+                                "no rotary");
     if (kernel == GQA_DECODE_TENSOR_CORE &&
         ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) || c->desc.head_dim != 128 ||
          c->desc.keys_post_position != 1))
@@ -1863,10 +1872,6 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
     if (use_tc < 0)
         return fail(GQA_EINVAL, "the tensor-core decode kernel needs a bf16 cache with d_h = 128, post-position keys "
                                 "and H_q/H_kv <= 128");
-    if (!use_tc && ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) ||
-                    c->desc.head_dim != 128 || !decode_split_supported(G)))
-        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 or FP8 E4M3 cache with d_h = 128 (and H_q/H_kv <= "
-                                "8 on the CUDA-core kernel)");
     if (c->meta_only)
         return fail(GQA_EINVAL, "attn_decode_static needs a cache with a device pool");
     if (!q || !out)
@@ -1925,6 +1930,10 @@ extern "C" int attn_decode_static(gqa_cache *c, int32_t B, const int32_t *seq_id
         return run_kernel(c, GQA_KERNEL_DECODE_CLUSTER, st, "clustered decode kernel (static scratch)",
                           [&](cudaEvent_t ev) { return launch_decode_cluster(pv, a, st, ev); });
     }
+    if (!use_tc && ((c->desc.dtype != GQA_DTYPE_BF16 && c->desc.dtype != GQA_DTYPE_FP8_E4M3) ||
+                    c->desc.head_dim != 128 || !decode_split_supported(G)))
+        return fail(GQA_EINVAL, "attn_decode_static needs a bf16 or FP8 E4M3 cache with d_h = 128 (and H_q/H_kv <= "
+                                "8 on the CUDA-core kernel)");
 
     if (use_tc) {
         // The plan of attn_decode (so the results are the same bits), with

@@ -110,6 +110,7 @@ struct DcParams {
     const __nv_bfloat16 *q;
     __nv_bfloat16 *out;
     const __nv_bfloat16 *app_k, *app_v;
+    const float *scales;                           // FP8 E4M3: scale of (block, slot) at block * 16 + slot
     int stride, num_pages, H_kv, H_q, G, window;
 };
 
@@ -167,6 +168,45 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// E4M3 codes 0, 1 of w as an f16 pair (lo) and codes 2, 3 (hi), the lower
+// code in the lower half: every E4M3 value is exact in f16.
+__device__ __forceinline__ void e4m3x4_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// FP8 E4M3 stage: a page block is 16 slots of 128 code bytes, one 128-byte
+// line each, swizzled by the TMA copy: 16-byte unit c of slot s sits at
+// s * 128 + (c xor (s % 8)) * 16.  K codes at 0, V codes at 2048, then the
+// 16 K and the 16 V row scales.
+constexpr int kQ8Block = kPageTokens * D;          // 2 KB
+__device__ __forceinline__ uint32_t q8_off(int s, int c) { return (uint32_t)(s << 7) + (uint32_t)(((c ^ (s & 7)) << 4)); }
+
 // Byte offset, within a landed page block, of 16-byte unit c (columns
 // 8c .. 8c + 7) of slot s: the pool's block layout (two groups of 8 slots,
 // each stored 128-byte chunk by chunk) as the 128-byte swizzle of the TMA
@@ -176,6 +216,20 @@ __device__ __forceinline__ uint32_t stage_off(int s, int c)
     return (uint32_t)((((s >> 3) << 4) + ((c >> 3) << 3) + (s & 7)) << 7) + (uint32_t)(((c & 7) ^ (s & 7)) << 4);
 }
 
+// Q8: the pool holds FP8 E4M3 codes and row scales.  Codes convert exactly
+// to f16, so both products run on f16 mma.sync: each lane's ldmatrix
+// register holds four consecutive codes of a key row (dims 4j .. 4j + 3 of a
+// 16-dim k-step), which is the B fragment of k indices 2j, 2j + 1 and
+// 2j + 8, 2j + 9 -- a fixed permutation of the dims inside each k-step that
+// q's A fragments follow (the contraction does not depend on the order).  q
+// enters f16 after an exact power-of-two scaling per head (undone, with the
+// key row's scale, on the fp32 score).  For O += P V the value scales are
+// folded into P: P' = P s_v / R, R the largest value scale the warp has met
+// (O is rescaled when R grows, as for the softmax maximum, and multiplied by
+// R at the end); ldmatrix.trans plus a byte permute give the key pairs of
+// the B fragments, whose n columns are the even and the odd dims of a
+// 16-dim unit (undone when O is combined).
+template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 {
@@ -208,6 +262,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
     const int r0 = lane >> 2, qc = (lane & 3) * 2;         // fragment row / column pair of this lane
     float o[D / 8][4];                                     // O rows r0, r0 + 8; columns 8j + qc, + 1
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float R = 0.f;                                         // Q8: largest value scale met so far (O is in units of R)
 
     if (warp == kWarps) {
         // ---- producer ---------------------------------------------------
@@ -224,13 +279,29 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                     break;
                 }
                 int page = tab[i];
-                if ((unsigned)page >= (unsigned)p.num_pages) {
+                const bool valid = (unsigned)page < (unsigned)p.num_pages;
+                if (!valid) {
                     if (kv == 0)
                         atomicOr(p.err, kErrPageId);
                     page = p.num_pages;                    // out of range: the box reads zeros
                 }
-                mbar_arrive_expect_tx(&s.full[st], kBlockBytes);
-                tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kBlockBytes, 0, 0, (page * 2 + kv) * p.H_kv + kvh);
+                const int blk = (page * 2 + kv) * p.H_kv + kvh;
+                if constexpr (Q8) {
+                    float *sdst = reinterpret_cast<float *>(s.ring[st] + 2 * kQ8Block) + 16 * kv;
+                    if (valid) {
+                        mbar_arrive_expect_tx(&s.full[st], kQ8Block + 64);
+                        tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kQ8Block, 0, 0, blk);
+                        bulk_load(sdst, p.scales + (size_t)blk * kPageTokens, 64, &s.full[st]);
+                    } else {
+                        for (int z = 0; z < kPageTokens; ++z)
+                            sdst[z] = 0.f;
+                        mbar_arrive_expect_tx(&s.full[st], kQ8Block);
+                        tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kQ8Block, 0, 0, blk);
+                    }
+                } else {
+                    mbar_arrive_expect_tx(&s.full[st], kBlockBytes);
+                    tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kBlockBytes, 0, 0, blk);
+                }
                 issued = i + 1;
             }
             // Every issued copy lands before the ring is reused or the CTA
@@ -249,7 +320,9 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
         // Q as the A operand of each k-step: rows r0 / r0 + 8 (zero past g),
         // columns 16 kk + qc, + 1 and 16 kk + 8 + qc, + 1.
         uint32_t qa[D / 16][4];
-        {
+        const float kScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+        float qs0 = kScale, qs1 = kScale;                  // score factor of rows r0, r0 + 8
+        if constexpr (!Q8) {
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * p.H_q + kvh * G + r0) * D);
             const uint32_t *q1 = q0 + 8 * D / 2;
 #pragma unroll
@@ -259,11 +332,53 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                 qa[kk][2] = r0 < G ? q0[8 * kk + 4 + qc / 2] : 0u;
                 qa[kk][3] = r0 + 8 < G ? q1[8 * kk + 4 + qc / 2] : 0u;
             }
+        } else {
+            // Rows r0 / r0 + 8, dims 16 kk + 4j .. + 3 (j = lane % 4): one
+            // 8-byte load each; scaled by 2^e so the row's largest |q| lies
+            // in [2^14, 2^15), then rounded to f16.
+            const uint2 *q0 = reinterpret_cast<const uint2 *>(p.q + ((size_t)b * p.H_q + kvh * G + r0) * D) + (lane & 3);
+            const uint2 *q1 = q0 + 8 * D / 4;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if (r0 < G) {
+                    const uint2 u = q0[4 * kk];
+                    a0 = fmaxf(fmaxf(a0, fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xffff0000u)))),
+                               fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xffff0000u))));
+                }
+                if (r0 + 8 < G) {
+                    const uint2 u = q1[4 * kk];
+                    a1 = fmaxf(fmaxf(a1, fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xffff0000u)))),
+                               fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xffff0000u))));
+                }
+            }
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+            auto pow2_exp = [](float a) {                  // e with a * 2^e in [2^14, 2^15), clamped
+                if (!(a > 0.f))
+                    return 0;
+                const int E = (int)((__float_as_uint(a) >> 23) & 0xff) - 127;
+                return max(-126, min(126, 14 - E));
+            };
+            const int e0 = pow2_exp(a0), e1 = pow2_exp(a1);
+            const float f0 = __uint_as_float((uint32_t)(e0 + 127) << 23), f1 = __uint_as_float((uint32_t)(e1 + 127) << 23);
+            qs0 = kScale * __uint_as_float((uint32_t)(127 - e0) << 23);
+            qs1 = kScale * __uint_as_float((uint32_t)(127 - e1) << 23);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint2 u0 = r0 < G ? q0[4 * kk] : make_uint2(0u, 0u);
+                const uint2 u1 = r0 + 8 < G ? q1[4 * kk] : make_uint2(0u, 0u);
+                qa[kk][0] = pack_f16x2(__uint_as_float(u0.x << 16) * f0, __uint_as_float(u0.x & 0xffff0000u) * f0);
+                qa[kk][2] = pack_f16x2(__uint_as_float(u0.y << 16) * f0, __uint_as_float(u0.y & 0xffff0000u) * f0);
+                qa[kk][1] = pack_f16x2(__uint_as_float(u1.x << 16) * f1, __uint_as_float(u1.x & 0xffff0000u) * f1);
+                qa[kk][3] = pack_f16x2(__uint_as_float(u1.y << 16) * f1, __uint_as_float(u1.y & 0xffff0000u) * f1);
+            }
         }
 #pragma unroll
         for (int j = 0; j < D / 8; ++j)
             o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        const float kScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
         const int mi = lane >> 3, rr = lane & 7;           // ldmatrix: matrix and row this lane addresses
         const uint32_t ring0 = smem_u32(s.ring[0]);
         for (int i = warp; i < npg; i += kWarps) {
@@ -275,9 +390,9 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                 }
                 break;
             }
-            const uint32_t kb = ring0 + (uint32_t)st * (2 * kBlockBytes), vb = kb + kBlockBytes;
+            const uint32_t kb = ring0 + (uint32_t)st * (2 * kBlockBytes), vb = kb + (Q8 ? kQ8Block : kBlockBytes);
             const int pos0 = (pfirst + i_lo + i) * kPageTokens;    // position of the page's slot 0
-            if (p.app_k && pos0 <= past && past < pos0 + kPageTokens) {
+            if (!Q8 && p.app_k && pos0 <= past && past < pos0 + kPageTokens) {
                 // The appended row: lanes 0-15 its K units, 16-31 its V units.
                 const int slot = past - pos0, kv = lane >> 4, c = lane & 15;
                 const __nv_bfloat16 *src = (kv ? p.app_v : p.app_k) + ((size_t)b * p.H_kv + kvh) * D + 8 * c;
@@ -291,12 +406,41 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
             }
             // S = Q K^T: n-tile 0 = keys 0-7, n-tile 1 = keys 8-15.
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float mul[2][2];                               // score factor per (n-tile, key of the lane)
+            float vsk[2][2];                               // Q8: value scale of those keys
+            if constexpr (!Q8) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb + stage_off(8 * (mi >> 1) + rr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                mma_bf16(sc[0], qa[kk], b0, b1);
-                mma_bf16(sc[1], qa[kk], b2, b3);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + stage_off(8 * (mi >> 1) + rr, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                    mma_bf16(sc[0], qa[kk], b0, b1);
+                    mma_bf16(sc[1], qa[kk], b2, b3);
+                }
+                mul[0][0] = mul[0][1] = mul[1][0] = mul[1][1] = 1.f;
+            } else {
+                // Matrices of one ldmatrix: (keys 0-7, k-step 2h), (keys
+                // 0-7, 2h + 1), (keys 8-15, 2h), (keys 8-15, 2h + 1).
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t w0, w1, w2, w3, lo, hi;
+                    ldsm_x4(kb + q8_off(8 * (mi >> 1) + rr, 2 * h + (mi & 1)), w0, w1, w2, w3);
+                    e4m3x4_f16(w0, lo, hi);
+                    mma_f16(sc[0], qa[2 * h], lo, hi);
+                    e4m3x4_f16(w1, lo, hi);
+                    mma_f16(sc[0], qa[2 * h + 1], lo, hi);
+                    e4m3x4_f16(w2, lo, hi);
+                    mma_f16(sc[1], qa[2 * h], lo, hi);
+                    e4m3x4_f16(w3, lo, hi);
+                    mma_f16(sc[1], qa[2 * h + 1], lo, hi);
+                }
+                const float *ksc = reinterpret_cast<const float *>(s.ring[st] + 2 * kQ8Block);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        mul[nt][e] = ksc[8 * nt + qc + e];
+                        vsk[nt][e] = ksc[kPageTokens + 8 * nt + qc + e];
+                    }
             }
             // Visible keys only, in exp2 units.
 #pragma unroll
@@ -304,7 +448,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = pos0 + 8 * nt + qc + (e & 1);
-                    sc[nt][e] = (t <= past && t >= ws) ? sc[nt][e] * kScale : -INFINITY;
+                    sc[nt][e] = (t <= past && t >= ws) ? sc[nt][e] * (e < 2 ? qs0 : qs1) * mul[nt][e & 1] : -INFINITY;
                 }
             float x0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
             float x1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -314,7 +458,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
             x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
             const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
             const float f0 = n0 == -INFINITY ? 0.f : n0, f1 = n1 == -INFINITY ? 0.f : n1;
-            const float a0 = ex2(m0 - f0), a1 = ex2(m1 - f1);   // 0 while nothing was visible
+            float a0 = ex2(m0 - f0), a1 = ex2(m1 - f1);   // 0 while nothing was visible
             m0 = n0;
             m1 = n1;
             float pr[2][4];
@@ -325,6 +469,19 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                     pr[nt][e] = ex2(sc[nt][e] - (e < 2 ? f0 : f1));
             l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
             l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+            float invR = 1.f;
+            if constexpr (Q8) {
+                // The page's largest value scale (all 16 keys: the quad holds them).
+                float vm = fmaxf(fmaxf(vsk[0][0], vsk[0][1]), fmaxf(vsk[1][0], vsk[1][1]));
+                vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
+                vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
+                if (vm > R) {                              // the same in every lane; O = 0 while R = 0
+                    a0 *= R / vm;
+                    a1 *= R / vm;
+                    R = vm;
+                }
+                invR = R > 0.f ? 1.f / R : 0.f;
+            }
             if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
@@ -334,16 +491,42 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                     o[j][3] *= a1;
                 }
             }
-            // O += P V: P (16 rows x 16 keys) is the A operand as the score
-            // fragments hold it; n-tile j = columns 8j .. 8j + 7.
-            const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
-                                    pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+            if constexpr (!Q8) {
+                // O += P V: P (16 rows x 16 keys) is the A operand as the
+                // score fragments hold it; n-tile j = columns 8j .. 8j + 7.
+                const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                                        pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + stage_off(8 * (mi & 1) + rr, 2 * j + (mi >> 1)), b0, b1, b2, b3);
-                mma_bf16(o[2 * j], pa, b0, b1);
-                mma_bf16(o[2 * j + 1], pa, b2, b3);
+                for (int j = 0; j < D / 16; ++j) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + stage_off(8 * (mi & 1) + rr, 2 * j + (mi >> 1)), b0, b1, b2, b3);
+                    mma_bf16(o[2 * j], pa, b0, b1);
+                    mma_bf16(o[2 * j + 1], pa, b2, b3);
+                }
+            } else {
+                // P' = P s_v / R in f16.  Matrices of one ldmatrix.trans:
+                // (keys 0-7, unit 2h), (keys 8-15, 2h), (keys 0-7, 2h + 1),
+                // (keys 8-15, 2h + 1); a register holds the codes of dims
+                // 16u + 2(lane / 4), + 1 for keys 2(lane % 4), + 1; a byte
+                // permute makes key pairs per dim.  n-tile 2u + par = the
+                // dims 16u + 2n + par.
+                const float s00 = vsk[0][0] * invR, s01 = vsk[0][1] * invR;
+                const float s10 = vsk[1][0] * invR, s11 = vsk[1][1] * invR;
+                const uint32_t pa[4] = {pack_f16x2(pr[0][0] * s00, pr[0][1] * s01), pack_f16x2(pr[0][2] * s00, pr[0][3] * s01),
+                                        pack_f16x2(pr[1][0] * s10, pr[1][1] * s11), pack_f16x2(pr[1][2] * s10, pr[1][3] * s11)};
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t w0, w1, w2, w3, e0lo, e0hi, e1lo, e1hi;
+                    ldsm_x4_t(vb + q8_off(8 * (mi & 1) + rr, 2 * h + (mi >> 1)), w0, w1, w2, w3);
+                    e4m3x4_f16(prmt(w0, 0x3120), e0lo, e0hi);
+                    e4m3x4_f16(prmt(w1, 0x3120), e1lo, e1hi);
+                    mma_f16(o[4 * h], pa, e0lo, e1lo);
+                    mma_f16(o[4 * h + 1], pa, e0hi, e1hi);
+                    e4m3x4_f16(prmt(w2, 0x3120), e0lo, e0hi);
+                    e4m3x4_f16(prmt(w3, 0x3120), e1lo, e1hi);
+                    mma_f16(o[4 * h + 2], pa, e0lo, e1lo);
+                    mma_f16(o[4 * h + 3], pa, e0hi, e1hi);
+                }
             }
             __syncwarp();
             if (lane == 0)
@@ -372,14 +555,28 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
             M0 = fmaxf(M0, s.wm[w][r0]);
             M1 = fmaxf(M1, s.wm[w][r0 + 8]);
         }
-        const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0), c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
-        float *w0 = red + ((size_t)warp * kRows + r0) * kRedStride + qc, *w1 = w0 + 8 * kRedStride;
+        const float rs = Q8 ? R : 1.f;                     // Q8: O is in units of R
+        const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0) * rs, c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1) * rs;
+        float *w0 = red + ((size_t)warp * kRows + r0) * kRedStride, *w1 = w0 + 8 * kRedStride;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j) {
-            if (r0 < G)
-                *reinterpret_cast<float2 *>(w0 + 8 * j) = make_float2(o[j][0] * c0, o[j][1] * c0);
-            if (r0 + 8 < G)
-                *reinterpret_cast<float2 *>(w1 + 8 * j) = make_float2(o[j][2] * c1, o[j][3] * c1);
+            if constexpr (!Q8) {
+                if (r0 < G)
+                    *reinterpret_cast<float2 *>(w0 + 8 * j + qc) = make_float2(o[j][0] * c0, o[j][1] * c0);
+                if (r0 + 8 < G)
+                    *reinterpret_cast<float2 *>(w1 + 8 * j + qc) = make_float2(o[j][2] * c1, o[j][3] * c1);
+            } else {
+                // n-tile j = 2u + par, column c: dim 16u + 2c + par.
+                const int d0 = 16 * (j >> 1) + 2 * qc + (j & 1);
+                if (r0 < G) {
+                    w0[d0] = o[j][0] * c0;
+                    w0[d0 + 2] = o[j][1] * c0;
+                }
+                if (r0 + 8 < G) {
+                    w1[d0] = o[j][2] * c1;
+                    w1[d0 + 2] = o[j][3] * c1;
+                }
+            }
         }
     }
     __syncthreads();
@@ -446,9 +643,13 @@ cudaError_t configure(int dev)
         return cudaErrorInvalidDevice;
     if (done[dev].load(std::memory_order_acquire))
         return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {decode_cluster_kernel<false>, decode_cluster_kernel<true>}) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     if (e == cudaSuccess)
         done[dev].store(true, std::memory_order_release);
     return e;
@@ -484,7 +685,8 @@ int decode_cluster_capacity(int cluster)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel, &cfg) != cudaSuccess) {
+    // Both instantiations have the same block, shared memory and registers.
+    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -496,20 +698,23 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
                                   cudaEvent_t ev_start)
 {
     const int G = pv.H_kv > 0 ? a.H_q / pv.H_kv : 0;
-    if (pv.d != D || pv.dtype != kDtypeBf16 || pv.rope || !decode_cluster_supported(G) || a.cluster < 1 ||
-        a.cluster > kMaxCluster || a.B < 1 || a.B > 65535 || pv.H_kv > 65535)
+    const bool q8 = pv.dtype == kDtypeFp8;
+    if (pv.d != D || (pv.dtype != kDtypeBf16 && !q8) || pv.rope || !decode_cluster_supported(G) || a.cluster < 1 ||
+        a.cluster > kMaxCluster || a.B < 1 || a.B > 65535 || pv.H_kv > 65535 || (q8 && (a.app_k || !pv.scales)))
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || (e = configure(dev)) != cudaSuccess)
         return e;
-    // The pool as 128-byte lines: [block][32 lines][64 elements]; a box is
-    // one page block (4 KB).
+    // bf16: the pool as 128-byte lines, [block][32 lines][64 elements]; FP8:
+    // [block][16 slots][128 codes].  A box is one page block (4 KB, 2 KB).
     CUtensorMap mkv;
-    const cuuint64_t kvdims[3] = {64, 32, (cuuint64_t)pv.num_pages * 2 * pv.H_kv};
-    const cuuint64_t kvstr[2] = {128, 32 * 128};
-    const cuuint32_t kvbox[3] = {64, 32, 1};
-    if (!encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox))
+    const cuuint64_t blocks = (cuuint64_t)pv.num_pages * 2 * pv.H_kv;
+    const cuuint64_t kvdims[3] = {64, 32, blocks}, kv8dims[3] = {128, 16, blocks};
+    const cuuint64_t kvstr[2] = {128, 32 * 128}, kv8str[2] = {128, 16 * 128};
+    const cuuint32_t kvbox[3] = {64, 32, 1}, kv8box[3] = {128, 16, 1};
+    if (!(q8 ? encode_tmap(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true, true)
+             : encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)))
         return cudaErrorInvalidValue;
     DcParams prm;
     if (a.host_seqs && a.B <= kInline) {
@@ -528,6 +733,7 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     prm.out = (__nv_bfloat16 *)a.out;
     prm.app_k = (const __nv_bfloat16 *)a.app_k;
     prm.app_v = (const __nv_bfloat16 *)a.app_v;
+    prm.scales = pv.scales;
     prm.stride = pv.stride;
     prm.num_pages = pv.num_pages;
     prm.H_kv = pv.H_kv;
@@ -548,7 +754,8 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_cluster_kernel, mkv, prm);
+    return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, mkv, prm)
+              : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, mkv, prm);
 }
 
 }  // namespace gqa

@@ -1188,17 +1188,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder()
 }
 
 bool encode_tmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
-                 const cuuint32_t *box, bool bytes)
+                 const cuuint32_t *box, bool bytes, bool bytes_swizzled)
 {
     auto fn = encoder();
     if (!fn)
         return false;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    // bytes: FP8 code blocks, copied as they are (the kernel lays them out).
+    // bytes: FP8 code blocks, copied as they are (the tensor-core kernel lays
+    // them out itself) or 128-byte swizzled (read by ldmatrix).
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              bytes && !bytes_swizzled ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_wait_probe(int32_t *err, uint64_t limit_ns, cudaStream_t st)

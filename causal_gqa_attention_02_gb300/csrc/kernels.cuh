@@ -165,10 +165,10 @@ struct DecodeLaunch {
 bool decode_split_supported(int group);
 
 // Tiled tensor map over `base` (bf16 elements, 128-byte swizzle; bytes:
-// uint8 elements, no swizzle) with the driver's encoder.  False if the
-// encoder is unavailable or refuses the shape.
+// uint8 elements, no swizzle unless bytes_swizzled) with the driver's
+// encoder.  False if the encoder is unavailable or refuses the shape.
 bool encode_tmap(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
-                 const cuuint32_t *box, bool bytes = false);
+                 const cuuint32_t *box, bool bytes = false, bool bytes_swizzled = false);
 
 // bf16, d = 128 single-token decode with each (entry, KV head) served by a
 // cluster of `cluster` CTAs that split its pages and merge their partials

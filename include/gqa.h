@@ -444,12 +444,13 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
                        const void *q, void *out, void *stream);
 
 /* Decode kernel of attn_decode and attn_decode_static.
- *  GQA_DECODE_AUTO         (default) for a bf16 cache with d_h = 128: the
- *                          clustered kernel when it can serve the call and
- *                          there are at most half as many (entry, KV head)
- *                          pairs as SMs, else tensor-core; CUDA-core for
- *                          other caches (an FP8 E4M3 cache decodes faster
- *                          on the CUDA-core kernel).
+ *  GQA_DECODE_AUTO         (default) for a bf16 or FP8 E4M3 cache with
+ *                          d_h = 128: the clustered kernel when it can serve
+ *                          the call and there are at most half as many
+ *                          (entry, KV head) pairs as SMs; else tensor-core
+ *                          for bf16 and CUDA-core for FP8 (which decodes a
+ *                          large batch faster there); CUDA-core for other
+ *                          caches.
  *  GQA_DECODE_TENSOR_CORE  the prefill kernel with one query row per
  *                          sequence: every KV head's key tiles are read once
  *                          by TMA, a sequence's tiles are split into ranges
@@ -468,11 +469,13 @@ int attn_decode_static(gqa_cache *cache, int32_t B, const int32_t *seq_ids, int3
  *                          CTAs that split its pages (each page's K and V
  *                          read once by TMA, both products on mma.sync) and
  *                          merge their partial (m, l, O) through distributed
- *                          shared memory; no workspace.  Needs a bf16 cache
+ *                          shared memory; no workspace.  FP8 E4M3 codes are
+ *                          read as stored (f16 products, scales on the
+ *                          scores and on P).  Needs a bf16 or FP8 E4M3 cache
  *                          with d_h = 128 and no rotary (else GQA_EINVAL
  *                          here), H_q / H_kv <= 16 and q (for the fused
- *                          append also k_new and v_new) 16-byte aligned
- *                          (else GQA_EINVAL from the decode call).
+ *                          append, bf16 only, also k_new and v_new) 16-byte
+ *                          aligned (else GQA_EINVAL from the decode call).
  * All compute the same softmax; they differ in rounding order only.
  * Errors: GQA_EINVAL (unknown choice, or a kernel that cannot serve this
  * cache). */

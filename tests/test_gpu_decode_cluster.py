@@ -211,3 +211,73 @@ def test_cluster_rejections():
         gqa.attn_decode(c, ids, q[:, 1: 1 + 4 * 2 * 128].view(1, 8, 128))
     assert e.value.name == "EINVAL"
     assert c.check() == 0
+
+
+def _filled_fp8(rng, H_kv, lengths, window=0, zero_rows=False):
+    B, d = len(lengths), 128
+    per_seq = workloads.pages_for(max(lengths) + 4) + 1
+    pages = 2 * sum(workloads.pages_for(L + 4) for L in lengths) + 8
+    c = gqa.Cache(H_kv, d, pages, B, per_seq, dtype="fp8", window=window)
+    m = oracle.CacheModel(pages, B, per_seq, H_kv, d, "fp8", window=window)
+    ids, mids = [c.seq_create() for _ in range(B)], [m.create() for _ in range(B)]
+    for b, L in enumerate(lengths):
+        k = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        v = workloads.normal_bf16(rng, (1, L, H_kv, d))
+        if zero_rows:
+            # rows of zeros: scale 0 and zero codes, in K and in V, including
+            # every V row of the first pages (the value-scale maximum stays 0)
+            k[0, ::7] = 0
+            v[0, : min(L, 40)] = 0
+            v[0, ::5] = 0
+        gqa.kv_append(c, [ids[b]], dev(k, DT), dev(v, DT))
+        oracle.append(m, [mids[b]], k, v)
+    return c, m, ids, mids
+
+
+FP8_CASES = [
+    (32, 8, [1, 17, 300, 2049, 5000], 0, False),
+    (48, 8, [8300], 0, False),             # the wide-GQA shape: clusters of 12
+    (128, 8, [700, 3000], 0, False),       # g = 16
+    (8, 8, [4097, 33], 0, True),           # g = 1, zero rows
+    (32, 8, [6000, 250, 1800], 500, False),
+    (24, 2, [40 * i + 9 for i in range(20)], 0, True),   # 20 entries: descriptors in device memory
+]
+
+
+@pytest.mark.parametrize("H_q,H_kv,lengths,window,zero_rows", FP8_CASES)
+def test_cluster_decode_fp8_cache(H_q, H_kv, lengths, window, zero_rows):
+    # The codes stream through the page ring as they are stored (half the
+    # bytes of bf16); both products run on f16 mma.sync with the scales
+    # applied to the scores and folded into P.  The automatic choice for an
+    # FP8 cache with few (entry, KV head) pairs.
+    rng = np.random.default_rng(380 + H_q + len(lengths) + window)
+    c, m, ids, mids = _filled_fp8(rng, H_kv, lengths, window, zero_rows)
+    q = workloads.normal_bf16(rng, (len(lengths), H_q, 128))
+    o = _decode(c, ids, dev(q, DT))
+    assert_close(host_f64(o, DT), oracle.decode(m, mids, q), DT, "fp8 cluster decode")
+    s = gqa.attn_decode_static(c, ids, dev(q, DT))
+    assert torch.equal(o.view(torch.int16), s.view(torch.int16)), "static decode differs"
+    c.set_decode_kernel("cluster")
+    o2 = _decode(c, ids, dev(q, DT))
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert c.check() == 0
+
+
+def test_cluster_decode_fp8_large_scores():
+    # q scaled by 40 and keys growing along the sequence: scores far from
+    # N(0,1), the per-head power-of-two scaling of q and the key scales
+    # carry the range.
+    H_q, H_kv, L = 16, 2, 3000
+    rng = np.random.default_rng(395)
+    c = gqa.Cache(H_kv, 128, workloads.pages_for(L) + 8, 1, workloads.pages_for(L) + 1, dtype="fp8")
+    m = oracle.CacheModel(workloads.pages_for(L) + 8, 1, workloads.pages_for(L) + 1, H_kv, 128, "fp8")
+    s, ms = c.seq_create(), m.create()
+    scale = (1.0 + 0.02 * (np.arange(L) // 16)).astype(np.float32)[:, None, None]
+    k = workloads.bf16_bits(rng.standard_normal(size=(L, H_kv, 128), dtype=np.float32) * scale)
+    v = workloads.normal_bf16(rng, (L, H_kv, 128))
+    gqa.kv_append(c, [s], dev(k[None], DT), dev(v[None], DT))
+    oracle.append(m, [ms], k[None], v[None])
+    q = workloads.bf16_bits(rng.standard_normal(size=(1, H_q, 128), dtype=np.float32) * np.float32(40.0))
+    o = _decode(c, [s], dev(q, DT))
+    assert_close(host_f64(o, DT), oracle.decode(m, [ms], q), DT, "fp8 cluster decode, large scores")
+    assert c.check() == 0
