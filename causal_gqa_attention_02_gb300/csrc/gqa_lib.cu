@@ -35,6 +35,10 @@ namespace {
 
 thread_local std::string t_err;
 
+// Largest per-call copy of the call's block-table rows sent with a prefill's
+// descriptors (larger calls read the pool's tables, uploaded first).
+constexpr size_t kCompactTableBytes = 1u << 20;
+
 // Fixed cost of one prefill work item (Q load, pipeline refill, epilogue)
 // in quarters of a key tile, for balancing items over the persistent grid.
 constexpr int64_t kItemCostQuarters = 2;
@@ -1088,11 +1092,36 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         return GQA_OK;
 
     cudaStream_t st = (cudaStream_t)stream;
-    if ((rc = upload_tables(c, st)) != GQA_OK)
-        return rc;
     const int G = H_q / c->desc.num_kv_heads;
     const bool use_tc = (c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) &&
                         c->desc.head_dim == 128 && c->cc >= 100 && prefill_tc_supported(G, c->desc.num_kv_heads);
+    // The call's own block-table rows (row b = entry b, every page of the
+    // sequence after this write) travel with its descriptors in one upload;
+    // the device's table array is brought up to date by the next call that
+    // reads it (its entries stay marked dirty).  One copy queued before the
+    // kernels instead of two.  Pre-position calls rotate the pool's pages
+    // by the pool's tables and keep them current.
+    const bool pre = use_tc && c->desc.keys_post_position == 0;
+    std::vector<int32_t> ctab;
+    int32_t cstride = 1;
+    if (!pre) {
+        for (int b = 0; b < B; ++b)
+            cstride = std::max<int32_t>(cstride, (int32_t)c->seqs[sds[b].row].pages.size());
+        if ((size_t)B * cstride * sizeof(int32_t) > kCompactTableBytes)
+            cstride = 0;                                 // too large: the kernels read the pool's tables
+    }
+    if (!pre && cstride > 0) {
+        ctab.assign((size_t)B * cstride, -1);
+        for (int b = 0; b < B; ++b) {
+            const int32_t row = sds[b].row;
+            const size_t np = c->seqs[row].pages.size();
+            std::copy(c->h_tab.begin() + (size_t)row * c->stride(), c->h_tab.begin() + (size_t)row * c->stride() + np,
+                      ctab.begin() + (size_t)b * cstride);
+            sds[b].row = b;
+        }
+    } else if ((rc = upload_tables(c, st)) != GQA_OK) {
+        return rc;
+    }
     // Pre-position keys on the tensor-core path: the kernel reads keys as
     // stored, so every distinct page the call reads is first copied, keys
     // rotated by their positions, to a compact scratch pool, and the kernel
@@ -1166,6 +1195,7 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     const size_t o_rpages = stg.add(rot_pages.data(), rot_pages.size());
     const size_t o_rtab = stg.add(rot_tab.data(), rot_tab.size());
     const size_t o_rsds = stg.add(rot_sds.data(), rot_sds.size());
+    const size_t o_ctab = stg.add(ctab.data(), ctab.size());
     if (pre_tc && (rc = ensure_rot(c, rot_pages.size() * 2 * (size_t)c->desc.num_kv_heads * 4096)) != GQA_OK)
         return rc;
     TcSplitWs ws;
@@ -1173,7 +1203,11 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         return rc;
     if ((rc = upload_stage(c, st)) != GQA_OK)
         return rc;
-    const PoolView pv = c->view();
+    PoolView pv = c->view();
+    if (!ctab.empty()) {
+        pv.tables = (const int32_t *)(c->d_stage + o_ctab);
+        pv.stride = cstride;
+    }
     const SeqDesc *d_sds = (const SeqDesc *)(c->d_stage + o_sds);
     if (!cows.empty() &&
         (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
