@@ -257,6 +257,13 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
         s.abort_ = 0;
         fence_barrier_init();
     }
+    // Launched as a programmatic dependent of the kernel before it in the
+    // stream (often the previous decode step): the set-up above overlaps
+    // that kernel's end; q, the pool, the tables and out are touched only
+    // after it has completed.  The next launch may be scheduled once every
+    // CTA of this one is resident.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     __syncthreads();
 
     const int r0 = lane >> 2, qc = (lane & 3) * 2;         // fragment row / column pair of this lane
@@ -747,13 +754,15 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)a.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, mkv, prm)
               : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, mkv, prm);
 }
