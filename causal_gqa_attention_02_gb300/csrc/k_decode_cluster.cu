@@ -23,13 +23,14 @@
 //  * grid (cs, H_kv, B) in clusters of cs CTAs along x: CTA r of the cluster
 //    of (b, kvh) takes pages [r P / cs, (r + 1) P / cs) of the P pages that
 //    hold visible keys;
-//  * sixteen producer lanes request the CTA's pages up front, as far as a
-//    ring of kStages stages allows: a stage is the page's K block and V block
-//    (4 KB each, one TMA box each, 128-byte swizzled, issued by two lanes),
-//    completed on an mbarrier.  Lane 2p + kv issues block kv of pages p,
-//    p + 8, ...: the copies of eight pages are issued at once, since one
-//    thread issuing them in turn leaves the SM's copy engine idle between
-//    boxes;
+//  * eight producer lanes request the CTA's pages up front, as far as a
+//    ring of kStages stages allows: a stage is the page's K block and V
+//    block, one TMA box (8 KB, 128-byte swizzled: the two blocks are the
+//    kv = 0, 1 neighbours of a [2 page + kv][head] view of the pool),
+//    completed on an mbarrier.  Lane p issues pages p, p + 8, ...: the
+//    copies of eight pages are issued at once, since one thread issuing them
+//    in turn leaves the SM's copy engine idle between boxes, and one box per
+//    page rather than one per block halves the engine's per-copy cost;
 //  * kWarps consumer warps take the pages round robin.  The group's g heads
 //    are the rows of a 16-row mma.sync m16n8k16 tile (bf16 operands, fp32
 //    accumulation; rows past g hold zeros): S = Q K^T over the page's 16 keys
@@ -231,7 +232,8 @@ __device__ __forceinline__ uint32_t stage_off(int s, int c)
 // 16-dim unit (undone when O is combined).
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
+decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_constant__ CUtensorMap mSc,
+                      const DcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     DcSmem &s = *reinterpret_cast<DcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -251,7 +253,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&s.full[i], 2);
+            mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
         }
         s.abort_ = 0;
@@ -273,12 +275,14 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
 
     if (warp == kWarps) {
         // ---- producer ---------------------------------------------------
-        if (lane < 2 * kIssuePages) {
-            const int kv = lane & 1;
-            if (lane == 0)
+        if (lane < kIssuePages) {
+            if (lane == 0) {
                 prefetch_tmap(&mKV);
-            int issued = 0;                                // pages lane issued: lane/2, lane/2 + 8, ...
-            for (int i = lane >> 1; i < npg; i += kIssuePages) {
+                if (Q8)
+                    prefetch_tmap(&mSc);
+            }
+            int issued = 0;                                // pages lane issued: lane, lane + 8, ...
+            for (int i = lane; i < npg; i += kIssuePages) {
                 const int st = i % kStages;
                 if (i >= kStages && !mbar_wait(&s.empty[st], ((i / kStages) - 1) & 1, &s.abort_)) {
                     s.abort_ = 1;
@@ -286,28 +290,20 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
                     break;
                 }
                 int page = tab[i];
-                const bool valid = (unsigned)page < (unsigned)p.num_pages;
-                if (!valid) {
-                    if (kv == 0)
-                        atomicOr(p.err, kErrPageId);
-                    page = p.num_pages;                    // out of range: the box reads zeros
+                if ((unsigned)page >= (unsigned)p.num_pages) {
+                    atomicOr(p.err, kErrPageId);
+                    page = p.num_pages;                    // out of range: the boxes read zeros
                 }
-                const int blk = (page * 2 + kv) * p.H_kv + kvh;
+                // One box holds the page's K block and V block (block
+                // indices (2 page + kv) H_kv + head, kv = 0, 1); FP8 adds
+                // one for their two rows of scales.
                 if constexpr (Q8) {
-                    float *sdst = reinterpret_cast<float *>(s.ring[st] + 2 * kQ8Block) + 16 * kv;
-                    if (valid) {
-                        mbar_arrive_expect_tx(&s.full[st], kQ8Block + 64);
-                        tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kQ8Block, 0, 0, blk);
-                        bulk_load(sdst, p.scales + (size_t)blk * kPageTokens, 64, &s.full[st]);
-                    } else {
-                        for (int z = 0; z < kPageTokens; ++z)
-                            sdst[z] = 0.f;
-                        mbar_arrive_expect_tx(&s.full[st], kQ8Block);
-                        tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kQ8Block, 0, 0, blk);
-                    }
+                    mbar_arrive_expect_tx(&s.full[st], 2 * kQ8Block + 2 * kPageTokens * 4);
+                    tma_load_4d(&mKV, &s.full[st], s.ring[st], 0, 0, kvh, 2 * page);
+                    tma_load_3d(&mSc, &s.full[st], s.ring[st] + 2 * kQ8Block, 0, kvh, 2 * page);
                 } else {
-                    mbar_arrive_expect_tx(&s.full[st], kBlockBytes);
-                    tma_load_3d(&mKV, &s.full[st], s.ring[st] + kv * kBlockBytes, 0, 0, blk);
+                    mbar_arrive_expect_tx(&s.full[st], 2 * kBlockBytes);
+                    tma_load_4d(&mKV, &s.full[st], s.ring[st], 0, 0, kvh, 2 * page);
                 }
                 issued = i + 1;
             }
@@ -315,7 +311,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const DcParams p)
             // ends (copies of earlier uses of a stage were waited for by
             // their consumers before the stage was issued again).
             const int never = 0;
-            for (int i = lane >> 1; i < issued; i += kIssuePages)
+            for (int i = lane; i < issued; i += kIssuePages)
                 if (i + kStages >= issued && !mbar_wait(&s.full[i % kStages], (i / kStages) & 1, &never)) {
                     s.abort_ = 1;
                     atomicOr(p.err, kErrTimeout);
@@ -713,16 +709,21 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || (e = configure(dev)) != cudaSuccess)
         return e;
-    // bf16: the pool as 128-byte lines, [block][32 lines][64 elements]; FP8:
-    // [block][16 slots][128 codes].  A box is one page block (4 KB, 2 KB).
-    CUtensorMap mkv;
-    const cuuint64_t blocks = (cuuint64_t)pv.num_pages * 2 * pv.H_kv;
-    const cuuint64_t kvdims[3] = {64, 32, blocks}, kv8dims[3] = {128, 16, blocks};
-    const cuuint64_t kvstr[2] = {128, 32 * 128}, kv8str[2] = {128, 16 * 128};
-    const cuuint32_t kvbox[3] = {64, 32, 1}, kv8box[3] = {128, 16, 1};
-    if (!(q8 ? encode_tmap(&mkv, 3, pv.pool, kv8dims, kv8str, kv8box, true, true)
-             : encode_tmap(&mkv, 3, pv.pool, kvdims, kvstr, kvbox)))
+    // The pool as [2 page + kv][head][lines][line bytes]: bf16 blocks of
+    // 32 lines of 64 elements, FP8 blocks of 16 slots of 128 codes; a box is
+    // one head's K and V blocks of a page (8 KB, 4 KB).  FP8 scales as
+    // [2 page + kv][head][16 floats, as 64 bytes]: a box holds both rows.
+    CUtensorMap mkv, msc;
+    const cuuint64_t H = (cuuint64_t)pv.H_kv, kvp = (cuuint64_t)pv.num_pages * 2;
+    const cuuint64_t kvdims[4] = {64, 32, H, kvp}, kv8dims[4] = {128, 16, H, kvp}, scdims[3] = {64, H, kvp};
+    const cuuint64_t kvstr[3] = {128, 4096, H * 4096}, kv8str[3] = {128, 2048, H * 2048}, scstr[2] = {64, H * 64};
+    const cuuint32_t kvbox[4] = {64, 32, 1, 2}, kv8box[4] = {128, 16, 1, 2}, scbox[3] = {64, 1, 2};
+    if (!(q8 ? encode_tmap(&mkv, 4, pv.pool, kv8dims, kv8str, kv8box, true, true) &&
+                   encode_tmap(&msc, 3, pv.scales, scdims, scstr, scbox, true, false)
+             : encode_tmap(&mkv, 4, pv.pool, kvdims, kvstr, kvbox)))
         return cudaErrorInvalidValue;
+    if (!q8)
+        msc = mkv;                                         // unused
     DcParams prm;
     if (a.host_seqs && a.B <= kInline) {
         prm.seqs = nullptr;
@@ -763,8 +764,8 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, mkv, prm)
-              : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, mkv, prm);
+    return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, mkv, msc, prm)
+              : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, mkv, msc, prm);
 }
 
 }  // namespace gqa
