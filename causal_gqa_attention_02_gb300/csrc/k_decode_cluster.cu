@@ -67,8 +67,14 @@ namespace {
 using namespace sm100;
 
 constexpr int D = 128;
-constexpr int kWarps = 8;                          // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;        // + one producer warp
+// Consumer warps: 8 for the wide form (16 MMA rows of heads; 64 accumulator
+// registers a lane), 12 for the narrow form (g <= 8: 16 keys or dims as MMA
+// rows and the heads as the 8 columns; 32 accumulator registers a lane, so
+// more warps fit and hide more latency).  One producer warp on top.
+template <bool NARROW> struct DcCfg {
+    static constexpr int kWarps = NARROW ? 12 : 8;
+    static constexpr int kThreads = (kWarps + 1) * 32;
+};
 constexpr int kStages = 24;
 constexpr int kIssuePages = 8;                     // pages whose copies are issued at once
 // A stage is refilled by the lane that filled it (page i and i + kStages
@@ -76,7 +82,8 @@ constexpr int kIssuePages = 8;                     // pages whose copies are iss
 // last copy into it; and by the warp that read it (page i and i + kStages
 // have one consumer warp), so stages free in each warp's own order.
 static_assert(kStages % kIssuePages == 0, "a stage must be refilled by the lane that filled it");
-static_assert(kStages % kWarps == 0, "a stage must be read by one consumer warp");
+static_assert(kStages % DcCfg<false>::kWarps == 0 && kStages % DcCfg<true>::kWarps == 0,
+              "a stage must be read by one consumer warp");
 constexpr int kBlockBytes = kPageTokens * D * 2;   // one page of one head: 4 KB
 constexpr int kMaxCluster = 16;
 constexpr int kRows = 16;                          // MMA rows: the group's heads, zero-padded
@@ -89,6 +96,7 @@ __host__ __device__ constexpr int slice_lo(int j, int cs) { return j * D / cs; }
 // The CTA whose slice holds column col.
 __device__ __forceinline__ int slice_owner(int col, int cs) { return ((col + 1) * cs - 1) / D; }
 constexpr int kInline = 16;                        // entries whose descriptors travel in the parameters
+template <int W>
 struct __align__(1024) DcSmem {
     unsigned char ring[kStages][2 * kBlockBytes];  // stage: K block, then V block
     // Received from the cluster's CTAs (rank r): unnormalised O rows,
@@ -96,11 +104,12 @@ struct __align__(1024) DcSmem {
     // holds it; and (m, l) per row.
     float in_o[kRows][kInStride];
     float in_m[kMaxCluster][kRows], in_l[kMaxCluster][kRows];
-    float wm[kWarps][kRows], wl[kWarps][kRows];    // per consumer warp
+    float wm[W][kRows], wl[W][kRows];              // per consumer warp
     uint64_t full[kStages], empty[kStages];
     int abort_;
 };
-static_assert(kWarps * kRows * kRedStride * sizeof(float) <= sizeof(DcSmem::ring), "the warp combine reuses the ring");
+static_assert(DcCfg<true>::kWarps * kRows * kRedStride * sizeof(float) <= sizeof(DcSmem<12>::ring),
+              "the warp combine reuses the ring");
 
 struct DcParams {
     const SeqDesc *seqs;                           // device descriptors, or null: inl[] holds them
@@ -194,6 +203,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel)
     return r;
 }
 
+__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     uint32_t r;
@@ -230,13 +246,15 @@ __device__ __forceinline__ uint32_t stage_off(int s, int c)
 // R at the end); ldmatrix.trans plus a byte permute give the key pairs of
 // the B fragments, whose n columns are the even and the odd dims of a
 // 16-dim unit (undone when O is combined).
-template <bool Q8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool Q8, bool NARROW>
+__global__ void __launch_bounds__(DcCfg<NARROW>::kThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_constant__ CUtensorMap mSc,
                       const DcParams p)
 {
+    constexpr int kWarps = DcCfg<NARROW>::kWarps;
     extern __shared__ unsigned char smem_raw[];
-    DcSmem &s = *reinterpret_cast<DcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    DcSmem<kWarps> &s =
+        *reinterpret_cast<DcSmem<kWarps> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
     const uint32_t rank = cluster_rank(), cs = cluster_ncta();
@@ -269,8 +287,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
     __syncthreads();
 
     const int r0 = lane >> 2, qc = (lane & 3) * 2;         // fragment row / column pair of this lane
-    float o[D / 8][4];                                     // O rows r0, r0 + 8; columns 8j + qc, + 1
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[D / 8][4];                                     // O rows r0, r0 + 8; columns 8j + qc, + 1 (narrow: tiles 0-7)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows r0, r0 + 8 (narrow: heads 2 c4, + 1)
     float R = 0.f;                                         // Q8: largest value scale met so far (O is in units of R)
 
     if (warp == kWarps) {
@@ -318,6 +336,226 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
                 }
         }
         __syncwarp();                                      // the warp meets the block barrier converged
+    } else if constexpr (NARROW) {
+        // ---- consumers, narrow form (g <= 8) ------------------------------
+        // S^T = K Q^T: the page's 16 keys are the MMA rows, the group's heads
+        // the 8 columns (none wasted for g = 8); O^T += V^T P^T: 16 dims as
+        // the rows of each of 8 MMA tiles.  This lane: keys (and dims) r4,
+        // r4 + 8 of a tile, heads 2 c4, 2 c4 + 1; m0 / m1, l0 / l1 are the
+        // running maximum and sum of those two heads.
+        const int r4 = lane >> 2, c4 = lane & 3;
+        const float kScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+        float qs0 = kScale, qs1 = kScale;                  // score factor of heads 2 c4, 2 c4 + 1
+        // Q^T as the B operand of k-step kk: head r4 (zero past g).
+        uint32_t qb[D / 16][2];
+        if constexpr (!Q8) {
+            const uint32_t *qh = reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * p.H_q + kvh * G + r4) * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qb[kk][0] = r4 < G ? qh[8 * kk + c4] : 0u;          // dims 16 kk + 2 c4, + 1
+                qb[kk][1] = r4 < G ? qh[8 * kk + 4 + c4] : 0u;      // dims 16 kk + 8 + 2 c4, + 1
+            }
+        } else {
+            // Dims 16 kk + 4 c4 .. + 3 (the code layout's permutation of the
+            // k-step); scaled by 2^e so the head's largest |q| lies in
+            // [2^14, 2^15), then rounded to f16.
+            const uint2 *qh = reinterpret_cast<const uint2 *>(p.q + ((size_t)b * p.H_q + kvh * G + r4) * D) + c4;
+            float a = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (r4 < G) {
+                    const uint2 u = qh[4 * kk];
+                    a = fmaxf(fmaxf(a, fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xffff0000u)))),
+                              fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xffff0000u))));
+                }
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            int e = 0;                                     // a * 2^e in [2^14, 2^15), clamped
+            if (a > 0.f)
+                e = max(-126, min(126, 14 - ((int)((__float_as_uint(a) >> 23) & 0xff) - 127)));
+            const float f = __uint_as_float((uint32_t)(e + 127) << 23);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint2 u = r4 < G ? qh[4 * kk] : make_uint2(0u, 0u);
+                qb[kk][0] = pack_f16x2(__uint_as_float(u.x << 16) * f, __uint_as_float(u.x & 0xffff0000u) * f);
+                qb[kk][1] = pack_f16x2(__uint_as_float(u.y << 16) * f, __uint_as_float(u.y & 0xffff0000u) * f);
+            }
+            const float qsh = kScale * __uint_as_float((uint32_t)(127 - e) << 23);   // head r4's factor
+            qs0 = __shfl_sync(0xffffffffu, qsh, 8 * c4);          // head 2 c4 sits in lanes 8 c4 ..
+            qs1 = __shfl_sync(0xffffffffu, qsh, 8 * c4 + 4);      // head 2 c4 + 1 in lanes 8 c4 + 4 ..
+        }
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j)
+            o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        const int mi = lane >> 3, rr = lane & 7;           // ldmatrix: matrix and row this lane addresses
+        const uint32_t ring0 = smem_u32(s.ring[0]);
+        for (int i = warp; i < npg; i += kWarps) {
+            const int st = i % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (i / kStages) & 1, &s.abort_))) {
+                if (lane == 0) {
+                    s.abort_ = 1;
+                    atomicOr(p.err, kErrTimeout);
+                }
+                break;
+            }
+            const uint32_t kb = ring0 + (uint32_t)st * (2 * kBlockBytes), vb = kb + (Q8 ? kQ8Block : kBlockBytes);
+            const int pos0 = (pfirst + i_lo + i) * kPageTokens;    // position of the page's slot 0
+            if (!Q8 && p.app_k && pos0 <= past && past < pos0 + kPageTokens) {
+                // The appended row: lanes 0-15 its K units, 16-31 its V units.
+                const int slot = past - pos0, kv = lane >> 4, c = lane & 15;
+                const __nv_bfloat16 *src = (kv ? p.app_v : p.app_k) + ((size_t)b * p.H_kv + kvh) * D + 8 * c;
+                const uint4 val = *reinterpret_cast<const uint4 *>(src);
+                *reinterpret_cast<uint4 *>(s.ring[st] + kv * kBlockBytes + stage_off(slot, c)) = val;
+                const int page = tab[i];
+                if ((unsigned)page < (unsigned)p.num_pages)
+                    *reinterpret_cast<uint4 *>(p.pool + (((size_t)page * 2 + kv) * p.H_kv + kvh) * kBlockBytes +
+                                               pool_in_block(2, slot, 16 * c)) = val;
+                __syncwarp();
+            }
+            // S^T: two accumulators (even and odd k-steps) halve the chain.
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            float k0s = 1.f, k1s = 1.f, v0s = 1.f, v1s = 1.f;   // Q8: scales of keys r4, r4 + 8
+            if constexpr (!Q8) {
+                // Matrices of one ldmatrix: (keys 0-7, dims 16 kk ..), (keys
+                // 8-15, same), (keys 0-7, dims 16 kk + 8 ..), (keys 8-15, same).
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(kb + stage_off(8 * (mi & 1) + rr, 2 * kk + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    mma_bf16((kk & 1) ? sb : sa, a, qb[kk][0], qb[kk][1]);
+                }
+            } else {
+                // Matrices: (keys 0-7, unit 2h), (keys 8-15, 2h), (keys 0-7,
+                // 2h + 1), (keys 8-15, 2h + 1); a register's four codes are
+                // dims 4 c4 .. + 3 of its key: k indices 2 c4, + 1 (lo) and
+                // 8 + 2 c4, + 1 (hi).
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t w0, w1, w2, w3, l0_, h0_, l1_, h1_;
+                    ldsm_x4(kb + q8_off(8 * (mi & 1) + rr, 2 * h + (mi >> 1)), w0, w1, w2, w3);
+                    e4m3x4_f16(w0, l0_, h0_);
+                    e4m3x4_f16(w1, l1_, h1_);
+                    const uint32_t ae[4] = {l0_, l1_, h0_, h1_};
+                    mma_f16(sa, ae, qb[2 * h][0], qb[2 * h][1]);
+                    e4m3x4_f16(w2, l0_, h0_);
+                    e4m3x4_f16(w3, l1_, h1_);
+                    const uint32_t ao[4] = {l0_, l1_, h0_, h1_};
+                    mma_f16(sb, ao, qb[2 * h + 1][0], qb[2 * h + 1][1]);
+                }
+                const float *ksc = reinterpret_cast<const float *>(s.ring[st] + 2 * kQ8Block);
+                k0s = ksc[r4];
+                k1s = ksc[8 + r4];
+                v0s = ksc[kPageTokens + r4];
+                v1s = ksc[kPageTokens + 8 + r4];
+            }
+            // Visible keys only, in exp2 units: sc = [key r4 | r4 + 8][head 2 c4 | + 1].
+            const int t0 = pos0 + r4, t1 = pos0 + 8 + r4;
+            const bool vis0 = t0 <= past && t0 >= ws, vis1 = t1 <= past && t1 >= ws;
+            float sc[4];
+            sc[0] = vis0 ? (sa[0] + sb[0]) * qs0 * k0s : -INFINITY;
+            sc[1] = vis0 ? (sa[1] + sb[1]) * qs1 * k0s : -INFINITY;
+            sc[2] = vis1 ? (sa[2] + sb[2]) * qs0 * k1s : -INFINITY;
+            sc[3] = vis1 ? (sa[3] + sb[3]) * qs1 * k1s : -INFINITY;
+            // Column maxima: the two keys here, then the 8 lanes of the same c4.
+            float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+            }
+            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+            const float f0 = n0 == -INFINITY ? 0.f : n0, f1 = n1 == -INFINITY ? 0.f : n1;
+            float a0 = ex2(m0 - f0), a1 = ex2(m1 - f1);   // 0 while nothing was visible
+            m0 = n0;
+            m1 = n1;
+            float pr[4] = {ex2(sc[0] - f0), ex2(sc[1] - f1), ex2(sc[2] - f0), ex2(sc[3] - f1)};
+            l0 = l0 * a0 + (pr[0] + pr[2]);                // this lane's keys; lanes summed at the end
+            l1 = l1 * a1 + (pr[1] + pr[3]);
+            if constexpr (Q8) {
+                // P' = P s_v / R, R the largest value scale met (all 16 keys
+                // of the page: max over the lanes of one c4).
+                float vm = fmaxf(v0s, v1s);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1)
+                    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                if (vm > R) {                              // the same in every lane; O = 0 while R = 0
+                    a0 *= R / vm;
+                    a1 *= R / vm;
+                    R = vm;
+                }
+                const float invR = R > 0.f ? 1.f / R : 0.f;
+                pr[0] *= v0s * invR;
+                pr[1] *= v0s * invR;
+                pr[2] *= v1s * invR;
+                pr[3] *= v1s * invR;
+            }
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    o[j][0] *= a0;
+                    o[j][1] *= a1;
+                    o[j][2] *= a0;
+                    o[j][3] *= a1;
+                }
+            }
+            // P^T as the B operand for head r4: keys 2 c4, + 1 (b0) and
+            // 8 + 2 c4, + 1 (b1).  Key k of head h sits in lane 4 (k % 8) +
+            // h / 2; each lane sends its two heads as (key r4, key r4 + 8)
+            // pairs, and the two lanes holding keys 2 c4 and 2 c4 + 1 of this
+            // head give b0, b1 by a byte permute.
+            const uint32_t ph0 = Q8 ? pack_f16x2(pr[0], pr[2]) : pack_bf16x2(pr[0], pr[2]);
+            const uint32_t ph1 = Q8 ? pack_f16x2(pr[1], pr[3]) : pack_bf16x2(pr[1], pr[3]);
+            const int sA = 8 * c4 + (r4 >> 1), sB = sA + 4;
+            const uint32_t xa0 = __shfl_sync(0xffffffffu, ph0, sA), xa1 = __shfl_sync(0xffffffffu, ph1, sA);
+            const uint32_t xb0 = __shfl_sync(0xffffffffu, ph0, sB), xb1 = __shfl_sync(0xffffffffu, ph1, sB);
+            const uint32_t X = (r4 & 1) ? xa1 : xa0, Y = (r4 & 1) ? xb1 : xb0;
+            const uint32_t pb0 = prmt2(X, Y, 0x5410), pb1 = prmt2(X, Y, 0x7632);
+            if constexpr (!Q8) {
+                // V^T of dims 16 j .. + 15: matrices (keys 0-7, dims 16 j ..),
+                // (keys 0-7, dims 16 j + 8 ..), (keys 8-15, 16 j ..), (keys
+                // 8-15, 16 j + 8 ..), transposed.
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    uint32_t a[4];
+                    ldsm_x4_t(vb + stage_off(8 * (mi >> 1) + rr, 2 * j + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    mma_bf16(o[j], a, pb0, pb1);
+                }
+            } else {
+                // Matrices (keys 0-7, unit 2h), (keys 0-7, 2h + 1), (keys
+                // 8-15, 2h), (keys 8-15, 2h + 1), transposed as code pairs; a
+                // byte permute makes key pairs per dim.  Tile 2h + par: rows
+                // r, r + 8 = dims 32h + 2r + par, 32h + 16 + 2r + par.
+#pragma unroll
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t w0, w1, w2, w3, e0[2], e1[2], e2[2], e3[2];
+                    ldsm_x4_t(vb + q8_off(8 * (mi >> 1) + rr, 2 * h + (mi & 1)), w0, w1, w2, w3);
+                    e4m3x4_f16(prmt(w0, 0x3120), e0[0], e0[1]);
+                    e4m3x4_f16(prmt(w1, 0x3120), e1[0], e1[1]);
+                    e4m3x4_f16(prmt(w2, 0x3120), e2[0], e2[1]);
+                    e4m3x4_f16(prmt(w3, 0x3120), e3[0], e3[1]);
+#pragma unroll
+                    for (int par = 0; par < 2; ++par) {
+                        const uint32_t a[4] = {e0[par], e1[par], e2[par], e3[par]};
+                        mma_f16(o[2 * h + par], a, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.empty[st]);
+        }
+        // Column sums over the 8 lanes of one c4.
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        if (r4 == 0) {
+            s.wm[warp][2 * c4] = m0;
+            s.wm[warp][2 * c4 + 1] = m1;
+            s.wl[warp][2 * c4] = l0;
+            s.wl[warp][2 * c4 + 1] = l1;
+        }
     } else {
         // ---- consumers --------------------------------------------------
         // Q as the A operand of each k-step: rows r0 / r0 + 8 (zero past g),
@@ -551,7 +789,37 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
     // ---- the CTA's partial: warps combined -----------------------------------
     const bool ok = s.abort_ == 0;
     float *red = reinterpret_cast<float *>(s.ring[0]);     // [kWarps][kRows][kRedStride]
-    if (warp < kWarps && ok) {
+    if constexpr (NARROW) {
+        if (warp < kWarps && ok) {
+            const int r4 = lane >> 2, c4 = lane & 3;
+            float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                M0 = fmaxf(M0, s.wm[w][2 * c4]);
+                M1 = fmaxf(M1, s.wm[w][2 * c4 + 1]);
+            }
+            const float rs = Q8 ? R : 1.f;                 // Q8: O is in units of R
+            const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0) * rs, c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1) * rs;
+            float *w0 = red + ((size_t)warp * kRows + 2 * c4) * kRedStride, *w1 = w0 + kRedStride;
+            const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j) {
+                // bf16: tile j rows r, r + 8 = dims 16j + r, + 8; FP8: tile
+                // 2h + par rows = dims 32h + 2r + par, + 16.
+                const int d0 = Q8 ? 32 * (j >> 1) + 2 * r4 + (j & 1) : 16 * j + r4;
+                const int d1 = d0 + (Q8 ? 16 : 8);
+                if (h0) {
+                    w0[d0] = o[j][0] * c0;
+                    w0[d1] = o[j][2] * c0;
+                }
+                if (h1) {
+                    w1[d0] = o[j][1] * c1;
+                    w1[d1] = o[j][3] * c1;
+                }
+            }
+        }
+    } else if (warp < kWarps && ok) {
+
         float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
@@ -585,7 +853,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
     __syncthreads();
     // ---- into the cluster: column slice j of every row goes to CTA j ----------
     if (ok) {
-        for (int e = threadIdx.x; e < G * D; e += kThreads) {
+        for (int e = threadIdx.x; e < G * D; e += DcCfg<NARROW>::kThreads) {
             const int row = e >> 7, col = e & (D - 1);
             float a = 0.f;
 #pragma unroll
@@ -595,7 +863,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
             st_cluster(&s.in_o[row][rank * (slice_lo(j + 1, (int)cs) - lo) + (col - lo)], (uint32_t)j, a);
         }
     }
-    for (int t = threadIdx.x; t < G * (int)cs; t += kThreads) {
+    for (int t = threadIdx.x; t < G * (int)cs; t += DcCfg<NARROW>::kThreads) {
         const int j = t / G, row = t - j * G;
         float M = -INFINITY, l = 0.f;
         for (int w = 0; w < kWarps; ++w)
@@ -626,7 +894,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
             s.in_m[r][row] *= inv;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * w; e += kThreads) {
+    for (int e = threadIdx.x; e < G * w; e += DcCfg<NARROW>::kThreads) {
         const int row = e / w, c = e - row * w;
         float a = 0.f;
         for (uint32_t r = 0; r < cs; ++r)
@@ -635,7 +903,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap mKV, const __grid_cons
     }
 }
 
-constexpr int kSmemBytes = (int)sizeof(DcSmem) + 1024;
+constexpr int kSmemBytes =
+    (int)(sizeof(DcSmem<12>) > sizeof(DcSmem<8>) ? sizeof(DcSmem<12>) : sizeof(DcSmem<8>)) + 1024;
 constexpr int kMaxDev = 64;
 
 // The shared-memory and cluster-size opt-ins are per device.
@@ -647,7 +916,8 @@ cudaError_t configure(int dev)
     if (done[dev].load(std::memory_order_acquire))
         return cudaSuccess;
     cudaError_t e = cudaSuccess;
-    for (auto k : {decode_cluster_kernel<false>, decode_cluster_kernel<true>}) {
+    for (auto k : {decode_cluster_kernel<false, false>, decode_cluster_kernel<true, false>,
+                   decode_cluster_kernel<false, true>, decode_cluster_kernel<true, true>}) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e == cudaSuccess)
@@ -678,7 +948,7 @@ int decode_cluster_capacity(int cluster)
         return v < 0 ? 0 : v;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cluster, 1, 1);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(DcCfg<true>::kThreads);
     cfg.dynamicSmemBytes = (size_t)kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -688,8 +958,9 @@ int decode_cluster_capacity(int cluster)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    // Both instantiations have the same block, shared memory and registers.
-    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<false>, &cfg) != cudaSuccess) {
+    // Every instantiation holds one CTA per SM (shared memory); the widest
+    // block stands for them all.
+    if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<false, true>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -751,8 +1022,9 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     if (ev_start)
         cudaEventRecord(ev_start, st);
     cudaLaunchConfig_t cfg = {};
+    const bool narrow = G <= 8;
     cfg.gridDim = dim3((unsigned)a.cluster, (unsigned)pv.H_kv, (unsigned)a.B);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(narrow ? DcCfg<true>::kThreads : DcCfg<false>::kThreads);
     cfg.dynamicSmemBytes = (size_t)kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -764,8 +1036,11 @@ cudaError_t launch_decode_cluster(const PoolView &pv, const ClusterDecodeLaunch 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, mkv, msc, prm)
-              : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, mkv, msc, prm);
+    if (narrow)
+        return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, true>, mkv, msc, prm)
+                  : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, true>, mkv, msc, prm);
+    return q8 ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, false>, mkv, msc, prm)
+              : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, false>, mkv, msc, prm);
 }
 
 }  // namespace gqa
