@@ -857,7 +857,19 @@ void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan 
             const int32_t j0 = window_start(sds[b].past + i0, c->desc.window) / 128;
             const int32_t tiles = i0 + rows_pos < sds[b].count ? 2 : 1;
             for (int32_t h = 0; h < c->desc.num_kv_heads; ++h)
-                items.push_back(TcItem{b, h, i0, nt, j0, tiles, -1, 0, 1, 0});
+            {
+                TcItem x{};
+                x.b = b;
+                x.kvh = h;
+                x.i0 = i0;
+                x.nt = nt;
+                x.j0 = j0;
+                x.tiles = (int8_t)tiles;
+                x.part = -1;
+                x.split = 0;
+                x.nsplit = 1;
+                items.push_back(x);
+            }
             split_tiles += (int64_t)(nt - j0) * c->desc.num_kv_heads;
         }
     // Pieces of at least kSplitMinTiles key tiles, sized for about
@@ -878,8 +890,8 @@ void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan 
             x.j0 = it.j0 + (int32_t)((int64_t)q * K / S);
             x.nt = it.j0 + (int32_t)((int64_t)(q + 1) * K / S);
             x.part = pl.slots + q;
-            x.split = q;
-            x.nsplit = S;
+            x.split = (int16_t)q;
+            x.nsplit = (int16_t)S;
             all.push_back(x);
         }
         pl.slots += S;
@@ -1201,7 +1213,23 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
     TcSplitWs ws;
     if (use_tc && (rc = tc_workspace(c, plan, ws)) != GQA_OK)
         return rc;
-    if ((rc = upload_stage(c, st)) != GQA_OK)
+    // A fused tensor-core call with nothing else to launch can carry its
+    // descriptors in the kernel parameters: then no copy precedes the kernel.
+    TcHostDesc hd;
+    if (use_tc && fused && cows.empty() && !pre_tc) {
+        hd.seqs = sds.data();
+        hd.n_seqs = B;
+        hd.items = plan.items.data();
+        hd.n_items = (int)plan.items.size();
+        hd.item_start = plan.item_start.data();
+        hd.n_start = (int)plan.item_start.size();
+        hd.zero_start = zstart.data();
+        hd.n_zero = (int)zstart.size();
+        hd.tables = ctab.empty() ? nullptr : ctab.data();
+        hd.n_tables = ctab.size();
+    }
+    const bool inl = use_tc && fused && cows.empty() && !pre_tc && prefill_tc_inline_fits(hd);
+    if (!inl && (rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     PoolView pv = c->view();
     if (!ctab.empty()) {
@@ -1248,7 +1276,7 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
             return launch_prefill_tc(pv, d_sds, (const TcItem *)(c->d_stage + o_items),
                                      (const int32_t *)(c->d_stage + o_start), plan.grid, B, n, H_q, q, out, ws, st, ev,
                                      nullptr, nullptr, fused ? k : nullptr, fused ? v : nullptr,
-                                     fused ? (const int64_t *)(c->d_stage + o_zero) : nullptr);
+                                     fused ? (const int64_t *)(c->d_stage + o_zero) : nullptr, inl ? &hd : nullptr);
         });
     }
     return run_kernel(c, GQA_KERNEL_ATTN_SIMT, st, "attention kernel", [&](cudaEvent_t ev) {

@@ -59,6 +59,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
+#include <type_traits>
 #include <atomic>
 
 #include "kernels.cuh"
@@ -156,6 +158,16 @@ struct TcParams {
     const int64_t *zero_start;    // fused: CTA c clears padding units zero_start[c] .. zero_start[c + 1] - 1
 };
 
+// The parameters of a launch that carries its descriptors (the kernel's INL
+// form): byte offsets into inl of seqs, items, item_start, zero_start and
+// tables (-1: the pointer in TcParams is used).  Only these launches pay
+// for the large parameter block.
+struct TcParamsInl : TcParams {
+    int32_t inl_off[5];
+    alignas(16) unsigned char inl[kTcInlineBytes];
+};
+static_assert(sizeof(TcParamsInl) + 7 * sizeof(CUtensorMap) <= 32764, "kernel parameter space");
+
 // Two FP8 E4M3 codes (low byte first) dequantised with their row's scale:
 // decode (exact, through f16), times the scale in fp32, rounded to a bf16
 // pair for the tensor cores.
@@ -182,17 +194,30 @@ __device__ __forceinline__ void abort_with(TcSmem &s, int32_t *err, int32_t bit)
 // masked, or split items); Q8: the pool holds FP8 E4M3 codes with a scale
 // per row (mKV then maps the code bytes).  All are template flags so the
 // plain path carries none of their instructions.
-template <bool ROPE, bool WIN, bool Q8>
+template <bool ROPE, bool WIN, bool Q8, bool INL = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKV,
                   const __grid_constant__ CUtensorMap mO, const __grid_constant__ CUtensorMap mKt,
                   const __grid_constant__ CUtensorMap mVt, const __grid_constant__ CUtensorMap mKp,
-                  const __grid_constant__ CUtensorMap mVp, const TcParams p)
+                  const __grid_constant__ CUtensorMap mVp,
+                  const __grid_constant__ typename std::conditional<INL, TcParamsInl, TcParams>::type p)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem &s = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i_begin = p.item_start[blockIdx.x], i_end = p.item_start[blockIdx.x + 1];
+    // The descriptors, from the parameters when the launch carries them.
+    auto inl_or = [&](int which, const void *ptr) -> const void * {
+        if constexpr (INL)
+            return p.inl_off[which] >= 0 ? static_cast<const void *>(p.inl + p.inl_off[which]) : ptr;
+        else
+            return ptr;
+    };
+    const SeqDesc *seqs = static_cast<const SeqDesc *>(inl_or(0, p.seqs));
+    const TcItem *items = static_cast<const TcItem *>(inl_or(1, p.items));
+    const int32_t *item_start = static_cast<const int32_t *>(inl_or(2, p.item_start));
+    const int64_t *zero_start = static_cast<const int64_t *>(inl_or(3, p.zero_start));
+    const int32_t *tables = static_cast<const int32_t *>(inl_or(4, p.tables));
+    const int i_begin = item_start[blockIdx.x], i_end = item_start[blockIdx.x + 1];
 
     if (warp == 1) {
         tmem_alloc(&s.tmem, 512);
@@ -292,7 +317,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         // TMA load that reads them.  Lane l holds elements 4l .. 4l + 3.
         auto append_row = [&](const TcItem &it, const SeqDesc &sd) {
             const int pos = sd.past;
-            const int pg = p.tables[(size_t)sd.row * p.stride + pos / kPageTokens];
+            const int pg = tables[(size_t)sd.row * p.stride + pos / kPageTokens];
             if (pg < 0 || pg >= p.num_pages) {
                 if (lane == 0)
                     atomicOr(p.err, kErrPageId);
@@ -386,7 +411,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         int zb = -1;
         uint4 *zb_base = nullptr;                         // out row zero_from of entry zb
         if (p.fused) {
-            const int64_t c0 = p.zero_start[blockIdx.x], c1 = p.zero_start[blockIdx.x + 1];
+            const int64_t c0 = zero_start[blockIdx.x], c1 = zero_start[blockIdx.x + 1];
             const int64_t mid = c0 + (c1 - c0) / 2;
             z_next = vside ? mid : c0;
             z_end = vside ? c1 : mid;
@@ -398,9 +423,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 while (u >= zb_end) {
                     ++zb;
                     zb_start = zb_end;
-                    zb_end = zb_start + (int64_t)(p.n - p.seqs[zb].zero_from) * row_units;
+                    zb_end = zb_start + (int64_t)(p.n - seqs[zb].zero_from) * row_units;
                     zb_base = reinterpret_cast<uint4 *>(p.out) +
-                              ((size_t)zb * p.n + p.seqs[zb].zero_from) * (size_t)row_units;
+                              ((size_t)zb * p.n + seqs[zb].zero_from) * (size_t)row_units;
                 }
                 zb_base[u - zb_start] = make_uint4(0, 0, 0, 0);
             }
@@ -449,7 +474,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (boxer) {
                 const int lp = 8 * j + my_pg;
                 if (lp < seq_pages) {
-                    ph = p.tables[(size_t)sd.row * p.stride + lp];
+                    ph = tables[(size_t)sd.row * p.stride + lp];
                     if (ph < 0)                            // released by the sliding window: never visible
                         ph = p.num_pages;
                     else if (ph >= p.num_pages) {
@@ -567,7 +592,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         // The first item's Q load is issued before the K loop.
         bool first_q_issued = false;
         if (!vside && i_begin < i_end) {
-            load_q(p.items[i_begin]);
+            load_q(items[i_begin]);
             first_q_issued = true;
         }
 #if GQA_PDL
@@ -577,8 +602,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
         for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-            const TcItem it = p.items[idx];
-            const SeqDesc sd = p.seqs[it.b];
+            const TcItem it = items[idx];
+            const SeqDesc sd = seqs[it.b];
             // The first K tile only needs a free stage; issue it before
             // waiting for the previous item to release the Q buffers.
             if (!load_tile(it, sd, WIN ? it.j0 : 0)) {
@@ -676,8 +701,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             int k = 0;
             if (warp == 1) {
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
-                    const bool two = p.items[idx].tiles > 1;
+                    const int nt = items[idx].nt, j0 = WIN ? items[idx].j0 : 0;
+                    const bool two = items[idx].tiles > 1;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int st = g % kKStages;
                         ok = (ns == 0 || mbar_wait(&s.s_free, (ns - 1) & 1, &s.abort_)) &&
@@ -724,8 +749,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                             break;
                 };
                 for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-                    const int nt = p.items[idx].nt, j0 = WIN ? p.items[idx].j0 : 0;
-                    const bool two = p.items[idx].tiles > 1;
+                    const int nt = items[idx].nt, j0 = WIN ? items[idx].j0 : 0;
+                    const bool two = items[idx].tiles > 1;
                     for (int j = j0; j < nt; ++j, ++g) {
                         const int sv = g % kVStages;
                         const bool order = kPvOrder && j + 1 < nt;
@@ -781,7 +806,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         // this item's last softmax, so the next item's first S overlaps the
         // epilogue.
         auto rotate_q = [&](const TcItem &iq, uint32_t parity) -> bool {
-            const SeqDesc sq = p.seqs[iq.b];
+            const SeqDesc sq = seqs[iq.b];
             const int relq = iq.i0 + t * p.rows_pos + r / p.G;
             if (!mbar_wait(&s.bar_q, parity, &s.abort_))
                 return false;
@@ -829,7 +854,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             return true;
         };
         auto prefetch_rows = [&](const TcItem &iq) {
-            const SeqDesc sq = p.seqs[iq.b];
+            const SeqDesc sq = seqs[iq.b];
             const int relq = iq.i0 + t * p.rows_pos + r / p.G;
             if (r < p.G * p.rows_pos && relq < sq.count) {
                 const char *row = reinterpret_cast<const char *>(p.rope + (size_t)(sq.past + relq) * (D / 2));
@@ -839,22 +864,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
         };
         if (ROPE && i_begin < i_end)
-            prefetch_rows(p.items[i_begin]);
-        if (ROPE && i_begin < i_end && !rotate_q(p.items[i_begin], 0)) {
+            prefetch_rows(items[i_begin]);
+        if (ROPE && i_begin < i_end && !rotate_q(items[i_begin], 0)) {
             ok = false;
             abort_with(s, p.err, kErrTimeout);
         }
         for (int idx = i_begin; ok && idx < i_end; ++idx, ++k) {
-            const TcItem it = p.items[idx];
-            const SeqDesc sd = p.seqs[it.b];
+            const TcItem it = items[idx];
+            const SeqDesc sd = seqs[it.b];
             if (ROPE && idx + 1 < i_end)
-                prefetch_rows(p.items[idx + 1]);         // the next item's table rows into L2
+                prefetch_rows(items[idx + 1]);         // the next item's table rows into L2
             if (t == 1 && it.tiles < 2) {
                 // No valid row in this item's second tile: nothing is issued
                 // for it (its rows are padding, zeroed with the cache write).
                 // Only the next item's rotation, which the S issuer awaits
                 // once per item, is this warpgroup's part.
-                if (ROPE && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
+                if (ROPE && idx + 1 < i_end && !rotate_q(items[idx + 1], (k + 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -966,7 +991,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             if (!ok)
                 break;
-            if (ROPE && idx + 1 < i_end && !rotate_q(p.items[idx + 1], (k + 1) & 1)) {
+            if (ROPE && idx + 1 < i_end && !rotate_q(items[idx + 1], (k + 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -1208,6 +1233,37 @@ cudaError_t launch_wait_probe(int32_t *err, uint64_t limit_ns, cudaStream_t st)
     return cudaGetLastError();
 }
 
+namespace {
+
+// Byte offsets of the host descriptors in TcParams::inl (16-byte aligned),
+// and the bytes they need.
+size_t inline_layout(const TcHostDesc &h, int32_t (&off)[5])
+{
+    const size_t bytes[5] = {(size_t)h.n_seqs * sizeof(SeqDesc), (size_t)h.n_items * sizeof(TcItem),
+                             (size_t)h.n_start * sizeof(int32_t), (size_t)h.n_zero * sizeof(int64_t),
+                             h.n_tables * sizeof(int32_t)};
+    const bool given[5] = {h.seqs != nullptr, h.items != nullptr, h.item_start != nullptr, h.zero_start != nullptr,
+                           h.tables != nullptr};
+    size_t at = 0;
+    for (int i = 0; i < 5; ++i) {
+        off[i] = -1;
+        if (!given[i])
+            continue;
+        at = (at + 15) & ~(size_t)15;
+        off[i] = (int32_t)std::min<size_t>(at, INT32_MAX);
+        at += bytes[i];
+    }
+    return at;
+}
+
+}  // namespace
+
+bool prefill_tc_inline_fits(const TcHostDesc &h)
+{
+    int32_t off[5];
+    return h.seqs && h.items && h.item_start && inline_layout(h, off) <= kTcInlineBytes;
+}
+
 bool prefill_tc_supported(int group, int H_kv) { return group >= 1 && group <= 128 && H_kv >= 1; }
 
 int prefill_tc_rows_per_tile(int group) { return 128 / group; }
@@ -1216,7 +1272,7 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
                               const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start, const void *app_k,
                               const void *app_v, const void *fused_k, const void *fused_v,
-                              const int64_t *d_zero_start)
+                              const int64_t *d_zero_start, const TcHostDesc *host)
 {
     if (pv.d != D || grid <= 0)
         return grid <= 0 ? cudaSuccess : cudaErrorInvalidValue;
@@ -1262,7 +1318,10 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     } else {
         mkt = mvt = mkp = mvp = mkv;               // unused
     }
-    TcParams prm;
+    // The INL form when the host descriptors fit the parameters.
+    const bool inl = host && prefill_tc_inline_fits(*host) && !q8 && !pv.rope;
+    TcParamsInl prmi;
+    TcParams &prm = prmi;
     prm.seqs = d_seqs;
     prm.items = d_items;
     prm.item_start = d_item_start;
@@ -1290,22 +1349,37 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     prm.fused = fused ? 1 : 0;
     prm.B = B;
     prm.zero_start = d_zero_start;
+    if (inl) {
+        inline_layout(*host, prmi.inl_off);
+        const void *src[5] = {host->seqs, host->items, host->item_start, host->zero_start, host->tables};
+        const size_t bytes[5] = {(size_t)host->n_seqs * sizeof(SeqDesc), (size_t)host->n_items * sizeof(TcItem),
+                                 (size_t)host->n_start * sizeof(int32_t), (size_t)host->n_zero * sizeof(int64_t),
+                                 host->n_tables * sizeof(int32_t)};
+        for (int i = 0; i < 5; ++i)
+            if (prmi.inl_off[i] >= 0 && bytes[i])
+                memcpy(prmi.inl + prmi.inl_off[i], src[i], bytes[i]);
+    }
     const int smem = (int)sizeof(TcSmem) + 1024;
     // The shared-memory opt-in is per device: remember it per device.
     constexpr int kMaxDev = 64;
-    static std::atomic<bool> attr_set[kMaxDev][6];
+    static std::atomic<bool> attr_set[kMaxDev][8];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
         return cudaErrorInvalidDevice;
-    const int which = q8 ? 4 + (pv.window > 0 || ws.ranged ? 1 : 0)
-                         : (pv.rope ? 1 : 0) + (pv.window > 0 || ws.ranged ? 2 : 0);
-    void (*const kern[6])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                          TcParams) = {
-        prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
-        prefill_tc_kernel<false, true, false>,  prefill_tc_kernel<true, true, false>,
-        prefill_tc_kernel<false, false, true>,  prefill_tc_kernel<false, true, true>};
+    const bool win = pv.window > 0 || ws.ranged;
+    const int which = inl ? 6 + (win ? 1 : 0) : q8 ? 4 + (win ? 1 : 0) : (pv.rope ? 1 : 0) + (win ? 2 : 0);
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                          TcParams);
+    using KernInl = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                             CUtensorMap, TcParamsInl);
+    const Kern kern[6] = {prefill_tc_kernel<false, false, false>, prefill_tc_kernel<true, false, false>,
+                          prefill_tc_kernel<false, true, false>,  prefill_tc_kernel<true, true, false>,
+                          prefill_tc_kernel<false, false, true>,  prefill_tc_kernel<false, true, true>};
+    const KernInl kern_inl[2] = {prefill_tc_kernel<false, false, false, true>,
+                                 prefill_tc_kernel<false, true, false, true>};
+    const void *fn = inl ? (const void *)kern_inl[which - 6] : (const void *)kern[which];
     if (!attr_set[dev][which].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kern[which], cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
         attr_set[dev][which].store(true, std::memory_order_release);
@@ -1323,9 +1397,14 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (inl)
+        return cudaLaunchKernelEx(&cfg, kern_inl[which - 6], mq, mkv, mo, mkt, mvt, mkp, mvp, prmi);
     return cudaLaunchKernelEx(&cfg, kern[which], mq, mkv, mo, mkt, mvt, mkp, mvp, prm);
 #else
-    kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, mkt, mvt, mkp, mvp, prm);
+    if (inl)
+        kern_inl[which - 6]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, mkt, mvt, mkp, mvp, prmi);
+    else
+        kern[which]<<<grid, kThreads, smem, st>>>(mq, mkv, mo, mkt, mvt, mkp, mvp, prm);
     return cudaGetLastError();
 #endif
 }

@@ -96,10 +96,12 @@ struct DecodeItem {
 // part - split .. part - split + nsplit - 1, and the CTA that finishes the
 // group's last split merges them into out.
 struct TcItem {
-    int32_t b, kvh, i0, nt;
-    int32_t j0, tiles;
-    int32_t part, split, nsplit, pad_;
+    int32_t b, kvh, i0, nt, j0;
+    int32_t part;
+    int16_t split, nsplit;    // nsplit is at most a few hundred (pieces sized for the SM count)
+    int8_t tiles, pad_[3];
 };
+static_assert(sizeof(TcItem) == 32, "TcItem layout");
 
 // Workspace of split items: slot s holds rows 0 .. slot_rows-1 of one query
 // tile (o[(s * slot_rows + row) * 128 + column]) and (m, l) per row
@@ -219,12 +221,32 @@ int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // new page to the pool once, and zeroes rows zero_from .. n-1 of out for
 // every entry; no cache-write launch precedes it.  Those rows, counted in
 // 16-byte units entry after entry, are cleared by CTA c from unit
-// d_zero_start[c] to d_zero_start[c + 1] (grid + 1 offsets).
+// d_zero_start[c] to d_zero_start[c + 1] (grid + 1 offsets).  `host`, if
+// given and it fits, supplies the descriptors in the launch parameters.
+// Host copies of a launch's descriptors.  When they fit kTcInlineBytes
+// (prefill_tc_inline_fits) the launch carries them in its parameters and
+// the device copies passed to launch_prefill_tc are not read, so no upload
+// has to precede the kernel.  `tables` replaces pv.tables (row stride
+// pv.stride) when given.
+struct TcHostDesc {
+    const SeqDesc *seqs = nullptr;
+    int n_seqs = 0;
+    const TcItem *items = nullptr;
+    int n_items = 0;
+    const int32_t *item_start = nullptr;
+    int n_start = 0;
+    const int64_t *zero_start = nullptr;
+    int n_zero = 0;
+    const int32_t *tables = nullptr;
+    size_t n_tables = 0;
+};
+constexpr size_t kTcInlineBytes = 28 * 1024;
+bool prefill_tc_inline_fits(const TcHostDesc &h);
 cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const TcItem *d_items,
                               const int32_t *d_item_start, int grid, int B, int n, int H_q, const void *q, void *out,
                               const TcSplitWs &ws, cudaStream_t st, cudaEvent_t ev_start = nullptr,
                               const void *app_k = nullptr, const void *app_v = nullptr,
                               const void *fused_k = nullptr, const void *fused_v = nullptr,
-                              const int64_t *d_zero_start = nullptr);
+                              const int64_t *d_zero_start = nullptr, const TcHostDesc *host = nullptr);
 
 }  // namespace gqa
