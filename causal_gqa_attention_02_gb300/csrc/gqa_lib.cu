@@ -929,6 +929,25 @@ void plan_tc(const gqa_cache *c, const std::vector<SeqDesc> &sds, int G, TcPlan 
     }
 }
 
+// Host descriptors of a tensor-core launch (no zero shares, the cache's own
+// tables), and whether the launch can carry them in its parameters.
+static TcHostDesc tc_host(const std::vector<SeqDesc> &sds, const TcPlan &plan)
+{
+    TcHostDesc h;
+    h.seqs = sds.data();
+    h.n_seqs = (int)sds.size();
+    h.items = plan.items.data();
+    h.n_items = (int)plan.items.size();
+    h.item_start = plan.item_start.data();
+    h.n_start = (int)plan.item_start.size();
+    return h;
+}
+
+static bool tc_inline_ok(const gqa_cache *c, const TcHostDesc &h)
+{
+    return c->desc.dtype == GQA_DTYPE_BF16 && c->desc.rope == 0 && prefill_tc_inline_fits(h);
+}
+
 // Fused prefill: the padding rows of out that no item stores (`units`
 // 16-byte units in all) are cleared by the CTAs after their items, the
 // least-loaded CTAs taking the most (water-filling their loads up to a
@@ -1228,7 +1247,7 @@ static int attn_prefill_impl(gqa_cache *c, int32_t B, const int32_t *seq_ids, in
         hd.tables = ctab.empty() ? nullptr : ctab.data();
         hd.n_tables = ctab.size();
     }
-    const bool inl = use_tc && fused && cows.empty() && !pre_tc && prefill_tc_inline_fits(hd);
+    const bool inl = use_tc && fused && cows.empty() && !pre_tc && tc_inline_ok(c, hd);
     if (!inl && (rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     PoolView pv = c->view();
@@ -1524,12 +1543,15 @@ static int decode_launch(gqa_cache *c, const PoolView &pv, const std::vector<Seq
         TcSplitWs ws;
         if ((rc = tc_workspace(c, plan, ws)) != GQA_OK)
             return rc;
-        if ((rc = upload_stage(c, st)) != GQA_OK)
+        const TcHostDesc hd = tc_host(sds, plan);
+        const bool inl = tc_inline_ok(c, hd);      // descriptors in the launch parameters: no copy
+        if (!inl && (rc = upload_stage(c, st)) != GQA_OK)
             return rc;
         return run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core decode kernel", [&](cudaEvent_t ev) {
             return launch_prefill_tc(pv, (const SeqDesc *)(c->d_stage + o_sds),
                                      (const TcItem *)(c->d_stage + o_items),
-                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev);
+                                     (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev,
+                                     nullptr, nullptr, nullptr, nullptr, nullptr, inl ? &hd : nullptr);
         });
     }
     if ((c->desc.dtype == GQA_DTYPE_BF16 || c->desc.dtype == GQA_DTYPE_FP8_E4M3) && c->desc.head_dim == 128 &&
@@ -1746,7 +1768,9 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     TcSplitWs ws;
     if ((rc = tc_workspace(c, plan, ws)) != GQA_OK)
         return rc;
-    if ((rc = upload_stage(c, st)) != GQA_OK)
+    const TcHostDesc hd = tc_host(sds, plan);
+    const bool inl = cows.empty() && tc_inline_ok(c, hd);   // descriptors in the launch parameters: no copy
+    if (!inl && (rc = upload_stage(c, st)) != GQA_OK)
         return rc;
     if (!cows.empty() &&
         (rc = run_kernel(c, GQA_KERNEL_COW_COPY, st, "copy-on-write kernel", [&](cudaEvent_t ev) {
@@ -1757,7 +1781,7 @@ int attn_decode_append(gqa_cache *c, int32_t B, const int32_t *seq_ids, int32_t 
     rc = run_kernel(c, GQA_KERNEL_PREFILL_TC, st, "tensor-core decode kernel", [&](cudaEvent_t ev) {
         return launch_prefill_tc(pv, (const SeqDesc *)(c->d_stage + o_sds), (const TcItem *)(c->d_stage + o_items),
                                  (const int32_t *)(c->d_stage + o_start), plan.grid, B, 1, H_q, q, out, ws, st, ev,
-                                 k_new, v_new);
+                                 k_new, v_new, nullptr, nullptr, nullptr, inl ? &hd : nullptr);
     });
     if (rc == GQA_OK)
         release_windows(c, B, seq_ids);

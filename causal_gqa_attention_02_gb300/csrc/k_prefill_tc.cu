@@ -1318,8 +1318,12 @@ cudaError_t launch_prefill_tc(const PoolView &pv, const SeqDesc *d_seqs, const T
     } else {
         mkt = mvt = mkp = mvp = mkv;               // unused
     }
-    // The INL form when the host descriptors fit the parameters.
-    const bool inl = host && prefill_tc_inline_fits(*host) && !q8 && !pv.rope;
+    // The INL form when the caller hands over host descriptors; the caller
+    // has skipped the upload of the device copies, so a form that cannot
+    // carry them is an error, not a fallback.
+    const bool inl = host != nullptr;
+    if (inl && (!prefill_tc_inline_fits(*host) || q8 || pv.rope))
+        return cudaErrorInvalidValue;
     TcParamsInl prmi;
     TcParams &prm = prmi;
     prm.seqs = d_seqs;

@@ -224,10 +224,11 @@ int prefill_tc_rows_per_tile(int group);   // positions per 128-row query tile
 // d_zero_start[c] to d_zero_start[c + 1] (grid + 1 offsets).  `host`, if
 // given and it fits, supplies the descriptors in the launch parameters.
 // Host copies of a launch's descriptors.  When they fit kTcInlineBytes
-// (prefill_tc_inline_fits) the launch carries them in its parameters and
-// the device copies passed to launch_prefill_tc are not read, so no upload
-// has to precede the kernel.  `tables` replaces pv.tables (row stride
-// pv.stride) when given.
+// (prefill_tc_inline_fits) and the pool is bf16 without rotation, the launch
+// can carry them in its parameters: the device copies passed to
+// launch_prefill_tc are then not read, so no upload has to precede the
+// kernel (a `host` that cannot be carried makes the launch fail).  `tables`
+// replaces pv.tables (row stride pv.stride) when given.
 struct TcHostDesc {
     const SeqDesc *seqs = nullptr;
     int n_seqs = 0;
