@@ -95,6 +95,37 @@ def test_rope_bf16_incremental_prefill_then_decode():
     assert c.check() == 0
 
 
+def test_rope_bf16_multi_token_chunks():
+    # Draft chunks of up to 4 rows over a rotary cache whose lengths are not
+    # on a page boundary: the new keys are rotated by their positions as
+    # written, and cache and outputs follow the oracle.
+    rng = np.random.default_rng(43)
+    B, H_q, H_kv, d, n = 2, 8, 2, 128, 4
+    P0 = [203, 90]
+    per_seq = workloads.pages_for(max(P0) + 3 * n) + 1
+    c, m, ids, mids = _caches(B, H_kv, d, "bf16", B * per_seq + 2, per_seq)
+    for b in range(B):
+        q0 = workloads.normal_bf16(rng, (1, P0[b], H_q, d))
+        k0 = workloads.normal_bf16(rng, (1, P0[b], H_kv, d))
+        v0 = workloads.normal_bf16(rng, (1, P0[b], H_kv, d))
+        gqa.attn_prefill(c, [ids[b]], dev(q0, "bf16"), dev(k0, "bf16"), dev(v0, "bf16"), [P0[b]])
+        oracle.prefill(m, [mids[b]], q0, k0, v0, [P0[b]], rope_base=BASE)
+    for T in ([3, 4], [4, 1], [2, 4]):
+        q = workloads.normal_bf16(rng, (B, n, H_q, d))
+        k = workloads.normal_bf16(rng, (B, n, H_kv, d))
+        v = workloads.normal_bf16(rng, (B, n, H_kv, d))
+        c.profile_read()
+        got = host_f64(gqa.attn_prefill(c, ids, dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"), T), "bf16")
+        launched = c.profile_read()
+        assert launched["prefill_tc"][0] == 1, launched
+        ref = oracle.prefill(m, mids, q, k, v, T, rope_base=BASE)
+        mask = np.arange(n)[None, :] < np.asarray(T)[:, None]
+        assert np.all(got[~mask] == 0)
+        assert_close(got[mask], ref[mask], "bf16", "rope multi-token chunk %s" % T)
+    _check_cache(c, m, ids, mids, "bf16")
+    assert c.check() == 0
+
+
 def test_rope_fp32_cuda_core_path():
     rng = np.random.default_rng(42)
     B, n, H_q, H_kv, d = 2, 37, 4, 2, 16
