@@ -717,8 +717,9 @@ def bench_wide(torch, gqa, dist, args, peaks, want_cpu=False):
                              "decode + profiling events)"},
            "queued_no_events": {"us_per_step": round(n_us, 2), "gbs": round(kv_bytes / steps / (n_us / 1e6) / 1e9, 1),
                                 "how": "the queued run again without per-launch events: device time per step "
-                                       "(block-table uploads when the sequence takes a new page, launch gaps and the fused append+decode kernel; "
-                                       "the descriptors travel in the launch parameters)"},
+                                       "(block-table uploads when the sequence takes a new page, launch gaps "
+                                       "and the fused append+decode kernel; the descriptors travel in the "
+                                       "launch parameters)"},
            "l2_flushed": {"us_per_step": round(sum(step_ms) / steps * 1e3, 2),
                           "gbs": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9, 1),
                           "frac_hbm": round(kv_bytes / (sum(step_ms) / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
